@@ -1,0 +1,238 @@
+"""Double-precision CPU oracle for the Mamba-2 selective state update.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+never calls it, and it shares no code with the CUDA library.
+
+The arithmetic lives in ``ssu_oracle.c`` (plain C, double precision); this
+module compiles it with gcc and marshals torch CPU tensors into it.  The
+semantics it follows are those of the "Mamba / SSU" page of the MATE
+documentation ("SSU at a glance" and the API reference) and of the recurrence
+written out in the article "ReplaySSM: Cache SSM Inputs, Not State"
+(section 三个瓶颈); ``ssu_oracle.c`` gives the passage for each step.
+
+Functions with no pin by the pages: the head -> group map (contiguous blocks,
+``g = h // (heads // groups)``) is a convention; parity for it is unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssu_oracle.c")
+_HDR = os.path.join(_HERE, "ssu_oracle.h")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "libssu_oracle.so")
+
+F32, F16, BF16, F64 = 0, 1, 2, 3
+OK, INVALID, ALIASING = 0, 1, 2
+SLOTS_STRIDED, SLOTS_PER_ROW = 0, 1
+TOUCH_READ, TOUCH_WRITTEN = 1, 2
+
+_DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16, torch.float64: F64}
+
+
+class OracleError(RuntimeError):
+    """The oracle rejected its inputs (``code`` is INVALID or ALIASING)."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"oracle rejected the inputs ({'aliasing' if code == ALIASING else 'invalid'}): {msg}")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    """Compile ``ssu_oracle.c`` into ``oracle/_build/libssu_oracle.so``."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = force or not os.path.exists(_LIB_PATH) or max(
+        os.path.getmtime(_SRC), os.path.getmtime(_HDR)) > os.path.getmtime(_LIB_PATH)
+    if stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall", "-Wextra",
+                        "-fno-fast-math", _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Table(ctypes.Structure):
+    _fields_ = [("entries", ctypes.c_void_p), ("s0", ctypes.c_int64), ("s1", ctypes.c_int64),
+                ("extent", ctypes.c_int64), ("mode", ctypes.c_int32)]
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("slots", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("groups", ctypes.c_int64),
+        ("state_dtype", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32),
+        ("dt_per_head", ctypes.c_int32),
+        ("state_in", ctypes.c_void_p), ("state_out", ctypes.c_void_p),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("B", ctypes.c_void_p),
+        ("C", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("y_exact", ctypes.c_void_p),
+        ("dt_softplus", ctypes.c_int32), ("disable_state_update", ctypes.c_int32),
+        ("pad_slot_id", ctypes.c_int64),
+        ("nseq", ctypes.c_int64), ("rows", ctypes.c_int64),
+        ("cu_seqlens", ctypes.c_void_p), ("num_accepted", ctypes.c_void_p),
+        ("read", _Table), ("dst", _Table),
+        ("slot_touched", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str):
+    """Load a compiled oracle from ``path`` and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    lib.orc_ssu_run.argtypes = [ctypes.POINTER(_Problem), ctypes.c_char_p, ctypes.c_int]
+    lib.orc_ssu_run.restype = ctypes.c_int
+    lib.orc_softplus.argtypes = [ctypes.c_double]
+    lib.orc_softplus.restype = ctypes.c_double
+    lib.orc_silu.argtypes = [ctypes.c_double]
+    lib.orc_silu.restype = ctypes.c_double
+    lib.orc_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
+    lib.orc_decode.restype = ctypes.c_double
+    lib.orc_encode.argtypes = [ctypes.c_double, ctypes.c_int]
+    lib.orc_encode.restype = ctypes.c_uint32
+    return lib
+
+
+def compile_source(src_path: str, out_path: str) -> str:
+    """Compile an oracle source file (the tests use this to build deliberately
+    broken copies and check that the pins catch them)."""
+    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fno-fast-math",
+                    "-I", _HERE, src_path, "-o", out_path, "-lm"], check=True)
+    return out_path
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = load_library(build())
+    return _lib
+
+
+def softplus(v: float, lib=None) -> float:
+    return (lib or _load()).orc_softplus(float(v))
+
+
+def silu(z: float, lib=None) -> float:
+    return (lib or _load()).orc_silu(float(z))
+
+
+def decode(bits: int, dtype: torch.dtype, lib=None) -> float:
+    return (lib or _load()).orc_decode(int(bits), _DTYPE_CODE[dtype])
+
+
+def encode(v: float, dtype: torch.dtype, lib=None) -> int:
+    return int((lib or _load()).orc_encode(float(v), _DTYPE_CODE[dtype]))
+
+
+@dataclass
+class Table:
+    """A slot table as the oracle reads it: ``entries`` flat, addressed by
+    ``b*s0 + step*s1`` (STRIDED) or ``cu_seqlens[b] + step`` (PER_ROW)."""
+    entries: torch.Tensor
+    s0: int = 1
+    s1: int = 0
+    mode: int = SLOTS_STRIDED
+
+    @staticmethod
+    def of(t: Optional[torch.Tensor], mode: int = SLOTS_STRIDED) -> Optional["Table"]:
+        """Stride view of a 1-D ``[n]`` table (as ``[n, 1]``) or a 2-D table."""
+        if t is None:
+            return None
+        if t.dim() == 1:
+            return Table(t, t.stride(0), t.stride(0), mode)
+        return Table(t, t.stride(0), t.stride(1), mode)
+
+
+def _cpu(t: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    return None if t is None else t.detach().to("cpu").contiguous()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+@dataclass
+class Result:
+    state: torch.Tensor        # pool after the call, state dtype
+    y: torch.Tensor            # [rows, heads, dim] io dtype
+    y_exact: torch.Tensor      # [rows, heads, dim] float64 before rounding
+    touched: torch.Tensor      # [slots] uint8, OR of TOUCH_READ / TOUCH_WRITTEN
+
+
+def ssu(state: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor,
+        B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
+        z: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+        dt_softplus: bool = False, read: Optional[Table] = None, dst: Optional[Table] = None,
+        pad_slot_id: int = -1, disable_state_update: bool = False,
+        cu_seqlens: Optional[torch.Tensor] = None, num_accepted: Optional[torch.Tensor] = None,
+        state_out: Optional[torch.Tensor] = None, lib=None) -> Result:
+    """Run the oracle.  Tensors may live anywhere; they are copied to the host.
+
+    Shapes: state ``[slots, heads, dim, dstate]``; x, z ``[rows, heads, dim]``;
+    dt ``[rows, heads, dim]`` or ``[rows, heads]`` (per-head step);
+    B, C ``[rows, groups, dstate]``; A, D, dt_bias ``[heads]`` fp32.
+    With ``cu_seqlens`` None every row is its own one-token sequence.
+    ``state_out`` (host, contiguous, same shape and dtype as ``state``) may be
+    given to avoid a copy of a large pool; it must already hold ``state``.
+    """
+    lib = lib or _load()
+    s_in = _cpu(state)
+    slots, heads, dim, dstate = s_in.shape
+    rows = x.shape[0]
+    groups = B.shape[1]
+    if state_out is None:
+        state_out = s_in.clone()
+    xs, dts, Bs, Cs, zs = _cpu(x), _cpu(dt), _cpu(B), _cpu(C), _cpu(z)
+    As = _cpu(A).to(torch.float32)
+    Ds = None if D is None else _cpu(D).to(torch.float32)
+    bs = None if dt_bias is None else _cpu(dt_bias).to(torch.float32)
+    y = torch.empty((rows, heads, dim), dtype=x.dtype)
+    y_exact = torch.empty((rows, heads, dim), dtype=torch.float64)
+    touched = torch.zeros(slots, dtype=torch.uint8)
+    cu = None if cu_seqlens is None else _cpu(cu_seqlens).to(torch.int64)
+    acc = None if num_accepted is None else _cpu(num_accepted).to(torch.int64)
+    nseq = rows if cu is None else cu.numel() - 1
+
+    keep = []
+
+    def table(tb: Optional[Table]) -> _Table:
+        if tb is None:
+            return _Table(None, 0, 0, 0, SLOTS_STRIDED)
+        e = _cpu(tb.entries).reshape(-1).to(torch.int64)
+        keep.append(e)
+        return _Table(e.data_ptr(), tb.s0, tb.s1, e.numel(), tb.mode)
+
+    pr = _Problem(
+        slots=slots, heads=heads, dim=dim, dstate=dstate, groups=groups,
+        state_dtype=_DTYPE_CODE[s_in.dtype], io_dtype=_DTYPE_CODE[xs.dtype],
+        dt_dtype=_DTYPE_CODE[dts.dtype], dt_per_head=int(dts.dim() == 2),
+        state_in=s_in.data_ptr(), state_out=state_out.data_ptr(),
+        x=xs.data_ptr(), dt=dts.data_ptr(), B=Bs.data_ptr(), C=Cs.data_ptr(), z=_ptr(zs),
+        A=As.data_ptr(), D=_ptr(Ds), dt_bias=_ptr(bs),
+        y=y.data_ptr(), y_exact=y_exact.data_ptr(),
+        dt_softplus=int(bool(dt_softplus)), disable_state_update=int(bool(disable_state_update)),
+        pad_slot_id=int(pad_slot_id), nseq=nseq, rows=rows,
+        cu_seqlens=_ptr(cu), num_accepted=_ptr(acc),
+        read=table(read), dst=table(dst), slot_touched=touched.data_ptr(),
+    )
+    for t, name in ((xs, "x"), (zs, "z")):
+        if t is not None and t.dtype != xs.dtype:
+            raise ValueError(f"{name} must have the io dtype")
+    if Bs.dtype != xs.dtype or Cs.dtype != xs.dtype:
+        raise ValueError("B and C must have the io dtype")
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_ssu_run(ctypes.byref(pr), err, 512)
+    if rc != OK:
+        raise OracleError(rc, err.value.decode())
+    return Result(state=state_out, y=y, y_exact=y_exact, touched=touched)

@@ -1,0 +1,393 @@
+/*
+ * ssu_oracle.c -- plain, slow, double-precision CPU definition of the Mamba-2
+ * selective state update (SSU).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker the CUDA path is compared
+ * against.  Only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark load it; the library under test never does, and the two share no
+ * code, header, table or helper.
+ *
+ * What it follows (page "Mamba / SSU" of the MATE documentation, unless noted):
+ *   - Intro paragraph: Mamba-2 keeps ONE decay per head, A[h].
+ *   - "SSU at a glance", rows State, A / D / dt_bias, B / C, Output,
+ *     dt_softplus: shapes, per-head fp32 parameters, heads divisible by groups.
+ *   - "SSU toolchain requirements": the recurrence runs in (at least) fp32 and
+ *     the state is stored back in the state dtype.  Here it runs in double and
+ *     is rounded to nearest-even only when stored.
+ *   - "SSU at a glance", rows Slot semantics and Variable-length and MTP
+ *     decode: slot tables addressed by strides, pad slots read as a zero state
+ *     and are never written, disable_state_update leaves the pool unchanged,
+ *     the read slot is seeded at max(num_accepted - 1, 0), every token
+ *     publishes its state to its own destination entry (or its own read-table
+ *     entry when no destination table is given), empty sequences are skipped.
+ *   - Article "ReplaySSM: Cache SSM Inputs, Not State" (lpnh.cn), section
+ *     三个瓶颈: S_t = alpha_t * S_{t-1} + Delta_t * v_t k_t^T, y_t = S_t q_t,
+ *     i.e. y is read from the UPDATED state; v = x, k = B, q = C,
+ *     alpha = exp(A * dt').
+ *   - The task's formula order: dt' = softplus(dt + dt_bias) (optional),
+ *     dA = exp(A[h] dt'), state = state*dA + dt'*x*B, y = state.C + D*x,
+ *     optional y *= silu(z).
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - head -> group map: contiguous blocks, g = h / (heads / groups).  PARITY
+ *     UNPINNED by the pages (they only require divisibility).
+ *   - no table at all: sequence b uses slot b for reading and writing.
+ *   - SLOTS_PER_ROW mode: entry = cu_seqlens[b] + t ("one entry per packed
+ *     row").  SLOTS_STRIDED mode: entry = b*s0 + t*s1 (page-literal).
+ *   - inputs in which one sequence writes a slot that another sequence reads
+ *     or writes have no deterministic answer; the oracle refuses them
+ *     (return code 2) instead of defining them.
+ *   - softplus is log(1 + e^v), evaluated as max(v,0) + log1p(exp(-|v|)).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "ssu_oracle.h"
+
+/* ------------------------------------------------------------------------ */
+/* Exact decoding of the stored formats into double.                        */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);              /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f + 1024), e - 25);  /* (1 + f/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32. */
+static double bf16_bits_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_elem(const void *base, int64_t i, int dtype)
+{
+    switch (dtype) {
+    case ORC_F32: return (double)((const float *)base)[i];
+    case ORC_F16: return half_bits_to_double(((const uint16_t *)base)[i]);
+    case ORC_BF16: return bf16_bits_to_double(((const uint16_t *)base)[i]);
+    case ORC_F64: return ((const double *)base)[i];
+    }
+    return NAN;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Round-to-nearest-even from double into a narrower binary format.        */
+/* frac_bits: stored fraction bits; emin: exponent of the smallest normal;  */
+/* emax: exponent of the largest finite value.                              */
+/* ------------------------------------------------------------------------ */
+static double round_to_format(double v, int frac_bits, int emin, int emax)
+{
+    if (v == 0.0 || isnan(v) || isinf(v))
+        return v;
+    int e2;
+    frexp(v, &e2);                 /* |v| = m * 2^e2, 0.5 <= m < 1 */
+    int lead = e2 - 1;             /* exponent of the leading bit   */
+    if (lead < emin)
+        lead = emin;               /* subnormal range: fixed quantum */
+    double quantum = ldexp(1.0, lead - frac_bits);
+    /* v / quantum is exact (division by a power of two); nearbyint rounds to
+     * nearest, ties to even, in the default rounding mode. */
+    double r = nearbyint(v / quantum) * quantum;
+    double maxfinite = ldexp(2.0 - ldexp(1.0, -frac_bits), emax);
+    if (fabs(r) > maxfinite)
+        return v > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
+static uint16_t double_to_half_bits(double v)
+{
+    double r = round_to_format(v, 10, -14, 15);
+    uint16_t sign = signbit(r) ? 0x8000 : 0;
+    double a = fabs(r);
+    if (isnan(r)) return 0x7e00;
+    if (isinf(r)) return sign | 0x7c00;
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, -14))                       /* subnormal */
+        return sign | (uint16_t)(a / ldexp(1.0, -24));
+    int e2;
+    double m = frexp(a, &e2);                      /* a = m 2^e2, m in [0.5,1) */
+    int biased = (e2 - 1) + 15;
+    uint16_t frac = (uint16_t)((m * 2.0 - 1.0) * 1024.0);
+    return sign | (uint16_t)(biased << 10) | frac;
+}
+
+static uint16_t double_to_bf16_bits(double v)
+{
+    if (isnan(v)) return 0x7fc0;
+    double r = round_to_format(v, 7, -126, 127);
+    float f = (float)r;                            /* exact: r fits in 8 bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+static void store_elem(void *base, int64_t i, int dtype, double v)
+{
+    switch (dtype) {
+    case ORC_F32: ((float *)base)[i] = (float)round_to_format(v, 23, -126, 127); break;
+    case ORC_F16: ((uint16_t *)base)[i] = double_to_half_bits(v); break;
+    case ORC_BF16: ((uint16_t *)base)[i] = double_to_bf16_bits(v); break;
+    case ORC_F64: ((double *)base)[i] = v; break;
+    }
+}
+
+/* Exposed so the tests can check the conversions against known encodings. */
+double orc_decode(uint32_t bits, int dtype)
+{
+    if (dtype == ORC_F32) {
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return load_elem(&(uint16_t){(uint16_t)bits}, 0, dtype);
+}
+
+uint32_t orc_encode(double v, int dtype)
+{
+    if (dtype == ORC_F32) {
+        float f = (float)round_to_format(v, 23, -126, 127);
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        return u;
+    }
+    if (dtype == ORC_F16) return double_to_half_bits(v);
+    return double_to_bf16_bits(v);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Scalar functions of the method.                                          */
+/* ------------------------------------------------------------------------ */
+
+/* softplus(v) = log(1 + e^v), in a form that neither overflows nor cancels. */
+double orc_softplus(double v)
+{
+    return fmax(v, 0.0) + log1p(exp(-fabs(v)));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+double orc_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Slot resolution ("Slot semantics" row).                                  */
+/* ------------------------------------------------------------------------ */
+
+static int64_t table_entry(const orc_table *t, int64_t b, int64_t step, int64_t row_start)
+{
+    if (t->mode == ORC_SLOTS_PER_ROW)
+        return row_start + step;
+    return b * t->s0 + step * t->s1;
+}
+
+/* Slot read or written by (sequence b, step) through table t.  Writes the
+ * slot to *slot, returns 0, or returns -1 when the entry is outside the
+ * table.  A NULL table means "no table": slot b. */
+static int resolve(const orc_table *t, int64_t b, int64_t step, int64_t row_start, int64_t *slot)
+{
+    if (t == NULL || t->entries == NULL) {
+        *slot = b;
+        return 0;
+    }
+    int64_t e = table_entry(t, b, step, row_start);
+    if (e < 0 || e >= t->extent)
+        return -1;
+    *slot = t->entries[e];
+    return 0;
+}
+
+static void set_err(char *err, int errlen, const char *msg, int64_t a, int64_t b)
+{
+    if (err && errlen > 0)
+        snprintf(err, (size_t)errlen, msg, (long long)a, (long long)b);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The update.                                                              */
+/* ------------------------------------------------------------------------ */
+
+int orc_ssu_run(const orc_problem *pr, char *err, int errlen)
+{
+    const int64_t H = pr->heads, P = pr->dim, N = pr->dstate, G = pr->groups;
+    if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0) {
+        set_err(err, errlen, "bad shape: heads=%lld groups=%lld", H, G);
+        return ORC_INVALID;
+    }
+    const int64_t heads_per_group = H / G;
+    const int64_t nseq = pr->nseq;
+    const orc_table *rtab = (pr->read.entries != NULL) ? &pr->read : NULL;
+    const orc_table *wtab = (pr->dst.entries != NULL) ? &pr->dst : rtab;
+
+    /* Sequence extents.  With no cu_seqlens, sequence b is row b, length 1. */
+    int64_t *start = malloc(sizeof(int64_t) * (size_t)(nseq + 1));
+    if (!start) return ORC_INVALID;
+    for (int64_t b = 0; b <= nseq; ++b)
+        start[b] = pr->cu_seqlens ? pr->cu_seqlens[b] : b;
+    if (start[0] != 0 || start[nseq] != pr->rows) {
+        set_err(err, errlen, "cu_seqlens must start at 0 and end at rows (%lld, got %lld)",
+                pr->rows, start[nseq]);
+        free(start);
+        return ORC_INVALID;
+    }
+    for (int64_t b = 0; b < nseq; ++b) {
+        if (start[b + 1] < start[b]) {
+            set_err(err, errlen, "cu_seqlens decreases at sequence %lld%lld", b, 0);
+            free(start);
+            return ORC_INVALID;
+        }
+    }
+
+    /* Resolve every slot first and check it. */
+    int64_t *seed = malloc(sizeof(int64_t) * (size_t)(nseq > 0 ? nseq : 1));
+    int64_t *wslot = malloc(sizeof(int64_t) * (size_t)(pr->rows > 0 ? pr->rows : 1));
+    int64_t *writer = malloc(sizeof(int64_t) * (size_t)pr->slots);
+    if (!seed || !wslot || !writer) {
+        free(start); free(seed); free(wslot); free(writer);
+        return ORC_INVALID;
+    }
+    int rc = ORC_OK;
+    for (int64_t s = 0; s < pr->slots; ++s)
+        writer[s] = -1;
+    for (int64_t b = 0; b < nseq && rc == ORC_OK; ++b) {
+        int64_t len = start[b + 1] - start[b];
+        if (len == 0) {
+            seed[b] = pr->pad_slot_id;
+            continue;
+        }
+        /* Seed step: max(num_accepted - 1, 0); none given => step 0. */
+        int64_t t_seed = 0;
+        if (pr->num_accepted != NULL) {
+            t_seed = pr->num_accepted[b] - 1;
+            if (t_seed < 0) t_seed = 0;
+        }
+        if (resolve(rtab, b, t_seed, start[b], &seed[b]) != 0) {
+            set_err(err, errlen, "read-table entry out of range (sequence %lld, step %lld)", b, t_seed);
+            rc = ORC_INVALID;
+            break;
+        }
+        if (seed[b] != pr->pad_slot_id && (seed[b] < 0 || seed[b] >= pr->slots)) {
+            set_err(err, errlen, "seed slot %lld of sequence %lld out of range", seed[b], b);
+            rc = ORC_INVALID;
+            break;
+        }
+        for (int64_t t = 0; t < len; ++t) {
+            int64_t r = start[b] + t, w;
+            if (resolve(wtab, b, t, start[b], &w) != 0) {
+                set_err(err, errlen, "destination entry out of range (sequence %lld, step %lld)", b, t);
+                rc = ORC_INVALID;
+                break;
+            }
+            if (w != pr->pad_slot_id && (w < 0 || w >= pr->slots)) {
+                set_err(err, errlen, "destination slot %lld of row %lld out of range", w, r);
+                rc = ORC_INVALID;
+                break;
+            }
+            wslot[r] = w;
+            if (w != pr->pad_slot_id && !pr->disable_state_update) {
+                if (writer[w] != -1 && writer[w] != b) {
+                    set_err(err, errlen, "slot %lld is written by two sequences (second: %lld)", w, b);
+                    rc = ORC_ALIASING;
+                    break;
+                }
+                writer[w] = b;
+            }
+        }
+    }
+    /* A seed that another sequence overwrites has no defined value. */
+    for (int64_t b = 0; b < nseq && rc == ORC_OK; ++b) {
+        if (start[b + 1] == start[b] || seed[b] == pr->pad_slot_id)
+            continue;
+        if (writer[seed[b]] != -1 && writer[seed[b]] != b) {
+            set_err(err, errlen, "seed slot %lld of sequence %lld is written by another sequence",
+                    seed[b], b);
+            rc = ORC_ALIASING;
+        }
+    }
+    if (rc != ORC_OK) {
+        free(start); free(seed); free(wslot); free(writer);
+        return rc;
+    }
+
+    if (pr->slot_touched != NULL) {
+        for (int64_t b = 0; b < nseq; ++b) {
+            if (start[b + 1] == start[b]) continue;
+            if (seed[b] != pr->pad_slot_id) pr->slot_touched[seed[b]] |= ORC_TOUCH_READ;
+            if (pr->disable_state_update) continue;
+            for (int64_t r = start[b]; r < start[b + 1]; ++r)
+                if (wslot[r] != pr->pad_slot_id) pr->slot_touched[wslot[r]] |= ORC_TOUCH_WRITTEN;
+        }
+    }
+
+    double *S = malloc(sizeof(double) * (size_t)N);
+    if (!S) {
+        free(start); free(seed); free(wslot); free(writer);
+        return ORC_INVALID;
+    }
+    for (int64_t b = 0; b < nseq; ++b) {
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t g = h / heads_per_group;
+            const double A = (double)pr->A[h];
+            const double Dh = pr->D ? (double)pr->D[h] : 0.0;
+            const double bias = pr->dt_bias ? (double)pr->dt_bias[h] : 0.0;
+            for (int64_t p = 0; p < P; ++p) {
+                if (start[b + 1] == start[b])
+                    continue;                       /* empty sequence: skipped */
+                /* Seed: a pad slot reads as a zero state.  Seeds come from the
+                 * input pool, which no write of this call touches. */
+                for (int64_t n = 0; n < N; ++n)
+                    S[n] = (seed[b] == pr->pad_slot_id)
+                               ? 0.0
+                               : load_elem(pr->state_in, ((seed[b] * H + h) * P + p) * N + n,
+                                           pr->state_dtype);
+                for (int64_t r = start[b]; r < start[b + 1]; ++r) {
+                    const int64_t xi = (r * H + h) * P + p;
+                    const int64_t dti = pr->dt_per_head ? (r * H + h) : xi;
+                    double d = load_elem(pr->dt, dti, pr->dt_dtype) + bias;
+                    if (pr->dt_softplus)
+                        d = orc_softplus(d);
+                    const double dA = exp(A * d);
+                    const double xv = load_elem(pr->x, xi, pr->io_dtype);
+                    const int64_t bc = (r * G + g) * N;
+                    double y = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        S[n] = S[n] * dA + d * xv * load_elem(pr->B, bc + n, pr->io_dtype);
+                        y += S[n] * load_elem(pr->C, bc + n, pr->io_dtype);
+                    }
+                    y += Dh * xv;
+                    if (pr->z != NULL)
+                        y *= orc_silu(load_elem(pr->z, xi, pr->io_dtype));
+                    if (pr->y_exact != NULL)
+                        pr->y_exact[xi] = y;
+                    store_elem(pr->y, xi, pr->io_dtype, y);
+                    /* Publish this token's state (never re-read: S stays in
+                     * double for the next token). */
+                    if (!pr->disable_state_update && wslot[r] != pr->pad_slot_id)
+                        for (int64_t n = 0; n < N; ++n)
+                            store_elem(pr->state_out, ((wslot[r] * H + h) * P + p) * N + n,
+                                       pr->state_dtype, S[n]);
+                }
+            }
+        }
+    }
+    free(S);
+    free(start); free(seed); free(wslot); free(writer);
+    return ORC_OK;
+}

@@ -1,0 +1,62 @@
+/*
+ * ssu_oracle.h -- interface of the double-precision CPU oracle for the
+ * Mamba-2 selective state update.  TEST INFRASTRUCTURE ONLY: used by the
+ * tests, the smoke check and the CPU-baseline leg of the benchmark, never by
+ * the library under test.  Host pointers only; every array is contiguous.
+ */
+#ifndef SSU_ORACLE_H
+#define SSU_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element formats (raw bits in host memory) */
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_F64 = 3 };
+/* return codes */
+enum { ORC_OK = 0, ORC_INVALID = 1, ORC_ALIASING = 2 };
+/* slot-table addressing */
+enum { ORC_SLOTS_STRIDED = 0, ORC_SLOTS_PER_ROW = 1 };
+/* bits of slot_touched[] */
+enum { ORC_TOUCH_READ = 1, ORC_TOUCH_WRITTEN = 2 };
+
+typedef struct {
+    const int64_t *entries;  /* NULL: no table                             */
+    int64_t s0, s1;          /* STRIDED: entry = b*s0 + step*s1            */
+    int64_t extent;          /* entries[0 .. extent-1] are addressable     */
+    int32_t mode;            /* ORC_SLOTS_STRIDED or ORC_SLOTS_PER_ROW     */
+} orc_table;
+
+typedef struct {
+    int64_t slots, heads, dim, dstate, groups;
+    int32_t state_dtype, io_dtype, dt_dtype;
+    int32_t dt_per_head;            /* dt is [rows, heads] instead of [rows, heads, dim] */
+    const void *state_in;           /* [slots, heads, dim, dstate], read only              */
+    void *state_out;                /* same shape; caller fills it with state_in first     */
+    const void *x, *dt, *B, *C, *z; /* x, z: [rows, heads, dim]; B, C: [rows, groups, dstate]; z may be NULL */
+    const float *A, *D, *dt_bias;   /* [heads] fp32; D and dt_bias may be NULL             */
+    void *y;                        /* [rows, heads, dim] in io_dtype, rounded to nearest even */
+    double *y_exact;                /* [rows, heads, dim] before rounding; may be NULL     */
+    int32_t dt_softplus, disable_state_update;
+    int64_t pad_slot_id;
+    int64_t nseq, rows;
+    const int64_t *cu_seqlens;      /* [nseq + 1]; NULL: sequence b is row b (one token)  */
+    const int64_t *num_accepted;    /* [nseq]; NULL: seed at step 0                       */
+    orc_table read, dst;            /* dst.entries NULL: publish through the read table   */
+    uint8_t *slot_touched;          /* [slots] or NULL: OR of ORC_TOUCH_* per slot         */
+} orc_problem;
+
+int orc_ssu_run(const orc_problem *problem, char *err, int errlen);
+
+double orc_softplus(double v);
+double orc_silu(double z);
+double orc_decode(uint32_t bits, int dtype);
+uint32_t orc_encode(double v, int dtype);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSU_ORACLE_H */

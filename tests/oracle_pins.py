@@ -1,0 +1,593 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` function takes a loaded oracle library (``lib``) and raises on a
+mismatch, so the same pins run against the real oracle (test_oracle_pins.py)
+and against deliberately broken copies of it (test_oracle_mutations.py).
+
+What pins what:
+  * closed forms of special cases (dt = 0, zero state, A = 0, x = 0, basis
+    vectors for B and C), evaluated here with numpy from the decoded inputs;
+  * the unrolled form of the recurrence given in the article "ReplaySSM:
+    Cache SSM Inputs, Not State" (section 核心做法):
+        S_h = gamma_{1:h} S_0 + sum_j gamma_{j+1:h} dt'_j x_j B_j,
+    gamma_{i:h} = prod_{m=i..h} exp(A dt'_m), against the oracle's
+    token-by-token loop;
+  * worked examples computed by hand (values in the comments);
+  * the slot effects of the call forms printed on the MATE "Mamba / SSU"
+    page (tests/golden/page_examples.json);
+  * invariants the page states: pad slots are never written,
+    disable_state_update leaves the pool unchanged, flat and 2-D tables
+    name the same entries for one sequence, empty sequences are skipped;
+  * format conversions against fixed encodings and numpy / torch casts.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+from ssu_testlib import f64, run_oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+LN2 = math.log(2.0)
+
+
+def _close(a, b, rtol=1e-12, atol=1e-12, what=""):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    if a.shape != b.shape or not np.all(np.abs(a - b) <= rtol * np.abs(b) + atol):
+        d = np.max(np.abs(a - b)) if a.shape == b.shape else "shape"
+        raise AssertionError(f"{what}: max abs diff {d}")
+
+
+def _dt_eff(w: workloads.Workload) -> np.ndarray:
+    """Processed step dt' as numpy float64 [rows, heads, dim]."""
+    d = f64(w.dt)
+    if d.ndim == 2:
+        d = np.repeat(d[:, :, None], w.x.shape[2], axis=2)
+    if w.dt_bias is not None:
+        d = d + f64(w.dt_bias)[None, :, None]
+    if w.dt_softplus:
+        d = np.logaddexp(0.0, d)          # log(1 + e^d), numpy's routine
+    return d
+
+
+def _silu_np(z):
+    return z * (1.0 / (1.0 + np.exp(-z)))
+
+
+def _problem(seed, **kw):
+    base = dict(slots=24, heads=4, dim=3, dstate=8, groups=2, nseq=3, max_len=3,
+                state_dtype=torch.float64, io_dtype=torch.bfloat16, tables="distinct")
+    base.update(kw)
+    return workloads.random_problem(seed, **base)
+
+
+# --------------------------------------------------------------------------
+# Format conversions (used for every stored value).
+# --------------------------------------------------------------------------
+def pin_conversions(lib):
+    enc, dec = oracle.encode, oracle.decode
+    f16, bf16 = torch.float16, torch.bfloat16
+    fixed = [
+        (1.0, f16, 0x3C00), (-2.0, f16, 0xC000), (65504.0, f16, 0x7BFF),
+        (2.0 ** -24, f16, 0x0001), (1 + 2.0 ** -11, f16, 0x3C00), (1 + 3 * 2.0 ** -11, f16, 0x3C02),
+        (65520.0, f16, 0x7C00), (2.0 ** -25, f16, 0x0000), (3 * 2.0 ** -26, f16, 0x0001),
+        (1.0, bf16, 0x3F80), (-0.5, bf16, 0xBF00), (1 + 2.0 ** -8, bf16, 0x3F80),
+        (1 + 3 * 2.0 ** -8, bf16, 0x3F82), (2.0 ** -133, bf16, 0x0001),
+    ]
+    for v, dt, bits in fixed:
+        got = enc(v, dt, lib=lib)
+        if got != bits:
+            raise AssertionError(f"encode({v!r}, {dt}) = {got:#06x}, expected {bits:#06x}")
+    for bits, dt, v in [(0x3C00, f16, 1.0), (0x0001, f16, 2.0 ** -24), (0x7BFF, f16, 65504.0),
+                        (0x3F80, bf16, 1.0), (0xC0A0, bf16, -5.0), (0x8001, f16, -(2.0 ** -24))]:
+        if dec(bits, dt, lib=lib) != v:
+            raise AssertionError(f"decode({bits:#06x}, {dt}) != {v}")
+    rng = np.random.default_rng(7)
+    vals = rng.standard_normal(4000) * np.exp(rng.uniform(-12, 10, 4000))
+    ref16 = vals.astype(np.float16).view(np.uint16)          # numpy's direct double -> half
+    for v, r in zip(vals, ref16):
+        if enc(v, f16, lib=lib) != int(r):
+            raise AssertionError(f"fp16 encode({v!r}) disagrees with numpy")
+    vals32 = vals.astype(np.float32)                         # exact in double
+    refbf = torch.from_numpy(vals32).to(bf16).view(torch.int16).numpy().view(np.uint16)
+    for v, r in zip(vals32, refbf):
+        if enc(float(v), bf16, lib=lib) != int(r):
+            raise AssertionError(f"bf16 encode({v!r}) disagrees with torch")
+    for v in vals[:500]:
+        if oracle.decode(enc(v, torch.float32, lib=lib), torch.float32, lib=lib) != float(np.float32(v)):
+            raise AssertionError("fp32 round trip")
+
+
+# --------------------------------------------------------------------------
+# Scalar functions.
+# --------------------------------------------------------------------------
+def pin_scalar_functions(lib):
+    sp, si = (lambda v: oracle.softplus(v, lib=lib)), (lambda v: oracle.silu(v, lib=lib))
+    _close(sp(0.0), LN2, what="softplus(0) = ln 2")
+    for v in np.linspace(-30, 30, 121):
+        _close(sp(v) - sp(-v), v, atol=1e-12, what="softplus(v) - softplus(-v) = v")
+        _close(si(v) - si(-v), v, atol=1e-12, what="silu(v) - silu(-v) = v")
+        _close(si(v) + si(-v), v * math.tanh(v / 2), atol=1e-12, what="silu(v) + silu(-v)")
+    _close(sp(-40.0), math.exp(-40.0), rtol=1e-12, atol=0, what="softplus(-40) = e^-40")
+    _close(sp(40.0), 40.0, rtol=1e-15, atol=0, what="softplus(40) = 40")
+    _close(si(0.0), 0.0, what="silu(0) = 0")
+
+
+# --------------------------------------------------------------------------
+# Hand-worked examples (heads 1, dim 1, dstate 2, groups 1, fp64 state).
+# --------------------------------------------------------------------------
+def _hand(lib, *, S0, A, dt, x, B, C, D=None, z=None, bias=None, softplus=False, cu=None, acc=None):
+    rows = len(x)
+    st = torch.tensor(S0, dtype=torch.float64).view(1, 1, 1, 2)
+    xs = torch.tensor(x, dtype=torch.float32).view(rows, 1, 1)
+    dts = torch.tensor(dt, dtype=torch.float32).view(rows, 1, 1)
+    Bs = torch.tensor(B, dtype=torch.float32).view(rows, 1, 2)
+    Cs = torch.tensor(C, dtype=torch.float32).view(rows, 1, 2)
+    zs = None if z is None else torch.tensor(z, dtype=torch.float32).view(rows, 1, 1)
+    t = lambda v: None if v is None else torch.tensor([v], dtype=torch.float32)
+    tab = torch.zeros(rows, dtype=torch.int64)
+    read = oracle.Table(tab, 0, 0, oracle.SLOTS_STRIDED)
+    r = oracle.ssu(st, xs, dts, t(A), Bs, Cs, D=t(D), z=zs, dt_bias=t(bias), dt_softplus=softplus,
+                   read=read, cu_seqlens=None if cu is None else torch.tensor(cu),
+                   num_accepted=None if acc is None else torch.tensor(acc), lib=lib)
+    return r.y_exact.view(-1).numpy(), r.state.view(-1).numpy()
+
+
+def pin_hand_worked(lib):
+    # 1) A = 0 so dA = 1; dt' = 0.5; S0 = [1, 2], x = 2, B = [1, .5], C = [1, 1], D = .5
+    #    S1 = [1 + .5*2*1, 2 + .5*2*.5] = [2, 2.5];  y = 2 + 2.5 + .5*2 = 5.5
+    y, s = _hand(lib, S0=[1, 2], A=0.0, dt=[0.5], x=[2.0], B=[[1, .5]], C=[[1, 1]], D=0.5)
+    _close(y, [5.5], what="hand 1 y")
+    _close(s, [2.0, 2.5], what="hand 1 state")
+    # 2) same with z = 2: y = 5.5 * 2 / (1 + e^-2)
+    y, _ = _hand(lib, S0=[1, 2], A=0.0, dt=[0.5], x=[2.0], B=[[1, .5]], C=[[1, 1]], D=0.5, z=[2.0])
+    _close(y, [5.5 * 2.0 / (1.0 + math.exp(-2.0))], what="hand 2 y (silu gate)")
+    # 3) softplus on, dt + bias = 0 -> dt' = ln 2; A = -1 -> dA = 1/2.
+    #    S0 = [4, -2], x = 1, B = [1, 1], C = [1, -1]:
+    #    S1 = [2 + ln2, -1 + ln2]; y = S1[0] - S1[1] = 3.
+    y, s = _hand(lib, S0=[4, -2], A=-1.0, dt=[0.75], bias=-0.75, x=[1.0], B=[[1, 1]], C=[[1, -1]],
+                 softplus=True)
+    _close(y, [3.0], what="hand 3 y")
+    _close(s, [2 + LN2, -1 + LN2], what="hand 3 state")
+    # 4) two tokens of one sequence, dt' = ln 2 each (dt = 0, softplus), A = -1, D = 0.5.
+    #    token 1: x = 2, B = [1, 0], C = [0, 1] -> S1 = [.5 + 2 ln2, 1], y1 = 1 + .5*2 = 2
+    #    token 2: x = -1, B = [0, 1], C = [1, 0] -> S2 = [.25 + ln2, .5 - ln2],
+    #             y2 = .25 + ln2 - .5 = ln2 - .25
+    #    both tokens publish to slot 0 (no destination table, read table [0, 0]);
+    #    the last one wins.
+    y, s = _hand(lib, S0=[1, 2], A=-1.0, dt=[0.0, 0.0], x=[2.0, -1.0], B=[[1, 0], [0, 1]],
+                 C=[[0, 1], [1, 0]], D=0.5, softplus=True, cu=[0, 2])
+    _close(y, [2.0, LN2 - 0.25], what="hand 4 y")
+    _close(s, [0.25 + LN2, 0.5 - LN2], what="hand 4 state")
+
+
+# --------------------------------------------------------------------------
+# Closed forms on random data.
+# --------------------------------------------------------------------------
+def _seed_state(w, res_touched=None):
+    """Seed state per sequence as numpy [nseq, heads, dim, dstate] (zeros for pad/no seed)."""
+    st = f64(w.state)
+    out = np.zeros((w.nseq,) + st.shape[1:])
+    lens = w.meta["lengths"]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    for b in range(w.nseq):
+        if lens[b] == 0:
+            continue
+        t = 0
+        if w.kind == "packed" and w.num_accepted is not None:
+            t = max(int(w.num_accepted[b]) - 1, 0)
+        if w.read is None:
+            s = b
+        elif w.slot_mode == workloads.SLOTS_PER_ROW:
+            s = int(w.read.reshape(-1)[cu[b] + t])
+        elif w.read.dim() == 1:
+            s = int(w.read[b + t])
+        else:
+            s = int(w.read[b, t])
+        if s != w.pad_slot_id:
+            out[b] = st[s]
+    return out
+
+
+def _groups_of(w):
+    H, G = w.x.shape[1], w.B.shape[1]
+    return np.arange(H) // (H // G)
+
+
+def pin_dt_zero(lib):
+    """dt' = 0 (dt = 0, no bias, softplus off): dA = 1 and no input term, so the
+    published state is bit-identical to the seed and y = S.C + D x (x silu(z))."""
+    for sd in (torch.float64, torch.float32, torch.float16, torch.bfloat16):
+        w = _problem(11, state_dtype=sd, dt_softplus=False, with_bias=False, kind="onetoken",
+                     tables="distinct", pad_frac=0.0)
+        w.dt.zero_()
+        r = run_oracle(w, lib=lib)
+        g = _groups_of(w)
+        Cn, xn, zn = f64(w.C), f64(w.x), f64(w.z)
+        S = _seed_state(w)
+        y = np.einsum("bhpn,bhn->bhp", S, Cn[:, g, :]) + f64(w.D)[None, :, None] * xn
+        y = y * _silu_np(zn)
+        _close(r.y_exact.numpy(), y, rtol=1e-12, atol=1e-12, what=f"dt=0 y ({sd})")
+        for b in range(w.nseq):
+            s_in, s_out = int(w.read[b]), int(w.dst[b])
+            if not torch.equal(r.state[s_out], w.state[s_in]):
+                raise AssertionError(f"dt=0 must leave the state bit-unchanged ({sd})")
+
+
+def pin_zero_state(lib):
+    """Zero seed (pad read): after one token S = dt' x B, so
+    y = dt' (B.C) x + D x, then times silu(z)."""
+    w = _problem(12, kind="onetoken", tables="distinct", pad_frac=0.0)
+    w.read[:] = w.pad_slot_id
+    r = run_oracle(w, lib=lib)
+    g = _groups_of(w)
+    d, xn = _dt_eff(w), f64(w.x)
+    BC = np.einsum("bhn,bhn->bh", f64(w.B)[:, g, :], f64(w.C)[:, g, :])
+    y = (d * BC[:, :, None] * xn + f64(w.D)[None, :, None] * xn) * _silu_np(f64(w.z))
+    _close(r.y_exact.numpy(), y, rtol=1e-11, atol=1e-12, what="zero-state y")
+    for b in range(w.nseq):
+        S = d[b][:, :, None] * xn[b][:, :, None] * f64(w.B)[b, g][:, None, :]
+        _close(f64(r.state[int(w.dst[b])]), S, rtol=1e-12, atol=1e-14, what="zero-state state")
+
+
+def pin_A_zero(lib):
+    """A = 0: dA = 1, S' = S + dt' x B."""
+    w = _problem(13, kind="onetoken", tables="inplace", pad_frac=0.0)
+    w.A.zero_()
+    r = run_oracle(w, lib=lib)
+    g = _groups_of(w)
+    S = _seed_state(w)
+    d, xn, Bn = _dt_eff(w), f64(w.x), f64(w.B)
+    for b in range(w.nseq):
+        ref = S[b] + (d[b] * xn[b])[:, :, None] * Bn[b, g][:, None, :]
+        _close(f64(r.state[int(w.dst[b])]), ref, rtol=1e-12, atol=1e-14, what="A=0 state")
+
+
+def pin_decay_only(lib):
+    """x = 0 over several tokens: S_T = exp(A * sum_t dt'_t) S_0 and
+    y_t = S_t . C_t (the D x term vanishes)."""
+    w = _problem(14, kind="packed", tables="distinct", pad_frac=0.0, max_len=4, allow_empty=False,
+                 with_z=False, nseq=3)
+    w.x.zero_()
+    r = run_oracle(w, lib=lib)
+    A, d, g = f64(w.A), _dt_eff(w), _groups_of(w)
+    S0 = _seed_state(w)
+    cu = np.concatenate([[0], np.cumsum(w.meta["lengths"])])
+    for b in range(w.nseq):
+        acc_d = np.zeros(d.shape[1:])
+        for t, row in enumerate(range(cu[b], cu[b + 1])):
+            acc_d = acc_d + d[row]
+            St = np.exp(A[:, None] * acc_d)[:, :, None] * S0[b]
+            yt = np.einsum("hpn,hn->hp", St, f64(w.C)[row, g])
+            _close(r.y_exact[row].numpy(), yt, rtol=1e-11, atol=1e-13, what="decay-only y")
+        last = int(w.dst[b, w.meta["lengths"][b] - 1])
+        _close(f64(r.state[last]), St, rtol=1e-11, atol=1e-14, what="decay-only state")
+
+
+def pin_unrolled(lib):
+    """Multi-token recurrence against its unrolled form (ReplaySSM, 核心做法):
+    S_h = gamma_{1:h} S_0 + sum_{j<=h} gamma_{j+1:h} dt'_j x_j B_j,  with
+    gamma_{i:h} = prod_{m=i..h} exp(A dt'_m); y_h = S_h . C_h + D x_h, gated."""
+    for sd in (torch.float64,):
+        w = _problem(15, kind="packed", tables="distinct", pad_frac=0.0, max_len=5, nseq=3,
+                     allow_empty=False, state_dtype=sd, heads=4, groups=2, dim=3, dstate=8,
+                     slots=40)
+        r = run_oracle(w, lib=lib)
+        A, d, g = f64(w.A), _dt_eff(w), _groups_of(w)
+        xn, Bn, Cn, Dn, zn = f64(w.x), f64(w.B), f64(w.C), f64(w.D), f64(w.z)
+        S0 = _seed_state(w)
+        cu = np.concatenate([[0], np.cumsum(w.meta["lengths"])])
+        for b in range(w.nseq):
+            rows = list(range(cu[b], cu[b + 1]))
+            alpha = [np.exp(A[:, None] * d[r_]) for r_ in rows]      # [heads, dim] each
+            for hidx in range(len(rows)):
+                gam = np.ones_like(alpha[0])
+                for m in range(0, hidx + 1):
+                    gam = gam * alpha[m]
+                S = gam[:, :, None] * S0[b]
+                for j in range(hidx + 1):
+                    gj = np.ones_like(alpha[0])
+                    for m in range(j + 1, hidx + 1):
+                        gj = gj * alpha[m]
+                    rj = rows[j]
+                    S = S + (gj * d[rj] * xn[rj])[:, :, None] * Bn[rj, g][:, None, :]
+                rh = rows[hidx]
+                y = np.einsum("hpn,hn->hp", S, Cn[rh, g]) + Dn[:, None] * xn[rh]
+                y = y * _silu_np(zn[rh])
+                _close(r.y_exact[rh].numpy(), y, rtol=1e-11, atol=1e-12, what="unrolled y")
+                _close(f64(r.state[int(w.dst[b, hidx])]), S, rtol=1e-11, atol=1e-13,
+                       what="unrolled state")
+
+
+def pin_basis_vectors(lib):
+    """B = e_j and C = e_k with j != k: only column j receives the input, and
+    y reads column k of the updated state."""
+    w = _problem(16, kind="onetoken", tables="distinct", pad_frac=0.0, with_z=False, groups=1)
+    j, k = 2, 5
+    w.B.zero_()
+    w.C.zero_()
+    w.B[:, :, j] = 1
+    w.C[:, :, k] = 1
+    r = run_oracle(w, lib=lib)
+    A, d, xn = f64(w.A), _dt_eff(w), f64(w.x)
+    S0 = _seed_state(w)
+    for b in range(w.nseq):
+        dA = np.exp(A[:, None] * d[b])
+        ref = dA[:, :, None] * S0[b]
+        ref[:, :, j] += d[b] * xn[b]
+        _close(f64(r.state[int(w.dst[b])]), ref, rtol=1e-12, atol=1e-14, what="basis state")
+        _close(r.y_exact[b].numpy(), ref[:, :, k] + f64(w.D)[:, None] * xn[b], what="basis y")
+
+
+def pin_group_map(lib):
+    """Convention (not fixed by the pages): head h uses group h // (heads/groups).
+    With B, C non-zero only in group 1 of 2, heads 2 and 3 of 4 get the input
+    term, heads 0 and 1 only decay."""
+    w = _problem(17, kind="onetoken", tables="distinct", pad_frac=0.0, heads=4, groups=2,
+                 with_z=False, with_D=False)
+    w.B[:, 0, :] = 0
+    w.C[:, 0, :] = 0
+    r = run_oracle(w, lib=lib)
+    A, d = f64(w.A), _dt_eff(w)
+    S0 = _seed_state(w)
+    for b in range(w.nseq):
+        out = f64(r.state[int(w.dst[b])])
+        dA = np.exp(A[:, None] * d[b])
+        _close(out[:2], dA[:2, :, None] * S0[b][:2], what="group 0 heads only decay")
+        if np.allclose(out[2:], dA[2:, :, None] * S0[b][2:]):
+            raise AssertionError("group 1 heads received no input")
+        _close(r.y_exact[b, :2].numpy(), np.zeros((2, w.x.shape[2])), what="group 0 y")
+
+
+# --------------------------------------------------------------------------
+# Slot semantics.
+# --------------------------------------------------------------------------
+def _golden():
+    with open(os.path.join(GOLDEN, "page_examples.json")) as f:
+        return json.load(f)
+
+
+def _page_problem(ex, heads=2, dim=2, dstate=4, groups=1, seed=21):
+    rows = ex.get("rows") or (ex["batch"] * ex.get("steps", 1))
+    g = torch.Generator().manual_seed(seed)
+    state = (torch.randn((ex["slots"], heads, dim, dstate), generator=g, dtype=torch.float64) * 0.5)
+    x = torch.randn((rows, heads, dim), generator=g).to(torch.bfloat16)
+    dt = torch.rand((rows, heads, dim), generator=g) * 0.2
+    A = -torch.rand(heads, generator=g)
+    B = torch.randn((rows, groups, dstate), generator=g).to(torch.bfloat16)
+    C = torch.randn((rows, groups, dstate), generator=g).to(torch.bfloat16)
+    return state, x, dt, A, B, C
+
+
+def _touched(res, bit):
+    return sorted(int(i) for i in torch.nonzero(res.touched & bit).view(-1))
+
+
+def pin_page_examples(lib):
+    gold = _golden()
+    # minimal one-token example
+    ex = gold["minimal_onetoken"]
+    state, x, dt, A, B, C = _page_problem(ex)
+    tab = torch.tensor(ex["read"])
+    res = oracle.ssu(state, x, dt, A, B, C, read=oracle.Table.of(tab), dst=oracle.Table.of(tab),
+                     pad_slot_id=ex["pad_slot_id"], lib=lib)
+    if _touched(res, oracle.TOUCH_READ) != ex["expect_seed_slots"]:
+        raise AssertionError("minimal example: seed slots")
+    if _touched(res, oracle.TOUCH_WRITTEN) != ex["expect_written_slots"]:
+        raise AssertionError("minimal example: written slots")
+    for s in ex["expect_untouched_slots"]:
+        if not torch.equal(res.state[s], state[s]):
+            raise AssertionError("minimal example: untouched slot changed")
+    # 2-D MTP example
+    ex = gold["mtp_2d"]
+    state, x, dt, A, B, C = _page_problem(ex)
+    read, dst = torch.tensor(ex["read"]), torch.tensor(ex["dst"])
+    res = oracle.ssu(state, x, dt, A, B, C, read=oracle.Table.of(read), dst=oracle.Table.of(dst),
+                     pad_slot_id=ex["pad_slot_id"], cu_seqlens=torch.tensor(ex["cu_seqlens"]),
+                     num_accepted=torch.tensor(ex["num_accepted"]), lib=lib)
+    if _touched(res, oracle.TOUCH_READ) != ex["expect_seed_slots"]:
+        raise AssertionError(f"MTP example: seed slots {_touched(res, oracle.TOUCH_READ)}")
+    if _touched(res, oracle.TOUCH_WRITTEN) != ex["expect_written_slots"]:
+        raise AssertionError("MTP example: written slots")
+    for s in range(14):
+        if not torch.equal(res.state[s], state[s]):
+            raise AssertionError("MTP example: a read-side slot changed")
+    # flat table, one sequence; also the same call with the table as [1, rows]
+    ex = gold["flat_one_sequence"]
+    state, x, dt, A, B, C = _page_problem(ex)
+    tab = torch.tensor(ex["read"])
+    common = dict(pad_slot_id=ex["pad_slot_id"], cu_seqlens=torch.tensor(ex["cu_seqlens"]),
+                  num_accepted=torch.tensor(ex["num_accepted"]), lib=lib)
+    flat = oracle.ssu(state, x, dt, A, B, C, read=oracle.Table.of(tab), dst=oracle.Table.of(tab), **common)
+    two_d = oracle.ssu(state, x, dt, A, B, C, read=oracle.Table.of(tab.view(1, -1)),
+                       dst=oracle.Table.of(tab.view(1, -1)), **common)
+    per_row = oracle.ssu(state, x, dt, A, B, C, read=oracle.Table.of(tab, oracle.SLOTS_PER_ROW),
+                         dst=oracle.Table.of(tab, oracle.SLOTS_PER_ROW), **common)
+    if _touched(flat, oracle.TOUCH_READ) != []:
+        raise AssertionError("flat example: the seed is the pad slot and must not count as read")
+    if _touched(flat, oracle.TOUCH_WRITTEN) != ex["expect_written_slots"]:
+        raise AssertionError("flat example: written slots")
+    if not torch.equal(flat.state[0], state[0]):
+        raise AssertionError("flat example: pad slot 0 was written")
+    for other in (two_d, per_row):
+        if not (torch.equal(other.state, flat.state) and torch.equal(other.y_exact, flat.y_exact)):
+            raise AssertionError("flat, 2-D and per-row tables must name the same entries")
+    # the seed is the pad: token 0 starts from zero, so y_0 = dt'_0 x_0 (B_0 . C_0)
+    bc = float(np.dot(f64(B)[0, 0], f64(C)[0, 0]))
+    _close(flat.y_exact[0].numpy(), f64(dt)[0] * f64(x)[0] * bc, rtol=1e-12, atol=1e-15,
+           what="flat example: zero seed")
+
+
+def pin_pad_never_written(lib):
+    """pad_slot_id = 0, a real slot full of data: it must stay byte-identical,
+    and a pad read must equal a read of an all-zero slot."""
+    w = _problem(31, kind="packed", tables="distinct", pad_slot_id=0, pad_frac=0.3,
+                 slot_mode=workloads.SLOTS_STRIDED, nseq=4, max_len=3, slots=40)
+    r = run_oracle(w, lib=lib)
+    if not torch.equal(r.state[0], w.state[0]):
+        raise AssertionError("pad slot was written")
+    zeroed = w.state.clone()
+    zeroed[0] = 0
+    r2 = run_oracle(workloads.replace(w, state=zeroed), lib=lib)
+    if not torch.equal(r2.y_exact, r.y_exact):
+        raise AssertionError("a pad read is not a zero state")
+
+
+def pin_disable_and_untouched(lib):
+    """disable_state_update leaves the pool bit-identical and changes no y;
+    slots that are not written keep their bytes."""
+    w = _problem(32, kind="packed", tables="distinct", nseq=4, max_len=3, slots=40,
+                 state_dtype=torch.bfloat16)
+    r = run_oracle(w, lib=lib)
+    written = set(_touched(r, oracle.TOUCH_WRITTEN))
+    for s in range(w.state.shape[0]):
+        if s not in written and not torch.equal(r.state[s], w.state[s]):
+            raise AssertionError(f"untouched slot {s} changed")
+    rd = run_oracle(workloads.replace(w, disable_state_update=True), lib=lib)
+    if not torch.equal(rd.state, w.state):
+        raise AssertionError("disable_state_update changed the pool")
+    if not torch.equal(rd.y_exact, r.y_exact):
+        raise AssertionError("disable_state_update changed y")
+
+
+def pin_table_forms(lib):
+    """No table == identity table; no destination table == destination equal to
+    the read table; one-token == packed with every length 1."""
+    w = _problem(33, kind="onetoken", tables="none", nseq=5, slots=5)
+    ident = torch.arange(5, dtype=torch.int32)
+    a = run_oracle(w, lib=lib)
+    b = run_oracle(workloads.replace(w, read=ident, dst=ident.clone()), lib=lib)
+    if not (torch.equal(a.state, b.state) and torch.equal(a.y_exact, b.y_exact)):
+        raise AssertionError("no table != identity table")
+    w = _problem(34, kind="packed", tables="read", nseq=3, max_len=3, slots=20)
+    a = run_oracle(w, lib=lib)
+    b = run_oracle(workloads.replace(w, dst=w.read.clone()), lib=lib)
+    if not (torch.equal(a.state, b.state) and torch.equal(a.y_exact, b.y_exact)):
+        raise AssertionError("absent destination table != destination = read table")
+    w = _problem(35, kind="onetoken", tables="distinct", nseq=4, slots=20)
+    a = run_oracle(w, lib=lib)
+    cu = torch.arange(0, 5, dtype=torch.int32)
+    b = run_oracle(workloads.replace(w, kind="packed", cu_seqlens=cu, read=w.read.view(4, 1),
+                                     dst=w.dst.view(4, 1), meta={"lengths": [1] * 4}), lib=lib)
+    if not (torch.equal(a.state, b.state) and torch.equal(a.y_exact, b.y_exact)):
+        raise AssertionError("one-token != packed with lengths 1")
+
+
+def pin_seed_position(lib):
+    """The read slot is table[b, max(num_accepted - 1, 0)].  Slot s holds the
+    constant s + 1, dt' = 0 and x = 0, so y = (s + 1) * sum(C) names s."""
+    nseq, steps, slots = 4, 4, 16
+    state = torch.arange(1, slots + 1, dtype=torch.float64).view(slots, 1, 1, 1).repeat(1, 1, 1, 2)
+    read = torch.arange(nseq * steps).view(nseq, steps)
+    rows = nseq * steps
+    x = torch.zeros((rows, 1, 1))
+    dt = torch.zeros((rows, 1, 1))
+    B = torch.zeros((rows, 1, 2))
+    C = torch.ones((rows, 1, 2))
+    for acc, t_seed in (([0, 1, 2, 4], [0, 0, 1, 3]), ([3, 3, 1, 2], [2, 2, 0, 1])):
+        res = oracle.ssu(state, x, dt, torch.zeros(1), B, C, read=oracle.Table.of(read),
+                         dst=oracle.Table.of(read + 0), cu_seqlens=torch.arange(0, rows + 1, steps),
+                         num_accepted=torch.tensor(acc), lib=lib)
+        for b in range(nseq):
+            expect = 2.0 * (read[b, t_seed[b]] + 1)
+            if res.y_exact[b * steps, 0, 0] != expect:
+                raise AssertionError(f"seed of sequence {b} with num_accepted {acc[b]}")
+
+
+def pin_seed_position_per_row(lib):
+    """PER_ROW addressing: sequence b's step t uses flat entry cu_seqlens[b] + t.
+    Lengths [2, 0, 3, 1] give cu_seqlens [0, 2, 2, 5, 6]; with num_accepted
+    [2, 1, 1, 1] the seeds are entries 1, -, 2, 5 (worked by hand)."""
+    slots, rows = 12, 6
+    state = torch.arange(1, slots + 1, dtype=torch.float64).view(slots, 1, 1, 1).repeat(1, 1, 1, 2)
+    tab = torch.tensor([7, 3, 9, 4, 10, 2])           # entry -> slot
+    cu = torch.tensor([0, 2, 2, 5, 6])
+    x, dt, B = torch.zeros((rows, 1, 1)), torch.zeros((rows, 1, 1)), torch.zeros((rows, 1, 2))
+    C = torch.ones((rows, 1, 2))
+    res = oracle.ssu(state, x, dt, torch.zeros(1), B, C,
+                     read=oracle.Table.of(tab, oracle.SLOTS_PER_ROW), cu_seqlens=cu,
+                     num_accepted=torch.tensor([2, 1, 1, 1]), lib=lib)
+    for row, seed_entry in ((0, 1), (2, 2), (5, 5)):
+        if res.y_exact[row, 0, 0] != 2.0 * (int(tab[seed_entry]) + 1):
+            raise AssertionError(f"per-row seed of the sequence starting at row {row}")
+    if _touched(res, oracle.TOUCH_WRITTEN) != sorted(tab.tolist()):
+        raise AssertionError("per-row: every row publishes to its own entry")
+
+
+def pin_per_head_dt(lib):
+    """A per-head step dt [rows, heads] is the full [rows, heads, dim] step with
+    each head's value repeated over dim."""
+    w = _problem(39, kind="packed", tables="distinct", nseq=3, max_len=3, slots=40, per_head_dt=True)
+    full = w.dt[:, :, None].expand(-1, -1, w.x.shape[2]).contiguous()
+    a = run_oracle(w, lib=lib)
+    b = run_oracle(workloads.replace(w, dt=full), lib=lib)
+    if not (torch.equal(a.state, b.state) and torch.equal(a.y_exact, b.y_exact)):
+        raise AssertionError("per-head dt differs from the broadcast full dt")
+    if torch.equal(w.dt[:, 0], w.dt[:, 1]):
+        raise AssertionError("test needs distinct per-head steps")
+
+
+def pin_aliasing_refused(lib):
+    """Cross-sequence aliasing has no deterministic answer and is refused;
+    a sequence reading its own later destination is fine."""
+    w = _problem(36, kind="packed", tables="distinct", pad_frac=0.0, nseq=3, max_len=2,
+                 allow_empty=False, slots=20)
+    bad = w.dst.clone()
+    bad[1, 0] = bad[0, 0]
+    try:
+        run_oracle(workloads.replace(w, dst=bad), lib=lib)
+        raise AssertionError("write-write collision accepted")
+    except oracle.OracleError as e:
+        if e.code != oracle.ALIASING:
+            raise
+    bad = w.dst.clone()
+    t0 = max(int(w.num_accepted[0]) - 1, 0)
+    bad[1, 0] = w.read[0, t0]
+    try:
+        run_oracle(workloads.replace(w, dst=bad), lib=lib)
+        raise AssertionError("overwritten seed accepted")
+    except oracle.OracleError as e:
+        if e.code != oracle.ALIASING:
+            raise
+    # the same tables are fine when nothing is written
+    run_oracle(workloads.replace(w, dst=bad, disable_state_update=True), lib=lib)
+    ok = w.dst.clone()
+    ok[0, 0] = w.read[0, t0]      # sequence 0 overwrites its own seed
+    run_oracle(workloads.replace(w, dst=ok), lib=lib)
+
+
+def pin_empty_sequences(lib):
+    """Empty sequences are skipped: nothing read, nothing written."""
+    w = _problem(37, kind="packed", tables="distinct", pad_frac=0.0, nseq=6, max_len=2, slots=40)
+    lens = w.meta["lengths"]
+    assert 0 in lens
+    r = run_oracle(w, lib=lib)
+    for b, L in enumerate(lens):
+        if L == 0:
+            for s in w.dst[b].tolist() + w.read[b].tolist():
+                if r.touched[s] != 0:
+                    raise AssertionError("an empty sequence touched a slot")
+
+
+def pin_bounded_decay(lib):
+    """A < 0 and dt' >= 0 give 0 < dA <= 1, so |S'| <= |S| + |dt' x B|."""
+    w = _problem(38, kind="onetoken", tables="distinct", pad_frac=0.0)
+    r = run_oracle(w, lib=lib)
+    g = _groups_of(w)
+    S0, d, xn, Bn = _seed_state(w), _dt_eff(w), f64(w.x), f64(w.B)
+    for b in range(w.nseq):
+        bound = np.abs(S0[b]) + np.abs((d[b] * xn[b])[:, :, None] * Bn[b, g][:, None, :])
+        if np.any(np.abs(f64(r.state[int(w.dst[b])])) > bound * (1 + 1e-12) + 1e-300):
+            raise AssertionError("decay bound violated")
+
+
+ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero, pin_zero_state,
+            pin_A_zero, pin_decay_only, pin_unrolled, pin_basis_vectors, pin_group_map,
+            pin_page_examples, pin_pad_never_written, pin_disable_and_untouched, pin_table_forms,
+            pin_seed_position, pin_seed_position_per_row, pin_per_head_dt, pin_aliasing_refused, pin_empty_sequences, pin_bounded_decay]

@@ -1,0 +1,62 @@
+"""Plant plausible mistakes in copies of the oracle's C source and check that
+the pins catch every one of them (no GPU needed).  The copies are compiled
+into a temporary directory; the real oracle is untouched."""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ssu_oracle.c")
+
+# (name, text in ssu_oracle.c, replacement)
+MUTATIONS = [
+    ("drop_D_term", "y += Dh * xv;", "y += 0.0 * xv;"),
+    ("y_from_old_state",
+     "S[n] = S[n] * dA + d * xv * load_elem(pr->B, bc + n, pr->io_dtype);\n"
+     "                        y += S[n] * load_elem(pr->C, bc + n, pr->io_dtype);",
+     "y += S[n] * load_elem(pr->C, bc + n, pr->io_dtype);\n"
+     "                        S[n] = S[n] * dA + d * xv * load_elem(pr->B, bc + n, pr->io_dtype);"),
+    ("decay_sign", "exp(A * d)", "exp(-A * d)"),
+    ("swap_B_C", "d * xv * load_elem(pr->B, bc + n", "d * xv * load_elem(pr->C, bc + n"),
+    ("drop_x", "d * xv * load_elem", "d * load_elem"),
+    ("softplus_sign", "log1p(exp(-fabs(v)))", "log1p(exp(fabs(v)))"),
+    ("gate_sigmoid", "return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    ("seed_off_by_one", "t_seed = pr->num_accepted[b] - 1;", "t_seed = pr->num_accepted[b];"),
+    ("group_modulo", "const int64_t g = h / heads_per_group;", "const int64_t g = h % G;"),
+    ("drop_bias", "+ bias;", "+ 0.0 * bias;"),
+    ("pad_written",
+     "if (!pr->disable_state_update && wslot[r] != pr->pad_slot_id)",
+     "if (!pr->disable_state_update && wslot[r] >= 0)"),
+    ("disable_ignored", "if (!pr->disable_state_update && wslot[r]", "if (wslot[r]"),
+    ("per_row_as_strided", "return row_start + step;", "return b + step;"),
+    ("publish_seed_entry", "if (resolve(wtab, b, t, start[b], &w) != 0)",
+     "if (resolve(wtab, b, 0, start[b], &w) != 0)"),
+    ("bf16_truncates", "double r = round_to_format(v, 7, -126, 127);", "double r = trunc(v * 128.0) / 128.0;"),
+    ("pad_reads_state", "S[n] = (seed[b] == pr->pad_slot_id)", "S[n] = (seed[b] < 0)"),
+    ("dt_per_head_wrong_head", "const int64_t dti = pr->dt_per_head ? (r * H + h) : xi;",
+     "const int64_t dti = pr->dt_per_head ? (r * H) : xi;"),
+]
+
+
+@pytest.fixture(scope="module")
+def src_text():
+    with open(SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(name, old, new, src_text, tmp_path):
+    assert src_text.count(old) >= 1, f"mutation {name}: pattern not found in the oracle source"
+    mutated = src_text.replace(old, new)
+    path = tmp_path / f"orc_{name}.c"
+    path.write_text(mutated)
+    lib = oracle.load_library(oracle.compile_source(str(path), str(tmp_path / f"lib_{name}.so")))
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(lib)
+        except Exception as e:            # AssertionError, OracleError, ...
+            caught.append(f"{pin.__name__}: {str(e)[:80]}")
+    assert caught, f"no pin caught the planted mistake {name}"

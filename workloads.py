@@ -1,0 +1,293 @@
+"""Seeded synthetic inputs for the selective state update.
+
+This module only draws random numbers and lays out tables; it holds none of
+the update's arithmetic.  The oracle, the CUDA tests and the benchmark all take
+their inputs from here.
+
+The five named workloads follow the shapes, dtypes and value distributions of
+the decode workloads this library is measured on:
+
+  tiny_onetoken   batch 2, heads 8, dim 8, dstate 128, groups 2; fp16 zero
+                  state; no slot tables (the minimal example of the MATE
+                  "Mamba / SSU" page).
+  b256_fp32       batch 256 one-token decode, heads 128, dim 64, dstate 128,
+                  groups 8, fp32 pool of 512 slots, random distinct read and
+                  destination slots with 5% pad (pad id 0), softplus with bias.
+  b1024_bf16      batch 1024 one-token decode, bf16 pool of 1024 slots,
+                  identity tables, pad id -1.
+  mtp_64x7_fp32   64 sequences x 7 speculative rows (448 rows), fp32 pool of
+                  1024 slots, 2-D read table arange(448).view(64, 7),
+                  destination table read + 448, num_accepted U{1..7}.
+  varlen_fp16     128 sequences with lengths U{0..8}, heads 64, groups 1,
+                  fp16 pool of 2048 slots, one flat [rows] read table (no
+                  destination table), 3% pad (pad id -1), read per packed row.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import torch
+
+SLOTS_STRIDED = 0   # entry = b*s0 + t*s1 (a flat table is addressed as [n, 1])
+SLOTS_PER_ROW = 1   # entry = cu_seqlens[b] + t (one entry per packed row)
+
+
+@dataclass
+class Workload:
+    name: str
+    kind: str                                  # "onetoken" or "packed"
+    state: torch.Tensor                        # [slots, heads, dim, dstate]
+    x: torch.Tensor                            # [rows, heads, dim]
+    dt: torch.Tensor                           # [rows, heads, dim] or [rows, heads]
+    A: torch.Tensor                            # [heads] fp32
+    B: torch.Tensor                            # [rows, groups, dstate]
+    C: torch.Tensor                            # [rows, groups, dstate]
+    D: Optional[torch.Tensor] = None           # [heads] fp32
+    z: Optional[torch.Tensor] = None           # [rows, heads, dim]
+    dt_bias: Optional[torch.Tensor] = None     # [heads] fp32
+    dt_softplus: bool = False
+    read: Optional[torch.Tensor] = None        # slot table (int32)
+    dst: Optional[torch.Tensor] = None         # slot table (int32)
+    slot_mode: int = SLOTS_STRIDED
+    pad_slot_id: int = -1
+    disable_state_update: bool = False
+    cu_seqlens: Optional[torch.Tensor] = None  # [nseq + 1] int32
+    num_accepted: Optional[torch.Tensor] = None  # [nseq] int32
+    dense_steps: int = 0                       # >0: dense [nseq, steps, ...] form, no cu_seqlens
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def rows(self) -> int:
+        return self.x.shape[0]
+
+    @property
+    def nseq(self) -> int:
+        if self.kind == "onetoken":
+            return self.rows
+        if self.cu_seqlens is not None:
+            return self.cu_seqlens.numel() - 1
+        return self.rows // self.dense_steps
+
+    def to(self, device) -> "Workload":
+        moved = {}
+        for k, v in self.__dict__.items():
+            moved[k] = v.to(device) if isinstance(v, torch.Tensor) else v
+        return replace(self, **moved)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _normal(shape, g, device, mean=0.0, std=1.0, dtype=torch.float32):
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    return (t * std + mean).to(dtype)
+
+
+def _uniform(shape, g, device, lo=0.0, hi=1.0):
+    return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
+
+
+def _decode_inputs(g, device, rows, heads, dim, dstate, groups, io_dtype):
+    """x, z, B, C ~ N(0,1) in the io dtype; dt ~ N(0,1) fp32;
+    dt_bias ~ N(-3, 0.5); A = -exp(U(0, 2.8)); D ~ N(0, 1)."""
+    x = _normal((rows, heads, dim), g, device, dtype=io_dtype)
+    z = _normal((rows, heads, dim), g, device, dtype=io_dtype)
+    dt = _normal((rows, heads, dim), g, device)
+    dt_bias = _normal((heads,), g, device, mean=-3.0, std=0.5)
+    A = -torch.exp(_uniform((heads,), g, device, 0.0, 2.8))
+    D = _normal((heads,), g, device)
+    B = _normal((rows, groups, dstate), g, device, dtype=io_dtype)
+    C = _normal((rows, groups, dstate), g, device, dtype=io_dtype)
+    return dict(x=x, z=z, dt=dt, dt_bias=dt_bias, A=A, D=D, B=B, C=C)
+
+
+def _pool(g, device, slots, heads, dim, dstate, dtype, std=0.1):
+    return _normal((slots, heads, dim, dstate), g, device, std=std, dtype=dtype)
+
+
+def tiny_onetoken(device="cpu", seed=1001) -> Workload:
+    g = _gen(seed, device)
+    batch, heads, dim, dstate, groups = 2, 8, 8, 128, 2
+    state = torch.zeros((batch, heads, dim, dstate), dtype=torch.float16, device=device)
+    x = _normal((batch, heads, dim), g, device, dtype=torch.bfloat16)
+    dt = _uniform((batch, heads, dim), g, device, 0.0, 0.1)
+    A = -_uniform((heads,), g, device)
+    B = _normal((batch, groups, dstate), g, device, dtype=torch.bfloat16)
+    C = _normal((batch, groups, dstate), g, device, dtype=torch.bfloat16)
+    return Workload("tiny_onetoken", "onetoken", state, x, dt, A, B, C)
+
+
+def _distinct_tables_with_pad(g, batch, slots, pad, n_pad, device):
+    """Read and destination tables whose non-pad entries are distinct slots,
+    disjoint between the two tables, never the pad slot; exactly ``n_pad``
+    entries of each table (at random positions) are the pad id."""
+    candidates = torch.tensor([s for s in range(slots) if s != pad], dtype=torch.int64)
+    perm = candidates[torch.randperm(candidates.numel(), generator=g)]
+    read = perm[:batch].clone()
+    dst = perm[batch:2 * batch].clone()
+    for t in (read, dst):
+        pos = torch.randperm(batch, generator=g)[:n_pad]
+        t[pos] = pad
+    return read.to(torch.int32).to(device), dst.to(torch.int32).to(device)
+
+
+def b256_fp32(device="cpu", seed=1002, in_place=False) -> Workload:
+    heads, dim, dstate, groups, slots, batch, pad = 128, 64, 128, 8, 512, 256, 0
+    g = _gen(seed, device)
+    inp = _decode_inputs(g, device, batch, heads, dim, dstate, groups, torch.bfloat16)
+    state = _pool(g, device, slots, heads, dim, dstate, torch.float32)
+    gh = _gen(seed + 7, "cpu")
+    read, dst = _distinct_tables_with_pad(gh, batch, slots, pad, round(0.05 * batch), device)
+    if in_place:
+        dst = read.clone()
+    return Workload("b256_fp32" + ("_inplace" if in_place else ""), "onetoken", state,
+                    dt_softplus=True, read=read, dst=dst, pad_slot_id=pad, **inp)
+
+
+def b1024_bf16(device="cpu", seed=1003) -> Workload:
+    heads, dim, dstate, groups, slots, batch = 128, 64, 128, 8, 1024, 1024
+    g = _gen(seed, device)
+    inp = _decode_inputs(g, device, batch, heads, dim, dstate, groups, torch.bfloat16)
+    state = _pool(g, device, slots, heads, dim, dstate, torch.bfloat16)
+    ident = torch.arange(batch, dtype=torch.int32, device=device)
+    return Workload("b1024_bf16", "onetoken", state, dt_softplus=True, read=ident,
+                    dst=ident.clone(), pad_slot_id=-1, **inp)
+
+
+def mtp_64x7_fp32(device="cpu", seed=1004) -> Workload:
+    heads, dim, dstate, groups, slots, nseq, steps = 128, 64, 128, 8, 1024, 64, 7
+    rows = nseq * steps
+    g = _gen(seed, device)
+    inp = _decode_inputs(g, device, rows, heads, dim, dstate, groups, torch.bfloat16)
+    state = _pool(g, device, slots, heads, dim, dstate, torch.float32)
+    gh = _gen(seed + 7, "cpu")
+    read = torch.arange(rows, dtype=torch.int32, device=device).view(nseq, steps)
+    dst = (read + rows).contiguous()
+    cu = torch.arange(0, rows + 1, steps, dtype=torch.int32, device=device)
+    acc = torch.randint(1, steps + 1, (nseq,), generator=gh, dtype=torch.int64).to(torch.int32).to(device)
+    return Workload("mtp_64x7_fp32", "packed", state, dt_softplus=True, read=read, dst=dst,
+                    pad_slot_id=-1, cu_seqlens=cu, num_accepted=acc, **inp)
+
+
+def varlen_fp16(device="cpu", seed=1005, disable_state_update=False,
+                slot_mode=SLOTS_PER_ROW) -> Workload:
+    heads, dim, dstate, groups, slots, nseq = 64, 64, 128, 1, 2048, 128
+    gh = _gen(seed + 7, "cpu")
+    lens = torch.randint(0, 9, (nseq,), generator=gh, dtype=torch.int64)
+    lens[int(torch.randint(0, nseq, (1,), generator=gh))] = 0   # at least one empty sequence
+    rows = int(lens.sum())
+    cu = torch.zeros(nseq + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lens, 0)
+    acc = torch.ones(nseq, dtype=torch.int64)
+    for b in range(nseq):
+        if lens[b] > 0:
+            acc[b] = int(torch.randint(1, int(lens[b]) + 1, (1,), generator=gh))
+    read = torch.randperm(slots, generator=gh)[:rows].clone()
+    n_pad = round(0.03 * rows)
+    read[torch.randperm(rows, generator=gh)[:n_pad]] = -1
+    g = _gen(seed, device)
+    inp = _decode_inputs(g, device, rows, heads, dim, dstate, groups, torch.bfloat16)
+    state = _pool(g, device, slots, heads, dim, dstate, torch.float16)
+    name = "varlen_fp16" + ("_disable" if disable_state_update else "")
+    if slot_mode == SLOTS_STRIDED:
+        name += "_strided"
+    return Workload(name, "packed", state, dt_softplus=True,
+                    read=read.to(torch.int32).to(device), dst=None, slot_mode=slot_mode,
+                    pad_slot_id=-1, disable_state_update=disable_state_update,
+                    cu_seqlens=cu.to(torch.int32).to(device),
+                    num_accepted=acc.to(torch.int32).to(device), meta={"lengths": lens.tolist()}, **inp)
+
+
+NAMED = {
+    "tiny_onetoken": tiny_onetoken,
+    "b256_fp32": b256_fp32,
+    "b1024_bf16": b1024_bf16,
+    "mtp_64x7_fp32": mtp_64x7_fp32,
+    "varlen_fp16": varlen_fp16,
+}
+
+
+def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads: int = 4,
+                   dim: int = 8, dstate: int = 16, groups: int = 2, nseq: int = 3,
+                   max_len: int = 3, state_dtype=torch.float32, io_dtype=torch.bfloat16,
+                   dt_dtype=torch.float32, per_head_dt: bool = False, with_D: bool = True,
+                   with_z: bool = True, with_bias: bool = True, dt_softplus: bool = True,
+                   tables: str = "distinct", pad_slot_id: int = -1, pad_frac: float = 0.2,
+                   slot_mode: int = SLOTS_STRIDED, with_accepted: bool = True,
+                   allow_empty: bool = True, disable_state_update: bool = False,
+                   state_std: float = 0.5, dense: bool = False, device="cpu") -> Workload:
+    """A small seeded problem for parity sweeps.
+
+    ``tables``: "none" (sequence b uses slot b), "read" (read table only),
+    "distinct" (read and destination tables of distinct, disjoint slots),
+    "inplace" (destination table equal to the read table).
+    For ``kind="packed"`` the read/destination tables are 2-D ``[nseq, max_len]``
+    in STRIDED mode, or flat ``[rows]`` in PER_ROW mode; ``dense`` makes every
+    sequence ``max_len`` long and drops cu_seqlens (the dense 4-D form).
+    """
+    gh = _gen(seed, "cpu")
+    if kind == "onetoken":
+        lens = torch.ones(nseq, dtype=torch.int64)
+    elif dense:
+        lens = torch.full((nseq,), max_len, dtype=torch.int64)
+    else:
+        lens = torch.randint(0 if allow_empty else 1, max_len + 1, (nseq,), generator=gh)
+    rows = int(lens.sum())
+    cu = torch.zeros(nseq + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(lens, 0)
+    per_seq = 1 if kind == "onetoken" else max_len
+    # entries needed by each table
+    if kind == "onetoken" or slot_mode == SLOTS_PER_ROW:
+        n_entries = rows if kind == "packed" else nseq
+    else:
+        n_entries = nseq * per_seq
+    need = n_entries * (2 if tables == "distinct" else 1)
+    usable = torch.tensor([s for s in range(slots) if s != pad_slot_id], dtype=torch.int64)
+    if tables != "none" and need > usable.numel():
+        raise ValueError(f"need {need} distinct slots, have {usable.numel()}")
+    perm = usable[torch.randperm(usable.numel(), generator=gh)]
+    read = dst = None
+    if tables != "none":
+        read = perm[:n_entries].clone()
+        if tables == "distinct":
+            dst = perm[n_entries:2 * n_entries].clone()
+        n_pad = int(round(pad_frac * n_entries))
+        for t in (read, dst):
+            if t is not None and n_pad > 0:
+                t[torch.randperm(n_entries, generator=gh)[:n_pad]] = pad_slot_id
+        if tables == "inplace":
+            dst = read.clone()
+        if kind == "packed" and slot_mode == SLOTS_STRIDED:
+            read = read.view(nseq, per_seq)
+            dst = None if dst is None else dst.view(nseq, per_seq)
+        read = read.to(torch.int32)
+        dst = None if dst is None else dst.to(torch.int32)
+    acc = None
+    if kind == "packed" and with_accepted:
+        acc = torch.ones(nseq, dtype=torch.int64)
+        for b in range(nseq):
+            if lens[b] > 0:
+                acc[b] = int(torch.randint(1, int(lens[b]) + 1, (1,), generator=gh))
+        acc = acc.to(torch.int32)
+    g = _gen(seed + 1, "cpu")
+    x = _normal((rows, heads, dim), g, "cpu", dtype=io_dtype)
+    z = _normal((rows, heads, dim), g, "cpu", dtype=io_dtype) if with_z else None
+    dt_shape = (rows, heads) if per_head_dt else (rows, heads, dim)
+    dt = (_normal(dt_shape, g, "cpu") if dt_softplus else _uniform(dt_shape, g, "cpu", 0.0, 0.2)).to(dt_dtype)
+    dt_bias = _normal((heads,), g, "cpu", mean=-1.0, std=0.5) if with_bias else None
+    A = -torch.exp(_uniform((heads,), g, "cpu", 0.0, 2.8))
+    D = _normal((heads,), g, "cpu") if with_D else None
+    B = _normal((rows, groups, dstate), g, "cpu", dtype=io_dtype)
+    C = _normal((rows, groups, dstate), g, "cpu", dtype=io_dtype)
+    state = _pool(g, "cpu", slots, heads, dim, dstate, state_dtype, std=state_std)
+    w = Workload(f"random_{kind}_{seed}", kind, state, x, dt, A, B, C, D=D, z=z, dt_bias=dt_bias,
+                 dt_softplus=dt_softplus, read=read, dst=dst, slot_mode=slot_mode,
+                 pad_slot_id=pad_slot_id, disable_state_update=disable_state_update,
+                 cu_seqlens=None if (kind == "onetoken" or dense) else cu.to(torch.int32),
+                 num_accepted=acc, dense_steps=max_len if dense else 0,
+                 meta={"lengths": lens.tolist()})
+    return w.to(device)
