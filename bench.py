@@ -1,0 +1,499 @@
+"""Benchmark of libssu's selective state update on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the update over one batch of the workload (default:
+batch-256 one-token decode, fp32 state pool; every step of the update runs in
+one kernel launch).  Inputs are resident in HBM when the timed region starts;
+the touched state (about 2 GB per step) is far larger than L2, so no flush is
+needed between steps.  Prints ONE JSON line.
+
+--impl reference times the CPU oracle (the plain double-precision definition)
+on the host cores, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "SSU state-updates/s and achieved HBM GB/s (% of GB300 peak) at batch 256"
+UNIT = "state-updates/s"
+FALLBACK_HBM_GBS = 6800.0
+
+DESCRIPTIONS = {
+    "b256_fp32": "one-token decode, batch 256, heads 128, dim 64, dstate 128, groups 8, fp32 state "
+                 "pool of 512 slots, random distinct read/destination slots with 5% pad (id 0), "
+                 "bf16 x/z/B/C, fp32 dt with bias and softplus, D",
+    "b1024_bf16": "one-token decode, batch 1024, heads 128, dim 64, dstate 128, groups 8, bf16 state "
+                  "pool of 1024 slots, identity tables",
+    "mtp_64x7_fp32": "MTP packed decode, 64 sequences x 7 rows, heads 128, dim 64, dstate 128, groups 8, "
+                     "fp32 pool of 1024 slots, 2-D read table, destination table read+448, "
+                     "num_accepted U{1..7}",
+    "varlen_fp16": "variable-length packed decode, 128 sequences of length U{0..8}, heads 64, dim 64, "
+                   "dstate 128, groups 1, fp16 pool of 2048 slots, flat per-row read table, 3% pad",
+    "tiny_onetoken": "one-token decode, batch 2, heads 8, dim 8, dstate 128, groups 2, fp16 zero state",
+}
+KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
+                  "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"]}
+
+
+# --------------------------------------------------------------------------
+# Accounting (host side, from the tables).
+# --------------------------------------------------------------------------
+def _lengths(w):
+    if w.kind == "onetoken":
+        return [1] * w.nseq
+    if w.cu_seqlens is not None:
+        cu = w.cu_seqlens.cpu().tolist()
+        return [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    return [w.dense_steps] * w.nseq
+
+
+def _entry_slot(table, w, b, t, cu):
+    if table is None:
+        return b
+    flat = table.reshape(-1)
+    if w.kind == "onetoken":
+        return int(flat[b])
+    if w.slot_mode == workloads.SLOTS_PER_ROW:
+        return int(flat[cu[b] + t])
+    if table.dim() == 1:
+        return int(flat[b + t])
+    return int(table[b, t])
+
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes one call must move: each non-pad seed read once, each non-pad
+    destination written once per token, plus every small operand once."""
+    H, P, N = w.state.shape[1:]
+    sb = H * P * N * w.state.element_size()
+    lens = _lengths(w)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    read_tab = None if w.read is None else w.read.cpu()
+    dst_tab = None if w.dst is None else w.dst.cpu()
+    acc = None if w.num_accepted is None else w.num_accepted.cpu().tolist()
+    seeds = writes = 0
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        t_seed = max(acc[b] - 1, 0) if (acc is not None and w.kind == "packed") else 0
+        if _entry_slot(read_tab, w, b, t_seed, cu) != w.pad_slot_id:
+            seeds += 1
+        if w.disable_state_update:
+            continue
+        wt = dst_tab if dst_tab is not None else read_tab
+        for t in range(L):
+            if _entry_slot(wt, w, b, t, cu) != w.pad_slot_id:
+                writes += 1
+    small = 0
+    for t in (w.x, w.dt, w.B, w.C, w.z, w.A, w.D, w.dt_bias, w.read, w.dst, w.cu_seqlens,
+              w.num_accepted):
+        if t is not None:
+            small += t.numel() * t.element_size()
+    small += w.x.numel() * w.x.element_size()     # y
+    return {"state_read": seeds * sb, "state_write": writes * sb, "small": small,
+            "total": (seeds + writes) * sb + small, "seeds": seeds, "writes": writes,
+            "state_bytes_per_unit": sb}
+
+
+def kernel_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "selective_state_update_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture in profiles/, if that
+    capture was taken of the kernel source as it is now."""
+    path = os.path.join(ROOT, "profiles", f"ssu_{kind}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    hm = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not hm or hm.group(1) != kernel_hash(kind):
+        return None
+    return int(m.group(1))
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------
+# Clocks sampled while the timed region runs.
+# --------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        # nvidia-smi numbers GPUs physically; name ours by its UUID.
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            self.dev = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            self.dev = str(device.index or 0)
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.dev), "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# Our arm.
+# --------------------------------------------------------------------------
+def _call(ssu, w, out, stream=None):
+    common = dict(D=w.D, z=w.z, dt_bias=w.dt_bias, dt_softplus=w.dt_softplus,
+                  state_batch_indices=w.read, dst_state_batch_indices=w.dst,
+                  pad_slot_id=w.pad_slot_id, disable_state_update=w.disable_state_update, out=out,
+                  stream=stream)
+    if w.kind == "onetoken":
+        return ssu.ssu_update_onetoken(w.state, w.x, w.dt, w.A, w.B, w.C, **common)
+    return ssu.ssu_update_packed(w.state, w.x, w.dt, w.A, w.B, w.C, cu_seqlens=w.cu_seqlens,
+                                 num_accepted_tokens=w.num_accepted, slot_mode=w.slot_mode, **common)
+
+
+def _per_step_inputs(w):
+    return [t for t in (w.x, w.dt, w.z, w.B, w.C, w.read, w.dst, w.cu_seqlens, w.num_accepted)
+            if t is not None]
+
+
+def run_ours(args, rank, world, device):
+    from selective_state_update_gb300 import build as ssu_build
+    import selective_state_update_gb300 as ssu
+    ssu_build.build()
+    ssu.lib()
+    gen = workloads.NAMED[args.workload]
+    w = gen(device=device, seed=1000 + 97 * rank + {"tiny_onetoken": 1, "b256_fp32": 2, "b1024_bf16": 3,
+                                                     "mtp_64x7_fp32": 4, "varlen_fp16": 5}[args.workload])
+    torch.cuda.synchronize()
+    acct = algorithmic_bytes(w)
+    tokens = w.rows
+    ssu.ssu_prewarm(state_dtype=w.state.dtype, io_dtype=w.x.dtype, heads=w.state.shape[1],
+                    dim=w.state.shape[2], dstate=w.state.shape[3], groups=w.B.shape[1],
+                    packed=w.kind == "packed")
+    stream = torch.cuda.current_stream()
+    out = torch.empty_like(w.x)
+    for _ in range(args.warmup):
+        _call(ssu, w, out)
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clocks:
+        whole0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            _call(ssu, w, out)
+            ev[i][1].record(stream)
+        whole1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = whole0.elapsed_time(whole1)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # End to end through the public call: per step, pinned host -> device
+    # copies of the step's inputs, the update, and y back to pinned host.
+    host_in = [t.cpu().pin_memory() for t in _per_step_inputs(w)]
+    dev_in = _per_step_inputs(w)
+    host_y = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_y.numel() * host_y.element_size()
+    e2e_steps = max(3, min(args.steps, 400))
+    for _ in range(2):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        _call(ssu, w, out)
+        host_y.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        _call(ssu, w, out)
+        host_y.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    peak, peak_src = hbm_peak()
+    achieved = acct["total"] / (launch_ms * 1e-3) / 1e9
+    kind = w.kind
+    result = {
+        "metric": METRIC,
+        "value": tokens * world * args.steps / (total_ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "sequences_per_gpu": w.nseq, "rows_per_gpu": tokens,
+                   "state_dtype": str(w.state.dtype).replace("torch.", ""),
+                   "io_dtype": str(w.x.dtype).replace("torch.", ""),
+                   "parallelism": f"{world} independent replicas (one pool and batch per GPU)",
+                   "l2": "no flush: inputs larger than L2 (%.2f GB of state moved per step)"
+                         % ((acct["state_read"] + acct["state_write"]) / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth",
+                     "traffic": profiled_traffic(kind, args.workload),
+                     "algorithmic_bytes_per_launch": acct["total"],
+                     "kernel": f"ssu_{kind}_kernel", "launch_ms": launch_ms},
+        "e2e": {"value": tokens * world * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    return result
+
+
+# --------------------------------------------------------------------------
+# The oracle on the host cores.
+# --------------------------------------------------------------------------
+def _sample_problem(w, seqs):
+    """The sequences `seqs` of workload `w` (CPU tensors) with a compact pool."""
+    from dataclasses import replace
+    lens = _lengths(w)
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    rows = [r for b in seqs for r in range(cu[b], cu[b + 1])]
+    sub_lens = [lens[b] for b in seqs]
+    pad = w.pad_slot_id
+
+    def rows_of(t):
+        if t is None:
+            return None
+        if w.kind == "onetoken":
+            return t.reshape(-1)[seqs]
+        if w.slot_mode == workloads.SLOTS_PER_ROW:
+            return t.reshape(-1)[rows]
+        return t[seqs]
+
+    rd, wr = rows_of(w.read), rows_of(w.dst)
+    used = sorted({int(v) for t in (rd, wr) if t is not None for v in t.reshape(-1).tolist()} - {pad})
+    order = ([pad] if 0 <= pad < w.state.shape[0] else []) + used
+    m = {s: i for i, s in enumerate(order)}
+    new_pad = m.get(pad, pad)
+    remap = lambda t: None if t is None else torch.tensor(
+        [new_pad if v == pad else m[v] for v in t.reshape(-1).tolist()], dtype=t.dtype).view(t.shape)
+    sel = lambda t: None if t is None else t[rows]
+    sub_cu = torch.tensor([sum(sub_lens[:i]) for i in range(len(sub_lens) + 1)], dtype=torch.int32)
+    return replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
+                   read=remap(rd), dst=remap(wr), pad_slot_id=new_pad,
+                   cu_seqlens=sub_cu if w.kind == "packed" else None,
+                   num_accepted=None if w.num_accepted is None else w.num_accepted[seqs], dense_steps=0)
+
+
+def _oracle_call(sub):
+    import oracle
+    mode = oracle.SLOTS_PER_ROW if sub.slot_mode == workloads.SLOTS_PER_ROW else oracle.SLOTS_STRIDED
+    return oracle.ssu(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, D=sub.D, z=sub.z, dt_bias=sub.dt_bias,
+                      dt_softplus=sub.dt_softplus, read=oracle.Table.of(sub.read, mode),
+                      dst=oracle.Table.of(sub.dst, mode), pad_slot_id=sub.pad_slot_id,
+                      disable_state_update=sub.disable_state_update, cu_seqlens=sub.cu_seqlens,
+                      num_accepted=sub.num_accepted if sub.kind == "packed" else None)
+
+
+def _cpu_workload(name):
+    return workloads.NAMED[name](device="cpu")
+
+
+def oracle_rate(w_cpu, budget_s: float):
+    """Time the oracle on samples of `w_cpu` for about `budget_s` seconds;
+    returns (sequence-token updates per second, description)."""
+    import oracle
+    oracle.build()
+    nseq = w_cpu.nseq
+    lens = _lengths(w_cpu)
+    done_tokens, spent, nsamples, idx = 0, 0.0, 0, 0
+    per = 1
+    while spent < budget_s:
+        seqs = [(idx + i) % nseq for i in range(per)]
+        idx += per
+        sub = _sample_problem(w_cpu, seqs)
+        t0 = time.perf_counter()
+        _oracle_call(sub)
+        dt = time.perf_counter() - t0
+        spent += dt
+        done_tokens += sum(lens[b] for b in seqs)
+        nsamples += 1
+        if dt < 0.5 and per < nseq:
+            per = min(nseq, per * 2)
+    return done_tokens / spent, f"{done_tokens} sequence-tokens in {nsamples} samples of consecutive sequences"
+
+
+def run_reference(args):
+    w_cpu = _cpu_workload(args.workload)
+    import oracle
+    oracle.build()
+    lens = _lengths(w_cpu)
+    # one step = the oracle on one sequence; size the run to end within minutes
+    steps_total = args.steps + args.warmup
+    seq_per_step = 1
+    for i in range(args.warmup):
+        _oracle_call(_sample_problem(w_cpu, [i % w_cpu.nseq]))
+    t0 = time.perf_counter()
+    tokens = 0
+    budget = 150.0
+    done_steps = 0
+    for i in range(args.steps):
+        b = (i * 37) % w_cpu.nseq
+        _oracle_call(_sample_problem(w_cpu, [b]))
+        tokens += lens[b]
+        done_steps += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    el = time.perf_counter() - t0
+    value = tokens / el
+    sample = (f"{done_steps} steps of one sequence each ({tokens} sequence-tokens) of the workload; "
+              f"{steps_total} requested")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": done_steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(done_steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(workloads.NAMED), default="b256_fp32")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    # The oracle baseline runs before the first GPU call (no fork after CUDA init).
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        w_cpu = _cpu_workload(args.workload)
+        rate, desc = oracle_rate(w_cpu, args.cpu_baseline_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+        del w_cpu
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (libssu has no CPU path)")
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(device)
+    res = run_ours(args, rank, world, device)
+    res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * ssu.h -- libssu: the Mamba-2 selective state update (SSU) on NVIDIA GB300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * What one call computes (MATE documentation, page "Mamba / SSU": intro
+ * paragraph, "SSU at a glance", API reference of selective_state_update; the
+ * recurrence as written in the article "ReplaySSM: Cache SSM Inputs, Not
+ * State", section 三个瓶颈).  For every token row r of a sequence, every head h
+ * and every dim row p, with g = h / (heads / groups):
+ *
+ *     dt'  = dt[r,h,p] (+ dt_bias[h]);  dt' = softplus(dt') if dt_softplus
+ *     dA   = exp(A[h] * dt')
+ *     S[n] = S[n] * dA + dt' * x[r,h,p] * B[r,g,n]          (n < dstate)
+ *     y[r,h,p] = sum_n S[n] * C[r,g,n] + D[h] * x[r,h,p]
+ *     y[r,h,p] *= z / (1 + exp(-z)),  z = z[r,h,p]            (when z given)
+ *
+ * S is one row of the state pool, read from the sequence's read slot, carried
+ * in fp32 across the sequence's tokens, and published (rounded to nearest
+ * even into the state dtype) to each token's destination slot.  y is
+ * computed in fp32 and rounded to nearest even into the io dtype.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device pointers on the current device;
+ *    the caller owns every buffer.  The library allocates no device memory,
+ *    copies nothing between host and device, and never synchronizes: one
+ *    call is one kernel launch on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  After ssu_prewarm the calls may be captured in
+ *    a CUDA graph.
+ *  - Host-detectable errors return a status, leave a message for
+ *    ssu_last_error(), and launch nothing.
+ *  - Errors only the device can see (a slot outside [0, slots) that is not
+ *    the pad id, a table entry outside the table, malformed cu_seqlens)
+ *    never trap: the kernel ORs an SSU_DEV_* bit into *d_status (when
+ *    d_status is not NULL) and skips the affected (sequence, head) unit:
+ *    none of its state rows and none of its y rows are written.
+ *  - Preconditions not checked: buffers do not overlap except where stated
+ *    (the pool may be read and written through the same slot); no sequence
+ *    writes a slot that another sequence of the same call reads or writes
+ *    (the result would depend on scheduling); y does not alias any input.
+ */
+#ifndef SSU_H
+#define SSU_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSU_OK = 0,
+    SSU_ERR_INVALID = 1,      /* an argument check failed (Python: ValueError)            */
+    SSU_ERR_UNSUPPORTED = 2,  /* the caller asked for something not implemented
+                                 (Python: NotImplementedError)                             */
+    SSU_ERR_CUDA = 3          /* a CUDA runtime call failed (launch or attribute query)    */
+} ssu_status;
+
+/* Element types.  The state pool may be any of the three (MATE "Mamba / SSU",
+ * SSU at a glance, row State).  x, z, y, B and C share one io type (row B / C:
+ * "with the x dtype"; row Output: "in the x dtype").  A, D and dt_bias are
+ * always fp32 (row A / D / dt_bias). */
+typedef enum { SSU_F32 = 0, SSU_F16 = 1, SSU_BF16 = 2 } ssu_dtype;
+
+/* Integer types of slot tables, cu_seqlens and num_accepted_tokens. */
+typedef enum { SSU_I32 = 0, SSU_I64 = 1 } ssu_itype;
+
+/* How a slot table is addressed for (sequence b, step t).
+ *  SSU_SLOTS_STRIDED: entry = b*s0 + t*s1.  This is the page's rule (Slot
+ *    semantics): a flat [n] table is addressed as [n, 1] (s0 = s1 = 1, entry
+ *    b + t) and a contiguous 2-D [seqs, steps] table as b*steps + t.
+ *  SSU_SLOTS_PER_ROW: entry = cu_seqlens[b] + t, one entry per packed row
+ *    (the flat form vLLM's MTP decode passes).  The two agree whenever the
+ *    strided form is free of collisions: one sequence per call, or every
+ *    sequence of length 1 with no empties.  With several sequences longer
+ *    than one token, the strided flat form makes neighbouring sequences share
+ *    entries and is only meaningful with disable_state_update. */
+typedef enum { SSU_SLOTS_STRIDED = 0, SSU_SLOTS_PER_ROW = 1 } ssu_slot_mode;
+
+typedef struct ssu_slot_table {
+    const void *entries;  /* device pointer to `type` entries; NULL = no table        */
+    int32_t type;         /* ssu_itype                                                  */
+    int32_t mode;         /* ssu_slot_mode                                              */
+    int64_t s0, s1;       /* strides in entries (SSU_SLOTS_STRIDED)                     */
+    int64_t extent;       /* entries [0, extent) may be addressed; others set
+                             SSU_DEV_BAD_ENTRY                                          */
+} ssu_slot_table;
+
+/* Bits ORed into *d_status by the kernels. */
+#define SSU_DEV_BAD_SLOT   0x1  /* slot not in [0, slots) and not pad_slot_id       */
+#define SSU_DEV_BAD_ENTRY  0x2  /* table entry index outside [0, extent)            */
+#define SSU_DEV_BAD_SEQLEN 0x4  /* cu_seqlens decreasing, negative or past `rows`   */
+
+/* Arguments of the MATE signature that this library does not implement.  Set
+ * the bit when the caller passed the argument; the call then fails with
+ * SSU_ERR_UNSUPPORTED instead of silently narrowing the semantics (the page
+ * raises NotImplementedError for rand_seed, "Stochastic rounding" row). */
+#define SSU_UNSUP_RAND_SEED          0x01  /* stochastic rounding                     */
+#define SSU_UNSUP_STATE_SCALE        0x02  /* quantised state scales                   */
+#define SSU_UNSUP_INTERMEDIATE       0x04  /* intermediate_states_buffer / indices / scales */
+#define SSU_UNSUP_CACHE_STEPS        0x08  /* cache_steps != 0                         */
+#define SSU_UNSUP_ALGORITHM          0x10  /* algorithm / backend other than "auto"   */
+
+/* Everything both update entry points share.  Strides are in elements. */
+typedef struct ssu_args {
+    int64_t slots, heads, dim, dstate, groups;
+    int32_t state_dtype;          /* ssu_dtype of the pool                                   */
+    int32_t io_dtype;             /* ssu_dtype of x, z, y, B, C (SSU_BF16 or SSU_F16 or SSU_F32) */
+    int32_t dt_dtype;             /* ssu_dtype of dt                                         */
+    int32_t dt_softplus;          /* nonzero: dt' = softplus(dt + dt_bias)                   */
+    int32_t disable_state_update; /* nonzero: the pool is not written (y still is)           */
+    int32_t reserved0;            /* must be 0                                               */
+    int64_t pad_slot_id;          /* slot id that reads as a zero state and is never written */
+    void *state;                  /* device [slots, heads, dim, dstate], contiguous, 16-byte
+                                     aligned; read and written in place                       */
+    const void *x;                /* device [rows, heads, dim] io_dtype                       */
+    const void *dt;               /* device [rows, heads, dim] dt_dtype; dt_stride[2] == 0
+                                     gives one step per head broadcast over dim              */
+    const void *B, *C;            /* device [rows, groups, dstate] io_dtype                   */
+    const void *z;                /* device [rows, heads, dim] io_dtype, or NULL (no gate)     */
+    const float *A;               /* device [heads]                                          */
+    const float *D;               /* device [heads] or NULL (no skip term)                   */
+    const float *dt_bias;         /* device [heads] or NULL                                  */
+    void *y;                      /* device [rows, heads, dim] io_dtype, output              */
+    int64_t x_stride[3], dt_stride[3], B_stride[3], C_stride[3], z_stride[3], y_stride[3];
+    int32_t *d_status;            /* device int32 or NULL; SSU_DEV_* bits are ORed in        */
+    uint32_t unsupported;         /* SSU_UNSUP_* bits; nonzero => SSU_ERR_UNSUPPORTED         */
+} ssu_args;
+
+/*
+ * One decode token per sequence: sequence b is row b (x, dt, z, y are
+ * [batch, heads, dim]; B, C are [batch, groups, dstate]).
+ * MATE "Mamba / SSU": intro paragraph (the one-token kernel); SSU at a glance,
+ * rows Sequence layout, State, Slot semantics.
+ *
+ *   read  NULL or read->entries NULL: sequence b reads slot b.  Otherwise the
+ *         slot at entry (b, 0) of the table (the mode is ignored: a one-token
+ *         call has cu_seqlens[b] = b).
+ *   dst   NULL or dst->entries NULL: the state is written back through the
+ *         read table (or to slot b without one).  Otherwise to entry (b, 0).
+ *   A read of pad_slot_id starts from zeros; a write to it is skipped.
+ * batch == 0 launches nothing and returns SSU_OK.
+ */
+ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch,
+                               const ssu_slot_table *read, const ssu_slot_table *dst,
+                               void *stream);
+
+/*
+ * Packed variable-length / multi-token (MTP) decode: `rows` packed rows split
+ * into `nseq` sequences.  MATE "Mamba / SSU": SSU at a glance, rows Sequence
+ * layout, Slot semantics, Variable-length and MTP decode; Graph capture
+ * (single launch, no host/device scalar copies).
+ *
+ *   cu_seqlens   device [nseq + 1] of meta_type: sequence b owns rows
+ *                [cu_seqlens[b], cu_seqlens[b+1]).  NULL selects the dense
+ *                form: every sequence is `steps` rows long (rows = nseq*steps),
+ *                i.e. x as [nseq, steps, heads, dim] flattened.
+ *   num_accepted device [nseq] of meta_type or NULL.  The read slot of
+ *                sequence b is at step max(num_accepted[b] - 1, 0) (step 0
+ *                without the array).
+ *   read, dst    slot tables addressed per their mode (see ssu_slot_mode).
+ *                No read table: sequence b reads and writes slot b (every
+ *                token overwrites it; the last token's state remains).  No
+ *                destination table: token t publishes through the read
+ *                table's entry (b, t).
+ * Every token publishes its state to its own destination slot unless that
+ * slot is pad_slot_id or disable_state_update is set.  Empty sequences are
+ * skipped.  The state carried between the tokens of a sequence stays in
+ * fp32; only the published copies are rounded.  A sequence may overwrite its
+ * own read slot (the read happens first).
+ * nseq == 0 launches nothing and returns SSU_OK.
+ */
+ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows,
+                             const void *cu_seqlens, int64_t steps,
+                             const void *num_accepted, int32_t meta_type,
+                             const ssu_slot_table *read, const ssu_slot_table *dst,
+                             void *stream);
+
+/*
+ * Get the kernel for one configuration ready before any CUDA graph capture:
+ * checks that the configuration is supported, loads the kernel's module on
+ * the current device and caches its launch attributes.  MATE "Mamba / SSU",
+ * Graph capture and prewarm_selective_state_update (kernels there are
+ * compiled at first use; here they are compiled ahead of time, so this only
+ * loads them).  `packed` selects the packed kernel instead of the one-token
+ * kernel.  Returns SSU_ERR_UNSUPPORTED for a dstate or dtype the kernels do
+ * not cover.
+ */
+ssu_status ssu_prewarm(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype,
+                       int64_t heads, int64_t dim, int64_t dstate, int64_t groups,
+                       int32_t packed);
+
+/* Message for the last non-OK status returned on this thread ("" if none). */
+const char *ssu_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSU_H */

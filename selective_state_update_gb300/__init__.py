@@ -1,0 +1,312 @@
+"""Python binding of libssu, the GB300 (sm_103a) selective state update.
+
+Argument marshalling only: tensors are checked for shape, their pointers and
+strides are packed into the C structs of ``include/ssu.h``, and the C entry
+point launches the CUDA kernel on the current torch stream.  Every step of the
+update runs in the CUDA kernels; there is no CPU or PyTorch fallback.  When
+``libssu.so`` is not built, every call raises.
+
+Entry points (same names as the C ABI):
+  ssu_update_onetoken  one decode token per sequence
+  ssu_update_packed    packed variable-length / MTP rows (cu_seqlens) or the
+                       dense [batch, steps, heads, dim] form
+  ssu_prewarm          load a configuration's kernel before graph capture
+and ``selective_state_update``, the MATE/FlashInfer-shaped call (MATE
+documentation, page "Mamba / SSU", API reference) that picks one of the two
+update entry points from the call shape.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_prewarm", "selective_state_update",
+           "SLOTS_STRIDED", "SLOTS_PER_ROW", "DEV_BAD_SLOT", "DEV_BAD_ENTRY", "DEV_BAD_SEQLEN",
+           "library_path", "lib"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_build", "libssu.so")
+
+# ssu.h constants
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
+SLOTS_STRIDED, SLOTS_PER_ROW = 0, 1
+DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN = 0x1, 0x2, 0x4
+UNSUP_RAND_SEED, UNSUP_STATE_SCALE, UNSUP_INTERMEDIATE, UNSUP_CACHE_STEPS, UNSUP_ALGORITHM = (
+    0x01, 0x02, 0x04, 0x08, 0x10)
+_DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+_ITYPE = {torch.int32: 0, torch.int64: 1}
+
+
+class SlotTable(ctypes.Structure):
+    _fields_ = [("entries", ctypes.c_void_p), ("type", ctypes.c_int32), ("mode", ctypes.c_int32),
+                ("s0", ctypes.c_int64), ("s1", ctypes.c_int64), ("extent", ctypes.c_int64)]
+
+
+_I64x3 = ctypes.c_int64 * 3
+
+
+class Args(ctypes.Structure):
+    _fields_ = [
+        ("slots", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("groups", ctypes.c_int64),
+        ("state_dtype", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32),
+        ("dt_softplus", ctypes.c_int32), ("disable_state_update", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32), ("pad_slot_id", ctypes.c_int64),
+        ("state", ctypes.c_void_p), ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p),
+        ("B", ctypes.c_void_p), ("C", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("y", ctypes.c_void_p),
+        ("x_stride", _I64x3), ("dt_stride", _I64x3), ("B_stride", _I64x3), ("C_stride", _I64x3),
+        ("z_stride", _I64x3), ("y_stride", _I64x3),
+        ("d_status", ctypes.c_void_p), ("unsupported", ctypes.c_uint32),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libssu (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libssu.so is not built ({_LIB_PATH} is missing); build it with "
+                "`python -m selective_state_update_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(_LIB_PATH)
+        p_args, p_tab = ctypes.POINTER(Args), ctypes.POINTER(SlotTable)
+        L.ssu_update_onetoken.argtypes = [p_args, ctypes.c_int64, p_tab, p_tab, ctypes.c_void_p]
+        L.ssu_update_onetoken.restype = ctypes.c_int
+        L.ssu_update_packed.argtypes = [p_args, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, p_tab, p_tab,
+                                        ctypes.c_void_p]
+        L.ssu_update_packed.restype = ctypes.c_int
+        L.ssu_prewarm.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
+        L.ssu_prewarm.restype = ctypes.c_int
+        L.ssu_last_error.argtypes = []
+        L.ssu_last_error.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _raise(rc: int):
+    msg = lib().ssu_last_error().decode(errors="replace")
+    if rc == ERR_INVALID:
+        raise ValueError(msg)
+    if rc == ERR_UNSUPPORTED:
+        raise NotImplementedError(msg)
+    raise RuntimeError(f"libssu: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _strides3(t: Optional[torch.Tensor]):
+    return _I64x3(*(t.stride() if t is not None else (0, 0, 0)))
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _table(t: Optional[torch.Tensor], mode: int) -> Optional[SlotTable]:
+    if t is None:
+        return None
+    _need(t.dtype in _ITYPE, "slot tables must be int32 or int64")
+    _need(t.is_cuda, "slot tables must be CUDA tensors")
+    if t.dim() == 1:
+        s0 = s1 = t.stride(0)
+        extent = (t.shape[0] - 1) * t.stride(0) + 1 if t.shape[0] > 0 else 0
+    elif t.dim() == 2:
+        s0, s1 = t.stride(0), t.stride(1)
+        extent = ((t.shape[0] - 1) * s0 + (t.shape[1] - 1) * s1 + 1) if t.numel() > 0 else 0
+    else:
+        raise ValueError("slot tables are [n] or [sequences, steps]")
+    return SlotTable(t.data_ptr(), _ITYPE[t.dtype], mode, s0, s1, extent)
+
+
+def _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, disable_state_update,
+          status, unsupported) -> Args:
+    _need(state.dim() == 4, "state must be [slots, heads, dim, dstate]")
+    slots, heads, dim, dstate = state.shape
+    _need(state.is_contiguous(), "state must be contiguous")
+    _need(state.dtype in _DTYPE and x.dtype in _DTYPE and dt.dtype in _DTYPE, "unsupported dtype")
+    rows = x.shape[0]
+    _need(x.dim() == 3 and tuple(x.shape[1:]) == (heads, dim), "x must be [rows, heads, dim]")
+    _need(dt.dim() == 3 and tuple(dt.shape) == (rows, heads, dim), "dt must be [rows, heads, dim]")
+    _need(B.dim() == 3 and B.shape[0] == rows and B.shape[2] == dstate, "B must be [rows, groups, dstate]")
+    groups = B.shape[1]
+    _need(tuple(C.shape) == tuple(B.shape), "C must have the shape of B")
+    _need(B.dtype == x.dtype and C.dtype == x.dtype, "B and C must have the dtype of x")
+    _need(tuple(out.shape) == (rows, heads, dim) and out.dtype == x.dtype, "out must be [rows, heads, dim] in x's dtype")
+    if z is not None:
+        _need(tuple(z.shape) == (rows, heads, dim) and z.dtype == x.dtype, "z must be [rows, heads, dim] in x's dtype")
+    for name, t in (("A", A), ("D", D), ("dt_bias", dt_bias)):
+        if t is not None:
+            _need(t.dtype == torch.float32 and t.numel() == heads and t.is_contiguous(),
+                  f"{name} must be a contiguous fp32 [heads] tensor")
+    tensors = [state, x, dt, A, B, C, D, z, dt_bias, out, status]
+    _need(all(t is None or t.is_cuda for t in tensors), "all tensors must be CUDA tensors")
+    if status is not None:
+        _need(status.dtype == torch.int32 and status.numel() >= 1, "status must be an int32 CUDA tensor")
+    return Args(
+        slots=slots, heads=heads, dim=dim, dstate=dstate, groups=groups,
+        state_dtype=_DTYPE[state.dtype], io_dtype=_DTYPE[x.dtype], dt_dtype=_DTYPE[dt.dtype],
+        dt_softplus=int(bool(dt_softplus)), disable_state_update=int(bool(disable_state_update)),
+        reserved0=0, pad_slot_id=int(pad_slot_id),
+        state=state.data_ptr(), x=x.data_ptr(), dt=dt.data_ptr(), B=B.data_ptr(), C=C.data_ptr(),
+        z=_ptr(z), A=A.data_ptr(), D=_ptr(D), dt_bias=_ptr(dt_bias), y=out.data_ptr(),
+        x_stride=_strides3(x), dt_stride=_strides3(dt), B_stride=_strides3(B), C_stride=_strides3(C),
+        z_stride=_strides3(z), y_stride=_strides3(out), d_status=_ptr(status), unsupported=unsupported)
+
+
+def _dt3(dt: torch.Tensor, x: torch.Tensor) -> torch.Tensor:
+    """A per-head step [rows, heads] is passed as a [rows, heads, dim] view
+    with stride 0 over dim (MATE prewarm: dt_dim = 1)."""
+    if dt.dim() == x.dim() - 1:
+        return dt.unsqueeze(-1).expand(*dt.shape, x.shape[-1])
+    return dt
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def ssu_update_onetoken(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+                        state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
+                        out=None, disable_state_update=False, status=None, stream=None,
+                        unsupported: int = 0) -> torch.Tensor:
+    """One decode token per sequence: x, dt, z are [batch, heads, dim] (dt may
+    be [batch, heads]), B and C [batch, groups, dstate].  The state is updated
+    in place; returns y ([batch, heads, dim], x's dtype)."""
+    dt = _dt3(dt, x)
+    if out is None:
+        out = torch.empty_like(x)
+    a = _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out,
+              disable_state_update, status, unsupported)
+    rt = _table(state_batch_indices, SLOTS_STRIDED)
+    wt = _table(dst_state_batch_indices, SLOTS_STRIDED)
+    rc = lib().ssu_update_onetoken(ctypes.byref(a), x.shape[0], None if rt is None else ctypes.byref(rt),
+                                   None if wt is None else ctypes.byref(wt), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    return out
+
+
+def ssu_update_packed(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+                      state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
+                      out=None, disable_state_update=False, cu_seqlens=None, num_accepted_tokens=None,
+                      slot_mode: int = SLOTS_STRIDED, status=None, stream=None,
+                      unsupported: int = 0) -> torch.Tensor:
+    """Packed rows: x is [rows, heads, dim] with ``cu_seqlens`` ([nseq+1]), or
+    the dense [nseq, steps, heads, dim] form without it (dt, z, B, C, out
+    shaped alike).  ``slot_mode`` selects the table addressing
+    (SLOTS_STRIDED: entry b*s0 + t*s1; SLOTS_PER_ROW: cu_seqlens[b] + t)."""
+    steps = 0
+    dense_shape = None
+    if x.dim() == 4:
+        _need(cu_seqlens is None, "the dense [batch, steps, heads, dim] form takes no cu_seqlens")
+        nseq, steps = x.shape[0], x.shape[1]
+        dense_shape = x.shape
+        flat = lambda t: None if t is None else t.reshape(nseq * steps, *t.shape[2:])
+        x, z, B, C = flat(x), flat(z), flat(B), flat(C)
+        dt = flat(dt)
+        if out is not None:
+            _need(tuple(out.shape) == tuple(dense_shape), "out must have the shape of x")
+            out_flat = out.view(nseq * steps, *out.shape[2:])
+        else:
+            out_flat = None
+    else:
+        _need(cu_seqlens is not None, "packed [rows, heads, dim] rows need cu_seqlens")
+        nseq = cu_seqlens.numel() - 1
+        out_flat = out
+    dt = _dt3(dt, x)
+    if out_flat is None:
+        out_flat = torch.empty_like(x)
+    meta_type = 0
+    for t in (cu_seqlens, num_accepted_tokens):
+        if t is not None:
+            _need(t.dtype in _ITYPE and t.is_cuda and t.is_contiguous(),
+                  "cu_seqlens / num_accepted_tokens must be contiguous int32/int64 CUDA tensors")
+    if cu_seqlens is not None and num_accepted_tokens is not None:
+        _need(cu_seqlens.dtype == num_accepted_tokens.dtype,
+              "cu_seqlens and num_accepted_tokens must share one dtype")
+    meta = cu_seqlens if cu_seqlens is not None else num_accepted_tokens
+    if meta is not None:
+        meta_type = _ITYPE[meta.dtype]
+    if num_accepted_tokens is not None:
+        _need(num_accepted_tokens.numel() >= nseq, "num_accepted_tokens needs one entry per sequence")
+    a = _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out_flat,
+              disable_state_update, status, unsupported)
+    rt = _table(state_batch_indices, slot_mode)
+    wt = _table(dst_state_batch_indices, slot_mode)
+    rc = lib().ssu_update_packed(ctypes.byref(a), nseq, x.shape[0], _ptr(cu_seqlens), steps,
+                                 _ptr(num_accepted_tokens), meta_type,
+                                 None if rt is None else ctypes.byref(rt),
+                                 None if wt is None else ctypes.byref(wt), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    if dense_shape is not None:
+        return out if out is not None else out_flat.view(dense_shape)
+    return out_flat
+
+
+def ssu_prewarm(*, state_dtype: torch.dtype, io_dtype: torch.dtype, heads: int, dim: int,
+                dstate: int, groups: int, dt_dtype: torch.dtype = torch.float32,
+                packed: bool = False) -> None:
+    """Load the kernel of one configuration on the current device, outside
+    any graph capture (MATE "Mamba / SSU", Graph capture)."""
+    rc = lib().ssu_prewarm(_DTYPE[state_dtype], _DTYPE[io_dtype], _DTYPE[dt_dtype], heads, dim,
+                           dstate, groups, int(bool(packed)))
+    if rc != OK:
+        _raise(rc)
+
+
+def selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
+                           state_batch_indices=None, pad_slot_id=-1, state_scale=None, out=None,
+                           disable_state_update=False, intermediate_states_buffer=None,
+                           intermediate_state_indices=None, intermediate_state_scales=None,
+                           rand_seed=None, philox_rounds=10, cache_steps=0, algorithm="auto",
+                           dst_state_batch_indices=None, cu_seqlens=None, num_accepted_tokens=None,
+                           backend="auto", slot_mode: int = SLOTS_STRIDED, status=None):
+    """The MATE / FlashInfer-shaped entry (argument order and defaults of the
+    MATE "Mamba / SSU" API reference).  The call shape picks the kernel: a 4-D
+    x, cu_seqlens or num_accepted_tokens go to the packed kernel, anything
+    else to the one-token kernel.  Arguments without implemented semantics
+    raise NotImplementedError."""
+    unsup = 0
+    if rand_seed is not None:
+        unsup |= UNSUP_RAND_SEED
+    if state_scale is not None:
+        unsup |= UNSUP_STATE_SCALE
+    if (intermediate_states_buffer is not None or intermediate_state_indices is not None
+            or intermediate_state_scales is not None):
+        unsup |= UNSUP_INTERMEDIATE
+    if cache_steps != 0:
+        unsup |= UNSUP_CACHE_STEPS
+    if algorithm != "auto" or backend != "auto":
+        unsup |= UNSUP_ALGORITHM
+    common = dict(D=D, z=z, dt_bias=dt_bias, dt_softplus=dt_softplus,
+                  state_batch_indices=state_batch_indices,
+                  dst_state_batch_indices=dst_state_batch_indices, pad_slot_id=pad_slot_id, out=out,
+                  disable_state_update=disable_state_update, status=status, unsupported=unsup)
+    if x.dim() == 4 or cu_seqlens is not None or num_accepted_tokens is not None:
+        if x.dim() == 3 and cu_seqlens is None:
+            # num_accepted_tokens alone on [batch, heads, dim]: one token per sequence
+            cu_seqlens = torch.arange(0, x.shape[0] + 1, device=x.device,
+                                      dtype=num_accepted_tokens.dtype)
+        return ssu_update_packed(state, x, dt, A, B, C, cu_seqlens=cu_seqlens,
+                                 num_accepted_tokens=num_accepted_tokens, slot_mode=slot_mode, **common)
+    return ssu_update_onetoken(state, x, dt, A, B, C, **common)

@@ -1,0 +1,215 @@
+// ssu_api.cpp -- the C ABI of libssu (include/ssu.h): argument checks, error
+// messages and kernel selection.  Nothing here touches device memory; each
+// update call is exactly one kernel launch on the caller's stream.
+#include "ssu.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "ssu_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+ssu_status fail(ssu_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+ssu_status ok() { return SSU_OK; }
+
+bool valid_dtype(int32_t d) { return d == SSU_F32 || d == SSU_F16 || d == SSU_BF16; }
+bool valid_itype(int32_t t) { return t == SSU_I32 || t == SSU_I64; }
+
+// dstate -> lanes per state row (16 elements per lane), or 0 if unsupported.
+int lanes_for(int64_t dstate) {
+    switch (dstate) {
+    case 16: return 1;
+    case 32: return 2;
+    case 64: return 4;
+    case 128: return 8;
+    case 256: return 16;
+    }
+    return 0;
+}
+
+const char *unsupported_name(uint32_t bits) {
+    if (bits & SSU_UNSUP_RAND_SEED) return "rand_seed (stochastic rounding is not implemented)";
+    if (bits & SSU_UNSUP_STATE_SCALE) return "state_scale";
+    if (bits & SSU_UNSUP_INTERMEDIATE) return "intermediate_states_buffer / indices / scales";
+    if (bits & SSU_UNSUP_CACHE_STEPS) return "cache_steps != 0";
+    if (bits & SSU_UNSUP_ALGORITHM) return "algorithm / backend other than 'auto'";
+    return "an unknown argument";
+}
+
+ssu_status check_shape(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype, int64_t heads,
+                       int64_t dim, int64_t dstate, int64_t groups, int *lanes) {
+    if (!valid_dtype(state_dtype)) return fail(SSU_ERR_INVALID, "state_dtype %d is not an ssu_dtype", state_dtype);
+    if (!valid_dtype(io_dtype)) return fail(SSU_ERR_INVALID, "io_dtype %d is not an ssu_dtype", io_dtype);
+    if (!valid_dtype(dt_dtype)) return fail(SSU_ERR_INVALID, "dt_dtype %d is not an ssu_dtype", dt_dtype);
+    if (heads <= 0 || dim <= 0 || dstate <= 0 || groups <= 0)
+        return fail(SSU_ERR_INVALID, "heads, dim, dstate and groups must be positive (got %lld, %lld, %lld, %lld)",
+                    (long long)heads, (long long)dim, (long long)dstate, (long long)groups);
+    if (heads % groups != 0)
+        return fail(SSU_ERR_INVALID, "heads (%lld) must be divisible by groups (%lld)", (long long)heads,
+                    (long long)groups);
+    if (heads > (1 << 30) || dim > (1 << 30))
+        return fail(SSU_ERR_INVALID, "heads and dim must be below 2^30");
+    *lanes = lanes_for(dstate);
+    if (*lanes == 0)
+        return fail(SSU_ERR_UNSUPPORTED, "dstate %lld is not supported (16, 32, 64, 128 or 256)", (long long)dstate);
+    return SSU_OK;
+}
+
+ssu_status check_strides(const char *name, const int64_t *s) {
+    for (int i = 0; i < 3; ++i)
+        if (s[i] < 0) return fail(SSU_ERR_INVALID, "%s_stride[%d] is negative", name, i);
+    return SSU_OK;
+}
+
+ssu_status check_table(const char *name, const ssu_slot_table *t, ssu::SlotTab *out) {
+    std::memset(out, 0, sizeof *out);
+    if (t == nullptr || t->entries == nullptr) return SSU_OK;
+    if (!valid_itype(t->type)) return fail(SSU_ERR_INVALID, "%s table: type %d is not an ssu_itype", name, t->type);
+    if (t->mode != SSU_SLOTS_STRIDED && t->mode != SSU_SLOTS_PER_ROW)
+        return fail(SSU_ERR_INVALID, "%s table: mode %d is not an ssu_slot_mode", name, t->mode);
+    if (t->extent < 0) return fail(SSU_ERR_INVALID, "%s table: negative extent", name);
+    if (t->s0 < 0 || t->s1 < 0) return fail(SSU_ERR_INVALID, "%s table: negative stride", name);
+    out->entries = t->entries;
+    out->s0 = t->s0;
+    out->s1 = t->s1;
+    out->extent = t->extent;
+    out->is_i64 = t->type == SSU_I64;
+    out->per_row = t->mode == SSU_SLOTS_PER_ROW;
+    return SSU_OK;
+}
+
+// Shared checks; fills everything in `kp` except the packed layout.
+ssu_status prepare(const ssu_args *a, const ssu_slot_table *read, const ssu_slot_table *dst,
+                   ssu::KParams *kp, int *lanes) {
+    if (a == nullptr) return fail(SSU_ERR_INVALID, "args is NULL");
+    if (a->unsupported != 0)
+        return fail(SSU_ERR_UNSUPPORTED, "not implemented: %s", unsupported_name(a->unsupported));
+    if (a->reserved0 != 0) return fail(SSU_ERR_INVALID, "reserved0 must be 0");
+    ssu_status st = check_shape(a->state_dtype, a->io_dtype, a->dt_dtype, a->heads, a->dim, a->dstate,
+                                a->groups, lanes);
+    if (st != SSU_OK) return st;
+    if (a->slots <= 0) return fail(SSU_ERR_INVALID, "slots must be positive");
+    if (!a->state || !a->x || !a->dt || !a->B || !a->C || !a->A || !a->y)
+        return fail(SSU_ERR_INVALID, "state, x, dt, A, B, C and y must not be NULL");
+    if (reinterpret_cast<uintptr_t>(a->state) % 16 != 0)
+        return fail(SSU_ERR_INVALID, "state must be 16-byte aligned");
+    if (a->y == a->x || a->y == a->z || a->y == a->dt || a->y == a->B || a->y == a->C || a->y == a->state)
+        return fail(SSU_ERR_INVALID, "y must not alias an input");
+    if ((st = check_strides("x", a->x_stride)) || (st = check_strides("dt", a->dt_stride)) ||
+        (st = check_strides("B", a->B_stride)) || (st = check_strides("C", a->C_stride)) ||
+        (st = check_strides("z", a->z_stride)) || (st = check_strides("y", a->y_stride)))
+        return st;
+    std::memset(kp, 0, sizeof *kp);
+    if ((st = check_table("read", read, &kp->rd)) || (st = check_table("destination", dst, &kp->wr)))
+        return st;
+    kp->slots = a->slots;
+    kp->H = static_cast<int32_t>(a->heads);
+    kp->P = static_cast<int32_t>(a->dim);
+    kp->N = static_cast<int32_t>(a->dstate);
+    kp->G = static_cast<int32_t>(a->groups);
+    kp->heads_per_group = static_cast<int32_t>(a->heads / a->groups);
+    kp->ptiles = static_cast<int32_t>((a->dim + ssu::kTileRows - 1) / ssu::kTileRows);
+    kp->io_dtype = a->io_dtype;
+    kp->dt_dtype = a->dt_dtype;
+    kp->softplus = a->dt_softplus != 0;
+    kp->disable = a->disable_state_update != 0;
+    kp->pad = a->pad_slot_id;
+    kp->state = a->state;
+    kp->x = a->x;
+    kp->dt = a->dt;
+    kp->B = a->B;
+    kp->C = a->C;
+    kp->z = a->z;
+    kp->A = a->A;
+    kp->D = a->D;
+    kp->dt_bias = a->dt_bias;
+    kp->y = a->y;
+    for (int i = 0; i < 3; ++i) {
+        kp->xs[i] = a->x_stride[i];
+        kp->dts[i] = a->dt_stride[i];
+        kp->Bs[i] = a->B_stride[i];
+        kp->Cs[i] = a->C_stride[i];
+        kp->zs[i] = a->z_stride[i];
+        kp->ys[i] = a->y_stride[i];
+    }
+    kp->status = a->d_status;
+    return SSU_OK;
+}
+
+ssu_status launched(cudaError_t e) {
+    if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+constexpr int64_t kMaxGrid = 0x7fffffffLL;
+
+}  // namespace
+
+extern "C" {
+
+ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch, const ssu_slot_table *read,
+                               const ssu_slot_table *dst, void *stream) {
+    ssu::KParams kp;
+    int lanes = 0;
+    ssu_status st = prepare(args, read, dst, &kp, &lanes);
+    if (st != SSU_OK) return st;
+    if (batch < 0) return fail(SSU_ERR_INVALID, "batch is negative");
+    if (batch == 0) return ok();
+    if (batch * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "batch * heads * dim tiles exceeds 2^31-1");
+    kp.nseq = batch;
+    kp.rows = batch;
+    return launched(ssu::launch_onetoken(args->state_dtype, lanes, kp, batch,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows, const void *cu_seqlens,
+                             int64_t steps, const void *num_accepted, int32_t meta_type,
+                             const ssu_slot_table *read, const ssu_slot_table *dst, void *stream) {
+    ssu::KParams kp;
+    int lanes = 0;
+    ssu_status st = prepare(args, read, dst, &kp, &lanes);
+    if (st != SSU_OK) return st;
+    if (nseq < 0 || rows < 0) return fail(SSU_ERR_INVALID, "nseq and rows must not be negative");
+    if ((cu_seqlens != nullptr || num_accepted != nullptr) && !valid_itype(meta_type))
+        return fail(SSU_ERR_INVALID, "meta_type %d is not an ssu_itype", meta_type);
+    if (cu_seqlens == nullptr) {
+        if (steps <= 0) return fail(SSU_ERR_INVALID, "dense form (no cu_seqlens) needs steps > 0");
+        if (rows != nseq * steps)
+            return fail(SSU_ERR_INVALID, "dense form: rows (%lld) must equal nseq * steps (%lld)", (long long)rows,
+                        (long long)(nseq * steps));
+    }
+    if (nseq == 0) return ok();
+    if (nseq * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "nseq * heads * dim tiles exceeds 2^31-1");
+    kp.nseq = nseq;
+    kp.rows = rows;
+    kp.steps = cu_seqlens == nullptr ? steps : 0;
+    kp.cu = cu_seqlens;
+    kp.acc = num_accepted;
+    kp.meta_is_i64 = meta_type == SSU_I64;
+    return launched(ssu::launch_packed(args->state_dtype, lanes, kp, static_cast<cudaStream_t>(stream)));
+}
+
+ssu_status ssu_prewarm(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype, int64_t heads, int64_t dim,
+                       int64_t dstate, int64_t groups, int32_t packed) {
+    int lanes = 0;
+    ssu_status st = check_shape(state_dtype, io_dtype, dt_dtype, heads, dim, dstate, groups, &lanes);
+    if (st != SSU_OK) return st;
+    cudaError_t e = packed ? ssu::prewarm_packed(state_dtype, lanes) : ssu::prewarm_onetoken(state_dtype, lanes);
+    if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "loading the kernel failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+const char *ssu_last_error(void) { return g_err; }
+
+}  // extern "C"

@@ -1,0 +1,274 @@
+// ssu_device.cuh -- device-side building blocks shared by the one-token and
+// the packed kernel, so that a packed call whose sequences all have one token
+// computes bit-for-bit what the one-token kernel computes.
+//
+// Thread layout of a work unit (one head, kTileRows dim rows, all of dstate):
+//   L = dstate / 16 lanes cover one state row; the CTA has kRowSlots * L
+//   threads; thread t serves row slot t / L and lane t % L, i.e. dim rows
+//   slot, slot + kRowSlots, slot + 2 kRowSlots, slot + 3 kRowSlots of the
+//   tile.  Within a row the thread owns the 16-byte chunks lane, lane + L,
+//   lane + 2L, ... so each load/store instruction of a warp touches whole
+//   128-byte lines.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "ssu_internal.h"
+
+namespace ssu {
+
+enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };  // ssu_dtype values
+
+// ---------------------------------------------------------------------------
+// Small operands (x, z, dt, B, C, y): dtype chosen at run time (uniform branch).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float load_small(const void *base, int64_t i, int dtype) {
+    if (dtype == kF32) return __ldg(static_cast<const float *>(base) + i);
+    if (dtype == kBF16) {
+        unsigned short u = __ldg(static_cast<const unsigned short *>(base) + i);
+        return __bfloat162float(__ushort_as_bfloat16(u));
+    }
+    unsigned short u = __ldg(static_cast<const unsigned short *>(base) + i);
+    return __half2float(__ushort_as_half(u));
+}
+
+__device__ __forceinline__ void store_small(void *base, int64_t i, int dtype, float v) {
+    if (dtype == kF32) {
+        static_cast<float *>(base)[i] = v;
+    } else if (dtype == kBF16) {
+        static_cast<__nv_bfloat16 *>(base)[i] = __float2bfloat16_rn(v);
+    } else {
+        static_cast<__half *>(base)[i] = __float2half_rn(v);
+    }
+}
+
+__device__ __forceinline__ int64_t load_index(const void *base, int64_t i, int is_i64) {
+    return is_i64 ? static_cast<int64_t>(__ldg(static_cast<const long long *>(base) + i))
+                  : static_cast<int64_t>(__ldg(static_cast<const int *>(base) + i));
+}
+
+__device__ __forceinline__ void flag(int32_t *status, int bit) {
+    if (status != nullptr) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------------------
+// State chunks: 16 bytes of the pool <-> floats, rounded to nearest even.
+// ---------------------------------------------------------------------------
+template <typename TS>
+struct StateChunk;
+
+template <>
+struct StateChunk<float> {
+    static constexpr int kVec = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float *v) {
+        v[0] = __uint_as_float(u.x);
+        v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z);
+        v[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float *v) {
+        return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3]));
+    }
+};
+
+template <>
+struct StateChunk<__half> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float *v) {
+        const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 f = __half22float2(h);
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *v) {
+        unsigned w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<unsigned *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+template <>
+struct StateChunk<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float *v) {
+        const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // bf16 -> fp32 is a shift: exact.
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack(const float *v) {
+        unsigned w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+            w[i] = *reinterpret_cast<unsigned *>(&h);
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// Streaming (evict-first) 16-byte accesses: each state byte is used once.
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    return __ldcs(static_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+    __stcs(static_cast<uint4 *>(p), v);
+}
+
+// ---------------------------------------------------------------------------
+// Per-thread view of a work unit.
+// ---------------------------------------------------------------------------
+template <typename TS, int L>
+struct Tile {
+    static constexpr int kVec = StateChunk<TS>::kVec;       // elements per 16-byte chunk
+    static constexpr int kChunks = kElemsPerThread / kVec;   // chunks per thread per row
+    static constexpr int kN = kElemsPerThread * L;           // dstate
+    static constexpr int kThreads = kRowSlots * L;
+
+    // Element offset (within a state row) of element i of this thread.
+    __device__ __forceinline__ static int elem(int lane, int i) {
+        return (lane + L * (i / kVec)) * kVec + (i % kVec);
+    }
+
+    // Load one row (16 elements) of this thread; row == nullptr gives zeros.
+    __device__ __forceinline__ static void load_row(const TS *row, int lane, float *s) {
+        if (row == nullptr) {
+#pragma unroll
+            for (int i = 0; i < kElemsPerThread; ++i) s[i] = 0.f;
+            return;
+        }
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+            uint4 u = ld_stream(row + (lane + L * k) * kVec);
+            StateChunk<TS>::unpack(u, s + k * kVec);
+        }
+    }
+
+    __device__ __forceinline__ static void store_row(TS *row, int lane, const float *s) {
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+            st_stream(row + (lane + L * k) * kVec, StateChunk<TS>::pack(s + k * kVec));
+    }
+
+    // This thread's 16 values of a dstate vector staged in shared memory.
+    __device__ __forceinline__ static void gather(const float *smem, int lane, float *v) {
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+#pragma unroll
+            for (int q = 0; q < kVec / 4; ++q) {
+                float4 f = *reinterpret_cast<const float4 *>(smem + (lane + L * k) * kVec + 4 * q);
+                v[k * kVec + 4 * q + 0] = f.x;
+                v[k * kVec + 4 * q + 1] = f.y;
+                v[k * kVec + 4 * q + 2] = f.z;
+                v[k * kVec + 4 * q + 3] = f.w;
+            }
+        }
+    }
+};
+
+// Sum over the L lanes of a row (lanes of a row are consecutive lane ids).
+template <int L>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int off = L / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// dt' for one (row, head, dim row): dt (+ bias), softplus if asked.
+// softplus(v) = log(1 + e^v) in the form max(v, 0) + log1p(e^-|v|).
+__device__ __forceinline__ float step_size(float dt, float bias, int softplus) {
+    float v = dt + bias;
+    if (softplus) v = fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
+    return v;
+}
+
+// One token applied to this thread's 16 elements of one state row:
+// S = S * dA + (dt' x) * B, and the partial sum of S * C over those elements.
+__device__ __forceinline__ float update_elems(float *s, const float *b, const float *c, float dA,
+                                              float dtx) {
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kElemsPerThread; ++i) {
+        s[i] = fmaf(s[i], dA, dtx * b[i]);
+        acc = fmaf(s[i], c[i], acc);
+    }
+    return acc;
+}
+
+// y = sum + D x, gated by silu(z) = z / (1 + e^-z) when z is given.
+__device__ __forceinline__ float output(float sum, float Dh, float x, bool has_z, float z) {
+    float y = fmaf(Dh, x, sum);
+    if (has_z) y *= z / (1.f + expf(-z));
+    return y;
+}
+
+// Stage B[r, g, :] and C[r, g, :] as fp32 in shared memory (all threads).
+template <int N, int NT>
+__device__ __forceinline__ void stage_bc(const KParams &p, int64_t r, int g, float *sB, float *sC) {
+    const int64_t bo = r * p.Bs[0] + g * p.Bs[1];
+    const int64_t co = r * p.Cs[0] + g * p.Cs[1];
+    for (int n = threadIdx.x; n < N; n += NT) {
+        sB[n] = load_small(p.B, bo + n * p.Bs[2], p.io_dtype);
+        sC[n] = load_small(p.C, co + n * p.Cs[2], p.io_dtype);
+    }
+}
+
+// Scalars of one (row r, head h, dim row pr): dA, dt' x, x, z.
+struct RowScalars {
+    float dA, dtx, x, z;
+};
+
+__device__ __forceinline__ RowScalars row_scalars(const KParams &p, int64_t r, int h, int pr,
+                                                  float Ah, float bias) {
+    RowScalars q;
+    const float dt = load_small(p.dt, r * p.dts[0] + h * p.dts[1] + pr * p.dts[2], p.dt_dtype);
+    q.x = load_small(p.x, r * p.xs[0] + h * p.xs[1] + pr * p.xs[2], p.io_dtype);
+    q.z = p.z ? load_small(p.z, r * p.zs[0] + h * p.zs[1] + pr * p.zs[2], p.io_dtype) : 0.f;
+    const float d = step_size(dt, bias, p.softplus);
+    q.dA = expf(Ah * d);
+    q.dtx = d * q.x;
+    return q;
+}
+
+// Slot at entry (b, t) of table `t`, or `fallback` without a table.  Returns
+// false (and flags) when the entry lies outside the table.
+__device__ __forceinline__ bool table_slot(const KParams &p, const SlotTab &t, int64_t b,
+                                           int64_t step, int64_t row_start, int64_t fallback,
+                                           int64_t *slot) {
+    if (t.entries == nullptr) {
+        *slot = fallback;
+        return true;
+    }
+    const int64_t e = t.per_row ? row_start + step : b * t.s0 + step * t.s1;
+    if (e < 0 || e >= t.extent) {
+        flag(p.status, 0x2);
+        return false;
+    }
+    *slot = load_index(t.entries, e, t.is_i64);
+    return true;
+}
+
+// A slot is usable if it is the pad id or inside the pool.
+__device__ __forceinline__ bool slot_ok(const KParams &p, int64_t s) {
+    if (s == p.pad || (s >= 0 && s < p.slots)) return true;
+    flag(p.status, 0x1);
+    return false;
+}
+
+}  // namespace ssu

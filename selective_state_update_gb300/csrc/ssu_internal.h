@@ -1,0 +1,59 @@
+// ssu_internal.h -- parameters shared by the host layer and the kernels of
+// libssu.  Not part of the public ABI (that is include/ssu.h).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace ssu {
+
+// Rows of one (head, dim-tile) work unit: a CTA updates kTileRows dim rows of
+// one head of one sequence.
+constexpr int kTileRows = 64;
+// Each thread holds kRowsPerThread rows x kElemsPerThread dstate elements.
+constexpr int kRowsPerThread = 4;
+constexpr int kElemsPerThread = 16;
+// Row slots per CTA: kTileRows / kRowsPerThread.  A CTA has
+// kRowSlots * L threads, L = dstate / kElemsPerThread lanes per row.
+constexpr int kRowSlots = kTileRows / kRowsPerThread;
+
+struct SlotTab {
+    const void *entries;  // nullptr: no table
+    int64_t s0, s1, extent;
+    int32_t is_i64;
+    int32_t per_row;
+};
+
+struct KParams {
+    // shape
+    int64_t slots;
+    int32_t H, P, N, G, heads_per_group, ptiles;
+    // dtypes (ssu_dtype values) of the small operands
+    int32_t io_dtype, dt_dtype;
+    int32_t softplus, disable;
+    int64_t pad;
+    // operands
+    void *state;
+    const void *x, *dt, *B, *C, *z;
+    const float *A, *D, *dt_bias;
+    void *y;
+    int64_t xs[3], dts[3], Bs[3], Cs[3], zs[3], ys[3];
+    // slot tables (rd.entries == nullptr: slot b; wr.entries == nullptr: use rd)
+    SlotTab rd, wr;
+    // packed layout
+    int64_t nseq, rows, steps;  // steps > 0 with cu == nullptr: dense form
+    const void *cu, *acc;
+    int32_t meta_is_i64;
+    int32_t *status;
+};
+
+// Launchers (one translation unit per kernel).  `lanes` = dstate / 16.
+cudaError_t launch_onetoken(int state_dtype, int lanes, const KParams &p, int64_t batch,
+                            cudaStream_t stream);
+cudaError_t launch_packed(int state_dtype, int lanes, const KParams &p, cudaStream_t stream);
+// Load the kernel's module and read its attributes (no launch).
+cudaError_t prewarm_onetoken(int state_dtype, int lanes);
+cudaError_t prewarm_packed(int state_dtype, int lanes);
+
+}  // namespace ssu

@@ -23,3 +23,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def libssu():
+    """Build (if needed) and load libssu; GPU tests fail loudly without it."""
+    from selective_state_update_gb300 import build as ssu_build
+    import selective_state_update_gb300 as ssu
+    ssu_build.build()
+    return ssu.lib()

@@ -1,0 +1,130 @@
+"""The C-ABI library builds, loads and exports what include/ssu.h declares;
+host-side argument checks fail before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import selective_state_update_gb300 as ssu
+from selective_state_update_gb300 import build as ssu_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libssu():
+    ssu_build.build()
+    return ssu.lib()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*(ssu_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("ssu_update_onetoken", "ssu_update_packed", "ssu_prewarm", "ssu_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libssu):
+    out = subprocess.run(["nm", "-D", "--defined-only", ssu.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    for n in declared_functions():
+        assert n in exported, f"{n} is declared in include/ but not exported"
+        assert hasattr(libssu, n)
+
+
+def test_header_compiles_as_c():
+    src = '#include "ssu.h"\nint main(void){ return (int)sizeof(ssu_args) > 0 ? 0 : 1; }\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-x",
+                        "c", "-", "-fsyntax-only"], input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_struct_layout_matches_the_header():
+    """ctypes mirrors of ssu_args / ssu_slot_table have the C sizes and offsets."""
+    probe = r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "ssu.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(ssu_args), sizeof(ssu_slot_table),
+         offsetof(ssu_args, pad_slot_id), offsetof(ssu_args, state), offsetof(ssu_args, x_stride),
+         offsetof(ssu_args, d_status), offsetof(ssu_slot_table, s0));
+  return 0;
+}
+'''
+    exe = os.path.join(ROOT, "selective_state_update_gb300", "_build", "layout_probe")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-x", "c", "-", "-o", exe],
+                   input=probe, text=True, check=True)
+    vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    A, T = ssu.Args, ssu.SlotTable
+    assert vals == [ctypes.sizeof(A), ctypes.sizeof(T), A.pad_slot_id.offset, A.state.offset,
+                    A.x_stride.offset, A.d_status.offset, T.s0.offset]
+
+
+def _args(**kw):
+    a = ssu.Args(slots=4, heads=4, dim=8, dstate=128, groups=2, state_dtype=0, io_dtype=2, dt_dtype=0,
+                 state=16, x=32, dt=48, B=64, C=80, A=96, y=112)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(unsupported=ssu.UNSUP_RAND_SEED), ssu.ERR_UNSUPPORTED, "rand_seed"),
+    (dict(unsupported=ssu.UNSUP_STATE_SCALE), ssu.ERR_UNSUPPORTED, "state_scale"),
+    (dict(groups=3), ssu.ERR_INVALID, "divisible"),
+    (dict(dstate=96), ssu.ERR_UNSUPPORTED, "dstate"),
+    (dict(state_dtype=7), ssu.ERR_INVALID, "state_dtype"),
+    (dict(state=8), ssu.ERR_INVALID, "aligned"),
+    (dict(y=32), ssu.ERR_INVALID, "alias"),
+    (dict(C=None), ssu.ERR_INVALID, "NULL"),
+    (dict(slots=0), ssu.ERR_INVALID, "slots"),
+    (dict(reserved0=1), ssu.ERR_INVALID, "reserved0"),
+])
+def test_host_checks_reject_before_launch(libssu, kw, code, needle):
+    a = _args(**kw)
+    rc = libssu.ssu_update_onetoken(ctypes.byref(a), 2, None, None, None)
+    assert rc == code
+    assert needle in libssu.ssu_last_error().decode()
+
+
+def test_negative_stride_and_bad_table(libssu):
+    a = _args()
+    a.x_stride[1] = -1
+    assert libssu.ssu_update_onetoken(ctypes.byref(a), 2, None, None, None) == ssu.ERR_INVALID
+    a = _args()
+    t = ssu.SlotTable(entries=128, type=5, mode=0, s0=1, s1=1, extent=2)
+    assert libssu.ssu_update_onetoken(ctypes.byref(a), 2, ctypes.byref(t), None, None) == ssu.ERR_INVALID
+    t = ssu.SlotTable(entries=128, type=0, mode=9, s0=1, s1=1, extent=2)
+    assert libssu.ssu_update_onetoken(ctypes.byref(a), 2, ctypes.byref(t), None, None) == ssu.ERR_INVALID
+
+
+def test_packed_dense_form_checks(libssu):
+    a = _args()
+    assert libssu.ssu_update_packed(ctypes.byref(a), 2, 5, None, 2, None, 0, None, None, None) == ssu.ERR_INVALID
+    assert "nseq * steps" in libssu.ssu_last_error().decode()
+    assert libssu.ssu_update_packed(ctypes.byref(a), 2, 4, None, 0, None, 0, None, None, None) == ssu.ERR_INVALID
+
+
+def test_empty_calls_launch_nothing(libssu):
+    a = _args()
+    assert libssu.ssu_update_onetoken(ctypes.byref(a), 0, None, None, None) == ssu.OK
+    assert libssu.ssu_update_packed(ctypes.byref(a), 0, 0, None, 1, None, 0, None, None, None) == ssu.OK
+
+
+def test_prewarm_rejects_unsupported_shapes(libssu):
+    assert libssu.ssu_prewarm(0, 2, 0, 8, 8, 100, 2, 0) == ssu.ERR_UNSUPPORTED
+    assert libssu.ssu_prewarm(0, 2, 0, 8, 8, 128, 3, 0) == ssu.ERR_INVALID
