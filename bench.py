@@ -234,9 +234,7 @@ def run_ours(args, rank, world, device):
     import selective_state_update_gb300 as ssu
     ssu_build.build()
     ssu.lib()
-    gen = workloads.NAMED[args.workload]
-    w = gen(device=device, seed=1000 + 97 * rank + {"tiny_onetoken": 1, "b256_fp32": 2, "b1024_bf16": 3,
-                                                     "mtp_64x7_fp32": 4, "varlen_fp16": 5}[args.workload])
+    w = make_workload(args, device, seed_offset=97 * rank)
     torch.cuda.synchronize()
     acct = algorithmic_bytes(w)
     tokens = w.rows
@@ -317,7 +315,8 @@ def run_ours(args, rank, world, device):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                               + (f" (batch {args.batch})" if args.batch else ""),
                    "sequences_per_gpu": w.nseq, "rows_per_gpu": tokens,
                    "state_dtype": str(w.state.dtype).replace("torch.", ""),
                    "io_dtype": str(w.x.dtype).replace("torch.", ""),
@@ -385,8 +384,22 @@ def _oracle_call(sub):
                       num_accepted=sub.num_accepted if sub.kind == "packed" else None)
 
 
-def _cpu_workload(name):
-    return workloads.NAMED[name](device="cpu")
+SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
+         "varlen_fp16": 1005}
+
+
+def make_workload(args, device, seed_offset=0):
+    gen = workloads.NAMED[args.workload]
+    kw = {}
+    if args.batch is not None:
+        if args.workload != "b256_fp32":
+            raise SystemExit("--batch applies to the b256_fp32 workload only")
+        kw["batch"] = args.batch
+    return gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
+
+
+def _cpu_workload(args):
+    return make_workload(args, "cpu")
 
 
 def oracle_rate(w_cpu, budget_s: float):
@@ -414,7 +427,7 @@ def oracle_rate(w_cpu, budget_s: float):
 
 
 def run_reference(args):
-    w_cpu = _cpu_workload(args.workload)
+    w_cpu = _cpu_workload(args)
     import oracle
     oracle.build()
     lens = _lengths(w_cpu)
@@ -456,6 +469,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.NAMED), default="b256_fp32")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="b256_fp32 at another batch size (profiling captures)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -474,7 +489,7 @@ def main():
     # The oracle baseline runs before the first GPU call (no fork after CUDA init).
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        w_cpu = _cpu_workload(args.workload)
+        w_cpu = _cpu_workload(args)
         rate, desc = oracle_rate(w_cpu, args.cpu_baseline_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}

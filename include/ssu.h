@@ -89,6 +89,8 @@ typedef struct ssu_slot_table {
 #define SSU_DEV_BAD_SLOT   0x1  /* slot not in [0, slots) and not pad_slot_id       */
 #define SSU_DEV_BAD_ENTRY  0x2  /* table entry index outside [0, extent)            */
 #define SSU_DEV_BAD_SEQLEN 0x4  /* cu_seqlens decreasing, negative or past `rows`   */
+#define SSU_DEV_TIMEOUT    0x8  /* an asynchronous state copy did not complete in
+                                   about a second; the unit was skipped           */
 
 /* Arguments of the MATE signature that this library does not implement.  Set
  * the bit when the caller passed the argument; the call then fails with
@@ -138,7 +140,8 @@ typedef struct ssu_args {
  *   dst   NULL or dst->entries NULL: the state is written back through the
  *         read table (or to slot b without one).  Otherwise to entry (b, 0).
  *   A read of pad_slot_id starts from zeros; a write to it is skipped.
- * batch == 0 launches nothing and returns SSU_OK.
+ * batch == 0 launches nothing and returns SSU_OK; the row operands may then
+ * be NULL.
  */
 ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch,
                                const ssu_slot_table *read, const ssu_slot_table *dst,
@@ -167,7 +170,9 @@ ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch,
  * skipped.  The state carried between the tokens of a sequence stays in
  * fp32; only the published copies are rounded.  A sequence may overwrite its
  * own read slot (the read happens first).
- * nseq == 0 launches nothing and returns SSU_OK.
+ * nseq == 0 or rows == 0 launches nothing and returns SSU_OK (every
+ * sequence is then empty; cu_seqlens is not read).  With rows == 0 the row
+ * operands (x, dt, B, C, z, y) may be NULL.
  */
 ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows,
                              const void *cu_seqlens, int64_t steps,

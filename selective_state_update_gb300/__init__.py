@@ -24,7 +24,7 @@ from typing import Optional
 import torch
 
 __all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_prewarm", "selective_state_update",
-           "SLOTS_STRIDED", "SLOTS_PER_ROW", "DEV_BAD_SLOT", "DEV_BAD_ENTRY", "DEV_BAD_SEQLEN",
+           "SLOTS_STRIDED", "SLOTS_PER_ROW", "DEV_BAD_SLOT", "DEV_BAD_ENTRY", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
            "library_path", "lib"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +33,7 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libssu.so")
 # ssu.h constants
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 SLOTS_STRIDED, SLOTS_PER_ROW = 0, 1
-DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN = 0x1, 0x2, 0x4
+DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 UNSUP_RAND_SEED, UNSUP_STATE_SCALE, UNSUP_INTERMEDIATE, UNSUP_CACHE_STEPS, UNSUP_ALGORITHM = (
     0x01, 0x02, 0x04, 0x08, 0x10)
 _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}

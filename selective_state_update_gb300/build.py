@@ -46,21 +46,23 @@ def _digest(extra_flags) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    """Compile every translation unit and link ``libssu.so``; returns its path."""
-    os.makedirs(OUT_DIR, exist_ok=True)
-    stamp = os.path.join(OUT_DIR, "libssu.sha256")
+def build(verbose: bool = False, force: bool = False, extra_flags=(), out_dir: str = OUT_DIR) -> str:
+    """Compile every translation unit and link ``libssu.so`` into ``out_dir``;
+    returns its path."""
+    os.makedirs(out_dir, exist_ok=True)
+    lib_path = os.path.join(out_dir, "libssu.so")
+    stamp = os.path.join(out_dir, "libssu.sha256")
     digest = _digest(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib_path
     nvcc = _nvcc()
     flags = ARCH + COMMON + list(extra_flags) + (["-Xptxas", "-v"] if verbose else [])
 
     def compile_one(name):
         src = os.path.join(CSRC, name)
-        obj = os.path.join(OUT_DIR, name + ".o")
+        obj = os.path.join(out_dir, name + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -73,15 +75,15 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"linking libssu.so failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":

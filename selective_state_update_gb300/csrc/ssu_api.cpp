@@ -90,7 +90,7 @@ ssu_status check_table(const char *name, const ssu_slot_table *t, ssu::SlotTab *
 }
 
 // Shared checks; fills everything in `kp` except the packed layout.
-ssu_status prepare(const ssu_args *a, const ssu_slot_table *read, const ssu_slot_table *dst,
+ssu_status prepare(const ssu_args *a, int64_t rows, const ssu_slot_table *read, const ssu_slot_table *dst,
                    ssu::KParams *kp, int *lanes) {
     if (a == nullptr) return fail(SSU_ERR_INVALID, "args is NULL");
     if (a->unsupported != 0)
@@ -100,11 +100,13 @@ ssu_status prepare(const ssu_args *a, const ssu_slot_table *read, const ssu_slot
                                 a->groups, lanes);
     if (st != SSU_OK) return st;
     if (a->slots <= 0) return fail(SSU_ERR_INVALID, "slots must be positive");
-    if (!a->state || !a->x || !a->dt || !a->B || !a->C || !a->A || !a->y)
-        return fail(SSU_ERR_INVALID, "state, x, dt, A, B, C and y must not be NULL");
+    if (!a->state || !a->A) return fail(SSU_ERR_INVALID, "state and A must not be NULL");
+    if (rows > 0 && (!a->x || !a->dt || !a->B || !a->C || !a->y))
+        return fail(SSU_ERR_INVALID, "x, dt, B, C and y must not be NULL");
     if (reinterpret_cast<uintptr_t>(a->state) % 16 != 0)
         return fail(SSU_ERR_INVALID, "state must be 16-byte aligned");
-    if (a->y == a->x || a->y == a->z || a->y == a->dt || a->y == a->B || a->y == a->C || a->y == a->state)
+    if (rows > 0 && (a->y == a->x || a->y == a->z || a->y == a->dt || a->y == a->B || a->y == a->C ||
+                     a->y == a->state))
         return fail(SSU_ERR_INVALID, "y must not alias an input");
     if ((st = check_strides("x", a->x_stride)) || (st = check_strides("dt", a->dt_stride)) ||
         (st = check_strides("B", a->B_stride)) || (st = check_strides("C", a->C_stride)) ||
@@ -162,9 +164,9 @@ ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch, const ssu_sl
                                const ssu_slot_table *dst, void *stream) {
     ssu::KParams kp;
     int lanes = 0;
-    ssu_status st = prepare(args, read, dst, &kp, &lanes);
-    if (st != SSU_OK) return st;
     if (batch < 0) return fail(SSU_ERR_INVALID, "batch is negative");
+    ssu_status st = prepare(args, batch, read, dst, &kp, &lanes);
+    if (st != SSU_OK) return st;
     if (batch == 0) return ok();
     if (batch * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "batch * heads * dim tiles exceeds 2^31-1");
     kp.nseq = batch;
@@ -178,9 +180,9 @@ ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows, c
                              const ssu_slot_table *read, const ssu_slot_table *dst, void *stream) {
     ssu::KParams kp;
     int lanes = 0;
-    ssu_status st = prepare(args, read, dst, &kp, &lanes);
-    if (st != SSU_OK) return st;
     if (nseq < 0 || rows < 0) return fail(SSU_ERR_INVALID, "nseq and rows must not be negative");
+    ssu_status st = prepare(args, rows, read, dst, &kp, &lanes);
+    if (st != SSU_OK) return st;
     if ((cu_seqlens != nullptr || num_accepted != nullptr) && !valid_itype(meta_type))
         return fail(SSU_ERR_INVALID, "meta_type %d is not an ssu_itype", meta_type);
     if (cu_seqlens == nullptr) {
@@ -189,7 +191,7 @@ ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows, c
             return fail(SSU_ERR_INVALID, "dense form: rows (%lld) must equal nseq * steps (%lld)", (long long)rows,
                         (long long)(nseq * steps));
     }
-    if (nseq == 0) return ok();
+    if (nseq == 0 || rows == 0) return ok();  // nothing to read or write
     if (nseq * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "nseq * heads * dim tiles exceeds 2^31-1");
     kp.nseq = nseq;
     kp.rows = rows;

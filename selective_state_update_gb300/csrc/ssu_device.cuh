@@ -51,6 +51,8 @@ __device__ __forceinline__ int64_t load_index(const void *base, int64_t i, int i
                   : static_cast<int64_t>(__ldg(static_cast<const int *>(base) + i));
 }
 
+enum : int { kDevBadSlot = 0x1, kDevBadEntry = 0x2, kDevBadSeqlen = 0x4, kDevTimeout = 0x8 };
+
 __device__ __forceinline__ void flag(int32_t *status, int bit) {
     if (status != nullptr) atomicOr(status, bit);
 }
@@ -123,6 +125,59 @@ struct StateChunk<__nv_bfloat16> {
     }
 };
 
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copy (TMA engine) of a contiguous state tile into shared
+// memory, completed on an mbarrier.  Inline PTX for sm_90+ / sm_103a.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+    // Make the initialised barrier visible to the async proxy (TMA).
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arrive once and expect `bytes` of transaction completions on this phase.
+__device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for phase `parity` of `bar`; gives up after about a second of
+// SM clock cycles (a copy that never lands) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 0; i < (1u << 26); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > 2000000000LL) break;
+    }
+    return false;
+}
+
 // Streaming (evict-first) 16-byte accesses: each state byte is used once.
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     return __ldcs(static_cast<const uint4 *>(p));
@@ -156,6 +211,15 @@ struct Tile {
 #pragma unroll
         for (int k = 0; k < kChunks; ++k) {
             uint4 u = ld_stream(row + (lane + L * k) * kVec);
+            StateChunk<TS>::unpack(u, s + k * kVec);
+        }
+    }
+
+    // Load one row (16 elements) of this thread from a tile in shared memory.
+    __device__ __forceinline__ static void load_row_smem(const TS *row, int lane, float *s) {
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k) {
+            uint4 u = *reinterpret_cast<const uint4 *>(row + (lane + L * k) * kVec);
             StateChunk<TS>::unpack(u, s + k * kVec);
         }
     }
@@ -257,7 +321,7 @@ __device__ __forceinline__ bool table_slot(const KParams &p, const SlotTab &t, i
     }
     const int64_t e = t.per_row ? row_start + step : b * t.s0 + step * t.s1;
     if (e < 0 || e >= t.extent) {
-        flag(p.status, 0x2);
+        flag(p.status, kDevBadEntry);
         return false;
     }
     *slot = load_index(t.entries, e, t.is_i64);
@@ -267,7 +331,7 @@ __device__ __forceinline__ bool table_slot(const KParams &p, const SlotTab &t, i
 // A slot is usable if it is the pad id or inside the pool.
 __device__ __forceinline__ bool slot_ok(const KParams &p, int64_t s) {
     if (s == p.pad || (s >= 0 && s < p.slots)) return true;
-    flag(p.status, 0x1);
+    flag(p.status, kDevBadSlot);
     return false;
 }
 

@@ -17,6 +17,16 @@ constexpr int kElemsPerThread = 16;
 // Row slots per CTA: kTileRows / kRowsPerThread.  A CTA has
 // kRowSlots * L threads, L = dstate / kElemsPerThread lanes per row.
 constexpr int kRowSlots = kTileRows / kRowsPerThread;
+// How many of a thread's rows the compute loops keep in flight at once
+// (more rows: more loads in flight, more registers, fewer resident CTAs).
+#ifndef SSU_ONETOKEN_UNROLL
+#define SSU_ONETOKEN_UNROLL 2
+#endif
+#ifndef SSU_PACKED_UNROLL
+#define SSU_PACKED_UNROLL 1
+#endif
+constexpr int kOnetokenUnroll = SSU_ONETOKEN_UNROLL;
+constexpr int kPackedUnroll = SSU_PACKED_UNROLL;
 
 struct SlotTab {
     const void *entries;  // nullptr: no table

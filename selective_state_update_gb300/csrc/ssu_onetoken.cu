@@ -9,11 +9,22 @@
 // Work unit: (sequence b, head h, tile of kTileRows dim rows); one CTA each,
 // ptile fastest so that neighbouring CTAs stream neighbouring bytes of the
 // same slot.  The path is HBM-bound: every state byte is read once and
-// written once with 16-byte streaming accesses; B and C of the unit's group
-// are staged once in shared memory; y is reduced over dstate with shuffles.
+// written once.  The tile (contiguous in the pool) arrives in shared memory
+// by one bulk asynchronous copy (TMA engine, mbarrier completion), so the
+// bytes in flight per SM are bounded by shared memory, not by registers;
+// meanwhile the CTA stages B and C of the unit's group in shared memory and
+// the per-row scalars in registers.  Results leave with 16-byte streaming
+// stores; y is reduced over dstate with shuffles.
 #include "ssu_device.cuh"
 
 namespace ssu {
+
+// Dynamic shared memory of a CTA: the state tile, B and C as fp32, the mbarrier.
+template <typename TS, int L>
+struct OnetokenSmem {
+    static constexpr int kTileBytes = kTileRows * Tile<TS, L>::kN * static_cast<int>(sizeof(TS));
+    static constexpr int kBytes = kTileBytes + 2 * Tile<TS, L>::kN * 4 + 16;
+};
 
 template <typename TS, int L>
 __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
@@ -21,8 +32,11 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     using T = Tile<TS, L>;
     constexpr int N = T::kN;
     constexpr int NT = T::kThreads;
-    __shared__ __align__(16) float sB[N];
-    __shared__ __align__(16) float sC[N];
+    extern __shared__ __align__(128) unsigned char smem[];
+    TS *tile = reinterpret_cast<TS *>(smem);
+    float *sB = reinterpret_cast<float *>(smem + OnetokenSmem<TS, L>::kTileBytes);
+    float *sC = sB + N;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sC + N);
 
     const int64_t unit = blockIdx.x;
     const int ptile = static_cast<int>(unit % p.ptiles);
@@ -44,19 +58,19 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     const int tid = threadIdx.x;
     const int lane = tid % L;
     const int slot_row = tid / L;
-    const int64_t head_rows = (static_cast<int64_t>(h)) * p.P;
+    const int row0 = ptile * kTileRows;
+    const int rows_here = min(kTileRows, p.P - row0);
+    const int64_t head_row0 = (static_cast<int64_t>(h)) * p.P + row0;
+    const bool seeded = rs != p.pad;
 
-    // Issue the state loads of all this thread's rows first.
-    float s[kRowsPerThread][kElemsPerThread];
-#pragma unroll
-    for (int j = 0; j < kRowsPerThread; ++j) {
-        const int pr = ptile * kTileRows + slot_row + j * kRowSlots;
-        const TS *row = nullptr;
-        if (pr < p.P && rs != p.pad)
-            row = static_cast<const TS *>(p.state) + ((rs * p.H) * p.P + head_rows + pr) * N;
-        T::load_row(row, lane, s[j]);
+    // One thread starts the bulk copy of the tile (rows_here contiguous rows);
+    // the others stage B, C and the per-row scalars meanwhile.
+    if (tid == 0 && seeded) {
+        const uint32_t bytes = static_cast<uint32_t>(rows_here) * N * sizeof(TS);
+        mbar_init(bar, 1);
+        mbar_arrive_expect(bar, bytes);
+        bulk_load(tile, static_cast<const TS *>(p.state) + (rs * p.H * p.P + head_row0) * N, bytes, bar);
     }
-
     stage_bc<N, NT>(p, b, g, sB, sC);
     const float Ah = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
@@ -64,36 +78,57 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     RowScalars q[kRowsPerThread];
 #pragma unroll
     for (int j = 0; j < kRowsPerThread; ++j) {
-        const int pr = ptile * kTileRows + slot_row + j * kRowSlots;
+        const int pr = row0 + slot_row + j * kRowSlots;
         q[j] = row_scalars(p, b, h, pr < p.P ? pr : 0, Ah, bias);
     }
     __syncthreads();
     float bv[kElemsPerThread], cv[kElemsPerThread];
     T::gather(sB, lane, bv);
     T::gather(sC, lane, cv);
+    if (seeded && !mbar_wait_bounded(bar, 0)) {
+        flag(p.status, kDevTimeout);
+        return;
+    }
 
     const bool write_state = !p.disable && ws != p.pad;
-#pragma unroll
+    TS *dst = static_cast<TS *>(p.state) + (ws * p.H * p.P + head_row0) * N;
+#pragma unroll(kOnetokenUnroll)
     for (int j = 0; j < kRowsPerThread; ++j) {
-        const int pr = ptile * kTileRows + slot_row + j * kRowSlots;
-        const float part = update_elems(s[j], bv, cv, q[j].dA, q[j].dtx);
+        const int r = slot_row + j * kRowSlots;  // row within the tile
+        float s[kElemsPerThread];
+        if (seeded && r < rows_here) {
+            T::load_row_smem(tile + r * N, lane, s);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kElemsPerThread; ++i) s[i] = 0.f;
+        }
+        const float part = update_elems(s, bv, cv, q[j].dA, q[j].dtx);
         const float sum = row_sum<L>(part);
-        if (pr < p.P) {
+        if (r < rows_here) {
             if (lane == 0) {
                 const float y = output(sum, Dh, q[j].x, p.z != nullptr, q[j].z);
-                store_small(p.y, b * p.ys[0] + h * p.ys[1] + pr * p.ys[2], p.io_dtype, y);
+                store_small(p.y, b * p.ys[0] + h * p.ys[1] + (row0 + r) * p.ys[2], p.io_dtype, y);
             }
-            if (write_state)
-                T::store_row(static_cast<TS *>(p.state) + ((ws * p.H) * p.P + head_rows + pr) * N,
-                             lane, s[j]);
+            if (write_state) T::store_row(dst + r * N, lane, s);
         }
     }
 }
 
+// Dynamic shared memory above the 48 KiB default needs an opt-in per kernel.
+template <typename TS, int L>
+static cudaError_t set_smem_attr() {
+    constexpr int bytes = OnetokenSmem<TS, L>::kBytes;
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(ssu_onetoken_kernel<TS, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 template <typename TS, int L>
 static cudaError_t launch_t(const KParams &p, int64_t batch, cudaStream_t stream) {
+    cudaError_t e = set_smem_attr<TS, L>();
+    if (e != cudaSuccess) return e;
     const int64_t units = batch * p.H * p.ptiles;
-    ssu_onetoken_kernel<TS, L><<<static_cast<unsigned>(units), Tile<TS, L>::kThreads, 0, stream>>>(p);
+    ssu_onetoken_kernel<TS, L><<<static_cast<unsigned>(units), Tile<TS, L>::kThreads,
+                                 OnetokenSmem<TS, L>::kBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -119,15 +154,21 @@ cudaError_t launch_onetoken(int state_dtype, int lanes, const KParams &p, int64_
     return cudaErrorInvalidValue;
 }
 
+template <typename TS, int L>
+static cudaError_t attrs_t() {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, L>);
+    return e != cudaSuccess ? e : set_smem_attr<TS, L>();
+}
+
 template <typename TS>
 static cudaError_t attrs_lanes(int lanes) {
-    cudaFuncAttributes a;
     switch (lanes) {
-    case 1: return cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, 1>);
-    case 2: return cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, 2>);
-    case 4: return cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, 4>);
-    case 8: return cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, 8>);
-    case 16: return cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, 16>);
+    case 1: return attrs_t<TS, 1>();
+    case 2: return attrs_t<TS, 2>();
+    case 4: return attrs_t<TS, 4>();
+    case 8: return attrs_t<TS, 8>();
+    case 16: return attrs_t<TS, 16>();
     }
     return cudaErrorInvalidValue;
 }

@@ -10,7 +10,8 @@ import workloads
 
 # Tolerances (GPU vs oracle).
 #  fp32 state: |d| <= 1e-5 |ref| + 1e-6
-#  fp16/bf16 state: at most one unit in the last place of the state dtype
+#  fp16/bf16 state: one unit in the last place of the state dtype, plus the
+#  fp32 tolerance (the recurrence itself runs in fp32)
 #  outputs y (bf16/fp16): |d| <= 1e-2 |ref| + 1e-2
 STATE_F32_RTOL, STATE_F32_ATOL = 1e-5, 1e-6
 Y_RTOL, Y_ATOL = 1e-2, 1e-2
@@ -55,14 +56,18 @@ def ulp_of(v: np.ndarray, dtype: torch.dtype) -> np.ndarray:
 
 
 def assert_state_close(got: torch.Tensor, ref: torch.Tensor, what: str = "state"):
-    """fp32: 1e-5 relative + 1e-6 absolute; fp16/bf16: within one ulp."""
+    """fp32: 1e-5 relative + 1e-6 absolute.  fp16/bf16: one ulp of the state
+    dtype at the value's magnitude, on top of the fp32 tolerance: the
+    recurrence is carried in fp32, so where cancellation makes a value tiny
+    its own ulp is finer than fp32 arithmetic on O(1) operands resolves."""
     assert got.dtype == ref.dtype and got.shape == ref.shape
     g, r = f64(got), f64(ref)
     d = np.abs(g - r)
     if got.dtype == torch.float32:
         bad = d > STATE_F32_RTOL * np.abs(r) + STATE_F32_ATOL
     else:
-        bad = d > ulp_of(np.maximum(np.abs(g), np.abs(r)), got.dtype) * (1 + 1e-12)
+        ulp = ulp_of(np.maximum(np.abs(g), np.abs(r)), got.dtype)
+        bad = d > ulp * (1 + 1e-12) + STATE_F32_RTOL * np.abs(r) + STATE_F32_ATOL
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "

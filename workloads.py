@@ -122,26 +122,35 @@ def tiny_onetoken(device="cpu", seed=1001) -> Workload:
 
 
 def _distinct_tables_with_pad(g, batch, slots, pad, n_pad, device):
-    """Read and destination tables whose non-pad entries are distinct slots,
-    disjoint between the two tables, never the pad slot; exactly ``n_pad``
-    entries of each table (at random positions) are the pad id."""
+    """Read and destination tables of ``batch`` entries each: exactly ``n_pad``
+    entries of each table (at random positions) are the pad id, and the other
+    entries are distinct slots, disjoint between the two tables, never the pad
+    slot (2 * (batch - n_pad) <= slots - 1 keeps this feasible)."""
     candidates = torch.tensor([s for s in range(slots) if s != pad], dtype=torch.int64)
-    perm = candidates[torch.randperm(candidates.numel(), generator=g)]
-    read = perm[:batch].clone()
-    dst = perm[batch:2 * batch].clone()
-    for t in (read, dst):
-        pos = torch.randperm(batch, generator=g)[:n_pad]
-        t[pos] = pad
-    return read.to(torch.int32).to(device), dst.to(torch.int32).to(device)
+    need = 2 * (batch - n_pad)
+    if need > candidates.numel():
+        raise ValueError(f"{need} distinct slots needed, {candidates.numel()} available")
+    perm = candidates[torch.randperm(candidates.numel(), generator=g)][:need]
+    tables = []
+    for k in range(2):
+        t = torch.full((batch,), pad, dtype=torch.int64)
+        keep = torch.ones(batch, dtype=torch.bool)
+        keep[torch.randperm(batch, generator=g)[:n_pad]] = False
+        t[keep] = perm[k * (batch - n_pad):(k + 1) * (batch - n_pad)]
+        tables.append(t.to(torch.int32).to(device))
+    return tables[0], tables[1]
 
 
-def b256_fp32(device="cpu", seed=1002, in_place=False) -> Workload:
-    heads, dim, dstate, groups, slots, batch, pad = 128, 64, 128, 8, 512, 256, 0
+def b256_fp32(device="cpu", seed=1002, in_place=False, batch=256) -> Workload:
+    """``batch`` other than 256 gives the same workload at another size (pool
+    of 2 * batch slots); profiling uses it for captures that must stay small."""
+    heads, dim, dstate, groups, pad = 128, 64, 128, 8, 0
+    slots = 2 * batch
     g = _gen(seed, device)
     inp = _decode_inputs(g, device, batch, heads, dim, dstate, groups, torch.bfloat16)
     state = _pool(g, device, slots, heads, dim, dstate, torch.float32)
     gh = _gen(seed + 7, "cpu")
-    read, dst = _distinct_tables_with_pad(gh, batch, slots, pad, round(0.05 * batch), device)
+    read, dst = _distinct_tables_with_pad(gh, batch, slots, pad, max(1, round(0.05 * batch)), device)
     if in_place:
         dst = read.clone()
     return Workload("b256_fp32" + ("_inplace" if in_place else ""), "onetoken", state,
