@@ -26,14 +26,20 @@ enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };  // ssu_dtype values
 // ---------------------------------------------------------------------------
 // Small operands (x, z, dt, B, C, y): dtype chosen at run time (uniform branch).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float load_small(const void *base, int64_t i, int dtype) {
-    if (dtype == kF32) return __ldg(static_cast<const float *>(base) + i);
-    if (dtype == kBF16) {
-        unsigned short u = __ldg(static_cast<const unsigned short *>(base) + i);
-        return __bfloat162float(__ushort_as_bfloat16(u));
-    }
-    unsigned short u = __ldg(static_cast<const unsigned short *>(base) + i);
-    return __half2float(__ushort_as_half(u));
+// Raw bits of element i of a small operand (32-bit types: the word; 16-bit
+// types: the half-word).  Loads that are only converted later can all be in
+// flight at once; converting right after each load would expose every
+// load's latency in turn.
+template <bool WIDE>
+__device__ __forceinline__ uint32_t load_bits(const void *base, int64_t i) {
+    if (WIDE) return __ldg(static_cast<const unsigned int *>(base) + i);
+    return __ldg(static_cast<const unsigned short *>(base) + i);
+}
+
+__device__ __forceinline__ float bits_to_float(uint32_t v, int dtype) {
+    if (dtype == kF32) return __uint_as_float(v);
+    if (dtype == kBF16) return __uint_as_float(v << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v)));
 }
 
 __device__ __forceinline__ void store_small(void *base, int64_t i, int dtype, float v) {
@@ -145,6 +151,10 @@ __device__ __forceinline__ void mbar_arrive_expect(uint64_t *bar, uint32_t bytes
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // global -> shared, `bytes` a multiple of 16, both addresses 16-byte aligned.
 __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
     asm volatile(
@@ -152,6 +162,51 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
             smem_addr(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// shared -> global bulk copy (TMA engine), tracked in the issuing thread's
+// bulk groups.  `bytes` a multiple of 16, both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_store(void *dst_gmem, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+                 "r"(smem_addr(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until all of this thread's bulk groups have completed (writes done).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier `id` over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier `id` over `nthreads` threads (a multiple of 32) that also returns
+// whether any participant passed `v` true.
+__device__ __forceinline__ bool barrier_or(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
@@ -224,6 +279,13 @@ struct Tile {
         }
     }
 
+    // Store one row (16 elements) of this thread into a tile in shared memory.
+    __device__ __forceinline__ static void store_row_smem(TS *row, int lane, const float *s) {
+#pragma unroll
+        for (int k = 0; k < kChunks; ++k)
+            *reinterpret_cast<uint4 *>(row + (lane + L * k) * kVec) = StateChunk<TS>::pack(s + k * kVec);
+    }
+
     __device__ __forceinline__ static void store_row(TS *row, int lane, const float *s) {
 #pragma unroll
         for (int k = 0; k < kChunks; ++k)
@@ -275,39 +337,23 @@ __device__ __forceinline__ float update_elems(float *s, const float *b, const fl
     return acc;
 }
 
-// y = sum + D x, gated by silu(z) = z / (1 + e^-z) when z is given.
-__device__ __forceinline__ float output(float sum, float Dh, float x, bool has_z, float z) {
-    float y = fmaf(Dh, x, sum);
-    if (has_z) y *= z / (1.f + expf(-z));
-    return y;
+// y = (sum + D x) * gate, gate = silu(z) (or 1 without z).
+__device__ __forceinline__ float output(float sum, float Dh, float x, float gate) {
+    return fmaf(Dh, x, sum) * gate;
 }
 
-// Stage B[r, g, :] and C[r, g, :] as fp32 in shared memory (all threads).
-template <int N, int NT>
-__device__ __forceinline__ void stage_bc(const KParams &p, int64_t r, int g, float *sB, float *sC) {
-    const int64_t bo = r * p.Bs[0] + g * p.Bs[1];
-    const int64_t co = r * p.Cs[0] + g * p.Cs[1];
-    for (int n = threadIdx.x; n < N; n += NT) {
-        sB[n] = load_small(p.B, bo + n * p.Bs[2], p.io_dtype);
-        sC[n] = load_small(p.C, co + n * p.Cs[2], p.io_dtype);
-    }
-}
-
-// Scalars of one (row r, head h, dim row pr): dA, dt' x, x, z.
-struct RowScalars {
-    float dA, dtx, x, z;
+// Inputs of one (row, head, dim row): dt, x, z (z = 0 without a gate).
+struct RowInputs {
+    float dt, x, z;
 };
 
-__device__ __forceinline__ RowScalars row_scalars(const KParams &p, int64_t r, int h, int pr,
-                                                  float Ah, float bias) {
-    RowScalars q;
-    const float dt = load_small(p.dt, r * p.dts[0] + h * p.dts[1] + pr * p.dts[2], p.dt_dtype);
-    q.x = load_small(p.x, r * p.xs[0] + h * p.xs[1] + pr * p.xs[2], p.io_dtype);
-    q.z = p.z ? load_small(p.z, r * p.zs[0] + h * p.zs[1] + pr * p.zs[2], p.io_dtype) : 0.f;
-    const float d = step_size(dt, bias, p.softplus);
-    q.dA = expf(Ah * d);
-    q.dtx = d * q.x;
-    return q;
+// Per-row scalars {dA, dt' x, x, gate}, gate = silu(z) / z * z = z / (1 + e^-z)
+// with a z input, 1 without.  Not inlined: both kernels get exactly the same
+// instructions, hence the same bits.
+static __device__ __noinline__ float4 row_scalars(RowInputs in, float Ah, float bias, int softplus, int has_z) {
+    const float d = step_size(in.dt, bias, softplus);
+    const float gate = has_z ? in.z / (1.f + expf(-in.z)) : 1.f;
+    return make_float4(expf(Ah * d), d * in.x, in.x, gate);
 }
 
 // Slot at entry (b, t) of table `t`, or `fallback` without a table.  Returns

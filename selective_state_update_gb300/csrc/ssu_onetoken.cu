@@ -6,129 +6,441 @@
 // section 三个瓶颈: read the state, decay it, add the rank-1 term, read y out
 // of the updated state, write the state back.
 //
-// Work unit: (sequence b, head h, tile of kTileRows dim rows); one CTA each,
-// ptile fastest so that neighbouring CTAs stream neighbouring bytes of the
-// same slot.  The path is HBM-bound: every state byte is read once and
-// written once.  The tile (contiguous in the pool) arrives in shared memory
-// by one bulk asynchronous copy (TMA engine, mbarrier completion), so the
-// bytes in flight per SM are bounded by shared memory, not by registers;
-// meanwhile the CTA stages B and C of the unit's group in shared memory and
-// the per-row scalars in registers.  Results leave with 16-byte streaming
-// stores; y is reduced over dstate with shuffles.
+// Work unit: (sequence b, head h, tile of kTileRows dim rows), numbered with
+// the dim tile fastest, then the head, then the sequence, so that units next
+// to each other in the numbering read neighbouring blocks of a slot.
+//
+// The kernel is persistent and warp-specialised.  Each CTA (one or two per
+// SM) walks the units u = blockIdx.x + k * gridDim.x through a ring of
+// kStages shared-memory stages:
+//   producer warp  pure data movement, one unit ahead: resolves the unit's
+//                  read/destination slots, copies B and C of the unit's group
+//                  and the per-row inputs dt, x, z into the stage, and starts
+//                  the bulk asynchronous copy (TMA engine) of the unit's state
+//                  tile (contiguous in the pool) into the stage; completion
+//                  arrives on the stage's "full" mbarrier;
+//   consumer warps wait for "full", turn each row's inputs into its scalars
+//                  {dA, dt' x, x, silu gate} (one thread per row), update the
+//                  tile rows in registers, write y (one store per row) and
+//                  the new state back into the stage; one thread then starts
+//                  a bulk asynchronous copy of the stage to the destination
+//                  slot and, once the previous unit's copy has read its stage
+//                  out, releases that stage on its "empty" mbarrier.
+// The producer runs up to kStages units ahead, so state reads stay in flight
+// while the consumers compute, and the TMA engine moves the state both ways:
+// the bytes in flight per SM are set by the ring size, not by registers, by
+// store issue or by CTA launch latency.  The path is HBM-bound; every state
+// byte is read once and written once.
+#include <atomic>
+
 #include "ssu_device.cuh"
 
 namespace ssu {
 
-// Dynamic shared memory of a CTA: the state tile, B and C as fp32, the mbarrier.
+constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Size of the pieces a state tile is moved in by the TMA engine.
+#ifndef SSU_LOAD_CHUNK
+#define SSU_LOAD_CHUNK 32768
+#endif
+#ifndef SSU_STORE_CHUNK
+#define SSU_STORE_CHUNK 32768
+#endif
+constexpr int kLoadChunk = SSU_LOAD_CHUNK;
+constexpr int kStoreChunk = SSU_STORE_CHUNK;
+
 template <typename TS, int L>
-struct OnetokenSmem {
-    static constexpr int kTileBytes = kTileRows * Tile<TS, L>::kN * static_cast<int>(sizeof(TS));
-    static constexpr int kBytes = kTileBytes + 2 * Tile<TS, L>::kN * 4 + 16;
+struct OnetokenPipe {
+    static constexpr int kN = Tile<TS, L>::kN;
+    static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
+    static constexpr int kStageBytes = align_up(kTileBytes + 2 * kN * 4 + kTileRows * 16 + 32, 128);
+    // Shared memory per CTA when two CTAs share an SM (228 KB per SM).
+    static constexpr int kHalfSm = 110 * 1024;
+    static constexpr int kCtasPerSm = (kHalfSm / kStageBytes >= 3) ? 2 : 1;
+    static constexpr int kRingBytes = kCtasPerSm == 2 ? kHalfSm : 2 * kHalfSm;
+    static constexpr int kStages = (kRingBytes / kStageBytes) < 6 ? (kRingBytes / kStageBytes) : 6;
+    static constexpr int kBarOffset = kStages * kStageBytes;
+    static constexpr int kBytes = kBarOffset + kStages * 16;
+    static constexpr int kConsumerWarps = (Tile<TS, L>::kThreads + 31) / 32;
+    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+    static_assert(kStages >= 2, "state tile too large for a pipelined ring");
 };
 
+// Per-stage header written by the producer.
+struct UnitHeader {
+    int64_t ws;        // destination slot
+    int32_t flags;     // kUnit* bits
+    float Dh, Ah, bias;  // D[h] (0 without D), A[h], dt_bias[h] (0 without)
+    int32_t reserved;
+};
+enum : int32_t { kUnitValid = 1, kUnitSeeded = 2, kUnitWrite = 4 };
+
 template <typename TS, int L>
-__global__ void __launch_bounds__(Tile<TS, L>::kThreads)
-    ssu_onetoken_kernel(const KParams p) {
-    using T = Tile<TS, L>;
-    constexpr int N = T::kN;
-    constexpr int NT = T::kThreads;
-    extern __shared__ __align__(128) unsigned char smem[];
-    TS *tile = reinterpret_cast<TS *>(smem);
-    float *sB = reinterpret_cast<float *>(smem + OnetokenSmem<TS, L>::kTileBytes);
-    float *sC = sB + N;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sC + N);
-
-    const int64_t unit = blockIdx.x;
-    const int ptile = static_cast<int>(unit % p.ptiles);
-    const int64_t bh = unit / p.ptiles;
-    const int h = static_cast<int>(bh % p.H);
-    const int64_t b = bh / p.H;
-    const int g = h / p.heads_per_group;
-
-    // Slots (uniform over the CTA).  One token: entry (b, 0), row_start b.
-    int64_t rs, ws;
-    if (!table_slot(p, p.rd, b, 0, b, b, &rs)) return;
-    if (p.wr.entries != nullptr) {
-        if (!table_slot(p, p.wr, b, 0, b, b, &ws)) return;
-    } else {
-        ws = rs;
+struct StageView {
+    using PS = OnetokenPipe<TS, L>;
+    TS *tile;
+    float *B, *C;
+    float4 *rowq;
+    UnitHeader *hd;
+    __device__ __forceinline__ StageView(unsigned char *smem, int s) {
+        unsigned char *base = smem + s * PS::kStageBytes;
+        tile = reinterpret_cast<TS *>(base);
+        B = reinterpret_cast<float *>(base + PS::kTileBytes);
+        C = B + PS::kN;
+        rowq = reinterpret_cast<float4 *>(C + PS::kN);
+        hd = reinterpret_cast<UnitHeader *>(rowq + kTileRows);
     }
-    if (!slot_ok(p, rs) || !slot_ok(p, ws)) return;
+};
 
-    const int tid = threadIdx.x;
-    const int lane = tid % L;
-    const int slot_row = tid / L;
-    const int row0 = ptile * kTileRows;
-    const int rows_here = min(kTileRows, p.P - row0);
-    const int64_t head_row0 = (static_cast<int64_t>(h)) * p.P + row0;
-    const bool seeded = rs != p.pad;
+struct UnitCoords {
+    int64_t b;
+    int h, g, row0, rows_here;
+};
 
-    // One thread starts the bulk copy of the tile (rows_here contiguous rows);
-    // the others stage B, C and the per-row scalars meanwhile.
-    if (tid == 0 && seeded) {
-        const uint32_t bytes = static_cast<uint32_t>(rows_here) * N * sizeof(TS);
-        mbar_init(bar, 1);
-        mbar_arrive_expect(bar, bytes);
-        bulk_load(tile, static_cast<const TS *>(p.state) + (rs * p.H * p.P + head_row0) * N, bytes, bar);
-    }
-    stage_bc<N, NT>(p, b, g, sB, sC);
-    const float Ah = __ldg(p.A + h);
-    const float Dh = p.D ? __ldg(p.D + h) : 0.f;
-    const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
-    RowScalars q[kRowsPerThread];
-#pragma unroll
-    for (int j = 0; j < kRowsPerThread; ++j) {
-        const int pr = row0 + slot_row + j * kRowSlots;
-        q[j] = row_scalars(p, b, h, pr < p.P ? pr : 0, Ah, bias);
-    }
-    __syncthreads();
-    float bv[kElemsPerThread], cv[kElemsPerThread];
-    T::gather(sB, lane, bv);
-    T::gather(sC, lane, cv);
-    if (seeded && !mbar_wait_bounded(bar, 0)) {
-        flag(p.status, kDevTimeout);
-        return;
-    }
+// Walks this CTA's units u = blockIdx.x + k * gridDim.x as (sequence, head,
+// dim tile) with additions and carries only: no 64-bit division per unit.
+struct UnitWalker {
+    int pt, h;          // current dim tile and head
+    int64_t b;          // current sequence
+    int d_pt, d_h;      // the stride gridDim.x as (tiles, heads, sequences)
+    int64_t d_b;
 
-    const bool write_state = !p.disable && ws != p.pad;
-    TS *dst = static_cast<TS *>(p.state) + (ws * p.H * p.P + head_row0) * N;
-#pragma unroll(kOnetokenUnroll)
-    for (int j = 0; j < kRowsPerThread; ++j) {
-        const int r = slot_row + j * kRowSlots;  // row within the tile
-        float s[kElemsPerThread];
-        if (seeded && r < rows_here) {
-            T::load_row_smem(tile + r * N, lane, s);
-        } else {
-#pragma unroll
-            for (int i = 0; i < kElemsPerThread; ++i) s[i] = 0.f;
+    __device__ __forceinline__ UnitWalker(const KParams &p) {
+        const int64_t u = blockIdx.x, step = gridDim.x;
+        pt = static_cast<int>(u % p.ptiles);
+        h = static_cast<int>((u / p.ptiles) % p.H);
+        b = u / (static_cast<int64_t>(p.ptiles) * p.H);
+        d_pt = static_cast<int>(step % p.ptiles);
+        d_h = static_cast<int>((step / p.ptiles) % p.H);
+        d_b = step / (static_cast<int64_t>(p.ptiles) * p.H);
+    }
+    __device__ __forceinline__ void advance(const KParams &p) {
+        pt += d_pt;
+        int carry = 0;
+        if (pt >= p.ptiles) {
+            pt -= p.ptiles;
+            carry = 1;
         }
-        const float part = update_elems(s, bv, cv, q[j].dA, q[j].dtx);
-        const float sum = row_sum<L>(part);
-        if (r < rows_here) {
-            if (lane == 0) {
-                const float y = output(sum, Dh, q[j].x, p.z != nullptr, q[j].z);
-                store_small(p.y, b * p.ys[0] + h * p.ys[1] + (row0 + r) * p.ys[2], p.io_dtype, y);
+        h += d_h + carry;
+        carry = 0;
+        if (h >= p.H) {
+            h -= p.H;
+            carry = 1;
+        }
+        b += d_b + carry;
+    }
+    __device__ __forceinline__ UnitCoords coords(const KParams &p) const {
+        UnitCoords c;
+        c.b = b;
+        c.h = h;
+        c.g = h / p.heads_per_group;
+        c.row0 = pt * kTileRows;
+        c.rows_here = min(kTileRows, p.P - c.row0);
+        return c;
+    }
+};
+
+// Everything the producer needs from global memory for one unit, loaded into
+// registers one unit ahead so that the loads are in flight while the producer
+// stages the previous unit or waits for a free stage.  The loads are issued
+// as raw bits, back to back, and converted only when the unit is staged.
+template <typename TS, int L>
+struct UnitOperands {
+    static constexpr int kN = Tile<TS, L>::kN;
+    static constexpr int kPerB = (kN + 31) / 32;
+    static constexpr int kPerRow = (kTileRows + 31) / 32;
+    UnitCoords c;
+    int64_t rs, ws;  // lane 0: raw slots (valid when entries_ok)
+    bool entries_ok;
+    uint32_t b[kPerB], cc[kPerB];
+    uint32_t dt[kPerRow], x[kPerRow], z[kPerRow];
+    float Ah, bias, Dh;
+
+    template <bool WIO, bool WDT>
+    __device__ __forceinline__ void load_operands(const KParams &p, int lane) {
+        const int64_t bo = c.b * p.Bs[0] + c.g * p.Bs[1];
+        const int64_t co = c.b * p.Cs[0] + c.g * p.Cs[1];
+#pragma unroll
+        for (int i = 0; i < kPerB; ++i) {
+            const int n = lane + 32 * i;
+            if (n < kN) {
+                b[i] = load_bits<WIO>(p.B, bo + n * p.Bs[2]);
+                cc[i] = load_bits<WIO>(p.C, co + n * p.Cs[2]);
             }
-            if (write_state) T::store_row(dst + r * N, lane, s);
         }
+#pragma unroll
+        for (int i = 0; i < kPerRow; ++i) {
+            const int pr = c.row0 + lane + 32 * i;
+            if (lane + 32 * i < c.rows_here) {
+                dt[i] = load_bits<WDT>(p.dt, c.b * p.dts[0] + c.h * p.dts[1] + pr * p.dts[2]);
+                x[i] = load_bits<WIO>(p.x, c.b * p.xs[0] + c.h * p.xs[1] + pr * p.xs[2]);
+                z[i] = p.z ? load_bits<WIO>(p.z, c.b * p.zs[0] + c.h * p.zs[1] + pr * p.zs[2]) : 0u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void load(const KParams &p, const UnitCoords &cu, int lane) {
+        c = cu;
+        entries_ok = true;
+        rs = ws = 0;
+        if (lane == 0) {
+            entries_ok = table_slot(p, p.rd, c.b, 0, c.b, c.b, &rs);
+            if (p.wr.entries != nullptr)
+                entries_ok = table_slot(p, p.wr, c.b, 0, c.b, c.b, &ws) && entries_ok;
+        }
+        const bool wio = p.io_dtype == kF32, wdt = p.dt_dtype == kF32;
+        if (wio) {
+            if (wdt) load_operands<true, true>(p, lane);
+            else load_operands<true, false>(p, lane);
+        } else {
+            if (wdt) load_operands<false, true>(p, lane);
+            else load_operands<false, false>(p, lane);
+        }
+        Ah = __ldg(p.A + c.h);
+        bias = p.dt_bias ? __ldg(p.dt_bias + c.h) : 0.f;
+        Dh = p.D ? __ldg(p.D + c.h) : 0.f;
+    }
+};
+
+// Stage one unit: header, B, C, row scalars, then the tile copy (or a plain
+// arrival when there is nothing to copy).  Returns false on a timed-out wait.
+template <typename TS, int L>
+__device__ __forceinline__ bool produce_unit(const KParams &p, const UnitOperands<TS, L> &op, int k,
+                                             unsigned char *smem, uint64_t *full, uint64_t *empty, int lane) {
+    using PS = OnetokenPipe<TS, L>;
+    constexpr int N = PS::kN;
+    constexpr int S = PS::kStages;
+    const int s = k % S;
+    const int round = k / S;
+    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1)) {
+        if (lane == 0) flag(p.status, kDevTimeout);
+        return false;
+    }
+    const StageView<TS, L> st(smem, s);
+    int32_t flags = 0;
+    if (lane == 0) {
+        const int64_t ws = (p.wr.entries != nullptr) ? op.ws : op.rs;
+        if (op.entries_ok && slot_ok(p, op.rs) && slot_ok(p, ws)) {
+            flags = kUnitValid;
+            if (op.rs != p.pad) flags |= kUnitSeeded;
+            if (!p.disable && ws != p.pad) flags |= kUnitWrite;
+        }
+        st.hd->ws = ws;
+        st.hd->flags = flags;
+        st.hd->Dh = op.Dh;
+        st.hd->Ah = op.Ah;
+        st.hd->bias = op.bias;
+    }
+#pragma unroll
+    for (int i = 0; i < UnitOperands<TS, L>::kPerB; ++i) {
+        const int n = lane + 32 * i;
+        if (n < N) {
+            st.B[n] = bits_to_float(op.b[i], p.io_dtype);
+            st.C[n] = bits_to_float(op.cc[i], p.io_dtype);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < UnitOperands<TS, L>::kPerRow; ++i) {
+        const int r = lane + 32 * i;
+        if (r < op.c.rows_here)
+            st.rowq[r] = make_float4(bits_to_float(op.dt[i], p.dt_dtype), bits_to_float(op.x[i], p.io_dtype),
+                                     bits_to_float(op.z[i], p.io_dtype), 0.f);
+    }
+    flags = __shfl_sync(0xffffffffu, flags, 0);
+    if (flags & kUnitSeeded) {
+        // The tile is copied as kLoadChunk-byte pieces issued by all lanes;
+        // lane 0 registers the total before any piece can complete.
+        const uint32_t bytes = static_cast<uint32_t>(op.c.rows_here) * N * sizeof(TS);
+        const int64_t rs = __shfl_sync(0xffffffffu, op.rs, 0);
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(
+            static_cast<const TS *>(p.state) + ((rs * p.H + op.c.h) * static_cast<int64_t>(p.P) + op.c.row0) * N);
+        if (lane == 0) mbar_arrive_expect(&full[s], bytes);
+        __syncwarp();
+        unsigned char *dst = reinterpret_cast<unsigned char *>(st.tile);
+        for (uint32_t off = static_cast<uint32_t>(lane) * kLoadChunk; off < bytes; off += 32u * kLoadChunk) {
+            const uint32_t n = bytes - off < static_cast<uint32_t>(kLoadChunk) ? bytes - off : kLoadChunk;
+            bulk_load(dst + off, src + off, n, &full[s]);
+        }
+        if (lane != 0) mbar_arrive(&full[s]);
+    } else {
+        mbar_arrive(&full[s]);
+    }
+    return true;
+}
+
+template <typename TS, int L>
+__device__ __forceinline__ void onetoken_producer(const KParams &p, int64_t units, unsigned char *smem,
+                                                  uint64_t *full, uint64_t *empty) {
+    const int lane = threadIdx.x & 31;
+    const int64_t step = gridDim.x;
+    // Two operand sets used in turn: the next unit's loads are issued before
+    // the current unit is staged (no register copies between them).
+    UnitOperands<TS, L> a, b;
+    UnitWalker walk(p);
+    int64_t u = blockIdx.x;
+    if (u < units) a.load(p, walk.coords(p), lane);
+    for (int k = 0; u < units; k += 2, u += 2 * step) {
+        walk.advance(p);
+        if (u + step < units) b.load(p, walk.coords(p), lane);
+        if (!produce_unit<TS, L>(p, a, k, smem, full, empty, lane)) return;
+        if (u + step >= units) break;
+        walk.advance(p);
+        if (u + 2 * step < units) a.load(p, walk.coords(p), lane);
+        if (!produce_unit<TS, L>(p, b, k + 1, smem, full, empty, lane)) return;
     }
 }
 
-// Dynamic shared memory above the 48 KiB default needs an opt-in per kernel.
 template <typename TS, int L>
-static cudaError_t set_smem_attr() {
-    constexpr int bytes = OnetokenSmem<TS, L>::kBytes;
-    if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(ssu_onetoken_kernel<TS, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+__device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t units, unsigned char *smem,
+                                                  uint64_t *full, uint64_t *empty) {
+    using T = Tile<TS, L>;
+    using PS = OnetokenPipe<TS, L>;
+    constexpr int N = PS::kN;
+    constexpr int S = PS::kStages;
+    constexpr int kConsumers = 32 * PS::kConsumerWarps;
+    const int tid = threadIdx.x;
+    const bool active = tid < T::kThreads;
+    const int lane = tid % L;
+    const int slot_row = tid / L;
+    int prev_s = -1;
+    int k = 0;
+    UnitWalker walk(p);
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++k, walk.advance(p)) {
+        const int s = k % S;
+        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1);
+        if (barrier_or(1, kConsumers, !ok)) {  // a wait gave up: every consumer stops here
+            if (tid == 0) {
+                flag(p.status, kDevTimeout);
+                bulk_wait_all();
+            }
+            return;
+        }
+        const StageView<TS, L> st(smem, s);
+        const int32_t flags = st.hd->flags;
+        const UnitCoords c = walk.coords(p);
+        if (flags & kUnitValid) {
+            // Row scalars, one thread per row, in place of the row inputs.
+            const float Ah = st.hd->Ah, bias = st.hd->bias;
+            for (int r = tid; r < c.rows_here; r += kConsumers) {
+                const float4 in = st.rowq[r];
+                st.rowq[r] = row_scalars(RowInputs{in.x, in.y, in.z}, Ah, bias, p.softplus, p.z != nullptr);
+            }
+            named_barrier(1, kConsumers);
+            if (active) {
+                const float Dh = st.hd->Dh;
+                float bv[kElemsPerThread], cv[kElemsPerThread];
+                T::gather(st.B, lane, bv);
+                T::gather(st.C, lane, cv);
+#pragma unroll(kOnetokenUnroll)
+                for (int j = 0; j < kRowsPerThread; ++j) {
+                    const int rr = slot_row + j * kRowSlots;  // row within the tile
+                    const bool live = rr < c.rows_here;
+                    const float4 q = st.rowq[live ? rr : 0];
+                    float sv[kElemsPerThread];
+                    if ((flags & kUnitSeeded) && live) {
+                        T::load_row_smem(st.tile + rr * N, lane, sv);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kElemsPerThread; ++i) sv[i] = 0.f;
+                    }
+                    const float sum = row_sum<L>(update_elems(sv, bv, cv, q.x, q.y));
+                    if (live) {
+                        if (lane == 0)
+                            store_small(p.y, c.b * p.ys[0] + c.h * p.ys[1] + (c.row0 + rr) * p.ys[2], p.io_dtype,
+                                        output(sum, Dh, q.z, q.w));
+                        // The new state goes back into the stage; the TMA
+                        // engine writes the whole tile to its destination.
+                        T::store_row_smem(st.tile + rr * N, lane, sv);
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        named_barrier(1, kConsumers);
+        if (tid == 0) {
+            if ((flags & kUnitValid) && (flags & kUnitWrite)) {
+                unsigned char *dst = reinterpret_cast<unsigned char *>(
+                    static_cast<TS *>(p.state) + ((st.hd->ws * p.H + c.h) * static_cast<int64_t>(p.P) + c.row0) * N);
+                const unsigned char *src = reinterpret_cast<const unsigned char *>(st.tile);
+                const uint32_t bytes = static_cast<uint32_t>(c.rows_here) * N * sizeof(TS);
+                for (uint32_t off = 0; off < bytes; off += kStoreChunk)
+                    bulk_store(dst + off, src + off, bytes - off < static_cast<uint32_t>(kStoreChunk) ? bytes - off
+                                                                                                    : kStoreChunk);
+            }
+            bulk_commit();
+            // The previous unit's tile has been read out by its store: its
+            // stage may be refilled.
+            if (prev_s >= 0) {
+                bulk_wait_read<1>();
+                mbar_arrive(&empty[prev_s]);
+            }
+        }
+        prev_s = s;
+    }
+    if (tid == 0) bulk_wait_all();
+}
+
+template <typename TS, int L>
+__global__ void __launch_bounds__(OnetokenPipe<TS, L>::kThreads)
+    ssu_onetoken_kernel(const KParams p, int64_t units) {
+    using PS = OnetokenPipe<TS, L>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + PS::kBarOffset);
+    uint64_t *empty = full + PS::kStages;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PS::kStages; ++s) {
+            mbar_init(&full[s], 32);
+            mbar_init(&empty[s], 1);
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x / 32 == PS::kConsumerWarps)
+        onetoken_producer<TS, L>(p, units, smem, full, empty);
+    else
+        onetoken_consumer<TS, L>(p, units, smem, full, empty);
+}
+
+// Number of SMs of the current device (cached per device).
+static int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// The ring needs more than the 48 KiB default of dynamic shared memory: opt
+// in once per device.
+template <typename TS, int L>
+static cudaError_t smem_opt_in() {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(ssu_onetoken_kernel<TS, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             OnetokenPipe<TS, L>::kBytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
 }
 
 template <typename TS, int L>
 static cudaError_t launch_t(const KParams &p, int64_t batch, cudaStream_t stream) {
-    cudaError_t e = set_smem_attr<TS, L>();
+    using PS = OnetokenPipe<TS, L>;
+    cudaError_t e = smem_opt_in<TS, L>();
     if (e != cudaSuccess) return e;
     const int64_t units = batch * p.H * p.ptiles;
-    ssu_onetoken_kernel<TS, L><<<static_cast<unsigned>(units), Tile<TS, L>::kThreads,
-                                 OnetokenSmem<TS, L>::kBytes, stream>>>(p);
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t slots_on_gpu = static_cast<int64_t>(sms) * PS::kCtasPerSm;
+    const int64_t grid = units < slots_on_gpu ? units : slots_on_gpu;
+    ssu_onetoken_kernel<TS, L><<<static_cast<unsigned>(grid), PS::kThreads, PS::kBytes, stream>>>(p, units);
     return cudaGetLastError();
 }
 
@@ -158,7 +470,9 @@ template <typename TS, int L>
 static cudaError_t attrs_t() {
     cudaFuncAttributes a;
     cudaError_t e = cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, L>);
-    return e != cudaSuccess ? e : set_smem_attr<TS, L>();
+    if (e != cudaSuccess) return e;
+    if (sm_count() <= 0) return cudaErrorInvalidDevice;
+    return smem_opt_in<TS, L>();
 }
 
 template <typename TS>

@@ -8,27 +8,28 @@
 // table); pad destinations are never written; empty sequences are skipped.
 // Section Graph capture: one launch, no host/device scalar copies.
 //
-// Work unit: (sequence b, head h, tile of kTileRows dim rows).  The seed tile
-// arrives in shared memory by one bulk asynchronous copy (TMA engine); the
-// unit's state then stays in shared memory as fp32 across the sequence's
-// tokens (each thread only ever touches its own elements), so it is read
-// from HBM once and written once per token, with 16-byte streaming stores.
-// B and C of each token are staged in shared memory, double-buffered so that
-// one barrier per token suffices.
+// Work unit: (sequence b, head h, tile of kTileRows dim rows), one CTA each.
+// The seed tile arrives in shared memory by one bulk asynchronous copy (TMA
+// engine, mbarrier completion); the unit's state then stays in shared memory
+// as fp32 across the sequence's tokens (each thread only ever touches its own
+// elements), so it is read from HBM once and written once per token, with
+// 16-byte streaming stores.  Each token's B, C and per-row scalars {dA,
+// dt' x, x, z} are loaded while the previous token computes and staged in
+// shared memory (double-buffered, one barrier per token); every row's
+// scalars are computed once, by one thread.
 #include "ssu_device.cuh"
 
 namespace ssu {
 
-// Dynamic shared memory of a CTA: the fp32 carried state tile (the seed lands
-// in it directly for an fp32 pool), the seed tile for a 16-bit pool, B and C
-// double-buffered as fp32, the mbarrier.
 template <typename TS, int L>
 struct PackedSmem {
     static constexpr int kN = Tile<TS, L>::kN;
     static constexpr int kCarryBytes = kTileRows * kN * 4;
     static constexpr int kSeedBytes = sizeof(TS) == 4 ? 0 : kTileRows * kN * static_cast<int>(sizeof(TS));
-    static constexpr int kBCOffset = kCarryBytes + kSeedBytes;
-    static constexpr int kBytes = kBCOffset + 4 * kN * 4 + 16;
+    static constexpr int kBCOffset = kCarryBytes + kSeedBytes;             // B[2][N], C[2][N]
+    static constexpr int kRowQOffset = kBCOffset + 4 * kN * 4;             // float4 [2][kTileRows]
+    static constexpr int kBarOffset = kRowQOffset + 2 * kTileRows * 16;
+    static constexpr int kBytes = kBarOffset + 16;
 };
 
 // The fp32 carry uses the element order of Tile<TS, L> (16-byte chunks of
@@ -60,24 +61,92 @@ __device__ __forceinline__ void carry_store(float *row, int lane, const float *s
                             s[k * kVec + 4 * q + 3]);
 }
 
+// One token's small operands, loaded into registers ahead of time (as raw
+// bits, back to back, so that they are in flight together) and staged in
+// shared memory afterwards, converted to fp32 and turned into row scalars.
+template <int N, int NT>
+struct TokenOperands {
+    static constexpr int kPerB = (N + NT - 1) / NT;
+    static constexpr int kPerRow = (kTileRows + NT - 1) / NT;
+    uint32_t b[kPerB], c[kPerB];
+    uint32_t dt[kPerRow], x[kPerRow], z[kPerRow];
+
+    template <bool WIO, bool WDT>
+    __device__ __forceinline__ void load_t(const KParams &p, int64_t r, int g, int h, int row0, int rows_here) {
+        const int64_t bo = r * p.Bs[0] + g * p.Bs[1];
+        const int64_t co = r * p.Cs[0] + g * p.Cs[1];
+#pragma unroll
+        for (int i = 0; i < kPerB; ++i) {
+            const int n = threadIdx.x + i * NT;
+            if (n < N) {
+                b[i] = load_bits<WIO>(p.B, bo + n * p.Bs[2]);
+                c[i] = load_bits<WIO>(p.C, co + n * p.Cs[2]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kPerRow; ++i) {
+            const int rr = threadIdx.x + i * NT;
+            if (rr < rows_here) {
+                const int pr = row0 + rr;
+                dt[i] = load_bits<WDT>(p.dt, r * p.dts[0] + h * p.dts[1] + pr * p.dts[2]);
+                x[i] = load_bits<WIO>(p.x, r * p.xs[0] + h * p.xs[1] + pr * p.xs[2]);
+                z[i] = p.z ? load_bits<WIO>(p.z, r * p.zs[0] + h * p.zs[1] + pr * p.zs[2]) : 0u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void load(const KParams &p, int64_t r, int g, int h, int row0, int rows_here) {
+        const bool wio = p.io_dtype == kF32, wdt = p.dt_dtype == kF32;
+        if (wio) {
+            if (wdt) load_t<true, true>(p, r, g, h, row0, rows_here);
+            else load_t<true, false>(p, r, g, h, row0, rows_here);
+        } else {
+            if (wdt) load_t<false, true>(p, r, g, h, row0, rows_here);
+            else load_t<false, false>(p, r, g, h, row0, rows_here);
+        }
+    }
+
+    __device__ __forceinline__ void stage(const KParams &p, float *sB, float *sC, float4 *rowq, int rows_here,
+                                          float Ah, float bias) const {
+#pragma unroll
+        for (int i = 0; i < kPerB; ++i) {
+            const int n = threadIdx.x + i * NT;
+            if (n < N) {
+                sB[n] = bits_to_float(b[i], p.io_dtype);
+                sC[n] = bits_to_float(c[i], p.io_dtype);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kPerRow; ++i) {
+            const int rr = threadIdx.x + i * NT;
+            if (rr < rows_here) {
+                const RowInputs in{bits_to_float(dt[i], p.dt_dtype), bits_to_float(x[i], p.io_dtype),
+                                   bits_to_float(z[i], p.io_dtype)};
+                rowq[rr] = row_scalars(in, Ah, bias, p.softplus, p.z != nullptr);
+            }
+        }
+    }
+};
+
 // One token applied to this thread's rows.  FIRST: the state comes from the
 // seed tile (state dtype; zeros when the seed is the pad slot); later tokens
 // read the fp32 carry.  The carry is written back (fp32, never re-rounded) and
-// the rounded copy is published to the destination row when `dst` is set.
+// the rounded copy is published to the destination rows when `dst` is set.
 template <typename TS, int L, bool FIRST>
 __device__ __forceinline__ void token_rows(const KParams &p, int64_t r, int h, int row0, int rows_here,
-                                           int slot_row, int lane, const TS *seed, bool seeded,
-                                           float *carry, TS *dst, const float *bv, const float *cv,
-                                           float Ah, float Dh, float bias) {
+                                           int slot_row, int lane, const TS *seed, bool seeded, float *carry,
+                                           TS *dst, const float *bv, const float *cv, const float4 *rowq,
+                                           float Dh) {
     using T = Tile<TS, L>;
     constexpr int N = T::kN;
 #pragma unroll(kPackedUnroll)
     for (int j = 0; j < kRowsPerThread; ++j) {
         const int rr = slot_row + j * kRowSlots;  // row within the tile
-        const RowScalars q = row_scalars(p, r, h, row0 + (rr < rows_here ? rr : 0), Ah, bias);
+        const bool live = rr < rows_here;
+        const float4 q = rowq[live ? rr : 0];
         float s[kElemsPerThread];
         if (FIRST) {
-            if (seeded && rr < rows_here) {
+            if (seeded && live) {
                 T::load_row_smem(seed + rr * N, lane, s);
             } else {
 #pragma unroll
@@ -86,13 +155,11 @@ __device__ __forceinline__ void token_rows(const KParams &p, int64_t r, int h, i
         } else {
             carry_load<TS, L>(carry + rr * N, lane, s);
         }
-        const float part = update_elems(s, bv, cv, q.dA, q.dtx);
-        const float sum = row_sum<L>(part);
-        if (rr < rows_here) {
-            if (lane == 0) {
-                const float y = output(sum, Dh, q.x, p.z != nullptr, q.z);
-                store_small(p.y, r * p.ys[0] + h * p.ys[1] + (row0 + rr) * p.ys[2], p.io_dtype, y);
-            }
+        const float sum = row_sum<L>(update_elems(s, bv, cv, q.x, q.y));
+        if (live) {
+            if (lane == 0)
+                store_small(p.y, r * p.ys[0] + h * p.ys[1] + (row0 + rr) * p.ys[2], p.io_dtype,
+                            output(sum, Dh, q.z, q.w));
             carry_store<TS, L>(carry + rr * N, lane, s);
             if (dst != nullptr) T::store_row(dst + rr * N, lane, s);
         }
@@ -111,7 +178,8 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     TS *seed = sizeof(TS) == 4 ? reinterpret_cast<TS *>(smem) : reinterpret_cast<TS *>(smem + SM::kCarryBytes);
     float *sB = reinterpret_cast<float *>(smem + SM::kBCOffset);  // [2][N]
     float *sC = sB + 2 * N;                                        // [2][N]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sC + 2 * N);
+    float4 *rowq = reinterpret_cast<float4 *>(smem + SM::kRowQOffset);  // [2][kTileRows]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + SM::kBarOffset);
 
     const int64_t unit = blockIdx.x;
     const int ptile = static_cast<int>(unit % p.ptiles);
@@ -170,7 +238,9 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     const float Ah = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
     const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
-    stage_bc<N, NT>(p, start, g, sB, sC);
+    TokenOperands<N, NT> ops;
+    ops.load(p, start, g, h, row0, rows_here);
+    ops.stage(p, sB, sC, rowq, rows_here, Ah, bias);
     __syncthreads();
     int timed_out = 0;
     if (seeded && !mbar_wait_bounded(bar, 0)) timed_out = 1;
@@ -182,9 +252,8 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     for (int64_t t = 0; t < len; ++t) {
         const int64_t r = start + t;
         const int buf = static_cast<int>(t & 1);
-        // Prefetch the next token's B and C into the other buffer; its last
-        // readers finished before the barrier that ended the previous token.
-        if (t + 1 < len) stage_bc<N, NT>(p, r + 1, g, sB + (buf ^ 1) * N, sC + (buf ^ 1) * N);
+        const bool more = t + 1 < len;
+        if (more) ops.load(p, r + 1, g, h, row0, rows_here);  // in flight during this token
 
         int64_t ws;
         table_slot(p, wt, b, t, start, b, &ws);
@@ -195,11 +264,13 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
         T::gather(sB + buf * N, lane, bv);
         T::gather(sC + buf * N, lane, cv);
         if (t == 0)
-            token_rows<TS, L, true>(p, r, h, row0, rows_here, slot_row, lane, seed, seeded, carry, dst, bv,
-                                    cv, Ah, Dh, bias);
+            token_rows<TS, L, true>(p, r, h, row0, rows_here, slot_row, lane, seed, seeded, carry, dst, bv, cv,
+                                    rowq + buf * kTileRows, Dh);
         else
-            token_rows<TS, L, false>(p, r, h, row0, rows_here, slot_row, lane, seed, seeded, carry, dst, bv,
-                                     cv, Ah, Dh, bias);
+            token_rows<TS, L, false>(p, r, h, row0, rows_here, slot_row, lane, seed, seeded, carry, dst, bv, cv,
+                                     rowq + buf * kTileRows, Dh);
+        // The other buffers were last read before the previous barrier.
+        if (more) ops.stage(p, sB + (buf ^ 1) * N, sC + (buf ^ 1) * N, rowq + (buf ^ 1) * kTileRows, rows_here, Ah, bias);
         __syncthreads();
     }
 }
