@@ -8,11 +8,14 @@
 
 namespace ssu {
 
-// Rows of one (head, dim-tile) work unit: a CTA updates kTileRows dim rows of
-// one head of one sequence.
-constexpr int kTileRows = 64;
 // Each thread holds kRowsPerThread rows x kElemsPerThread dstate elements.
-constexpr int kRowsPerThread = 4;
+#ifndef SSU_ROWS_PER_THREAD
+#define SSU_ROWS_PER_THREAD 4
+#endif
+constexpr int kRowsPerThread = SSU_ROWS_PER_THREAD;
+// Rows of one (head, dim-tile) work unit: kTileRows dim rows of one head of
+// one sequence.
+constexpr int kTileRows = 16 * kRowsPerThread;
 constexpr int kElemsPerThread = 16;
 // Row slots per CTA: kTileRows / kRowsPerThread.  A CTA has
 // kRowSlots * L threads, L = dstate / kElemsPerThread lanes per row.

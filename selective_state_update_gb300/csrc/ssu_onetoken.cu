@@ -47,6 +47,12 @@ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 #define SSU_STORE_CHUNK 32768
 #endif
 constexpr int kLoadChunk = SSU_LOAD_CHUNK;
+#ifndef SSU_PRODUCER_WARPS
+#define SSU_PRODUCER_WARPS 2
+#endif
+#ifndef SSU_DIRECT_STORE
+#define SSU_DIRECT_STORE 0
+#endif
 constexpr int kStoreChunk = SSU_STORE_CHUNK;
 
 template <typename TS, int L>
@@ -62,7 +68,8 @@ struct OnetokenPipe {
     static constexpr int kBarOffset = kStages * kStageBytes;
     static constexpr int kBytes = kBarOffset + kStages * 16;
     static constexpr int kConsumerWarps = (Tile<TS, L>::kThreads + 31) / 32;
-    static constexpr int kThreads = 32 * (kConsumerWarps + 1);
+    static constexpr int kProducerWarps = SSU_PRODUCER_WARPS;
+    static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
     static_assert(kStages >= 2, "state tile too large for a pipelined ring");
 };
 
@@ -105,8 +112,7 @@ struct UnitWalker {
     int d_pt, d_h;      // the stride gridDim.x as (tiles, heads, sequences)
     int64_t d_b;
 
-    __device__ __forceinline__ UnitWalker(const KParams &p) {
-        const int64_t u = blockIdx.x, step = gridDim.x;
+    __device__ __forceinline__ UnitWalker(const KParams &p, int64_t u, int64_t step) {
         pt = static_cast<int>(u % p.ptiles);
         h = static_cast<int>((u / p.ptiles) % p.H);
         b = u / (static_cast<int64_t>(p.ptiles) * p.H);
@@ -268,25 +274,28 @@ __device__ __forceinline__ bool produce_unit(const KParams &p, const UnitOperand
     return true;
 }
 
+// Producer warp `w` of kProducerWarps stages the CTA's units k = w, w + P,
+// w + 2P, ... (P = kProducerWarps), i.e. global units blockIdx.x + k * gridDim.x.
 template <typename TS, int L>
 __device__ __forceinline__ void onetoken_producer(const KParams &p, int64_t units, unsigned char *smem,
-                                                  uint64_t *full, uint64_t *empty) {
+                                                  uint64_t *full, uint64_t *empty, int w) {
+    constexpr int P = OnetokenPipe<TS, L>::kProducerWarps;
     const int lane = threadIdx.x & 31;
-    const int64_t step = gridDim.x;
+    const int64_t step = static_cast<int64_t>(P) * gridDim.x;
     // Two operand sets used in turn: the next unit's loads are issued before
     // the current unit is staged (no register copies between them).
     UnitOperands<TS, L> a, b;
-    UnitWalker walk(p);
-    int64_t u = blockIdx.x;
+    int64_t u = blockIdx.x + static_cast<int64_t>(w) * gridDim.x;
+    UnitWalker walk(p, u, step);
     if (u < units) a.load(p, walk.coords(p), lane);
-    for (int k = 0; u < units; k += 2, u += 2 * step) {
+    for (int k = w; u < units; k += 2 * P, u += 2 * step) {
         walk.advance(p);
         if (u + step < units) b.load(p, walk.coords(p), lane);
         if (!produce_unit<TS, L>(p, a, k, smem, full, empty, lane)) return;
         if (u + step >= units) break;
         walk.advance(p);
         if (u + 2 * step < units) a.load(p, walk.coords(p), lane);
-        if (!produce_unit<TS, L>(p, b, k + 1, smem, full, empty, lane)) return;
+        if (!produce_unit<TS, L>(p, b, k + P, smem, full, empty, lane)) return;
     }
 }
 
@@ -304,7 +313,7 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
     const int slot_row = tid / L;
     int prev_s = -1;
     int k = 0;
-    UnitWalker walk(p);
+    UnitWalker walk(p, blockIdx.x, gridDim.x);
     for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++k, walk.advance(p)) {
         const int s = k % S;
         const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1);
@@ -328,6 +337,10 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
             named_barrier(1, kConsumers);
             if (active) {
                 const float Dh = st.hd->Dh;
+#if SSU_DIRECT_STORE
+                TS *dst = static_cast<TS *>(p.state) +
+                          ((st.hd->ws * p.H + c.h) * static_cast<int64_t>(p.P) + c.row0) * N;
+#endif
                 float bv[kElemsPerThread], cv[kElemsPerThread];
                 T::gather(st.B, lane, bv);
                 T::gather(st.C, lane, cv);
@@ -348,13 +361,22 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
                         if (lane == 0)
                             store_small(p.y, c.b * p.ys[0] + c.h * p.ys[1] + (c.row0 + rr) * p.ys[2], p.io_dtype,
                                         output(sum, Dh, q.z, q.w));
+#if SSU_DIRECT_STORE
+                        if (flags & kUnitWrite) T::store_row(dst + rr * N, lane, sv);
+#else
                         // The new state goes back into the stage; the TMA
                         // engine writes the whole tile to its destination.
                         T::store_row_smem(st.tile + rr * N, lane, sv);
+#endif
                     }
                 }
             }
         }
+#if SSU_DIRECT_STORE
+        __syncwarp();
+        if ((tid & 31) == 0) mbar_arrive(&empty[s]);
+        continue;
+#endif
         fence_proxy_async_smem();
         named_barrier(1, kConsumers);
         if (tid == 0) {
@@ -390,12 +412,13 @@ __global__ void __launch_bounds__(OnetokenPipe<TS, L>::kThreads)
     if (threadIdx.x == 0) {
         for (int s = 0; s < PS::kStages; ++s) {
             mbar_init(&full[s], 32);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], SSU_DIRECT_STORE ? PS::kConsumerWarps : 1);
         }
     }
     __syncthreads();
-    if (threadIdx.x / 32 == PS::kConsumerWarps)
-        onetoken_producer<TS, L>(p, units, smem, full, empty);
+    const int warp = threadIdx.x / 32;
+    if (warp >= PS::kConsumerWarps)
+        onetoken_producer<TS, L>(p, units, smem, full, empty, warp - PS::kConsumerWarps);
     else
         onetoken_consumer<TS, L>(p, units, smem, full, empty);
 }
