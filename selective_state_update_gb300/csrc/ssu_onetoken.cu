@@ -47,6 +47,9 @@ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 #define SSU_STORE_CHUNK 32768
 #endif
 constexpr int kLoadChunk = SSU_LOAD_CHUNK;
+#ifndef SSU_ONETOKEN_CTAS
+#define SSU_ONETOKEN_CTAS 0
+#endif
 #ifndef SSU_PRODUCER_WARPS
 #define SSU_PRODUCER_WARPS 2
 #endif
@@ -60,10 +63,15 @@ struct OnetokenPipe {
     static constexpr int kN = Tile<TS, L>::kN;
     static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
     static constexpr int kStageBytes = align_up(kTileBytes + 2 * kN * 4 + kTileRows * 16 + 32, 128);
-    // Shared memory per CTA when two CTAs share an SM (228 KB per SM).
-    static constexpr int kHalfSm = 110 * 1024;
-    static constexpr int kCtasPerSm = (kHalfSm / kStageBytes >= 3) ? 2 : 1;
-    static constexpr int kRingBytes = kCtasPerSm == 2 ? kHalfSm : 2 * kHalfSm;
+    // Dynamic shared memory an SM can give its CTAs (228 KB less the 1 KB
+    // each CTA reserves).  Small (16-bit) stages: three CTAs of four stages,
+    // so three consumer groups share the SM; fp32 stages: two CTAs of three.
+    static constexpr int kSmemPerSm = 222 * 1024;
+    static constexpr int kCtasPerSm = SSU_ONETOKEN_CTAS > 0                 ? SSU_ONETOKEN_CTAS
+                                      : (kSmemPerSm / 3 - 1024) / kStageBytes >= 4 ? 3
+                                      : (kSmemPerSm / 2 - 1024) / kStageBytes >= 3 ? 2
+                                                                                   : 1;
+    static constexpr int kRingBytes = kSmemPerSm / kCtasPerSm - 1024;
     static constexpr int kStages = (kRingBytes / kStageBytes) < 6 ? (kRingBytes / kStageBytes) : 6;
     static constexpr int kBarOffset = kStages * kStageBytes;
     static constexpr int kBytes = kBarOffset + kStages * 16;
@@ -71,6 +79,12 @@ struct OnetokenPipe {
     static constexpr int kProducerWarps = SSU_PRODUCER_WARPS;
     static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
     static_assert(kStages >= 2, "state tile too large for a pipelined ring");
+    // A producer waits for stage s to be free by the parity of the "empty"
+    // phase it needs.  When it starts unit k it has finished its previous unit
+    // k - kProducerWarps, whose wait guaranteed that every unit up to
+    // k - kProducerWarps - kStages had been released; the parity test is
+    // unambiguous once unit k - 2 kStages is released, hence this bound.
+    static_assert(kProducerWarps <= kStages, "more producer warps than stages breaks the parity waits");
 };
 
 // Per-stage header written by the producer.
