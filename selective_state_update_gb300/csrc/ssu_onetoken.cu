@@ -67,7 +67,10 @@ struct OnetokenPipe {
     // each CTA reserves).  Small (16-bit) stages: three CTAs of four stages,
     // so three consumer groups share the SM; fp32 stages: two CTAs of three.
     static constexpr int kSmemPerSm = 222 * 1024;
-    static constexpr int kCtasPerSm = SSU_ONETOKEN_CTAS > 0                 ? SSU_ONETOKEN_CTAS
+    static constexpr int kCtasPerSm = (SSU_ONETOKEN_CTAS > 0 &&
+                                       (kSmemPerSm / (SSU_ONETOKEN_CTAS > 0 ? SSU_ONETOKEN_CTAS : 1) - 1024) /
+                                               kStageBytes >= 2)
+                                          ? SSU_ONETOKEN_CTAS
                                       : (kSmemPerSm / 3 - 1024) / kStageBytes >= 4 ? 3
                                       : (kSmemPerSm / 2 - 1024) / kStageBytes >= 3 ? 2
                                                                                    : 1;
