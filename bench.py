@@ -145,6 +145,28 @@ def hbm_peak():
 
 
 # --------------------------------------------------------------------------
+# Several GPUs: independent replicas (each rank owns its own pool and batch;
+# sequences never cross ranks, so there is no data exchange).  Timing takes
+# the slowest rank; throughput counts the work of all ranks.
+# --------------------------------------------------------------------------
+def max_over_ranks(value: float, device) -> float:
+    """Largest `value` over the ranks of the default process group (the value
+    itself without one)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(units_per_rank: int, world: int, steps: int, slowest_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the time of
+    the slowest rank."""
+    return units_per_rank * world * steps / (slowest_ms * 1e-3)
+
+
+# --------------------------------------------------------------------------
 # Clocks sampled while the timed region runs.
 # --------------------------------------------------------------------------
 class ClockSampler:
@@ -265,10 +287,7 @@ def run_ours(args, rank, world, device):
         torch.distributed.barrier()
     total_ms = whole0.elapsed_time(whole1)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, device)
 
     # End to end through the public call: per step, pinned host -> device
     # copies of the step's inputs, the update, and y back to pinned host.
@@ -294,17 +313,14 @@ def run_ours(args, rank, world, device):
         host_y.copy_(out, non_blocking=True)
     torch.cuda.synchronize()
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, device)
 
     peak, peak_src = hbm_peak()
     achieved = acct["total"] / (launch_ms * 1e-3) / 1e9
     kind = w.kind
     result = {
         "metric": METRIC,
-        "value": tokens * world * args.steps / (total_ms * 1e-3),
+        "value": aggregate_rate(tokens, world, args.steps, total_ms),
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -328,7 +344,7 @@ def run_ours(args, rank, world, device):
                      "traffic": profiled_traffic(kind, args.workload),
                      "algorithmic_bytes_per_launch": acct["total"],
                      "kernel": f"ssu_{kind}_kernel", "launch_ms": launch_ms},
-        "e2e": {"value": tokens * world * e2e_steps / e2e_s, "unit": UNIT,
+        "e2e": {"value": aggregate_rate(tokens, world, e2e_steps, e2e_s * 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
@@ -392,8 +408,8 @@ def make_workload(args, device, seed_offset=0):
     gen = workloads.NAMED[args.workload]
     kw = {}
     if args.batch is not None:
-        if args.workload != "b256_fp32":
-            raise SystemExit("--batch applies to the b256_fp32 workload only")
+        if args.workload not in ("b256_fp32", "mtp_64x7_fp32"):
+            raise SystemExit("--batch applies to the b256_fp32 and mtp_64x7_fp32 workloads only")
         kw["batch"] = args.batch
     return gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
 
@@ -470,7 +486,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(workloads.NAMED), default="b256_fp32")
     ap.add_argument("--batch", type=int, default=None,
-                    help="b256_fp32 at another batch size (profiling captures)")
+                    help="b256_fp32 / mtp_64x7_fp32 with another number of sequences (profiling captures)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

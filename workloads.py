@@ -167,8 +167,11 @@ def b1024_bf16(device="cpu", seed=1003) -> Workload:
                     dst=ident.clone(), pad_slot_id=-1, **inp)
 
 
-def mtp_64x7_fp32(device="cpu", seed=1004) -> Workload:
-    heads, dim, dstate, groups, slots, nseq, steps = 128, 64, 128, 8, 1024, 64, 7
+def mtp_64x7_fp32(device="cpu", seed=1004, batch=64) -> Workload:
+    """``batch`` other than 64 gives the same workload with another number of
+    sequences (pool of 16 * batch slots); profiling uses it for small captures."""
+    heads, dim, dstate, groups, steps = 128, 64, 128, 8, 7
+    nseq, slots = batch, 16 * batch
     rows = nseq * steps
     g = _gen(seed, device)
     inp = _decode_inputs(g, device, rows, heads, dim, dstate, groups, torch.bfloat16)
