@@ -26,7 +26,7 @@ constexpr int kRowSlots = kTileRows / kRowsPerThread;
 #define SSU_ONETOKEN_UNROLL 2
 #endif
 #ifndef SSU_PACKED_UNROLL
-#define SSU_PACKED_UNROLL 1
+#define SSU_PACKED_UNROLL 2
 #endif
 constexpr int kOnetokenUnroll = SSU_ONETOKEN_UNROLL;
 constexpr int kPackedUnroll = SSU_PACKED_UNROLL;

@@ -419,8 +419,19 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
     if (tid == 0) bulk_wait_all();
 }
 
+// Register budget of the kernel (the min-CTAs launch bound): for 16-bit pools
+// the CTAs per SM the ring allows (three); for fp32 pools the budget of up to
+// four CTAs but never under 80 registers a thread, which measured faster than
+// the larger allocation two CTAs would permit.
 template <typename TS, int L>
-__global__ void __launch_bounds__(OnetokenPipe<TS, L>::kThreads)
+constexpr int onetoken_min_ctas() {
+    constexpr int threads = OnetokenPipe<TS, L>::kThreads;
+    constexpr int by_regs = 65536 / (threads * 80);
+    return sizeof(TS) != 4 ? OnetokenPipe<TS, L>::kCtasPerSm : (by_regs < 1 ? 1 : (by_regs > 4 ? 4 : by_regs));
+}
+
+template <typename TS, int L>
+__global__ void __launch_bounds__(OnetokenPipe<TS, L>::kThreads, (onetoken_min_ctas<TS, L>()))
     ssu_onetoken_kernel(const KParams p, int64_t units) {
     using PS = OnetokenPipe<TS, L>;
     extern __shared__ __align__(128) unsigned char smem[];

@@ -166,8 +166,17 @@ __device__ __forceinline__ void token_rows(const KParams &p, int64_t r, int h, i
     }
 }
 
+// CTAs per SM that the shared memory of one CTA allows (228 KB per SM, 1 KB
+// of it reserved per CTA), at most 8: the register allocation is held to
+// what that many resident CTAs can share.
 template <typename TS, int L>
-__global__ void __launch_bounds__(Tile<TS, L>::kThreads)
+constexpr int packed_min_ctas() {
+    constexpr int fit = (228 * 1024) / (PackedSmem<TS, L>::kBytes + 1024);
+    return fit < 1 ? 1 : (fit > 8 ? 8 : fit);
+}
+
+template <typename TS, int L>
+__global__ void __launch_bounds__(Tile<TS, L>::kThreads, (packed_min_ctas<TS, L>()))
     ssu_packed_kernel(const KParams p) {
     using T = Tile<TS, L>;
     using SM = PackedSmem<TS, L>;
