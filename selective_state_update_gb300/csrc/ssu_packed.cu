@@ -14,9 +14,9 @@
 // as fp32 across the sequence's tokens (each thread only ever touches its own
 // elements), so it is read from HBM once and written once per token, with
 // 16-byte streaming stores.  Each token's B, C and per-row scalars {dA,
-// dt' x, x, z} are loaded while the previous token computes and staged in
-// shared memory (double-buffered, one barrier per token); every row's
-// scalars are computed once, by one thread.
+// dt' x, x, gate} are loaded two tokens ahead and staged in shared memory
+// (double-buffered, one barrier per token); every row's scalars are computed
+// once, by one thread.
 #include "ssu_device.cuh"
 
 namespace ssu {
@@ -247,9 +247,13 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads, (packed_min_ctas<TS, L>
     const float Ah = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
     const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
-    TokenOperands<N, NT> ops;
-    ops.load(p, start, g, h, row0, rows_here);
-    ops.stage(p, sB, sC, rowq, rows_here, Ah, bias);
+    // Two operand sets in turn: the operands of token t + 2 are loaded while
+    // token t computes and staged at the end of token t + 1, so their loads
+    // have two tokens' time to arrive.
+    TokenOperands<N, NT> ops0, ops1;
+    ops0.load(p, start, g, h, row0, rows_here);
+    ops0.stage(p, sB, sC, rowq, rows_here, Ah, bias);
+    if (len > 1) ops1.load(p, start + 1, g, h, row0, rows_here);
     __syncthreads();
     int timed_out = 0;
     if (seeded && !mbar_wait_bounded(bar, 0)) timed_out = 1;
@@ -258,12 +262,10 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads, (packed_min_ctas<TS, L>
         return;
     }
 
-    for (int64_t t = 0; t < len; ++t) {
+    // Token t reads staging buffers t & 1; the staging of token t + 1 goes to
+    // the other buffers, last read before the previous barrier.
+    auto token = [&](int64_t t, int buf) {
         const int64_t r = start + t;
-        const int buf = static_cast<int>(t & 1);
-        const bool more = t + 1 < len;
-        if (more) ops.load(p, r + 1, g, h, row0, rows_here);  // in flight during this token
-
         int64_t ws;
         table_slot(p, wt, b, t, start, b, &ws);
         TS *dst = (!p.disable && ws != p.pad)
@@ -278,8 +280,16 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads, (packed_min_ctas<TS, L>
         else
             token_rows<TS, L, false>(p, r, h, row0, rows_here, slot_row, lane, seed, seeded, carry, dst, bv, cv,
                                      rowq + buf * kTileRows, Dh);
-        // The other buffers were last read before the previous barrier.
-        if (more) ops.stage(p, sB + (buf ^ 1) * N, sC + (buf ^ 1) * N, rowq + (buf ^ 1) * kTileRows, rows_here, Ah, bias);
+    };
+    for (int64_t t = 0; t < len; t += 2) {
+        if (t + 2 < len) ops0.load(p, start + t + 2, g, h, row0, rows_here);
+        token(t, 0);
+        if (t + 1 < len) ops1.stage(p, sB + N, sC + N, rowq + kTileRows, rows_here, Ah, bias);
+        __syncthreads();
+        if (t + 1 >= len) break;
+        if (t + 3 < len) ops1.load(p, start + t + 3, g, h, row0, rows_here);
+        token(t + 1, 1);
+        if (t + 2 < len) ops0.stage(p, sB, sC, rowq, rows_here, Ah, bias);
         __syncthreads();
     }
 }
