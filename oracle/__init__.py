@@ -85,6 +85,24 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _ReplayProblem(ctypes.Structure):
+    _fields_ = [
+        ("slots", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("groups", ctypes.c_int64),
+        ("state_dtype", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32),
+        ("dt_per_head", ctypes.c_int32),
+        ("ckpt_in", ctypes.c_void_p), ("ckpt_out", ctypes.c_void_p),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("B", ctypes.c_void_p),
+        ("C", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("y_exact", ctypes.c_void_p),
+        ("dt_softplus", ctypes.c_int32), ("pad_slot_id", ctypes.c_int64), ("batch", ctypes.c_int64),
+        ("slot_of", ctypes.c_void_p), ("len", ctypes.c_int64),
+        ("xbuf", ctypes.c_void_p), ("dtbuf", ctypes.c_void_p), ("Bbuf", ctypes.c_void_p),
+        ("count_in", ctypes.c_void_p), ("count_out", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -93,6 +111,8 @@ def load_library(path: str):
     lib = ctypes.CDLL(path)
     lib.orc_ssu_run.argtypes = [ctypes.POINTER(_Problem), ctypes.c_char_p, ctypes.c_int]
     lib.orc_ssu_run.restype = ctypes.c_int
+    lib.orc_replay_run.argtypes = [ctypes.POINTER(_ReplayProblem), ctypes.c_char_p, ctypes.c_int]
+    lib.orc_replay_run.restype = ctypes.c_int
     lib.orc_softplus.argtypes = [ctypes.c_double]
     lib.orc_softplus.restype = ctypes.c_double
     lib.orc_silu.argtypes = [ctypes.c_double]
@@ -236,3 +256,59 @@ def ssu(state: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor,
     if rc != OK:
         raise OracleError(rc, err.value.decode())
     return Result(state=state_out, y=y, y_exact=y_exact, touched=touched)
+
+
+@dataclass
+class ReplayResult:
+    ckpt: torch.Tensor         # checkpoints after the call
+    y: torch.Tensor            # [batch, heads, dim] io dtype
+    y_exact: torch.Tensor      # float64 before rounding
+    xbuf: torch.Tensor         # buffers after the call
+    dtbuf: torch.Tensor
+    Bbuf: torch.Tensor
+    count: torch.Tensor        # [batch] int64 entries buffered after the call
+
+
+def replay(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+           C: torch.Tensor, xbuf: torch.Tensor, dtbuf: torch.Tensor, Bbuf: torch.Tensor,
+           count: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+           dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
+           slot_of: Optional[torch.Tensor] = None, pad_slot_id: int = -1, lib=None) -> ReplayResult:
+    """One ReplaySSM decode step (one token per sequence) on the host.
+
+    ckpt ``[slots, heads, dim, dstate]``; xbuf ``[slots, L, heads, dim]`` (x's dtype);
+    dtbuf ``[slots, L, heads, dim]`` fp32; Bbuf ``[slots, L, groups, dstate]`` (x's dtype);
+    count ``[batch]`` entries buffered per sequence.  Inputs are not modified."""
+    lib = lib or _load()
+    c_in = _cpu(ckpt)
+    slots, heads, dim, dstate = c_in.shape
+    batch = x.shape[0]
+    groups = B.shape[1]
+    L = xbuf.shape[1]
+    c_out = c_in.clone()
+    xs, dts, Bs, Cs, zs = _cpu(x), _cpu(dt), _cpu(B), _cpu(C), _cpu(z)
+    As = _cpu(A).to(torch.float32)
+    Ds = None if D is None else _cpu(D).to(torch.float32)
+    bs = None if dt_bias is None else _cpu(dt_bias).to(torch.float32)
+    xb, db, Bb = _cpu(xbuf).clone(), _cpu(dtbuf).to(torch.float32).clone(), _cpu(Bbuf).clone()
+    cin = _cpu(count).to(torch.int64)
+    cout = torch.zeros(batch, dtype=torch.int64)
+    so = None if slot_of is None else _cpu(slot_of).to(torch.int64)
+    y = torch.empty((batch, heads, dim), dtype=x.dtype)
+    y_exact = torch.empty((batch, heads, dim), dtype=torch.float64)
+    if Bs.dtype != xs.dtype or Cs.dtype != xs.dtype or xb.dtype != xs.dtype or Bb.dtype != xs.dtype:
+        raise ValueError("B, C and the x / B buffers must have the io dtype")
+    pr = _ReplayProblem(
+        slots=slots, heads=heads, dim=dim, dstate=dstate, groups=groups,
+        state_dtype=_DTYPE_CODE[c_in.dtype], io_dtype=_DTYPE_CODE[xs.dtype], dt_dtype=_DTYPE_CODE[dts.dtype],
+        dt_per_head=int(dts.dim() == 2), ckpt_in=c_in.data_ptr(), ckpt_out=c_out.data_ptr(),
+        x=xs.data_ptr(), dt=dts.data_ptr(), B=Bs.data_ptr(), C=Cs.data_ptr(), z=_ptr(zs),
+        A=As.data_ptr(), D=_ptr(Ds), dt_bias=_ptr(bs), y=y.data_ptr(), y_exact=y_exact.data_ptr(),
+        dt_softplus=int(bool(dt_softplus)), pad_slot_id=int(pad_slot_id), batch=batch,
+        slot_of=_ptr(so), len=L, xbuf=xb.data_ptr(), dtbuf=db.data_ptr(), Bbuf=Bb.data_ptr(),
+        count_in=cin.data_ptr(), count_out=cout.data_ptr())
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_replay_run(ctypes.byref(pr), err, 512)
+    if rc != OK:
+        raise OracleError(rc, err.value.decode())
+    return ReplayResult(ckpt=c_out, y=y, y_exact=y_exact, xbuf=xb, dtbuf=db, Bbuf=Bb, count=cout)

@@ -391,3 +391,153 @@ int orc_ssu_run(const orc_problem *pr, char *err, int errlen)
     free(start); free(seed); free(wslot); free(writer);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* ReplaySSM decode step (article "ReplaySSM: Cache SSM Inputs, Not State", */
+/* section 核心做法): the state of a slot is a checkpoint S_ckpt plus the     */
+/* inputs (v, Delta, k) = (x, dt', B) of the c steps since the last fold.    */
+/* Each call appends the current token's inputs as entry c.  While the      */
+/* buffer is not full (c + 1 < L) y is read out of checkpoint and buffer     */
+/* without forming the state (the unrolled recurrence):                      */
+/*   y = gamma_{0:c} (S_ckpt . q) + sum_j gamma_{j+1:c} Delta_j v_j (k_j . q) */
+/* with gamma_{i:c} = prod_{m=i..c} exp(A Delta_m), q = C, plus D x and the  */
+/* silu gate, and nothing but the new entry is written.  When it is full     */
+/* (c + 1 = L) the buffer is folded into the checkpoint step by step, the    */
+/* state is written back once, y is read out of it, and the buffer empties. */
+/* Readings: on a fold step y comes from the folded state (so that L = 1 is  */
+/* the plain update, as the article states); a pad slot has no history:     */
+/* zero state, the current token only, nothing written, count 0.            */
+/* ------------------------------------------------------------------------ */
+int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
+{
+    const int64_t H = pr->heads, P = pr->dim, N = pr->dstate, G = pr->groups, Lb = pr->len;
+    if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0 || Lb < 1) {
+        set_err(err, errlen, "bad shape: heads=%lld len=%lld", H, Lb);
+        return ORC_INVALID;
+    }
+    const int64_t heads_per_group = H / G;
+    int64_t *owner = malloc(sizeof(int64_t) * (size_t)pr->slots);
+    double *S = malloc(sizeof(double) * (size_t)N);
+    if (!owner || !S) {
+        free(owner); free(S);
+        return ORC_INVALID;
+    }
+    for (int64_t s = 0; s < pr->slots; ++s)
+        owner[s] = -1;
+    int rc = ORC_OK;
+    for (int64_t b = 0; b < pr->batch && rc == ORC_OK; ++b) {
+        const int64_t slot = pr->slot_of ? pr->slot_of[b] : b;
+        if (slot == pr->pad_slot_id)
+            continue;
+        if (slot < 0 || slot >= pr->slots) {
+            set_err(err, errlen, "slot %lld of sequence %lld out of range", slot, b);
+            rc = ORC_INVALID;
+        } else if (owner[slot] != -1) {
+            set_err(err, errlen, "slot %lld is used by two sequences (second: %lld)", slot, b);
+            rc = ORC_ALIASING;
+        } else if (pr->count_in[b] < 0 || pr->count_in[b] >= Lb) {
+            set_err(err, errlen, "buffered count %lld of sequence %lld not in [0, L)", pr->count_in[b], b);
+            rc = ORC_INVALID;
+        } else {
+            owner[slot] = b;
+        }
+    }
+    if (rc != ORC_OK) {
+        free(owner); free(S);
+        return rc;
+    }
+    for (int64_t b = 0; b < pr->batch; ++b) {
+        const int64_t slot = pr->slot_of ? pr->slot_of[b] : b;
+        const int pad = slot == pr->pad_slot_id;
+        const int64_t c = pad ? 0 : pr->count_in[b];
+        const int fold = pad || c + 1 == Lb;
+        pr->count_out[b] = (pad || fold) ? 0 : c + 1;
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t g = h / heads_per_group;
+            const double A = (double)pr->A[h];
+            const double Dh = pr->D ? (double)pr->D[h] : 0.0;
+            const double bias = pr->dt_bias ? (double)pr->dt_bias[h] : 0.0;
+            const int64_t bc_now = (b * G + g) * N;
+            for (int64_t p = 0; p < P; ++p) {
+                const int64_t xi = (b * H + h) * P + p;
+                const int64_t dti = pr->dt_per_head ? (b * H + h) : xi;
+                double d = load_elem(pr->dt, dti, pr->dt_dtype) + bias;
+                if (pr->dt_softplus)
+                    d = orc_softplus(d);
+                const double xv = load_elem(pr->x, xi, pr->io_dtype);
+                double y;
+                if (fold) {
+                    /* S_ckpt, then each buffered step, then the current one. */
+                    for (int64_t n = 0; n < N; ++n)
+                        S[n] = pad ? 0.0
+                                   : load_elem(pr->ckpt_in, ((slot * H + h) * P + p) * N + n, pr->state_dtype);
+                    for (int64_t j = 0; j < c; ++j) {
+                        const int64_t e = ((slot * Lb + j) * H + h) * P + p;
+                        const double dj = (double)pr->dtbuf[e];
+                        const double xj = load_elem(pr->xbuf, e, pr->io_dtype);
+                        const double aj = exp(A * dj);
+                        const int64_t be = ((slot * Lb + j) * G + g) * N;
+                        for (int64_t n = 0; n < N; ++n)
+                            S[n] = S[n] * aj + dj * xj * load_elem(pr->Bbuf, be + n, pr->io_dtype);
+                    }
+                    const double a = exp(A * d);
+                    y = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        S[n] = S[n] * a + d * xv * load_elem(pr->B, bc_now + n, pr->io_dtype);
+                        y += S[n] * load_elem(pr->C, bc_now + n, pr->io_dtype);
+                    }
+                    if (!pad)
+                        for (int64_t n = 0; n < N; ++n)
+                            store_elem(pr->ckpt_out, ((slot * H + h) * P + p) * N + n, pr->state_dtype, S[n]);
+                } else {
+                    /* Output from checkpoint and buffer: walk the entries from
+                     * the newest (the current token, entry c) to the oldest,
+                     * w = gamma_{j+1:c}; after the walk w = gamma_{0:c}. */
+                    double w = 1.0, hist = 0.0, kq;
+                    kq = 0.0;
+                    for (int64_t n = 0; n < N; ++n)
+                        kq += load_elem(pr->B, bc_now + n, pr->io_dtype) * load_elem(pr->C, bc_now + n, pr->io_dtype);
+                    hist += w * d * xv * kq;
+                    w *= exp(A * d);
+                    for (int64_t j = c - 1; j >= 0; --j) {
+                        const int64_t e = ((slot * Lb + j) * H + h) * P + p;
+                        const double dj = (double)pr->dtbuf[e];
+                        const double xj = load_elem(pr->xbuf, e, pr->io_dtype);
+                        const int64_t be = ((slot * Lb + j) * G + g) * N;
+                        kq = 0.0;
+                        for (int64_t n = 0; n < N; ++n)
+                            kq += load_elem(pr->Bbuf, be + n, pr->io_dtype) * load_elem(pr->C, bc_now + n, pr->io_dtype);
+                        hist += w * dj * xj * kq;
+                        w *= exp(A * dj);
+                    }
+                    double sq = 0.0;
+                    for (int64_t n = 0; n < N; ++n)
+                        sq += load_elem(pr->ckpt_in, ((slot * H + h) * P + p) * N + n, pr->state_dtype) *
+                              load_elem(pr->C, bc_now + n, pr->io_dtype);
+                    y = w * sq + hist;
+                    /* Append the current token as entry c (v and k keep their
+                     * bits; the processed step is stored in fp32). */
+                    const int64_t e = ((slot * Lb + c) * H + h) * P + p;
+                    memcpy((char *)pr->xbuf + e * (pr->io_dtype == ORC_F32 ? 4 : 2),
+                           (const char *)pr->x + xi * (pr->io_dtype == ORC_F32 ? 4 : 2),
+                           pr->io_dtype == ORC_F32 ? 4 : 2);
+                    pr->dtbuf[e] = (float)d;
+                    if (h % heads_per_group == 0 && p == 0) {
+                        const int64_t be = ((slot * Lb + c) * G + g) * N;
+                        const size_t es = pr->io_dtype == ORC_F32 ? 4 : 2;
+                        memcpy((char *)pr->Bbuf + be * es, (const char *)pr->B + bc_now * es, es * (size_t)N);
+                    }
+                }
+                y += Dh * xv;
+                if (pr->z != NULL)
+                    y *= orc_silu(load_elem(pr->z, xi, pr->io_dtype));
+                if (pr->y_exact != NULL)
+                    pr->y_exact[xi] = y;
+                store_elem(pr->y, xi, pr->io_dtype, y);
+            }
+        }
+    }
+    free(owner);
+    free(S);
+    return ORC_OK;
+}

@@ -50,6 +50,33 @@ typedef struct {
 
 int orc_ssu_run(const orc_problem *problem, char *err, int errlen);
 
+/* One decode token per sequence with the state kept as a checkpoint plus a
+ * buffer of the inputs of the steps since the last fold (article "ReplaySSM:
+ * Cache SSM Inputs, Not State", section 核心做法).  All arrays contiguous. */
+typedef struct {
+    int64_t slots, heads, dim, dstate, groups;
+    int32_t state_dtype, io_dtype, dt_dtype;
+    int32_t dt_per_head;
+    const void *ckpt_in;            /* [slots, heads, dim, dstate] checkpoints, read only        */
+    void *ckpt_out;                 /* same shape; caller fills it with ckpt_in first            */
+    const void *x, *dt, *B, *C, *z; /* current token: x, z [batch, heads, dim]; B, C [batch, groups, dstate] */
+    const float *A, *D, *dt_bias;
+    void *y;                        /* [batch, heads, dim] io dtype                               */
+    double *y_exact;                /* [batch, heads, dim] or NULL                                */
+    int32_t dt_softplus;
+    int64_t pad_slot_id;
+    int64_t batch;
+    const int64_t *slot_of;         /* [batch] slot of each sequence; NULL: slot b                */
+    int64_t len;                    /* buffer length L >= 1                                       */
+    void *xbuf;                     /* [slots, L, heads, dim] io dtype, in/out                    */
+    float *dtbuf;                   /* [slots, L, heads, dim] fp32 processed steps, in/out         */
+    void *Bbuf;                     /* [slots, L, groups, dstate] io dtype, in/out                */
+    const int64_t *count_in;        /* [batch] entries buffered before the call (0 <= c < L)      */
+    int64_t *count_out;             /* [batch] entries buffered after the call                    */
+} orc_replay_problem;
+
+int orc_replay_run(const orc_replay_problem *problem, char *err, int errlen);
+
 double orc_softplus(double v);
 double orc_silu(double z);
 double orc_decode(uint32_t bits, int dtype);

@@ -587,7 +587,147 @@ def pin_bounded_decay(lib):
             raise AssertionError("decay bound violated")
 
 
+# --------------------------------------------------------------------------
+# ReplaySSM decode step (article "ReplaySSM: Cache SSM Inputs, Not State",
+# section 核心做法): checkpoint + buffer of the inputs since the last fold.
+# --------------------------------------------------------------------------
+def _replay_scenario(seed, L, counts, heads=4, dim=3, dstate=8, groups=2, io=torch.bfloat16,
+                     state_dtype=torch.float64, with_z=True, pad_last=False):
+    """Sequences b with counts[b] buffered steps each, built from explicit
+    token histories; returns the replay inputs and, per sequence, the plain
+    token-by-token history to compare with."""
+    g = torch.Generator().manual_seed(seed)
+    nseq = len(counts)
+    slots = 2 * nseq + 3
+    slot_of = torch.randperm(slots, generator=g)[:nseq]
+    if pad_last:
+        slot_of[-1] = -1
+    ckpt = (torch.randn((slots, heads, dim, dstate), generator=g, dtype=torch.float64) * 0.5).to(state_dtype)
+    xbuf = torch.randn((slots, L, heads, dim), generator=g).to(io)
+    dtbuf = torch.rand((slots, L, heads, dim), generator=g) * 0.3
+    Bbuf = torch.randn((slots, L, groups, dstate), generator=g).to(io)
+    x = torch.randn((nseq, heads, dim), generator=g).to(io)
+    dt = torch.rand((nseq, heads, dim), generator=g) * 0.3
+    B = torch.randn((nseq, groups, dstate), generator=g).to(io)
+    C = torch.randn((nseq, groups, dstate), generator=g).to(io)
+    z = torch.randn((nseq, heads, dim), generator=g).to(io) if with_z else None
+    A = -torch.exp(torch.rand(heads, generator=g) * 2.0)
+    D = torch.randn(heads, generator=g)
+    count = torch.tensor(counts, dtype=torch.int64)
+    return dict(ckpt=ckpt, x=x, dt=dt, A=A, B=B, C=C, xbuf=xbuf, dtbuf=dtbuf, Bbuf=Bbuf, count=count,
+                D=D, z=z, slot_of=slot_of)
+
+
+def _plain_history(sc, b, lib):
+    """The same sequence run token by token by the plain update: buffered
+    entries first (their processed steps as dt, softplus off), then the
+    current token; all tokens publish to the sequence's slot."""
+    s = int(sc["slot_of"][b])
+    c = int(sc["count"][b])
+    xs = torch.cat([sc["xbuf"][s, :c], sc["x"][b:b + 1]])
+    dts = torch.cat([sc["dtbuf"][s, :c], sc["dt"][b:b + 1]])
+    Bs = torch.cat([sc["Bbuf"][s, :c], sc["B"][b:b + 1]])
+    Cs = torch.cat([sc["C"][b:b + 1].expand(c, -1, -1), sc["C"][b:b + 1]])
+    zs = None if sc["z"] is None else torch.cat([sc["z"][b:b + 1].expand(c, -1, -1), sc["z"][b:b + 1]])
+    tab = torch.full((1, c + 1), s, dtype=torch.int64)
+    return oracle.ssu(sc["ckpt"], xs, dts, sc["A"], Bs, Cs, D=sc["D"], z=zs, read=oracle.Table.of(tab),
+                      cu_seqlens=torch.tensor([0, c + 1]), lib=lib)
+
+
+def _run_replay(sc, lib, **kw):
+    return oracle.replay(sc["ckpt"], sc["x"], sc["dt"], sc["A"], sc["B"], sc["C"], sc["xbuf"], sc["dtbuf"],
+                         sc["Bbuf"], sc["count"], D=sc["D"], z=sc["z"], slot_of=sc["slot_of"], lib=lib, **kw)
+
+
+def pin_replay_lossless(lib):
+    """The method is lossless: y from checkpoint + buffer equals the plain
+    recurrence run over the buffered steps and the current one, and a fold
+    leaves in the checkpoint the state the plain recurrence reaches."""
+    L = 5
+    counts = [0, 1, 2, 3, 4, 4, 2]
+    sc = _replay_scenario(41, L, counts)
+    r = _run_replay(sc, lib)
+    for b, c in enumerate(counts):
+        h = _plain_history(sc, b, lib)
+        _close(r.y_exact[b].numpy(), h.y_exact[c].numpy(), rtol=1e-11, atol=1e-12, what=f"replay y (c={c})")
+        s = int(sc["slot_of"][b])
+        if c + 1 == L:
+            _close(f64(r.ckpt[s]), f64(h.state[s]), rtol=1e-11, atol=1e-13, what="folded checkpoint")
+            if int(r.count[b]) != 0:
+                raise AssertionError("a fold must empty the buffer")
+        else:
+            if not torch.equal(r.ckpt[s], sc["ckpt"][s]):
+                raise AssertionError("a step that does not fold must not write the checkpoint")
+            if int(r.count[b]) != c + 1:
+                raise AssertionError("a step that does not fold buffers one more entry")
+
+
+def pin_replay_buffer_entries(lib):
+    """A step that does not fold appends the current token as entry c: x and
+    B with their bits, the processed step dt' (softplus(dt + bias)) in fp32;
+    older entries and other slots are untouched."""
+    L = 4
+    counts = [0, 2, 1]
+    sc = _replay_scenario(42, L, counts)
+    bias = torch.full((sc["x"].shape[1],), -0.5)
+    r = _run_replay(sc, lib, dt_bias=bias, dt_softplus=True)
+    groups = sc["B"].shape[1]
+    for b, c in enumerate(counts):
+        s = int(sc["slot_of"][b])
+        if not torch.equal(r.xbuf[s, c], sc["x"][b]):
+            raise AssertionError("appended x")
+        if not torch.equal(r.Bbuf[s, c], sc["B"][b]):
+            raise AssertionError("appended B")
+        d = np.logaddexp(0.0, f64(sc["dt"][b]) + f64(bias)[:, None])
+        _close(r.dtbuf[s, c].double().numpy(), d, rtol=1e-7, atol=1e-9, what="appended processed step")
+        if not (torch.equal(r.xbuf[s, :c], sc["xbuf"][s, :c]) and torch.equal(r.dtbuf[s, :c], sc["dtbuf"][s, :c])):
+            raise AssertionError("older entries changed")
+        assert groups == r.Bbuf.shape[2]
+    used = set(int(v) for v in sc["slot_of"])
+    for s in range(sc["ckpt"].shape[0]):
+        if s not in used and not (torch.equal(r.xbuf[s], sc["xbuf"][s]) and torch.equal(r.ckpt[s], sc["ckpt"][s])):
+            raise AssertionError("a slot no sequence uses changed")
+
+
+def pin_replay_buffer_len_one(lib):
+    """L = 1: the buffer is always empty, every step folds, and the step is
+    the plain update (the article's bit-for-bit anchor)."""
+    sc = _replay_scenario(43, 1, [0, 0, 0], state_dtype=torch.float32)
+    bias = torch.full((sc["x"].shape[1],), -1.0)
+    r = _run_replay(sc, lib, dt_bias=bias, dt_softplus=True)
+    plain = oracle.ssu(sc["ckpt"], sc["x"], sc["dt"], sc["A"], sc["B"], sc["C"], D=sc["D"], z=sc["z"],
+                       dt_bias=bias, dt_softplus=True, read=oracle.Table.of(sc["slot_of"]), lib=lib)
+    if not (torch.equal(r.y_exact, plain.y_exact) and torch.equal(r.ckpt, plain.state)):
+        raise AssertionError("L = 1 differs from the plain update")
+    if torch.any(r.count != 0):
+        raise AssertionError("L = 1 leaves entries in the buffer")
+
+
+def pin_replay_pad_and_aliasing(lib):
+    """A pad slot has no history: y is the zero-state closed form and nothing
+    is written; two sequences on one slot are refused."""
+    sc = _replay_scenario(44, 3, [1, 2], with_z=False, pad_last=True)
+    r = _run_replay(sc, lib)
+    b = 1
+    gi = np.arange(sc["x"].shape[1]) // (sc["x"].shape[1] // sc["B"].shape[1])
+    d, xn = f64(sc["dt"][b]), f64(sc["x"][b])
+    bc = np.einsum("hn,hn->h", f64(sc["B"][b])[gi], f64(sc["C"][b])[gi])
+    _close(r.y_exact[b].numpy(), d * bc[:, None] * xn + f64(sc["D"])[:, None] * xn, what="pad replay y")
+    if not torch.equal(r.ckpt, sc["ckpt"]) or int(r.count[b]) != 0:
+        raise AssertionError("pad bookkeeping: nothing is written and no entry is kept")
+    sc2 = _replay_scenario(45, 3, [1, 1])
+    sc2["slot_of"][1] = sc2["slot_of"][0]
+    try:
+        _run_replay(sc2, lib)
+        raise AssertionError("two sequences on one slot accepted")
+    except oracle.OracleError as e:
+        if e.code != oracle.ALIASING:
+            raise
+
+
 ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero, pin_zero_state,
             pin_A_zero, pin_decay_only, pin_unrolled, pin_basis_vectors, pin_group_map,
             pin_page_examples, pin_pad_never_written, pin_disable_and_untouched, pin_table_forms,
-            pin_seed_position, pin_seed_position_per_row, pin_per_head_dt, pin_aliasing_refused, pin_empty_sequences, pin_bounded_decay]
+            pin_seed_position, pin_seed_position_per_row, pin_per_head_dt, pin_aliasing_refused,
+            pin_replay_lossless, pin_replay_buffer_entries, pin_replay_buffer_len_one,
+            pin_replay_pad_and_aliasing, pin_empty_sequences, pin_bounded_decay]

@@ -35,6 +35,15 @@ MUTATIONS = [
      "if (resolve(wtab, b, 0, start[b], &w) != 0)"),
     ("bf16_truncates", "double r = round_to_format(v, 7, -126, 127);", "double r = trunc(v * 128.0) / 128.0;"),
     ("pad_reads_state", "S[n] = (seed[b] == pr->pad_slot_id)", "S[n] = (seed[b] < 0)"),
+    ("replay_gamma_skips_current", "hist += w * d * xv * kq;\n                    w *= exp(A * d);",
+     "hist += w * d * xv * kq;"),
+    ("replay_fold_skips_buffer", "for (int64_t j = 0; j < c; ++j) {", "for (int64_t j = 0; j < 0; ++j) {"),
+    ("replay_append_position", "const int64_t e = ((slot * Lb + c) * H + h) * P + p;",
+     "const int64_t e = ((slot * Lb + c + 1) * H + h) * P + p;"),
+    ("replay_count_not_reset", "pr->count_out[b] = (pad || fold) ? 0 : c + 1;",
+     "pr->count_out[b] = pad ? 0 : c + 1;"),
+    ("replay_decay_before_term", "hist += w * dj * xj * kq;\n                        w *= exp(A * dj);",
+     "w *= exp(A * dj);\n                        hist += w * dj * xj * kq;"),
     ("dt_per_head_wrong_head", "const int64_t dti = pr->dt_per_head ? (r * H + h) : xi;",
      "const int64_t dti = pr->dt_per_head ? (r * H) : xi;"),
 ]
