@@ -91,6 +91,7 @@ typedef struct ssu_slot_table {
 #define SSU_DEV_BAD_SEQLEN 0x4  /* cu_seqlens decreasing, negative or past `rows`   */
 #define SSU_DEV_TIMEOUT    0x8  /* an asynchronous state copy did not complete in
                                    about a second; the unit was skipped           */
+#define SSU_DEV_BAD_COUNT  0x10 /* ssu_replay_update: a buffered count outside [0, L) */
 
 /* Arguments of the MATE signature that this library does not implement.  Set
  * the bit when the caller passed the argument; the call then fails with
@@ -179,6 +180,51 @@ ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows,
                              const void *num_accepted, int32_t meta_type,
                              const ssu_slot_table *read, const ssu_slot_table *dst,
                              void *stream);
+
+/*
+ * The decode state of a slot kept as a checkpoint plus a buffer of the inputs
+ * of the steps since the last fold (article "ReplaySSM: Cache SSM Inputs, Not
+ * State", sections 核心做法 and 数据与边界: the checkpoint is read every step
+ * but written once every L steps).  For each slot s the buffer holds up to
+ * L - 1 entries j (the inputs of one past step): x and B as given, and the
+ * processed step dt' = softplus(dt + dt_bias) in fp32, so that a fold repeats
+ * exactly the updates the plain step would have made.
+ */
+typedef struct ssu_replay_buffers {
+    int64_t len;               /* L, 1 <= L <= 32                                         */
+    void *x;                   /* device [slots, L, heads, dim] io_dtype, contiguous       */
+    float *dt;                 /* device [slots, L, heads, dim] fp32, contiguous           */
+    void *B;                   /* device [slots, L, groups, dstate] io_dtype, contiguous   */
+    const int32_t *count_in;   /* device [batch]: entries buffered for sequence b          */
+    int32_t *count_out;        /* device [batch]: entries after the call (written); must
+                                  not alias count_in                                      */
+} ssu_replay_buffers;
+
+/*
+ * One decode token per sequence on the checkpoint + buffer form of the state
+ * (article "ReplaySSM: Cache SSM Inputs, Not State", section 核心做法).
+ * args->state is the checkpoint pool; x, dt, z, B, C, y are one row per
+ * sequence as for ssu_update_onetoken; `slots` gives sequence b's slot at
+ * entry b (NULL: slot b); checkpoint and buffers are read and written through
+ * that one slot.  With c = count_in[b]:
+ *   c + 1 <  L  y is read out of checkpoint and buffer without forming the
+ *               state, y = (gamma S_ckpt.C + sum_j gamma_j dt'_j x_j (B_j.C)
+ *               + D x) * silu(z), gamma products of exp(A dt') from the entry
+ *               after j to the current token; the current token is appended
+ *               as entry c and count_out[b] = c + 1; the checkpoint is not
+ *               written;
+ *   c + 1 == L  the buffer is folded into the checkpoint (the entries, then
+ *               the current token, in order, carried in fp32), the state is
+ *               written back once, y is read out of it, count_out[b] = 0.
+ * L = 1 is exactly ssu_update_onetoken with the destination equal to the read
+ * slot.  A pad slot reads as a zero state with no history: y from the current
+ * token alone, nothing written, count_out[b] = 0.  A count outside [0, L) sets
+ * SSU_DEV_BAD_COUNT and skips the sequence.  disable_state_update must be 0.
+ * The dstate and dtype rules of ssu_update_onetoken apply.  batch == 0
+ * launches nothing.
+ */
+ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot_table *slots,
+                             const ssu_replay_buffers *rb, void *stream);
 
 /*
  * Get the kernel for one configuration ready before any CUDA graph capture:

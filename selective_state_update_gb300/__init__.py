@@ -8,6 +8,8 @@ update runs in the CUDA kernels; there is no CPU or PyTorch fallback.  When
 
 Entry points (same names as the C ABI):
   ssu_update_onetoken  one decode token per sequence
+  ssu_replay_update    one decode token per sequence, state kept as a
+                       checkpoint plus a buffer of recent inputs
   ssu_update_packed    packed variable-length / MTP rows (cu_seqlens) or the
                        dense [batch, steps, heads, dim] form
   ssu_prewarm          load a configuration's kernel before graph capture
@@ -23,7 +25,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_prewarm", "selective_state_update",
+__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_prewarm",
+           "selective_state_update",
            "SLOTS_STRIDED", "SLOTS_PER_ROW", "DEV_BAD_SLOT", "DEV_BAD_ENTRY", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
            "library_path", "lib"]
 
@@ -33,7 +36,7 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libssu.so")
 # ssu.h constants
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 SLOTS_STRIDED, SLOTS_PER_ROW = 0, 1
-DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN, DEV_TIMEOUT, DEV_BAD_COUNT = 0x1, 0x2, 0x4, 0x8, 0x10
 UNSUP_RAND_SEED, UNSUP_STATE_SCALE, UNSUP_INTERMEDIATE, UNSUP_CACHE_STEPS, UNSUP_ALGORITHM = (
     0x01, 0x02, 0x04, 0x08, 0x10)
 _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -65,6 +68,11 @@ class Args(ctypes.Structure):
     ]
 
 
+class ReplayBuffers(ctypes.Structure):
+    _fields_ = [("len", ctypes.c_int64), ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p),
+                ("B", ctypes.c_void_p), ("count_in", ctypes.c_void_p), ("count_out", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -88,6 +96,9 @@ def lib():
                                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, p_tab, p_tab,
                                         ctypes.c_void_p]
         L.ssu_update_packed.restype = ctypes.c_int
+        L.ssu_replay_update.argtypes = [p_args, ctypes.c_int64, p_tab, ctypes.POINTER(ReplayBuffers),
+                                        ctypes.c_void_p]
+        L.ssu_replay_update.restype = ctypes.c_int
         L.ssu_prewarm.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
         L.ssu_prewarm.restype = ctypes.c_int
@@ -261,6 +272,48 @@ def ssu_update_packed(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     if dense_shape is not None:
         return out if out is not None else out_flat.view(dense_shape)
     return out_flat
+
+
+def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, count_out=None, D=None, z=None,
+                      dt_bias=None, dt_softplus=False, state_batch_indices=None, pad_slot_id=-1, out=None,
+                      status=None, stream=None):
+    """One decode token per sequence on the checkpoint + buffer form of the
+    state (article "ReplaySSM: Cache SSM Inputs, Not State", section 核心做法).
+
+    ``state`` holds the checkpoints ``[slots, heads, dim, dstate]``; the buffers
+    are ``x_buf`` ``[slots, L, heads, dim]`` (x's dtype), ``dt_buf`` (same
+    shape, fp32 processed steps) and ``B_buf`` ``[slots, L, groups, dstate]``;
+    ``count_in`` ``[batch]`` int32 gives the entries buffered per sequence.
+    Returns ``(y, count_out)``; pass ``count_out`` as the next call's
+    ``count_in``."""
+    dt = _dt3(dt, x)
+    if out is None:
+        out = torch.empty_like(x)
+    batch = x.shape[0]
+    if count_out is None:
+        count_out = torch.empty_like(count_in)
+    slots, heads, dim, dstate = state.shape
+    _need(x_buf.dim() == 4 and x_buf.shape[0] == slots and tuple(x_buf.shape[2:]) == (heads, dim),
+          "x_buf must be [slots, L, heads, dim]")
+    L = x_buf.shape[1]
+    _need(x_buf.dtype == x.dtype and x_buf.is_contiguous(), "x_buf must be contiguous in x's dtype")
+    _need(tuple(dt_buf.shape) == tuple(x_buf.shape) and dt_buf.dtype == torch.float32 and dt_buf.is_contiguous(),
+          "dt_buf must be a contiguous fp32 tensor shaped like x_buf")
+    _need(B_buf.dim() == 4 and tuple(B_buf.shape) == (slots, L, B.shape[1], dstate) and B_buf.dtype == x.dtype
+          and B_buf.is_contiguous(), "B_buf must be [slots, L, groups, dstate], contiguous, in x's dtype")
+    for t in (count_in, count_out):
+        _need(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and t.numel() >= batch,
+              "counts must be contiguous int32 CUDA tensors with one entry per sequence")
+    _need(all(t.is_cuda for t in (x_buf, dt_buf, B_buf)), "buffers must be CUDA tensors")
+    a = _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, status, 0)
+    rt = _table(state_batch_indices, SLOTS_STRIDED)
+    rb = ReplayBuffers(L, x_buf.data_ptr(), dt_buf.data_ptr(), B_buf.data_ptr(), count_in.data_ptr(),
+                       count_out.data_ptr())
+    rc = lib().ssu_replay_update(ctypes.byref(a), batch, None if rt is None else ctypes.byref(rt),
+                                 ctypes.byref(rb), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    return out, count_out
 
 
 def ssu_prewarm(*, state_dtype: torch.dtype, io_dtype: torch.dtype, heads: int, dim: int,

@@ -24,7 +24,7 @@ LIB = os.path.join(OUT_DIR, "libssu.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["ssu_api.cpp", "ssu_onetoken.cu", "ssu_packed.cu"]
+SOURCES = ["ssu_api.cpp", "ssu_onetoken.cu", "ssu_packed.cu", "ssu_replay.cu"]
 HEADERS = ["ssu_internal.h", "ssu_device.cuh"]
 
 

@@ -202,6 +202,34 @@ ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows, c
     return launched(ssu::launch_packed(args->state_dtype, lanes, kp, static_cast<cudaStream_t>(stream)));
 }
 
+ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot_table *slots,
+                             const ssu_replay_buffers *rb, void *stream) {
+    ssu::KParams kp;
+    int lanes = 0;
+    if (batch < 0) return fail(SSU_ERR_INVALID, "batch is negative");
+    ssu_status st = prepare(args, batch, slots, nullptr, &kp, &lanes);
+    if (st != SSU_OK) return st;
+    if (args->disable_state_update) return fail(SSU_ERR_INVALID, "disable_state_update is not defined for the replay step");
+    if (rb == nullptr) return fail(SSU_ERR_INVALID, "replay buffers are NULL");
+    if (rb->len < 1 || rb->len > ssu::kMaxReplayLen)
+        return fail(SSU_ERR_UNSUPPORTED, "buffer length %lld is not supported (1..%d)", (long long)rb->len,
+                    ssu::kMaxReplayLen);
+    if (batch == 0) return ok();
+    if (!rb->x || !rb->dt || !rb->B || !rb->count_in || !rb->count_out)
+        return fail(SSU_ERR_INVALID, "replay buffers and counts must not be NULL");
+    if (rb->count_out == rb->count_in) return fail(SSU_ERR_INVALID, "count_out must not alias count_in");
+    if (batch * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "batch * heads * dim tiles exceeds 2^31-1");
+    kp.nseq = batch;
+    kp.rows = batch;
+    kp.rlen = static_cast<int32_t>(rb->len);
+    kp.xbuf = rb->x;
+    kp.dtbuf = rb->dt;
+    kp.Bbuf = rb->B;
+    kp.cnt_in = rb->count_in;
+    kp.cnt_out = rb->count_out;
+    return launched(ssu::launch_replay(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
+}
+
 ssu_status ssu_prewarm(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype, int64_t heads, int64_t dim,
                        int64_t dstate, int64_t groups, int32_t packed) {
     int lanes = 0;

@@ -57,7 +57,7 @@ __device__ __forceinline__ int64_t load_index(const void *base, int64_t i, int i
                   : static_cast<int64_t>(__ldg(static_cast<const int *>(base) + i));
 }
 
-enum : int { kDevBadSlot = 0x1, kDevBadEntry = 0x2, kDevBadSeqlen = 0x4, kDevTimeout = 0x8 };
+enum : int { kDevBadSlot = 0x1, kDevBadEntry = 0x2, kDevBadSeqlen = 0x4, kDevTimeout = 0x8, kDevBadCount = 0x10 };
 
 __device__ __forceinline__ void flag(int32_t *status, int bit) {
     if (status != nullptr) atomicOr(status, bit);
@@ -347,13 +347,20 @@ struct RowInputs {
     float dt, x, z;
 };
 
-// Per-row scalars {dA, dt' x, x, gate}, gate = silu(z) / z * z = z / (1 + e^-z)
-// with a z input, 1 without.  Not inlined: both kernels get exactly the same
-// instructions, hence the same bits.
+// The processed step dt' and the decay exp(A dt').  Not inlined, so that the
+// kernels, and a later fold of a buffered step, all get the same bits.
+static __device__ __noinline__ float processed_step(float dt, float bias, int softplus) {
+    return step_size(dt, bias, softplus);
+}
+static __device__ __noinline__ float decay(float Ah, float d) { return expf(Ah * d); }
+
+// Per-row scalars {dA, dt' x, x, gate}: gate is the factor y is multiplied
+// by, silu(z) = z / (1 + e^-z) with a z input, 1 without.  Not inlined: every
+// kernel gets exactly the same instructions, hence the same bits.
 static __device__ __noinline__ float4 row_scalars(RowInputs in, float Ah, float bias, int softplus, int has_z) {
-    const float d = step_size(in.dt, bias, softplus);
+    const float d = processed_step(in.dt, bias, softplus);
     const float gate = has_z ? in.z / (1.f + expf(-in.z)) : 1.f;
-    return make_float4(expf(Ah * d), d * in.x, in.x, gate);
+    return make_float4(decay(Ah, d), d * in.x, in.x, gate);
 }
 
 // Slot at entry (b, t) of table `t`, or `fallback` without a table.  Returns

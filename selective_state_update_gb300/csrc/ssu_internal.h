@@ -59,6 +59,13 @@ struct KParams {
     const void *cu, *acc;
     int32_t meta_is_i64;
     int32_t *status;
+    // checkpoint + buffer form (ssu_replay_update)
+    int32_t rlen;
+    void *xbuf;
+    float *dtbuf;
+    void *Bbuf;
+    const int32_t *cnt_in;
+    int32_t *cnt_out;
 };
 
 // Launchers (one translation unit per kernel).  `lanes` = dstate / 16.
@@ -68,5 +75,9 @@ cudaError_t launch_packed(int state_dtype, int lanes, const KParams &p, cudaStre
 // Load the kernel's module and read its attributes (no launch).
 cudaError_t prewarm_onetoken(int state_dtype, int lanes);
 cudaError_t prewarm_packed(int state_dtype, int lanes);
+cudaError_t launch_replay(int state_dtype, int lanes, const KParams &p, int64_t batch, cudaStream_t stream);
+
+// Largest buffer length of the checkpoint + buffer form.
+constexpr int kMaxReplayLen = 32;
 
 }  // namespace ssu

@@ -1,0 +1,186 @@
+"""The checkpoint + buffer form of the decode state (article "ReplaySSM: Cache
+SSM Inputs, Not State", section 核心做法) on the GPU, through libssu's C ABI:
+against the oracle element by element, L = 1 against the plain one-token
+kernel bit for bit, L steps against L plain steps, and the full-size batch-256
+workload on sampled sequences."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_update_gb300 as ssu
+import workloads
+from gpu_harness import DEV, run_gpu
+from ssu_testlib import STATE_F32_ATOL, STATE_F32_RTOL, assert_state_close, assert_y_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_replay_gpu(w, status=None):
+    g = w.to(DEV)
+    y, cnt = ssu.ssu_replay_update(g.state, g.x, g.dt, g.A, g.B, g.C, g.xbuf, g.dtbuf, g.Bbuf, g.count, D=g.D,
+                                   z=g.z, dt_bias=g.dt_bias, dt_softplus=g.dt_softplus,
+                                   state_batch_indices=g.read, pad_slot_id=g.pad_slot_id, status=status)
+    torch.cuda.synchronize()
+    return g, y, cnt
+
+
+def run_replay_oracle(w):
+    return oracle.replay(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count, D=w.D, z=w.z,
+                         dt_bias=w.dt_bias, dt_softplus=w.dt_softplus, slot_of=w.read, pad_slot_id=w.pad_slot_id)
+
+
+def check_against_oracle(w):
+    ref = run_replay_oracle(w)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g, y, cnt = run_replay_gpu(w, status)
+    assert int(status.item()) == 0
+    assert_y_close(y, ref.y_exact)
+    assert torch.equal(cnt.cpu().long(), ref.count)
+    written = torch.zeros(w.state.shape[0], dtype=torch.bool)
+    L = w.xbuf.shape[1]
+    for b in range(w.nseq):
+        s = b if w.read is None else int(w.read[b])
+        if s != w.pad_slot_id and int(w.count[b]) + 1 == L:
+            written[s] = True
+    got = g.state.cpu()
+    assert torch.equal(got[~written], w.state[~written]), "a checkpoint that does not fold changed"
+    if written.any():
+        assert_state_close(got[written], ref.ckpt[written], what="folded checkpoint")
+    assert torch.equal(g.xbuf.cpu(), ref.xbuf), "x buffer"
+    assert torch.equal(g.Bbuf.cpu(), ref.Bbuf), "B buffer"
+    d, r = f64(g.dtbuf), f64(ref.dtbuf)
+    assert np.all(np.abs(d - r) <= STATE_F32_RTOL * np.abs(r) + STATE_F32_ATOL), "dt buffer"
+    return g, y
+
+
+@pytest.mark.parametrize("buffer_len", [1, 2, 5, 16])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_replay_against_oracle(libssu, buffer_len, state_dtype):
+    w = workloads.replay_problem(10 + buffer_len, slots=40, heads=4, groups=2, dim=16, dstate=64, nseq=12,
+                                 buffer_len=buffer_len, state_dtype=state_dtype)
+    check_against_oracle(w)
+
+
+@pytest.mark.parametrize("dstate", [16, 32, 128, 256])
+@pytest.mark.parametrize("dim", [8, 64, 100])
+def test_replay_shapes(libssu, dstate, dim):
+    w = workloads.replay_problem(20 + dstate + dim, slots=24, heads=6, groups=3, dim=dim, dstate=dstate, nseq=5,
+                                 buffer_len=6)
+    check_against_oracle(w)
+
+
+@pytest.mark.parametrize("io_dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("flags", [(True, True, True, True), (False, False, False, False), (True, False, True, False)])
+def test_replay_io_and_flags(libssu, io_dtype, flags):
+    with_D, with_z, with_bias, softplus = flags
+    w = workloads.replay_problem(30, slots=32, heads=4, groups=1, dim=16, dstate=128, nseq=8, buffer_len=4,
+                                 io_dtype=io_dtype, with_D=with_D, with_z=with_z, with_bias=with_bias,
+                                 dt_softplus=softplus)
+    check_against_oracle(w)
+
+
+def test_replay_no_table_and_pad_zero(libssu):
+    check_against_oracle(workloads.replay_problem(31, slots=6, nseq=6, tables=False, buffer_len=3))
+    check_against_oracle(workloads.replay_problem(32, slots=20, nseq=8, pad_slot_id=0, pad_frac=0.3))
+
+
+def test_buffer_len_one_is_the_plain_step_bitwise(libssu):
+    """L = 1: every step folds and equals the one-token kernel writing back to
+    the read slot, bit for bit (the article's anchor)."""
+    w = workloads.replay_problem(33, slots=48, heads=8, groups=2, dim=64, dstate=128, nseq=16, buffer_len=1)
+    g, y, cnt = run_replay_gpu(w)
+    p = replace(w, kind="onetoken", dst=w.read.clone()).to(DEV)
+    y_plain = run_gpu(p)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_plain) and torch.equal(g.state, p.state)
+    assert int(cnt.abs().sum()) == 0
+
+
+def test_l_steps_equal_l_plain_steps(libssu):
+    """From empty buffers, L steps on the checkpoint + buffer form fold into
+    exactly the fp32 state L plain steps produce (bit for bit); the folding
+    step's y is bit-identical and the others agree within the output
+    tolerance."""
+    L, nseq = 6, 10
+    base = workloads.replay_problem(34, slots=32, heads=4, groups=2, dim=64, dstate=128, nseq=nseq, buffer_len=L,
+                                    pad_frac=0.0)
+    gen = torch.Generator().manual_seed(77)
+    steps = []
+    for t in range(L):
+        steps.append(dict(x=torch.randn(base.x.shape, generator=gen).to(base.x.dtype),
+                          dt=torch.randn(base.dt.shape, generator=gen),
+                          z=torch.randn(base.z.shape, generator=gen).to(base.z.dtype),
+                          B=torch.randn(base.B.shape, generator=gen).to(base.B.dtype),
+                          C=torch.randn(base.C.shape, generator=gen).to(base.C.dtype)))
+    rep = replace(base, count=torch.zeros(nseq, dtype=torch.int32)).to(DEV)
+    plain = replace(base, kind="onetoken", dst=base.read.clone()).to(DEV)
+    for t, inp in enumerate(steps):
+        r = replace(rep, **{k: v.to(DEV) for k, v in inp.items()})
+        y_r, cnt = ssu.ssu_replay_update(r.state, r.x, r.dt, r.A, r.B, r.C, r.xbuf, r.dtbuf, r.Bbuf, r.count,
+                                         D=r.D, z=r.z, dt_bias=r.dt_bias, dt_softplus=r.dt_softplus,
+                                         state_batch_indices=r.read)
+        rep = replace(rep, count=cnt)
+        pl = replace(plain, **{k: v.to(DEV) for k, v in inp.items()})
+        y_p = run_gpu(pl)
+        torch.cuda.synchronize()
+        if t + 1 < L:
+            assert_y_close(y_r, y_p.cpu().double())
+            assert int(cnt.cpu().sum()) == (t + 1) * nseq
+        else:
+            assert torch.equal(y_r, y_p)
+            assert torch.equal(rep.state, plain.state), "folded checkpoint differs from the plain steps"
+            assert int(cnt.cpu().abs().sum()) == 0
+
+
+def test_bad_count_sets_status(libssu):
+    w = workloads.replay_problem(35, slots=20, nseq=4, buffer_len=4, pad_frac=0.0)
+    w.count[2] = 9
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    run_replay_gpu(w, status)
+    assert int(status.item()) == ssu.DEV_BAD_COUNT
+
+
+def test_replay_b256_sampled(libssu):
+    """The full-size batch-256 workload: sampled sequences against the oracle
+    (compact copies of their slots), the rest by properties: checkpoints of
+    sequences that do not fold are unchanged, counts advance."""
+    w = workloads.replay_b256_fp32()
+    L = w.meta["buffer_len"]
+    g = w.to(DEV)
+    before = g.state.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y, cnt = ssu.ssu_replay_update(g.state, g.x, g.dt, g.A, g.B, g.C, g.xbuf, g.dtbuf, g.Bbuf, g.count, D=g.D,
+                                   z=g.z, dt_bias=g.dt_bias, dt_softplus=True, state_batch_indices=g.read,
+                                   pad_slot_id=g.pad_slot_id, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    expect = torch.where((w.count + 1 == L) | (w.read == w.pad_slot_id), 0, w.count + 1)
+    assert torch.equal(cnt.cpu(), expect.to(torch.int32))
+    fold_slots = [int(w.read[b]) for b in range(w.nseq) if int(w.read[b]) != 0 and int(w.count[b]) + 1 == L]
+    keep = torch.ones(w.state.shape[0], dtype=torch.bool, device=DEV)
+    keep[torch.tensor(fold_slots, device=DEV)] = False
+    assert torch.equal(before[keep], g.state[keep])
+    del before
+    sample = [b for b in range(w.nseq) if int(w.count[b]) + 1 == L][:6] + [0, 1, 2, 3, 100, 200]
+    sample += [b for b in range(w.nseq) if int(w.read[b]) == 0][:3]
+    sample = sorted(set(sample))
+    slots = [int(w.read[b]) for b in sample]
+    order = [0] + sorted(set(s for s in slots if s != 0))
+    m = {s: i for i, s in enumerate(order)}
+    idx = torch.tensor(order)
+    sub = replace(w, state=w.state[idx], xbuf=w.xbuf[idx], dtbuf=w.dtbuf[idx], Bbuf=w.Bbuf[idx],
+                  read=torch.tensor([m[s] if s != 0 else 0 for s in slots], dtype=torch.int32),
+                  count=w.count[sample], x=w.x[sample], dt=w.dt[sample], z=w.z[sample], B=w.B[sample],
+                  C=w.C[sample])
+    ref = run_replay_oracle(sub)
+    assert_y_close(y[sample].cpu(), ref.y_exact, what="y (sampled)")
+    for i, b in enumerate(sample):
+        s = slots[i]
+        if s != 0 and int(w.count[b]) + 1 == L:
+            assert_state_close(g.state[s].cpu(), ref.ckpt[m[s]], what="folded checkpoint (sampled)")
+        if s != 0 and int(w.count[b]) + 1 < L:
+            c = int(w.count[b])
+            assert torch.equal(g.xbuf[s, c].cpu(), ref.xbuf[m[s], c])

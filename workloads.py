@@ -55,6 +55,11 @@ class Workload:
     cu_seqlens: Optional[torch.Tensor] = None  # [nseq + 1] int32
     num_accepted: Optional[torch.Tensor] = None  # [nseq] int32
     dense_steps: int = 0                       # >0: dense [nseq, steps, ...] form, no cu_seqlens
+    # checkpoint + buffer form (kind "replay"): state holds the checkpoints
+    xbuf: Optional[torch.Tensor] = None        # [slots, L, heads, dim] io dtype
+    dtbuf: Optional[torch.Tensor] = None       # [slots, L, heads, dim] fp32 processed steps
+    Bbuf: Optional[torch.Tensor] = None        # [slots, L, groups, dstate] io dtype
+    count: Optional[torch.Tensor] = None       # [batch] int32 buffered entries per sequence
     meta: dict = field(default_factory=dict)
 
     @property
@@ -63,7 +68,7 @@ class Workload:
 
     @property
     def nseq(self) -> int:
-        if self.kind == "onetoken":
+        if self.kind in ("onetoken", "replay"):
             return self.rows
         if self.cu_seqlens is not None:
             return self.cu_seqlens.numel() - 1
@@ -214,13 +219,86 @@ def varlen_fp16(device="cpu", seed=1005, disable_state_update=False,
                     num_accepted=acc.to(torch.int32).to(device), meta={"lengths": lens.tolist()}, **inp)
 
 
+def _replay_buffers(g, device, slots, L, heads, dim, dstate, groups, io_dtype):
+    """A history of buffered steps: x, B ~ N(0,1) in the io dtype; processed
+    steps dt' ~ U(0.001, 0.2) in fp32."""
+    xbuf = _normal((slots, L, heads, dim), g, device, dtype=io_dtype)
+    dtbuf = _uniform((slots, L, heads, dim), g, device, 0.001, 0.2)
+    Bbuf = _normal((slots, L, groups, dstate), g, device, dtype=io_dtype)
+    return xbuf, dtbuf, Bbuf
+
+
+def replay_b256_fp32(device="cpu", seed=1006, batch=256, buffer_len=16) -> Workload:
+    """Batch-256 decode on the checkpoint + buffer form: the b256_fp32 shapes
+    and distributions, one slot table (read = write), a buffer of
+    ``buffer_len`` entries per slot, sequence b holding b % L entries so that
+    every step folds 1/L of the sequences."""
+    heads, dim, dstate, groups, pad = 128, 64, 128, 8, 0
+    slots = 2 * batch
+    g = _gen(seed, device)
+    inp = _decode_inputs(g, device, batch, heads, dim, dstate, groups, torch.bfloat16)
+    state = _pool(g, device, slots, heads, dim, dstate, torch.float32)
+    xbuf, dtbuf, Bbuf = _replay_buffers(g, device, slots, buffer_len, heads, dim, dstate, groups, torch.bfloat16)
+    gh = _gen(seed + 7, "cpu")
+    read, _ = _distinct_tables_with_pad(gh, batch, slots, pad, max(1, round(0.05 * batch)), device)
+    count = (torch.arange(batch, dtype=torch.int32) % buffer_len).to(device)
+    return Workload("replay_b256_fp32", "replay", state, dt_softplus=True, read=read, pad_slot_id=pad,
+                    xbuf=xbuf, dtbuf=dtbuf, Bbuf=Bbuf, count=count, meta={"buffer_len": buffer_len}, **inp)
+
+
+def replay_problem(seed: int, *, slots: int = 16, heads: int = 4, dim: int = 8, dstate: int = 16,
+                   groups: int = 2, nseq: int = 4, buffer_len: int = 4, state_dtype=torch.float32,
+                   io_dtype=torch.bfloat16, with_D: bool = True, with_z: bool = True, with_bias: bool = True,
+                   dt_softplus: bool = True, pad_slot_id: int = -1, pad_frac: float = 0.2,
+                   tables: bool = True, device="cpu") -> Workload:
+    """A small seeded problem on the checkpoint + buffer form: distinct slots
+    (some pad), counts U{0..L-1}, random buffered histories."""
+    gh = _gen(seed, "cpu")
+    read = None
+    if tables:
+        usable = torch.tensor([s for s in range(slots) if s != pad_slot_id], dtype=torch.int64)
+        if nseq > usable.numel():
+            raise ValueError("not enough slots")
+        read = usable[torch.randperm(usable.numel(), generator=gh)[:nseq]].clone()
+        n_pad = int(round(pad_frac * nseq))
+        if n_pad:
+            read[torch.randperm(nseq, generator=gh)[:n_pad]] = pad_slot_id
+        read = read.to(torch.int32)
+    count = torch.randint(0, buffer_len, (nseq,), generator=gh, dtype=torch.int64).to(torch.int32)
+    g = _gen(seed + 1, "cpu")
+    x = _normal((nseq, heads, dim), g, "cpu", dtype=io_dtype)
+    z = _normal((nseq, heads, dim), g, "cpu", dtype=io_dtype) if with_z else None
+    dt = _normal((nseq, heads, dim), g, "cpu") if dt_softplus else _uniform((nseq, heads, dim), g, "cpu", 0.0, 0.2)
+    dt_bias = _step_bias(g, heads, dt_softplus) if with_bias else None
+    A = -torch.exp(_uniform((heads,), g, "cpu", 0.0, 2.8))
+    D = _normal((heads,), g, "cpu") if with_D else None
+    B = _normal((nseq, groups, dstate), g, "cpu", dtype=io_dtype)
+    C = _normal((nseq, groups, dstate), g, "cpu", dtype=io_dtype)
+    state = _pool(g, "cpu", slots, heads, dim, dstate, state_dtype, std=0.5)
+    xbuf, dtbuf, Bbuf = _replay_buffers(g, "cpu", slots, buffer_len, heads, dim, dstate, groups, io_dtype)
+    w = Workload(f"replay_{seed}", "replay", state, x, dt, A, B, C, D=D, z=z, dt_bias=dt_bias,
+                 dt_softplus=dt_softplus, read=read, pad_slot_id=pad_slot_id, xbuf=xbuf, dtbuf=dtbuf, Bbuf=Bbuf,
+                 count=count, meta={"buffer_len": buffer_len})
+    return w.to(device)
+
+
 NAMED = {
     "tiny_onetoken": tiny_onetoken,
     "b256_fp32": b256_fp32,
     "b1024_bf16": b1024_bf16,
     "mtp_64x7_fp32": mtp_64x7_fp32,
     "varlen_fp16": varlen_fp16,
+    "replay_b256_fp32": replay_b256_fp32,
 }
+
+
+def _step_bias(g, heads, softplus):
+    """dt_bias for the small problems: N(-1, 0.5) before a softplus; without
+    one U(0, 0.1), so that dt' = dt + bias stays >= 0 (A < 0 and dt' >= 0 keep
+    the recurrence decaying, 0 < exp(A dt') <= 1)."""
+    if softplus:
+        return _normal((heads,), g, "cpu", mean=-1.0, std=0.5)
+    return _uniform((heads,), g, "cpu", 0.0, 0.1)
 
 
 def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads: int = 4,
@@ -290,7 +368,7 @@ def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads:
     z = _normal((rows, heads, dim), g, "cpu", dtype=io_dtype) if with_z else None
     dt_shape = (rows, heads) if per_head_dt else (rows, heads, dim)
     dt = (_normal(dt_shape, g, "cpu") if dt_softplus else _uniform(dt_shape, g, "cpu", 0.0, 0.2)).to(dt_dtype)
-    dt_bias = _normal((heads,), g, "cpu", mean=-1.0, std=0.5) if with_bias else None
+    dt_bias = _step_bias(g, heads, dt_softplus) if with_bias else None
     A = -torch.exp(_uniform((heads,), g, "cpu", 0.0, 2.8))
     D = _normal((heads,), g, "cpu") if with_D else None
     B = _normal((rows, groups, dstate), g, "cpu", dtype=io_dtype)
