@@ -47,16 +47,20 @@ DESCRIPTIONS = {
     "varlen_fp16": "variable-length packed decode, 128 sequences of length U{0..8}, heads 64, dim 64, "
                    "dstate 128, groups 1, fp16 pool of 2048 slots, flat per-row read table, 3% pad",
     "tiny_onetoken": "one-token decode, batch 2, heads 8, dim 8, dstate 128, groups 2, fp16 zero state",
+    "replay_b256_fp32": "one-token decode on the checkpoint + buffer form (ReplaySSM), batch 256, heads 128, "
+                        "dim 64, dstate 128, groups 8, fp32 checkpoints (512 slots), buffer length 16, "
+                        "sequence b starting with b % 16 buffered entries (1/16 of the sequences fold per step)",
 }
 KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
-                  "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"]}
+                  "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
+                  "replay": ["ssu_replay.cu", "ssu_device.cuh", "ssu_internal.h"]}
 
 
 # --------------------------------------------------------------------------
 # Accounting (host side, from the tables).
 # --------------------------------------------------------------------------
 def _lengths(w):
-    if w.kind == "onetoken":
+    if w.kind in ("onetoken", "replay"):
         return [1] * w.nseq
     if w.cu_seqlens is not None:
         cu = w.cu_seqlens.cpu().tolist()
@@ -77,9 +81,41 @@ def _entry_slot(table, w, b, t, cu):
     return int(table[b, t])
 
 
+def replay_bytes(w) -> dict:
+    """Bytes one call on the checkpoint + buffer form must move: every non-pad
+    sequence reads its checkpoint and its c buffered entries (x, dt' per head
+    row, B per group); a folding sequence writes the checkpoint back, any
+    other appends one entry; plus the small operands and the counts."""
+    H, P, N = w.state.shape[1:]
+    G = w.B.shape[1]
+    sb = H * P * N * w.state.element_size()
+    io = w.x.element_size()
+    entry = H * P * (io + 4) + G * N * io
+    L = w.xbuf.shape[1]
+    counts = w.count.cpu().tolist()
+    slots = w.read.cpu().tolist() if w.read is not None else list(range(w.nseq))
+    rd = wr = folds = 0
+    for b, c in enumerate(counts):
+        if slots[b] == w.pad_slot_id:
+            continue
+        rd += sb + c * entry
+        if c + 1 == L:
+            wr += sb
+            folds += 1
+        else:
+            wr += entry
+    small = sum(t.numel() * t.element_size() for t in (w.x, w.dt, w.B, w.C, w.z, w.A, w.D, w.dt_bias, w.read)
+                if t is not None)
+    small += w.x.numel() * w.x.element_size() + 2 * w.count.numel() * 4
+    return {"state_read": rd, "state_write": wr, "small": small, "total": rd + wr + small, "folds": folds,
+            "state_bytes_per_unit": sb}
+
+
 def algorithmic_bytes(w) -> dict:
     """Bytes one call must move: each non-pad seed read once, each non-pad
     destination written once per token, plus every small operand once."""
+    if w.kind == "replay":
+        return replay_bytes(w)
     H, P, N = w.state.shape[1:]
     sb = H * P * N * w.state.element_size()
     lens = _lengths(w)
@@ -242,6 +278,15 @@ def _call(ssu, w, out, stream=None):
                   stream=stream)
     if w.kind == "onetoken":
         return ssu.ssu_update_onetoken(w.state, w.x, w.dt, w.A, w.B, w.C, **common)
+    if w.kind == "replay":
+        # steady decode: this step's counts are the last step's output
+        spare = w.meta.setdefault("count_spare", torch.empty_like(w.count))
+        y, cnt = ssu.ssu_replay_update(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count,
+                                       count_out=spare, D=w.D, z=w.z, dt_bias=w.dt_bias,
+                                       dt_softplus=w.dt_softplus, state_batch_indices=w.read,
+                                       pad_slot_id=w.pad_slot_id, out=out, stream=stream)
+        w.meta["count_spare"], w.count = w.count, cnt
+        return y
     return ssu.ssu_update_packed(w.state, w.x, w.dt, w.A, w.B, w.C, cu_seqlens=w.cu_seqlens,
                                  num_accepted_tokens=w.num_accepted, slot_mode=w.slot_mode, **common)
 
@@ -369,7 +414,7 @@ def _sample_problem(w, seqs):
     def rows_of(t):
         if t is None:
             return None
-        if w.kind == "onetoken":
+        if w.kind in ("onetoken", "replay"):
             return t.reshape(-1)[seqs]
         if w.slot_mode == workloads.SLOTS_PER_ROW:
             return t.reshape(-1)[rows]
@@ -384,6 +429,10 @@ def _sample_problem(w, seqs):
         [new_pad if v == pad else m[v] for v in t.reshape(-1).tolist()], dtype=t.dtype).view(t.shape)
     sel = lambda t: None if t is None else t[rows]
     sub_cu = torch.tensor([sum(sub_lens[:i]) for i in range(len(sub_lens) + 1)], dtype=torch.int32)
+    if w.kind == "replay":
+        return replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
+                       read=remap(rd), pad_slot_id=new_pad, xbuf=w.xbuf[order], dtbuf=w.dtbuf[order],
+                       Bbuf=w.Bbuf[order], count=w.count[seqs], meta=dict(w.meta))
     return replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
                    read=remap(rd), dst=remap(wr), pad_slot_id=new_pad,
                    cu_seqlens=sub_cu if w.kind == "packed" else None,
@@ -392,6 +441,10 @@ def _sample_problem(w, seqs):
 
 def _oracle_call(sub):
     import oracle
+    if sub.kind == "replay":
+        return oracle.replay(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, sub.xbuf, sub.dtbuf, sub.Bbuf, sub.count,
+                             D=sub.D, z=sub.z, dt_bias=sub.dt_bias, dt_softplus=sub.dt_softplus,
+                             slot_of=sub.read, pad_slot_id=sub.pad_slot_id)
     mode = oracle.SLOTS_PER_ROW if sub.slot_mode == workloads.SLOTS_PER_ROW else oracle.SLOTS_STRIDED
     return oracle.ssu(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, D=sub.D, z=sub.z, dt_bias=sub.dt_bias,
                       dt_softplus=sub.dt_softplus, read=oracle.Table.of(sub.read, mode),
@@ -401,15 +454,15 @@ def _oracle_call(sub):
 
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
-         "varlen_fp16": 1005}
+         "varlen_fp16": 1005, "replay_b256_fp32": 1006}
 
 
 def make_workload(args, device, seed_offset=0):
     gen = workloads.NAMED[args.workload]
     kw = {}
     if args.batch is not None:
-        if args.workload not in ("b256_fp32", "mtp_64x7_fp32"):
-            raise SystemExit("--batch applies to the b256_fp32 and mtp_64x7_fp32 workloads only")
+        if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32"):
+            raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32 and replay_b256_fp32 workloads only")
         kw["batch"] = args.batch
     return gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
 

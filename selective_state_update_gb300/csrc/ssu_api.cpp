@@ -227,6 +227,12 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
     kp.Bbuf = rb->B;
     kp.cnt_in = rb->count_in;
     kp.cnt_out = rb->count_out;
+    {
+        const int64_t io = args->io_dtype == SSU_F32 ? 4 : 2;
+        const bool aligned = reinterpret_cast<uintptr_t>(rb->x) % 16 == 0 && reinterpret_cast<uintptr_t>(rb->dt) % 16 == 0 &&
+                             reinterpret_cast<uintptr_t>(rb->B) % 16 == 0;
+        kp.rbulk = aligned && (args->dim * io) % 16 == 0 && (args->dim * 4) % 16 == 0 && (args->dstate * io) % 16 == 0;
+    }
     return launched(ssu::launch_replay(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
 }
 

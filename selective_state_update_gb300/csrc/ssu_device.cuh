@@ -363,6 +363,54 @@ static __device__ __noinline__ float4 row_scalars(RowInputs in, float Ah, float 
     return make_float4(decay(Ah, d), d * in.x, in.x, gate);
 }
 
+// (sequence, head, dim tile) of a work unit of the one-token style kernels.
+struct UnitCoords {
+    int64_t b;
+    int h, g, row0, rows_here;
+};
+
+// Walks this CTA's units u = blockIdx.x + k * gridDim.x as (sequence, head,
+// dim tile) with additions and carries only: no 64-bit division per unit.
+struct UnitWalker {
+    int pt, h;          // current dim tile and head
+    int64_t b;          // current sequence
+    int d_pt, d_h;      // the stride gridDim.x as (tiles, heads, sequences)
+    int64_t d_b;
+
+    __device__ __forceinline__ UnitWalker(const KParams &p, int64_t u, int64_t step) {
+        pt = static_cast<int>(u % p.ptiles);
+        h = static_cast<int>((u / p.ptiles) % p.H);
+        b = u / (static_cast<int64_t>(p.ptiles) * p.H);
+        d_pt = static_cast<int>(step % p.ptiles);
+        d_h = static_cast<int>((step / p.ptiles) % p.H);
+        d_b = step / (static_cast<int64_t>(p.ptiles) * p.H);
+    }
+    __device__ __forceinline__ void advance(const KParams &p) {
+        pt += d_pt;
+        int carry = 0;
+        if (pt >= p.ptiles) {
+            pt -= p.ptiles;
+            carry = 1;
+        }
+        h += d_h + carry;
+        carry = 0;
+        if (h >= p.H) {
+            h -= p.H;
+            carry = 1;
+        }
+        b += d_b + carry;
+    }
+    __device__ __forceinline__ UnitCoords coords(const KParams &p) const {
+        UnitCoords c;
+        c.b = b;
+        c.h = h;
+        c.g = h / p.heads_per_group;
+        c.row0 = pt * kTileRows;
+        c.rows_here = min(kTileRows, p.P - c.row0);
+        return c;
+    }
+};
+
 // Slot at entry (b, t) of table `t`, or `fallback` without a table.  Returns
 // false (and flags) when the entry lies outside the table.
 __device__ __forceinline__ bool table_slot(const KParams &p, const SlotTab &t, int64_t b,

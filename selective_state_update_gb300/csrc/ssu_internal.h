@@ -66,6 +66,7 @@ struct KParams {
     void *Bbuf;
     const int32_t *cnt_in;
     int32_t *cnt_out;
+    int32_t rbulk;  // buffer rows are 16-byte aligned: stage them with bulk copies
 };
 
 // Launchers (one translation unit per kernel).  `lanes` = dstate / 16.

@@ -116,53 +116,6 @@ struct StageView {
     }
 };
 
-struct UnitCoords {
-    int64_t b;
-    int h, g, row0, rows_here;
-};
-
-// Walks this CTA's units u = blockIdx.x + k * gridDim.x as (sequence, head,
-// dim tile) with additions and carries only: no 64-bit division per unit.
-struct UnitWalker {
-    int pt, h;          // current dim tile and head
-    int64_t b;          // current sequence
-    int d_pt, d_h;      // the stride gridDim.x as (tiles, heads, sequences)
-    int64_t d_b;
-
-    __device__ __forceinline__ UnitWalker(const KParams &p, int64_t u, int64_t step) {
-        pt = static_cast<int>(u % p.ptiles);
-        h = static_cast<int>((u / p.ptiles) % p.H);
-        b = u / (static_cast<int64_t>(p.ptiles) * p.H);
-        d_pt = static_cast<int>(step % p.ptiles);
-        d_h = static_cast<int>((step / p.ptiles) % p.H);
-        d_b = step / (static_cast<int64_t>(p.ptiles) * p.H);
-    }
-    __device__ __forceinline__ void advance(const KParams &p) {
-        pt += d_pt;
-        int carry = 0;
-        if (pt >= p.ptiles) {
-            pt -= p.ptiles;
-            carry = 1;
-        }
-        h += d_h + carry;
-        carry = 0;
-        if (h >= p.H) {
-            h -= p.H;
-            carry = 1;
-        }
-        b += d_b + carry;
-    }
-    __device__ __forceinline__ UnitCoords coords(const KParams &p) const {
-        UnitCoords c;
-        c.b = b;
-        c.h = h;
-        c.g = h / p.heads_per_group;
-        c.row0 = pt * kTileRows;
-        c.rows_here = min(kTileRows, p.P - c.row0);
-        return c;
-    }
-};
-
 // Everything the producer needs from global memory for one unit, loaded into
 // registers one unit ahead so that the loads are in flight while the producer
 // stages the previous unit or waits for a free stage.  The loads are issued

@@ -17,37 +17,66 @@
 // about a read.
 //
 // Work unit: (sequence b, head h, tile of kTileRows dim rows), one CTA each.
-// The checkpoint tile arrives by one bulk asynchronous copy (TMA engine,
-// mbarrier completion) while the CTA stages the entries' B vectors, C and
-// the per-row, per-entry scalars {exp(A dt'_j), dt'_j x_j} in shared memory.
+// One thread requests the checkpoint tile and every buffered entry of the
+// tile (x rows, dt' rows, B of the group) as bulk asynchronous copies (TMA
+// engine) completing on one mbarrier, so all of a unit's reads are in flight
+// together; meanwhile the CTA loads the current token and computes its row
+// scalars.
 #include <atomic>
 
 #include "ssu_device.cuh"
 
 namespace ssu {
 
-// Dynamic shared memory for a buffer of `len` entries: the checkpoint tile,
-// B of every entry and the current token, C, the B.C dot products, the
-// per-row per-entry decays and input terms, the current token's row scalars
-// and the readout coefficients of each row, the mbarrier.
+// Dynamic shared memory for a buffer of `len` entries: the checkpoint tile;
+// the buffered entries as stored (x rows and dt' rows of this tile, B of the
+// group); C and the current token's B as fp32; the B.C dot products; per-row
+// per-entry decays and input terms (for a fold); the current token's row
+// scalars and each row's readout coefficients; the mbarrier.
 template <typename TS, int L>
 struct ReplaySmem {
     static constexpr int kN = Tile<TS, L>::kN;
     static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
-    int tile, bs, cs, dots, rowa, rowb, rowq, rowg, bar, bytes;
-    __host__ __device__ explicit ReplaySmem(int len) {
+    int tile, xe, de, be, cs, bc, dots, rowa, rowb, rowq, rowg, bar, bytes;
+    __host__ __device__ static int up(int v) { return (v + 127) / 128 * 128; }
+    __host__ __device__ ReplaySmem(int len, int io) {
         tile = 0;
-        bs = kTileBytes;                          // float [len][N]
-        cs = bs + len * kN * 4;                   // float [N]
-        dots = cs + kN * 4;                       // float [len], padded to 32
-        rowa = dots + ((len + 31) / 32) * 32 * 4;  // float [len][kTileRows]
-        rowb = rowa + len * kTileRows * 4;        // float [len][kTileRows]
-        rowq = rowb + len * kTileRows * 4;        // float4 [kTileRows]
-        rowg = rowq + kTileRows * 16;             // float2 [kTileRows]
-        bar = rowg + kTileRows * 8;               // uint64
+        xe = up(kTileBytes);                      // io   [len][kTileRows]
+        de = up(xe + len * kTileRows * io);       // f32  [len][kTileRows]
+        be = up(de + len * kTileRows * 4);        // io   [len][N]
+        cs = up(be + len * kN * io);              // f32  [N]
+        bc = up(cs + kN * 4);                     // f32  [N]
+        dots = up(bc + kN * 4);                   // f32  [len]
+        rowa = up(dots + len * 4);                // f32  [len][kTileRows]
+        rowb = up(rowa + len * kTileRows * 4);    // f32  [len][kTileRows]
+        rowq = up(rowb + len * kTileRows * 4);    // f32x4 [kTileRows]
+        rowg = up(rowq + kTileRows * 16);         // f32x2 [kTileRows]
+        bar = up(rowg + kTileRows * 8);           // u64
         bytes = bar + 16;
     }
 };
+
+__device__ __forceinline__ float raw_to_float(const unsigned char *base, int i, int io_dtype) {
+    if (io_dtype == kF32) return reinterpret_cast<const float *>(base)[i];
+    return bits_to_float(reinterpret_cast<const unsigned short *>(base)[i], io_dtype);
+}
+
+// Not inlined: the readout walk of a row from the newest entry to the oldest,
+// w = gamma_{j+1:c} along the way and gamma_{0:c} at the end.
+static __device__ __noinline__ float2 readout_walk(int c, int r, float Ah, float dA_now, float dtx_now,
+                                                   const float *de, const unsigned char *xe, const float *dots,
+                                                   int io_dtype) {
+    float w = 1.f;
+    float hist = fmaf(w * dtx_now, dots[c], 0.f);
+    w *= dA_now;
+    for (int j = c - 1; j >= 0; --j) {
+        const float d = de[j * kTileRows + r];
+        const float x = raw_to_float(xe, j * kTileRows + r, io_dtype);
+        hist = fmaf(w * (d * x), dots[j], hist);
+        w *= decay(Ah, d);
+    }
+    return make_float2(w, hist);
+}
 
 template <typename TS, int L>
 __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
@@ -57,10 +86,14 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     constexpr int NT = T::kThreads;
     extern __shared__ __align__(128) unsigned char smem[];
     const int len = p.rlen;
-    const ReplaySmem<TS, L> lay(len);
+    const int io = p.io_dtype == kF32 ? 4 : 2;
+    const ReplaySmem<TS, L> lay(len, io);
     TS *tile = reinterpret_cast<TS *>(smem + lay.tile);
-    float *sB = reinterpret_cast<float *>(smem + lay.bs);
+    unsigned char *xe = smem + lay.xe;
+    float *de = reinterpret_cast<float *>(smem + lay.de);
+    unsigned char *be = smem + lay.be;
     float *sC = reinterpret_cast<float *>(smem + lay.cs);
+    float *sBc = reinterpret_cast<float *>(smem + lay.bc);
     float *dots = reinterpret_cast<float *>(smem + lay.dots);
     float *rowa = reinterpret_cast<float *>(smem + lay.rowa);
     float *rowb = reinterpret_cast<float *>(smem + lay.rowb);
@@ -94,119 +127,129 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
     const int row0 = ptile * kTileRows;
     const int rows_here = min(kTileRows, p.P - row0);
     const int64_t head_row0 = static_cast<int64_t>(h) * p.P + row0;
+    // Everything the unit reads from the slot -- the checkpoint tile and each
+    // buffered entry's x rows, dt' rows and B -- is requested at once, as
+    // bulk asynchronous copies completing on one mbarrier.
+    const bool bulk_entries = p.rbulk != 0;
     if (tid == 0 && !pad) {
-        const uint32_t bytes = static_cast<uint32_t>(rows_here) * N * sizeof(TS);
+        uint32_t bytes = static_cast<uint32_t>(rows_here) * N * sizeof(TS);
+        if (bulk_entries) bytes += static_cast<uint32_t>(c) * (rows_here * (io + 4) + N * io);
         mbar_init(bar, 1);
         mbar_arrive_expect(bar, bytes);
-        bulk_load(tile, static_cast<const TS *>(p.state) + (s * p.H * p.P + head_row0) * N, bytes, bar);
+        bulk_load(tile, static_cast<const TS *>(p.state) + (s * p.H * p.P + head_row0) * N,
+                  static_cast<uint32_t>(rows_here) * N * sizeof(TS), bar);
+        if (bulk_entries) {
+            for (int j = 0; j < c; ++j) {
+                const int64_t e = ((s * len + j) * p.H + h) * static_cast<int64_t>(p.P) + row0;
+                bulk_load(xe + j * kTileRows * io, static_cast<const unsigned char *>(p.xbuf) + e * io,
+                          static_cast<uint32_t>(rows_here) * io, bar);
+                bulk_load(de + j * kTileRows, p.dtbuf + e, static_cast<uint32_t>(rows_here) * 4, bar);
+                const int64_t eb = ((s * len + j) * p.G + g) * static_cast<int64_t>(N);
+                bulk_load(be + j * N * io, static_cast<const unsigned char *>(p.Bbuf) + eb * io,
+                          static_cast<uint32_t>(N) * io, bar);
+            }
+        }
+    }
+    if (!pad && !bulk_entries) {
+        // Unaligned buffers: plain loads of the same entries.
+        for (int i = tid; i < c * rows_here; i += NT) {
+            const int j = i / rows_here, r = i % rows_here;
+            const int64_t e = ((s * len + j) * p.H + h) * static_cast<int64_t>(p.P) + row0 + r;
+            de[j * kTileRows + r] = __ldg(p.dtbuf + e);
+            if (io == 4)
+                reinterpret_cast<unsigned int *>(xe)[j * kTileRows + r] = load_bits<true>(p.xbuf, e);
+            else
+                reinterpret_cast<unsigned short *>(xe)[j * kTileRows + r] =
+                    static_cast<unsigned short>(load_bits<false>(p.xbuf, e));
+        }
+        for (int i = tid; i < c * N; i += NT) {
+            const int j = i / N, n = i % N;
+            const int64_t eb = ((s * len + j) * p.G + g) * static_cast<int64_t>(N) + n;
+            if (io == 4)
+                reinterpret_cast<unsigned int *>(be)[j * N + n] = load_bits<true>(p.Bbuf, eb);
+            else
+                reinterpret_cast<unsigned short *>(be)[j * N + n] = static_cast<unsigned short>(load_bits<false>(p.Bbuf, eb));
+        }
     }
 
-    // B of the entries and of the current token (entry c), C.
-    const int64_t bo = b * p.Bs[0] + g * p.Bs[1];
-    for (int i = tid; i < (c + 1) * N; i += NT) {
-        const int j = i / N, n = i % N;
-        float v;
-        if (j < c) {
-            const int64_t e = ((s * len + j) * p.G + g) * static_cast<int64_t>(N) + n;
-            v = bits_to_float(p.io_dtype == kF32 ? load_bits<true>(p.Bbuf, e) : load_bits<false>(p.Bbuf, e),
-                              p.io_dtype);
-        } else {
-            v = bits_to_float(p.io_dtype == kF32 ? load_bits<true>(p.B, bo + n * p.Bs[2])
-                                                 : load_bits<false>(p.B, bo + n * p.Bs[2]),
-                              p.io_dtype);
-        }
-        sB[j * N + n] = v;
-    }
-    const int64_t co = b * p.Cs[0] + g * p.Cs[1];
-    for (int n = tid; n < N; n += NT)
-        sC[n] = bits_to_float(p.io_dtype == kF32 ? load_bits<true>(p.C, co + n * p.Cs[2])
-                                                 : load_bits<false>(p.C, co + n * p.Cs[2]),
-                              p.io_dtype);
-    // Per row and entry: exp(A dt'_j) and dt'_j x_j.
+    // The current token: B, C, and the row scalars; its entry is appended
+    // when the buffer does not fill.
     const float Ah = __ldg(p.A + h);
     const float Dh = p.D ? __ldg(p.D + h) : 0.f;
     const float bias = p.dt_bias ? __ldg(p.dt_bias + h) : 0.f;
-    for (int i = tid; i < c * rows_here; i += NT) {
-        const int j = i / rows_here, r = i % rows_here;
-        const int64_t e = ((s * len + j) * p.H + h) * static_cast<int64_t>(p.P) + row0 + r;
-        const float d = __ldg(p.dtbuf + e);
-        const float x = bits_to_float(p.io_dtype == kF32 ? load_bits<true>(p.xbuf, e) : load_bits<false>(p.xbuf, e),
-                                      p.io_dtype);
-        rowa[j * kTileRows + r] = decay(Ah, d);
-        rowb[j * kTileRows + r] = d * x;
+    const int64_t bo = b * p.Bs[0] + g * p.Bs[1];
+    const int64_t co = b * p.Cs[0] + g * p.Cs[1];
+    const bool append_b = !fold && h % p.heads_per_group == 0 && ptile == 0;
+    for (int n = tid; n < N; n += NT) {
+        const uint32_t bb = io == 4 ? load_bits<true>(p.B, bo + n * p.Bs[2]) : load_bits<false>(p.B, bo + n * p.Bs[2]);
+        const uint32_t cb = io == 4 ? load_bits<true>(p.C, co + n * p.Cs[2]) : load_bits<false>(p.C, co + n * p.Cs[2]);
+        sBc[n] = bits_to_float(bb, p.io_dtype);
+        sC[n] = bits_to_float(cb, p.io_dtype);
+        if (append_b) {
+            const int64_t e = ((s * len + c) * p.G + g) * static_cast<int64_t>(N) + n;
+            if (io == 4)
+                static_cast<unsigned int *>(p.Bbuf)[e] = bb;
+            else
+                static_cast<unsigned short *>(p.Bbuf)[e] = static_cast<unsigned short>(bb);
+        }
     }
-    // The current token: row scalars, and its entry when it is buffered.
     for (int r = tid; r < rows_here; r += NT) {
         const int pr = row0 + r;
-        const uint32_t xb = p.io_dtype == kF32 ? load_bits<true>(p.x, b * p.xs[0] + h * p.xs[1] + pr * p.xs[2])
-                                               : load_bits<false>(p.x, b * p.xs[0] + h * p.xs[1] + pr * p.xs[2]);
-        const float dtv = bits_to_float(
-            p.dt_dtype == kF32 ? load_bits<true>(p.dt, b * p.dts[0] + h * p.dts[1] + pr * p.dts[2])
-                               : load_bits<false>(p.dt, b * p.dts[0] + h * p.dts[1] + pr * p.dts[2]),
-            p.dt_dtype);
-        float zv = 0.f;
-        if (p.z)
-            zv = bits_to_float(p.io_dtype == kF32 ? load_bits<true>(p.z, b * p.zs[0] + h * p.zs[1] + pr * p.zs[2])
-                                                  : load_bits<false>(p.z, b * p.zs[0] + h * p.zs[1] + pr * p.zs[2]),
-                               p.io_dtype);
-        const float4 q = row_scalars(RowInputs{dtv, bits_to_float(xb, p.io_dtype), zv}, Ah, bias, p.softplus,
-                                     p.z != nullptr);
-        rowq[r] = q;
-        rowa[c * kTileRows + r] = q.x;
-        rowb[c * kTileRows + r] = q.y;
+        const int64_t xo = b * p.xs[0] + h * p.xs[1] + pr * p.xs[2];
+        const int64_t dto = b * p.dts[0] + h * p.dts[1] + pr * p.dts[2];
+        const int64_t zo = b * p.zs[0] + h * p.zs[1] + pr * p.zs[2];
+        const uint32_t xb = io == 4 ? load_bits<true>(p.x, xo) : load_bits<false>(p.x, xo);
+        const uint32_t db = p.dt_dtype == kF32 ? load_bits<true>(p.dt, dto) : load_bits<false>(p.dt, dto);
+        const uint32_t zb = p.z ? (io == 4 ? load_bits<true>(p.z, zo) : load_bits<false>(p.z, zo)) : 0u;
+        const float dtv = bits_to_float(db, p.dt_dtype);
+        rowq[r] = row_scalars(RowInputs{dtv, bits_to_float(xb, p.io_dtype), bits_to_float(zb, p.io_dtype)}, Ah, bias,
+                              p.softplus, p.z != nullptr);
         if (!fold) {
             const int64_t e = ((s * len + c) * p.H + h) * static_cast<int64_t>(p.P) + pr;
             p.dtbuf[e] = processed_step(dtv, bias, p.softplus);
-            if (p.io_dtype == kF32)
+            if (io == 4)
                 static_cast<unsigned int *>(p.xbuf)[e] = xb;
             else
                 static_cast<unsigned short *>(p.xbuf)[e] = static_cast<unsigned short>(xb);
         }
     }
-    // The group's B is appended once, by the first head of the group.
-    if (!fold && h % p.heads_per_group == 0 && ptile == 0) {
-        for (int n = tid; n < N; n += NT) {
-            const int64_t e = ((s * len + c) * p.G + g) * static_cast<int64_t>(N) + n;
-            if (p.io_dtype == kF32)
-                static_cast<unsigned int *>(p.Bbuf)[e] = load_bits<true>(p.B, bo + n * p.Bs[2]);
-            else
-                static_cast<unsigned short *>(p.Bbuf)[e] =
-                    static_cast<unsigned short>(load_bits<false>(p.B, bo + n * p.Bs[2]));
-        }
-    }
     __syncthreads();
+    int timed_out = 0;
+    if (!pad && !mbar_wait_bounded(bar, 0)) timed_out = 1;
+    if (__syncthreads_or(timed_out)) {
+        if (tid == 0) flag(p.status, kDevTimeout);
+        return;
+    }
 
     if (!fold) {
-        // B_j . C for every entry and the current token: one warp (or the
+        // B_j . C for the entries and the current token: one warp (or the
         // whole CTA when it is narrower than a warp) per dot.
         constexpr int W = NT < 32 ? NT : 32;
         constexpr unsigned kMask = W == 32 ? 0xffffffffu : (1u << W) - 1u;
         const int warp = tid / W, wl = tid % W;
         for (int j = warp; j <= c; j += NT / W) {
             float acc = 0.f;
-            for (int n = wl; n < N; n += W) acc = fmaf(sB[j * N + n], sC[n], acc);
+            for (int n = wl; n < N; n += W)
+                acc = fmaf(j < c ? raw_to_float(be, j * N + n, p.io_dtype) : sBc[n], sC[n], acc);
 #pragma unroll
             for (int off = W / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(kMask, acc, off);
             if (wl == 0) dots[j] = acc;
         }
         __syncthreads();
-        // Readout coefficients of each row: walk the entries from the newest
-        // (the current token) to the oldest; w = gamma_{j+1:c}, and after the
-        // walk w = gamma_{0:c}, the weight of the checkpoint.
         for (int r = tid; r < rows_here; r += NT) {
-            float w = 1.f, hist = 0.f;
-            for (int j = c; j >= 0; --j) {
-                hist = fmaf(w * rowb[j * kTileRows + r], dots[j], hist);
-                w *= rowa[j * kTileRows + r];
-            }
-            rowg[r] = make_float2(w, hist);
+            const float4 q = rowq[r];
+            rowg[r] = readout_walk(c, r, Ah, q.x, q.y, de, xe, dots, p.io_dtype);
         }
-    }
-    int timed_out = 0;
-    if (!pad && !mbar_wait_bounded(bar, 0)) timed_out = 1;
-    if (__syncthreads_or(timed_out)) {
-        if (tid == 0) flag(p.status, kDevTimeout);
-        return;
+        __syncthreads();
+    } else if (c > 0) {
+        // Decay and input term of every entry and row, for the fold.
+        for (int i = tid; i < c * rows_here; i += NT) {
+            const int j = i / rows_here, r = i % rows_here;
+            const float d = de[j * kTileRows + r];
+            rowa[j * kTileRows + r] = decay(Ah, d);
+            rowb[j * kTileRows + r] = d * raw_to_float(xe, j * kTileRows + r, p.io_dtype);
+        }
+        __syncthreads();
     }
 
     const int lane = tid % L;
@@ -231,13 +274,14 @@ __global__ void __launch_bounds__(Tile<TS, L>::kThreads)
             float bv[kElemsPerThread];
             // The buffered steps in order, as the plain update made them ...
             for (int e = 0; e < c; ++e) {
-                T::gather(sB + e * N, lane, bv);
+#pragma unroll
+                for (int i = 0; i < kElemsPerThread; ++i) bv[i] = raw_to_float(be, e * N + T::elem(lane, i), p.io_dtype);
                 const float a = rowa[e * kTileRows + rq], dx = rowb[e * kTileRows + rq];
 #pragma unroll
                 for (int i = 0; i < kElemsPerThread; ++i) sv[i] = fmaf(sv[i], a, dx * bv[i]);
             }
             // ... then the current token, whose state y is read from.
-            T::gather(sB + c * N, lane, bv);
+            T::gather(sBc, lane, bv);
             const float sum = row_sum<L>(update_elems(sv, bv, cv, q.x, q.y));
             y = output(sum, Dh, q.z, q.w);
             if (live && !pad) T::store_row(ckpt + rr * N, lane, sv);
@@ -262,7 +306,7 @@ static cudaError_t smem_opt_in() {
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
     e = cudaFuncSetAttribute(ssu_replay_kernel<TS, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ReplaySmem<TS, L>(kMaxReplayLen).bytes);
+                             ReplaySmem<TS, L>(kMaxReplayLen, 4).bytes);
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
     return e;
 }
@@ -273,7 +317,7 @@ static cudaError_t launch_t(const KParams &p, int64_t batch, cudaStream_t stream
     if (e != cudaSuccess) return e;
     const int64_t units = batch * p.H * p.ptiles;
     ssu_replay_kernel<TS, L><<<static_cast<unsigned>(units), Tile<TS, L>::kThreads,
-                               ReplaySmem<TS, L>(p.rlen).bytes, stream>>>(p);
+                               ReplaySmem<TS, L>(p.rlen, p.io_dtype == kF32 ? 4 : 2).bytes, stream>>>(p);
     return cudaGetLastError();
 }
 
