@@ -53,7 +53,7 @@ DESCRIPTIONS = {
 }
 KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
-                  "replay": ["ssu_replay.cu", "ssu_device.cuh", "ssu_internal.h"]}
+                  "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"]}
 
 
 # --------------------------------------------------------------------------

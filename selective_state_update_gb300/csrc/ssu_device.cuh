@@ -352,14 +352,20 @@ struct RowInputs {
 static __device__ __noinline__ float processed_step(float dt, float bias, int softplus) {
     return step_size(dt, bias, softplus);
 }
-static __device__ __noinline__ float decay(float Ah, float d) { return expf(Ah * d); }
+// exp(A dt') with the product rounded on its own (never fused into an
+// FMA), so that an inlined copy gives the bits of the call.
+__device__ __forceinline__ float decay_inline(float Ah, float d) { return expf(__fmul_rn(Ah, d)); }
+static __device__ __noinline__ float decay(float Ah, float d) { return decay_inline(Ah, d); }
 
-// Per-row scalars {dA, dt' x, x, gate}: gate is the factor y is multiplied
-// by, silu(z) = z / (1 + e^-z) with a z input, 1 without.  Not inlined: every
+// The factor y is multiplied by: silu(z) = z / (1 + e^-z) with a z input,
+// 1 without.  Not inlined, like the two above.
+static __device__ __noinline__ float silu_gate(float z, int has_z) { return has_z ? z / (1.f + expf(-z)) : 1.f; }
+
+// Per-row scalars {dA, dt' x, x, gate}, from the calls above only: every
 // kernel gets exactly the same instructions, hence the same bits.
 static __device__ __noinline__ float4 row_scalars(RowInputs in, float Ah, float bias, int softplus, int has_z) {
     const float d = processed_step(in.dt, bias, softplus);
-    const float gate = has_z ? in.z / (1.f + expf(-in.z)) : 1.f;
+    const float gate = silu_gate(in.z, has_z);
     return make_float4(decay(Ah, d), d * in.x, in.x, gate);
 }
 
@@ -435,5 +441,67 @@ __device__ __forceinline__ bool slot_ok(const KParams &p, int64_t s) {
     flag(p.status, kDevBadSlot);
     return false;
 }
+
+// Everything the producer needs from global memory for one unit, loaded into
+// registers one unit ahead so that the loads are in flight while the producer
+// stages the previous unit or waits for a free stage.  The loads are issued
+// as raw bits, back to back, and converted only when the unit is staged.
+template <typename TS, int L>
+struct UnitOperands {
+    static constexpr int kN = Tile<TS, L>::kN;
+    static constexpr int kPerB = (kN + 31) / 32;
+    static constexpr int kPerRow = (kTileRows + 31) / 32;
+    UnitCoords c;
+    int64_t rs, ws;  // lane 0: raw slots (valid when entries_ok)
+    bool entries_ok;
+    uint32_t b[kPerB], cc[kPerB];
+    uint32_t dt[kPerRow], x[kPerRow], z[kPerRow];
+    float Ah, bias, Dh;
+
+    template <bool WIO, bool WDT>
+    __device__ __forceinline__ void load_operands(const KParams &p, int lane) {
+        const int64_t bo = c.b * p.Bs[0] + c.g * p.Bs[1];
+        const int64_t co = c.b * p.Cs[0] + c.g * p.Cs[1];
+#pragma unroll
+        for (int i = 0; i < kPerB; ++i) {
+            const int n = lane + 32 * i;
+            if (n < kN) {
+                b[i] = load_bits<WIO>(p.B, bo + n * p.Bs[2]);
+                cc[i] = load_bits<WIO>(p.C, co + n * p.Cs[2]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kPerRow; ++i) {
+            const int pr = c.row0 + lane + 32 * i;
+            if (lane + 32 * i < c.rows_here) {
+                dt[i] = load_bits<WDT>(p.dt, c.b * p.dts[0] + c.h * p.dts[1] + pr * p.dts[2]);
+                x[i] = load_bits<WIO>(p.x, c.b * p.xs[0] + c.h * p.xs[1] + pr * p.xs[2]);
+                z[i] = p.z ? load_bits<WIO>(p.z, c.b * p.zs[0] + c.h * p.zs[1] + pr * p.zs[2]) : 0u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void load(const KParams &p, const UnitCoords &cu, int lane) {
+        c = cu;
+        entries_ok = true;
+        rs = ws = 0;
+        if (lane == 0) {
+            entries_ok = table_slot(p, p.rd, c.b, 0, c.b, c.b, &rs);
+            if (p.wr.entries != nullptr)
+                entries_ok = table_slot(p, p.wr, c.b, 0, c.b, c.b, &ws) && entries_ok;
+        }
+        const bool wio = p.io_dtype == kF32, wdt = p.dt_dtype == kF32;
+        if (wio) {
+            if (wdt) load_operands<true, true>(p, lane);
+            else load_operands<true, false>(p, lane);
+        } else {
+            if (wdt) load_operands<false, true>(p, lane);
+            else load_operands<false, false>(p, lane);
+        }
+        Ah = __ldg(p.A + c.h);
+        bias = p.dt_bias ? __ldg(p.dt_bias + c.h) : 0.f;
+        Dh = p.D ? __ldg(p.D + c.h) : 0.f;
+    }
+};
 
 }  // namespace ssu

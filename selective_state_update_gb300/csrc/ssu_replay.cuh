@@ -1,0 +1,759 @@
+// ssu_replay.cuh -- decode on the checkpoint + buffer form of the state.
+//
+// Article "ReplaySSM: Cache SSM Inputs, Not State", section 核心做法: the
+// state of a slot is a checkpoint plus the inputs (v, dt', k) = (x, dt', B) of
+// the steps since the last fold.  Unrolled, the state after the current step
+// c is
+//     S_c = gamma_{0:c} S_ckpt + sum_{j<=c} gamma_{j+1:c} dt'_j x_j B_j^T,
+//     gamma_{i:c} = prod_{m=i..c} exp(A dt'_m),
+// so y = S_c . C can be read out without forming S_c:
+//     y = gamma_{0:c} (S_ckpt . C) + sum_j gamma_{j+1:c} dt'_j x_j (B_j . C).
+// A step that does not fill the buffer does exactly that and appends its
+// inputs; the checkpoint is read but not written.  The step that fills it
+// folds the entries into the checkpoint in order (the plain update, carried in
+// fp32, with the plain kernels' decays bit for bit), reads y out of the result
+// and writes the checkpoint back once.  Section 数据与边界: the checkpoint is
+// read every step and written once every L steps, so the state traffic per
+// step drops from a read and a write to about a read.
+//
+// Work unit: (sequence b, head h, tile of kTileRows dim rows), numbered as in
+// the one-token kernel.  The kernel is persistent and warp-specialised, with a
+// ring of shared-memory stages per CTA:
+//   producer warps  one unit each in turn, operands loaded a unit ahead:
+//                   resolve the slot and the buffered count c, write the
+//                   count for the next step, compute the current token's row
+//                   scalars {dA, dt' x, x, gate} into the stage, append its
+//                   entry (x, dt', and B once per group) when the buffer does
+//                   not fill, stage B and C, and request the checkpoint tile
+//                   and the c buffered entries of the tile (x rows, dt' rows,
+//                   B of the group) as bulk asynchronous copies (TMA engine)
+//                   completing on the stage's "full" mbarrier;
+//   consumer warps  first what is independent across rows and entries (B_j . C
+//                   dots, one warp per dot; each entry's decay and input term
+//                   per row), then either the readout (the walk over the
+//                   entries, split in contiguous parts over the threads of a
+//                   row; y from the checkpoint rows) or the fold (entries in
+//                   order, then the current token; y; the tile back into the
+//                   stage, from where one thread stores it to the checkpoint
+//                   with a bulk copy).  A stage is released on its "empty"
+//                   mbarrier once read, or once its store has read it out.
+// The kernel is compiled per dtype of the 16/32-bit operands (IO), which
+// keeps the consumer's code small and free of dtype branches.
+#pragma once
+
+#include <atomic>
+
+#include "ssu_device.cuh"
+
+namespace ssu {
+
+#ifndef SSU_REPLAY_CTAS
+#define SSU_REPLAY_CTAS 0
+#endif
+#ifndef SSU_REPLAY_MAX_STAGES
+#define SSU_REPLAY_MAX_STAGES 6
+#endif
+
+template <typename TS, int L>
+struct ReplayPipe {
+    static constexpr int kN = Tile<TS, L>::kN;
+    static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
+    static constexpr int kConsumerWarps = (Tile<TS, L>::kThreads + 31) / 32;
+    static constexpr int kConsumers = 32 * kConsumerWarps;
+    // The readout walk of a row is split over kParts threads (contiguous
+    // ranges of entries), rows over kRowThreads threads.
+    static constexpr int kParts = kConsumers > kTileRows ? kConsumers / kTileRows : 1;
+    static constexpr int kRowThreads = kConsumers / kParts;
+    // Producer warps take units in turn; a producer waits for its stage by
+    // the parity of the "empty" phase, which is unambiguous only with no more
+    // producers than stages, so a one-stage ring runs one producer.
+    static constexpr int kProducerWarps = 2;
+    static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+    // Dynamic shared memory an SM can give its CTAs (228 KB less 1 KB per CTA).
+    static constexpr int kSmemPerSm = 222 * 1024;
+    // Register budget: two CTAs per SM where a tile and a few KB of entries
+    // fit twice in half of the SM's shared memory and two CTAs still leave
+    // 128 registers a thread.
+    static constexpr int kMinCtas =
+        (kSmemPerSm / 2 - 1024) / (kTileBytes + 4096) >= 2 && 65536 / (2 * kThreads) >= 128 ? 2 : 1;
+};
+
+// Per-stage header written by the producer.
+struct ReplayHeader {
+    int64_t slot;
+    int32_t flags;  // kR* bits
+    int32_t c;      // buffered entries of the slot (0 for a pad slot)
+    float Dh, Ah;
+    int32_t reserved[2];
+};
+enum : int32_t { kRValid = 1, kRSeeded = 2, kRFold = 4 };
+
+// Most threads a row's readout walk is split over (see ReplayPipe::kParts).
+constexpr int kMaxWalkParts = 4;
+
+// Shared-memory layout, fixed per launch by the buffer length and the size of
+// the 16/32-bit operands.  A stage holds the checkpoint tile, up to len - 1
+// buffered entries as stored (x rows and dt' rows of the tile, B of the
+// group), the current token's B and C as fp32, the row scalars and the
+// header.  After the ring: the CTA's scratch for the unit being computed (B .
+// C dots; per-entry decays and input terms; the parts of each row's readout
+// walk) and the mbarriers.
+struct ReplayLayout {
+    int xe, de, be, bc, cs, rowq, hd, stage;
+    int stages, producers, dots, rowa, rowb, rowg, bars, bytes, ctas;
+
+    __host__ __device__ static int up(int v) { return (v + 127) / 128 * 128; }
+
+    __host__ __device__ void place(int tile_bytes, int n, int len, int io) {
+        const int ent = len - 1;
+        xe = up(tile_bytes);                 // io  [ent][kTileRows]
+        de = up(xe + ent * kTileRows * io);  // f32 [ent][kTileRows]
+        be = up(de + ent * kTileRows * 4);   // io  [ent][n]
+        bc = up(be + ent * n * io);          // f32 [n]
+        cs = bc + n * 4;                     // f32 [n]
+        rowq = up(cs + n * 4);               // f32x4 [kTileRows]
+        hd = rowq + kTileRows * 16;          // ReplayHeader
+        stage = up(hd + static_cast<int>(sizeof(ReplayHeader)));
+    }
+    // Ring of `stages` stages followed by the scratch and the barriers.
+    __host__ __device__ void finish(int len) {
+        dots = stages * stage;                                 // f32 [len]
+        rowa = up(dots + len * 4);                             // f32 [len - 1][kTileRows]
+        rowb = up(rowa + (len - 1) * kTileRows * 4);           // f32 [len - 1][kTileRows]
+        rowg = up(rowb + (len - 1) * kTileRows * 4);           // f32x2 [kMaxWalkParts][kTileRows]
+        bars = up(rowg + kMaxWalkParts * kTileRows * 8);       // u64 full[stages], empty[stages]
+        bytes = bars + 2 * 8 * stages;
+    }
+    static int scratch(int len) {
+        return up(len * 4) + 2 * up((len - 1) * kTileRows * 4) + up(kMaxWalkParts * kTileRows * 8) +
+               2 * 8 * SSU_REPLAY_MAX_STAGES;
+    }
+    // Two CTAs per SM when registers allow two (max_ctas) and each still gets
+    // a ring of two stages, else one CTA with as many stages as fit (at most
+    // SSU_REPLAY_MAX_STAGES; a single stage -- fp32 checkpoints of dstate 256
+    // with long fp32 buffers -- runs without overlap).  Returns false when
+    // not even one stage fits.
+    bool choose(int tile_bytes, int n, int len, int io, int smem_per_sm, int max_ctas, int max_producers) {
+        place(tile_bytes, n, len, io);
+        const int sc = scratch(len);
+        auto fit = [&](int k) { return (smem_per_sm / k - 1024 - sc) / stage; };
+        ctas = SSU_REPLAY_CTAS > 0 && SSU_REPLAY_CTAS <= max_ctas && fit(SSU_REPLAY_CTAS) >= 2
+                   ? SSU_REPLAY_CTAS
+                   : (max_ctas >= 2 && fit(2) >= 2 ? 2 : 1);
+        stages = fit(ctas);
+        if (stages > SSU_REPLAY_MAX_STAGES) stages = SSU_REPLAY_MAX_STAGES;
+        if (stages < 1) return false;
+        producers = stages < max_producers ? stages : max_producers;
+        finish(len);
+        return true;
+    }
+};
+
+// Element i of a buffer stored in the io dtype IO, as fp32.
+template <int IO>
+__device__ __forceinline__ float io_at(const unsigned char *base, int i) {
+    if constexpr (IO == kF32)
+        return reinterpret_cast<const float *>(base)[i];
+    else
+        return bits_to_float(reinterpret_cast<const unsigned short *>(base)[i], IO);
+}
+
+// This thread's 16 values of one buffered B entry (stored in the io dtype),
+// as fp32, in the element layout of Tile::gather: vector loads of each
+// thread's contiguous chunks.
+template <typename TS, int L, int IO>
+__device__ __forceinline__ void gather_entry(const unsigned char *row, int lane, float *v) {
+    using T = Tile<TS, L>;
+    constexpr int V = T::kVec;
+#pragma unroll
+    for (int k = 0; k < T::kChunks; ++k) {
+        const int off = (lane + L * k) * V;
+        if constexpr (IO == kF32) {
+#pragma unroll
+            for (int q = 0; q < V / 4; ++q) {
+                const float4 f = reinterpret_cast<const float4 *>(row)[off / 4 + q];
+                v[k * V + 4 * q + 0] = f.x;
+                v[k * V + 4 * q + 1] = f.y;
+                v[k * V + 4 * q + 2] = f.z;
+                v[k * V + 4 * q + 3] = f.w;
+            }
+        } else {
+            uint32_t w[V / 2];
+            if constexpr (V == 8) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(row + off * 2);
+                w[0] = u.x;
+                w[1] = u.y;
+                w[2] = u.z;
+                w[3] = u.w;
+            } else {
+                const uint2 u = *reinterpret_cast<const uint2 *>(row + off * 2);
+                w[0] = u.x;
+                w[1] = u.y;
+            }
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                v[k * V + 2 * i] = bits_to_float(w[i] & 0xffffu, IO);
+                v[k * V + 2 * i + 1] = bits_to_float(w[i] >> 16, IO);
+            }
+        }
+    }
+}
+
+// B_j . C for the c buffered entries (j < c) and the current token (j = c):
+// one warp per dot (lanes over consecutive elements: no bank conflicts), kQ
+// dots per warp interleaved, all kWarps consumer warps taking part.
+template <int N, int kWarps, int IO>
+__device__ __forceinline__ void entry_dots(int c, const unsigned char *be, const float *sB, const float *sC,
+                                           float *dots, int warp, int wl) {
+    constexpr int kPer = (N + 31) / 32;
+    constexpr int kQ = 4;
+    float cv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) cv[i] = wl + 32 * i < N ? sC[wl + 32 * i] : 0.f;
+    for (int base = 0; base <= c; base += kQ * kWarps) {
+        float acc[kQ];
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+            const int j = base + warp + q * kWarps;
+            acc[q] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int n = wl + 32 * i;
+                if (n < N) {
+                    const float bvl = j < c ? io_at<IO>(be, j * N + n) : (j == c ? sB[n] : 0.f);
+                    acc[q] = fmaf(bvl, cv[i], acc[q]);
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], off);
+        }
+        if (wl == 0) {
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) {
+                const int j = base + warp + q * kWarps;
+                if (j <= c) dots[j] = acc[q];
+            }
+        }
+    }
+}
+
+// Each buffered entry's decay exp(A dt'_j) and input term dt'_j x_j for every
+// row of the tile, into rowa / rowb ([entry][kTileRows]); loads of a batch
+// issued before its arithmetic.  A fold (kExact) takes the decays from the
+// plain kernels' function, so that the folded state is theirs bit for bit; a
+// readout, which only produces y, takes the fast exponential.
+template <int kThreads, int IO, bool kExact>
+__device__ __forceinline__ void entry_terms(int c, int rows, float Ah, const float *de, const unsigned char *xe,
+                                            float *rowa, float *rowb, int tid) {
+    constexpr int kB = 4;
+    const int total = c * kTileRows;
+    for (int i0 = tid; i0 < total; i0 += kB * kThreads) {
+        float d[kB], x[kB];
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+            const int i = i0 + q * kThreads;
+            const bool ok = i < total && i % kTileRows < rows;
+            d[q] = ok ? de[i] : 0.f;
+            x[q] = ok ? io_at<IO>(xe, i) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+            const int i = i0 + q * kThreads;
+            if (i < total && i % kTileRows < rows) {
+                rowa[i] = kExact ? decay(Ah, d[q]) : __expf(Ah * d[q]);
+                rowb[i] = d[q] * x[q];
+            }
+        }
+    }
+}
+
+// Part `part` of the readout walk of row r over entries c (the current token:
+// decay dA, term dtx) down to 0, split into kParts contiguous ranges, part 0
+// the newest.  For its range [lo, hi] it returns {prod of the decays, sum of
+// each term weighted by B_j . C and by the decays of the newer entries of the
+// range}; the parts combine newest first (see the readout).
+template <int kParts>
+__device__ __forceinline__ float2 walk_part(int c, int part, int r, float dA, float dtx, const float *rowa,
+                                            const float *rowb, const float *dots) {
+    const int per = (c + kParts) / kParts;  // ceil((c + 1) / kParts)
+    const int hi = c - part * per;
+    const int lo = hi - per + 1 > 0 ? hi - per + 1 : 0;
+    float hist = 0.f, w = 1.f;
+    int j = hi;
+    if (j == c && j >= lo) {
+        hist = fmaf(w * dtx, dots[c], hist);
+        w *= dA;
+        --j;
+    }
+    for (; j - 3 >= lo; j -= 4) {
+        float a[4], bb[4], dd[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            a[t] = rowa[(j - t) * kTileRows + r];
+            bb[t] = rowb[(j - t) * kTileRows + r];
+            dd[t] = dots[j - t];
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            hist = fmaf(w * bb[t], dd[t], hist);
+            w *= a[t];
+        }
+    }
+    for (; j >= lo; --j) {
+        hist = fmaf(w * rowb[j * kTileRows + r], dots[j], hist);
+        w *= rowa[j * kTileRows + r];
+    }
+    return make_float2(w, hist);
+}
+
+// The operands of one unit plus its slot's buffered count (lane 0).
+template <typename TS, int L>
+struct ReplayOperands : UnitOperands<TS, L> {
+    int cnt;
+    __device__ __forceinline__ void load(const KParams &p, const UnitCoords &cu, int lane) {
+        UnitOperands<TS, L>::load(p, cu, lane);
+        cnt = lane == 0 ? __ldg(p.cnt_in + cu.b) : 0;
+    }
+};
+
+// Stage one unit (see the file comment).  Returns false on a timed-out wait.
+template <typename TS, int L, int IO>
+__device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLayout &lay,
+                                               const ReplayOperands<TS, L> &op, int k, unsigned char *smem,
+                                               uint64_t *full, uint64_t *empty, int lane) {
+    constexpr int N = ReplayPipe<TS, L>::kN;
+    constexpr int io = IO == kF32 ? 4 : 2;
+    const int S = lay.stages;
+    const int s = k % S;
+    const int round = k / S;
+    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1)) {
+        if (lane == 0) flag(p.status, kDevTimeout);
+        return false;
+    }
+    unsigned char *base = smem + s * lay.stage;
+    ReplayHeader *hd = reinterpret_cast<ReplayHeader *>(base + lay.hd);
+    float *sB = reinterpret_cast<float *>(base + lay.bc);
+    float *sC = reinterpret_cast<float *>(base + lay.cs);
+    float4 *rowq = reinterpret_cast<float4 *>(base + lay.rowq);
+    const int len = p.rlen;
+    const UnitCoords &cu = op.c;
+
+    int32_t flags = 0, c = 0;
+    if (lane == 0) {
+        if (op.entries_ok && slot_ok(p, op.rs)) {
+            if (op.rs == p.pad) {
+                flags = kRValid | kRFold;  // zero state, nothing buffered, nothing written
+            } else if (op.cnt < 0 || op.cnt >= len) {
+                flag(p.status, kDevBadCount);
+            } else {
+                c = op.cnt;
+                flags = kRValid | kRSeeded | (c + 1 == len ? kRFold : 0);
+            }
+        }
+        if ((flags & kRValid) && cu.h == 0 && cu.row0 == 0) p.cnt_out[cu.b] = (flags & kRFold) ? 0 : c + 1;
+        hd->slot = op.rs;
+        hd->flags = flags;
+        hd->c = c;
+        hd->Dh = op.Dh;
+        hd->Ah = op.Ah;
+    }
+    flags = __shfl_sync(0xffffffffu, flags, 0);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    const int64_t rs = __shfl_sync(0xffffffffu, op.rs, 0);
+    const bool append = (flags & kRValid) && !(flags & kRFold);
+
+#pragma unroll
+    for (int i = 0; i < UnitOperands<TS, L>::kPerB; ++i) {
+        const int n = lane + 32 * i;
+        if (n < N) {
+            sB[n] = bits_to_float(op.b[i], IO);
+            sC[n] = bits_to_float(op.cc[i], IO);
+            if (append && cu.h % p.heads_per_group == 0 && cu.row0 == 0) {
+                const int64_t e = ((rs * len + c) * p.G + cu.g) * static_cast<int64_t>(N) + n;
+                if constexpr (io == 4)
+                    static_cast<unsigned int *>(p.Bbuf)[e] = op.b[i];
+                else
+                    static_cast<unsigned short *>(p.Bbuf)[e] = static_cast<unsigned short>(op.b[i]);
+            }
+        }
+    }
+    // The current token's row scalars, from the same calls the plain kernels
+    // make (bit-identical), and its buffered entry.
+#pragma unroll
+    for (int i = 0; i < UnitOperands<TS, L>::kPerRow; ++i) {
+        const int r = lane + 32 * i;
+        if (r < cu.rows_here && (flags & kRValid)) {
+            const float xv = bits_to_float(op.x[i], IO);
+            const float d = processed_step(bits_to_float(op.dt[i], p.dt_dtype), op.bias, p.softplus);
+            rowq[r] = make_float4(decay(op.Ah, d), d * xv, xv, silu_gate(bits_to_float(op.z[i], IO), p.z != nullptr));
+            if (append) {
+                const int64_t e = ((rs * len + c) * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + r;
+                p.dtbuf[e] = d;
+                if constexpr (io == 4)
+                    static_cast<unsigned int *>(p.xbuf)[e] = op.x[i];
+                else
+                    static_cast<unsigned short *>(p.xbuf)[e] = static_cast<unsigned short>(op.x[i]);
+            }
+        }
+    }
+
+    if (!(flags & kRSeeded)) {
+        mbar_arrive(&full[s]);
+        return true;
+    }
+    unsigned char *xe = base + lay.xe;
+    float *de = reinterpret_cast<float *>(base + lay.de);
+    unsigned char *be = base + lay.be;
+    const int rows = cu.rows_here;
+    const bool bulk_entries = p.rbulk != 0;
+    if (!bulk_entries) {
+        // Buffers not 16-byte aligned: plain loads of the same entries.
+        for (int i = lane; i < c * rows; i += 32) {
+            const int j = i / rows, r = i % rows;
+            const int64_t e = ((rs * len + j) * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + r;
+            de[j * kTileRows + r] = __ldg(p.dtbuf + e);
+            if constexpr (io == 4)
+                reinterpret_cast<unsigned int *>(xe)[j * kTileRows + r] = load_bits<true>(p.xbuf, e);
+            else
+                reinterpret_cast<unsigned short *>(xe)[j * kTileRows + r] =
+                    static_cast<unsigned short>(load_bits<false>(p.xbuf, e));
+        }
+        for (int i = lane; i < c * N; i += 32) {
+            const int j = i / N, n = i % N;
+            const int64_t e = ((rs * len + j) * p.G + cu.g) * static_cast<int64_t>(N) + n;
+            if constexpr (io == 4)
+                reinterpret_cast<unsigned int *>(be)[j * N + n] = load_bits<true>(p.Bbuf, e);
+            else
+                reinterpret_cast<unsigned short *>(be)[j * N + n] = static_cast<unsigned short>(load_bits<false>(p.Bbuf, e));
+        }
+    }
+    // The checkpoint tile and (aligned buffers) every buffered entry, as bulk
+    // copies; lane 0 registers the total before any copy can complete.
+    const uint32_t tile_bytes = static_cast<uint32_t>(rows) * N * sizeof(TS);
+    uint32_t bytes = tile_bytes;
+    if (bulk_entries) bytes += static_cast<uint32_t>(c) * (rows * (io + 4) + N * io);
+    if (lane == 0) mbar_arrive_expect(&full[s], bytes);
+    __syncwarp();
+    if (lane == 0)
+        bulk_load(base, static_cast<const TS *>(p.state) + ((rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0) * N,
+                  tile_bytes, &full[s]);
+    if (bulk_entries) {
+        for (int j = lane; j < c; j += 32) {
+            const int64_t e = ((rs * len + j) * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0;
+            bulk_load(xe + j * kTileRows * io, static_cast<const unsigned char *>(p.xbuf) + e * io,
+                      static_cast<uint32_t>(rows) * io, &full[s]);
+            bulk_load(de + j * kTileRows, p.dtbuf + e, static_cast<uint32_t>(rows) * 4, &full[s]);
+            const int64_t eb = ((rs * len + j) * p.G + cu.g) * static_cast<int64_t>(N);
+            bulk_load(be + j * N * io, static_cast<const unsigned char *>(p.Bbuf) + eb * io,
+                      static_cast<uint32_t>(N) * io, &full[s]);
+        }
+    }
+    if (lane != 0) mbar_arrive(&full[s]);
+    return true;
+}
+
+// Producer warp `w` stages the CTA's units k = w, w + P, w + 2P, ...
+// (P = lay.producers), i.e. global units blockIdx.x + k * gridDim.x.
+template <typename TS, int L, int IO>
+__device__ __forceinline__ void replay_producer(const KParams &p, const ReplayLayout &lay, int64_t units,
+                                                unsigned char *smem, uint64_t *full, uint64_t *empty, int w) {
+    const int P = lay.producers;
+    if (w >= P) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t step = static_cast<int64_t>(P) * gridDim.x;
+    ReplayOperands<TS, L> a, b;
+    int64_t u = blockIdx.x + static_cast<int64_t>(w) * gridDim.x;
+    UnitWalker walk(p, u, step);
+    if (u < units) a.load(p, walk.coords(p), lane);
+    for (int k = w; u < units; k += 2 * P, u += 2 * step) {
+        walk.advance(p);
+        if (u + step < units) b.load(p, walk.coords(p), lane);
+        if (!produce_replay<TS, L, IO>(p, lay, a, k, smem, full, empty, lane)) return;
+        if (u + step >= units) break;
+        walk.advance(p);
+        if (u + 2 * step < units) a.load(p, walk.coords(p), lane);
+        if (!produce_replay<TS, L, IO>(p, lay, b, k + P, smem, full, empty, lane)) return;
+    }
+}
+
+template <typename TS, int L, int IO>
+__device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLayout &lay, int64_t units,
+                                                unsigned char *smem, uint64_t *full, uint64_t *empty) {
+    using T = Tile<TS, L>;
+    using PS = ReplayPipe<TS, L>;
+    constexpr int N = PS::kN;
+    constexpr int kConsumers = PS::kConsumers;
+    constexpr int kParts = PS::kParts;
+    constexpr int io = IO == kF32 ? 4 : 2;
+    static_assert(kParts <= kMaxWalkParts, "walk split over more parts than the scratch holds");
+    const int S = lay.stages;
+    const int tid = threadIdx.x;
+    const bool active = tid < T::kThreads;
+    const int lane = tid % L;
+    const int slot_row = tid / L;
+    const int warp = tid / 32, wl = tid % 32;
+    float *dots = reinterpret_cast<float *>(smem + lay.dots);
+    float *rowa = reinterpret_cast<float *>(smem + lay.rowa);
+    float *rowb = reinterpret_cast<float *>(smem + lay.rowb);
+    float2 *rowg = reinterpret_cast<float2 *>(smem + lay.rowg);
+    int pending = -1;  // stage whose checkpoint store may still be reading it (thread 0)
+    int k = 0;
+    UnitWalker walk(p, blockIdx.x, gridDim.x);
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++k, walk.advance(p)) {
+        const int s = k % S;
+        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1);
+        if (barrier_or(1, kConsumers, !ok)) {  // a wait gave up: every consumer stops here
+            if (tid == 0) {
+                flag(p.status, kDevTimeout);
+                bulk_wait_all();
+            }
+            return;
+        }
+        unsigned char *base = smem + s * lay.stage;
+        const ReplayHeader *hd = reinterpret_cast<const ReplayHeader *>(base + lay.hd);
+        const int32_t flags = hd->flags;
+        const bool fold = (flags & kRFold) != 0;
+        const bool seeded = (flags & kRSeeded) != 0;
+        const bool stores = (flags & kRValid) && fold && seeded;
+        const UnitCoords cu = walk.coords(p);
+        if (flags & kRValid) {
+            const int c = hd->c;
+            const int rows = cu.rows_here;
+            const float Ah = hd->Ah, Dh = hd->Dh;
+            TS *tile = reinterpret_cast<TS *>(base);
+            const unsigned char *xe = base + lay.xe;
+            const float *de = reinterpret_cast<const float *>(base + lay.de);
+            const unsigned char *be = base + lay.be;
+            const float *sB = reinterpret_cast<const float *>(base + lay.bc);
+            const float *sC = reinterpret_cast<const float *>(base + lay.cs);
+            const float4 *rowq = reinterpret_cast<const float4 *>(base + lay.rowq);
+            float cv[kElemsPerThread];
+            if (active) T::gather(sC, lane, cv);
+            if (!fold) {
+                entry_dots<N, PS::kConsumerWarps, IO>(c, be, sB, sC, dots, warp, wl);
+                entry_terms<kConsumers, IO, false>(c, rows, Ah, de, xe, rowa, rowb, tid);
+                named_barrier(1, kConsumers);
+                // The walk: part tid / kRowThreads of rows tid % kRowThreads, ...
+                const int part = tid / PS::kRowThreads;
+                for (int r = tid % PS::kRowThreads; r < rows; r += PS::kRowThreads) {
+                    const float4 q = rowq[r];
+                    rowg[part * kTileRows + r] = walk_part<kParts>(c, part, r, q.x, q.y, rowa, rowb, dots);
+                }
+                named_barrier(1, kConsumers);
+                if (active) {
+                    // ... and the readout: y = gamma_{0:c} (S_ckpt . C) + the
+                    // history term, gated; all rows first, then the stores.
+                    float yv[kRowsPerThread];
+#pragma unroll
+                    for (int j = 0; j < kRowsPerThread; ++j) {
+                        const int rr = slot_row + j * kRowSlots;  // row within the tile
+                        const int rq = rr < rows ? rr : 0;
+                        float sv[kElemsPerThread];
+                        T::load_row_smem(tile + rq * N, lane, sv);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
+                        const float sum = row_sum<L>(acc);
+                        // Parts newest first: hist += w * hist_part, w *= w_part.
+                        float wgt = 1.f, hist = 0.f;
+#pragma unroll
+                        for (int q = 0; q < kParts; ++q) {
+                            const float2 g = rowg[q * kTileRows + rq];
+                            hist = fmaf(wgt, g.y, hist);
+                            wgt *= g.x;
+                        }
+                        const float4 q = rowq[rq];
+                        yv[j] = output(fmaf(wgt, sum, hist), Dh, q.z, q.w);
+                    }
+                    if (lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < kRowsPerThread; ++j) {
+                            const int rr = slot_row + j * kRowSlots;
+                            if (rr < rows)
+                                store_small(p.y, cu.b * p.ys[0] + cu.h * p.ys[1] + (cu.row0 + rr) * p.ys[2], IO,
+                                            yv[j]);
+                        }
+                    }
+                }
+            } else {
+                if (c > 0) {
+                    entry_terms<kConsumers, IO, true>(c, rows, Ah, de, xe, rowa, rowb, tid);
+                    named_barrier(1, kConsumers);
+                }
+                if (active) {
+                    float bv[kElemsPerThread];
+                    for (int j = 0; j < kRowsPerThread; ++j) {
+                        const int rr = slot_row + j * kRowSlots;
+                        const bool live = rr < rows;
+                        const int rq = live ? rr : 0;
+                        float sv[kElemsPerThread];
+                        if (seeded && live) {
+                            T::load_row_smem(tile + rr * N, lane, sv);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < kElemsPerThread; ++i) sv[i] = 0.f;
+                        }
+                        // The buffered steps in order, as the plain update made them ...
+                        for (int e = 0; e < c; ++e) {
+                            gather_entry<TS, L, IO>(be + e * N * io, lane, bv);
+                            const float a = rowa[e * kTileRows + rq], dx = rowb[e * kTileRows + rq];
+#pragma unroll
+                            for (int i = 0; i < kElemsPerThread; ++i) sv[i] = fmaf(sv[i], a, dx * bv[i]);
+                        }
+                        // ... then the current token, whose state y is read from.
+                        T::gather(sB, lane, bv);
+                        const float4 q = rowq[rq];
+                        const float sum = row_sum<L>(update_elems(sv, bv, cv, q.x, q.y));
+                        if (live && lane == 0)
+                            store_small(p.y, cu.b * p.ys[0] + cu.h * p.ys[1] + (cu.row0 + rr) * p.ys[2], IO,
+                                        output(sum, Dh, q.z, q.w));
+                        if (live && seeded) T::store_row_smem(tile + rr * N, lane, sv);
+                    }
+                }
+            }
+        }
+        if (stores) fence_proxy_async_smem();
+        named_barrier(1, kConsumers);
+        if (tid == 0) {
+            if (stores) {
+                unsigned char *dst = reinterpret_cast<unsigned char *>(
+                    static_cast<TS *>(p.state) + ((hd->slot * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0) * N);
+                bulk_store(dst, base, static_cast<uint32_t>(cu.rows_here) * N * sizeof(TS));
+                bulk_commit();
+                if (S == 1) {
+                    // One stage: the producer needs it back before the next unit.
+                    bulk_wait_read<0>();
+                    mbar_arrive(&empty[s]);
+                } else {
+                    // The previous store has had a unit's time to read its stage out.
+                    if (pending >= 0) {
+                        bulk_wait_read<1>();
+                        mbar_arrive(&empty[pending]);
+                    }
+                    pending = s;
+                }
+            } else {
+                if (pending >= 0) {
+                    bulk_wait_read<0>();
+                    mbar_arrive(&empty[pending]);
+                    pending = -1;
+                }
+                mbar_arrive(&empty[s]);
+            }
+        }
+    }
+    if (tid == 0) bulk_wait_all();
+}
+
+template <typename TS, int L, int IO>
+__global__ void __launch_bounds__(ReplayPipe<TS, L>::kThreads, ReplayPipe<TS, L>::kMinCtas)
+    ssu_replay_kernel(const KParams p, const ReplayLayout lay, int64_t units) {
+    using PS = ReplayPipe<TS, L>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
+    uint64_t *empty = full + lay.stages;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < lay.stages; ++s) {
+            mbar_init(&full[s], 32);
+            mbar_init(&empty[s], 1);
+        }
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32;
+    if (warp >= PS::kConsumerWarps)
+        replay_producer<TS, L, IO>(p, lay, units, smem, full, empty, warp - PS::kConsumerWarps);
+    else
+        replay_consumer<TS, L, IO>(p, lay, units, smem, full, empty);
+}
+
+// Number of SMs of the current device (cached per device).
+static int replay_sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+// Once per device: opt in to the largest dynamic shared memory a CTA takes,
+// and find how many CTAs of the kernel fit an SM by registers.
+template <typename TS, int L, int IO>
+static cudaError_t prepare_replay_kernel(int *reg_ctas) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        e = cudaFuncSetAttribute(ssu_replay_kernel<TS, L, IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ReplayPipe<TS, L>::kSmemPerSm - 1024);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes a;
+        e = cudaFuncGetAttributes(&a, ssu_replay_kernel<TS, L, IO>);
+        if (e != cudaSuccess) return e;
+        const int regs = (a.numRegs + 7) / 8 * 8;  // allocated per thread in units of 8
+        n = regs > 0 ? 65536 / (regs * ReplayPipe<TS, L>::kThreads) : 1;
+        if (n < 1) n = 1;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    *reg_ctas = n;
+    return cudaSuccess;
+}
+
+template <typename TS, int L, int IO>
+static cudaError_t launch_replay_t(const KParams &p, int64_t batch, cudaStream_t stream) {
+    using PS = ReplayPipe<TS, L>;
+    int reg_ctas = 0;
+    cudaError_t e = prepare_replay_kernel<TS, L, IO>(&reg_ctas);
+    if (e != cudaSuccess) return e;
+    ReplayLayout lay;
+    if (!lay.choose(PS::kTileBytes, PS::kN, p.rlen, IO == kF32 ? 4 : 2, PS::kSmemPerSm, reg_ctas,
+                    PS::kProducerWarps))
+        return cudaErrorInvalidConfiguration;
+    const int64_t units = batch * p.H * p.ptiles;
+    const int sms = replay_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t slots_on_gpu = static_cast<int64_t>(sms) * lay.ctas;
+    const int64_t grid = units < slots_on_gpu ? units : slots_on_gpu;
+    ssu_replay_kernel<TS, L, IO><<<static_cast<unsigned>(grid), PS::kThreads, lay.bytes, stream>>>(p, lay, units);
+    return cudaGetLastError();
+}
+
+template <typename TS, int IO>
+static cudaError_t launch_replay_lanes(int lanes, const KParams &p, int64_t batch, cudaStream_t stream) {
+    switch (lanes) {
+    case 1: return launch_replay_t<TS, 1, IO>(p, batch, stream);
+    case 2: return launch_replay_t<TS, 2, IO>(p, batch, stream);
+    case 4: return launch_replay_t<TS, 4, IO>(p, batch, stream);
+    case 8: return launch_replay_t<TS, 8, IO>(p, batch, stream);
+    case 16: return launch_replay_t<TS, 16, IO>(p, batch, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// The replay launcher for operands of dtype IO (instantiated in one
+// translation unit per IO).
+template <int IO>
+cudaError_t launch_replay_io(int state_dtype, int lanes, const KParams &p, int64_t batch, cudaStream_t stream) {
+    switch (state_dtype) {
+    case kF32: return launch_replay_lanes<float, IO>(lanes, p, batch, stream);
+    case kF16: return launch_replay_lanes<__half, IO>(lanes, p, batch, stream);
+    case kBF16: return launch_replay_lanes<__nv_bfloat16, IO>(lanes, p, batch, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+extern template cudaError_t launch_replay_io<kF32>(int, int, const KParams &, int64_t, cudaStream_t);
+extern template cudaError_t launch_replay_io<kF16>(int, int, const KParams &, int64_t, cudaStream_t);
+extern template cudaError_t launch_replay_io<kBF16>(int, int, const KParams &, int64_t, cudaStream_t);
+
+}  // namespace ssu

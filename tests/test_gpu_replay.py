@@ -82,6 +82,26 @@ def test_replay_io_and_flags(libssu, io_dtype, flags):
     check_against_oracle(w)
 
 
+@pytest.mark.parametrize("state_dtype,io_dtype,buffer_len", [
+    (torch.float32, torch.bfloat16, 7), (torch.bfloat16, torch.bfloat16, 16), (torch.float32, torch.float32, 32),
+    (torch.float16, torch.float32, 3)])
+def test_replay_many_units_per_cta(libssu, state_dtype, io_dtype, buffer_len):
+    """Far more (sequence, head, dim tile) units than resident CTAs, so each
+    CTA walks many units through its ring of stages, folding and non-folding
+    units interleaved; two dim tiles per head."""
+    w = workloads.replay_problem(40 + buffer_len, slots=96, heads=24, groups=4, dim=128, dstate=64, nseq=80,
+                                 buffer_len=buffer_len, state_dtype=state_dtype, io_dtype=io_dtype, pad_frac=0.1)
+    check_against_oracle(w)
+
+
+def test_replay_largest_stage(libssu):
+    """fp32 checkpoints of dstate 256 with the longest fp32 buffers: the
+    largest stage, a ring of one stage."""
+    w = workloads.replay_problem(41, slots=40, heads=8, groups=2, dim=64, dstate=256, nseq=36, buffer_len=32,
+                                 state_dtype=torch.float32, io_dtype=torch.float32, pad_frac=0.1)
+    check_against_oracle(w)
+
+
 def test_replay_no_table_and_pad_zero(libssu):
     check_against_oracle(workloads.replay_problem(31, slots=6, nseq=6, tables=False, buffer_len=3))
     check_against_oracle(workloads.replay_problem(32, slots=20, nseq=8, pad_slot_id=0, pad_frac=0.3))
