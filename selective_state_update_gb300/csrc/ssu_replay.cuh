@@ -28,14 +28,14 @@
 //                   and the c buffered entries of the tile (x rows, dt' rows,
 //                   B of the group) as bulk asynchronous copies (TMA engine)
 //                   completing on the stage's "full" mbarrier;
-//   consumer warps  first what is independent across rows and entries (B_j . C
-//                   dots, one warp per dot; each entry's decay and input term
-//                   per row), then either the readout (the walk over the
-//                   entries, split in contiguous parts over the threads of a
-//                   row; y from the checkpoint rows) or the fold (entries in
-//                   order, then the current token; y; the tile back into the
-//                   stage, from where one thread stores it to the checkpoint
-//                   with a bulk copy).  A stage is released on its "empty"
+//   consumer warps  either the readout -- S_ckpt . C per row beside the B_j . C
+//                   dots (one warp per dot), then the walk over the entries,
+//                   split in contiguous parts over the lanes of a row and
+//                   combined by shuffles, and y -- or the fold -- each entry's
+//                   decay and input term per row, the entries in order, then
+//                   the current token; y; the tile back into the stage, from
+//                   where one thread stores it to the checkpoint with a bulk
+//                   copy.  A stage is released on its "empty"
 //                   mbarrier once read, or once its store has read it out.
 // The kernel is compiled per dtype of the 16/32-bit operands (IO), which
 // keeps the consumer's code small and free of dtype branches.
@@ -53,6 +53,11 @@ namespace ssu {
 #ifndef SSU_REPLAY_MAX_STAGES
 #define SSU_REPLAY_MAX_STAGES 6
 #endif
+// Size of the pieces the checkpoint tile is requested in (lanes in turn).
+#ifndef SSU_REPLAY_TILE_CHUNK
+#define SSU_REPLAY_TILE_CHUNK 32768
+#endif
+constexpr uint32_t kReplayTileChunk = SSU_REPLAY_TILE_CHUNK;
 
 template <typename TS, int L>
 struct ReplayPipe {
@@ -60,10 +65,6 @@ struct ReplayPipe {
     static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
     static constexpr int kConsumerWarps = (Tile<TS, L>::kThreads + 31) / 32;
     static constexpr int kConsumers = 32 * kConsumerWarps;
-    // The readout walk of a row is split over kParts threads (contiguous
-    // ranges of entries), rows over kRowThreads threads.
-    static constexpr int kParts = kConsumers > kTileRows ? kConsumers / kTileRows : 1;
-    static constexpr int kRowThreads = kConsumers / kParts;
     // Producer warps take units in turn; a producer waits for its stage by
     // the parity of the "empty" phase, which is unambiguous only with no more
     // producers than stages, so a one-stage ring runs one producer.
@@ -88,27 +89,31 @@ struct ReplayHeader {
 };
 enum : int32_t { kRValid = 1, kRSeeded = 2, kRFold = 4 };
 
-// Most threads a row's readout walk is split over (see ReplayPipe::kParts).
-constexpr int kMaxWalkParts = 4;
+// Stage strides (elements) between the buffered entries' x rows and dt'
+// rows: a tile's rows plus 16 bytes, so that the lanes of a row, which read
+// neighbouring entries of the same row at once, fall in different banks.
+template <int IO>
+__host__ __device__ constexpr int x_stride() { return kTileRows + (IO == kF32 ? 4 : 8); }
+constexpr int kDtStride = kTileRows + 4;
 
 // Shared-memory layout, fixed per launch by the buffer length and the size of
 // the 16/32-bit operands.  A stage holds the checkpoint tile, up to len - 1
 // buffered entries as stored (x rows and dt' rows of the tile, B of the
 // group), the current token's B and C as fp32, the row scalars and the
 // header.  After the ring: the CTA's scratch for the unit being computed (B .
-// C dots; per-entry decays and input terms; the parts of each row's readout
-// walk) and the mbarriers.
+// C dots; per-entry decays and input terms of a fold) and the mbarriers.
 struct ReplayLayout {
     int xe, de, be, bc, cs, rowq, hd, stage;
-    int stages, producers, dots, rowa, rowb, rowg, bars, bytes, ctas;
+    int stages, producers, dots, rowa, rowb, bars, bytes, ctas;
 
     __host__ __device__ static int up(int v) { return (v + 127) / 128 * 128; }
 
     __host__ __device__ void place(int tile_bytes, int n, int len, int io) {
         const int ent = len - 1;
-        xe = up(tile_bytes);                 // io  [ent][kTileRows]
-        de = up(xe + ent * kTileRows * io);  // f32 [ent][kTileRows]
-        be = up(de + ent * kTileRows * 4);   // io  [ent][n]
+        const int xs = kTileRows + 16 / io;
+        xe = up(tile_bytes);                 // io  [ent][xs]
+        de = up(xe + ent * xs * io);         // f32 [ent][kDtStride]
+        be = up(de + ent * kDtStride * 4);   // io  [ent][n]
         bc = up(be + ent * n * io);          // f32 [n]
         cs = bc + n * 4;                     // f32 [n]
         rowq = up(cs + n * 4);               // f32x4 [kTileRows]
@@ -120,13 +125,11 @@ struct ReplayLayout {
         dots = stages * stage;                                 // f32 [len]
         rowa = up(dots + len * 4);                             // f32 [len - 1][kTileRows]
         rowb = up(rowa + (len - 1) * kTileRows * 4);           // f32 [len - 1][kTileRows]
-        rowg = up(rowb + (len - 1) * kTileRows * 4);           // f32x2 [kMaxWalkParts][kTileRows]
-        bars = up(rowg + kMaxWalkParts * kTileRows * 8);       // u64 full[stages], empty[stages]
+        bars = up(rowb + (len - 1) * kTileRows * 4);           // u64 full[stages], empty[stages]
         bytes = bars + 2 * 8 * stages;
     }
     static int scratch(int len) {
-        return up(len * 4) + 2 * up((len - 1) * kTileRows * 4) + up(kMaxWalkParts * kTileRows * 8) +
-               2 * 8 * SSU_REPLAY_MAX_STAGES;
+        return up(len * 4) + 2 * up((len - 1) * kTileRows * 4) + 2 * 8 * SSU_REPLAY_MAX_STAGES;
     }
     // Two CTAs per SM when registers allow two (max_ctas) and each still gets
     // a ring of two stages, else one CTA with as many stages as fit (at most
@@ -199,53 +202,92 @@ __device__ __forceinline__ void gather_entry(const unsigned char *row, int lane,
     }
 }
 
-// B_j . C for the c buffered entries (j < c) and the current token (j = c):
-// one warp per dot (lanes over consecutive elements: no bank conflicts), kQ
-// dots per warp interleaved, all kWarps consumer warps taking part.
-template <int N, int kWarps, int IO>
-__device__ __forceinline__ void entry_dots(int c, const unsigned char *be, const float *sB, const float *sC,
-                                           float *dots, int warp, int wl) {
-    constexpr int kPer = (N + 31) / 32;
-    constexpr int kQ = 4;
-    float cv[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) cv[i] = wl + 32 * i < N ? sC[wl + 32 * i] : 0.f;
-    for (int base = 0; base <= c; base += kQ * kWarps) {
-        float acc[kQ];
-#pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-            const int j = base + warp + q * kWarps;
-            acc[q] = 0.f;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) {
-                const int n = wl + 32 * i;
-                if (n < N) {
-                    const float bvl = j < c ? io_at<IO>(be, j * N + n) : (j == c ? sB[n] : 0.f);
-                    acc[q] = fmaf(bvl, cv[i], acc[q]);
-                }
-            }
+// V consecutive elements of a buffer stored in the io dtype IO, as fp32, with
+// one vector load (V * sizeof <= 16 bytes, aligned).
+template <int IO, int V>
+__device__ __forceinline__ void io_vec(const unsigned char *base, int i, float *v) {
+    if constexpr (IO == kF32) {
+        static_assert(V == 2 || V == 4, "fp32 vectors of 2 or 4");
+        if constexpr (V == 4) {
+            const float4 f = reinterpret_cast<const float4 *>(base)[i / 4];
+            v[0] = f.x, v[1] = f.y, v[2] = f.z, v[3] = f.w;
+        } else {
+            const float2 f = reinterpret_cast<const float2 *>(base)[i / 2];
+            v[0] = f.x, v[1] = f.y;
+        }
+    } else {
+        static_assert(V == 2 || V == 4 || V == 8, "16-bit vectors of 2, 4 or 8");
+        uint32_t w[V / 2];
+        if constexpr (V == 8) {
+            const uint4 u = reinterpret_cast<const uint4 *>(base)[i / 8];
+            w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+        } else if constexpr (V == 4) {
+            const uint2 u = reinterpret_cast<const uint2 *>(base)[i / 4];
+            w[0] = u.x, w[1] = u.y;
+        } else {
+            w[0] = reinterpret_cast<const uint32_t *>(base)[i / 2];
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-            for (int q = 0; q < kQ; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], off);
-        }
-        if (wl == 0) {
-#pragma unroll
-            for (int q = 0; q < kQ; ++q) {
-                const int j = base + warp + q * kWarps;
-                if (j <= c) dots[j] = acc[q];
-            }
+        for (int k = 0; k < V / 2; ++k) {
+            v[2 * k] = bits_to_float(w[k] & 0xffffu, IO);
+            v[2 * k + 1] = bits_to_float(w[k] >> 16, IO);
         }
     }
 }
 
+// B_j . C for the c buffered entries (j < c) and the current token (j = c):
+// eight lanes per dot, kConsumers / 8 dots at a time.  Lane s of a dot takes
+// the chunks s, s + 8, ... of V elements (V * sizeof(io) <= 16 bytes), so a
+// warp's loads of one chunk index cover whole 128-byte lines per dot.
+template <int N, int kConsumers, int IO>
+__device__ __forceinline__ void entry_dots(int c, const unsigned char *be, const float *sB, const float *sC,
+                                           float *dots, int tid) {
+    constexpr int kIo = IO == kF32 ? 4 : 2;
+    constexpr int kPer = N / 8;                                   // elements per lane
+    constexpr int V = kPer < 16 / kIo ? kPer : 16 / kIo;          // elements per chunk
+    constexpr int kChunks = kPer / V;
+    constexpr int kDots = kConsumers / 8;
+    static_assert(kPer % V == 0 && V >= 2, "dstate must be a multiple of 16");
+    const int grp = tid / 8, seg = tid % 8;
+    float cv[kPer];
+#pragma unroll
+    for (int k = 0; k < kChunks; ++k) {
+        const int n = (seg + 8 * k) * V;
+#pragma unroll
+        for (int v = 0; v < V; ++v) cv[k * V + v] = sC[n + v];
+    }
+    for (int base = 0; base <= c; base += kDots) {  // same trip count for every thread
+        const int j = base + grp;
+        float acc[2] = {0.f, 0.f};
+        if (j < c) {
+#pragma unroll
+            for (int k = 0; k < kChunks; ++k) {
+                float bv[V];
+                io_vec<IO, V>(be, j * N + (seg + 8 * k) * V, bv);
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v & 1] = fmaf(bv[v], cv[k * V + v], acc[v & 1]);
+            }
+        } else if (j == c) {
+#pragma unroll
+            for (int k = 0; k < kChunks; ++k) {
+                const int n = (seg + 8 * k) * V;
+#pragma unroll
+                for (int v = 0; v < V; ++v) acc[v & 1] = fmaf(sB[n + v], cv[k * V + v], acc[v & 1]);
+            }
+        }
+        float d = acc[0] + acc[1];
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        if (seg == 0 && j <= c) dots[j] = d;
+    }
+}
+
 // Each buffered entry's decay exp(A dt'_j) and input term dt'_j x_j for every
-// row of the tile, into rowa / rowb ([entry][kTileRows]); loads of a batch
-// issued before its arithmetic.  A fold (kExact) takes the decays from the
-// plain kernels' function, so that the folded state is theirs bit for bit; a
-// readout, which only produces y, takes the fast exponential.
-template <int kThreads, int IO, bool kExact>
+// row of the tile, into rowa / rowb ([entry][kTileRows]), for a fold; loads
+// of a batch issued before its arithmetic.  The decays come from the plain
+// kernels' function, so that the folded state is theirs bit for bit.
+template <int kThreads, int IO>
 __device__ __forceinline__ void entry_terms(int c, int rows, float Ah, const float *de, const unsigned char *xe,
                                             float *rowa, float *rowb, int tid) {
     constexpr int kB = 4;
@@ -255,58 +297,20 @@ __device__ __forceinline__ void entry_terms(int c, int rows, float Ah, const flo
 #pragma unroll
         for (int q = 0; q < kB; ++q) {
             const int i = i0 + q * kThreads;
-            const bool ok = i < total && i % kTileRows < rows;
-            d[q] = ok ? de[i] : 0.f;
-            x[q] = ok ? io_at<IO>(xe, i) : 0.f;
+            const int j = i / kTileRows, r = i % kTileRows;
+            const bool ok = i < total && r < rows;
+            d[q] = ok ? de[j * kDtStride + r] : 0.f;
+            x[q] = ok ? io_at<IO>(xe, j * x_stride<IO>() + r) : 0.f;
         }
 #pragma unroll
         for (int q = 0; q < kB; ++q) {
             const int i = i0 + q * kThreads;
             if (i < total && i % kTileRows < rows) {
-                rowa[i] = kExact ? decay(Ah, d[q]) : __expf(Ah * d[q]);
+                rowa[i] = decay(Ah, d[q]);
                 rowb[i] = d[q] * x[q];
             }
         }
     }
-}
-
-// Part `part` of the readout walk of row r over entries c (the current token:
-// decay dA, term dtx) down to 0, split into kParts contiguous ranges, part 0
-// the newest.  For its range [lo, hi] it returns {prod of the decays, sum of
-// each term weighted by B_j . C and by the decays of the newer entries of the
-// range}; the parts combine newest first (see the readout).
-template <int kParts>
-__device__ __forceinline__ float2 walk_part(int c, int part, int r, float dA, float dtx, const float *rowa,
-                                            const float *rowb, const float *dots) {
-    const int per = (c + kParts) / kParts;  // ceil((c + 1) / kParts)
-    const int hi = c - part * per;
-    const int lo = hi - per + 1 > 0 ? hi - per + 1 : 0;
-    float hist = 0.f, w = 1.f;
-    int j = hi;
-    if (j == c && j >= lo) {
-        hist = fmaf(w * dtx, dots[c], hist);
-        w *= dA;
-        --j;
-    }
-    for (; j - 3 >= lo; j -= 4) {
-        float a[4], bb[4], dd[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            a[t] = rowa[(j - t) * kTileRows + r];
-            bb[t] = rowb[(j - t) * kTileRows + r];
-            dd[t] = dots[j - t];
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            hist = fmaf(w * bb[t], dd[t], hist);
-            w *= a[t];
-        }
-    }
-    for (; j >= lo; --j) {
-        hist = fmaf(w * rowb[j * kTileRows + r], dots[j], hist);
-        w *= rowa[j * kTileRows + r];
-    }
-    return make_float2(w, hist);
 }
 
 // The operands of one unit plus its slot's buffered count (lane 0).
@@ -326,21 +330,18 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
                                                uint64_t *full, uint64_t *empty, int lane) {
     constexpr int N = ReplayPipe<TS, L>::kN;
     constexpr int io = IO == kF32 ? 4 : 2;
+    constexpr int kPerB = UnitOperands<TS, L>::kPerB;
+    constexpr int kPerRow = UnitOperands<TS, L>::kPerRow;
     const int S = lay.stages;
     const int s = k % S;
     const int round = k / S;
-    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1)) {
-        if (lane == 0) flag(p.status, kDevTimeout);
-        return false;
-    }
-    unsigned char *base = smem + s * lay.stage;
-    ReplayHeader *hd = reinterpret_cast<ReplayHeader *>(base + lay.hd);
-    float *sB = reinterpret_cast<float *>(base + lay.bc);
-    float *sC = reinterpret_cast<float *>(base + lay.cs);
-    float4 *rowq = reinterpret_cast<float4 *>(base + lay.rowq);
     const int len = p.rlen;
     const UnitCoords &cu = op.c;
 
+    // First everything that does not touch the stage, while the consumers
+    // may still hold it: the unit's flags and count, the current token's row
+    // scalars (the same calls the plain kernels make: bit-identical), and its
+    // appended entry.
     int32_t flags = 0, c = 0;
     if (lane == 0) {
         if (op.entries_ok && slot_ok(p, op.rs)) {
@@ -354,24 +355,16 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
             }
         }
         if ((flags & kRValid) && cu.h == 0 && cu.row0 == 0) p.cnt_out[cu.b] = (flags & kRFold) ? 0 : c + 1;
-        hd->slot = op.rs;
-        hd->flags = flags;
-        hd->c = c;
-        hd->Dh = op.Dh;
-        hd->Ah = op.Ah;
     }
     flags = __shfl_sync(0xffffffffu, flags, 0);
     c = __shfl_sync(0xffffffffu, c, 0);
     const int64_t rs = __shfl_sync(0xffffffffu, op.rs, 0);
     const bool append = (flags & kRValid) && !(flags & kRFold);
-
+    if (append && cu.h % p.heads_per_group == 0 && cu.row0 == 0) {
 #pragma unroll
-    for (int i = 0; i < UnitOperands<TS, L>::kPerB; ++i) {
-        const int n = lane + 32 * i;
-        if (n < N) {
-            sB[n] = bits_to_float(op.b[i], IO);
-            sC[n] = bits_to_float(op.cc[i], IO);
-            if (append && cu.h % p.heads_per_group == 0 && cu.row0 == 0) {
+        for (int i = 0; i < kPerB; ++i) {
+            const int n = lane + 32 * i;
+            if (n < N) {
                 const int64_t e = ((rs * len + c) * p.G + cu.g) * static_cast<int64_t>(N) + n;
                 if constexpr (io == 4)
                     static_cast<unsigned int *>(p.Bbuf)[e] = op.b[i];
@@ -380,15 +373,15 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
             }
         }
     }
-    // The current token's row scalars, from the same calls the plain kernels
-    // make (bit-identical), and its buffered entry.
+    float4 rq[kPerRow];
 #pragma unroll
-    for (int i = 0; i < UnitOperands<TS, L>::kPerRow; ++i) {
+    for (int i = 0; i < kPerRow; ++i) {
         const int r = lane + 32 * i;
+        rq[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (r < cu.rows_here && (flags & kRValid)) {
             const float xv = bits_to_float(op.x[i], IO);
             const float d = processed_step(bits_to_float(op.dt[i], p.dt_dtype), op.bias, p.softplus);
-            rowq[r] = make_float4(decay(op.Ah, d), d * xv, xv, silu_gate(bits_to_float(op.z[i], IO), p.z != nullptr));
+            rq[i] = make_float4(decay(op.Ah, d), d * xv, xv, silu_gate(bits_to_float(op.z[i], IO), p.z != nullptr));
             if (append) {
                 const int64_t e = ((rs * len + c) * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + r;
                 p.dtbuf[e] = d;
@@ -398,6 +391,37 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
                     static_cast<unsigned short *>(p.xbuf)[e] = static_cast<unsigned short>(op.x[i]);
             }
         }
+    }
+
+    // Then the stage: header, B, C, row scalars, the copies.
+    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1)) {
+        if (lane == 0) flag(p.status, kDevTimeout);
+        return false;
+    }
+    unsigned char *base = smem + s * lay.stage;
+    ReplayHeader *hd = reinterpret_cast<ReplayHeader *>(base + lay.hd);
+    float *sB = reinterpret_cast<float *>(base + lay.bc);
+    float *sC = reinterpret_cast<float *>(base + lay.cs);
+    float4 *rowq = reinterpret_cast<float4 *>(base + lay.rowq);
+    if (lane == 0) {
+        hd->slot = op.rs;
+        hd->flags = flags;
+        hd->c = c;
+        hd->Dh = op.Dh;
+        hd->Ah = op.Ah;
+    }
+#pragma unroll
+    for (int i = 0; i < kPerB; ++i) {
+        const int n = lane + 32 * i;
+        if (n < N) {
+            sB[n] = bits_to_float(op.b[i], IO);
+            sC[n] = bits_to_float(op.cc[i], IO);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kPerRow; ++i) {
+        const int r = lane + 32 * i;
+        if (r < cu.rows_here) rowq[r] = rq[i];
     }
 
     if (!(flags & kRSeeded)) {
@@ -414,11 +438,11 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
         for (int i = lane; i < c * rows; i += 32) {
             const int j = i / rows, r = i % rows;
             const int64_t e = ((rs * len + j) * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + r;
-            de[j * kTileRows + r] = __ldg(p.dtbuf + e);
+            de[j * kDtStride + r] = __ldg(p.dtbuf + e);
             if constexpr (io == 4)
-                reinterpret_cast<unsigned int *>(xe)[j * kTileRows + r] = load_bits<true>(p.xbuf, e);
+                reinterpret_cast<unsigned int *>(xe)[j * x_stride<IO>() + r] = load_bits<true>(p.xbuf, e);
             else
-                reinterpret_cast<unsigned short *>(xe)[j * kTileRows + r] =
+                reinterpret_cast<unsigned short *>(xe)[j * x_stride<IO>() + r] =
                     static_cast<unsigned short>(load_bits<false>(p.xbuf, e));
         }
         for (int i = lane; i < c * N; i += 32) {
@@ -431,21 +455,28 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
         }
     }
     // The checkpoint tile and (aligned buffers) every buffered entry, as bulk
-    // copies; lane 0 registers the total before any copy can complete.
+    // copies; lane 0 registers the total before any copy can complete.  (One
+    // copy per entry and buffer measured faster than one run per buffer of a
+    // head-major buffer layout.)
     const uint32_t tile_bytes = static_cast<uint32_t>(rows) * N * sizeof(TS);
     uint32_t bytes = tile_bytes;
     if (bulk_entries) bytes += static_cast<uint32_t>(c) * (rows * (io + 4) + N * io);
     if (lane == 0) mbar_arrive_expect(&full[s], bytes);
     __syncwarp();
-    if (lane == 0)
-        bulk_load(base, static_cast<const TS *>(p.state) + ((rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0) * N,
-                  tile_bytes, &full[s]);
+    {
+        const unsigned char *src = reinterpret_cast<const unsigned char *>(
+            static_cast<const TS *>(p.state) + ((rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0) * N);
+        for (uint32_t off = static_cast<uint32_t>(lane) * kReplayTileChunk; off < tile_bytes;
+             off += 32u * kReplayTileChunk)
+            bulk_load(base + off, src + off, tile_bytes - off < kReplayTileChunk ? tile_bytes - off : kReplayTileChunk,
+                      &full[s]);
+    }
     if (bulk_entries) {
         for (int j = lane; j < c; j += 32) {
             const int64_t e = ((rs * len + j) * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0;
-            bulk_load(xe + j * kTileRows * io, static_cast<const unsigned char *>(p.xbuf) + e * io,
+            bulk_load(xe + j * x_stride<IO>() * io, static_cast<const unsigned char *>(p.xbuf) + e * io,
                       static_cast<uint32_t>(rows) * io, &full[s]);
-            bulk_load(de + j * kTileRows, p.dtbuf + e, static_cast<uint32_t>(rows) * 4, &full[s]);
+            bulk_load(de + j * kDtStride, p.dtbuf + e, static_cast<uint32_t>(rows) * 4, &full[s]);
             const int64_t eb = ((rs * len + j) * p.G + cu.g) * static_cast<int64_t>(N);
             bulk_load(be + j * N * io, static_cast<const unsigned char *>(p.Bbuf) + eb * io,
                       static_cast<uint32_t>(N) * io, &full[s]);
@@ -486,19 +517,15 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
     using PS = ReplayPipe<TS, L>;
     constexpr int N = PS::kN;
     constexpr int kConsumers = PS::kConsumers;
-    constexpr int kParts = PS::kParts;
     constexpr int io = IO == kF32 ? 4 : 2;
-    static_assert(kParts <= kMaxWalkParts, "walk split over more parts than the scratch holds");
     const int S = lay.stages;
     const int tid = threadIdx.x;
     const bool active = tid < T::kThreads;
     const int lane = tid % L;
     const int slot_row = tid / L;
-    const int warp = tid / 32, wl = tid % 32;
     float *dots = reinterpret_cast<float *>(smem + lay.dots);
     float *rowa = reinterpret_cast<float *>(smem + lay.rowa);
     float *rowb = reinterpret_cast<float *>(smem + lay.rowb);
-    float2 *rowg = reinterpret_cast<float2 *>(smem + lay.rowg);
     int pending = -1;  // stage whose checkpoint store may still be reading it (thread 0)
     int k = 0;
     UnitWalker walk(p, blockIdx.x, gridDim.x);
@@ -533,40 +560,77 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
             float cv[kElemsPerThread];
             if (active) T::gather(sC, lane, cv);
             if (!fold) {
-                entry_dots<N, PS::kConsumerWarps, IO>(c, be, sB, sC, dots, warp, wl);
-                entry_terms<kConsumers, IO, false>(c, rows, Ah, de, xe, rowa, rowb, tid);
-                named_barrier(1, kConsumers);
-                // The walk: part tid / kRowThreads of rows tid % kRowThreads, ...
-                const int part = tid / PS::kRowThreads;
-                for (int r = tid % PS::kRowThreads; r < rows; r += PS::kRowThreads) {
-                    const float4 q = rowq[r];
-                    rowg[part * kTileRows + r] = walk_part<kParts>(c, part, r, q.x, q.y, rowa, rowb, dots);
-                }
-                named_barrier(1, kConsumers);
+                // S_ckpt . C of this thread's rows (every lane of a row ends
+                // with the sum) beside the B_j . C dots.
+                float rsum[kRowsPerThread];
                 if (active) {
-                    // ... and the readout: y = gamma_{0:c} (S_ckpt . C) + the
-                    // history term, gated; all rows first, then the stores.
-                    float yv[kRowsPerThread];
 #pragma unroll
                     for (int j = 0; j < kRowsPerThread; ++j) {
                         const int rr = slot_row + j * kRowSlots;  // row within the tile
-                        const int rq = rr < rows ? rr : 0;
                         float sv[kElemsPerThread];
-                        T::load_row_smem(tile + rq * N, lane, sv);
+                        T::load_row_smem(tile + (rr < rows ? rr : 0) * N, lane, sv);
                         float acc = 0.f;
 #pragma unroll
                         for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
-                        const float sum = row_sum<L>(acc);
-                        // Parts newest first: hist += w * hist_part, w *= w_part.
-                        float wgt = 1.f, hist = 0.f;
+                        rsum[j] = row_sum<L>(acc);
+                    }
+                }
+                entry_dots<N, kConsumers, IO>(c, be, sB, sC, dots, tid);
+                named_barrier(1, kConsumers);
+                if (active) {
+                    // The walk of each row over entries c (the current token)
+                    // down to 0, split in L contiguous parts, lane 0 the
+                    // newest: each lane folds its part into {product of the
+                    // decays, sum of the terms dt'_j x_j (B_j . C) weighted by
+                    // the decays of the newer entries of the part}; the parts
+                    // combine newest first, (w1, h1) then (w2, h2) giving
+                    // (w1 w2, h1 + w1 h2).  The readout only produces y, so
+                    // its decays take the fast exponential.
+                    const int per = (c + L) / L;  // ceil((c + 1) / L)
+                    const int hi = c - lane * per;
+                    const int lo = hi - per + 1 > 0 ? hi - per + 1 : 0;
+                    float w[kRowsPerThread], hs[kRowsPerThread];
+                    float4 q[kRowsPerThread];
+                    int rq[kRowsPerThread];
 #pragma unroll
-                        for (int q = 0; q < kParts; ++q) {
-                            const float2 g = rowg[q * kTileRows + rq];
-                            hist = fmaf(wgt, g.y, hist);
-                            wgt *= g.x;
+                    for (int j = 0; j < kRowsPerThread; ++j) {
+                        const int rr = slot_row + j * kRowSlots;
+                        rq[j] = rr < rows ? rr : 0;
+                        q[j] = rowq[rq[j]];
+                        w[j] = 1.f;
+                        hs[j] = 0.f;
+                    }
+                    int e = hi;
+                    if (e == c) {
+                        const float dc = dots[c];
+#pragma unroll
+                        for (int j = 0; j < kRowsPerThread; ++j) {
+                            hs[j] = fmaf(q[j].y, dc, 0.f);
+                            w[j] = q[j].x;
                         }
-                        const float4 q = rowq[rq];
-                        yv[j] = output(fmaf(wgt, sum, hist), Dh, q.z, q.w);
+                        --e;
+                    }
+                    for (; e >= lo; --e) {
+                        const float de_ = dots[e];
+#pragma unroll
+                        for (int j = 0; j < kRowsPerThread; ++j) {
+                            const float d = de[e * kDtStride + rq[j]];
+                            const float t = d * io_at<IO>(xe, e * x_stride<IO>() + rq[j]);
+                            hs[j] = fmaf(w[j] * t, de_, hs[j]);
+                            w[j] *= __expf(Ah * d);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 1; off < L; off <<= 1) {
+#pragma unroll
+                        for (int j = 0; j < kRowsPerThread; ++j) {
+                            const float w2 = __shfl_down_sync(0xffffffffu, w[j], off);
+                            const float h2 = __shfl_down_sync(0xffffffffu, hs[j], off);
+                            if ((lane & (2 * off - 1)) == 0) {
+                                hs[j] = fmaf(w[j], h2, hs[j]);
+                                w[j] *= w2;
+                            }
+                        }
                     }
                     if (lane == 0) {
 #pragma unroll
@@ -574,13 +638,13 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
                             const int rr = slot_row + j * kRowSlots;
                             if (rr < rows)
                                 store_small(p.y, cu.b * p.ys[0] + cu.h * p.ys[1] + (cu.row0 + rr) * p.ys[2], IO,
-                                            yv[j]);
+                                            output(fmaf(w[j], rsum[j], hs[j]), Dh, q[j].z, q[j].w));
                         }
                     }
                 }
             } else {
                 if (c > 0) {
-                    entry_terms<kConsumers, IO, true>(c, rows, Ah, de, xe, rowa, rowb, tid);
+                    entry_terms<kConsumers, IO>(c, rows, Ah, de, xe, rowa, rowb, tid);
                     named_barrier(1, kConsumers);
                 }
                 if (active) {
