@@ -92,6 +92,7 @@ typedef struct ssu_slot_table {
 #define SSU_DEV_TIMEOUT    0x8  /* an asynchronous state copy did not complete in
                                    about a second; the unit was skipped           */
 #define SSU_DEV_BAD_COUNT  0x10 /* ssu_replay_update: a buffered count outside [0, L) */
+#define SSU_DEV_BAD_COPY   0x20 /* ssu_batch_copy: a copy longer than max_bytes      */
 
 /* Arguments of the MATE signature that this library does not implement.  Set
  * the bit when the caller passed the argument; the call then fails with
@@ -225,6 +226,39 @@ typedef struct ssu_replay_buffers {
  */
 ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot_table *slots,
                              const ssu_replay_buffers *rb, void *stream);
+
+/*
+ * One copy of a batch: `bytes` bytes from device address `src` to device
+ * address `dst` (any alignment; 16-byte aligned addresses take the vector
+ * path).
+ */
+typedef struct ssu_copy {
+    uint64_t src;
+    uint64_t dst;
+    uint64_t bytes;
+} ssu_copy;
+
+/*
+ * Batched state copies with memmove semantics (digest of vLLM PR #50729,
+ * section 实现拆解: speculative decoding moves and shifts slot state inside
+ * one buffer, so a copy's source and destination may overlap).  Each copy
+ * leaves in its destination the bytes its source held before the copy, also
+ * when the two ranges overlap; copies that do not overlap themselves run at
+ * full parallelism, and only the ones that do are moved in order (by one
+ * CTA each).
+ *   copies     device [n] descriptors, 8-byte aligned.
+ *   max_bytes  an upper bound on every copy's `bytes`; it sizes the grid.  A
+ *              copy longer than max_bytes sets SSU_DEV_BAD_COPY and is
+ *              skipped.
+ *   d_status   device int32 or NULL (SSU_DEV_* bits ORed in).
+ * Different copies of one call must not overlap one another (no copy reads
+ * or writes bytes another copy writes); the result would depend on
+ * scheduling.  Copies with bytes == 0 or src == dst do nothing.  n == 0 or
+ * max_bytes == 0 launches nothing.  No article on the pages gives this an
+ * API; the descriptor form is this library's.
+ */
+ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes, int32_t *d_status,
+                          void *stream);
 
 /*
  * Get the kernel for one configuration ready before any CUDA graph capture:

@@ -38,6 +38,8 @@ TOUCH_READ, TOUCH_WRITTEN = 1, 2
 
 _DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16, torch.float64: F64}
 
+from .memcopy import batch_copy  # noqa: E402  (batched copies with memmove semantics)
+
 
 class OracleError(RuntimeError):
     """The oracle rejected its inputs (``code`` is INVALID or ALIASING)."""

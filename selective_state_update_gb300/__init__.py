@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
                        checkpoint plus a buffer of recent inputs
   ssu_update_packed    packed variable-length / MTP rows (cu_seqlens) or the
                        dense [batch, steps, heads, dim] form
+  ssu_batch_copy       batched state copies with memmove semantics
   ssu_prewarm          load a configuration's kernel before graph capture
 and ``selective_state_update``, the MATE/FlashInfer-shaped call (MATE
 documentation, page "Mamba / SSU", API reference) that picks one of the two
@@ -25,7 +26,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_prewarm",
+__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_batch_copy", "copy_table",
+           "slot_copies", "ssu_prewarm",
            "selective_state_update",
            "SLOTS_STRIDED", "SLOTS_PER_ROW", "DEV_BAD_SLOT", "DEV_BAD_ENTRY", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
            "library_path", "lib"]
@@ -36,7 +38,7 @@ _LIB_PATH = os.path.join(_PKG, "_build", "libssu.so")
 # ssu.h constants
 OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA = 0, 1, 2, 3
 SLOTS_STRIDED, SLOTS_PER_ROW = 0, 1
-DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN, DEV_TIMEOUT, DEV_BAD_COUNT = 0x1, 0x2, 0x4, 0x8, 0x10
+DEV_BAD_SLOT, DEV_BAD_ENTRY, DEV_BAD_SEQLEN, DEV_TIMEOUT, DEV_BAD_COUNT, DEV_BAD_COPY = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 UNSUP_RAND_SEED, UNSUP_STATE_SCALE, UNSUP_INTERMEDIATE, UNSUP_CACHE_STEPS, UNSUP_ALGORITHM = (
     0x01, 0x02, 0x04, 0x08, 0x10)
 _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -99,6 +101,9 @@ def lib():
         L.ssu_replay_update.argtypes = [p_args, ctypes.c_int64, p_tab, ctypes.POINTER(ReplayBuffers),
                                         ctypes.c_void_p]
         L.ssu_replay_update.restype = ctypes.c_int
+        L.ssu_batch_copy.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+        L.ssu_batch_copy.restype = ctypes.c_int
         L.ssu_prewarm.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
         L.ssu_prewarm.restype = ctypes.c_int
@@ -314,6 +319,44 @@ def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
     if rc != OK:
         _raise(rc)
     return out, count_out
+
+
+def ssu_batch_copy(copies: torch.Tensor, max_bytes: int, status: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Batched copies with memmove semantics (see ``include/ssu.h``).
+
+    ``copies`` is a contiguous int64 CUDA tensor ``[n, 3]`` of (source
+    address, destination address, bytes), e.g. from ``copy_table`` or
+    ``slot_copies``; ``max_bytes`` bounds every copy's length."""
+    _need(copies.dtype == torch.int64 and copies.dim() == 2 and copies.shape[1] == 3 and copies.is_contiguous(),
+          "copies must be a contiguous int64 [n, 3] tensor")
+    _need(copies.is_cuda or copies.numel() == 0, "copies must be a CUDA tensor")
+    _need(max_bytes >= 0, "max_bytes must not be negative")
+    if status is not None:
+        _need(status.dtype == torch.int32 and status.is_cuda, "status must be an int32 CUDA tensor")
+    rc = lib().ssu_batch_copy(copies.data_ptr() if copies.numel() else None, copies.shape[0], max_bytes,
+                              _ptr(status), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+
+
+def copy_table(entries, device) -> torch.Tensor:
+    """Descriptors ``[n, 3]`` from (source address, destination address,
+    bytes) triples."""
+    return torch.tensor(list(entries), dtype=torch.int64).reshape(-1, 3).to(device)
+
+
+def slot_copies(pool: torch.Tensor, src_slots: torch.Tensor, dst_slots: torch.Tensor) -> torch.Tensor:
+    """Descriptors copying whole slots of a contiguous pool ``[slots, ...]``:
+    slot src_slots[i] to slot dst_slots[i] (addresses computed on the device,
+    no host round trip)."""
+    _need(pool.is_contiguous(), "pool must be contiguous")
+    _need(src_slots.shape == dst_slots.shape and src_slots.dim() == 1, "slot lists must be 1-D and equal in length")
+    slot_bytes = pool[0].numel() * pool.element_size()
+    base = pool.data_ptr()
+    s = src_slots.to(device=pool.device, dtype=torch.int64) * slot_bytes + base
+    d = dst_slots.to(device=pool.device, dtype=torch.int64) * slot_bytes + base
+    return torch.stack([s, d, torch.full_like(s, slot_bytes)], dim=1).contiguous()
 
 
 def ssu_prewarm(*, state_dtype: torch.dtype, io_dtype: torch.dtype, heads: int, dim: int,

@@ -236,6 +236,17 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
     return launched(ssu::launch_replay(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
 }
 
+ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes, int32_t *d_status,
+                          void *stream) {
+    if (n < 0) return fail(SSU_ERR_INVALID, "n is negative");
+    if (n == 0 || max_bytes == 0) return ok();
+    if (copies == nullptr) return fail(SSU_ERR_INVALID, "copies is NULL");
+    if (reinterpret_cast<uintptr_t>(copies) % 8 != 0) return fail(SSU_ERR_INVALID, "copies must be 8-byte aligned");
+    if (d_status != nullptr && reinterpret_cast<uintptr_t>(d_status) % 4 != 0)
+        return fail(SSU_ERR_INVALID, "d_status must be 4-byte aligned");
+    return launched(ssu::launch_copy(copies, n, max_bytes, d_status, static_cast<cudaStream_t>(stream)));
+}
+
 ssu_status ssu_prewarm(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype, int64_t heads, int64_t dim,
                        int64_t dstate, int64_t groups, int32_t packed) {
     int lanes = 0;

@@ -57,7 +57,8 @@ __device__ __forceinline__ int64_t load_index(const void *base, int64_t i, int i
                   : static_cast<int64_t>(__ldg(static_cast<const int *>(base) + i));
 }
 
-enum : int { kDevBadSlot = 0x1, kDevBadEntry = 0x2, kDevBadSeqlen = 0x4, kDevTimeout = 0x8, kDevBadCount = 0x10 };
+enum : int { kDevBadSlot = 0x1, kDevBadEntry = 0x2, kDevBadSeqlen = 0x4, kDevTimeout = 0x8, kDevBadCount = 0x10,
+             kDevBadCopy = 0x20 };
 
 __device__ __forceinline__ void flag(int32_t *status, int bit) {
     if (status != nullptr) atomicOr(status, bit);

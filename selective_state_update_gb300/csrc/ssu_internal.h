@@ -77,6 +77,8 @@ cudaError_t launch_packed(int state_dtype, int lanes, const KParams &p, cudaStre
 cudaError_t prewarm_onetoken(int state_dtype, int lanes);
 cudaError_t prewarm_packed(int state_dtype, int lanes);
 cudaError_t launch_replay(int state_dtype, int lanes, const KParams &p, int64_t batch, cudaStream_t stream);
+// Batched copies (ssu_batch_copy): `copies` device [n] {src, dst, bytes}.
+cudaError_t launch_copy(const void *copies, int64_t n, uint64_t max_bytes, int32_t *status, cudaStream_t stream);
 
 // Largest buffer length of the checkpoint + buffer form.
 constexpr int kMaxReplayLen = 32;

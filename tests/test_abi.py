@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("ssu_update_onetoken", "ssu_update_packed", "ssu_prewarm", "ssu_last_error"):
+    for n in ("ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_batch_copy", "ssu_prewarm",
+              "ssu_last_error"):
         assert n in names
 
 
@@ -128,3 +129,14 @@ def test_empty_calls_launch_nothing(libssu):
 def test_prewarm_rejects_unsupported_shapes(libssu):
     assert libssu.ssu_prewarm(0, 2, 0, 8, 8, 100, 2, 0) == ssu.ERR_UNSUPPORTED
     assert libssu.ssu_prewarm(0, 2, 0, 8, 8, 128, 3, 0) == ssu.ERR_INVALID
+
+
+def test_batch_copy_host_checks(libssu):
+    """ssu_batch_copy: argument checks before any launch."""
+    assert libssu.ssu_batch_copy(None, -1, 16, None, None) == ssu.ERR_INVALID
+    assert libssu.ssu_batch_copy(None, 0, 16, None, None) == ssu.OK
+    assert libssu.ssu_batch_copy(None, 3, 0, None, None) == ssu.OK
+    assert libssu.ssu_batch_copy(None, 3, 16, None, None) == ssu.ERR_INVALID
+    assert "NULL" in libssu.ssu_last_error().decode()
+    assert libssu.ssu_batch_copy(12, 3, 16, None, None) == ssu.ERR_INVALID
+    assert "aligned" in libssu.ssu_last_error().decode()
