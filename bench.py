@@ -50,10 +50,15 @@ DESCRIPTIONS = {
     "replay_b256_fp32": "one-token decode on the checkpoint + buffer form (ReplaySSM), batch 256, heads 128, "
                         "dim 64, dstate 128, groups 8, fp32 checkpoints (512 slots), buffer length 16, "
                         "sequence b starting with b % 16 buffered entries (1/16 of the sequences fold per step)",
+    "copy_slots_b256_fp32": "256 whole-slot state copies of 4 MiB (heads 128, dim 64, dstate 128, fp32) between "
+                            "random disjoint slot sets of a 512-slot pool; steps alternate the direction",
 }
+COPY_METRIC = "whole-slot state copies/s and achieved HBM GB/s (read + write)"
+COPY_UNIT = "copies/s"
 KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
-                  "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"]}
+                  "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"],
+                  "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"]}
 
 
 # --------------------------------------------------------------------------
@@ -397,6 +402,101 @@ def run_ours(args, rank, world, device):
     return result
 
 
+def run_copy(args, rank, world, device):
+    """The slot-copy workload: one step = one ssu_batch_copy call moving every
+    copy of the batch (even steps source -> destination, odd steps back)."""
+    from selective_state_update_gb300 import build as ssu_build
+    import selective_state_update_gb300 as ssu
+    ssu_build.build()
+    ssu.lib()
+    w = make_workload(args, device, seed_offset=97 * rank)
+    slot_bytes = w.state[0].numel() * w.state.element_size()
+    tables = [ssu.slot_copies(w.state, w.src, w.dst), ssu.slot_copies(w.state, w.dst, w.src)]
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    call = lambda i: ssu.ssu_batch_copy(tables[i % 2], slot_bytes, status=status)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clocks:
+        whole0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            call(i)
+            ev[i][1].record(stream)
+        whole1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(whole0.elapsed_time(whole1), device)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if int(status.item()) != 0:
+        raise SystemExit(f"ssu_batch_copy reported status {int(status.item())}")
+    # End to end: the step's descriptor table from pinned host memory, the
+    # copies, the status word back to pinned host memory.
+    host_tabs = [t.cpu().pin_memory() for t in tables]
+    host_status = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    h2d = host_tabs[0].numel() * 8
+    e2e_steps = max(3, min(args.steps, 400))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        tables[i % 2].copy_(host_tabs[i % 2], non_blocking=True)
+        call(i)
+        host_status.copy_(status, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, device)
+    n = w.nseq
+    algo = 2 * n * slot_bytes + 2 * n * 24
+    peak, peak_src = hbm_peak()
+    achieved = algo / (launch_ms * 1e-3) / 1e9
+    return {
+        "metric": COPY_METRIC, "value": aggregate_rate(n, world, args.steps, total_ms), "unit": COPY_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                               + (f" (batch {args.batch})" if args.batch else ""),
+                   "copies_per_gpu": n, "bytes_per_copy": slot_bytes,
+                   "parallelism": f"{world} independent replicas (one pool per GPU)",
+                   "l2": "no flush: %.2f GB moved per step" % (algo / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("copy", args.workload),
+                     "algorithmic_bytes_per_launch": algo, "kernel": "ssu_copy_kernel", "launch_ms": launch_ms},
+        "e2e": {"value": aggregate_rate(n, world, e2e_steps, e2e_s * 1e3), "unit": COPY_UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
+def copy_oracle_rate(w_cpu, budget_s: float):
+    """The copy oracle on samples of the slot-copy workload: each sample a
+    few whole-slot copies applied to a compact buffer of their slots."""
+    import numpy as np
+    import oracle
+    nbytes = w_cpu.state[0].numel() * w_cpu.state.element_size()
+    done, spent, samples, idx, per = 0, 0.0, 0, 0, 4
+    n = w_cpu.nseq
+    while spent < budget_s:
+        ids = [(idx + i) % n for i in range(per)]
+        idx += per
+        # compact buffer: the sampled source slots, then room for their destinations
+        srcs = w_cpu.state[w_cpu.src[ids]].contiguous().view(-1).view(torch.uint8).numpy()
+        buf = np.concatenate([srcs, np.zeros_like(srcs)])
+        copies = [(i * nbytes, (per + i) * nbytes, nbytes) for i in range(per)]
+        t0 = time.perf_counter()
+        oracle.batch_copy(buf, copies)
+        spent += time.perf_counter() - t0
+        done += per
+        samples += 1
+    return done / spent, f"{done} copies of {nbytes} bytes in {samples} samples"
+
+
 # --------------------------------------------------------------------------
 # The oracle on the host cores.
 # --------------------------------------------------------------------------
@@ -454,15 +554,16 @@ def _oracle_call(sub):
 
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
-         "varlen_fp16": 1005, "replay_b256_fp32": 1006}
+         "varlen_fp16": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007}
 
 
 def make_workload(args, device, seed_offset=0):
     gen = workloads.NAMED[args.workload]
     kw = {}
     if args.batch is not None:
-        if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32"):
-            raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32 and replay_b256_fp32 workloads only")
+        if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "copy_slots_b256_fp32"):
+            raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32, replay_b256_fp32 and "
+                             "copy_slots_b256_fp32 workloads only")
         kw["batch"] = args.batch
     return gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
 
@@ -499,6 +600,17 @@ def run_reference(args):
     w_cpu = _cpu_workload(args)
     import oracle
     oracle.build()
+    if getattr(w_cpu, "kind", "") == "copy":
+        budget = min(150.0, 1.0 + 0.05 * (args.steps + args.warmup))
+        value, sample = copy_oracle_rate(w_cpu, budget)
+        return {
+            "impl": "reference", "metric": COPY_METRIC, "value": value, "unit": COPY_UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "cpu_baseline": {"value": value, "unit": COPY_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": COPY_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     lens = _lengths(w_cpu)
     # one step = the oracle on one sequence; size the run to end within minutes
     steps_total = args.steps + args.warmup
@@ -557,11 +669,17 @@ def main():
 
     # The oracle baseline runs before the first GPU call (no fork after CUDA init).
     cpu = None
+    is_copy = args.workload.startswith("copy_")
     if rank == 0 and not args.no_cpu_baseline:
         w_cpu = _cpu_workload(args)
-        rate, desc = oracle_rate(w_cpu, args.cpu_baseline_seconds)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+        if is_copy:
+            rate, desc = copy_oracle_rate(w_cpu, args.cpu_baseline_seconds)
+            cpu = {"value": rate, "unit": COPY_UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{desc} of {args.workload} (numpy, one thread)"}
+        else:
+            rate, desc = oracle_rate(w_cpu, args.cpu_baseline_seconds)
+            cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
         del w_cpu
 
     if not torch.cuda.is_available():
@@ -571,7 +689,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
-    res = run_ours(args, rank, world, device)
+    res = run_copy(args, rank, world, device) if is_copy else run_ours(args, rank, world, device)
     res["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(res), flush=True)

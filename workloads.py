@@ -21,6 +21,10 @@ the decode workloads this library is measured on:
   varlen_fp16     128 sequences with lengths U{0..8}, heads 64, groups 1,
                   fp16 pool of 2048 slots, one flat [rows] read table (no
                   destination table), 3% pad (pad id -1), read per packed row.
+
+Two more exercise the neighbouring rows: replay_b256_fp32 (the checkpoint +
+buffer form on the b256 shapes) and copy_slots_b256_fp32 (whole-slot state
+copies in the b256 pool).
 """
 from __future__ import annotations
 
@@ -282,6 +286,35 @@ def replay_problem(seed: int, *, slots: int = 16, heads: int = 4, dim: int = 8, 
     return w.to(device)
 
 
+@dataclass
+class CopyWorkload:
+    """Whole-slot copies inside one state pool: slot src[i] to slot dst[i]."""
+    name: str
+    state: torch.Tensor                        # [slots, heads, dim, dstate]
+    src: torch.Tensor                          # [n] int64 slots
+    dst: torch.Tensor                          # [n] int64 slots, disjoint from src
+    kind: str = "copy"
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def nseq(self) -> int:
+        return self.src.numel()
+
+    def to(self, device) -> "CopyWorkload":
+        return replace(self, state=self.state.to(device), src=self.src.to(device), dst=self.dst.to(device))
+
+
+def copy_slots_b256_fp32(device="cpu", seed=1007, batch=256) -> CopyWorkload:
+    """``batch`` whole-slot copies of 4 MiB (heads 128, dim 64, dstate 128,
+    fp32) between random distinct slots of a pool of 2 * batch slots, sources
+    and destinations disjoint (the slot moves of speculative decoding)."""
+    slots = 2 * batch
+    g = _gen(seed, device)
+    state = _pool(g, device, slots, 128, 64, 128, torch.float32)
+    perm = torch.randperm(slots, generator=_gen(seed + 1, "cpu"))
+    return CopyWorkload("copy_slots_b256_fp32", state, perm[:batch].to(device), perm[batch:].to(device))
+
+
 NAMED = {
     "tiny_onetoken": tiny_onetoken,
     "b256_fp32": b256_fp32,
@@ -289,6 +322,7 @@ NAMED = {
     "mtp_64x7_fp32": mtp_64x7_fp32,
     "varlen_fp16": varlen_fp16,
     "replay_b256_fp32": replay_b256_fp32,
+    "copy_slots_b256_fp32": copy_slots_b256_fp32,
 }
 
 
