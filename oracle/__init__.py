@@ -102,8 +102,12 @@ class _ReplayProblem(ctypes.Structure):
         ("slot_of", ctypes.c_void_p), ("len", ctypes.c_int64),
         ("xbuf", ctypes.c_void_p), ("dtbuf", ctypes.c_void_p), ("Bbuf", ctypes.c_void_p),
         ("count_in", ctypes.c_void_p), ("count_out", ctypes.c_void_p),
+        ("shadow_format", ctypes.c_int32), ("shadow", ctypes.c_void_p), ("shadow_scale", ctypes.c_void_p),
     ]
 
+
+# Formats of the low-precision read copy (ssu_oracle.h, ORC_SHADOW_*).
+SHADOW_NONE, SHADOW_F16, SHADOW_E4M3 = 0, 1, 2
 
 _lib = None
 
@@ -123,6 +127,13 @@ def load_library(path: str):
     lib.orc_decode.restype = ctypes.c_double
     lib.orc_encode.argtypes = [ctypes.c_double, ctypes.c_int]
     lib.orc_encode.restype = ctypes.c_uint32
+    lib.orc_shadow_refresh.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    lib.orc_shadow_refresh.restype = ctypes.c_int
+    lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e4m3_decode.restype = ctypes.c_double
     return lib
 
 
@@ -269,18 +280,25 @@ class ReplayResult:
     dtbuf: torch.Tensor
     Bbuf: torch.Tensor
     count: torch.Tensor        # [batch] int64 entries buffered after the call
+    shadow: Optional[torch.Tensor] = None        # read copy after the call
+    shadow_scale: Optional[torch.Tensor] = None
 
 
 def replay(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
            C: torch.Tensor, xbuf: torch.Tensor, dtbuf: torch.Tensor, Bbuf: torch.Tensor,
            count: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
            dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
-           slot_of: Optional[torch.Tensor] = None, pad_slot_id: int = -1, lib=None) -> ReplayResult:
+           slot_of: Optional[torch.Tensor] = None, pad_slot_id: int = -1, shadow: Optional[torch.Tensor] = None,
+           shadow_scale: Optional[torch.Tensor] = None, shadow_format: int = SHADOW_NONE, lib=None) -> ReplayResult:
     """One ReplaySSM decode step (one token per sequence) on the host.
 
     ckpt ``[slots, heads, dim, dstate]``; xbuf ``[slots, L, heads, dim]`` (x's dtype);
     dtbuf ``[slots, L, heads, dim]`` fp32; Bbuf ``[slots, L, groups, dstate]`` (x's dtype);
-    count ``[batch]`` entries buffered per sequence.  Inputs are not modified."""
+    count ``[batch]`` entries buffered per sequence.  With a read copy
+    (``shadow_format`` SHADOW_F16: ``shadow`` fp16 codes as int16/float16,
+    SHADOW_E4M3: uint8 codes and ``shadow_scale [slots, heads, dim]`` fp32),
+    steps that do not fold read it instead of the checkpoint and a fold
+    rewrites it.  Inputs are not modified."""
     lib = lib or _load()
     c_in = _cpu(ckpt)
     slots, heads, dim, dstate = c_in.shape
@@ -309,8 +327,35 @@ def replay(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tenso
         dt_softplus=int(bool(dt_softplus)), pad_slot_id=int(pad_slot_id), batch=batch,
         slot_of=_ptr(so), len=L, xbuf=xb.data_ptr(), dtbuf=db.data_ptr(), Bbuf=Bb.data_ptr(),
         count_in=cin.data_ptr(), count_out=cout.data_ptr())
+    sh = sc = None
+    if shadow_format != SHADOW_NONE:
+        sh = _cpu(shadow).clone()
+        sc = None if shadow_scale is None else _cpu(shadow_scale).to(torch.float32).clone()
+        pr.shadow_format, pr.shadow, pr.shadow_scale = shadow_format, sh.data_ptr(), _ptr(sc)
     err = ctypes.create_string_buffer(512)
     rc = lib.orc_replay_run(ctypes.byref(pr), err, 512)
     if rc != OK:
         raise OracleError(rc, err.value.decode())
-    return ReplayResult(ckpt=c_out, y=y, y_exact=y_exact, xbuf=xb, dtbuf=db, Bbuf=Bb, count=cout)
+    return ReplayResult(ckpt=c_out, y=y, y_exact=y_exact, xbuf=xb, dtbuf=db, Bbuf=Bb, count=cout, shadow=sh,
+                        shadow_scale=sc)
+
+
+def shadow_refresh(state: torch.Tensor, shadow_format: int, lib=None):
+    """The read copy of a state pool ``[..., dstate]``: (codes, row scales)
+    -- fp16 codes as float16 and no scales for SHADOW_F16, uint8 E4M3 codes
+    and fp32 scales of shape ``state.shape[:-1]`` for SHADOW_E4M3."""
+    lib = lib or _load()
+    st = _cpu(state).contiguous()
+    dstate = st.shape[-1]
+    rows = st.numel() // dstate
+    if shadow_format == SHADOW_F16:
+        codes, scale = torch.empty(st.shape, dtype=torch.float16), None
+    elif shadow_format == SHADOW_E4M3:
+        codes, scale = torch.empty(st.shape, dtype=torch.uint8), torch.empty(st.shape[:-1], dtype=torch.float32)
+    else:
+        raise ValueError("unknown read-copy format")
+    rc = lib.orc_shadow_refresh(st.data_ptr(), _DTYPE_CODE[st.dtype], rows, dstate, shadow_format, codes.data_ptr(),
+                                _ptr(scale))
+    if rc != OK:
+        raise OracleError(rc, "shadow refresh failed")
+    return codes, scale

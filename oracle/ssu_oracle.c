@@ -172,6 +172,97 @@ uint32_t orc_encode(double v, int dtype)
 }
 
 /* ------------------------------------------------------------------------ */
+/* The low-precision read copy (ReplaySSM, 低精度读写分离).                 */
+/* ------------------------------------------------------------------------ */
+
+/* OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; exponent
+ * field 0 holds subnormals f * 2^-9; S.1111.111 is NaN, so the largest finite
+ * value is 1.75 * 2^8 = 448 and there are no infinities. */
+double orc_e4m3_decode(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xf;
+    int f = code & 7;
+    double v;
+    if (e == 15 && f == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)f, -9);
+    else
+        v = ldexp((double)(f + 8), e - 10);  /* (1 + f/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Round to nearest even onto the E4M3 grid, values past the largest finite
+ * one clamped to +-448 ("saturate to finite").  NaN maps to the NaN code. */
+uint8_t orc_e4m3_encode(float v)
+{
+    if (isnan(v))
+        return 0x7f;
+    uint8_t sign = signbit(v) ? 0x80 : 0;
+    double r = fabs(round_to_format((double)v, 3, -6, 8));
+    if (isinf(r) || r > 448.0)
+        r = 448.0;
+    if (r == 0.0)
+        return sign;
+    if (r < ldexp(1.0, -6))                     /* subnormal: r = f * 2^-9 */
+        return sign | (uint8_t)(r / ldexp(1.0, -9));
+    int e2;
+    double m = frexp(r, &e2);                   /* r = m 2^e2, m in [0.5, 1) */
+    int biased = (e2 - 1) + 7;
+    uint8_t frac = (uint8_t)((m * 2.0 - 1.0) * 8.0);
+    return sign | (uint8_t)(biased << 3) | frac;
+}
+
+/* One state row into its read copy (format per orc_shadow_refresh). */
+static void shadow_row(const double *v, int64_t n, int32_t format, void *codes, float *scale)
+{
+    if (format == ORC_SHADOW_F16) {
+        for (int64_t i = 0; i < n; ++i)
+            ((uint16_t *)codes)[i] = double_to_half_bits(v[i]);
+        return;
+    }
+    /* the row values are fp32 numbers, so these are exact fp32 operations */
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i)
+        if ((float)fabs(v[i]) > amax)
+            amax = (float)fabs(v[i]);
+    volatile float s = amax > 0.0f ? amax / 448.0f : 1.0f;  /* fp32 division */
+    *scale = s;
+    for (int64_t i = 0; i < n; ++i) {
+        volatile float q = (float)v[i] / s;                  /* fp32 division */
+        ((uint8_t *)codes)[i] = orc_e4m3_encode(q);
+    }
+}
+
+static double shadow_value(const void *codes, const float *scale, int64_t row, int64_t n, int64_t i, int32_t format)
+{
+    if (format == ORC_SHADOW_F16)
+        return half_bits_to_double(((const uint16_t *)codes)[row * n + i]);
+    return orc_e4m3_decode(((const uint8_t *)codes)[row * n + i]) * (double)scale[row];
+}
+
+int orc_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate, int32_t format,
+                       void *shadow, float *scale)
+{
+    if (format != ORC_SHADOW_F16 && format != ORC_SHADOW_E4M3)
+        return ORC_INVALID;
+    if (format == ORC_SHADOW_E4M3 && scale == NULL)
+        return ORC_INVALID;
+    double *v = malloc(sizeof(double) * (size_t)dstate);
+    if (!v)
+        return ORC_INVALID;
+    const size_t cb = format == ORC_SHADOW_F16 ? 2 : 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t i = 0; i < dstate; ++i)
+            v[i] = load_elem(state, r * dstate + i, state_dtype);
+        shadow_row(v, dstate, format, (char *)shadow + (size_t)(r * dstate) * cb, scale ? scale + r : NULL);
+    }
+    free(v);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Scalar functions of the method.                                          */
 /* ------------------------------------------------------------------------ */
 
@@ -415,6 +506,12 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
         set_err(err, errlen, "bad shape: heads=%lld len=%lld", H, Lb);
         return ORC_INVALID;
     }
+    if (pr->shadow_format != ORC_SHADOW_NONE &&
+        ((pr->shadow_format != ORC_SHADOW_F16 && pr->shadow_format != ORC_SHADOW_E4M3) || pr->shadow == NULL ||
+         (pr->shadow_format == ORC_SHADOW_E4M3 && pr->shadow_scale == NULL))) {
+        set_err(err, errlen, "bad read copy (format %lld, or its arrays missing)", pr->shadow_format, 0);
+        return ORC_INVALID;
+    }
     const int64_t heads_per_group = H / G;
     int64_t *owner = malloc(sizeof(int64_t) * (size_t)pr->slots);
     double *S = malloc(sizeof(double) * (size_t)N);
@@ -486,9 +583,19 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
                         S[n] = S[n] * a + d * xv * load_elem(pr->B, bc_now + n, pr->io_dtype);
                         y += S[n] * load_elem(pr->C, bc_now + n, pr->io_dtype);
                     }
-                    if (!pad)
+                    if (!pad) {
+                        const int64_t row = (slot * H + h) * P + p;
                         for (int64_t n = 0; n < N; ++n)
-                            store_elem(pr->ckpt_out, ((slot * H + h) * P + p) * N + n, pr->state_dtype, S[n]);
+                            store_elem(pr->ckpt_out, row * N + n, pr->state_dtype, S[n]);
+                        if (pr->shadow_format != ORC_SHADOW_NONE) {
+                            /* the read copy of the checkpoint as stored */
+                            for (int64_t n = 0; n < N; ++n)
+                                S[n] = load_elem(pr->ckpt_out, row * N + n, pr->state_dtype);
+                            shadow_row(S, N, pr->shadow_format,
+                                       (char *)pr->shadow + (size_t)(row * N) * (pr->shadow_format == ORC_SHADOW_F16 ? 2 : 1),
+                                       pr->shadow_scale ? pr->shadow_scale + row : NULL);
+                        }
+                    }
                 } else {
                     /* Output from checkpoint and buffer: walk the entries from
                      * the newest (the current token, entry c) to the oldest,
@@ -510,9 +617,13 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
                         hist += w * dj * xj * kq;
                         w *= exp(A * dj);
                     }
+                    /* S_ckpt . C, from the read copy when there is one */
                     double sq = 0.0;
+                    const int64_t row = (slot * H + h) * P + p;
                     for (int64_t n = 0; n < N; ++n)
-                        sq += load_elem(pr->ckpt_in, ((slot * H + h) * P + p) * N + n, pr->state_dtype) *
+                        sq += (pr->shadow_format != ORC_SHADOW_NONE
+                                   ? shadow_value(pr->shadow, pr->shadow_scale, row, N, n, pr->shadow_format)
+                                   : load_elem(pr->ckpt_in, row * N + n, pr->state_dtype)) *
                               load_elem(pr->C, bc_now + n, pr->io_dtype);
                     y = w * sq + hist;
                     /* Append the current token as entry c (v and k keep their

@@ -73,7 +73,28 @@ typedef struct {
     void *Bbuf;                     /* [slots, L, groups, dstate] io dtype, in/out                */
     const int64_t *count_in;        /* [batch] entries buffered before the call (0 <= c < L)      */
     int64_t *count_out;             /* [batch] entries buffered after the call                    */
+    int32_t shadow_format;          /* ORC_SHADOW_*: the low-precision read copy, or none         */
+    void *shadow;                   /* [slots, heads, dim, dstate] codes, in/out (NULL: none)     */
+    float *shadow_scale;            /* [slots, heads, dim] row scales (E4M3), in/out              */
 } orc_replay_problem;
+
+/* Low-precision read copy of the checkpoints (article "ReplaySSM", section
+ * 低精度读写分离): steps that do not fold read it instead of the checkpoint;
+ * a fold rewrites it from the new checkpoint.
+ *   ORC_SHADOW_F16   binary16, round to nearest even.
+ *   ORC_SHADOW_E4M3  OCP FP8 E4M3 (bias 7, 3 fraction bits, no infinities,
+ *                    largest 448) with one fp32 scale per state row:
+ *                    scale = amax / 448 (1 for an all-zero row), computed in
+ *                    fp32; code = E4M3(v / scale) with the quotient in fp32,
+ *                    rounded to nearest even and clamped to +-448. */
+enum { ORC_SHADOW_NONE = 0, ORC_SHADOW_F16 = 1, ORC_SHADOW_E4M3 = 2 };
+
+/* The read copy of `rows` state rows of `dstate` elements (`state` in
+ * state_dtype); `scale` may be NULL for ORC_SHADOW_F16. */
+int orc_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate, int32_t format,
+                       void *shadow, float *scale);
+uint8_t orc_e4m3_encode(float v);
+double orc_e4m3_decode(uint8_t code);
 
 int orc_replay_run(const orc_replay_problem *problem, char *err, int errlen);
 

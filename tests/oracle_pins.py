@@ -725,9 +725,129 @@ def pin_replay_pad_and_aliasing(lib):
             raise
 
 
+def pin_e4m3_codes(lib):
+    """OCP FP8 E4M3 as the read copy stores it: every finite code decodes and
+    re-encodes to itself; random values (normal, subnormal, ties) encode as
+    torch's float8_e4m3fn cast does; past 448 the encoder clamps to +-448;
+    NaN keeps the NaN code."""
+    for code in range(256):
+        v = lib.orc_e4m3_decode(code)
+        if (code & 0x7f) == 0x7f:
+            if not np.isnan(v):
+                raise AssertionError("E4M3 NaN code")
+            continue
+        if lib.orc_e4m3_encode(v) != code and not (v == 0.0 and code == 0x80 and lib.orc_e4m3_encode(v) == 0):
+            if not (code == 0x80 and lib.orc_e4m3_encode(-0.0) == 0x80):
+                raise AssertionError(f"E4M3 code {code:#x} does not round-trip")
+    g = torch.Generator().manual_seed(61)
+    vals = torch.cat([(torch.rand(4000, generator=g) - 0.5) * 900, (torch.rand(2000, generator=g) - 0.5) * 0.03,
+                      torch.tensor([2.0 ** -10, 3 * 2.0 ** -10, 1.0625, 1.1875, 17.0, 456.0, -464.0])])
+    want = vals.to(torch.float8_e4m3fn).view(torch.uint8)
+    got = torch.tensor([lib.orc_e4m3_encode(float(v)) for v in vals], dtype=torch.uint8)
+    if not torch.equal(got, want):
+        raise AssertionError(f"E4M3 encoding differs from torch on {int((got != want).sum())} values")
+    for v, c in ((470.0, 0x7e), (-1e30, 0xfe), (float("inf"), 0x7e), (float("nan"), 0x7f)):
+        if lib.orc_e4m3_encode(v) != c:
+            raise AssertionError(f"E4M3 of {v}")
+
+
+def pin_shadow_refresh(lib):
+    """The read copy of a pool: fp16 codes are torch's round-to-nearest-even
+    cast; E4M3 codes and row scales equal a restatement with torch's
+    float8_e4m3fn cast (scale = amax / 448 in fp32, codes of v / scale); an
+    all-zero row gets scale 1 and zero codes."""
+    g = torch.Generator().manual_seed(62)
+    st = torch.randn((3, 2, 4, 32), generator=g) * torch.rand((3, 2, 4, 1), generator=g) * 5
+    st[1, 0, 2] = 0.0
+    h, none = oracle.shadow_refresh(st, oracle.SHADOW_F16, lib=lib)
+    if none is not None or not torch.equal(h, st.half()):
+        raise AssertionError("fp16 read copy")
+    codes, scale = oracle.shadow_refresh(st, oracle.SHADOW_E4M3, lib=lib)
+    amax = st.abs().amax(dim=-1)
+    want_scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    want_codes = (st / want_scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    if not (torch.equal(scale, want_scale) and torch.equal(codes, want_codes)):
+        raise AssertionError("E4M3 read copy")
+    if float(scale[1, 0, 2]) != 1.0 or int(codes[1, 0, 2].abs().sum()) != 0:
+        raise AssertionError("zero row")
+    bf = st.to(torch.bfloat16)  # a 16-bit pool: the copy is of the stored values
+    c16, s16 = oracle.shadow_refresh(bf, oracle.SHADOW_E4M3, lib=lib)
+    c32, s32 = oracle.shadow_refresh(bf.float(), oracle.SHADOW_E4M3, lib=lib)
+    if not (torch.equal(c16, c32) and torch.equal(s16, s32)):
+        raise AssertionError("bf16 pool read copy")
+
+
+def _e4m3_dequant(codes, scale):
+    return codes.view(torch.float8_e4m3fn).to(torch.float64) * scale.to(torch.float64)[..., None]
+
+
+def pin_replay_read_copy(lib):
+    """Steps that do not fold read the copy: with a checkpoint already on the
+    copy's grid (E4M3 codes times a row scale, or fp16 values) y is exactly
+    the y read from the checkpoint; with a general checkpoint y moves by no
+    more than the copy's rounding (half an E4M3 ulp, relative 2^-4, or the
+    subnormal quantum 2^-10 scale, per element), and does move.  A fold
+    writes the checkpoint and the copy of it; other steps leave the copy."""
+    L = 4
+    counts = [0, 1, 2, 3, 3, 2]
+    sc = _replay_scenario(44, L, counts, state_dtype=torch.float32)
+    ck = sc["ckpt"]
+    # a checkpoint on the E4M3 grid: codes times a power-of-two row scale,
+    # each row holding one 448 (so amax / 448 is that scale): its copy is exact
+    codes0, scale0 = oracle.shadow_refresh(ck, oracle.SHADOW_E4M3, lib=lib)
+    codes0[..., 0] = 0x7e
+    pow2 = torch.exp2(torch.round(torch.log2(scale0)))
+    grid = _e4m3_dequant(codes0, pow2).to(torch.float32)
+    sg = dict(sc, ckpt=grid)
+    cg, sgs = oracle.shadow_refresh(grid, oracle.SHADOW_E4M3, lib=lib)
+    plain = _run_replay(sg, lib)
+    r = _run_replay(sg, lib, shadow=cg, shadow_scale=sgs, shadow_format=oracle.SHADOW_E4M3)
+    if not torch.equal(r.y_exact, plain.y_exact):
+        raise AssertionError("an exact read copy must give the checkpoint's y")
+    h16 = ck.half().float()
+    sh = dict(sc, ckpt=h16)
+    p16 = _run_replay(sh, lib)
+    r16 = _run_replay(sh, lib, shadow=h16.half(), shadow_format=oracle.SHADOW_F16)
+    if not torch.equal(r16.y_exact, p16.y_exact):
+        raise AssertionError("an exact fp16 read copy must give the checkpoint's y")
+    # general checkpoint: bounded, nonzero change of the readout y
+    codes, scale = oracle.shadow_refresh(ck, oracle.SHADOW_E4M3, lib=lib)
+    plain = _run_replay(sc, lib)
+    r = _run_replay(sc, lib, shadow=codes, shadow_scale=scale, shadow_format=oracle.SHADOW_E4M3)
+    moved = False
+    for b, c in enumerate(counts):
+        s = int(sc["slot_of"][b])
+        if c + 1 == L:
+            if not torch.equal(r.y_exact[b], plain.y_exact[b]):
+                raise AssertionError("a folding step reads the checkpoint, not the copy")
+            cs, ss = oracle.shadow_refresh(r.ckpt[s], oracle.SHADOW_E4M3, lib=lib)
+            if not (torch.equal(r.shadow[s], cs) and torch.equal(r.shadow_scale[s], ss)):
+                raise AssertionError("a fold must rewrite the read copy from the new checkpoint")
+            continue
+        if not (torch.equal(r.shadow[s], codes[s]) and torch.equal(r.shadow_scale[s], scale[s])):
+            raise AssertionError("a step that does not fold must not write the read copy")
+        # |dy| <= gate * gamma * sum_n (2^-4 |S_n| + 2^-10 scale) |C_n|
+        g = sc["slot_of"]
+        Cb = sc["C"][b].double()
+        heads_per_group = ck.shape[1] // Cb.shape[0]
+        gamma = (plain.y_exact[b] - r.y_exact[b]).abs()
+        for h in range(ck.shape[1]):
+            Cg = Cb[h // heads_per_group]
+            err = (ck[s, h].double().abs() * 2.0 ** -4 + 2.0 ** -10 * scale[s, h].double()[:, None]) @ Cg.abs()
+            zz = sc["z"][b, h].double()
+            gate = (zz / (1 + torch.exp(-zz))).abs()
+            if not torch.all(gamma[h] <= gate * err * (1 + 1e-9) + 1e-12):
+                raise AssertionError("read-copy error above its bound")
+        if float(gamma.max()) > 0:
+            moved = True
+    if not moved:
+        raise AssertionError("the readout did not use the read copy")
+
+
 ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero, pin_zero_state,
             pin_A_zero, pin_decay_only, pin_unrolled, pin_basis_vectors, pin_group_map,
             pin_page_examples, pin_pad_never_written, pin_disable_and_untouched, pin_table_forms,
             pin_seed_position, pin_seed_position_per_row, pin_per_head_dt, pin_aliasing_refused,
             pin_replay_lossless, pin_replay_buffer_entries, pin_replay_buffer_len_one,
-            pin_replay_pad_and_aliasing, pin_empty_sequences, pin_bounded_decay]
+            pin_replay_pad_and_aliasing, pin_empty_sequences, pin_bounded_decay, pin_e4m3_codes,
+            pin_shadow_refresh, pin_replay_read_copy]

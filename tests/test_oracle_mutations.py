@@ -46,6 +46,14 @@ MUTATIONS = [
      "w *= exp(A * dj);\n                        hist += w * dj * xj * kq;"),
     ("dt_per_head_wrong_head", "const int64_t dti = pr->dt_per_head ? (r * H + h) : xi;",
      "const int64_t dti = pr->dt_per_head ? (r * H) : xi;"),
+    # the low-precision read copy of the checkpoint
+    ("read_copy_ignored", "sq += (pr->shadow_format != ORC_SHADOW_NONE", "sq += (0"),
+    ("e4m3_scale_240", "amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    ("fold_skips_read_copy",
+     "if (pr->shadow_format != ORC_SHADOW_NONE) {\n                            /* the read copy",
+     "if (0) {\n                            /* the read copy"),
+    ("e4m3_no_saturation", "if (isinf(r) || r > 448.0)\n        r = 448.0;", ""),
+    ("e4m3_exponent_bias", "ldexp((double)(f + 8), e - 10)", "ldexp((double)(f + 8), e - 11)"),
 ]
 
 
