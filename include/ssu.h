@@ -199,7 +199,27 @@ typedef struct ssu_replay_buffers {
     const int32_t *count_in;   /* device [batch]: entries buffered for sequence b          */
     int32_t *count_out;        /* device [batch]: entries after the call (written); must
                                   not alias count_in                                      */
+    /* Optional low-precision read copy of the checkpoints (article
+     * "ReplaySSM", section 低精度读写分离): steps that do not fold read it
+     * instead of the checkpoint, a fold rewrites it from the new checkpoint
+     * (as ssu_shadow_refresh would).  It never feeds the recurrence. */
+    int32_t shadow_format;     /* SSU_SHADOW_NONE, _F16 or _E4M3                          */
+    int32_t reserved0;         /* must be 0                                               */
+    void *shadow;              /* device [slots, heads, dim, dstate]: fp16 values or E4M3
+                                  codes (one byte), 16-byte aligned                       */
+    float *shadow_scale;       /* device [slots, heads, dim] fp32 row scales (E4M3 only),
+                                  16-byte aligned                                         */
 } ssu_replay_buffers;
+
+/* Formats of the read copy.  E4M3 is OCP FP8 E4M3 (bias 7, 3 fraction bits,
+ * no infinities, largest 448) with one fp32 scale per state row:
+ * scale = amax / 448 over the row's stored values (1 for an all-zero row),
+ * code = E4M3(v / scale) rounded to nearest even and clamped to +-448, the
+ * quotient and the scale computed in fp32.  F16 is binary16, round to nearest
+ * even. */
+#define SSU_SHADOW_NONE 0
+#define SSU_SHADOW_F16  1
+#define SSU_SHADOW_E4M3 2
 
 /*
  * One decode token per sequence on the checkpoint + buffer form of the state
@@ -221,6 +241,9 @@ typedef struct ssu_replay_buffers {
  * slot.  A pad slot reads as a zero state with no history: y from the current
  * token alone, nothing written, count_out[b] = 0.  A count outside [0, L) sets
  * SSU_DEV_BAD_COUNT and skips the sequence.  disable_state_update must be 0.
+ * With a read copy (rb->shadow_format != SSU_SHADOW_NONE) the S_ckpt.C of a
+ * step that does not fold comes from the copy; dim must be a multiple of 4
+ * for E4M3 (row scales move in 16-byte pieces).
  * The dstate and dtype rules of ssu_update_onetoken apply.  batch == 0
  * launches nothing.
  */
@@ -259,6 +282,16 @@ typedef struct ssu_copy {
  */
 ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes, int32_t *d_status,
                           void *stream);
+
+/*
+ * The read copy (see ssu_replay_buffers) of `rows` consecutive state rows of
+ * `dstate` elements: state rows r in [0, rows) of `state` (state_dtype) into
+ * `shadow` rows (format SSU_SHADOW_F16 or SSU_SHADOW_E4M3) and, for E4M3,
+ * `scale[r]`.  Use it to build the copy of checkpoints written by other
+ * means (a prefill, a copy).  rows == 0 launches nothing.
+ */
+ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate,
+                              int32_t format, void *shadow, float *scale, void *stream);
 
 /*
  * Get the kernel for one configuration ready before any CUDA graph capture:

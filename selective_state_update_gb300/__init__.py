@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
                        checkpoint plus a buffer of recent inputs
   ssu_update_packed    packed variable-length / MTP rows (cu_seqlens) or the
                        dense [batch, steps, heads, dim] form
+  ssu_shadow_refresh   the low-precision read copy of checkpoints
   ssu_batch_copy       batched state copies with memmove semantics
   ssu_prewarm          load a configuration's kernel before graph capture
 and ``selective_state_update``, the MATE/FlashInfer-shaped call (MATE
@@ -26,7 +27,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_batch_copy", "copy_table",
+__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_shadow_refresh",
+           "ssu_batch_copy", "copy_table",
            "slot_copies", "ssu_prewarm",
            "selective_state_update",
            "SLOTS_STRIDED", "SLOTS_PER_ROW", "DEV_BAD_SLOT", "DEV_BAD_ENTRY", "DEV_BAD_SEQLEN", "DEV_TIMEOUT",
@@ -72,7 +74,23 @@ class Args(ctypes.Structure):
 
 class ReplayBuffers(ctypes.Structure):
     _fields_ = [("len", ctypes.c_int64), ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p),
-                ("B", ctypes.c_void_p), ("count_in", ctypes.c_void_p), ("count_out", ctypes.c_void_p)]
+                ("B", ctypes.c_void_p), ("count_in", ctypes.c_void_p), ("count_out", ctypes.c_void_p),
+                ("shadow_format", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("shadow", ctypes.c_void_p),
+                ("shadow_scale", ctypes.c_void_p)]
+
+
+# formats of the read copy (SSU_SHADOW_*)
+SHADOW_NONE, SHADOW_F16, SHADOW_E4M3 = 0, 1, 2
+
+
+def _shadow_format(shadow: Optional[torch.Tensor]) -> int:
+    if shadow is None:
+        return SHADOW_NONE
+    if shadow.dtype == torch.float16:
+        return SHADOW_F16
+    if shadow.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        return SHADOW_E4M3
+    raise ValueError("a read copy is float16 (fp16 values) or uint8 / float8_e4m3fn (E4M3 codes)")
 
 
 _lib = None
@@ -104,6 +122,9 @@ def lib():
         L.ssu_batch_copy.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
                                      ctypes.c_void_p]
         L.ssu_batch_copy.restype = ctypes.c_int
+        L.ssu_shadow_refresh.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        L.ssu_shadow_refresh.restype = ctypes.c_int
         L.ssu_prewarm.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
         L.ssu_prewarm.restype = ctypes.c_int
@@ -281,7 +302,7 @@ def ssu_update_packed(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
 
 def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, count_out=None, D=None, z=None,
                       dt_bias=None, dt_softplus=False, state_batch_indices=None, pad_slot_id=-1, out=None,
-                      status=None, stream=None):
+                      status=None, stream=None, shadow=None, shadow_scale=None):
     """One decode token per sequence on the checkpoint + buffer form of the
     state (article "ReplaySSM: Cache SSM Inputs, Not State", section 核心做法).
 
@@ -312,13 +333,42 @@ def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
     _need(all(t.is_cuda for t in (x_buf, dt_buf, B_buf)), "buffers must be CUDA tensors")
     a = _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, status, 0)
     rt = _table(state_batch_indices, SLOTS_STRIDED)
+    fmt = _shadow_format(shadow)
+    if fmt != SHADOW_NONE:
+        _need(shadow.is_cuda and shadow.is_contiguous() and tuple(shadow.shape) == tuple(state.shape),
+              "the read copy must be a contiguous CUDA tensor shaped like the checkpoints")
+        if fmt == SHADOW_E4M3:
+            _need(shadow_scale is not None and shadow_scale.dtype == torch.float32 and shadow_scale.is_cuda
+                  and shadow_scale.is_contiguous() and tuple(shadow_scale.shape) == tuple(state.shape[:-1]),
+                  "an E4M3 read copy needs contiguous fp32 row scales [slots, heads, dim]")
     rb = ReplayBuffers(L, x_buf.data_ptr(), dt_buf.data_ptr(), B_buf.data_ptr(), count_in.data_ptr(),
-                       count_out.data_ptr())
+                       count_out.data_ptr(), fmt, 0, _ptr(shadow),
+                       _ptr(shadow_scale) if fmt == SHADOW_E4M3 else None)
     rc = lib().ssu_replay_update(ctypes.byref(a), batch, None if rt is None else ctypes.byref(rt),
                                  ctypes.byref(rb), _stream(stream))
     if rc != OK:
         _raise(rc)
     return out, count_out
+
+
+def ssu_shadow_refresh(state: torch.Tensor, shadow: torch.Tensor, shadow_scale: Optional[torch.Tensor] = None,
+                       stream=None) -> None:
+    """The low-precision read copy of a contiguous state tensor ``[..., dstate]``
+    into ``shadow`` (float16, or uint8 / float8_e4m3fn E4M3 codes with fp32
+    ``shadow_scale`` of shape ``state.shape[:-1]``)."""
+    fmt = _shadow_format(shadow)
+    _need(fmt != SHADOW_NONE, "shadow must be given")
+    _need(state.is_cuda and state.is_contiguous() and shadow.is_cuda and shadow.is_contiguous()
+          and shadow.shape == state.shape, "state and shadow must be contiguous CUDA tensors of one shape")
+    if fmt == SHADOW_E4M3:
+        _need(shadow_scale is not None and shadow_scale.dtype == torch.float32 and shadow_scale.is_contiguous()
+              and tuple(shadow_scale.shape) == tuple(state.shape[:-1]), "E4M3 needs fp32 row scales")
+    dstate = state.shape[-1]
+    rc = lib().ssu_shadow_refresh(state.data_ptr(), _DTYPE[state.dtype], state.numel() // dstate, dstate, fmt,
+                                  shadow.data_ptr(), _ptr(shadow_scale) if fmt == SHADOW_E4M3 else None,
+                                  _stream(stream))
+    if rc != OK:
+        _raise(rc)
 
 
 def ssu_batch_copy(copies: torch.Tensor, max_bytes: int, status: Optional[torch.Tensor] = None,

@@ -233,6 +233,22 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
                              reinterpret_cast<uintptr_t>(rb->B) % 16 == 0;
         kp.rbulk = aligned && (args->dim * io) % 16 == 0 && (args->dim * 4) % 16 == 0 && (args->dstate * io) % 16 == 0;
     }
+    if (rb->reserved0 != 0) return fail(SSU_ERR_INVALID, "replay buffers: reserved0 must be 0");
+    kp.shadow_fmt = rb->shadow_format;
+    if (rb->shadow_format != SSU_SHADOW_NONE) {
+        if (rb->shadow_format != SSU_SHADOW_F16 && rb->shadow_format != SSU_SHADOW_E4M3)
+            return fail(SSU_ERR_INVALID, "shadow_format %d is not an SSU_SHADOW_* value", rb->shadow_format);
+        if (rb->shadow == nullptr || reinterpret_cast<uintptr_t>(rb->shadow) % 16 != 0)
+            return fail(SSU_ERR_INVALID, "the read copy must be a 16-byte aligned device pointer");
+        if (rb->shadow_format == SSU_SHADOW_E4M3) {
+            if (rb->shadow_scale == nullptr || reinterpret_cast<uintptr_t>(rb->shadow_scale) % 16 != 0)
+                return fail(SSU_ERR_INVALID, "E4M3 row scales must be a 16-byte aligned device pointer");
+            if (args->dim % 4 != 0)
+                return fail(SSU_ERR_UNSUPPORTED, "an E4M3 read copy needs dim to be a multiple of 4");
+        }
+        kp.shadow = rb->shadow;
+        kp.shadow_scale = rb->shadow_scale;
+    }
     return launched(ssu::launch_replay(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
 }
 
@@ -245,6 +261,19 @@ ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes,
     if (d_status != nullptr && reinterpret_cast<uintptr_t>(d_status) % 4 != 0)
         return fail(SSU_ERR_INVALID, "d_status must be 4-byte aligned");
     return launched(ssu::launch_copy(copies, n, max_bytes, d_status, static_cast<cudaStream_t>(stream)));
+}
+
+ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate,
+                              int32_t format, void *shadow, float *scale, void *stream) {
+    if (!valid_dtype(state_dtype)) return fail(SSU_ERR_INVALID, "state_dtype %d is not an ssu_dtype", state_dtype);
+    if (format != SSU_SHADOW_F16 && format != SSU_SHADOW_E4M3)
+        return fail(SSU_ERR_INVALID, "format %d is not SSU_SHADOW_F16 or SSU_SHADOW_E4M3", format);
+    if (rows < 0 || dstate <= 0 || dstate > 4096) return fail(SSU_ERR_INVALID, "rows must be >= 0, dstate in [1, 4096]");
+    if (rows == 0) return ok();
+    if (!state || !shadow || (format == SSU_SHADOW_E4M3 && !scale))
+        return fail(SSU_ERR_INVALID, "state, shadow (and scale for E4M3) must not be NULL");
+    return launched(ssu::launch_shadow_refresh(state, state_dtype, rows, static_cast<int>(dstate), format, shadow,
+                                               scale, static_cast<cudaStream_t>(stream)));
 }
 
 ssu_status ssu_prewarm(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype, int64_t heads, int64_t dim,

@@ -15,6 +15,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "ssu_internal.h"
@@ -34,6 +35,22 @@ template <bool WIDE>
 __device__ __forceinline__ uint32_t load_bits(const void *base, int64_t i) {
     if (WIDE) return __ldg(static_cast<const unsigned int *>(base) + i);
     return __ldg(static_cast<const unsigned short *>(base) + i);
+}
+
+__device__ __forceinline__ float to_float(float v) { return v; }
+__device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// The low-precision read copy of a state row (article "ReplaySSM", section
+// 低精度读写分离), E4M3 form: scale = amax / 448 in fp32 (1 for an all-zero
+// row), code = E4M3(v / scale), the quotient in fp32, rounded to nearest even
+// and clamped to +-448 (the conversion's saturate-to-finite mode).
+__device__ __forceinline__ float shadow_scale_of(float amax) { return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f; }
+__device__ __forceinline__ unsigned char e4m3_code(float v) {
+    return static_cast<unsigned char>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_value(unsigned int code) {
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3)));
 }
 
 __device__ __forceinline__ float bits_to_float(uint32_t v, int dtype) {

@@ -67,7 +67,13 @@ struct KParams {
     const int32_t *cnt_in;
     int32_t *cnt_out;
     int32_t rbulk;  // buffer rows are 16-byte aligned: stage them with bulk copies
+    // low-precision read copy of the checkpoints (kShadow*)
+    int32_t shadow_fmt;
+    void *shadow;
+    float *shadow_scale;
 };
+
+enum : int32_t { kShadowNone = 0, kShadowF16 = 1, kShadowE4M3 = 2 };
 
 // Launchers (one translation unit per kernel).  `lanes` = dstate / 16.
 cudaError_t launch_onetoken(int state_dtype, int lanes, const KParams &p, int64_t batch,
@@ -77,6 +83,9 @@ cudaError_t launch_packed(int state_dtype, int lanes, const KParams &p, cudaStre
 cudaError_t prewarm_onetoken(int state_dtype, int lanes);
 cudaError_t prewarm_packed(int state_dtype, int lanes);
 cudaError_t launch_replay(int state_dtype, int lanes, const KParams &p, int64_t batch, cudaStream_t stream);
+// The read copy of `rows` state rows (ssu_shadow_refresh).
+cudaError_t launch_shadow_refresh(const void *state, int state_dtype, int64_t rows, int dstate, int format,
+                                  void *shadow, float *scale, cudaStream_t stream);
 // Batched copies (ssu_batch_copy): `copies` device [n] {src, dst, bytes}.
 cudaError_t launch_copy(const void *copies, int64_t n, uint64_t max_bytes, int32_t *status, cudaStream_t stream);
 

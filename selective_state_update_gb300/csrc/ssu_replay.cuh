@@ -70,6 +70,10 @@ struct ReplayPipe {
     // producers than stages, so a one-stage ring runs one producer.
     static constexpr int kProducerWarps = 2;
     static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+    // Where the E4M3 row scales of a read copy sit in a stage: after the
+    // largest copy tile (one byte per element), inside the checkpoint tile.
+    static constexpr int kShadowScaleOffset = kTileRows * kN;
+    static_assert(kShadowScaleOffset + kTileRows * 4 <= kTileBytes, "read-copy scales do not fit the tile");
     // Dynamic shared memory an SM can give its CTAs (228 KB less 1 KB per CTA).
     static constexpr int kSmemPerSm = 222 * 1024;
     // Register budget: two CTAs per SM where a tile and a few KB of entries
@@ -313,6 +317,102 @@ __device__ __forceinline__ void entry_terms(int c, int rows, float Ah, const flo
     }
 }
 
+// This thread's 16 values of row rr of a read copy staged in shared memory
+// (E4M3 codes times nothing -- the caller applies the row scale -- or fp16),
+// in the element layout of Tile::gather.
+template <typename TS, int L>
+__device__ __forceinline__ void load_copy_row(const unsigned char *tile, int rr, int lane, int fmt, float *v) {
+    using T = Tile<TS, L>;
+    constexpr int V = T::kVec;
+    constexpr int N = T::kN;
+#pragma unroll
+    for (int k = 0; k < T::kChunks; ++k) {
+        const int e0 = (lane + L * k) * V;
+        if (fmt == kShadowE4M3) {
+            uint32_t w[V / 4];
+            if constexpr (V == 8) {
+                const uint2 u = *reinterpret_cast<const uint2 *>(tile + rr * N + e0);
+                w[0] = u.x, w[1] = u.y;
+            } else {
+                w[0] = *reinterpret_cast<const uint32_t *>(tile + rr * N + e0);
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i) v[k * V + i] = e4m3_value((w[i / 4] >> (8 * (i % 4))) & 0xffu);
+        } else {
+            uint32_t w[V / 2];
+            const unsigned char *src = tile + (rr * N + e0) * 2;
+            if constexpr (V == 8) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(src);
+                w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+            } else {
+                const uint2 u = *reinterpret_cast<const uint2 *>(src);
+                w[0] = u.x, w[1] = u.y;
+            }
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                v[k * V + 2 * i] = bits_to_float(w[i] & 0xffffu, kF16);
+                v[k * V + 2 * i + 1] = bits_to_float(w[i] >> 16, kF16);
+            }
+        }
+    }
+}
+
+// Writes the read copy of one folded state row (this thread's 16 values `sv`
+// as the pool stores them) to global memory: E4M3 codes and the row scale,
+// or fp16.  Every lane of the row takes part (the row maximum is a shuffle);
+// only `live` rows are written.
+template <typename TS, int L>
+__device__ __forceinline__ void write_copy_row(const KParams &p, int64_t row, int lane, bool live, const float *sv) {
+    using T = Tile<TS, L>;
+    constexpr int V = T::kVec;
+    constexpr int N = T::kN;
+    float st[kElemsPerThread];
+    if constexpr (sizeof(TS) == 4) {
+#pragma unroll
+        for (int i = 0; i < kElemsPerThread; ++i) st[i] = sv[i];
+    } else {
+#pragma unroll
+        for (int k = 0; k < T::kChunks; ++k) StateChunk<TS>::unpack(StateChunk<TS>::pack(sv + k * V), st + k * V);
+    }
+    if (p.shadow_fmt == kShadowE4M3) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kElemsPerThread; ++i) amax = fmaxf(amax, fabsf(st[i]));
+#pragma unroll
+        for (int off = L / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float sc = shadow_scale_of(amax);
+        if (!live) return;
+        unsigned char *out = static_cast<unsigned char *>(p.shadow) + row * N;
+#pragma unroll
+        for (int k = 0; k < T::kChunks; ++k) {
+            uint32_t w[V / 4] = {};
+#pragma unroll
+            for (int i = 0; i < V; ++i) w[i / 4] |= uint32_t(e4m3_code(__fdiv_rn(st[k * V + i], sc))) << (8 * (i % 4));
+            unsigned char *dst = out + (lane + L * k) * V;
+            if constexpr (V == 8)
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+            else
+                *reinterpret_cast<uint32_t *>(dst) = w[0];
+        }
+        if (lane == 0) p.shadow_scale[row] = sc;
+    } else if (live) {
+        unsigned char *out = static_cast<unsigned char *>(p.shadow) + row * N * 2;
+#pragma unroll
+        for (int k = 0; k < T::kChunks; ++k) {
+            uint32_t w[V / 2];
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i)
+                w[i] = uint32_t(__half_as_ushort(__float2half_rn(st[k * V + 2 * i]))) |
+                       (uint32_t(__half_as_ushort(__float2half_rn(st[k * V + 2 * i + 1]))) << 16);
+            unsigned char *dst = out + (lane + L * k) * V * 2;
+            if constexpr (V == 8)
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            else
+                *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+        }
+    }
+}
+
 // The operands of one unit plus its slot's buffered count (lane 0).
 template <typename TS, int L>
 struct ReplayOperands : UnitOperands<TS, L> {
@@ -458,14 +558,23 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
     // copies; lane 0 registers the total before any copy can complete.  (One
     // copy per entry and buffer measured faster than one run per buffer of a
     // head-major buffer layout.)
-    const uint32_t tile_bytes = static_cast<uint32_t>(rows) * N * sizeof(TS);
-    uint32_t bytes = tile_bytes;
+    // A step that does not fold reads the read copy when there is one
+    // (codes, then E4M3 row scales at kShadowScaleOffset), else the tile.
+    const bool read_copy = p.shadow_fmt != kShadowNone && !(flags & kRFold);
+    const int64_t row_first = (rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0;
+    const uint32_t tile_bytes =
+        static_cast<uint32_t>(rows) * N * (read_copy ? (p.shadow_fmt == kShadowF16 ? 2 : 1) : sizeof(TS));
+    const uint32_t scale_bytes = read_copy && p.shadow_fmt == kShadowE4M3 ? static_cast<uint32_t>(rows) * 4 : 0;
+    uint32_t bytes = tile_bytes + scale_bytes;
     if (bulk_entries) bytes += static_cast<uint32_t>(c) * (rows * (io + 4) + N * io);
     if (lane == 0) mbar_arrive_expect(&full[s], bytes);
     __syncwarp();
+    if (scale_bytes != 0 && lane == 31)
+        bulk_load(base + ReplayPipe<TS, L>::kShadowScaleOffset, p.shadow_scale + row_first, scale_bytes, &full[s]);
     {
-        const unsigned char *src = reinterpret_cast<const unsigned char *>(
-            static_cast<const TS *>(p.state) + ((rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0) * N);
+        const unsigned char *src =
+            read_copy ? static_cast<const unsigned char *>(p.shadow) + row_first * N * (p.shadow_fmt == kShadowF16 ? 2 : 1)
+                      : reinterpret_cast<const unsigned char *>(static_cast<const TS *>(p.state) + row_first * N);
         for (uint32_t off = static_cast<uint32_t>(lane) * kReplayTileChunk; off < tile_bytes;
              off += 32u * kReplayTileChunk)
             bulk_load(base + off, src + off, tile_bytes - off < kReplayTileChunk ? tile_bytes - off : kReplayTileChunk,
@@ -563,7 +672,7 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
                 // S_ckpt . C of this thread's rows (every lane of a row ends
                 // with the sum) beside the B_j . C dots.
                 float rsum[kRowsPerThread];
-                if (active) {
+                if (active && p.shadow_fmt == kShadowNone) {
 #pragma unroll
                     for (int j = 0; j < kRowsPerThread; ++j) {
                         const int rr = slot_row + j * kRowSlots;  // row within the tile
@@ -573,6 +682,21 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
 #pragma unroll
                         for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
                         rsum[j] = row_sum<L>(acc);
+                    }
+                } else if (active) {
+                    // from the read copy: codes (times the row scale) or fp16
+                    const unsigned char *copy = reinterpret_cast<const unsigned char *>(tile);
+                    const float *rscale = reinterpret_cast<const float *>(copy + PS::kShadowScaleOffset);
+#pragma unroll
+                    for (int j = 0; j < kRowsPerThread; ++j) {
+                        const int rr = slot_row + j * kRowSlots;
+                        const int rq = rr < rows ? rr : 0;
+                        float sv[kElemsPerThread];
+                        load_copy_row<TS, L>(copy, rq, lane, p.shadow_fmt, sv);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
+                        rsum[j] = row_sum<L>(acc) * (p.shadow_fmt == kShadowE4M3 ? rscale[rq] : 1.f);
                     }
                 }
                 entry_dots<N, kConsumers, IO>(c, be, sB, sC, dots, tid);
@@ -675,6 +799,9 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
                             store_small(p.y, cu.b * p.ys[0] + cu.h * p.ys[1] + (cu.row0 + rr) * p.ys[2], IO,
                                         output(sum, Dh, q.z, q.w));
                         if (live && seeded) T::store_row_smem(tile + rr * N, lane, sv);
+                        if (seeded && p.shadow_fmt != kShadowNone)
+                            write_copy_row<TS, L>(p, (hd->slot * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + rr,
+                                                  lane, live, sv);
                     }
                 }
             }

@@ -1,0 +1,63 @@
+// ssu_shadow.cu -- the low-precision read copy of state rows.
+//
+// Article "ReplaySSM: Cache SSM Inputs, Not State", section 低精度读写分离:
+// the steps that do not fold read the checkpoint only to form the output, so
+// they can read a low-precision copy of it while the recurrence keeps the
+// full-precision checkpoint; the copy never feeds the recurrence.  This
+// kernel builds the copy of rows written by other means; a fold of the
+// replay kernel rewrites the copy of the rows it folds with the same
+// arithmetic (shadow_scale / e4m3_code in ssu_device.cuh).
+//
+// One warp per state row: the row's largest magnitude (an exact maximum),
+// its scale amax / 448 in fp32, then each element's code.
+#include "ssu_device.cuh"
+
+namespace ssu {
+
+template <typename TS>
+__global__ void __launch_bounds__(256)
+    ssu_shadow_refresh_kernel(const TS *state, int64_t rows, int dstate, int format, void *shadow, float *scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; r < rows; r += nwarps) {
+        const TS *row = state + r * dstate;
+        if (format == kShadowF16) {
+            __half *out = static_cast<__half *>(shadow) + r * dstate;
+            for (int n = lane; n < dstate; n += 32) out[n] = __float2half_rn(to_float(row[n]));
+            continue;
+        }
+        float amax = 0.f;
+        for (int n = lane; n < dstate; n += 32) amax = fmaxf(amax, fabsf(to_float(row[n])));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float s = shadow_scale_of(amax);
+        if (lane == 0) scale[r] = s;
+        unsigned char *out = static_cast<unsigned char *>(shadow) + r * dstate;
+        for (int n = lane; n < dstate; n += 32) out[n] = e4m3_code(__fdiv_rn(to_float(row[n]), s));
+    }
+}
+
+cudaError_t launch_shadow_refresh(const void *state, int state_dtype, int64_t rows, int dstate, int format,
+                                  void *shadow, float *scale, cudaStream_t stream) {
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    const unsigned g = static_cast<unsigned>(blocks);
+    switch (state_dtype) {
+    case kF32:
+        ssu_shadow_refresh_kernel<float><<<g, 256, 0, stream>>>(static_cast<const float *>(state), rows, dstate,
+                                                                format, shadow, scale);
+        break;
+    case kF16:
+        ssu_shadow_refresh_kernel<__half><<<g, 256, 0, stream>>>(static_cast<const __half *>(state), rows, dstate,
+                                                                 format, shadow, scale);
+        break;
+    case kBF16:
+        ssu_shadow_refresh_kernel<__nv_bfloat16><<<g, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(state), rows, dstate, format, shadow, scale);
+        break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ssu

@@ -59,9 +59,11 @@ def test_struct_layout_matches_the_header():
 #include <stdio.h>
 #include "ssu.h"
 int main(void) {
-  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(ssu_args), sizeof(ssu_slot_table),
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\n", sizeof(ssu_args), sizeof(ssu_slot_table),
          offsetof(ssu_args, pad_slot_id), offsetof(ssu_args, state), offsetof(ssu_args, x_stride),
-         offsetof(ssu_args, d_status), offsetof(ssu_slot_table, s0));
+         offsetof(ssu_args, d_status), offsetof(ssu_slot_table, s0), sizeof(ssu_replay_buffers),
+         offsetof(ssu_replay_buffers, shadow_format), offsetof(ssu_replay_buffers, shadow_scale),
+         sizeof(ssu_copy));
   return 0;
 }
 '''
@@ -70,9 +72,10 @@ int main(void) {
     subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-x", "c", "-", "-o", exe],
                    input=probe, text=True, check=True)
     vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
-    A, T = ssu.Args, ssu.SlotTable
+    A, T, R = ssu.Args, ssu.SlotTable, ssu.ReplayBuffers
     assert vals == [ctypes.sizeof(A), ctypes.sizeof(T), A.pad_slot_id.offset, A.state.offset,
-                    A.x_stride.offset, A.d_status.offset, T.s0.offset]
+                    A.x_stride.offset, A.d_status.offset, T.s0.offset, ctypes.sizeof(R), R.shadow_format.offset,
+                    R.shadow_scale.offset, 24]
 
 
 def _args(**kw):
@@ -140,3 +143,11 @@ def test_batch_copy_host_checks(libssu):
     assert "NULL" in libssu.ssu_last_error().decode()
     assert libssu.ssu_batch_copy(12, 3, 16, None, None) == ssu.ERR_INVALID
     assert "aligned" in libssu.ssu_last_error().decode()
+
+
+def test_shadow_refresh_host_checks(libssu):
+    assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 3, 32, 48, None) == ssu.ERR_INVALID     # format
+    assert libssu.ssu_shadow_refresh(16, 9, 4, 128, 2, 32, 48, None) == ssu.ERR_INVALID     # state dtype
+    assert libssu.ssu_shadow_refresh(16, 0, 0, 128, 2, None, None, None) == ssu.OK          # nothing to do
+    assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 2, 32, None, None) == ssu.ERR_INVALID   # E4M3 without scales
+    assert "NULL" in libssu.ssu_last_error().decode()

@@ -204,3 +204,102 @@ def test_replay_b256_sampled(libssu):
         if s != 0 and int(w.count[b]) + 1 < L:
             c = int(w.count[b])
             assert torch.equal(g.xbuf[s, c].cpu(), ref.xbuf[m[s], c])
+
+
+# ---------------------------------------------------------------------------
+# The low-precision read copy (article "ReplaySSM", section 低精度读写分离).
+# ---------------------------------------------------------------------------
+_FMT = {"f16": (oracle.SHADOW_F16, torch.float16), "e4m3": (oracle.SHADOW_E4M3, torch.uint8)}
+
+
+@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16, torch.bfloat16])
+def test_shadow_refresh_is_the_oracles(libssu, fmt, state_dtype):
+    """The GPU's read copy of a pool equals the oracle's bit for bit (the
+    codes are decided in fp32 on both sides)."""
+    code, dtype = _FMT[fmt]
+    g = torch.Generator().manual_seed(70)
+    st = (torch.randn((5, 3, 20, 128), generator=g) * torch.rand((5, 3, 20, 1), generator=g) * 3).to(state_dtype)
+    st[2, 1, 7] = 0
+    want, want_scale = oracle.shadow_refresh(st, code)
+    sh = torch.empty(st.shape, dtype=dtype, device=DEV)
+    sc = torch.empty(st.shape[:-1], dtype=torch.float32, device=DEV) if fmt == "e4m3" else None
+    ssu.ssu_shadow_refresh(st.to(DEV), sh, sc)
+    torch.cuda.synchronize()
+    assert torch.equal(sh.cpu().view(want.dtype), want)
+    if fmt == "e4m3":
+        assert torch.equal(sc.cpu(), want_scale)
+
+
+def _check_read_copy(w, fmt):
+    code, dtype = _FMT[fmt]
+    sh0, sc0 = oracle.shadow_refresh(w.state, code)
+    ref = oracle.replay(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count, D=w.D, z=w.z,
+                        dt_bias=w.dt_bias, dt_softplus=w.dt_softplus, slot_of=w.read, pad_slot_id=w.pad_slot_id,
+                        shadow=sh0, shadow_scale=sc0, shadow_format=code)
+    g = w.to(DEV)
+    sh = sh0.to(DEV).view(dtype)
+    sc = None if sc0 is None else sc0.to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y, cnt = ssu.ssu_replay_update(g.state, g.x, g.dt, g.A, g.B, g.C, g.xbuf, g.dtbuf, g.Bbuf, g.count, D=g.D,
+                                   z=g.z, dt_bias=g.dt_bias, dt_softplus=g.dt_softplus, state_batch_indices=g.read,
+                                   pad_slot_id=g.pad_slot_id, status=status, shadow=sh, shadow_scale=sc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_y_close(y, ref.y_exact)
+    assert torch.equal(cnt.cpu().long(), ref.count)
+    L = w.xbuf.shape[1]
+    got = g.state.cpu()
+    folded = [int(w.read[b]) if w.read is not None else b for b in range(w.nseq)
+              if (int(w.read[b]) if w.read is not None else b) != w.pad_slot_id and int(w.count[b]) + 1 == L]
+    keep = torch.ones(w.state.shape[0], dtype=torch.bool)
+    keep[folded] = False
+    assert torch.equal(got[keep], w.state[keep])
+    if folded:
+        assert_state_close(got[folded], ref.ckpt[folded], what="folded checkpoint")
+    # the read copy: untouched where nothing folds; where a slot folds, the
+    # copy of the checkpoint the GPU wrote (same decisions, same fp32 values)
+    sh_got = sh.cpu().view(sh0.dtype)
+    assert torch.equal(sh_got[keep], sh0[keep]), "a read copy changed without a fold"
+    if folded:
+        want, want_scale = oracle.shadow_refresh(got[folded], code)
+        assert torch.equal(sh_got[folded], want), "a fold's read copy differs from the copy of its checkpoint"
+        if sc is not None:
+            assert torch.equal(sc.cpu()[folded], want_scale)
+            assert torch.equal(sc.cpu()[keep], sc0[keep])
+    assert torch.equal(g.xbuf.cpu(), ref.xbuf) and torch.equal(g.Bbuf.cpu(), ref.Bbuf)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("buffer_len", [1, 3, 16])
+def test_replay_read_copy_against_oracle(libssu, fmt, state_dtype, buffer_len):
+    w = workloads.replay_problem(80 + buffer_len, slots=40, heads=4, groups=2, dim=16, dstate=64, nseq=12,
+                                 buffer_len=buffer_len, state_dtype=state_dtype)
+    _check_read_copy(w, fmt)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("dstate,dim", [(16, 8), (128, 100), (256, 64)])
+def test_replay_read_copy_shapes(libssu, fmt, dstate, dim):
+    if fmt == "e4m3" and dim % 4:
+        pytest.skip("E4M3 row scales need dim % 4 == 0")
+    w = workloads.replay_problem(90 + dstate + dim, slots=24, heads=6, groups=3, dim=dim, dstate=dstate, nseq=5,
+                                 buffer_len=5)
+    _check_read_copy(w, fmt)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+def test_replay_read_copy_many_units(libssu, fmt):
+    w = workloads.replay_problem(95, slots=96, heads=24, groups=4, dim=128, dstate=64, nseq=80, buffer_len=7,
+                                 pad_frac=0.1)
+    _check_read_copy(w, fmt)
+
+
+def test_read_copy_e4m3_needs_dim_multiple_of_4(libssu):
+    w = workloads.replay_problem(96, slots=8, heads=2, groups=1, dim=6, dstate=32, nseq=2, buffer_len=2).to(DEV)
+    sh = torch.zeros(w.state.shape, dtype=torch.uint8, device=DEV)
+    sc = torch.ones(w.state.shape[:-1], dtype=torch.float32, device=DEV)
+    with pytest.raises(NotImplementedError):
+        ssu.ssu_replay_update(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count, D=w.D,
+                              z=w.z, state_batch_indices=w.read, shadow=sh, shadow_scale=sc)
