@@ -50,6 +50,10 @@ DESCRIPTIONS = {
     "replay_b256_fp32": "one-token decode on the checkpoint + buffer form (ReplaySSM), batch 256, heads 128, "
                         "dim 64, dstate 128, groups 8, fp32 checkpoints (512 slots), buffer length 16, "
                         "sequence b starting with b % 16 buffered entries (1/16 of the sequences fold per step)",
+    "replay_e4m3_b256_fp32": "replay_b256_fp32 with an E4M3 read copy of the checkpoints (one fp32 scale per "
+                             "state row): steps that do not fold read the copy, folds rewrite it",
+    "replay_f16copy_b256_fp32": "replay_b256_fp32 with an fp16 read copy of the checkpoints: steps that do not "
+                                "fold read the copy, folds rewrite it",
     "copy_slots_b256_fp32": "256 whole-slot state copies of 4 MiB (heads 128, dim 64, dstate 128, fp32) between "
                             "random disjoint slot sets of a 512-slot pool; steps alternate the direction",
 }
@@ -94,6 +98,10 @@ def replay_bytes(w) -> dict:
     H, P, N = w.state.shape[1:]
     G = w.B.shape[1]
     sb = H * P * N * w.state.element_size()
+    # a read copy: what a step that does not fold reads instead of the
+    # checkpoint, and what a fold writes besides it
+    cb = sb if w.shadow is None else (H * P * N * w.shadow.element_size()
+                                      + (0 if w.shadow_scale is None else H * P * 4))
     io = w.x.element_size()
     entry = H * P * (io + 4) + G * N * io
     L = w.xbuf.shape[1]
@@ -103,9 +111,9 @@ def replay_bytes(w) -> dict:
     for b, c in enumerate(counts):
         if slots[b] == w.pad_slot_id:
             continue
-        rd += sb + c * entry
+        rd += (sb if c + 1 == L else cb) + c * entry
         if c + 1 == L:
-            wr += sb
+            wr += sb + (cb if w.shadow is not None else 0)
             folds += 1
         else:
             wr += entry
@@ -289,7 +297,8 @@ def _call(ssu, w, out, stream=None):
         y, cnt = ssu.ssu_replay_update(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count,
                                        count_out=spare, D=w.D, z=w.z, dt_bias=w.dt_bias,
                                        dt_softplus=w.dt_softplus, state_batch_indices=w.read,
-                                       pad_slot_id=w.pad_slot_id, out=out, stream=stream)
+                                       pad_slot_id=w.pad_slot_id, out=out, stream=stream, shadow=w.shadow,
+                                       shadow_scale=w.shadow_scale)
         w.meta["count_spare"], w.count = w.count, cnt
         return y
     return ssu.ssu_update_packed(w.state, w.x, w.dt, w.A, w.B, w.C, cu_seqlens=w.cu_seqlens,
@@ -530,9 +539,14 @@ def _sample_problem(w, seqs):
     sel = lambda t: None if t is None else t[rows]
     sub_cu = torch.tensor([sum(sub_lens[:i]) for i in range(len(sub_lens) + 1)], dtype=torch.int32)
     if w.kind == "replay":
-        return replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
-                       read=remap(rd), pad_slot_id=new_pad, xbuf=w.xbuf[order], dtbuf=w.dtbuf[order],
-                       Bbuf=w.Bbuf[order], count=w.count[seqs], meta=dict(w.meta))
+        sub = replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
+                      read=remap(rd), pad_slot_id=new_pad, xbuf=w.xbuf[order], dtbuf=w.dtbuf[order],
+                      Bbuf=w.Bbuf[order], count=w.count[seqs], meta=dict(w.meta))
+        if w.shadow is not None:
+            import oracle
+            fmt = oracle.SHADOW_F16 if w.shadow.dtype == torch.float16 else oracle.SHADOW_E4M3
+            sub.shadow, sub.shadow_scale = oracle.shadow_refresh(sub.state, fmt)
+        return sub
     return replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
                    read=remap(rd), dst=remap(wr), pad_slot_id=new_pad,
                    cu_seqlens=sub_cu if w.kind == "packed" else None,
@@ -544,7 +558,10 @@ def _oracle_call(sub):
     if sub.kind == "replay":
         return oracle.replay(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, sub.xbuf, sub.dtbuf, sub.Bbuf, sub.count,
                              D=sub.D, z=sub.z, dt_bias=sub.dt_bias, dt_softplus=sub.dt_softplus,
-                             slot_of=sub.read, pad_slot_id=sub.pad_slot_id)
+                             slot_of=sub.read, pad_slot_id=sub.pad_slot_id, shadow=sub.shadow,
+                             shadow_scale=sub.shadow_scale,
+                             shadow_format=oracle.SHADOW_NONE if sub.shadow is None else
+                             (oracle.SHADOW_F16 if sub.shadow.dtype == torch.float16 else oracle.SHADOW_E4M3))
     mode = oracle.SLOTS_PER_ROW if sub.slot_mode == workloads.SLOTS_PER_ROW else oracle.SLOTS_STRIDED
     return oracle.ssu(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, D=sub.D, z=sub.z, dt_bias=sub.dt_bias,
                       dt_softplus=sub.dt_softplus, read=oracle.Table.of(sub.read, mode),
@@ -554,18 +571,25 @@ def _oracle_call(sub):
 
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
-         "varlen_fp16": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007}
+         "varlen_fp16": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008,
+         "replay_f16copy_b256_fp32": 1009}
 
 
 def make_workload(args, device, seed_offset=0):
     gen = workloads.NAMED[args.workload]
     kw = {}
     if args.batch is not None:
-        if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "copy_slots_b256_fp32"):
+        if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
+                                 "replay_f16copy_b256_fp32", "copy_slots_b256_fp32"):
             raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32, replay_b256_fp32 and "
                              "copy_slots_b256_fp32 workloads only")
         kw["batch"] = args.batch
-    return gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
+    w = gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
+    if getattr(w, "shadow", None) is not None and str(device) != "cpu":
+        # the read copy of the checkpoints, built by the library
+        import selective_state_update_gb300 as ssu
+        ssu.ssu_shadow_refresh(w.state, w.shadow, w.shadow_scale)
+    return w
 
 
 def _cpu_workload(args):

@@ -212,11 +212,12 @@ typedef struct ssu_replay_buffers {
 } ssu_replay_buffers;
 
 /* Formats of the read copy.  E4M3 is OCP FP8 E4M3 (bias 7, 3 fraction bits,
- * no infinities, largest 448) with one fp32 scale per state row:
- * scale = amax / 448 over the row's stored values (1 for an all-zero row),
- * code = E4M3(v / scale) rounded to nearest even and clamped to +-448, the
- * quotient and the scale computed in fp32.  F16 is binary16, round to nearest
- * even. */
+ * no infinities, largest 448) with one fp32 scale per state row: over the
+ * row's stored values, scale = amax / 448 and factor = 448 / amax (both 1
+ * for an all-zero row, the factor clamped to the largest finite float), in
+ * fp32; code = E4M3(v * factor), the product in fp32, rounded to nearest even
+ * and clamped to +-448; the value read is E4M3(code) * scale.  F16 is
+ * binary16, round to nearest even. */
 #define SSU_SHADOW_NONE 0
 #define SSU_SHADOW_F16  1
 #define SSU_SHADOW_E4M3 2

@@ -39,6 +39,7 @@
  *     (return code 2) instead of defining them.
  *   - softplus is log(1 + e^v), evaluated as max(v,0) + log1p(exp(-|v|)).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -228,9 +229,12 @@ static void shadow_row(const double *v, int64_t n, int32_t format, void *codes, 
         if ((float)fabs(v[i]) > amax)
             amax = (float)fabs(v[i]);
     volatile float s = amax > 0.0f ? amax / 448.0f : 1.0f;  /* fp32 division */
+    volatile float f = amax > 0.0f ? 448.0f / amax : 1.0f;  /* fp32 division */
+    if (!(f <= FLT_MAX))
+        f = FLT_MAX;
     *scale = s;
     for (int64_t i = 0; i < n; ++i) {
-        volatile float q = (float)v[i] / s;                  /* fp32 division */
+        volatile float q = (float)v[i] * f;                  /* fp32 product */
         ((uint8_t *)codes)[i] = orc_e4m3_encode(q);
     }
 }

@@ -84,9 +84,11 @@ typedef struct {
  *   ORC_SHADOW_F16   binary16, round to nearest even.
  *   ORC_SHADOW_E4M3  OCP FP8 E4M3 (bias 7, 3 fraction bits, no infinities,
  *                    largest 448) with one fp32 scale per state row:
- *                    scale = amax / 448 (1 for an all-zero row), computed in
- *                    fp32; code = E4M3(v / scale) with the quotient in fp32,
- *                    rounded to nearest even and clamped to +-448. */
+ *                    scale = amax / 448 and factor = 448 / amax (both 1 for
+ *                    an all-zero row, the factor clamped to FLT_MAX), computed
+ *                    in fp32; code = E4M3(v * factor) with the product in
+ *                    fp32, rounded to nearest even and clamped to +-448;
+ *                    value = E4M3 value * scale. */
 enum { ORC_SHADOW_NONE = 0, ORC_SHADOW_F16 = 1, ORC_SHADOW_E4M3 = 2 };
 
 /* The read copy of `rows` state rows of `dstate` elements (`state` in

@@ -42,16 +42,28 @@ __device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
 __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // The low-precision read copy of a state row (article "ReplaySSM", section
-// 低精度读写分离), E4M3 form: scale = amax / 448 in fp32 (1 for an all-zero
-// row), code = E4M3(v / scale), the quotient in fp32, rounded to nearest even
-// and clamped to +-448 (the conversion's saturate-to-finite mode).
+// 低精度读写分离), E4M3 form: over the row's stored values, the dequantising
+// scale amax / 448 and the quantising factor 448 / amax (both fp32, both 1
+// for an all-zero row, the factor clamped to the largest finite float);
+// code = E4M3(v * factor), the product in fp32, rounded to nearest even and
+// clamped to +-448 (the conversion's saturate-to-finite mode).
 __device__ __forceinline__ float shadow_scale_of(float amax) { return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f; }
+__device__ __forceinline__ float shadow_factor_of(float amax) {
+    return amax > 0.f ? fminf(__fdiv_rn(448.f, amax), 3.402823466e38f) : 1.f;
+}
 __device__ __forceinline__ unsigned char e4m3_code(float v) {
     return static_cast<unsigned char>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
 }
-__device__ __forceinline__ float e4m3_value(unsigned int code) {
-    return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3)));
+// Two values from two codes (the low byte first), one conversion.
+__device__ __forceinline__ float2 e4m3x2_values(unsigned int codes) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
+    return __half22float2(__half2(h));
 }
+// Two codes (a in the low byte) from two values, one conversion.
+__device__ __forceinline__ unsigned int e4m3x2_codes(float a, float b) {
+    return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
 
 __device__ __forceinline__ float bits_to_float(uint32_t v, int dtype) {
     if (dtype == kF32) return __uint_as_float(v);

@@ -337,7 +337,11 @@ __device__ __forceinline__ void load_copy_row(const unsigned char *tile, int rr,
                 w[0] = *reinterpret_cast<const uint32_t *>(tile + rr * N + e0);
             }
 #pragma unroll
-            for (int i = 0; i < V; ++i) v[k * V + i] = e4m3_value((w[i / 4] >> (8 * (i % 4))) & 0xffu);
+            for (int i = 0; i < V / 2; ++i) {
+                const float2 f = e4m3x2_values(w[i / 2] >> (16 * (i % 2)));
+                v[k * V + 2 * i] = f.x;
+                v[k * V + 2 * i + 1] = f.y;
+            }
         } else {
             uint32_t w[V / 2];
             const unsigned char *src = tile + (rr * N + e0) * 2;
@@ -361,7 +365,7 @@ __device__ __forceinline__ void load_copy_row(const unsigned char *tile, int rr,
 // as the pool stores them) to global memory: E4M3 codes and the row scale,
 // or fp16.  Every lane of the row takes part (the row maximum is a shuffle);
 // only `live` rows are written.
-template <typename TS, int L>
+template <typename TS, int L, int SH>
 __device__ __forceinline__ void write_copy_row(const KParams &p, int64_t row, int lane, bool live, const float *sv) {
     using T = Tile<TS, L>;
     constexpr int V = T::kVec;
@@ -374,20 +378,22 @@ __device__ __forceinline__ void write_copy_row(const KParams &p, int64_t row, in
 #pragma unroll
         for (int k = 0; k < T::kChunks; ++k) StateChunk<TS>::unpack(StateChunk<TS>::pack(sv + k * V), st + k * V);
     }
-    if (p.shadow_fmt == kShadowE4M3) {
+    if constexpr (SH == kShadowE4M3) {
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < kElemsPerThread; ++i) amax = fmaxf(amax, fabsf(st[i]));
 #pragma unroll
         for (int off = L / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float sc = shadow_scale_of(amax);
+        const float sc = shadow_scale_of(amax), f = shadow_factor_of(amax);
         if (!live) return;
         unsigned char *out = static_cast<unsigned char *>(p.shadow) + row * N;
 #pragma unroll
         for (int k = 0; k < T::kChunks; ++k) {
             uint32_t w[V / 4] = {};
 #pragma unroll
-            for (int i = 0; i < V; ++i) w[i / 4] |= uint32_t(e4m3_code(__fdiv_rn(st[k * V + i], sc))) << (8 * (i % 4));
+            for (int i = 0; i < V / 2; ++i)
+                w[i / 2] |= e4m3x2_codes(__fmul_rn(st[k * V + 2 * i], f), __fmul_rn(st[k * V + 2 * i + 1], f))
+                            << (16 * (i % 2));
             unsigned char *dst = out + (lane + L * k) * V;
             if constexpr (V == 8)
                 *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
@@ -395,7 +401,7 @@ __device__ __forceinline__ void write_copy_row(const KParams &p, int64_t row, in
                 *reinterpret_cast<uint32_t *>(dst) = w[0];
         }
         if (lane == 0) p.shadow_scale[row] = sc;
-    } else if (live) {
+    } else if (SH == kShadowF16 && live) {
         unsigned char *out = static_cast<unsigned char *>(p.shadow) + row * N * 2;
 #pragma unroll
         for (int k = 0; k < T::kChunks; ++k) {
@@ -424,7 +430,7 @@ struct ReplayOperands : UnitOperands<TS, L> {
 };
 
 // Stage one unit (see the file comment).  Returns false on a timed-out wait.
-template <typename TS, int L, int IO>
+template <typename TS, int L, int IO, int SH>
 __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLayout &lay,
                                                const ReplayOperands<TS, L> &op, int k, unsigned char *smem,
                                                uint64_t *full, uint64_t *empty, int lane) {
@@ -560,11 +566,11 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
     // head-major buffer layout.)
     // A step that does not fold reads the read copy when there is one
     // (codes, then E4M3 row scales at kShadowScaleOffset), else the tile.
-    const bool read_copy = p.shadow_fmt != kShadowNone && !(flags & kRFold);
+    const bool read_copy = SH != kShadowNone && !(flags & kRFold);
     const int64_t row_first = (rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0;
     const uint32_t tile_bytes =
-        static_cast<uint32_t>(rows) * N * (read_copy ? (p.shadow_fmt == kShadowF16 ? 2 : 1) : sizeof(TS));
-    const uint32_t scale_bytes = read_copy && p.shadow_fmt == kShadowE4M3 ? static_cast<uint32_t>(rows) * 4 : 0;
+        static_cast<uint32_t>(rows) * N * (read_copy ? (SH == kShadowF16 ? 2 : 1) : sizeof(TS));
+    const uint32_t scale_bytes = read_copy && SH == kShadowE4M3 ? static_cast<uint32_t>(rows) * 4 : 0;
     uint32_t bytes = tile_bytes + scale_bytes;
     if (bulk_entries) bytes += static_cast<uint32_t>(c) * (rows * (io + 4) + N * io);
     if (lane == 0) mbar_arrive_expect(&full[s], bytes);
@@ -573,7 +579,7 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
         bulk_load(base + ReplayPipe<TS, L>::kShadowScaleOffset, p.shadow_scale + row_first, scale_bytes, &full[s]);
     {
         const unsigned char *src =
-            read_copy ? static_cast<const unsigned char *>(p.shadow) + row_first * N * (p.shadow_fmt == kShadowF16 ? 2 : 1)
+            read_copy ? static_cast<const unsigned char *>(p.shadow) + row_first * N * (SH == kShadowF16 ? 2 : 1)
                       : reinterpret_cast<const unsigned char *>(static_cast<const TS *>(p.state) + row_first * N);
         for (uint32_t off = static_cast<uint32_t>(lane) * kReplayTileChunk; off < tile_bytes;
              off += 32u * kReplayTileChunk)
@@ -597,7 +603,7 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
 
 // Producer warp `w` stages the CTA's units k = w, w + P, w + 2P, ...
 // (P = lay.producers), i.e. global units blockIdx.x + k * gridDim.x.
-template <typename TS, int L, int IO>
+template <typename TS, int L, int IO, int SH>
 __device__ __forceinline__ void replay_producer(const KParams &p, const ReplayLayout &lay, int64_t units,
                                                 unsigned char *smem, uint64_t *full, uint64_t *empty, int w) {
     const int P = lay.producers;
@@ -611,15 +617,15 @@ __device__ __forceinline__ void replay_producer(const KParams &p, const ReplayLa
     for (int k = w; u < units; k += 2 * P, u += 2 * step) {
         walk.advance(p);
         if (u + step < units) b.load(p, walk.coords(p), lane);
-        if (!produce_replay<TS, L, IO>(p, lay, a, k, smem, full, empty, lane)) return;
+        if (!produce_replay<TS, L, IO, SH>(p, lay, a, k, smem, full, empty, lane)) return;
         if (u + step >= units) break;
         walk.advance(p);
         if (u + 2 * step < units) a.load(p, walk.coords(p), lane);
-        if (!produce_replay<TS, L, IO>(p, lay, b, k + P, smem, full, empty, lane)) return;
+        if (!produce_replay<TS, L, IO, SH>(p, lay, b, k + P, smem, full, empty, lane)) return;
     }
 }
 
-template <typename TS, int L, int IO>
+template <typename TS, int L, int IO, int SH>
 __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLayout &lay, int64_t units,
                                                 unsigned char *smem, uint64_t *full, uint64_t *empty) {
     using T = Tile<TS, L>;
@@ -672,16 +678,18 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
                 // S_ckpt . C of this thread's rows (every lane of a row ends
                 // with the sum) beside the B_j . C dots.
                 float rsum[kRowsPerThread];
-                if (active && p.shadow_fmt == kShadowNone) {
+                if constexpr (SH == kShadowNone) {
+                    if (active) {
 #pragma unroll
-                    for (int j = 0; j < kRowsPerThread; ++j) {
-                        const int rr = slot_row + j * kRowSlots;  // row within the tile
-                        float sv[kElemsPerThread];
-                        T::load_row_smem(tile + (rr < rows ? rr : 0) * N, lane, sv);
-                        float acc = 0.f;
+                        for (int j = 0; j < kRowsPerThread; ++j) {
+                            const int rr = slot_row + j * kRowSlots;  // row within the tile
+                            float sv[kElemsPerThread];
+                            T::load_row_smem(tile + (rr < rows ? rr : 0) * N, lane, sv);
+                            float acc = 0.f;
 #pragma unroll
-                        for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
-                        rsum[j] = row_sum<L>(acc);
+                            for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
+                            rsum[j] = row_sum<L>(acc);
+                        }
                     }
                 } else if (active) {
                     // from the read copy: codes (times the row scale) or fp16
@@ -692,11 +700,11 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
                         const int rr = slot_row + j * kRowSlots;
                         const int rq = rr < rows ? rr : 0;
                         float sv[kElemsPerThread];
-                        load_copy_row<TS, L>(copy, rq, lane, p.shadow_fmt, sv);
+                        load_copy_row<TS, L>(copy, rq, lane, SH, sv);
                         float acc = 0.f;
 #pragma unroll
                         for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
-                        rsum[j] = row_sum<L>(acc) * (p.shadow_fmt == kShadowE4M3 ? rscale[rq] : 1.f);
+                        rsum[j] = row_sum<L>(acc) * (SH == kShadowE4M3 ? rscale[rq] : 1.f);
                     }
                 }
                 entry_dots<N, kConsumers, IO>(c, be, sB, sC, dots, tid);
@@ -799,9 +807,11 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
                             store_small(p.y, cu.b * p.ys[0] + cu.h * p.ys[1] + (cu.row0 + rr) * p.ys[2], IO,
                                         output(sum, Dh, q.z, q.w));
                         if (live && seeded) T::store_row_smem(tile + rr * N, lane, sv);
-                        if (seeded && p.shadow_fmt != kShadowNone)
-                            write_copy_row<TS, L>(p, (hd->slot * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + rr,
-                                                  lane, live, sv);
+                        if constexpr (SH != kShadowNone) {
+                            if (seeded)
+                                write_copy_row<TS, L, SH>(
+                                    p, (hd->slot * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0 + rr, lane, live, sv);
+                        }
                     }
                 }
             }
@@ -839,7 +849,7 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
     if (tid == 0) bulk_wait_all();
 }
 
-template <typename TS, int L, int IO>
+template <typename TS, int L, int IO, int SH>
 __global__ void __launch_bounds__(ReplayPipe<TS, L>::kThreads, ReplayPipe<TS, L>::kMinCtas)
     ssu_replay_kernel(const KParams p, const ReplayLayout lay, int64_t units) {
     using PS = ReplayPipe<TS, L>;
@@ -855,9 +865,9 @@ __global__ void __launch_bounds__(ReplayPipe<TS, L>::kThreads, ReplayPipe<TS, L>
     __syncthreads();
     const int warp = threadIdx.x / 32;
     if (warp >= PS::kConsumerWarps)
-        replay_producer<TS, L, IO>(p, lay, units, smem, full, empty, warp - PS::kConsumerWarps);
+        replay_producer<TS, L, IO, SH>(p, lay, units, smem, full, empty, warp - PS::kConsumerWarps);
     else
-        replay_consumer<TS, L, IO>(p, lay, units, smem, full, empty);
+        replay_consumer<TS, L, IO, SH>(p, lay, units, smem, full, empty);
 }
 
 // Number of SMs of the current device (cached per device).
@@ -876,7 +886,7 @@ static int replay_sm_count() {
 
 // Once per device: opt in to the largest dynamic shared memory a CTA takes,
 // and find how many CTAs of the kernel fit an SM by registers.
-template <typename TS, int L, int IO>
+template <typename TS, int L, int IO, int SH>
 static cudaError_t prepare_replay_kernel(int *reg_ctas) {
     static std::atomic<int> cache[64];
     int dev = 0;
@@ -885,11 +895,11 @@ static cudaError_t prepare_replay_kernel(int *reg_ctas) {
     if (dev < 0 || dev >= 64) dev = 0;
     int n = cache[dev].load(std::memory_order_relaxed);
     if (n == 0) {
-        e = cudaFuncSetAttribute(ssu_replay_kernel<TS, L, IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(ssu_replay_kernel<TS, L, IO, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ReplayPipe<TS, L>::kSmemPerSm - 1024);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes a;
-        e = cudaFuncGetAttributes(&a, ssu_replay_kernel<TS, L, IO>);
+        e = cudaFuncGetAttributes(&a, ssu_replay_kernel<TS, L, IO, SH>);
         if (e != cudaSuccess) return e;
         const int regs = (a.numRegs + 7) / 8 * 8;  // allocated per thread in units of 8
         n = regs > 0 ? 65536 / (regs * ReplayPipe<TS, L>::kThreads) : 1;
@@ -900,11 +910,11 @@ static cudaError_t prepare_replay_kernel(int *reg_ctas) {
     return cudaSuccess;
 }
 
-template <typename TS, int L, int IO>
+template <typename TS, int L, int IO, int SH>
 static cudaError_t launch_replay_t(const KParams &p, int64_t batch, cudaStream_t stream) {
     using PS = ReplayPipe<TS, L>;
     int reg_ctas = 0;
-    cudaError_t e = prepare_replay_kernel<TS, L, IO>(&reg_ctas);
+    cudaError_t e = prepare_replay_kernel<TS, L, IO, SH>(&reg_ctas);
     if (e != cudaSuccess) return e;
     ReplayLayout lay;
     if (!lay.choose(PS::kTileBytes, PS::kN, p.rlen, IO == kF32 ? 4 : 2, PS::kSmemPerSm, reg_ctas,
@@ -915,18 +925,24 @@ static cudaError_t launch_replay_t(const KParams &p, int64_t batch, cudaStream_t
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int64_t slots_on_gpu = static_cast<int64_t>(sms) * lay.ctas;
     const int64_t grid = units < slots_on_gpu ? units : slots_on_gpu;
-    ssu_replay_kernel<TS, L, IO><<<static_cast<unsigned>(grid), PS::kThreads, lay.bytes, stream>>>(p, lay, units);
+    ssu_replay_kernel<TS, L, IO, SH><<<static_cast<unsigned>(grid), PS::kThreads, lay.bytes, stream>>>(p, lay, units);
     return cudaGetLastError();
 }
 
 template <typename TS, int IO>
 static cudaError_t launch_replay_lanes(int lanes, const KParams &p, int64_t batch, cudaStream_t stream) {
-    switch (lanes) {
-    case 1: return launch_replay_t<TS, 1, IO>(p, batch, stream);
-    case 2: return launch_replay_t<TS, 2, IO>(p, batch, stream);
-    case 4: return launch_replay_t<TS, 4, IO>(p, batch, stream);
-    case 8: return launch_replay_t<TS, 8, IO>(p, batch, stream);
-    case 16: return launch_replay_t<TS, 16, IO>(p, batch, stream);
+    // one kernel per read-copy format: each carries only its own paths
+    switch (lanes * 4 + p.shadow_fmt) {
+#define SSU_REPLAY_CASE(LN)                                                                          \
+    case LN * 4 + kShadowNone: return launch_replay_t<TS, LN, IO, kShadowNone>(p, batch, stream);   \
+    case LN * 4 + kShadowF16: return launch_replay_t<TS, LN, IO, kShadowF16>(p, batch, stream);     \
+    case LN * 4 + kShadowE4M3: return launch_replay_t<TS, LN, IO, kShadowE4M3>(p, batch, stream);
+        SSU_REPLAY_CASE(1)
+        SSU_REPLAY_CASE(2)
+        SSU_REPLAY_CASE(4)
+        SSU_REPLAY_CASE(8)
+        SSU_REPLAY_CASE(16)
+#undef SSU_REPLAY_CASE
     }
     return cudaErrorInvalidValue;
 }

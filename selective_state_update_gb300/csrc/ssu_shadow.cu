@@ -9,7 +9,8 @@
 // arithmetic (shadow_scale / e4m3_code in ssu_device.cuh).
 //
 // One warp per state row: the row's largest magnitude (an exact maximum),
-// its scale amax / 448 in fp32, then each element's code.
+// its scale amax / 448 and factor 448 / amax in fp32, then each element's
+// code.
 #include "ssu_device.cuh"
 
 namespace ssu {
@@ -30,10 +31,10 @@ __global__ void __launch_bounds__(256)
         for (int n = lane; n < dstate; n += 32) amax = fmaxf(amax, fabsf(to_float(row[n])));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float s = shadow_scale_of(amax);
-        if (lane == 0) scale[r] = s;
+        const float f = shadow_factor_of(amax);
+        if (lane == 0) scale[r] = shadow_scale_of(amax);
         unsigned char *out = static_cast<unsigned char *>(shadow) + r * dstate;
-        for (int n = lane; n < dstate; n += 32) out[n] = e4m3_code(__fdiv_rn(to_float(row[n]), s));
+        for (int n = lane; n < dstate; n += 32) out[n] = e4m3_code(__fmul_rn(to_float(row[n]), f));
     }
 }
 

@@ -754,8 +754,8 @@ def pin_e4m3_codes(lib):
 def pin_shadow_refresh(lib):
     """The read copy of a pool: fp16 codes are torch's round-to-nearest-even
     cast; E4M3 codes and row scales equal a restatement with torch's
-    float8_e4m3fn cast (scale = amax / 448 in fp32, codes of v / scale); an
-    all-zero row gets scale 1 and zero codes."""
+    float8_e4m3fn cast (scale = amax / 448 and factor 448 / amax in fp32,
+    codes of v * factor); an all-zero row gets scale 1 and zero codes."""
     g = torch.Generator().manual_seed(62)
     st = torch.randn((3, 2, 4, 32), generator=g) * torch.rand((3, 2, 4, 1), generator=g) * 5
     st[1, 0, 2] = 0.0
@@ -765,7 +765,8 @@ def pin_shadow_refresh(lib):
     codes, scale = oracle.shadow_refresh(st, oracle.SHADOW_E4M3, lib=lib)
     amax = st.abs().amax(dim=-1)
     want_scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
-    want_codes = (st / want_scale[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    factor = torch.where(amax > 0, 448.0 / amax, torch.ones_like(amax))
+    want_codes = (st * factor[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
     if not (torch.equal(scale, want_scale) and torch.equal(codes, want_codes)):
         raise AssertionError("E4M3 read copy")
     if float(scale[1, 0, 2]) != 1.0 or int(codes[1, 0, 2].abs().sum()) != 0:

@@ -49,6 +49,7 @@ MUTATIONS = [
     # the low-precision read copy of the checkpoint
     ("read_copy_ignored", "sq += (pr->shadow_format != ORC_SHADOW_NONE", "sq += (0"),
     ("e4m3_scale_240", "amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
+    ("e4m3_factor_240", "amax > 0.0f ? 448.0f / amax : 1.0f", "amax > 0.0f ? 240.0f / amax : 1.0f"),
     ("fold_skips_read_copy",
      "if (pr->shadow_format != ORC_SHADOW_NONE) {\n                            /* the read copy",
      "if (0) {\n                            /* the read copy"),

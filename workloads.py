@@ -64,6 +64,8 @@ class Workload:
     dtbuf: Optional[torch.Tensor] = None       # [slots, L, heads, dim] fp32 processed steps
     Bbuf: Optional[torch.Tensor] = None        # [slots, L, groups, dstate] io dtype
     count: Optional[torch.Tensor] = None       # [batch] int32 buffered entries per sequence
+    shadow: Optional[torch.Tensor] = None      # read copy of the checkpoints (fp16 or uint8 E4M3 codes)
+    shadow_scale: Optional[torch.Tensor] = None  # [slots, heads, dim] fp32 E4M3 row scales
     meta: dict = field(default_factory=dict)
 
     @property
@@ -250,6 +252,28 @@ def replay_b256_fp32(device="cpu", seed=1006, batch=256, buffer_len=16) -> Workl
                     xbuf=xbuf, dtbuf=dtbuf, Bbuf=Bbuf, count=count, meta={"buffer_len": buffer_len}, **inp)
 
 
+def replay_e4m3_b256_fp32(device="cpu", seed=1008, batch=256, buffer_len=16) -> Workload:
+    """replay_b256_fp32 with an E4M3 read copy of the checkpoints (codes and
+    row scales allocated here, filled by the caller with the copy of the
+    checkpoints: the copy's arithmetic is not this module's)."""
+    w = replay_b256_fp32(device=device, seed=seed, batch=batch, buffer_len=buffer_len)
+    w.name = "replay_e4m3_b256_fp32"
+    w.shadow = torch.zeros(w.state.shape, dtype=torch.uint8, device=device)
+    w.shadow_scale = torch.ones(w.state.shape[:-1], dtype=torch.float32, device=device)
+    w.meta["shadow_format"] = "e4m3"
+    return w
+
+
+def replay_f16copy_b256_fp32(device="cpu", seed=1009, batch=256, buffer_len=16) -> Workload:
+    """replay_b256_fp32 with an fp16 read copy of the checkpoints (allocated
+    here, filled by the caller)."""
+    w = replay_b256_fp32(device=device, seed=seed, batch=batch, buffer_len=buffer_len)
+    w.name = "replay_f16copy_b256_fp32"
+    w.shadow = torch.zeros(w.state.shape, dtype=torch.float16, device=device)
+    w.meta["shadow_format"] = "f16"
+    return w
+
+
 def replay_problem(seed: int, *, slots: int = 16, heads: int = 4, dim: int = 8, dstate: int = 16,
                    groups: int = 2, nseq: int = 4, buffer_len: int = 4, state_dtype=torch.float32,
                    io_dtype=torch.bfloat16, with_D: bool = True, with_z: bool = True, with_bias: bool = True,
@@ -322,6 +346,8 @@ NAMED = {
     "mtp_64x7_fp32": mtp_64x7_fp32,
     "varlen_fp16": varlen_fp16,
     "replay_b256_fp32": replay_b256_fp32,
+    "replay_e4m3_b256_fp32": replay_e4m3_b256_fp32,
+    "replay_f16copy_b256_fp32": replay_f16copy_b256_fp32,
     "copy_slots_b256_fp32": copy_slots_b256_fp32,
 }
 
