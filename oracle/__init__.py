@@ -106,6 +106,20 @@ class _ReplayProblem(ctypes.Structure):
     ]
 
 
+class _SsdProblem(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("groups", ctypes.c_int64), ("nchunks", ctypes.c_int64),
+        ("nseq", ctypes.c_int64),
+        ("io_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+        ("z", ctypes.c_void_p), ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("dt_softplus", ctypes.c_int32), ("dt_lo", ctypes.c_double), ("dt_hi", ctypes.c_double),
+        ("cu_chunk", ctypes.c_void_p), ("seq_idx", ctypes.c_void_p), ("initial_states", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("y_exact", ctypes.c_void_p), ("states", ctypes.c_void_p),
+    ]
+
+
 # Formats of the low-precision read copy (ssu_oracle.h, ORC_SHADOW_*).
 SHADOW_NONE, SHADOW_F16, SHADOW_E4M3 = 0, 1, 2
 
@@ -127,6 +141,8 @@ def load_library(path: str):
     lib.orc_decode.restype = ctypes.c_double
     lib.orc_encode.argtypes = [ctypes.c_double, ctypes.c_int]
     lib.orc_encode.restype = ctypes.c_uint32
+    lib.orc_ssd_run.argtypes = [ctypes.POINTER(_SsdProblem), ctypes.c_char_p, ctypes.c_int]
+    lib.orc_ssd_run.restype = ctypes.c_int
     lib.orc_shadow_refresh.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     lib.orc_shadow_refresh.restype = ctypes.c_int
@@ -359,3 +375,52 @@ def shadow_refresh(state: torch.Tensor, shadow_format: int, lib=None):
     if rc != OK:
         raise OracleError(rc, "shadow refresh failed")
     return codes, scale
+
+
+@dataclass
+class SsdResult:
+    y: torch.Tensor            # [tokens, heads, dim] io dtype
+    y_exact: torch.Tensor      # float64 before rounding
+    states: torch.Tensor       # [nchunks, heads, dim, dstate]: the state at the end of each chunk
+
+
+def ssd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+        cu_chunk_seqlens: torch.Tensor, seq_idx: torch.Tensor, nseq: int, D: Optional[torch.Tensor] = None,
+        z: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
+        dt_limit=(0.0, float("inf")), initial_states: Optional[torch.Tensor] = None,
+        state_dtype: Optional[torch.dtype] = None, lib=None) -> SsdResult:
+    """Packed variable-length SSD prefill on the host (MATE "Mamba / SSU",
+    SSD packed prefill): x ``[tokens, heads, dim]``, dt ``[tokens, heads]``,
+    B, C ``[tokens, groups, dstate]``; chunk c covers tokens
+    ``[cu_chunk_seqlens[c], cu_chunk_seqlens[c+1])`` and belongs to sequence
+    ``seq_idx[c]``.  Returns y and the state at the end of every chunk, in
+    ``state_dtype`` (default: initial_states' dtype, else C's)."""
+    lib = lib or _load()
+    xs, dts, Bs, Cs, zs = _cpu(x), _cpu(dt), _cpu(B), _cpu(C), _cpu(z)
+    tokens, heads, dim = xs.shape
+    groups, dstate = Bs.shape[1], Bs.shape[2]
+    cu = _cpu(cu_chunk_seqlens).to(torch.int64).contiguous()
+    si = _cpu(seq_idx).to(torch.int64).contiguous()
+    nchunks = si.numel()
+    init = None if initial_states is None else _cpu(initial_states).contiguous()
+    sdt = state_dtype or (init.dtype if init is not None else Cs.dtype)
+    As = _cpu(A).to(torch.float32)
+    Ds = None if D is None else _cpu(D).to(torch.float32)
+    bs = None if dt_bias is None else _cpu(dt_bias).to(torch.float32)
+    y = torch.empty((tokens, heads, dim), dtype=xs.dtype)
+    y_exact = torch.empty((tokens, heads, dim), dtype=torch.float64)
+    states = torch.empty((nchunks, heads, dim, dstate), dtype=sdt)
+    if init is not None and init.dtype != sdt:
+        init = init.to(sdt)
+    pr = _SsdProblem(
+        tokens=tokens, heads=heads, dim=dim, dstate=dstate, groups=groups, nchunks=nchunks, nseq=nseq,
+        io_dtype=_DTYPE_CODE[xs.dtype], dt_dtype=_DTYPE_CODE[dts.dtype], state_dtype=_DTYPE_CODE[sdt],
+        x=xs.data_ptr(), dt=dts.data_ptr(), B=Bs.data_ptr(), C=Cs.data_ptr(), z=_ptr(zs), A=As.data_ptr(),
+        D=_ptr(Ds), dt_bias=_ptr(bs), dt_softplus=int(bool(dt_softplus)), dt_lo=float(dt_limit[0]),
+        dt_hi=float(dt_limit[1]), cu_chunk=cu.data_ptr(), seq_idx=si.data_ptr(), initial_states=_ptr(init),
+        y=y.data_ptr(), y_exact=y_exact.data_ptr(), states=states.data_ptr())
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_ssd_run(ctypes.byref(pr), err, 512)
+    if rc != OK:
+        raise OracleError(rc, err.value.decode())
+    return SsdResult(y=y, y_exact=y_exact, states=states)

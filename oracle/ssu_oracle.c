@@ -656,3 +656,79 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
     free(S);
     return ORC_OK;
 }
+
+
+/* ------------------------------------------------------------------------ */
+/* Packed variable-length SSD prefill (MATE "Mamba / SSU", SSD packed        */
+/* prefill; API reference of ssd_combined_fwd_varlen): the recurrence over   */
+/* each sequence's tokens, chunk by chunk in order, the entering state of a  */
+/* chunk decided by seq_idx (the page: seq_idx, not last_chunk_indices, is   */
+/* the authority), dt clamped to dt_limit after softplus.                    */
+/* ------------------------------------------------------------------------ */
+int orc_ssd_run(const orc_ssd_problem *pr, char *err, int errlen)
+{
+    const int64_t H = pr->heads, P = pr->dim, N = pr->dstate, G = pr->groups, T = pr->tokens;
+    if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0 || pr->nchunks < 0 || T < 0 || pr->nseq < 0) {
+        set_err(err, errlen, "bad shape: heads=%lld groups=%lld", H, G);
+        return ORC_INVALID;
+    }
+    if (pr->cu_chunk[0] != 0 || pr->cu_chunk[pr->nchunks] != T) {
+        set_err(err, errlen, "cu_chunk_seqlens must start at 0 and end at tokens (%lld)", T, 0);
+        return ORC_INVALID;
+    }
+    for (int64_t c = 0; c < pr->nchunks; ++c) {
+        if (pr->cu_chunk[c + 1] < pr->cu_chunk[c]) {
+            set_err(err, errlen, "cu_chunk_seqlens decreases at chunk %lld", c, 0);
+            return ORC_INVALID;
+        }
+        if (pr->seq_idx[c] < 0 || pr->seq_idx[c] >= pr->nseq) {
+            set_err(err, errlen, "seq_idx[%lld] = %lld out of range", c, pr->seq_idx[c]);
+            return ORC_INVALID;
+        }
+    }
+    const int64_t hpg = H / G;
+    double *S = malloc(sizeof(double) * (size_t)N);
+    if (!S)
+        return ORC_INVALID;
+    for (int64_t h = 0; h < H; ++h) {
+        const int64_t g = h / hpg;
+        const double A = (double)pr->A[h];
+        const double Dh = pr->D ? (double)pr->D[h] : 0.0;
+        const double bias = pr->dt_bias ? (double)pr->dt_bias[h] : 0.0;
+        for (int64_t p = 0; p < P; ++p) {
+            for (int64_t c = 0; c < pr->nchunks; ++c) {
+                const int64_t b = pr->seq_idx[c];
+                if (c == 0 || pr->seq_idx[c] != pr->seq_idx[c - 1]) {
+                    /* the chunk opens sequence b */
+                    for (int64_t n = 0; n < N; ++n)
+                        S[n] = pr->initial_states
+                                   ? load_elem(pr->initial_states, ((b * H + h) * P + p) * N + n, pr->state_dtype)
+                                   : 0.0;
+                }
+                for (int64_t t = pr->cu_chunk[c]; t < pr->cu_chunk[c + 1]; ++t) {
+                    double d = load_elem(pr->dt, t * H + h, pr->dt_dtype) + bias;
+                    if (pr->dt_softplus)
+                        d = orc_softplus(d);
+                    d = fmin(fmax(d, pr->dt_lo), pr->dt_hi);
+                    const double a = exp(A * d);
+                    const double xv = load_elem(pr->x, (t * H + h) * P + p, pr->io_dtype);
+                    double y = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        S[n] = S[n] * a + d * xv * load_elem(pr->B, (t * G + g) * N + n, pr->io_dtype);
+                        y += S[n] * load_elem(pr->C, (t * G + g) * N + n, pr->io_dtype);
+                    }
+                    y += Dh * xv;
+                    if (pr->z != NULL)
+                        y *= orc_silu(load_elem(pr->z, (t * H + h) * P + p, pr->io_dtype));
+                    if (pr->y_exact != NULL)
+                        pr->y_exact[(t * H + h) * P + p] = y;
+                    store_elem(pr->y, (t * H + h) * P + p, pr->io_dtype, y);
+                }
+                for (int64_t n = 0; n < N; ++n)
+                    store_elem(pr->states, ((c * H + h) * P + p) * N + n, pr->state_dtype, S[n]);
+            }
+        }
+    }
+    free(S);
+    return ORC_OK;
+}

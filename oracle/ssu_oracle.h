@@ -78,6 +78,37 @@ typedef struct {
     float *shadow_scale;            /* [slots, heads, dim] row scales (E4M3), in/out              */
 } orc_replay_problem;
 
+/* Packed variable-length SSD prefill (MATE documentation, page "Mamba / SSU",
+ * "SSD packed prefill" and the API reference of ssd_combined_fwd_varlen).
+ * What it computes is the Mamba-2 recurrence over each sequence's tokens
+ * (the chunked five-stage evaluation is a reordering of it): for token t of
+ * head h, dim row p, g = h / (heads / groups),
+ *     dt' = clamp(softplus?(dt[t,h] + dt_bias[h]), dt_lo, dt_hi)
+ *     S[n] = S[n] exp(A[h] dt') + dt' x[t,h,p] B[t,g,n]
+ *     y[t,h,p] = (sum_n S[n] C[t,g,n] + D[h] x[t,h,p]) * silu(z[t,h,p])
+ * Chunk c covers tokens [cu_chunk[c], cu_chunk[c+1]); chunks are visited in
+ * order; a chunk opens a sequence when c == 0 or seq_idx[c] != seq_idx[c-1],
+ * and its entering state is then initial_states[seq_idx[c]] (zero without
+ * initial states); otherwise it is the state the previous chunk left.  The
+ * state is carried in double; states[c] = the state at the end of chunk c,
+ * rounded to state_dtype.  All arrays contiguous. */
+typedef struct {
+    int64_t tokens, heads, dim, dstate, groups, nchunks, nseq;
+    int32_t io_dtype, dt_dtype, state_dtype;
+    const void *x, *dt, *B, *C, *z;   /* x, z [tokens, heads, dim]; dt [tokens, heads]; B, C [tokens, groups, dstate] */
+    const float *A, *D, *dt_bias;     /* [heads]; D, dt_bias may be NULL                               */
+    int32_t dt_softplus;
+    double dt_lo, dt_hi;              /* dt_limit                                                      */
+    const int64_t *cu_chunk;          /* [nchunks + 1]                                                 */
+    const int64_t *seq_idx;           /* [nchunks], each in [0, nseq)                                  */
+    const void *initial_states;       /* [nseq, heads, dim, dstate] in state_dtype, or NULL            */
+    void *y;                          /* [tokens, heads, dim] io_dtype                                 */
+    double *y_exact;                  /* [tokens, heads, dim] or NULL                                  */
+    void *states;                     /* [nchunks, heads, dim, dstate] state_dtype                      */
+} orc_ssd_problem;
+
+int orc_ssd_run(const orc_ssd_problem *problem, char *err, int errlen);
+
 /* Low-precision read copy of the checkpoints (article "ReplaySSM", section
  * 低精度读写分离): steps that do not fold read it instead of the checkpoint;
  * a fold rewrites it from the new checkpoint.

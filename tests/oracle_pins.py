@@ -845,10 +845,144 @@ def pin_replay_read_copy(lib):
         raise AssertionError("the readout did not use the read copy")
 
 
+def _ssd_run(w, lib, **kw):
+    args = dict(D=w.D, z=w.z, dt_bias=w.dt_bias, dt_softplus=w.dt_softplus, dt_limit=w.dt_limit,
+                initial_states=w.initial_states, lib=lib)
+    args.update(kw)
+    return oracle.ssd(w.x, w.dt, w.A, w.B, w.C, w.cu_chunk_seqlens, w.seq_idx, w.nseq, **args)
+
+
+def pin_ssd_equals_token_loop(lib):
+    """The SSD prefill over packed sequences is the selective state update
+    run token by token over each sequence from its initial state: y and the
+    final states equal the packed update's (same double arithmetic), for any
+    chunk size."""
+    lengths = [5, 37, 16, 1]
+    for q in (4, 16):
+        w = workloads.ssd_problem(51, lengths, heads=4, dim=3, dstate=8, groups=2, chunk_size=q,
+                                  state_dtype=torch.float32)
+        r = _ssd_run(w, lib)
+        width = max(lengths)
+        tab = torch.arange(w.nseq, dtype=torch.int64).view(-1, 1).repeat(1, width)
+        ref = oracle.ssu(w.initial_states, w.x, w.dt, w.A, w.B, w.C, D=w.D, z=w.z, dt_bias=w.dt_bias,
+                         dt_softplus=True, read=oracle.Table.of(tab), cu_seqlens=w.cu_seqlens.to(torch.int64),
+                         lib=lib)
+        if not torch.equal(r.y_exact, ref.y_exact):
+            raise AssertionError("SSD y differs from the token loop")
+        last = w.last_chunk_indices.long()
+        if not torch.equal(r.states[last], ref.state):
+            raise AssertionError("SSD final states differ from the token loop")
+
+
+def _ssd_chunked_numpy(w):
+    """The five stages of the chunked evaluation, in float64 numpy: per chunk
+    the cumulative decay, the chunk's own state contribution, the state
+    passed between chunks (seq_idx decides where a sequence opens), C . B^T
+    and the chunk scan.  Returns (y, states at chunk ends)."""
+    x, dt, B, C = (w.x.double().numpy(), w.dt.double().numpy(), w.B.double().numpy(), w.C.double().numpy())
+    A = w.A.double().numpy()
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    hpg = H // G
+    d = dt + (w.dt_bias.double().numpy() if w.dt_bias is not None else 0.0)
+    if w.dt_softplus:
+        d = np.logaddexp(0.0, d)
+    d = np.clip(d, w.dt_limit[0], w.dt_limit[1])
+    cu = w.cu_chunk_seqlens.long().numpy()
+    si = w.seq_idx.long().numpy()
+    init = None if w.initial_states is None else w.initial_states.double().numpy()
+    y = np.zeros((T, H, P))
+    states = np.zeros((len(si), H, P, N))
+    S = np.zeros((H, P, N))
+    for c in range(len(si)):
+        t0, t1 = cu[c], cu[c + 1]
+        if c == 0 or si[c] != si[c - 1]:
+            S = init[si[c]].copy() if init is not None else np.zeros((H, P, N))
+        for h in range(H):
+            g = h // hpg
+            acs = np.cumsum(A[h] * d[t0:t1, h])                       # stage 1
+            Bc, Cc, xc, dc = B[t0:t1, g], C[t0:t1, g], x[t0:t1, h], d[t0:t1, h]
+            wgt = np.exp(acs[-1] - acs) * dc if t1 > t0 else np.zeros(0)
+            Sc = (xc * wgt[:, None]).T @ Bc                             # stage 2: [P, N]
+            CB = Cc @ Bc.T                                               # stage 4: [L, L]
+            L = np.tril(np.exp(acs[:, None] - acs[None, :]))
+            yc = np.exp(acs)[:, None] * (Cc @ S[h].T) + (CB * L) @ (xc * dc[:, None])   # stage 5
+            if w.D is not None:
+                yc = yc + w.D[h].item() * xc
+            if w.z is not None:
+                zz = w.z[t0:t1, h].double().numpy()
+                yc = yc * zz / (1 + np.exp(-zz))
+            y[t0:t1, h] = yc
+            S[h] = (np.exp(acs[-1]) if t1 > t0 else 1.0) * S[h] + Sc       # stage 3
+        states[c] = S
+    return y, states
+
+
+def pin_ssd_chunked_form(lib):
+    """The oracle's token loop equals the chunked five-stage evaluation
+    (written out independently in numpy) to double rounding, for y and the
+    state at the end of every chunk, with ragged last chunks, several
+    sequences, a clamped dt and without initial states."""
+    cases = [dict(lengths=[9, 33, 2], chunk_size=8),
+             dict(lengths=[17, 17], chunk_size=16, dt_limit=(0.02, 0.3), with_init=False),
+             dict(lengths=[50], chunk_size=64, with_z=False, with_D=False)]
+    for i, kw in enumerate(cases):
+        lengths = kw.pop("lengths")
+        w = workloads.ssd_problem(52 + i, lengths, heads=4, dim=3, dstate=8, groups=2, state_dtype=torch.float64,
+                                  **kw)
+        r = _ssd_run(w, lib, state_dtype=torch.float64)
+        y, st = _ssd_chunked_numpy(w)
+        _close(r.y_exact.numpy(), y, rtol=1e-10, atol=1e-12, what=f"SSD y, case {i}")
+        _close(r.states.numpy(), st, rtol=1e-10, atol=1e-12, what=f"SSD states, case {i}")
+
+
+def pin_ssd_seq_idx_authority(lib):
+    """seq_idx alone decides where a sequence opens: re-labelling chunk 2
+    as sequence 1's makes it start from sequence 1's initial state, whatever
+    last_chunk_indices says, and chunk 3 continue from it."""
+    w = workloads.ssd_problem(55, [40, 40], heads=2, dim=2, dstate=4, groups=1, chunk_size=16,
+                              state_dtype=torch.float64)
+    relabel = w.seq_idx.clone()
+    relabel[2] = 1
+    r = _ssd_run(w, lib, **{})
+    r2 = oracle.ssd(w.x, w.dt, w.A, w.B, w.C, w.cu_chunk_seqlens, relabel, w.nseq, D=w.D, z=w.z,
+                    dt_bias=w.dt_bias, dt_softplus=True, initial_states=w.initial_states, lib=lib)
+    if not torch.equal(r.states[:2], r2.states[:2]):
+        raise AssertionError("chunks before the relabelled one must not change")
+    # chunk 2 alone from sequence 1's initial state, via the token loop
+    t0, t1 = int(w.cu_chunk_seqlens[2]), int(w.cu_chunk_seqlens[3])
+    sub = slice(t0, t1)
+    tab = torch.ones((1, t1 - t0), dtype=torch.int64)
+    ref = oracle.ssu(w.initial_states, w.x[sub], w.dt[sub], w.A, w.B[sub], w.C[sub], D=w.D, z=w.z[sub],
+                     dt_bias=w.dt_bias, dt_softplus=True, read=oracle.Table.of(tab),
+                     cu_seqlens=torch.tensor([0, t1 - t0]), lib=lib)
+    if not torch.equal(r2.states[2], ref.state[1]):
+        raise AssertionError("a relabelled chunk must open from its sequence's initial state")
+    if torch.equal(r2.states[3], r.states[3]):
+        raise AssertionError("the chunk after a relabelled one continues from it")
+
+
+def pin_ssd_dt_limit(lib):
+    """x = 0 leaves only the decay: the state at the end is
+    exp(A sum_t clamp(softplus(dt + bias), lo, hi)) times the initial state
+    (closed form, with values below, inside and above the limits)."""
+    w = workloads.ssd_problem(56, [30], heads=3, dim=2, dstate=4, groups=1, chunk_size=8, state_dtype=torch.float64,
+                              dt_limit=(0.2, 0.6))
+    w.x = torch.zeros_like(w.x)
+    r = _ssd_run(w, lib)
+    d = np.clip(np.logaddexp(0.0, w.dt.double().numpy() + w.dt_bias.double().numpy()), 0.2, 0.6)
+    if not (np.any(d == 0.2) and np.any(d == 0.6) and np.any((d > 0.2) & (d < 0.6))):
+        raise AssertionError("the case must exercise both limits")
+    decay = np.exp(w.A.double().numpy() * d.sum(axis=0))
+    want = decay[:, None, None] * w.initial_states[0].double().numpy()
+    _close(r.states[-1].numpy(), want, rtol=1e-12, atol=1e-15, what="dt_limit closed form")
+
+
 ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero, pin_zero_state,
             pin_A_zero, pin_decay_only, pin_unrolled, pin_basis_vectors, pin_group_map,
             pin_page_examples, pin_pad_never_written, pin_disable_and_untouched, pin_table_forms,
             pin_seed_position, pin_seed_position_per_row, pin_per_head_dt, pin_aliasing_refused,
             pin_replay_lossless, pin_replay_buffer_entries, pin_replay_buffer_len_one,
             pin_replay_pad_and_aliasing, pin_empty_sequences, pin_bounded_decay, pin_e4m3_codes,
-            pin_shadow_refresh, pin_replay_read_copy]
+            pin_shadow_refresh, pin_replay_read_copy, pin_ssd_equals_token_loop, pin_ssd_chunked_form,
+            pin_ssd_seq_idx_authority, pin_ssd_dt_limit]

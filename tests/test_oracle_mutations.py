@@ -55,6 +55,13 @@ MUTATIONS = [
      "if (0) {\n                            /* the read copy"),
     ("e4m3_no_saturation", "if (isinf(r) || r > 448.0)\n        r = 448.0;", ""),
     ("e4m3_exponent_bias", "ldexp((double)(f + 8), e - 10)", "ldexp((double)(f + 8), e - 11)"),
+    # SSD prefill
+    ("ssd_seq_idx_ignored", "if (c == 0 || pr->seq_idx[c] != pr->seq_idx[c - 1]) {", "if (c == 0) {"),
+    ("ssd_dt_limit_dropped", "d = fmin(fmax(d, pr->dt_lo), pr->dt_hi);", "d = d;"),
+    ("ssd_initial_ignored", "S[n] = pr->initial_states\n", "S[n] = 0 && pr->initial_states\n"),
+    ("ssd_decay_after_input",
+     "S[n] = S[n] * a + d * xv * load_elem(pr->B, (t * G + g) * N + n, pr->io_dtype);",
+     "S[n] = (S[n] + d * xv * load_elem(pr->B, (t * G + g) * N + n, pr->io_dtype)) * a;"),
 ]
 
 

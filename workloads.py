@@ -339,17 +339,6 @@ def copy_slots_b256_fp32(device="cpu", seed=1007, batch=256) -> CopyWorkload:
     return CopyWorkload("copy_slots_b256_fp32", state, perm[:batch].to(device), perm[batch:].to(device))
 
 
-NAMED = {
-    "tiny_onetoken": tiny_onetoken,
-    "b256_fp32": b256_fp32,
-    "b1024_bf16": b1024_bf16,
-    "mtp_64x7_fp32": mtp_64x7_fp32,
-    "varlen_fp16": varlen_fp16,
-    "replay_b256_fp32": replay_b256_fp32,
-    "replay_e4m3_b256_fp32": replay_e4m3_b256_fp32,
-    "replay_f16copy_b256_fp32": replay_f16copy_b256_fp32,
-    "copy_slots_b256_fp32": copy_slots_b256_fp32,
-}
 
 
 def _step_bias(g, heads, softplus):
@@ -441,3 +430,111 @@ def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads:
                  num_accepted=acc, dense_steps=max_len if dense else 0,
                  meta={"lengths": lens.tolist()})
     return w.to(device)
+
+
+# ---------------------------------------------------------------------------
+# Packed variable-length SSD prefill.
+# ---------------------------------------------------------------------------
+@dataclass
+class SsdWorkload:
+    name: str
+    x: torch.Tensor                      # [tokens, heads, dim] io dtype
+    dt: torch.Tensor                     # [tokens, heads] fp32
+    A: torch.Tensor                      # [heads] fp32
+    B: torch.Tensor                      # [tokens, groups, dstate]
+    C: torch.Tensor                      # [tokens, groups, dstate]
+    cu_seqlens: torch.Tensor             # [nseq + 1] int32
+    cu_chunk_seqlens: torch.Tensor       # [nchunks + 1] int32
+    seq_idx: torch.Tensor                # [nchunks] int32
+    last_chunk_indices: torch.Tensor     # [nseq] int32
+    chunk_size: int
+    D: Optional[torch.Tensor] = None
+    z: Optional[torch.Tensor] = None
+    dt_bias: Optional[torch.Tensor] = None
+    dt_softplus: bool = True
+    dt_limit: tuple = (0.0, float("inf"))
+    initial_states: Optional[torch.Tensor] = None   # [nseq, heads, dim, dstate]
+    state_dtype: torch.dtype = torch.float32
+    kind: str = "ssd"
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def nseq(self) -> int:
+        return self.cu_seqlens.numel() - 1
+
+    @property
+    def tokens(self) -> int:
+        return self.x.shape[0]
+
+    def to(self, device) -> "SsdWorkload":
+        moved = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in self.__dict__.items()}
+        return replace(self, **moved)
+
+
+def ssd_chunks(lengths, chunk_size):
+    """Chunking of packed sequences as vLLM's Mamba-2 prefill lays it out:
+    each sequence cut into chunks of ``chunk_size`` tokens from its first
+    token, the last one partial; no chunk spans two sequences.  Returns
+    (cu_seqlens, cu_chunk_seqlens, seq_idx, last_chunk_indices), int32."""
+    cu, cu_chunk, seq_idx, last = [0], [0], [], []
+    for b, n in enumerate(lengths):
+        if n < 1:
+            raise ValueError("every prefill sequence has at least one token")
+        start = cu[-1]
+        for k in range((n + chunk_size - 1) // chunk_size):
+            cu_chunk.append(start + min((k + 1) * chunk_size, n))
+            seq_idx.append(b)
+        last.append(len(seq_idx) - 1)
+        cu.append(start + n)
+    t = lambda v: torch.tensor(v, dtype=torch.int32)
+    return t(cu), t(cu_chunk), t(seq_idx), t(last)
+
+
+def ssd_problem(seed: int, lengths, *, heads=4, dim=8, dstate=16, groups=2, chunk_size=16,
+                io_dtype=torch.bfloat16, state_dtype=torch.float32, with_init=True, with_D=True, with_z=True,
+                with_bias=True, dt_softplus=True, dt_limit=(0.0, float("inf")), device="cpu",
+                name=None) -> SsdWorkload:
+    """A seeded SSD prefill problem: x, z, B, C ~ N(0,1) in the io dtype; dt ~
+    N(0,1) fp32 per (token, head); dt_bias as the decode workloads; A =
+    -exp(U(0, 2.8)); D ~ N(0,1); initial states N(0, 0.1)."""
+    cu, cu_chunk, seq_idx, last = ssd_chunks(list(lengths), chunk_size)
+    tokens = int(cu[-1])
+    g = _gen(seed, "cpu")
+    x = _normal((tokens, heads, dim), g, "cpu", dtype=io_dtype)
+    z = _normal((tokens, heads, dim), g, "cpu", dtype=io_dtype) if with_z else None
+    dt = _normal((tokens, heads), g, "cpu") if dt_softplus else _uniform((tokens, heads), g, "cpu", 0.0, 0.1)
+    dt_bias = _step_bias(g, heads, dt_softplus) if with_bias else None
+    A = -torch.exp(_uniform((heads,), g, "cpu", 0.0, 2.8))
+    D = _normal((heads,), g, "cpu") if with_D else None
+    B = _normal((tokens, groups, dstate), g, "cpu", dtype=io_dtype)
+    C = _normal((tokens, groups, dstate), g, "cpu", dtype=io_dtype)
+    init = _normal((len(lengths), heads, dim, dstate), g, "cpu", std=0.1, dtype=state_dtype) if with_init else None
+    w = SsdWorkload(name or f"ssd_{seed}", x, dt, A, B, C, cu, cu_chunk, seq_idx, last, chunk_size, D=D, z=z,
+                    dt_bias=dt_bias, dt_softplus=dt_softplus, dt_limit=dt_limit, initial_states=init,
+                    state_dtype=state_dtype)
+    return w.to(device)
+
+
+def ssd_prefill_16k_bf16(device="cpu", seed=1010, batch=8) -> SsdWorkload:
+    """Mamba-2 prefill on the decode workloads' layer shape (heads 128, dim 64,
+    dstate 128, groups 8), chunk 256, bf16 x/z/B/C, fp32 dt with bias and
+    softplus, fp32 initial and returned states; ``batch`` sequences with
+    lengths U{1024..3072} (about 2048 tokens each, ragged last chunks)."""
+    gl = _gen(seed + 3, "cpu")
+    lengths = torch.randint(1024, 3073, (batch,), generator=gl).tolist()
+    return ssd_problem(seed, lengths, heads=128, dim=64, dstate=128, groups=8, chunk_size=256, device=device,
+                       name="ssd_prefill_16k_bf16")
+
+
+NAMED = {
+    "tiny_onetoken": tiny_onetoken,
+    "b256_fp32": b256_fp32,
+    "b1024_bf16": b1024_bf16,
+    "mtp_64x7_fp32": mtp_64x7_fp32,
+    "varlen_fp16": varlen_fp16,
+    "replay_b256_fp32": replay_b256_fp32,
+    "replay_e4m3_b256_fp32": replay_e4m3_b256_fp32,
+    "replay_f16copy_b256_fp32": replay_f16copy_b256_fp32,
+    "copy_slots_b256_fp32": copy_slots_b256_fp32,
+    "ssd_prefill_16k_bf16": ssd_prefill_16k_bf16,
+}
