@@ -56,13 +56,19 @@ DESCRIPTIONS = {
                                 "fold read the copy, folds rewrite it",
     "copy_slots_b256_fp32": "256 whole-slot state copies of 4 MiB (heads 128, dim 64, dstate 128, fp32) between "
                             "random disjoint slot sets of a 512-slot pool; steps alternate the direction",
+    "ssd_prefill_16k_bf16": "packed variable-length SSD prefill, 8 sequences of U{1024..3072} tokens (14269 in "
+                            "all), heads 128, dim 64, dstate 128, groups 8, chunk 256, bf16 x/z/B/C/y, fp32 dt "
+                            "with bias and softplus, D, fp32 initial and final states",
 }
 COPY_METRIC = "whole-slot state copies/s and achieved HBM GB/s (read + write)"
 COPY_UNIT = "copies/s"
+SSD_METRIC = "SSD prefill tokens/s and achieved HBM GB/s (inputs and outputs once)"
+SSD_UNIT = "tokens/s"
 KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"],
-                  "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"]}
+                  "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"],
+                  "ssd": ["ssu_ssd.cu", "ssu_device.cuh", "ssu_internal.h"]}
 
 
 # --------------------------------------------------------------------------
@@ -506,6 +512,158 @@ def copy_oracle_rate(w_cpu, budget_s: float):
     return done / spent, f"{done} copies of {nbytes} bytes in {samples} samples"
 
 
+def ssd_accounting(w) -> dict:
+    """Bytes the prefill must move at least (every input read once, y and the
+    returned states written once) and the tensor-core work of the chunked
+    evaluation, per call."""
+    T, H, P = w.x.shape
+    G, N = w.B.shape[1], w.B.shape[2]
+    io = w.x.element_size()
+    sb = H * P * N * torch.finfo(w.state_dtype).bits // 8
+    nseq = w.nseq
+    meta = (w.cu_chunk_seqlens.numel() + w.seq_idx.numel() + w.last_chunk_indices.numel()) * 4
+    inputs = (T * H * P * io * (2 if w.z is not None else 1) + T * H * w.dt.element_size() + 2 * T * G * N * io
+              + (nseq * sb if w.initial_states is not None else 0) + meta)
+    outputs = T * H * P * io + nseq * sb
+    nchunks = w.seq_idx.numel()
+    ch = nchunks * H
+    # chunk states, then per 64-token block of the scan: C . S_in^T and the
+    # causal C . B^T and M . X products (full 16 x 16 tiles up to the diagonal)
+    lens = (w.cu_chunk_seqlens[1:] - w.cu_chunk_seqlens[:-1]).tolist()
+    causal = sum(sum((t // 16 + 1) * 16 for t in range(0, L, 16)) * 16 for L in lens)  # (t, s) pairs, 16-row tiles
+    flops = H * (2 * T * P * N + 2 * T * N * P + 2 * causal * N + 2 * causal * P)
+    return {"inputs": inputs, "outputs": outputs, "total": inputs + outputs, "flops": flops,
+            "workspace": 4 * ch * P * N * 4, "tokens": T}
+
+
+def run_ssd(args, rank, world, device):
+    """The SSD prefill workload: one step = one ssu_ssd_prefill call over the
+    packed batch (three kernel launches)."""
+    from selective_state_update_gb300 import build as ssu_build
+    import selective_state_update_gb300 as ssu
+    ssu_build.build()
+    ssu.lib()
+    w = make_workload(args, device, seed_offset=97 * rank)
+    acct = ssd_accounting(w)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    out = torch.empty_like(w.x)
+
+    def call():
+        return ssu.ssu_ssd_prefill(w.x, w.dt, w.A, w.B, w.C, w.chunk_size, w.cu_chunk_seqlens, w.seq_idx,
+                                   w.last_chunk_indices, out=out, D=w.D, z=w.z, dt_bias=w.dt_bias,
+                                   dt_softplus=w.dt_softplus, dt_limit=w.dt_limit,
+                                   initial_states=w.initial_states, state_dtype=w.state_dtype, nseq=w.nseq,
+                                   status=status)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clocks:
+        whole0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        whole1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(whole0.elapsed_time(whole1), device)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if int(status.item()) != 0:
+        raise SystemExit(f"ssu_ssd_prefill reported status {int(status.item())}")
+    # End to end: the step's inputs from pinned host memory, the prefill, y
+    # and the returned states back to pinned host memory.
+    dev_in = [t for t in (w.x, w.dt, w.z, w.B, w.C, w.initial_states, w.cu_chunk_seqlens, w.seq_idx,
+                          w.last_chunk_indices) if t is not None]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_y = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    _, st = call()
+    host_s = torch.empty(st.shape, dtype=st.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_y.numel() * host_y.element_size() + host_s.numel() * host_s.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        _, st = call()
+        host_y.copy_(out, non_blocking=True)
+        host_s.copy_(st, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, device)
+    peak, peak_src = hbm_peak()
+    achieved = acct["total"] / (call_ms * 1e-3) / 1e9
+    return {
+        "metric": SSD_METRIC, "value": aggregate_rate(acct["tokens"], world, args.steps, total_ms),
+        "unit": SSD_UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "tokens_per_gpu": acct["tokens"], "chunks": int(w.seq_idx.numel()),
+                   "parallelism": f"{world} independent replicas (one packed batch per GPU)",
+                   "l2": "no flush: %.2f GB of inputs and outputs per step" % (acct["total"] / 1e9),
+                   "tensor_flops_per_call": acct["flops"],
+                   "workspace_bytes_moved_per_call": acct["workspace"]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("ssd", args.workload),
+                     "algorithmic_bytes_per_launch": acct["total"],
+                     "kernel": "ssd prefill call (ssd_chunk_state + ssd_state_pass + ssd_chunk_scan)",
+                     "launch_ms": call_ms},
+        "e2e": {"value": aggregate_rate(acct["tokens"], world, e2e_steps, e2e_s * 1e3), "unit": SSD_UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
+def ssd_oracle_rate(w_cpu, budget_s: float, heads_per_sample: int = 16):
+    """The oracle's packed SSD on samples of the prefill workload: each sample
+    one whole sequence on one block of `heads_per_sample` heads (whole
+    groups), sequences and head blocks in turn; a token counts as
+    heads_per_sample / heads of a token."""
+    import oracle
+    oracle.build()
+    H, G = w_cpu.x.shape[1], w_cpu.B.shape[1]
+    hs = max(heads_per_sample, H // G)
+    gs = hs // (H // G)
+    cu = w_cpu.cu_seqlens.tolist()
+    cuc = w_cpu.cu_chunk_seqlens.tolist()
+    si = w_cpu.seq_idx.tolist()
+    done, spent, samples = 0.0, 0.0, 0
+    while spent < budget_s:
+        b = samples % w_cpu.nseq
+        h0 = (samples // w_cpu.nseq * hs) % H
+        g0 = h0 // (H // G)
+        lo, hi = cu[b], cu[b + 1]
+        chunks = [c for c in range(len(si)) if si[c] == b]
+        sub_cu = torch.tensor([cuc[c] - lo for c in chunks] + [cuc[chunks[-1] + 1] - lo], dtype=torch.int32)
+        hsl, gsl = slice(h0, h0 + hs), slice(g0, g0 + gs)
+        sub = lambda t, sl: None if t is None else t[lo:hi, sl].contiguous()
+        t0 = time.perf_counter()
+        oracle.ssd(sub(w_cpu.x, hsl), sub(w_cpu.dt, hsl), w_cpu.A[hsl], sub(w_cpu.B, gsl), sub(w_cpu.C, gsl),
+                   sub_cu, torch.zeros(len(chunks), dtype=torch.int32), 1,
+                   D=None if w_cpu.D is None else w_cpu.D[hsl], z=sub(w_cpu.z, hsl),
+                   dt_bias=None if w_cpu.dt_bias is None else w_cpu.dt_bias[hsl], dt_softplus=w_cpu.dt_softplus,
+                   dt_limit=w_cpu.dt_limit,
+                   initial_states=None if w_cpu.initial_states is None else
+                   w_cpu.initial_states[b:b + 1, hsl].contiguous(),
+                   state_dtype=w_cpu.state_dtype)
+        spent += time.perf_counter() - t0
+        done += (hi - lo) * hs / H
+        samples += 1
+    return done / spent, (f"{samples} samples of one whole sequence on {hs} of {H} heads "
+                          f"({done:.0f} token-equivalents)")
+
+
 # --------------------------------------------------------------------------
 # The oracle on the host cores.
 # --------------------------------------------------------------------------
@@ -572,7 +730,7 @@ def _oracle_call(sub):
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
          "varlen_fp16": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008,
-         "replay_f16copy_b256_fp32": 1009}
+         "replay_f16copy_b256_fp32": 1009, "ssd_prefill_16k_bf16": 1010}
 
 
 def make_workload(args, device, seed_offset=0):
@@ -624,6 +782,17 @@ def run_reference(args):
     w_cpu = _cpu_workload(args)
     import oracle
     oracle.build()
+    if getattr(w_cpu, "kind", "") == "ssd":
+        budget = min(150.0, 5.0 + 1.0 * (args.steps + args.warmup))
+        value, sample = ssd_oracle_rate(w_cpu, budget)
+        return {
+            "impl": "reference", "metric": SSD_METRIC, "value": value, "unit": SSD_UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * ssd_accounting(w_cpu)["tokens"] / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "cpu_baseline": {"value": value, "unit": SSD_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": SSD_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     if getattr(w_cpu, "kind", "") == "copy":
         budget = min(150.0, 1.0 + 0.05 * (args.steps + args.warmup))
         value, sample = copy_oracle_rate(w_cpu, budget)
@@ -694,9 +863,14 @@ def main():
     # The oracle baseline runs before the first GPU call (no fork after CUDA init).
     cpu = None
     is_copy = args.workload.startswith("copy_")
+    is_ssd = args.workload.startswith("ssd_")
     if rank == 0 and not args.no_cpu_baseline:
         w_cpu = _cpu_workload(args)
-        if is_copy:
+        if is_ssd:
+            rate, desc = ssd_oracle_rate(w_cpu, args.cpu_baseline_seconds)
+            cpu = {"value": rate, "unit": SSD_UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+        elif is_copy:
             rate, desc = copy_oracle_rate(w_cpu, args.cpu_baseline_seconds)
             cpu = {"value": rate, "unit": COPY_UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{desc} of {args.workload} (numpy, one thread)"}
@@ -713,7 +887,8 @@ def main():
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
-    res = run_copy(args, rank, world, device) if is_copy else run_ours(args, rank, world, device)
+    run = run_ssd if is_ssd else (run_copy if is_copy else run_ours)
+    res = run(args, rank, world, device)
     res["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(res), flush=True)

@@ -252,6 +252,69 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
                              const ssu_replay_buffers *rb, void *stream);
 
 /*
+ * Packed variable-length SSD prefill (MATE documentation, page "Mamba / SSU",
+ * section "SSD packed prefill" and the API reference of
+ * ssd_combined_fwd_varlen).  For every token t of a packed batch, head h,
+ * dim row p, g = h / (heads / groups):
+ *     dt'  = clamp(softplus?(dt[t,h] + dt_bias[h]), dt_min, dt_max)
+ *     S[n] = S[n] exp(A[h] dt') + dt' x[t,h,p] B[t,g,n]
+ *     y[t,h,p] = (sum_n S[n] C[t,g,n] + D[h] x[t,h,p]) * silu(z[t,h,p])
+ * evaluated chunk by chunk (cumulative decays, chunk states, state passing,
+ * C . B^T, chunk scan).  Chunk c covers tokens [cu_chunk_seqlens[c],
+ * cu_chunk_seqlens[c+1]) (at most chunk_size tokens); chunk c opens a
+ * sequence when c == 0 or seq_idx[c] != seq_idx[c-1] -- seq_idx, not
+ * last_chunk_indices, decides -- and then starts from
+ * initial_states[seq_idx[c]] (zero without initial states); otherwise it
+ * continues from the previous chunk's state.  `states` receives the state at
+ * the end of every chunk ([nchunks, heads, dim, dstate]) when
+ * return_intermediate is set, otherwise the state at the end of chunk
+ * last_chunk_indices[b] for every sequence b ([nseq, heads, dim, dstate]),
+ * in state_dtype.  Implemented: x, z, B, C and y bf16, contiguous; dt fp32 /
+ * fp16 / bf16 [tokens, heads]; dim 64; dstate 64 or 128; chunk_size 64, 128
+ * or 256 (others return SSU_ERR_UNSUPPORTED).  The contractions run on the
+ * tensor cores with bf16 operands and fp32 accumulation; the chunk states
+ * use a two-part bf16 split of the decay-weighted x.  `workspace` is
+ * caller-owned device memory of at least ssu_ssd_workspace_size() bytes,
+ * 256-byte aligned; its contents need no initialisation.  Malformed chunks
+ * (negative, decreasing, longer than chunk_size or past `tokens`) set
+ * SSU_DEV_BAD_SEQLEN and produce no y; a seq_idx outside [0, nseq), or (without
+ * return_intermediate) a last_chunk_indices entry outside [0, nchunks), sets
+ * SSU_DEV_BAD_ENTRY and leaves the states it concerns unwritten.  Host-side
+ * errors (NULL pointers, unaligned tensors, a short workspace) return
+ * SSU_ERR_INVALID before anything is launched.
+ */
+typedef struct ssu_ssd_args {
+    int64_t tokens, heads, dim, dstate, groups, nseq, nchunks, chunk_size;
+    int32_t io_dtype;              /* SSU_BF16                                              */
+    int32_t dt_dtype, state_dtype; /* ssu_dtype                                             */
+    int32_t meta_type;             /* SSU_I32 / SSU_I64: cu_chunk_seqlens, seq_idx, last... */
+    int32_t dt_softplus;
+    int32_t return_intermediate;
+    float dt_min, dt_max;          /* dt_limit; (0, +inf) leaves dt' unclamped above        */
+    const void *x;                 /* device [tokens, heads, dim]                           */
+    const void *dt;                /* device [tokens, heads]                                */
+    const void *B, *C;             /* device [tokens, groups, dstate]                       */
+    const void *z;                 /* device [tokens, heads, dim] or NULL                   */
+    const float *A, *D, *dt_bias;  /* device [heads] fp32; D and dt_bias may be NULL        */
+    const void *cu_chunk_seqlens;  /* device [nchunks + 1]                                  */
+    const void *seq_idx;           /* device [nchunks]                                      */
+    const void *last_chunk_indices;/* device [nseq]                                         */
+    const void *initial_states;    /* device [nseq, heads, dim, dstate] state_dtype, or NULL */
+    void *y;                       /* device [tokens, heads, dim] (out)                     */
+    void *states;                  /* device, see above (out)                               */
+    void *workspace;
+    uint64_t workspace_bytes;
+    int32_t *d_status;             /* device int32 or NULL                                  */
+} ssu_ssd_args;
+
+/* Workspace ssu_ssd_prefill needs for these sizes (bytes, into *bytes). */
+ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t dim, int64_t dstate, int64_t chunk_size,
+                                  uint64_t *bytes);
+
+/* One packed SSD prefill call: three kernel launches on `stream`. */
+ssu_status ssu_ssd_prefill(const ssu_ssd_args *args, void *stream);
+
+/*
  * One copy of a batch: `bytes` bytes from device address `src` to device
  * address `dst` (any alignment; 16-byte aligned addresses take the vector
  * path).

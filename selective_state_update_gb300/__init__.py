@@ -13,6 +13,8 @@ Entry points (same names as the C ABI):
   ssu_update_packed    packed variable-length / MTP rows (cu_seqlens) or the
                        dense [batch, steps, heads, dim] form
   ssu_shadow_refresh   the low-precision read copy of checkpoints
+  ssu_ssd_prefill      packed variable-length SSD prefill (and
+                       ssd_combined_fwd_varlen, the MATE-shaped call)
   ssu_batch_copy       batched state copies with memmove semantics
   ssu_prewarm          load a configuration's kernel before graph capture
 and ``selective_state_update``, the MATE/FlashInfer-shaped call (MATE
@@ -28,6 +30,7 @@ from typing import Optional
 import torch
 
 __all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_shadow_refresh",
+           "ssu_ssd_prefill", "ssd_combined_fwd_varlen",
            "ssu_batch_copy", "copy_table",
            "slot_copies", "ssu_prewarm",
            "selective_state_update",
@@ -79,6 +82,23 @@ class ReplayBuffers(ctypes.Structure):
                 ("shadow_scale", ctypes.c_void_p)]
 
 
+class SsdArgs(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64), ("dstate", ctypes.c_int64),
+        ("groups", ctypes.c_int64), ("nseq", ctypes.c_int64), ("nchunks", ctypes.c_int64),
+        ("chunk_size", ctypes.c_int64),
+        ("io_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32), ("state_dtype", ctypes.c_int32),
+        ("meta_type", ctypes.c_int32), ("dt_softplus", ctypes.c_int32), ("return_intermediate", ctypes.c_int32),
+        ("dt_min", ctypes.c_float), ("dt_max", ctypes.c_float),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+        ("z", ctypes.c_void_p), ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("cu_chunk_seqlens", ctypes.c_void_p), ("seq_idx", ctypes.c_void_p),
+        ("last_chunk_indices", ctypes.c_void_p), ("initial_states", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("states", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_uint64), ("d_status", ctypes.c_void_p),
+    ]
+
+
 # formats of the read copy (SSU_SHADOW_*)
 SHADOW_NONE, SHADOW_F16, SHADOW_E4M3 = 0, 1, 2
 
@@ -122,6 +142,10 @@ def lib():
         L.ssu_batch_copy.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
                                      ctypes.c_void_p]
         L.ssu_batch_copy.restype = ctypes.c_int
+        L.ssu_ssd_workspace_size.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(ctypes.c_uint64)]
+        L.ssu_ssd_workspace_size.restype = ctypes.c_int
+        L.ssu_ssd_prefill.argtypes = [ctypes.POINTER(SsdArgs), ctypes.c_void_p]
+        L.ssu_ssd_prefill.restype = ctypes.c_int
         L.ssu_shadow_refresh.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.ssu_shadow_refresh.restype = ctypes.c_int
@@ -349,6 +373,84 @@ def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
     if rc != OK:
         _raise(rc)
     return out, count_out
+
+
+_SSD_WORKSPACE = {}
+
+
+def _ssd_workspace(device, nbytes: int) -> torch.Tensor:
+    """A per-device workspace that only grows (the "cached workspace" of the
+    MATE page): a steady-state call allocates nothing."""
+    key = str(device)
+    ws = _SSD_WORKSPACE.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _SSD_WORKSPACE[key] = ws
+    return ws
+
+
+def ssu_ssd_prefill(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, last_chunk_indices=None,
+                    out=None, D=None, z=None, dt_bias=None, dt_softplus=False, dt_limit=(0.0, float("inf")),
+                    initial_states=None, return_intermediate_states=False, state_dtype=None, nseq=None,
+                    status=None, stream=None):
+    """Packed variable-length SSD prefill (see ``include/ssu.h``).  x ``[tokens,
+    heads, dim]`` bf16, dt ``[tokens, heads]``, B, C ``[tokens, groups,
+    dstate]`` bf16.  Returns (y, states)."""
+    _need(x.dim() == 3 and dt.dim() == 2 and B.dim() == 3 and C.shape == B.shape, "x, dt, B, C shapes")
+    tokens, heads, dim = x.shape
+    groups, dstate = B.shape[1], B.shape[2]
+    _need(dt.shape == (tokens, heads) and B.shape[0] == tokens, "dt must be [tokens, heads], B [tokens, ...]")
+    for t in (x, dt, B, C, z, out, initial_states):
+        _need(t is None or (t.is_cuda and t.is_contiguous()), "tensors must be contiguous CUDA tensors")
+    meta = cu_chunk_seqlens.dtype
+    _need(meta in _ITYPE and seq_idx.dtype == meta and (last_chunk_indices is None or last_chunk_indices.dtype == meta),
+          "cu_chunk_seqlens, seq_idx and last_chunk_indices share one integer dtype")
+    nchunks = seq_idx.numel()
+    if nseq is None:
+        nseq = last_chunk_indices.numel() if last_chunk_indices is not None else initial_states.shape[0]
+    sdt = state_dtype or (initial_states.dtype if initial_states is not None else C.dtype)
+    out = out if out is not None else torch.empty_like(x)
+    states = torch.empty(((nchunks if return_intermediate_states else nseq), heads, dim, dstate), dtype=sdt,
+                         device=x.device)
+    if initial_states is not None and initial_states.dtype != sdt:
+        initial_states = initial_states.to(sdt)
+    nbytes = ctypes.c_uint64(0)
+    rc = lib().ssu_ssd_workspace_size(nchunks, heads, dim, dstate, chunk_size, ctypes.byref(nbytes))
+    if rc != OK:
+        _raise(rc)
+    ws = _ssd_workspace(x.device, nbytes.value)
+    hi = float(dt_limit[1])
+    a = SsdArgs(tokens=tokens, heads=heads, dim=dim, dstate=dstate, groups=groups, nseq=nseq, nchunks=nchunks,
+                chunk_size=chunk_size, io_dtype=_DTYPE.get(x.dtype, -1), dt_dtype=_DTYPE[dt.dtype],
+                state_dtype=_DTYPE[sdt], meta_type=_ITYPE[meta], dt_softplus=int(bool(dt_softplus)),
+                return_intermediate=int(bool(return_intermediate_states)), dt_min=float(dt_limit[0]),
+                dt_max=min(hi, 3.4028234663852886e38),
+                x=x.data_ptr(), dt=dt.data_ptr(), B=B.data_ptr(), C=C.data_ptr(), z=_ptr(z), A=A.data_ptr(),
+                D=_ptr(D), dt_bias=_ptr(dt_bias), cu_chunk_seqlens=cu_chunk_seqlens.data_ptr(),
+                seq_idx=seq_idx.data_ptr(), last_chunk_indices=_ptr(last_chunk_indices),
+                initial_states=_ptr(initial_states), y=out.data_ptr(), states=states.data_ptr(),
+                workspace=ws.data_ptr(), workspace_bytes=ws.numel(), d_status=_ptr(status))
+    rc = lib().ssu_ssd_prefill(ctypes.byref(a), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    return out, states
+
+
+def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seqlens, last_chunk_indices, seq_idx,
+                            out=None, D=None, z=None, dt_bias=None, dt_softplus=False, dt_limit=(0.0, float("inf")),
+                            initial_states=None, return_intermediate_states=False, state_dtype=None,
+                            checkpoint_token_indices=None, checkpoint_state_slots=None, checkpoint_states=None):
+    """The MATE-shaped prefill call (MATE "Mamba / SSU", API reference of
+    ssd_combined_fwd_varlen): y into ``out`` (allocated when None), returns
+    the state buffer.  The checkpoint_* arguments are not implemented and
+    raise."""
+    if any(v is not None for v in (checkpoint_token_indices, checkpoint_state_slots, checkpoint_states)):
+        raise NotImplementedError("checkpoint_* (replay checkpoints during prefill) is not implemented")
+    _, states = ssu_ssd_prefill(x, dt, A, B, C, chunk_size, cu_chunk_seqlens, seq_idx, last_chunk_indices, out=out,
+                                D=D, z=z, dt_bias=dt_bias, dt_softplus=dt_softplus, dt_limit=dt_limit,
+                                initial_states=initial_states, return_intermediate_states=return_intermediate_states,
+                                state_dtype=state_dtype, nseq=cu_seqlens.numel() - 1)
+    return states
 
 
 def ssu_shadow_refresh(state: torch.Tensor, shadow: torch.Tensor, shadow_scale: Optional[torch.Tensor] = None,

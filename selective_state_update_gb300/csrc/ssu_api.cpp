@@ -263,6 +263,84 @@ ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes,
     return launched(ssu::launch_copy(copies, n, max_bytes, d_status, static_cast<cudaStream_t>(stream)));
 }
 
+ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t dim, int64_t dstate, int64_t chunk_size,
+                                  uint64_t *bytes) {
+    if (!bytes) return fail(SSU_ERR_INVALID, "bytes is NULL");
+    if (nchunks < 0 || heads <= 0 || dim <= 0 || dstate <= 0 || chunk_size <= 0)
+        return fail(SSU_ERR_INVALID, "sizes must be positive (nchunks >= 0)");
+    const uint64_t ch = static_cast<uint64_t>(nchunks) * heads;
+    auto up = [](uint64_t v) { return (v + 255) / 256 * 256; };
+    *bytes = up(ch * dim * dstate * 4) + 2 * up(ch * chunk_size * 4) + up(ch * 4);
+    return ok();
+}
+
+ssu_status ssu_ssd_prefill(const ssu_ssd_args *a, void *stream) {
+    if (a == nullptr) return fail(SSU_ERR_INVALID, "args is NULL");
+    if (a->tokens < 0 || a->nseq < 0 || a->nchunks < 0) return fail(SSU_ERR_INVALID, "negative sizes");
+    if (a->heads <= 0 || a->groups <= 0 || a->heads % a->groups != 0)
+        return fail(SSU_ERR_INVALID, "heads (%lld) must be a positive multiple of groups (%lld)", (long long)a->heads,
+                    (long long)a->groups);
+    if (a->io_dtype != SSU_BF16) return fail(SSU_ERR_UNSUPPORTED, "the SSD prefill takes bf16 x, z, B, C and y");
+    if (!valid_dtype(a->dt_dtype) || !valid_dtype(a->state_dtype)) return fail(SSU_ERR_INVALID, "bad dtype");
+    if (!valid_itype(a->meta_type)) return fail(SSU_ERR_INVALID, "meta_type %d is not an ssu_itype", a->meta_type);
+    if (a->dim != 64) return fail(SSU_ERR_UNSUPPORTED, "the SSD prefill supports dim 64 (got %lld)", (long long)a->dim);
+    if (a->dstate != 64 && a->dstate != 128)
+        return fail(SSU_ERR_UNSUPPORTED, "the SSD prefill supports dstate 64 or 128 (got %lld)", (long long)a->dstate);
+    if (a->chunk_size != 64 && a->chunk_size != 128 && a->chunk_size != 256)
+        return fail(SSU_ERR_UNSUPPORTED, "chunk_size %lld is not supported (64, 128, 256)", (long long)a->chunk_size);
+    if (!(a->dt_min <= a->dt_max)) return fail(SSU_ERR_INVALID, "dt_limit must satisfy min <= max");
+    if (a->nchunks == 0 || a->tokens == 0) return ok();
+    if (a->nchunks > 65535 * 64 || a->heads > 65535) return fail(SSU_ERR_INVALID, "too many chunks or heads");
+    if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->cu_chunk_seqlens || !a->seq_idx || !a->y || !a->states ||
+        (!a->return_intermediate && !a->last_chunk_indices) || !a->workspace)
+        return fail(SSU_ERR_INVALID, "a required pointer is NULL");
+    const void *aligned[] = {a->x, a->B, a->C, a->y, a->states, a->workspace, a->z, a->initial_states};
+    for (const void *q : aligned)
+        if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return fail(SSU_ERR_INVALID, "tensors must be 16-byte aligned");
+    uint64_t need = 0;
+    ssu_ssd_workspace_size(a->nchunks, a->heads, a->dim, a->dstate, a->chunk_size, &need);
+    if (a->workspace_bytes < need)
+        return fail(SSU_ERR_INVALID, "workspace of %lld bytes is smaller than the %lld needed",
+                    (long long)a->workspace_bytes, (long long)need);
+    ssu::SsdParams p{};
+    p.tokens = a->tokens;
+    p.nchunks = a->nchunks;
+    p.nseq = a->nseq;
+    p.H = static_cast<int32_t>(a->heads);
+    p.G = static_cast<int32_t>(a->groups);
+    p.hpg = static_cast<int32_t>(a->heads / a->groups);
+    p.P = static_cast<int32_t>(a->dim);
+    p.N = static_cast<int32_t>(a->dstate);
+    p.Q = static_cast<int32_t>(a->chunk_size);
+    p.dt_dtype = a->dt_dtype;
+    p.state_dtype = a->state_dtype;
+    p.softplus = a->dt_softplus != 0;
+    p.intermediate = a->return_intermediate != 0;
+    p.meta_i64 = a->meta_type == SSU_I64;
+    p.dt_lo = a->dt_min;
+    p.dt_hi = a->dt_max;
+    p.x = a->x, p.dt = a->dt, p.B = a->B, p.C = a->C, p.z = a->z;
+    p.A = a->A, p.D = a->D, p.dt_bias = a->dt_bias;
+    p.cu_chunk = a->cu_chunk_seqlens, p.seq_idx = a->seq_idx, p.last_chunk = a->last_chunk_indices;
+    p.init = a->initial_states;
+    p.y = a->y;
+    p.states = a->states;
+    p.status = a->d_status;
+    {
+        const uint64_t ch = static_cast<uint64_t>(a->nchunks) * a->heads;
+        auto up = [](uint64_t v) { return (v + 255) / 256 * 256; };
+        unsigned char *w = static_cast<unsigned char *>(a->workspace);
+        p.ws_state = reinterpret_cast<float *>(w);
+        w += up(ch * a->dim * a->dstate * 4);
+        p.ws_acs = reinterpret_cast<float *>(w);
+        w += up(ch * a->chunk_size * 4);
+        p.ws_dtp = reinterpret_cast<float *>(w);
+        w += up(ch * a->chunk_size * 4);
+        p.ws_dec = reinterpret_cast<float *>(w);
+    }
+    return launched(ssu::launch_ssd(p, static_cast<cudaStream_t>(stream)));
+}
+
 ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate,
                               int32_t format, void *shadow, float *scale, void *stream) {
     if (!valid_dtype(state_dtype)) return fail(SSU_ERR_INVALID, "state_dtype %d is not an ssu_dtype", state_dtype);

@@ -151,3 +151,64 @@ def test_shadow_refresh_host_checks(libssu):
     assert libssu.ssu_shadow_refresh(16, 0, 0, 128, 2, None, None, None) == ssu.OK          # nothing to do
     assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 2, 32, None, None) == ssu.ERR_INVALID   # E4M3 without scales
     assert "NULL" in libssu.ssu_last_error().decode()
+
+
+def test_ssd_args_layout_matches_the_header():
+    probe = r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "ssu.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu\n", sizeof(ssu_ssd_args), offsetof(ssu_ssd_args, dt_min),
+         offsetof(ssu_ssd_args, x), offsetof(ssu_ssd_args, workspace_bytes), offsetof(ssu_ssd_args, d_status));
+  return 0;
+}
+'''
+    exe = os.path.join(ROOT, "selective_state_update_gb300", "_build", "ssd_layout_probe")
+    os.makedirs(os.path.dirname(exe), exist_ok=True)
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-x", "c", "-", "-o", exe],
+                   input=probe, text=True, check=True)
+    vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    S = ssu.SsdArgs
+    assert vals == [ctypes.sizeof(S), S.dt_min.offset, S.x.offset, S.workspace_bytes.offset, S.d_status.offset]
+
+
+def _ssd_args(**kw):
+    a = ssu.SsdArgs(tokens=100, heads=4, dim=64, dstate=128, groups=2, nseq=2, nchunks=3, chunk_size=64,
+                    io_dtype=2, dt_dtype=0, state_dtype=0, meta_type=0, dt_softplus=1, dt_min=0.0, dt_max=1e30,
+                    x=256, dt=512, B=768, C=1024, A=1280, cu_chunk_seqlens=1536, seq_idx=1792,
+                    last_chunk_indices=2048, y=2304, states=2560, workspace=4096, workspace_bytes=1 << 30)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("kw,code,needle", [
+    (dict(io_dtype=0), ssu.ERR_UNSUPPORTED, "bf16"),
+    (dict(dim=32), ssu.ERR_UNSUPPORTED, "dim 64"),
+    (dict(dstate=96), ssu.ERR_UNSUPPORTED, "dstate"),
+    (dict(chunk_size=100), ssu.ERR_UNSUPPORTED, "chunk_size"),
+    (dict(groups=3), ssu.ERR_INVALID, "multiple of groups"),
+    (dict(meta_type=4), ssu.ERR_INVALID, "meta_type"),
+    (dict(dt_min=2.0, dt_max=1.0), ssu.ERR_INVALID, "dt_limit"),
+    (dict(B=None), ssu.ERR_INVALID, "NULL"),
+    (dict(last_chunk_indices=None), ssu.ERR_INVALID, "NULL"),
+    (dict(x=264), ssu.ERR_INVALID, "aligned"),
+    (dict(workspace_bytes=1024), ssu.ERR_INVALID, "workspace"),
+    (dict(tokens=-1), ssu.ERR_INVALID, "negative"),
+])
+def test_ssd_host_checks_reject_before_launch(libssu, kw, code, needle):
+    a = _ssd_args(**kw)
+    assert libssu.ssu_ssd_prefill(ctypes.byref(a), None) == code
+    assert needle in libssu.ssu_last_error().decode()
+
+
+def test_ssd_workspace_size_and_empty_call(libssu):
+    n = ctypes.c_uint64(0)
+    assert libssu.ssu_ssd_workspace_size(3, 4, 64, 128, 64, ctypes.byref(n)) == ssu.OK
+    up = lambda v: (v + 255) // 256 * 256
+    assert n.value == up(12 * 64 * 128 * 4) + 2 * up(12 * 64 * 4) + up(12 * 4)
+    assert libssu.ssu_ssd_workspace_size(3, 0, 64, 128, 64, ctypes.byref(n)) == ssu.ERR_INVALID
+    # no chunks: nothing to do, nothing launched, no pointer looked at
+    a = _ssd_args(nchunks=0, x=None, B=None, workspace=None)
+    assert libssu.ssu_ssd_prefill(ctypes.byref(a), None) == ssu.OK

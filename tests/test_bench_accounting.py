@@ -1,0 +1,33 @@
+"""bench.py's byte and flop accounting for the SSD prefill, against counts
+worked out by hand for a one-chunk problem (CPU only)."""
+import bench
+import workloads
+
+
+def test_ssd_accounting_one_chunk():
+    # 16 tokens, heads 2, dim 8, dstate 16, groups 1, chunk 16: one full chunk
+    w = workloads.ssd_problem(1, [16], heads=2, dim=8, dstate=16, groups=1, chunk_size=16)
+    a = bench.ssd_accounting(w)
+    x = 16 * 2 * 8 * 2            # bf16 x (z and y the same size)
+    dt = 16 * 2 * 4               # fp32 dt
+    bc = 2 * 16 * 1 * 16 * 2      # bf16 B and C
+    st = 1 * 2 * 8 * 16 * 4       # one fp32 state per sequence
+    meta = (2 + 1 + 1) * 4        # cu_chunk_seqlens, seq_idx, last_chunk_indices (int32)
+    assert a["inputs"] == 2 * x + dt + bc + st + meta
+    assert a["outputs"] == x + st
+    assert a["total"] == a["inputs"] + a["outputs"]
+    # per head: chunk state 2TPN, C . S_in^T 2TNP, and one 16 x 16 causal tile
+    # for C . B^T (2 * 256 * N) and M . X (2 * 256 * P)
+    assert a["flops"] == 2 * (2 * 16 * 8 * 16 + 2 * 16 * 16 * 8 + 2 * 256 * 16 + 2 * 256 * 8)
+    assert a["workspace"] == 4 * 1 * 2 * 8 * 16 * 4
+    assert a["tokens"] == 16
+
+
+def test_ssd_accounting_ragged_tiles():
+    # a 17-token chunk of a 32-token chunk size counts two 16-row tiles: 16 + 32 columns
+    w = workloads.ssd_problem(2, [17], heads=1, dim=8, dstate=16, groups=1, chunk_size=32, with_z=False,
+                              with_init=False)
+    a = bench.ssd_accounting(w)
+    causal = (16 + 32) * 16
+    assert a["flops"] == 2 * 17 * 8 * 16 * 2 + 2 * causal * 16 + 2 * causal * 8
+    assert a["outputs"] == 17 * 8 * 2 + 8 * 16 * 4
