@@ -532,13 +532,18 @@ def ssd_accounting(w) -> dict:
     lens = (w.cu_chunk_seqlens[1:] - w.cu_chunk_seqlens[:-1]).tolist()
     causal = sum(sum((t // 16 + 1) * 16 for t in range(0, L, 16)) * 16 for L in lens)  # (t, s) pairs, 16-row tiles
     flops = H * (2 * T * P * N + 2 * T * N * P + 2 * causal * N + 2 * causal * P)
+    # the chunk states cross the workspace four times (written, read and
+    # replaced by the entering states, read by the scan); the C . B^T tiles
+    # are written once per (chunk, group) and read by each head of the group
+    tiles = (w.chunk_size // 16) * (w.chunk_size // 16 + 1) // 2
+    cb = nchunks * G * tiles * 256 * 4
     return {"inputs": inputs, "outputs": outputs, "total": inputs + outputs, "flops": flops,
-            "workspace": 4 * ch * P * N * 4, "tokens": T}
+            "workspace": 4 * ch * P * N * 4 + cb * (1 + H // G), "tokens": T}
 
 
 def run_ssd(args, rank, world, device):
     """The SSD prefill workload: one step = one ssu_ssd_prefill call over the
-    packed batch (three kernel launches)."""
+    packed batch (four kernel launches)."""
     from selective_state_update_gb300 import build as ssu_build
     import selective_state_update_gb300 as ssu
     ssu_build.build()
@@ -607,7 +612,8 @@ def run_ssd(args, rank, world, device):
         "unit": SSD_UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                               + (f" (batch {args.batch})" if args.batch else ""),
                    "tokens_per_gpu": acct["tokens"], "chunks": int(w.seq_idx.numel()),
                    "parallelism": f"{world} independent replicas (one packed batch per GPU)",
                    "l2": "no flush: %.2f GB of inputs and outputs per step" % (acct["total"] / 1e9),
@@ -616,11 +622,11 @@ def run_ssd(args, rank, world, device):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("ssd", args.workload),
                      "algorithmic_bytes_per_launch": acct["total"],
-                     "kernel": "ssd prefill call (ssd_chunk_state + ssd_state_pass + ssd_chunk_scan)",
+                     "kernel": "ssd prefill call (ssd_chunk_state + ssd_state_pass + ssd_chunk_cb + ssd_chunk_scan)",
                      "launch_ms": call_ms},
         "e2e": {"value": aggregate_rate(acct["tokens"], world, e2e_steps, e2e_s * 1e3), "unit": SSD_UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -738,9 +744,9 @@ def make_workload(args, device, seed_offset=0):
     kw = {}
     if args.batch is not None:
         if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
-                                 "replay_f16copy_b256_fp32", "copy_slots_b256_fp32"):
-            raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32, replay_b256_fp32 and "
-                             "copy_slots_b256_fp32 workloads only")
+                                 "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16"):
+            raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32, replay_b256_fp32, "
+                             "copy_slots_b256_fp32 and ssd_prefill_16k_bf16 workloads only")
         kw["batch"] = args.batch
     w = gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
     if getattr(w, "shadow", None) is not None and str(device) != "cpu":

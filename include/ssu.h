@@ -307,11 +307,14 @@ typedef struct ssu_ssd_args {
     int32_t *d_status;             /* device int32 or NULL                                  */
 } ssu_ssd_args;
 
-/* Workspace ssu_ssd_prefill needs for these sizes (bytes, into *bytes). */
-ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t dim, int64_t dstate, int64_t chunk_size,
-                                  uint64_t *bytes);
+/* Workspace ssu_ssd_prefill needs for these sizes (bytes, into *bytes):
+ * the chunk states (fp32), per-chunk prefix sums, dt' and decays, and the
+ * causal C . B^T tiles of every (chunk, group) in fp32. */
+ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t groups, int64_t dim, int64_t dstate,
+                                  int64_t chunk_size, uint64_t *bytes);
 
-/* One packed SSD prefill call: three kernel launches on `stream`. */
+/* One packed SSD prefill call: four kernel launches on `stream` (at most
+ * 65535 chunks and 65535 heads per call). */
 ssu_status ssu_ssd_prefill(const ssu_ssd_args *args, void *stream);
 
 /*

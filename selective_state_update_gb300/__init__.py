@@ -142,7 +142,7 @@ def lib():
         L.ssu_batch_copy.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
                                      ctypes.c_void_p]
         L.ssu_batch_copy.restype = ctypes.c_int
-        L.ssu_ssd_workspace_size.argtypes = [ctypes.c_int64] * 5 + [ctypes.POINTER(ctypes.c_uint64)]
+        L.ssu_ssd_workspace_size.argtypes = [ctypes.c_int64] * 6 + [ctypes.POINTER(ctypes.c_uint64)]
         L.ssu_ssd_workspace_size.restype = ctypes.c_int
         L.ssu_ssd_prefill.argtypes = [ctypes.POINTER(SsdArgs), ctypes.c_void_p]
         L.ssu_ssd_prefill.restype = ctypes.c_int
@@ -415,7 +415,7 @@ def ssu_ssd_prefill(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, 
     if initial_states is not None and initial_states.dtype != sdt:
         initial_states = initial_states.to(sdt)
     nbytes = ctypes.c_uint64(0)
-    rc = lib().ssu_ssd_workspace_size(nchunks, heads, dim, dstate, chunk_size, ctypes.byref(nbytes))
+    rc = lib().ssu_ssd_workspace_size(nchunks, heads, groups, dim, dstate, chunk_size, ctypes.byref(nbytes))
     if rc != OK:
         _raise(rc)
     ws = _ssd_workspace(x.device, nbytes.value)

@@ -263,14 +263,33 @@ ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes,
     return launched(ssu::launch_copy(copies, n, max_bytes, d_status, static_cast<cudaStream_t>(stream)));
 }
 
-ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t dim, int64_t dstate, int64_t chunk_size,
-                                  uint64_t *bytes) {
-    if (!bytes) return fail(SSU_ERR_INVALID, "bytes is NULL");
-    if (nchunks < 0 || heads <= 0 || dim <= 0 || dstate <= 0 || chunk_size <= 0)
-        return fail(SSU_ERR_INVALID, "sizes must be positive (nchunks >= 0)");
-    const uint64_t ch = static_cast<uint64_t>(nchunks) * heads;
+// Workspace carve-up of the SSD prefill: chunk states, prefix sums, dt',
+// chunk decays, C . B^T tiles, their diagonals; each part 256-byte aligned.
+struct SsdWorkspace {
+    uint64_t state, acs, dtp, dec, cb, cbd, total;
+};
+static SsdWorkspace ssd_workspace(uint64_t nchunks, uint64_t heads, uint64_t groups, uint64_t dim, uint64_t dstate,
+                                  uint64_t chunk_size) {
     auto up = [](uint64_t v) { return (v + 255) / 256 * 256; };
-    *bytes = up(ch * dim * dstate * 4) + 2 * up(ch * chunk_size * 4) + up(ch * 4);
+    const uint64_t ch = nchunks * heads, cg = nchunks * groups;
+    const uint64_t tiles = (chunk_size / 16) * (chunk_size / 16 + 1) / 2;
+    SsdWorkspace w{};
+    w.state = 0;
+    w.acs = w.state + up(ch * dim * dstate * 4);
+    w.dtp = w.acs + up(ch * chunk_size * 4);
+    w.dec = w.dtp + up(ch * chunk_size * 4);
+    w.cb = w.dec + up(ch * 4);
+    w.cbd = w.cb + up(cg * tiles * 256 * 4);
+    w.total = w.cbd + up(cg * chunk_size * 4);
+    return w;
+}
+
+ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t groups, int64_t dim, int64_t dstate,
+                                  int64_t chunk_size, uint64_t *bytes) {
+    if (!bytes) return fail(SSU_ERR_INVALID, "bytes is NULL");
+    if (nchunks < 0 || heads <= 0 || groups <= 0 || dim <= 0 || dstate <= 0 || chunk_size <= 0)
+        return fail(SSU_ERR_INVALID, "sizes must be positive (nchunks >= 0)");
+    *bytes = ssd_workspace(nchunks, heads, groups, dim, dstate, chunk_size).total;
     return ok();
 }
 
@@ -290,15 +309,15 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *a, void *stream) {
         return fail(SSU_ERR_UNSUPPORTED, "chunk_size %lld is not supported (64, 128, 256)", (long long)a->chunk_size);
     if (!(a->dt_min <= a->dt_max)) return fail(SSU_ERR_INVALID, "dt_limit must satisfy min <= max");
     if (a->nchunks == 0 || a->tokens == 0) return ok();
-    if (a->nchunks > 65535 * 64 || a->heads > 65535) return fail(SSU_ERR_INVALID, "too many chunks or heads");
+    if (a->nchunks > 65535 || a->heads > 65535) return fail(SSU_ERR_INVALID, "more than 65535 chunks or heads");
     if (!a->x || !a->dt || !a->B || !a->C || !a->A || !a->cu_chunk_seqlens || !a->seq_idx || !a->y || !a->states ||
         (!a->return_intermediate && !a->last_chunk_indices) || !a->workspace)
         return fail(SSU_ERR_INVALID, "a required pointer is NULL");
     const void *aligned[] = {a->x, a->B, a->C, a->y, a->states, a->workspace, a->z, a->initial_states};
     for (const void *q : aligned)
         if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return fail(SSU_ERR_INVALID, "tensors must be 16-byte aligned");
-    uint64_t need = 0;
-    ssu_ssd_workspace_size(a->nchunks, a->heads, a->dim, a->dstate, a->chunk_size, &need);
+    const SsdWorkspace wl = ssd_workspace(a->nchunks, a->heads, a->groups, a->dim, a->dstate, a->chunk_size);
+    const uint64_t need = wl.total;
     if (a->workspace_bytes < need)
         return fail(SSU_ERR_INVALID, "workspace of %lld bytes is smaller than the %lld needed",
                     (long long)a->workspace_bytes, (long long)need);
@@ -327,16 +346,13 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *a, void *stream) {
     p.states = a->states;
     p.status = a->d_status;
     {
-        const uint64_t ch = static_cast<uint64_t>(a->nchunks) * a->heads;
-        auto up = [](uint64_t v) { return (v + 255) / 256 * 256; };
         unsigned char *w = static_cast<unsigned char *>(a->workspace);
-        p.ws_state = reinterpret_cast<float *>(w);
-        w += up(ch * a->dim * a->dstate * 4);
-        p.ws_acs = reinterpret_cast<float *>(w);
-        w += up(ch * a->chunk_size * 4);
-        p.ws_dtp = reinterpret_cast<float *>(w);
-        w += up(ch * a->chunk_size * 4);
-        p.ws_dec = reinterpret_cast<float *>(w);
+        p.ws_state = reinterpret_cast<float *>(w + wl.state);
+        p.ws_acs = reinterpret_cast<float *>(w + wl.acs);
+        p.ws_dtp = reinterpret_cast<float *>(w + wl.dtp);
+        p.ws_dec = reinterpret_cast<float *>(w + wl.dec);
+        p.ws_cb = reinterpret_cast<float *>(w + wl.cb);
+        p.ws_cbd = reinterpret_cast<float *>(w + wl.cbd);
     }
     return launched(ssu::launch_ssd(p, static_cast<cudaStream_t>(stream)));
 }

@@ -98,6 +98,8 @@ struct SsdParams {
     float *ws_state;                 // [nchunks, H, P, N]
     float *ws_acs, *ws_dtp;          // [nchunks, H, Q]
     float *ws_dec;                   // [nchunks, H]
+    float *ws_cb;                    // [nchunks, G, causal 16 x 16 tiles of Q, 256] (fragment order)
+    float *ws_cbd;                   // [nchunks, G, Q]
     int32_t *status;
 };
 cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream);

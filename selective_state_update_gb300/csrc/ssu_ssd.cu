@@ -15,20 +15,29 @@
 // silu(z).  A chunk opens a sequence when seq_idx changes (the page: seq_idx
 // is the authority); its S_in is then the initial state (or zero).
 //
-// Three kernels over a caller-owned workspace:
-//   chunk_state  one CTA per (chunk, head): dt', the cumulative sums, and
-//                Sc as a tensor-core product (mma.sync bf16, fp32
-//                accumulation) of the decay-weighted x -- split into a bf16
-//                high and low part so the state keeps ~2^-17 relative
-//                precision -- with B; Sc goes to the workspace;
-//   state_pass   one CTA per (sequence run, head): walks the run's chunks,
-//                replaces each Sc in the workspace by the chunk's entering
-//                state and writes the states the call returns;
-//   chunk_scan   one CTA per (chunk, head, 64-token block): y from the
-//                entering state (C . S_in^T) and the causal C . B^T products
-//                times the decays and dt' x, on the tensor cores (bf16
-//                operands, fp32 accumulation; the entering state and the
-//                decayed C . B^T weights as bf16 high + low parts).
+// Four kernels over a caller-owned workspace; every contraction runs on the
+// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation), with
+// operands staged in shared memory in the inputs' own row layout by 16-byte
+// cp.async and read as fragments with ldmatrix:
+//   chunk_state  one CTA per (head, chunk): dt', the prefix and suffix sums
+//                of a, and Sc = (w x)^T B with w_t = exp(sum_{s>t} a) dt'_t;
+//                w x is split into a bf16 high and low part so that Sc keeps
+//                ~2^-17 relative precision (the returned states need it);
+//   state_pass   one CTA per (run of a sequence's chunks, head): replaces
+//                each Sc in the workspace by the chunk's entering state and
+//                writes the returned states;
+//   chunk_cb     one CTA per (group, chunk): the causal 16 x 16 tiles of
+//                C . B^T in fp32, stored in mma fragment order so that the
+//                heads of the group read them back with coalesced loads, and
+//                the diagonal C_t . B_t on its own;
+//   chunk_scan   one CTA per (head, chunk): y from the entering state
+//                (C . S_in^T scaled by exp(cs_t)) and from the strictly causal
+//                weights (C . B^T) exp(cs_t - cs_s) dt'_s times x, the state
+//                and the weights as bf16 high + low parts (one-part bf16
+//                operands measured errors of up to 2.4 % of a token's row);
+//                the diagonal weight (C_t . B_t) dt'_t and D are applied in
+//                fp32, since the two can cancel for every dim row of a token
+//                (both multiply x_t).
 #include <cstdint>
 
 #include "ssu_device.cuh"
@@ -36,11 +45,10 @@
 namespace ssu {
 
 // ---------------------------------------------------------------------------
-// Tensor-core helpers: m16n8k16, A row-major (16 x 16), B column-major
-// (16 x 8), fp32 accumulators.  Fragment of lane l (g = l / 4, q = l % 4):
-// A regs {A[g][2q..2q+1]}, {A[g+8][2q..]}, {A[g][2q+8..]}, {A[g+8][2q+8..]};
-// B regs {B[2q..2q+1][g]}, {B[2q+8..2q+9][g]}; D {D[g][2q..2q+1]},
-// {D[g+8][2q..2q+1]}.
+// Tensor-core and staging helpers.  mma m16n8k16: A row-major (16 x 16), B
+// "column-major" (16 x 8), fp32 accumulators.  Fragment of lane l (g = l/4,
+// q = l%4): A {A[g][2q..2q+1]}, {A[g+8][2q..]}, {A[g][2q+8..]}, {A[g+8][2q+8..]};
+// B {B[2q..2q+1][g]}, {B[2q+8..2q+9][g]}; D {D[g][2q..2q+1]}, {D[g+8][2q..2q+1]}.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mma_bf16(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -48,6 +56,33 @@ __device__ __forceinline__ void mma_bf16(float *d, const uint32_t *a, uint32_t b
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 b16 matrices from shared memory; lanes 8i..8i+7 give the row
+// addresses of matrix i.  Lane l receives (row l/4, columns 2(l%4), 2(l%4)+1)
+// of each matrix, or with .trans (rows 2(l%4), 2(l%4)+1, column l/4).
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, const void *smem_row) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem_row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t *r, const void *smem_row) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem_row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
+// 16 bytes global -> shared, asynchronously; `valid` false fills zeros and
+// reads nothing.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(a), "l"(gmem), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
 // Two floats as bf16x2 (x0 in the low half), round to nearest even.
@@ -68,6 +103,17 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 
 __device__ __forceinline__ int64_t meta_at(const void *p, int64_t i, int is_i64) { return load_index(p, i, is_i64); }
 
+// The causal 16 x 16 tiles (row tile m, column tile j <= m) of a chunk of Q
+// tokens, numbered row tile by row tile.
+__host__ __device__ constexpr int cb_tiles(int Q) { return (Q / 16) * (Q / 16 + 1) / 2; }
+__device__ __forceinline__ int cb_tile(int m, int j) { return m * (m + 1) / 2 + j; }
+
+// Index of (chunk c, head h) in the per-(chunk, head) workspace arrays:
+// head-major, so that the chunks of one sequence and head are neighbours.
+__device__ __forceinline__ int64_t ws_unit(const SsdParams &p, int64_t c, int h) {
+    return static_cast<int64_t>(h) * p.nchunks + c;
+}
+
 // dt' of token t, head h: dt (+ bias), softplus, clamped to [lo, hi].
 __device__ __forceinline__ float ssd_step(const SsdParams &p, int64_t t, int h) {
     const int64_t i = t * p.H + h;
@@ -77,15 +123,13 @@ __device__ __forceinline__ float ssd_step(const SsdParams &p, int64_t t, int h) 
     return fminf(fmaxf(v, p.dt_lo), p.dt_hi);
 }
 
-// Inclusive prefix sums of v[0..n) in shared memory by a 128-thread block
-// (n <= 256), in place; `tmp` holds 8 floats.
-__device__ void block_scan_256(float *v, int n, float *tmp) {
+// Inclusive prefix sums of v[0..n) in shared memory, one value per thread of
+// a block of kThreads >= n threads, in place; `tmp` holds kThreads/32 floats.
+template <int kThreads>
+__device__ void block_scan(float *v, int n, float *tmp) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // each thread two consecutive values
-    float a = 2 * tid < n ? v[2 * tid] : 0.f;
-    float b = 2 * tid + 1 < n ? v[2 * tid + 1] : 0.f;
-    b += a;
-    float s = b;
+    const float a = tid < n ? v[tid] : 0.f;
+    float s = a;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float o = __shfl_up_sync(0xffffffffu, s, off);
@@ -95,38 +139,50 @@ __device__ void block_scan_256(float *v, int n, float *tmp) {
     __syncthreads();
     float base = 0.f;
     for (int w = 0; w < warp; ++w) base += tmp[w];
-    const float excl = base + s - b;  // sum of everything before this thread's pair
-    if (2 * tid < n) v[2 * tid] = excl + a;
-    if (2 * tid + 1 < n) v[2 * tid + 1] = excl + b;
+    if (tid < n) v[tid] = base + s;
     __syncthreads();
 }
 
+// Rows [0, Q) of a bf16 tensor with row stride `stride` starting at row t0,
+// `cols` columns from column c0, into shared-memory rows of `ld` elements;
+// rows from L on are zero.  One 16-byte cp.async per 8 columns.
+template <int kThreads>
+__device__ __forceinline__ void stage_rows(__nv_bfloat16 *dst, int ld, const __nv_bfloat16 *src, int64_t t0,
+                                           int64_t stride, int64_t c0, int Q, int L, int cols) {
+    const int per_row = cols / 8;
+    for (int i = threadIdx.x; i < Q * per_row; i += kThreads) {
+        const int r = i / per_row, k = (i % per_row) * 8;
+        const bool ok = r < L;
+        const __nv_bfloat16 *s = ok ? src + (t0 + r) * stride + c0 + k : src;
+        cp_async16(dst + r * ld + k, s, ok);
+    }
+}
+
 // ---------------------------------------------------------------------------
-// Stage 1-2: per (chunk, head) the cumulative sums and the chunk's own state.
+// Stages 1-2: per (head, chunk) the cumulative sums and the chunk's own state.
 // ---------------------------------------------------------------------------
 template <int Q, int P, int N>
 struct ChunkStateSmem {
-    static constexpr int kPad = 8;  // bf16 elements of padding per transposed row
-    static constexpr int kT = Q + kPad;
-    __nv_bfloat16 xt[P][kT];  // x of the chunk, transposed: xt[p][t]
-    __nv_bfloat16 bt[N][kT];  // B of the chunk's group, transposed: bt[n][t]
-    float a[Q];               // A dt'
-    float cs[Q];              // inclusive cumulative sums of a
-    float rs[Q];              // inclusive cumulative sums of a reversed
-    float w[Q];               // dt', then exp(sum of the later a) dt'
+    __nv_bfloat16 xs[Q][P + 8];  // x of the chunk, xs[t][p]
+    __nv_bfloat16 bs[Q][N + 8];  // B of the chunk's group, bs[t][n]
+    float cs[Q];                 // inclusive cumulative sums of a
+    float rs[Q];                 // inclusive cumulative sums of a, reversed
+    float w[Q];                  // dt', then exp(sum of the later a) dt'
     float tmp[8];
 };
 
+constexpr int kStateThreads = 256;
+
 template <int Q, int P, int N>
-__global__ void __launch_bounds__(128) ssd_chunk_state_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const SsdParams p) {
+    static_assert(P == 64 && N % 64 == 0 && Q <= kStateThreads, "tiling");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<ChunkStateSmem<Q, P, N> *>(smem_raw);
-    const int c = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
     const int g = h / p.hpg;
     const int64_t t0 = meta_at(p.cu_chunk, c, p.meta_i64), t1 = meta_at(p.cu_chunk, c + 1, p.meta_i64);
-    const int L = static_cast<int>(t1 - t0);
     if (c == 0 && h == 0 && !p.intermediate) {  // every sequence's last chunk must name a chunk
-        for (int64_t s = tid; s < p.nseq; s += 128) {
+        for (int64_t s = tid; s < p.nseq; s += kStateThreads) {
             const int64_t lc = meta_at(p.last_chunk, s, p.meta_i64);
             if (lc < 0 || lc >= p.nchunks) flag(p.status, kDevBadEntry);
         }
@@ -135,79 +191,73 @@ __global__ void __launch_bounds__(128) ssd_chunk_state_kernel(const SsdParams p)
         if (tid == 0) flag(p.status, kDevBadSeqlen);
         return;
     }
-    float *ws_acs = p.ws_acs + (static_cast<int64_t>(c) * p.H + h) * Q;
-    float *ws_dtp = p.ws_dtp + (static_cast<int64_t>(c) * p.H + h) * Q;
-    // dt', a = A dt'
+    const int L = static_cast<int>(t1 - t0);
+    // the chunk's x and B rows, in flight while the decays are formed
+    stage_rows<kStateThreads>(&sm.xs[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.x), t0,
+                              static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
+    stage_rows<kStateThreads>(&sm.bs[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.B), t0,
+                              static_cast<int64_t>(p.G) * N, static_cast<int64_t>(g) * N, Q, L, N);
+    float *ws_acs = p.ws_acs + ws_unit(p, c, h) * Q;
+    float *ws_dtp = p.ws_dtp + ws_unit(p, c, h) * Q;
     const float Ah = p.A[h];
-    for (int t = tid; t < Q; t += 128) {
-        const float d = t < L ? ssd_step(p, t0 + t, h) : 0.f;
-        ws_dtp[t] = d;
-        sm.w[t] = d;
-        sm.a[t] = t < L ? Ah * d : 0.f;
-        sm.cs[t] = sm.a[t];
+    if (tid < Q) {
+        const float d = tid < L ? ssd_step(p, t0 + tid, h) : 0.f;
+        ws_dtp[tid] = d;
+        sm.w[tid] = d;
+        sm.cs[tid] = tid < L ? Ah * d : 0.f;
+        sm.rs[tid] = 0.f;
     }
     __syncthreads();
-    for (int t = tid; t < Q; t += 128) sm.rs[t] = t < L ? sm.a[L - 1 - t] : 0.f;  // a reversed
+    if (tid < L) sm.rs[tid] = sm.cs[L - 1 - tid];  // a reversed
     __syncthreads();
-    block_scan_256(sm.cs, Q, sm.tmp);
+    block_scan<kStateThreads>(sm.cs, Q, sm.tmp);
     // rs[i] = sum of a over the last i + 1 tokens, summed from the end so the
-    // decays of recent tokens carry no cancellation
-    block_scan_256(sm.rs, Q, sm.tmp);
-    for (int t = tid; t < Q; t += 128) {
-        ws_acs[t] = sm.cs[t];
-        const float later = t + 1 < L ? sm.rs[L - 2 - t] : 0.f;  // sum_{s>t} a_s
-        sm.w[t] = t < L ? expf(later) * sm.w[t] : 0.f;
+    // weights of recent tokens carry no cancellation
+    block_scan<kStateThreads>(sm.rs, Q, sm.tmp);
+    if (tid < Q) {
+        ws_acs[tid] = sm.cs[tid];
+        const float later = tid + 1 < L ? sm.rs[L - 2 - tid] : 0.f;  // sum_{s>t} a_s
+        sm.w[tid] = tid < L ? expf(later) * sm.w[tid] : 0.f;
     }
-    if (tid == 0) p.ws_dec[static_cast<int64_t>(c) * p.H + h] = L > 0 ? expf(sm.rs[L - 1]) : 1.f;
-    // x (transposed) and B (transposed) of the chunk, zero beyond L
-    for (int i = tid; i < Q * (P / 8); i += 128) {
-        const int t = i / (P / 8), p8 = (i % (P / 8)) * 8;
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (t < L) u = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.x) +
-                                                         ((t0 + t) * p.H + h) * static_cast<int64_t>(P) + p8);
-        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&u);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sm.xt[p8 + k][t] = e[k];
-    }
-    for (int i = tid; i < Q * (N / 8); i += 128) {
-        const int t = i / (N / 8), n8 = (i % (N / 8)) * 8;
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (t < L) u = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.B) +
-                                                         ((t0 + t) * p.G + g) * static_cast<int64_t>(N) + n8);
-        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&u);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sm.bt[n8 + k][t] = e[k];
-    }
+    if (tid == 0) p.ws_dec[ws_unit(p, c, h)] = L > 0 ? expf(sm.rs[L - 1]) : 1.f;
+    cp_async_wait_all();
     __syncthreads();
-    // Sc[p][n] = sum_t (w_t x[t][p]) B[t][n]: M = P rows, N columns, K = t.
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3;
-    for (int pb = warp * 16; pb < P; pb += 64) {
-        float acc[N / 8][4];
+
+    // Sc[p][n] = sum_t (w_t x[t][p]) B[t][n]: M = P, N, K = t.  Warp w: rows
+    // p0 = 16 (w % 4), columns from n0 = (N / 2)(w / 4).
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
+    const int p0 = (warp & 3) * 16, n0 = (warp >> 2) * (N / 2);
+    constexpr int NT = N / 16;  // n-tiles of 8 per warp
+    float acc[NT][4];
 #pragma unroll
-        for (int j = 0; j < N / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        for (int k0 = 0; k0 < L; k0 += 16) {
-            uint32_t ahi[4], alo[4];
-            const int r0 = pb + gq, r1 = pb + gq + 8, c0 = k0 + 2 * q, c1 = k0 + 2 * q + 8;
-            const float w00 = sm.w[c0], w01 = sm.w[c0 + 1], w10 = sm.w[c1], w11 = sm.w[c1 + 1];
-            split_bf16(__bfloat162float(sm.xt[r0][c0]) * w00, __bfloat162float(sm.xt[r0][c0 + 1]) * w01, &ahi[0], &alo[0]);
-            split_bf16(__bfloat162float(sm.xt[r1][c0]) * w00, __bfloat162float(sm.xt[r1][c0 + 1]) * w01, &ahi[1], &alo[1]);
-            split_bf16(__bfloat162float(sm.xt[r0][c1]) * w10, __bfloat162float(sm.xt[r0][c1 + 1]) * w11, &ahi[2], &alo[2]);
-            split_bf16(__bfloat162float(sm.xt[r1][c1]) * w10, __bfloat162float(sm.xt[r1][c1 + 1]) * w11, &ahi[3], &alo[3]);
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    for (int k0 = 0; k0 < L; k0 += 16) {
+        // A = (w x)^T: matrices (p 0-7 | 8-15) x (t 0-7 | 8-15) of xs, transposed
+        uint32_t ax[4], ahi[4], alo[4];
+        ldsm_x4_trans(ax, &sm.xs[k0 + (lane & 7) + (mi >> 1) * 8][p0 + (mi & 1) * 8]);
+        const float w0 = sm.w[k0 + 2 * q], w1 = sm.w[k0 + 2 * q + 1];
+        const float w8 = sm.w[k0 + 2 * q + 8], w9 = sm.w[k0 + 2 * q + 9];
+        split_bf16(bf16_lo(ax[0]) * w0, bf16_hi(ax[0]) * w1, &ahi[0], &alo[0]);
+        split_bf16(bf16_lo(ax[1]) * w0, bf16_hi(ax[1]) * w1, &ahi[1], &alo[1]);
+        split_bf16(bf16_lo(ax[2]) * w8, bf16_hi(ax[2]) * w9, &ahi[2], &alo[2]);
+        split_bf16(bf16_lo(ax[3]) * w8, bf16_hi(ax[3]) * w9, &ahi[3], &alo[3]);
 #pragma unroll
-            for (int j = 0; j < N / 8; ++j) {
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&sm.bt[8 * j + gq][c0]);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&sm.bt[8 * j + gq][c1]);
-                mma_bf16(acc[j], ahi, b0, b1);
-                mma_bf16(acc[j], alo, b0, b1);
-            }
+        for (int j = 0; j < NT; j += 2) {
+            // B[t][n]: matrices (t 0-7 | 8-15) x (n-tile j | j+1), transposed
+            uint32_t b[4];
+            ldsm_x4_trans(b, &sm.bs[k0 + (lane & 7) + (mi & 1) * 8][n0 + 8 * j + (mi >> 1) * 8]);
+            mma_bf16(acc[j], ahi, b[0], b[1]);
+            mma_bf16(acc[j], alo, b[0], b[1]);
+            mma_bf16(acc[j + 1], ahi, b[2], b[3]);
+            mma_bf16(acc[j + 1], alo, b[2], b[3]);
         }
-        float *out = p.ws_state + ((static_cast<int64_t>(c) * p.H + h) * P) * N;
+    }
+    float *out = p.ws_state + ws_unit(p, c, h) * P * N;
 #pragma unroll
-        for (int j = 0; j < N / 8; ++j) {
-            const int n = 8 * j + 2 * q;
-            *reinterpret_cast<float2 *>(out + (pb + gq) * N + n) = make_float2(acc[j][0], acc[j][1]);
-            *reinterpret_cast<float2 *>(out + (pb + gq + 8) * N + n) = make_float2(acc[j][2], acc[j][3]);
-        }
+    for (int j = 0; j < NT; ++j) {
+        const int n = n0 + 8 * j + 2 * q;
+        *reinterpret_cast<float2 *>(out + (p0 + gq) * N + n) = make_float2(acc[j][0], acc[j][1]);
+        *reinterpret_cast<float2 *>(out + (p0 + gq + 8) * N + n) = make_float2(acc[j][2], acc[j][3]);
     }
 }
 
@@ -233,8 +283,17 @@ __device__ __forceinline__ float4 load_state4(const void *base, int64_t i) {
     }
 }
 
+constexpr int kPassThreads = 256;
+constexpr int kPassList = 256;  // returned states a run keeps in its list
+
+// One CTA per (chunk c0, head); only a chunk that opens a run of its
+// sequence's chunks works: it walks the run, the next chunk's Sc loaded
+// while the current one is replaced.
 template <int P, int N, typename TS>
-__global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdParams p) {
+    __shared__ int nlist;
+    __shared__ int64_t list_chunk[kPassList];
+    __shared__ int64_t list_seq[kPassList];
     const int c0 = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
     const int64_t b = meta_at(p.seq_idx, c0, p.meta_i64);
     if (c0 > 0 && meta_at(p.seq_idx, c0 - 1, p.meta_i64) == b) return;  // not the first chunk of a run
@@ -242,211 +301,297 @@ __global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdParams p) 
         if (tid == 0) flag(p.status, kDevBadEntry);
         return;
     }
-    constexpr int kPer = P * N / (256 * 4);  // float4 per thread
-    float4 S[kPer];
+    // the sequences whose returned state is the end of a chunk of this
+    // sequence from c0 on (chunks past the run's end are never reached)
+    if (tid == 0) nlist = 0;
+    __syncthreads();
+    if (!p.intermediate) {
+        for (int64_t s = tid; s < p.nseq; s += kPassThreads) {
+            const int64_t lc = meta_at(p.last_chunk, s, p.meta_i64);
+            if (lc >= c0 && lc < p.nchunks && meta_at(p.seq_idx, lc, p.meta_i64) == b) {
+                const int k = atomicAdd(&nlist, 1);
+                if (k < kPassList) list_chunk[k] = lc, list_seq[k] = s;
+            }
+        }
+    }
+    __syncthreads();
+    const bool overflow = nlist > kPassList;
+    const int nl = nlist < kPassList ? nlist : kPassList;
+
+    constexpr int kPer = P * N / (kPassThreads * 4);  // float4 per thread
+    const int64_t PN = static_cast<int64_t>(P) * N;
+    const int64_t hs = static_cast<int64_t>(h) * PN;
+    float *ws0 = p.ws_state + ws_unit(p, 0, h) * PN;  // this head's chunks, contiguous
+    float4 S[kPer], sc[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const int64_t e = (static_cast<int64_t>(k) * 256 + tid) * 4;
-        S[k] = p.init ? load_state4<TS>(p.init, ((b * p.H + h) * P) * static_cast<int64_t>(N) + e)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t e = (static_cast<int64_t>(k) * kPassThreads + tid) * 4;
+        S[k] = p.init ? load_state4<TS>(p.init, b * p.H * PN + hs + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        sc[k] = __ldcs(reinterpret_cast<const float4 *>(ws0 + c0 * PN + e));
     }
-    for (int c = c0; c < p.nchunks; ++c) {
-        if (c > c0 && meta_at(p.seq_idx, c, p.meta_i64) != b) break;
-        float *ws = p.ws_state + ((static_cast<int64_t>(c) * p.H + h) * P) * N;
-        const float dec = p.ws_dec[static_cast<int64_t>(c) * p.H + h];
-        float4 sc[kPer];
+    for (int64_t c = c0;; ++c) {
+        float *ws = ws0 + c * PN;
+        const float dec = p.ws_dec[ws_unit(p, c, h)];
+        const bool more = c + 1 < p.nchunks && meta_at(p.seq_idx, c + 1, p.meta_i64) == b;
+        float4 nx[kPer];
+        if (c + 1 < p.nchunks) {  // the next chunk's Sc (read one chunk ahead, also past the run's end)
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) sc[k] = *reinterpret_cast<const float4 *>(ws + (k * 256 + tid) * 4);
+            for (int k = 0; k < kPer; ++k) nx[k] = __ldcs(reinterpret_cast<const float4 *>(ws + PN + (k * kPassThreads + tid) * 4));
+        }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            *reinterpret_cast<float4 *>(ws + (k * 256 + tid) * 4) = S[k];  // the state entering chunk c
+            *reinterpret_cast<float4 *>(ws + (k * kPassThreads + tid) * 4) = S[k];  // the state entering chunk c
             S[k] = make_float4(fmaf(dec, S[k].x, sc[k].x), fmaf(dec, S[k].y, sc[k].y), fmaf(dec, S[k].z, sc[k].z),
                                fmaf(dec, S[k].w, sc[k].w));
         }
         if (p.intermediate) {
 #pragma unroll
             for (int k = 0; k < kPer; ++k)
-                store_state4(static_cast<TS *>(p.states) + ((static_cast<int64_t>(c) * p.H + h) * P) * N +
-                                 (k * 256 + tid) * 4, S[k]);
+                store_state4(static_cast<TS *>(p.states) + c * p.H * PN + hs + (k * kPassThreads + tid) * 4, S[k]);
         } else {
-            for (int64_t s = 0; s < p.nseq; ++s) {
-                if (meta_at(p.last_chunk, s, p.meta_i64) != c) continue;
+            for (int i = 0; i < nl; ++i) {
+                if (list_chunk[i] != c) continue;
 #pragma unroll
                 for (int k = 0; k < kPer; ++k)
-                    store_state4(static_cast<TS *>(p.states) + ((s * p.H + h) * P) * static_cast<int64_t>(N) +
-                                     (k * 256 + tid) * 4, S[k]);
+                    store_state4(static_cast<TS *>(p.states) + list_seq[i] * p.H * PN + hs +
+                                     (k * kPassThreads + tid) * 4,
+                                 S[k]);
             }
+            if (overflow) {  // more such sequences than the list holds: find the rest
+                for (int64_t s = 0; s < p.nseq; ++s) {
+                    if (meta_at(p.last_chunk, s, p.meta_i64) != c) continue;
+                    bool listed = false;
+                    for (int i = 0; i < nl; ++i) listed |= list_seq[i] == s;
+                    if (listed) continue;
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k)
+                        store_state4(static_cast<TS *>(p.states) + s * p.H * PN + hs + (k * kPassThreads + tid) * 4,
+                                     S[k]);
+                }
+            }
+        }
+        if (!more) break;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) sc[k] = nx[k];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 4: C . B^T per (group, chunk), causal 16 x 16 tiles in fragment order.
+// ---------------------------------------------------------------------------
+template <int Q, int N>
+struct ChunkCbSmem {
+    __nv_bfloat16 cm[Q][N + 8];  // C rows, cm[t][n]
+    __nv_bfloat16 bm[Q][N + 8];  // B rows, bm[s][n]
+};
+
+constexpr int kCbThreads = 256;
+
+template <int Q, int N>
+__global__ void __launch_bounds__(kCbThreads) ssd_chunk_cb_kernel(const SsdParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    auto &sm = *reinterpret_cast<ChunkCbSmem<Q, N> *>(smem_raw);
+    const int g = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
+    const int64_t t0 = meta_at(p.cu_chunk, c, p.meta_i64), t1 = meta_at(p.cu_chunk, c + 1, p.meta_i64);
+    if (t0 < 0 || t1 < t0 || t1 - t0 > Q || t1 > p.tokens) return;  // flagged by chunk_state
+    const int L = static_cast<int>(t1 - t0);
+    const int64_t gs = static_cast<int64_t>(p.G) * N, g0 = static_cast<int64_t>(g) * N;
+    stage_rows<kCbThreads>(&sm.cm[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.C), t0, gs, g0, Q, L, N);
+    stage_rows<kCbThreads>(&sm.bm[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.B), t0, gs, g0, Q, L, N);
+    cp_async_wait_all();
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
+    const int mt_end = (L + 15) / 16;  // row tiles holding tokens
+    float *cb = p.ws_cb + (static_cast<int64_t>(c) * p.G + g) * cb_tiles(Q) * 256;
+    float *cbd = p.ws_cbd + (static_cast<int64_t>(c) * p.G + g) * Q;
+    for (int tile = warp; tile < mt_end * (mt_end + 1) / 2; tile += kCbThreads / 32) {
+        int m = 0;
+        while ((m + 1) * (m + 2) / 2 <= tile) ++m;
+        const int j = tile - m * (m + 1) / 2;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int k0 = 0; k0 < N; k0 += 16) {
+            uint32_t a[4], b[4];
+            // C: matrices (t 0-7 | 8-15) x (n 0-7 | 8-15) of cm
+            ldsm_x4(a, &sm.cm[16 * m + (lane & 7) + (mi & 1) * 8][k0 + (mi >> 1) * 8]);
+            // B[k = n][col = s] = bm[s][n]: matrices (n 0-7 | 8-15) x (s 0-7 | 8-15)
+            ldsm_x4(b, &sm.bm[16 * j + (lane & 7) + (mi >> 1) * 8][k0 + (mi & 1) * 8]);
+            mma_bf16(acc[0], a, b[0], b[1]);
+            mma_bf16(acc[1], a, b[2], b[3]);
+        }
+        float4 *o = reinterpret_cast<float4 *>(cb + static_cast<int64_t>(tile) * 256 + lane * 8);
+        o[0] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        o[1] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+        if (j == m) {  // the diagonal: (row gq, col 2q + e) of columns 0-7, (row gq + 8, col 8 + 2q + e) of 8-15
+            if (gq == 2 * q) cbd[16 * m + gq] = acc[0][0], cbd[16 * m + gq + 8] = acc[1][2];
+            if (gq == 2 * q + 1) cbd[16 * m + gq] = acc[0][1], cbd[16 * m + gq + 8] = acc[1][3];
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// Stages 4-5: the chunk scan, one CTA per (chunk, head, 64-token block).
+// Stage 5: the chunk scan, one CTA per (head, chunk).
 // ---------------------------------------------------------------------------
 template <int Q, int P, int N>
 struct ChunkScanSmem {
-    static constexpr int kPadN = 8, kPadT = 8;
-    __nv_bfloat16 cm[64][N + kPadN];  // C of the block's tokens, cm[t][n]
-    __nv_bfloat16 bm[Q][N + kPadN];   // B of the chunk's tokens up to the block's end, bm[s][n]
-    __nv_bfloat16 xt[P][Q + kPadT];   // x transposed, xt[p][s]
-    __nv_bfloat16 sin[P][N + kPadN];  // entering state, bf16 high part, sin[p][n]
-    __nv_bfloat16 slo[P][N + kPadN];  // and the bf16 low part of what is left
-    float cs[Q], dtp[Q];
+    __nv_bfloat16 xs[Q][P + 8];  // x rows, xs[s][p]
+    __nv_bfloat16 zy[Q][P + 8];  // z rows, replaced row by row by y before its store
+    __nv_bfloat16 ss[P][N + 8];  // entering state, bf16 high part, ss[p][n]
+    __nv_bfloat16 sl[P][N + 8];  // and the bf16 low part of what is left
+    float cs[Q];                 // inclusive cumulative sums of a, times log2(e)
+    float dtp[Q];                // dt'
+    float cbd[Q];                // C_t . B_t
 };
 
 template <int Q, int P, int N>
-__global__ void __launch_bounds__(128) ssd_chunk_scan_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p) {
+    static_assert(P == 64 && Q % 64 == 0, "tiling");
+    constexpr int kThreads = Q;  // Q / 32 warps, each the row tiles m and Q/16 - 1 - m
     extern __shared__ __align__(16) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<ChunkScanSmem<Q, P, N> *>(smem_raw);
-    const int c = blockIdx.x, h = blockIdx.y, blk = blockIdx.z, tid = threadIdx.x;
+    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
     const int g = h / p.hpg;
     const int64_t t0 = meta_at(p.cu_chunk, c, p.meta_i64), t1 = meta_at(p.cu_chunk, c + 1, p.meta_i64);
     if (t0 < 0 || t1 < t0 || t1 - t0 > Q || t1 > p.tokens) return;  // flagged by chunk_state
     const int L = static_cast<int>(t1 - t0);
-    const int tb0 = blk * 64;
-    if (tb0 >= L) return;
-    const int send = min(L, tb0 + 64);  // tokens s < send can reach this block
-    const float *wcs = p.ws_acs + (static_cast<int64_t>(c) * p.H + h) * Q;
-    const float *wdt = p.ws_dtp + (static_cast<int64_t>(c) * p.H + h) * Q;
-    for (int t = tid; t < Q; t += 128) {
-        sm.cs[t] = wcs[t];
-        sm.dtp[t] = wdt[t];
-    }
-    for (int i = tid; i < 64 * (N / 8); i += 128) {
-        const int t = i / (N / 8), n8 = (i % (N / 8)) * 8;
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (tb0 + t < L)
-            u = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.C) +
-                                                 ((t0 + tb0 + t) * p.G + g) * static_cast<int64_t>(N) + n8);
-        *reinterpret_cast<uint4 *>(&sm.cm[t][n8]) = u;
-    }
-    for (int i = tid; i < send * (N / 8); i += 128) {
-        const int s = i / (N / 8), n8 = (i % (N / 8)) * 8;
-        *reinterpret_cast<uint4 *>(&sm.bm[s][n8]) = *reinterpret_cast<const uint4 *>(
-            static_cast<const __nv_bfloat16 *>(p.B) + ((t0 + s) * p.G + g) * static_cast<int64_t>(N) + n8);
-    }
-    for (int i = tid; i < Q * (P / 8); i += 128) {
-        const int s = i / (P / 8), p8 = (i % (P / 8)) * 8;
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (s < send)
-            u = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.x) +
-                                                 ((t0 + s) * p.H + h) * static_cast<int64_t>(P) + p8);
-        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&u);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sm.xt[p8 + k][s] = e[k];
-    }
+    if (L == 0) return;
+    stage_rows<kThreads>(&sm.xs[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.x), t0,
+                         static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
+    if (p.z)
+        stage_rows<kThreads>(&sm.zy[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.z), t0,
+                             static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
     {
-        const float *ws = p.ws_state + ((static_cast<int64_t>(c) * p.H + h) * P) * N;
-        for (int i = tid; i < P * N / 4; i += 128) {
-            const float4 v = *reinterpret_cast<const float4 *>(ws + i * 4);
-            const int pp = (i * 4) / N, n = (i * 4) % N;
+        const int64_t ch = ws_unit(p, c, h);
+        const float4 *ws = reinterpret_cast<const float4 *>(p.ws_state + ch * P * N);
+        constexpr int kPer = P * N / 4 / kThreads;  // float4 of the entering state per thread
+        float4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) v[k] = __ldcs(ws + k * kThreads + tid);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = k * kThreads + tid, pp = (i * 4) / N, n = (i * 4) % N;
             uint2 hi, lo;
-            split_bf16(v.x, v.y, &hi.x, &lo.x);
-            split_bf16(v.z, v.w, &hi.y, &lo.y);
-            *reinterpret_cast<uint2 *>(&sm.sin[pp][n]) = hi;
-            *reinterpret_cast<uint2 *>(&sm.slo[pp][n]) = lo;
+            split_bf16(v[k].x, v[k].y, &hi.x, &lo.x);
+            split_bf16(v[k].z, v[k].w, &hi.y, &lo.y);
+            *reinterpret_cast<uint2 *>(&sm.ss[pp][n]) = hi;
+            *reinterpret_cast<uint2 *>(&sm.sl[pp][n]) = lo;
+        }
+        constexpr float kLog2e = 1.4426950408889634f;
+        for (int t = tid; t < Q; t += kThreads) {
+            sm.cs[t] = p.ws_acs[ch * Q + t] * kLog2e;
+            sm.dtp[t] = p.ws_dtp[ch * Q + t];
+            sm.cbd[t] = p.ws_cbd[(static_cast<int64_t>(c) * p.G + g) * Q + t];
         }
     }
+    cp_async_wait_all();
     __syncthreads();
 
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3;
-    const int tb = tb0 + warp * 16;  // this warp's 16 tokens
-    if (tb >= L) return;
-    // C fragments of the warp's rows for every k-step over n
-    uint32_t cf[N / 16][4];
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
+    const __nv_bfloat16 *Cg = static_cast<const __nv_bfloat16 *>(p.C);
+    const float *cbg = p.ws_cb + (static_cast<int64_t>(c) * p.G + g) * cb_tiles(Q) * 256;
+    const float Dh = p.D ? p.D[h] : 0.f;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+        const int m = half ? Q / 16 - 1 - warp : warp;
+        if (16 * m >= L) continue;
+        const int ta = 16 * m + gq, tc = ta + 8;  // the two rows this lane holds
+        float acc[P / 8][4];
 #pragma unroll
-    for (int ks = 0; ks < N / 16; ++ks) {
-        const int r0 = warp * 16 + gq, n0 = ks * 16 + 2 * q;
-        cf[ks][0] = *reinterpret_cast<const uint32_t *>(&sm.cm[r0][n0]);
-        cf[ks][1] = *reinterpret_cast<const uint32_t *>(&sm.cm[r0 + 8][n0]);
-        cf[ks][2] = *reinterpret_cast<const uint32_t *>(&sm.cm[r0][n0 + 8]);
-        cf[ks][3] = *reinterpret_cast<const uint32_t *>(&sm.cm[r0 + 8][n0 + 8]);
-    }
-    // y from the entering state: (C . S_in^T) scaled by exp(cs_t), S_in as
-    // the sum of its bf16 high and low parts
-    float yacc[P / 8][4];
+        for (int j = 0; j < P / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        // y from the entering state, C . S_in^T; C fragments straight from global memory
+        uint32_t cf[N / 16][4];
+        {
+            const unsigned int *ra = reinterpret_cast<const unsigned int *>(Cg + ((t0 + ta) * p.G + g) * N);
+            const unsigned int *rc = reinterpret_cast<const unsigned int *>(Cg + ((t0 + tc) * p.G + g) * N);
 #pragma unroll
-    for (int j = 0; j < P / 8; ++j) yacc[j][0] = yacc[j][1] = yacc[j][2] = yacc[j][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < N / 16; ++ks) {
-#pragma unroll
-        for (int j = 0; j < P / 8; ++j) {
-            const int r = 8 * j + gq, n0 = ks * 16 + 2 * q;
-            mma_bf16(yacc[j], cf[ks], *reinterpret_cast<const uint32_t *>(&sm.sin[r][n0]),
-                     *reinterpret_cast<const uint32_t *>(&sm.sin[r][n0 + 8]));
-            mma_bf16(yacc[j], cf[ks], *reinterpret_cast<const uint32_t *>(&sm.slo[r][n0]),
-                     *reinterpret_cast<const uint32_t *>(&sm.slo[r][n0 + 8]));
+            for (int ks = 0; ks < N / 16; ++ks) {
+                const int n2 = 8 * ks + q;  // (16 ks + 2 q) / 2
+                cf[ks][0] = ta < L ? __ldg(ra + n2) : 0u;
+                cf[ks][1] = tc < L ? __ldg(rc + n2) : 0u;
+                cf[ks][2] = ta < L ? __ldg(ra + n2 + 4) : 0u;
+                cf[ks][3] = tc < L ? __ldg(rc + n2 + 4) : 0u;
+            }
         }
-    }
-    const int ta = tb + gq, tc = tb + gq + 8;  // the two rows this lane holds
-    const float ea = expf(sm.cs[min(ta, Q - 1)]), ec = expf(sm.cs[min(tc, Q - 1)]);
-#pragma unroll
-    for (int j = 0; j < P / 8; ++j) {
-        yacc[j][0] *= ea;
-        yacc[j][1] *= ea;
-        yacc[j][2] *= ec;
-        yacc[j][3] *= ec;
-    }
-    // causal part, 16 tokens s at a time
-    for (int sb = 0; sb <= tb; sb += 16) {
-        float cb[2][4];
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) cb[jj][0] = cb[jj][1] = cb[jj][2] = cb[jj][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int s = sb + 8 * jj + gq;
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&sm.bm[s][ks * 16 + 2 * q]);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&sm.bm[s][ks * 16 + 2 * q + 8]);
-                mma_bf16(cb[jj], cf[ks], b0, b1);
+            for (int j = 0; j < P / 8; j += 2) {
+                // S_in^T: B[k = n][col = p] = ss[p][n]: matrices (n 0-7 | 8-15) x (p-tile j | j+1)
+                uint32_t b[4], bl[4];
+                ldsm_x4(b, &sm.ss[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]);
+                ldsm_x4(bl, &sm.sl[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]);
+                mma_bf16(acc[j], cf[ks], b[0], b[1]);
+                mma_bf16(acc[j + 1], cf[ks], b[2], b[3]);
+                mma_bf16(acc[j], cf[ks], bl[0], bl[1]);
+                mma_bf16(acc[j + 1], cf[ks], bl[2], bl[3]);
             }
         }
-        // M[t][s] = CB exp(cs_t - cs_s) dt'_s for s <= t (and s < L), else 0,
-        // as a bf16 high and low part: the diagonal term alone can nearly
-        // cancel D x_t, so M keeps ~2^-17 relative precision
-        uint32_t mf[4], ml[4];
+        const float csa = sm.cs[ta], csc = sm.cs[tc];
+        const float ea = exp2f(csa), ec = exp2f(csc);
 #pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-            const int s0 = sb + 8 * jj + 2 * q, s1 = s0 + 1;
-            const float ws0 = s0 < send ? sm.dtp[s0] : 0.f, ws1 = s1 < send ? sm.dtp[s1] : 0.f;
-            const float csa = sm.cs[min(ta, Q - 1)], csc = sm.cs[min(tc, Q - 1)];
-            const float m00 = s0 <= ta ? cb[jj][0] * expf(csa - sm.cs[s0]) * ws0 : 0.f;
-            const float m01 = s1 <= ta ? cb[jj][1] * expf(csa - sm.cs[s1]) * ws1 : 0.f;
-            const float m10 = s0 <= tc ? cb[jj][2] * expf(csc - sm.cs[s0]) * ws0 : 0.f;
-            const float m11 = s1 <= tc ? cb[jj][3] * expf(csc - sm.cs[s1]) * ws1 : 0.f;
-            split_bf16(m00, m01, &mf[2 * jj], &ml[2 * jj]);
-            split_bf16(m10, m11, &mf[2 * jj + 1], &ml[2 * jj + 1]);
+        for (int j = 0; j < P / 8; ++j) acc[j][0] *= ea, acc[j][1] *= ea, acc[j][2] *= ec, acc[j][3] *= ec;
+        // strictly causal part, 16 tokens s at a time; the next tile's C . B^T
+        // is loaded while this one is used
+        const float4 *row_tiles = reinterpret_cast<const float4 *>(cbg + static_cast<int64_t>(cb_tile(m, 0)) * 256) +
+                                  lane * 2;
+        float4 v0 = __ldg(row_tiles), v1 = __ldg(row_tiles + 1);
+        for (int js = 0; js <= m; ++js) {
+            const float cb[2][4] = {{v0.x, v0.y, v0.z, v0.w}, {v1.x, v1.y, v1.z, v1.w}};
+            if (js < m) v0 = __ldg(row_tiles + (js + 1) * 64), v1 = __ldg(row_tiles + (js + 1) * 64 + 1);
+            // M[t][s] = CB exp(cs_t - cs_s) dt'_s for s < t, else 0 (dt' is 0 from L on)
+            uint32_t mf[4], ml[4];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int s0 = 16 * js + 8 * jj + 2 * q, s1 = s0 + 1;
+                const float d0 = sm.dtp[s0], d1 = sm.dtp[s1], e0 = sm.cs[s0], e1 = sm.cs[s1];
+                const float m00 = s0 < ta ? cb[jj][0] * exp2f(csa - e0) * d0 : 0.f;
+                const float m01 = s1 < ta ? cb[jj][1] * exp2f(csa - e1) * d1 : 0.f;
+                const float m10 = s0 < tc ? cb[jj][2] * exp2f(csc - e0) * d0 : 0.f;
+                const float m11 = s1 < tc ? cb[jj][3] * exp2f(csc - e1) * d1 : 0.f;
+                split_bf16(m00, m01, &mf[2 * jj], &ml[2 * jj]);
+                split_bf16(m10, m11, &mf[2 * jj + 1], &ml[2 * jj + 1]);
+            }
+            // (A operand order: {rows g, k 2q}, {rows g+8, k 2q}, {rows g, k 2q+8}, {rows g+8, k 2q+8})
+#pragma unroll
+            for (int j = 0; j < P / 8; j += 2) {
+                // X: B[k = s][col = p] = xs[s][p]: matrices (s 0-7 | 8-15) x (p-tile j | j+1), transposed
+                uint32_t b[4];
+                ldsm_x4_trans(b, &sm.xs[16 * js + (lane & 7) + (mi & 1) * 8][8 * j + (mi >> 1) * 8]);
+                mma_bf16(acc[j], mf, b[0], b[1]);
+                mma_bf16(acc[j + 1], mf, b[2], b[3]);
+                mma_bf16(acc[j], ml, b[0], b[1]);
+                mma_bf16(acc[j + 1], ml, b[2], b[3]);
+            }
         }
-        // A operand order: {rows g, k 2q}, {rows g+8, k 2q}, {rows g, k 2q+8},
-        // {rows g+8, k 2q+8} -- the order mf and ml are filled in
+        // epilogue: + ((C_t . B_t) dt'_t + D) x_t in fp32, gate, store
+        const float wa = fmaf(sm.cbd[ta], sm.dtp[ta], Dh), wc = fmaf(sm.cbd[tc], sm.dtp[tc], Dh);
 #pragma unroll
         for (int j = 0; j < P / 8; ++j) {
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&sm.xt[8 * j + gq][sb + 2 * q]);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&sm.xt[8 * j + gq][sb + 2 * q + 8]);
-            mma_bf16(yacc[j], mf, b0, b1);
-            mma_bf16(yacc[j], ml, b0, b1);
-        }
-    }
-    // epilogue: + D x, gate, store
-    const float Dh = p.D ? p.D[h] : 0.f;
+            const int pp = 8 * j + 2 * q;
 #pragma unroll
-    for (int j = 0; j < P / 8; ++j) {
-        const int pp = 8 * j + 2 * q;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int t = half ? tc : ta;
-            if (t >= L) continue;
-            const int64_t o = ((t0 + t) * p.H + h) * static_cast<int64_t>(P) + pp;
-            const uint32_t xb = *reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(p.x) + o);
-            float v0 = fmaf(Dh, bf16_lo(xb), yacc[j][2 * half]);
-            float v1 = fmaf(Dh, bf16_hi(xb), yacc[j][2 * half + 1]);
-            if (p.z) {
-                const uint32_t zb = *reinterpret_cast<const uint32_t *>(static_cast<const __nv_bfloat16 *>(p.z) + o);
-                v0 *= silu_gate(bf16_lo(zb), 1);
-                v1 *= silu_gate(bf16_hi(zb), 1);
+            for (int r = 0; r < 2; ++r) {
+                const int t = r ? tc : ta;
+                if (t >= L) continue;
+                const uint32_t xb = *reinterpret_cast<const uint32_t *>(&sm.xs[t][pp]);
+                const float wd = r ? wc : wa;
+                float v0 = fmaf(wd, bf16_lo(xb), acc[j][2 * r]);
+                float v1 = fmaf(wd, bf16_hi(xb), acc[j][2 * r + 1]);
+                uint32_t *zy = reinterpret_cast<uint32_t *>(&sm.zy[t][pp]);
+                if (p.z) {
+                    const uint32_t zb = *zy;
+                    v0 *= silu_gate(bf16_lo(zb), 1);
+                    v1 *= silu_gate(bf16_hi(zb), 1);
+                }
+                *zy = pack_bf16(v0, v1);  // this lane's z element becomes its y element
             }
-            *reinterpret_cast<uint32_t *>(static_cast<__nv_bfloat16 *>(p.y) + o) = pack_bf16(v0, v1);
+        }
+        // the warp's 16 rows of y, 16 bytes per lane and store
+        __syncwarp();
+        for (int i = lane; i < 16 * (P / 8); i += 32) {
+            const int t = 16 * m + i / (P / 8), k = (i % (P / 8)) * 8;
+            if (t < L)
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y) + ((t0 + t) * p.H + h) * static_cast<int64_t>(P) + k) =
+                    *reinterpret_cast<const uint4 *>(&sm.zy[t][k]);
         }
     }
 }
@@ -454,27 +599,34 @@ __global__ void __launch_bounds__(128) ssd_chunk_scan_kernel(const SsdParams p) 
 // ---------------------------------------------------------------------------
 // Launch.
 // ---------------------------------------------------------------------------
+template <typename K>
+static cudaError_t allow_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
 template <int Q, int P, int N>
 static cudaError_t launch_qpn(const SsdParams &p, cudaStream_t stream) {
-    const size_t s1 = sizeof(ChunkStateSmem<Q, P, N>), s3 = sizeof(ChunkScanSmem<Q, P, N>);
-    cudaError_t e = cudaFuncSetAttribute(ssd_chunk_state_kernel<Q, P, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(s1));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(ssd_chunk_scan_kernel<Q, P, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(s3));
-    if (e != cudaSuccess) return e;
-    const dim3 g1(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.H));
-    ssd_chunk_state_kernel<Q, P, N><<<g1, 128, s1, stream>>>(p);
+    const size_t s1 = sizeof(ChunkStateSmem<Q, P, N>), s4 = sizeof(ChunkCbSmem<Q, N>),
+                 s5 = sizeof(ChunkScanSmem<Q, P, N>);
+    cudaError_t e;
+    if ((e = allow_smem(ssd_chunk_state_kernel<Q, P, N>, s1)) != cudaSuccess) return e;
+    if ((e = allow_smem(ssd_chunk_cb_kernel<Q, N>, s4)) != cudaSuccess) return e;
+    if ((e = allow_smem(ssd_chunk_scan_kernel<Q, P, N>, s5)) != cudaSuccess) return e;
+    const dim3 g1(static_cast<unsigned>(p.H), static_cast<unsigned>(p.nchunks));
+    ssd_chunk_state_kernel<Q, P, N><<<g1, kStateThreads, s1, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const dim3 g3(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.H));
     switch (p.state_dtype) {
-    case kF32: ssd_state_pass_kernel<P, N, float><<<g1, 256, 0, stream>>>(p); break;
-    case kF16: ssd_state_pass_kernel<P, N, __half><<<g1, 256, 0, stream>>>(p); break;
-    case kBF16: ssd_state_pass_kernel<P, N, __nv_bfloat16><<<g1, 256, 0, stream>>>(p); break;
+    case kF32: ssd_state_pass_kernel<P, N, float><<<g3, kPassThreads, 0, stream>>>(p); break;
+    case kF16: ssd_state_pass_kernel<P, N, __half><<<g3, kPassThreads, 0, stream>>>(p); break;
+    case kBF16: ssd_state_pass_kernel<P, N, __nv_bfloat16><<<g3, kPassThreads, 0, stream>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const dim3 g3(static_cast<unsigned>(p.nchunks), static_cast<unsigned>(p.H), Q / 64);
-    ssd_chunk_scan_kernel<Q, P, N><<<g3, 128, s3, stream>>>(p);
+    const dim3 g4(static_cast<unsigned>(p.G), static_cast<unsigned>(p.nchunks));
+    ssd_chunk_cb_kernel<Q, N><<<g4, kCbThreads, s4, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ssd_chunk_scan_kernel<Q, P, N><<<g1, Q, s5, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -205,10 +205,13 @@ def test_ssd_host_checks_reject_before_launch(libssu, kw, code, needle):
 
 def test_ssd_workspace_size_and_empty_call(libssu):
     n = ctypes.c_uint64(0)
-    assert libssu.ssu_ssd_workspace_size(3, 4, 64, 128, 64, ctypes.byref(n)) == ssu.OK
+    assert libssu.ssu_ssd_workspace_size(3, 4, 2, 64, 128, 64, ctypes.byref(n)) == ssu.OK
     up = lambda v: (v + 255) // 256 * 256
-    assert n.value == up(12 * 64 * 128 * 4) + 2 * up(12 * 64 * 4) + up(12 * 4)
-    assert libssu.ssu_ssd_workspace_size(3, 0, 64, 128, 64, ctypes.byref(n)) == ssu.ERR_INVALID
+    tiles = 4 * 5 // 2  # causal 16 x 16 tiles of a 64-token chunk
+    assert n.value == (up(12 * 64 * 128 * 4) + 2 * up(12 * 64 * 4) + up(12 * 4) + up(6 * tiles * 256 * 4)
+                       + up(6 * 64 * 4))
+    assert libssu.ssu_ssd_workspace_size(3, 0, 2, 64, 128, 64, ctypes.byref(n)) == ssu.ERR_INVALID
+    assert libssu.ssu_ssd_workspace_size(3, 4, 0, 64, 128, 64, ctypes.byref(n)) == ssu.ERR_INVALID
     # no chunks: nothing to do, nothing launched, no pointer looked at
     a = _ssd_args(nchunks=0, x=None, B=None, workspace=None)
     assert libssu.ssu_ssd_prefill(ctypes.byref(a), None) == ssu.OK

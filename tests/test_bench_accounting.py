@@ -19,7 +19,7 @@ def test_ssd_accounting_one_chunk():
     # per head: chunk state 2TPN, C . S_in^T 2TNP, and one 16 x 16 causal tile
     # for C . B^T (2 * 256 * N) and M . X (2 * 256 * P)
     assert a["flops"] == 2 * (2 * 16 * 8 * 16 + 2 * 16 * 16 * 8 + 2 * 256 * 16 + 2 * 256 * 8)
-    assert a["workspace"] == 4 * 1 * 2 * 8 * 16 * 4
+    assert a["workspace"] == 4 * 1 * 2 * 8 * 16 * 4 + 1 * 256 * 4 * (1 + 2)
     assert a["tokens"] == 16
 
 
