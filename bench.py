@@ -535,8 +535,9 @@ def ssd_accounting(w) -> dict:
     # the chunk states cross the workspace four times (written, read and
     # replaced by the entering states, read by the scan); the C . B^T tiles
     # are written once per (chunk, group) and read by each head of the group
-    tiles = (w.chunk_size // 16) * (w.chunk_size // 16 + 1) // 2
-    cb = nchunks * G * tiles * 256 * 4
+    Q = w.chunk_size
+    tiles = (Q // 16) * (Q // 16 + 1) // 2
+    cb = nchunks * G * tiles * 256 * 4  # the causal part of C . B^T
     return {"inputs": inputs, "outputs": outputs, "total": inputs + outputs, "flops": flops,
             "workspace": 4 * ch * P * N * 4 + cb * (1 + H // G), "tokens": T}
 

@@ -309,7 +309,7 @@ typedef struct ssu_ssd_args {
 
 /* Workspace ssu_ssd_prefill needs for these sizes (bytes, into *bytes):
  * the chunk states (fp32), per-chunk prefix sums, dt' and decays, and the
- * causal C . B^T tiles of every (chunk, group) in fp32. */
+ * causal 16 x 16 tiles of C . B^T of every (chunk, group) in fp32. */
 ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t groups, int64_t dim, int64_t dstate,
                                   int64_t chunk_size, uint64_t *bytes);
 

@@ -264,7 +264,7 @@ ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes,
 }
 
 // Workspace carve-up of the SSD prefill: chunk states, prefix sums, dt',
-// chunk decays, C . B^T tiles, their diagonals; each part 256-byte aligned.
+// chunk decays, C . B^T tiles, their diagonal; each part 256-byte aligned.
 struct SsdWorkspace {
     uint64_t state, acs, dtp, dec, cb, cbd, total;
 };

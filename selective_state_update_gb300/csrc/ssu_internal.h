@@ -95,11 +95,11 @@ struct SsdParams {
     const void *init;                // [nseq, H, P, N] state dtype or NULL
     void *y;                         // [tokens, H, P] bf16
     void *states;                    // [nchunks or nseq, H, P, N] state dtype
-    float *ws_state;                 // [nchunks, H, P, N]
-    float *ws_acs, *ws_dtp;          // [nchunks, H, Q]
-    float *ws_dec;                   // [nchunks, H]
-    float *ws_cb;                    // [nchunks, G, causal 16 x 16 tiles of Q, 256] (fragment order)
-    float *ws_cbd;                   // [nchunks, G, Q]
+    float *ws_state;                 // [H, nchunks, P*N]: chunk states (fp32), then entering states (bf16 hi | lo)
+    float *ws_acs, *ws_dtp;          // [H, nchunks, Q]
+    float *ws_dec;                   // [H, nchunks]
+    float *ws_cb;                    // [nchunks, G, causal 16 x 16 tiles of Q, 256] C . B^T (fragment order)
+    float *ws_cbd;                   // [nchunks, G, Q] C_t . B_t
     int32_t *status;
 };
 cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream);

@@ -24,8 +24,8 @@
 //                w x is split into a bf16 high and low part so that Sc keeps
 //                ~2^-17 relative precision (the returned states need it);
 //   state_pass   one CTA per (run of a sequence's chunks, head): replaces
-//                each Sc in the workspace by the chunk's entering state and
-//                writes the returned states;
+//                each Sc in the workspace by the chunk's entering state (as
+//                bf16 high and low parts) and writes the returned states;
 //   chunk_cb     one CTA per (group, chunk): the causal 16 x 16 tiles of
 //                C . B^T in fp32, stored in mma fragment order so that the
 //                heads of the group read them back with coalesced loads, and
@@ -98,10 +98,28 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t *hi, uin
     *lo = pack_bf16(x0 - h0, x1 - h1);
 }
 
+// 2^x by the special-function unit (PTX ex2.approx.ftz: relative error
+// below 2^-22, results below 2^-126 flushed to zero); x <= 0 here.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 __device__ __forceinline__ int64_t meta_at(const void *p, int64_t i, int is_i64) { return load_index(p, i, is_i64); }
+
+// Element (p, n) of a P x N state in the order the tensor cores read a
+// K-major operand without swizzle: 8 x 8 core matrices (8 rows p of 8
+// consecutive n), stored one after another along n, then along p.  The
+// chunk states are kept in this order in the workspace (fp32), and the
+// entering states as its bf16 high and low parts.
+template <int N>
+__host__ __device__ constexpr int canon(int p, int n) {
+    return (p >> 3) * (N * 8) + (n >> 3) * 64 + (p & 7) * 8 + (n & 7);
+}
 
 // The causal 16 x 16 tiles (row tile m, column tile j <= m) of a chunk of Q
 // tokens, numbered row tile by row tile.
@@ -176,7 +194,7 @@ constexpr int kStateThreads = 256;
 template <int Q, int P, int N>
 __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const SsdParams p) {
     static_assert(P == 64 && N % 64 == 0 && Q <= kStateThreads, "tiling");
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<ChunkStateSmem<Q, P, N> *>(smem_raw);
     const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
     const int g = h / p.hpg;
@@ -256,8 +274,8 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const int n = n0 + 8 * j + 2 * q;
-        *reinterpret_cast<float2 *>(out + (p0 + gq) * N + n) = make_float2(acc[j][0], acc[j][1]);
-        *reinterpret_cast<float2 *>(out + (p0 + gq + 8) * N + n) = make_float2(acc[j][2], acc[j][3]);
+        *reinterpret_cast<float2 *>(out + canon<N>(p0 + gq, n)) = make_float2(acc[j][0], acc[j][1]);
+        *reinterpret_cast<float2 *>(out + canon<N>(p0 + gq + 8, n)) = make_float2(acc[j][2], acc[j][3]);
     }
 }
 
@@ -318,15 +336,20 @@ __global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdP
     const bool overflow = nlist > kPassList;
     const int nl = nlist < kPassList ? nlist : kPassList;
 
-    constexpr int kPer = P * N / (kPassThreads * 4);  // float4 per thread
+    // Thread tid holds the groups e = 4 (k kPassThreads + tid) of the canonical
+    // order: four consecutive n of one row p.
+    constexpr int kPer = P * N / (kPassThreads * 4);
     const int64_t PN = static_cast<int64_t>(P) * N;
     const int64_t hs = static_cast<int64_t>(h) * PN;
     float *ws0 = p.ws_state + ws_unit(p, 0, h) * PN;  // this head's chunks, contiguous
+    int uoff[kPer];                                   // the groups in the [P][N] layout of the states
     float4 S[kPer], sc[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
-        const int64_t e = (static_cast<int64_t>(k) * kPassThreads + tid) * 4;
-        S[k] = p.init ? load_state4<TS>(p.init, b * p.H * PN + hs + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int e = 4 * (k * kPassThreads + tid);
+        const int pp = (e / (N * 8)) * 8 + (e % 64) / 8, nn = ((e / 64) % (N / 8)) * 8 + (e % 8);
+        uoff[k] = pp * N + nn;
+        S[k] = p.init ? load_state4<TS>(p.init, b * p.H * PN + hs + uoff[k]) : make_float4(0.f, 0.f, 0.f, 0.f);
         sc[k] = __ldcs(reinterpret_cast<const float4 *>(ws0 + c0 * PN + e));
     }
     for (int64_t c = c0;; ++c) {
@@ -336,26 +359,32 @@ __global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdP
         float4 nx[kPer];
         if (c + 1 < p.nchunks) {  // the next chunk's Sc (read one chunk ahead, also past the run's end)
 #pragma unroll
-            for (int k = 0; k < kPer; ++k) nx[k] = __ldcs(reinterpret_cast<const float4 *>(ws + PN + (k * kPassThreads + tid) * 4));
+            for (int k = 0; k < kPer; ++k)
+                nx[k] = __ldcs(reinterpret_cast<const float4 *>(ws + PN + 4 * (k * kPassThreads + tid)));
         }
+        __syncthreads();  // every thread has read chunk c's Sc before its slot is overwritten
+        // the state entering chunk c, as bf16 high and low parts in canonical order
+        unsigned char *slot = reinterpret_cast<unsigned char *>(ws);
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            *reinterpret_cast<float4 *>(ws + (k * kPassThreads + tid) * 4) = S[k];  // the state entering chunk c
+            const int e = 4 * (k * kPassThreads + tid);
+            uint2 hi, lo;
+            split_bf16(S[k].x, S[k].y, &hi.x, &lo.x);
+            split_bf16(S[k].z, S[k].w, &hi.y, &lo.y);
+            *reinterpret_cast<uint2 *>(slot + 2 * e) = hi;
+            *reinterpret_cast<uint2 *>(slot + 2 * PN + 2 * e) = lo;
             S[k] = make_float4(fmaf(dec, S[k].x, sc[k].x), fmaf(dec, S[k].y, sc[k].y), fmaf(dec, S[k].z, sc[k].z),
                                fmaf(dec, S[k].w, sc[k].w));
         }
         if (p.intermediate) {
 #pragma unroll
-            for (int k = 0; k < kPer; ++k)
-                store_state4(static_cast<TS *>(p.states) + c * p.H * PN + hs + (k * kPassThreads + tid) * 4, S[k]);
+            for (int k = 0; k < kPer; ++k) store_state4(static_cast<TS *>(p.states) + c * p.H * PN + hs + uoff[k], S[k]);
         } else {
             for (int i = 0; i < nl; ++i) {
                 if (list_chunk[i] != c) continue;
 #pragma unroll
                 for (int k = 0; k < kPer; ++k)
-                    store_state4(static_cast<TS *>(p.states) + list_seq[i] * p.H * PN + hs +
-                                     (k * kPassThreads + tid) * 4,
-                                 S[k]);
+                    store_state4(static_cast<TS *>(p.states) + list_seq[i] * p.H * PN + hs + uoff[k], S[k]);
             }
             if (overflow) {  // more such sequences than the list holds: find the rest
                 for (int64_t s = 0; s < p.nseq; ++s) {
@@ -365,8 +394,7 @@ __global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdP
                     if (listed) continue;
 #pragma unroll
                     for (int k = 0; k < kPer; ++k)
-                        store_state4(static_cast<TS *>(p.states) + s * p.H * PN + hs + (k * kPassThreads + tid) * 4,
-                                     S[k]);
+                        store_state4(static_cast<TS *>(p.states) + s * p.H * PN + hs + uoff[k], S[k]);
                 }
             }
         }
@@ -430,7 +458,18 @@ __global__ void __launch_bounds__(kCbThreads) ssd_chunk_cb_kernel(const SsdParam
 }
 
 // ---------------------------------------------------------------------------
-// Stage 5: the chunk scan, one CTA per (head, chunk).
+// Stage 5: the chunk scan, one CTA per (head, chunk); warp w takes the row
+// tiles w and Q/16 - 1 - w (16 tokens each) so that the causal work is
+// balanced.  Per row tile:
+//   Y1 = C . S_in^T, scaled by exp(cs_t)   (S_in as bf16 high + low parts,
+//                                           split once by the state pass)
+//   Y2 = sum over column tiles j of W_j . x_j, W[t][s] = (C . B^T)
+//        exp(cs_t - cs_s) dt'_s for s < t, as bf16 high + low parts; for a
+//        tile that lies wholly before the rows the decay factors through the
+//        tile's last token r, exp(cs_t - cs_r) exp(cs_r - cs_s), both at most
+//        1 (cs only decreases), the second with dt'_s kept per column (E)
+//   y = Y1 + Y2 + ((C_t . B_t) dt'_t + D) x_t   (the diagonal in fp32: it can
+//        cancel D for every dim row of a token), gated by silu(z).
 // ---------------------------------------------------------------------------
 template <int Q, int P, int N>
 struct ChunkScanSmem {
@@ -441,13 +480,14 @@ struct ChunkScanSmem {
     float cs[Q];                 // inclusive cumulative sums of a, times log2(e)
     float dtp[Q];                // dt'
     float cbd[Q];                // C_t . B_t
+    float E[Q];                  // exp(cs_r - cs_s) dt'_s, r the last token of s's 16-token tile
 };
 
 template <int Q, int P, int N>
 __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p) {
     static_assert(P == 64 && Q % 64 == 0, "tiling");
-    constexpr int kThreads = Q;  // Q / 32 warps, each the row tiles m and Q/16 - 1 - m
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int kThreads = Q;  // Q / 32 warps
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<ChunkScanSmem<Q, P, N> *>(smem_raw);
     const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
     const int g = h / p.hpg;
@@ -460,29 +500,23 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
     if (p.z)
         stage_rows<kThreads>(&sm.zy[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.z), t0,
                              static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
-    {
-        const int64_t ch = ws_unit(p, c, h);
-        const float4 *ws = reinterpret_cast<const float4 *>(p.ws_state + ch * P * N);
-        constexpr int kPer = P * N / 4 / kThreads;  // float4 of the entering state per thread
-        float4 v[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) v[k] = __ldcs(ws + k * kThreads + tid);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i = k * kThreads + tid, pp = (i * 4) / N, n = (i * 4) % N;
-            uint2 hi, lo;
-            split_bf16(v[k].x, v[k].y, &hi.x, &lo.x);
-            split_bf16(v[k].z, v[k].w, &hi.y, &lo.y);
-            *reinterpret_cast<uint2 *>(&sm.ss[pp][n]) = hi;
-            *reinterpret_cast<uint2 *>(&sm.sl[pp][n]) = lo;
-        }
-        constexpr float kLog2e = 1.4426950408889634f;
-        for (int t = tid; t < Q; t += kThreads) {
-            sm.cs[t] = p.ws_acs[ch * Q + t] * kLog2e;
-            sm.dtp[t] = p.ws_dtp[ch * Q + t];
-            sm.cbd[t] = p.ws_cbd[(static_cast<int64_t>(c) * p.G + g) * Q + t];
+    const int64_t ch = ws_unit(p, c, h);
+    {  // the entering state's parts, from the canonical order into padded rows
+        const unsigned char *slot = reinterpret_cast<const unsigned char *>(p.ws_state + ch * P * N);
+        for (int i = tid; i < 2 * P * N / 8; i += kThreads) {
+            const int part = i / (P * N / 8), b = (i % (P * N / 8)) * 16;
+            const int pp = (b / (N * 16)) * 8 + (b % 128) / 16, n8 = ((b / 128) % (N / 8)) * 8;
+            cp_async16(part ? &sm.sl[pp][n8] : &sm.ss[pp][n8], slot + part * (P * N * 2) + b, true);
         }
     }
+    constexpr float kLog2e = 1.4426950408889634f;
+    for (int t = tid; t < Q; t += kThreads) {
+        sm.cs[t] = p.ws_acs[ch * Q + t] * kLog2e;
+        sm.dtp[t] = p.ws_dtp[ch * Q + t];
+        sm.cbd[t] = p.ws_cbd[(static_cast<int64_t>(c) * p.G + g) * Q + t];
+    }
+    __syncthreads();
+    for (int t = tid; t < Q; t += kThreads) sm.E[t] = t < L ? ex2_fast(sm.cs[t | 15] - sm.cs[t]) * sm.dtp[t] : 0.f;
     cp_async_wait_all();
     __syncthreads();
 
@@ -538,18 +572,28 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
         for (int js = 0; js <= m; ++js) {
             const float cb[2][4] = {{v0.x, v0.y, v0.z, v0.w}, {v1.x, v1.y, v1.z, v1.w}};
             if (js < m) v0 = __ldg(row_tiles + (js + 1) * 64), v1 = __ldg(row_tiles + (js + 1) * 64 + 1);
-            // M[t][s] = CB exp(cs_t - cs_s) dt'_s for s < t, else 0 (dt' is 0 from L on)
             uint32_t mf[4], ml[4];
+            if (js < m) {  // the tile lies wholly before the rows: decays through its last token
+                const float r = sm.cs[16 * js + 15];
+                const float Ra = ex2_fast(csa - r), Rc = ex2_fast(csc - r);
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int s0 = 16 * js + 8 * jj + 2 * q, s1 = s0 + 1;
-                const float d0 = sm.dtp[s0], d1 = sm.dtp[s1], e0 = sm.cs[s0], e1 = sm.cs[s1];
-                const float m00 = s0 < ta ? cb[jj][0] * exp2f(csa - e0) * d0 : 0.f;
-                const float m01 = s1 < ta ? cb[jj][1] * exp2f(csa - e1) * d1 : 0.f;
-                const float m10 = s0 < tc ? cb[jj][2] * exp2f(csc - e0) * d0 : 0.f;
-                const float m11 = s1 < tc ? cb[jj][3] * exp2f(csc - e1) * d1 : 0.f;
-                split_bf16(m00, m01, &mf[2 * jj], &ml[2 * jj]);
-                split_bf16(m10, m11, &mf[2 * jj + 1], &ml[2 * jj + 1]);
+                for (int jj = 0; jj < 2; ++jj) {
+                    const float2 e = *reinterpret_cast<const float2 *>(&sm.E[16 * js + 8 * jj + 2 * q]);
+                    split_bf16(cb[jj][0] * Ra * e.x, cb[jj][1] * Ra * e.y, &mf[2 * jj], &ml[2 * jj]);
+                    split_bf16(cb[jj][2] * Rc * e.x, cb[jj][3] * Rc * e.y, &mf[2 * jj + 1], &ml[2 * jj + 1]);
+                }
+            } else {  // the diagonal tile: W[t][s] for s < t, one exponential each
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int s0 = 16 * js + 8 * jj + 2 * q, s1 = s0 + 1;
+                    const float d0 = sm.dtp[s0], d1 = sm.dtp[s1], e0 = sm.cs[s0], e1 = sm.cs[s1];
+                    const float m00 = s0 < ta ? cb[jj][0] * ex2_fast(csa - e0) * d0 : 0.f;
+                    const float m01 = s1 < ta ? cb[jj][1] * ex2_fast(csa - e1) * d1 : 0.f;
+                    const float m10 = s0 < tc ? cb[jj][2] * ex2_fast(csc - e0) * d0 : 0.f;
+                    const float m11 = s1 < tc ? cb[jj][3] * ex2_fast(csc - e1) * d1 : 0.f;
+                    split_bf16(m00, m01, &mf[2 * jj], &ml[2 * jj]);
+                    split_bf16(m10, m11, &mf[2 * jj + 1], &ml[2 * jj + 1]);
+                }
             }
             // (A operand order: {rows g, k 2q}, {rows g+8, k 2q}, {rows g, k 2q+8}, {rows g+8, k 2q+8})
 #pragma unroll
@@ -579,8 +623,9 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
                 uint32_t *zy = reinterpret_cast<uint32_t *>(&sm.zy[t][pp]);
                 if (p.z) {
                     const uint32_t zb = *zy;
-                    v0 *= silu_gate(bf16_lo(zb), 1);
-                    v1 *= silu_gate(bf16_hi(zb), 1);
+                    const float z0 = bf16_lo(zb), z1 = bf16_hi(zb);
+                    v0 *= __fdividef(z0, 1.f + __expf(-z0));
+                    v1 *= __fdividef(z1, 1.f + __expf(-z1));
                 }
                 *zy = pack_bf16(v0, v1);  // this lane's z element becomes its y element
             }
