@@ -68,7 +68,7 @@ KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_interna
                   "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"],
-                  "ssd": ["ssu_ssd.cu", "ssu_device.cuh", "ssu_internal.h"]}
+                  "ssd": ["ssu_ssd.cu", "ssu_ssd_params.h", "ssu_device.cuh", "ssu_internal.h"]}
 
 
 # --------------------------------------------------------------------------

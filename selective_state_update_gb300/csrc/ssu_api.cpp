@@ -8,6 +8,7 @@
 #include <cstring>
 
 #include "ssu_internal.h"
+#include "ssu_ssd_params.h"
 
 namespace {
 

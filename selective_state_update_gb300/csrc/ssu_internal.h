@@ -83,26 +83,6 @@ cudaError_t launch_packed(int state_dtype, int lanes, const KParams &p, cudaStre
 cudaError_t prewarm_onetoken(int state_dtype, int lanes);
 cudaError_t prewarm_packed(int state_dtype, int lanes);
 cudaError_t launch_replay(int state_dtype, int lanes, const KParams &p, int64_t batch, cudaStream_t stream);
-// Packed variable-length SSD prefill (ssu_ssd_prefill).
-struct SsdParams {
-    int64_t tokens, nchunks, nseq;
-    int32_t H, G, hpg, P, N, Q;
-    int32_t dt_dtype, state_dtype, softplus, intermediate, meta_i64;
-    float dt_lo, dt_hi;
-    const void *x, *dt, *B, *C, *z;  // x, z [tokens, H, P] bf16; dt [tokens, H]; B, C [tokens, G, N] bf16
-    const float *A, *D, *dt_bias;
-    const void *cu_chunk, *seq_idx, *last_chunk;
-    const void *init;                // [nseq, H, P, N] state dtype or NULL
-    void *y;                         // [tokens, H, P] bf16
-    void *states;                    // [nchunks or nseq, H, P, N] state dtype
-    float *ws_state;                 // [H, nchunks, P*N]: chunk states (fp32), then entering states (bf16 hi | lo)
-    float *ws_acs, *ws_dtp;          // [H, nchunks, Q]
-    float *ws_dec;                   // [H, nchunks]
-    float *ws_cb;                    // [nchunks, G, causal 16 x 16 tiles of Q, 256] C . B^T (fragment order)
-    float *ws_cbd;                   // [nchunks, G, Q] C_t . B_t
-    int32_t *status;
-};
-cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream);
 
 // The read copy of `rows` state rows (ssu_shadow_refresh).
 cudaError_t launch_shadow_refresh(const void *state, int state_dtype, int64_t rows, int dstate, int format,

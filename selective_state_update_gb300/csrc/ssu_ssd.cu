@@ -41,6 +41,7 @@
 #include <cstdint>
 
 #include "ssu_device.cuh"
+#include "ssu_ssd_params.h"
 
 namespace ssu {
 
@@ -259,15 +260,20 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
         split_bf16(bf16_lo(ax[1]) * w0, bf16_hi(ax[1]) * w1, &ahi[1], &alo[1]);
         split_bf16(bf16_lo(ax[2]) * w8, bf16_hi(ax[2]) * w9, &ahi[2], &alo[2]);
         split_bf16(bf16_lo(ax[3]) * w8, bf16_hi(ax[3]) * w9, &ahi[3], &alo[3]);
+        // the high part for every n-tile, then the low part: no accumulator is
+        // used twice in a row
+        uint32_t bb[NT / 2][4];
 #pragma unroll
         for (int j = 0; j < NT; j += 2) {
             // B[t][n]: matrices (t 0-7 | 8-15) x (n-tile j | j+1), transposed
-            uint32_t b[4];
-            ldsm_x4_trans(b, &sm.bs[k0 + (lane & 7) + (mi & 1) * 8][n0 + 8 * j + (mi >> 1) * 8]);
-            mma_bf16(acc[j], ahi, b[0], b[1]);
-            mma_bf16(acc[j], alo, b[0], b[1]);
-            mma_bf16(acc[j + 1], ahi, b[2], b[3]);
-            mma_bf16(acc[j + 1], alo, b[2], b[3]);
+            ldsm_x4_trans(bb[j / 2], &sm.bs[k0 + (lane & 7) + (mi & 1) * 8][n0 + 8 * j + (mi >> 1) * 8]);
+            mma_bf16(acc[j], ahi, bb[j / 2][0], bb[j / 2][1]);
+            mma_bf16(acc[j + 1], ahi, bb[j / 2][2], bb[j / 2][3]);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; j += 2) {
+            mma_bf16(acc[j], alo, bb[j / 2][0], bb[j / 2][1]);
+            mma_bf16(acc[j + 1], alo, bb[j / 2][2], bb[j / 2][3]);
         }
     }
     float *out = p.ws_state + ws_unit(p, c, h) * P * N;
@@ -495,6 +501,24 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
     if (t0 < 0 || t1 < t0 || t1 - t0 > Q || t1 > p.tokens) return;  // flagged by chunk_state
     const int L = static_cast<int>(t1 - t0);
     if (L == 0) return;
+    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
+    const __nv_bfloat16 *Cg = static_cast<const __nv_bfloat16 *>(p.C);
+    // C fragments (A of C . S_in^T) of row tile m, straight from global memory
+    uint32_t cf[N / 16][4];
+    auto load_cf = [&](int m) {
+        const int ta = 16 * m + gq, tc = ta + 8;
+        const unsigned int *ra = reinterpret_cast<const unsigned int *>(Cg + ((t0 + ta) * p.G + g) * N);
+        const unsigned int *rc = reinterpret_cast<const unsigned int *>(Cg + ((t0 + tc) * p.G + g) * N);
+#pragma unroll
+        for (int ks = 0; ks < N / 16; ++ks) {
+            const int n2 = 8 * ks + q;  // (16 ks + 2 q) / 2
+            cf[ks][0] = ta < L ? __ldg(ra + n2) : 0u;
+            cf[ks][1] = tc < L ? __ldg(rc + n2) : 0u;
+            cf[ks][2] = ta < L ? __ldg(ra + n2 + 4) : 0u;
+            cf[ks][3] = tc < L ? __ldg(rc + n2 + 4) : 0u;
+        }
+    };
+    load_cf(warp);  // the first row tile's, in flight during the staging below
     stage_rows<kThreads>(&sm.xs[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.x), t0,
                          static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
     if (p.z)
@@ -520,8 +544,6 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
     cp_async_wait_all();
     __syncthreads();
 
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
-    const __nv_bfloat16 *Cg = static_cast<const __nv_bfloat16 *>(p.C);
     const float *cbg = p.ws_cb + (static_cast<int64_t>(c) * p.G + g) * cb_tiles(Q) * 256;
     const float Dh = p.D ? p.D[h] : 0.f;
 #pragma unroll 1
@@ -532,32 +554,22 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
         float acc[P / 8][4];
 #pragma unroll
         for (int j = 0; j < P / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        // y from the entering state, C . S_in^T; C fragments straight from global memory
-        uint32_t cf[N / 16][4];
-        {
-            const unsigned int *ra = reinterpret_cast<const unsigned int *>(Cg + ((t0 + ta) * p.G + g) * N);
-            const unsigned int *rc = reinterpret_cast<const unsigned int *>(Cg + ((t0 + tc) * p.G + g) * N);
-#pragma unroll
-            for (int ks = 0; ks < N / 16; ++ks) {
-                const int n2 = 8 * ks + q;  // (16 ks + 2 q) / 2
-                cf[ks][0] = ta < L ? __ldg(ra + n2) : 0u;
-                cf[ks][1] = tc < L ? __ldg(rc + n2) : 0u;
-                cf[ks][2] = ta < L ? __ldg(ra + n2 + 4) : 0u;
-                cf[ks][3] = tc < L ? __ldg(rc + n2 + 4) : 0u;
-            }
-        }
+        // y from the entering state, C . S_in^T (the high parts for every p-tile,
+        // then the low parts: no accumulator is used twice in a row)
+        if (half) load_cf(m);
 #pragma unroll
         for (int ks = 0; ks < N / 16; ++ks) {
 #pragma unroll
-            for (int j = 0; j < P / 8; j += 2) {
-                // S_in^T: B[k = n][col = p] = ss[p][n]: matrices (n 0-7 | 8-15) x (p-tile j | j+1)
-                uint32_t b[4], bl[4];
-                ldsm_x4(b, &sm.ss[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]);
-                ldsm_x4(bl, &sm.sl[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]);
-                mma_bf16(acc[j], cf[ks], b[0], b[1]);
-                mma_bf16(acc[j + 1], cf[ks], b[2], b[3]);
-                mma_bf16(acc[j], cf[ks], bl[0], bl[1]);
-                mma_bf16(acc[j + 1], cf[ks], bl[2], bl[3]);
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                for (int j = 0; j < P / 8; j += 2) {
+                    // S_in^T: B[k = n][col = p] = ss[p][n]: matrices (n 0-7 | 8-15) x (p-tile j | j+1)
+                    uint32_t b[4];
+                    ldsm_x4(b, part ? &sm.sl[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]
+                                    : &sm.ss[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]);
+                    mma_bf16(acc[j], cf[ks], b[0], b[1]);
+                    mma_bf16(acc[j + 1], cf[ks], b[2], b[3]);
+                }
             }
         }
         const float csa = sm.cs[ta], csc = sm.cs[tc];
@@ -568,10 +580,12 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
         // is loaded while this one is used
         const float4 *row_tiles = reinterpret_cast<const float4 *>(cbg + static_cast<int64_t>(cb_tile(m, 0)) * 256) +
                                   lane * 2;
-        float4 v0 = __ldg(row_tiles), v1 = __ldg(row_tiles + 1);
+        float4 v0 = __ldg(row_tiles), v1 = __ldg(row_tiles + 1), w0 = v0, w1 = v1;
+        if (m > 0) w0 = __ldg(row_tiles + 64), w1 = __ldg(row_tiles + 65);
         for (int js = 0; js <= m; ++js) {
             const float cb[2][4] = {{v0.x, v0.y, v0.z, v0.w}, {v1.x, v1.y, v1.z, v1.w}};
-            if (js < m) v0 = __ldg(row_tiles + (js + 1) * 64), v1 = __ldg(row_tiles + (js + 1) * 64 + 1);
+            v0 = w0, v1 = w1;  // two tiles ahead in flight
+            if (js + 2 <= m) w0 = __ldg(row_tiles + (js + 2) * 64), w1 = __ldg(row_tiles + (js + 2) * 64 + 1);
             uint32_t mf[4], ml[4];
             if (js < m) {  // the tile lies wholly before the rows: decays through its last token
                 const float r = sm.cs[16 * js + 15];
@@ -596,15 +610,18 @@ __global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p)
                 }
             }
             // (A operand order: {rows g, k 2q}, {rows g+8, k 2q}, {rows g, k 2q+8}, {rows g+8, k 2q+8})
+            uint32_t bx[P / 16][4];
 #pragma unroll
             for (int j = 0; j < P / 8; j += 2) {
                 // X: B[k = s][col = p] = xs[s][p]: matrices (s 0-7 | 8-15) x (p-tile j | j+1), transposed
-                uint32_t b[4];
-                ldsm_x4_trans(b, &sm.xs[16 * js + (lane & 7) + (mi & 1) * 8][8 * j + (mi >> 1) * 8]);
-                mma_bf16(acc[j], mf, b[0], b[1]);
-                mma_bf16(acc[j + 1], mf, b[2], b[3]);
-                mma_bf16(acc[j], ml, b[0], b[1]);
-                mma_bf16(acc[j + 1], ml, b[2], b[3]);
+                ldsm_x4_trans(bx[j / 2], &sm.xs[16 * js + (lane & 7) + (mi & 1) * 8][8 * j + (mi >> 1) * 8]);
+                mma_bf16(acc[j], mf, bx[j / 2][0], bx[j / 2][1]);
+                mma_bf16(acc[j + 1], mf, bx[j / 2][2], bx[j / 2][3]);
+            }
+#pragma unroll
+            for (int j = 0; j < P / 8; j += 2) {
+                mma_bf16(acc[j], ml, bx[j / 2][0], bx[j / 2][1]);
+                mma_bf16(acc[j + 1], ml, bx[j / 2][2], bx[j / 2][3]);
             }
         }
         // epilogue: + ((C_t . B_t) dt'_t + D) x_t in fp32, gate, store
