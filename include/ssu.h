@@ -318,6 +318,23 @@ ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t groups
 ssu_status ssu_ssd_prefill(const ssu_ssd_args *args, void *stream);
 
 /*
+ * ssu_ssd_prefill on a workspace the library owns, for callers that hold no
+ * device memory of their own for it; the pages have no counterpart (their
+ * wrapper caches a workspace it allocates).  args->workspace must be NULL and
+ * args->workspace_bytes 0.  The workspace the call needs
+ * (ssu_ssd_workspace_size) must fit SSU_SSD_STATIC_SCRATCH_BYTES (64 MiB: for
+ * heads 128, groups 8, dim 64, dstate 128 and chunk 256, up to 12 chunks);
+ * a larger call returns SSU_ERR_INVALID before anything runs.  Nothing is
+ * allocated: the scratch is a device array of the library, looked up once per
+ * device on the first call made with that device current -- make that first
+ * call before capturing a graph.  The scratch needs no initialisation.  Calls
+ * that overlap in time (other streams, other threads) share the scratch and
+ * corrupt each other's results: serialise them.
+ */
+#define SSU_SSD_STATIC_SCRATCH_BYTES (64ull << 20)
+ssu_status ssu_ssd_prefill_static(const ssu_ssd_args *args, void *stream);
+
+/*
  * One copy of a batch: `bytes` bytes from device address `src` to device
  * address `dst` (any alignment; 16-byte aligned addresses take the vector
  * path).

@@ -30,7 +30,7 @@ from typing import Optional
 import torch
 
 __all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_shadow_refresh",
-           "ssu_ssd_prefill", "ssd_combined_fwd_varlen",
+           "ssu_ssd_prefill", "ssu_ssd_prefill_static", "ssd_combined_fwd_varlen",
            "ssu_batch_copy", "copy_table",
            "slot_copies", "ssu_prewarm",
            "selective_state_update",
@@ -146,6 +146,8 @@ def lib():
         L.ssu_ssd_workspace_size.restype = ctypes.c_int
         L.ssu_ssd_prefill.argtypes = [ctypes.POINTER(SsdArgs), ctypes.c_void_p]
         L.ssu_ssd_prefill.restype = ctypes.c_int
+        L.ssu_ssd_prefill_static.argtypes = [ctypes.POINTER(SsdArgs), ctypes.c_void_p]
+        L.ssu_ssd_prefill_static.restype = ctypes.c_int
         L.ssu_shadow_refresh.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                          ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.ssu_shadow_refresh.restype = ctypes.c_int
@@ -431,6 +433,52 @@ def ssu_ssd_prefill(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, 
                 initial_states=_ptr(initial_states), y=out.data_ptr(), states=states.data_ptr(),
                 workspace=ws.data_ptr(), workspace_bytes=ws.numel(), d_status=_ptr(status))
     rc = lib().ssu_ssd_prefill(ctypes.byref(a), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    return out, states
+
+
+SSD_STATIC_SCRATCH_BYTES = 64 << 20  # SSU_SSD_STATIC_SCRATCH_BYTES
+
+
+def ssu_ssd_prefill_static(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, last_chunk_indices=None,
+                           out=None, D=None, z=None, dt_bias=None, dt_softplus=False, dt_limit=(0.0, float("inf")),
+                           initial_states=None, return_intermediate_states=False, state_dtype=None, nseq=None,
+                           status=None, stream=None):
+    """ssu_ssd_prefill on the library's own scratch (``ssu_ssd_prefill_static``
+    in ``include/ssu.h``): no workspace is allocated; the call's workspace must
+    fit SSD_STATIC_SCRATCH_BYTES, and calls must not overlap in time.
+    Returns (y, states)."""
+    _need(x.dim() == 3 and dt.dim() == 2 and B.dim() == 3 and C.shape == B.shape, "x, dt, B, C shapes")
+    tokens, heads, dim = x.shape
+    groups, dstate = B.shape[1], B.shape[2]
+    _need(dt.shape == (tokens, heads) and B.shape[0] == tokens, "dt must be [tokens, heads], B [tokens, ...]")
+    for t in (x, dt, B, C, z, out, initial_states):
+        _need(t is None or (t.is_cuda and t.is_contiguous()), "tensors must be contiguous CUDA tensors")
+    meta = cu_chunk_seqlens.dtype
+    _need(meta in _ITYPE and seq_idx.dtype == meta and (last_chunk_indices is None or last_chunk_indices.dtype == meta),
+          "cu_chunk_seqlens, seq_idx and last_chunk_indices share one integer dtype")
+    nchunks = seq_idx.numel()
+    if nseq is None:
+        nseq = last_chunk_indices.numel() if last_chunk_indices is not None else initial_states.shape[0]
+    sdt = state_dtype or (initial_states.dtype if initial_states is not None else C.dtype)
+    out = out if out is not None else torch.empty_like(x)
+    states = torch.empty(((nchunks if return_intermediate_states else nseq), heads, dim, dstate), dtype=sdt,
+                         device=x.device)
+    if initial_states is not None and initial_states.dtype != sdt:
+        initial_states = initial_states.to(sdt)
+    hi = float(dt_limit[1])
+    a = SsdArgs(tokens=tokens, heads=heads, dim=dim, dstate=dstate, groups=groups, nseq=nseq, nchunks=nchunks,
+                chunk_size=chunk_size, io_dtype=_DTYPE.get(x.dtype, -1), dt_dtype=_DTYPE[dt.dtype],
+                state_dtype=_DTYPE[sdt], meta_type=_ITYPE[meta], dt_softplus=int(bool(dt_softplus)),
+                return_intermediate=int(bool(return_intermediate_states)), dt_min=float(dt_limit[0]),
+                dt_max=min(hi, 3.4028234663852886e38),
+                x=x.data_ptr(), dt=dt.data_ptr(), B=B.data_ptr(), C=C.data_ptr(), z=_ptr(z), A=A.data_ptr(),
+                D=_ptr(D), dt_bias=_ptr(dt_bias), cu_chunk_seqlens=cu_chunk_seqlens.data_ptr(),
+                seq_idx=seq_idx.data_ptr(), last_chunk_indices=_ptr(last_chunk_indices),
+                initial_states=_ptr(initial_states), y=out.data_ptr(), states=states.data_ptr(),
+                workspace=None, workspace_bytes=0, d_status=_ptr(status))
+    rc = lib().ssu_ssd_prefill_static(ctypes.byref(a), _stream(stream))
     if rc != OK:
         _raise(rc)
     return out, states

@@ -358,6 +358,27 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *a, void *stream) {
     return launched(ssu::launch_ssd(p, static_cast<cudaStream_t>(stream)));
 }
 
+ssu_status ssu_ssd_prefill_static(const ssu_ssd_args *args, void *stream) {
+    if (args == nullptr) return fail(SSU_ERR_INVALID, "args is NULL");
+    if (args->workspace != nullptr || args->workspace_bytes != 0)
+        return fail(SSU_ERR_INVALID, "workspace must be NULL and workspace_bytes 0 (the library's scratch is used)");
+    uint64_t need = 0;
+    const ssu_status st = ssu_ssd_workspace_size(args->nchunks, args->heads, args->groups, args->dim, args->dstate,
+                                                 args->chunk_size, &need);
+    if (st != SSU_OK) return st;
+    if (need > ssu::kSsdStaticScratchBytes)
+        return fail(SSU_ERR_INVALID, "the call needs %llu bytes of workspace; the library's scratch holds %llu",
+                    (unsigned long long)need, (unsigned long long)ssu::kSsdStaticScratchBytes);
+    if (args->nchunks == 0 || args->tokens == 0) return ssu_ssd_prefill(args, stream);
+    void *scratch = nullptr;
+    const cudaError_t e = ssu::ssd_static_scratch(&scratch);
+    if (e != cudaSuccess) return fail(SSU_ERR_CUDA, "looking up the scratch failed: %s", cudaGetErrorString(e));
+    ssu_ssd_args a = *args;
+    a.workspace = scratch;
+    a.workspace_bytes = ssu::kSsdStaticScratchBytes;
+    return ssu_ssd_prefill(&a, stream);
+}
+
 ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate,
                               int32_t format, void *shadow, float *scale, void *stream) {
     if (!valid_dtype(state_dtype)) return fail(SSU_ERR_INVALID, "state_dtype %d is not an ssu_dtype", state_dtype);

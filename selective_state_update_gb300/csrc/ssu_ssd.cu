@@ -39,6 +39,7 @@
 //                fp32, since the two can cancel for every dim row of a token
 //                (both multiply x_t).
 #include <cstdint>
+#include <mutex>
 
 #include "ssu_device.cuh"
 #include "ssu_ssd_params.h"
@@ -423,7 +424,7 @@ constexpr int kCbThreads = 256;
 
 template <int Q, int N>
 __global__ void __launch_bounds__(kCbThreads) ssd_chunk_cb_kernel(const SsdParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<ChunkCbSmem<Q, N> *>(smem_raw);
     const int g = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
     const int64_t t0 = meta_at(p.cu_chunk, c, p.meta_i64), t1 = meta_at(p.cu_chunk, c + 1, p.meta_i64);
@@ -704,6 +705,33 @@ cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream) {
     case 256 * 1000 + 128: return launch_qpn<256, 64, 128>(p, stream);
     }
     return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// Library-owned scratch for ssu_ssd_prefill_static: the workspace of one call
+// (at most kSsdStaticScratchBytes), a file-scope device array, so that such a
+// call allocates nothing.  Nothing in it needs to start at zero: the kernels
+// write every part of the workspace before they read it.  Calls that overlap
+// in time share it and corrupt each other's results.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_ssd_scratch[kSsdStaticScratchBytes];
+
+cudaError_t ssd_static_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    static std::mutex lock;
+    static void *addr[kMaxDevices] = {};
+    std::lock_guard<std::mutex> guard(lock);
+    if (addr[dev] == nullptr) {  // once per device, with that device current
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_ssd_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 }  // namespace ssu

@@ -29,4 +29,10 @@ struct SsdParams {
 };
 cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream);
 
+// The library-owned workspace of ssu_ssd_prefill_static on the current
+// device: kSsdStaticScratchBytes at *ptr (looked up once per device).
+constexpr size_t kSsdStaticScratchBytes = size_t(64) << 20;
+constexpr int kMaxDevices = 64;
+cudaError_t ssd_static_scratch(void **ptr);
+
 }  // namespace ssu
