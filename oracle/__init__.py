@@ -106,6 +106,24 @@ class _ReplayProblem(ctypes.Structure):
     ]
 
 
+class _VerifyProblem(ctypes.Structure):
+    _fields_ = [
+        ("slots", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64),
+        ("dstate", ctypes.c_int64), ("groups", ctypes.c_int64),
+        ("state_dtype", ctypes.c_int32), ("io_dtype", ctypes.c_int32), ("dt_dtype", ctypes.c_int32),
+        ("dt_per_head", ctypes.c_int32),
+        ("ckpt_in", ctypes.c_void_p), ("ckpt_out", ctypes.c_void_p),
+        ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("B", ctypes.c_void_p),
+        ("C", ctypes.c_void_p), ("z", ctypes.c_void_p),
+        ("A", ctypes.c_void_p), ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("y", ctypes.c_void_p), ("y_exact", ctypes.c_void_p),
+        ("dt_softplus", ctypes.c_int32), ("pad_slot_id", ctypes.c_int64), ("batch", ctypes.c_int64),
+        ("ntok", ctypes.c_int64), ("slot_of", ctypes.c_void_p), ("len", ctypes.c_int64),
+        ("xbuf", ctypes.c_void_p), ("dtbuf", ctypes.c_void_p), ("Bbuf", ctypes.c_void_p),
+        ("count_in", ctypes.c_void_p), ("count_out", ctypes.c_void_p),
+    ]
+
+
 class _SsdProblem(ctypes.Structure):
     _fields_ = [
         ("tokens", ctypes.c_int64), ("heads", ctypes.c_int64), ("dim", ctypes.c_int64),
@@ -133,6 +151,8 @@ def load_library(path: str):
     lib.orc_ssu_run.restype = ctypes.c_int
     lib.orc_replay_run.argtypes = [ctypes.POINTER(_ReplayProblem), ctypes.c_char_p, ctypes.c_int]
     lib.orc_replay_run.restype = ctypes.c_int
+    lib.orc_replay_verify_run.argtypes = [ctypes.POINTER(_VerifyProblem), ctypes.c_char_p, ctypes.c_int]
+    lib.orc_replay_verify_run.restype = ctypes.c_int
     lib.orc_softplus.argtypes = [ctypes.c_double]
     lib.orc_softplus.restype = ctypes.c_double
     lib.orc_silu.argtypes = [ctypes.c_double]
@@ -354,6 +374,53 @@ def replay(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tenso
         raise OracleError(rc, err.value.decode())
     return ReplayResult(ckpt=c_out, y=y, y_exact=y_exact, xbuf=xb, dtbuf=db, Bbuf=Bb, count=cout, shadow=sh,
                         shadow_scale=sc)
+
+
+def replay_verify(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                  C: torch.Tensor, xbuf: torch.Tensor, dtbuf: torch.Tensor, Bbuf: torch.Tensor, count: torch.Tensor,
+                  D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                  dt_bias: Optional[torch.Tensor] = None, dt_softplus: bool = False,
+                  slot_of: Optional[torch.Tensor] = None, pad_slot_id: int = -1, lib=None) -> ReplayResult:
+    """Speculative decoding on the checkpoint + buffer form (article
+    "ReplaySSM", section 投机解码回滚) on the host: x ``[batch, T, heads, dim]``,
+    dt ``[batch, T, heads, dim]`` (or ``[batch, T, heads]``), B, C ``[batch, T,
+    groups, dstate]``; the other arguments as for :func:`replay`.  Returns the
+    drafts' outputs ``[batch, T, heads, dim]``, the checkpoints and buffers
+    after the call and the committed count (the drafts are appended but not
+    committed).  Inputs are not modified."""
+    lib = lib or _load()
+    c_in = _cpu(ckpt)
+    slots, heads, dim, dstate = c_in.shape
+    batch, T = x.shape[0], x.shape[1]
+    groups = B.shape[2]
+    L = xbuf.shape[1]
+    c_out = c_in.clone()
+    xs, dts, Bs, Cs, zs = _cpu(x), _cpu(dt), _cpu(B), _cpu(C), _cpu(z)
+    As = _cpu(A).to(torch.float32)
+    Ds = None if D is None else _cpu(D).to(torch.float32)
+    bs = None if dt_bias is None else _cpu(dt_bias).to(torch.float32)
+    xb, db, Bb = _cpu(xbuf).clone(), _cpu(dtbuf).to(torch.float32).clone(), _cpu(Bbuf).clone()
+    cin = _cpu(count).to(torch.int64)
+    cout = torch.zeros(batch, dtype=torch.int64)
+    so = None if slot_of is None else _cpu(slot_of).to(torch.int64)
+    y = torch.empty((batch, T, heads, dim), dtype=x.dtype)
+    y_exact = torch.empty((batch, T, heads, dim), dtype=torch.float64)
+    if Bs.dtype != xs.dtype or Cs.dtype != xs.dtype or xb.dtype != xs.dtype or Bb.dtype != xs.dtype:
+        raise ValueError("B, C and the x / B buffers must have the io dtype")
+    pr = _VerifyProblem(
+        slots=slots, heads=heads, dim=dim, dstate=dstate, groups=groups,
+        state_dtype=_DTYPE_CODE[c_in.dtype], io_dtype=_DTYPE_CODE[xs.dtype], dt_dtype=_DTYPE_CODE[dts.dtype],
+        dt_per_head=int(dts.dim() == 3), ckpt_in=c_in.data_ptr(), ckpt_out=c_out.data_ptr(),
+        x=xs.data_ptr(), dt=dts.data_ptr(), B=Bs.data_ptr(), C=Cs.data_ptr(), z=_ptr(zs),
+        A=As.data_ptr(), D=_ptr(Ds), dt_bias=_ptr(bs), y=y.data_ptr(), y_exact=y_exact.data_ptr(),
+        dt_softplus=int(bool(dt_softplus)), pad_slot_id=int(pad_slot_id), batch=batch, ntok=T,
+        slot_of=_ptr(so), len=L, xbuf=xb.data_ptr(), dtbuf=db.data_ptr(), Bbuf=Bb.data_ptr(),
+        count_in=cin.data_ptr(), count_out=cout.data_ptr())
+    err = ctypes.create_string_buffer(512)
+    rc = lib.orc_replay_verify_run(ctypes.byref(pr), err, 512)
+    if rc != OK:
+        raise OracleError(rc, err.value.decode())
+    return ReplayResult(ckpt=c_out, y=y, y_exact=y_exact, xbuf=xb, dtbuf=db, Bbuf=Bb, count=cout)
 
 
 def shadow_refresh(state: torch.Tensor, shadow_format: int, lib=None):

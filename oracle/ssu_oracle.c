@@ -157,7 +157,10 @@ double orc_decode(uint32_t bits, int dtype)
         memcpy(&f, &bits, sizeof f);
         return (double)f;
     }
-    return load_elem(&(uint16_t){(uint16_t)bits}, 0, dtype);
+    if (dtype != ORC_F16 && dtype != ORC_BF16)
+        return 0.0; /* 64-bit values do not fit the 32 bits */
+    const uint16_t h = (uint16_t)bits;
+    return load_elem(&h, 0, dtype);
 }
 
 uint32_t orc_encode(double v, int dtype)
@@ -649,6 +652,150 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
                 if (pr->y_exact != NULL)
                     pr->y_exact[xi] = y;
                 store_elem(pr->y, xi, pr->io_dtype, y);
+            }
+        }
+    }
+    free(owner);
+    free(S);
+    return ORC_OK;
+}
+
+
+/* ------------------------------------------------------------------------ */
+/* Speculative decoding on the checkpoint + buffer form (article            */
+/* "ReplaySSM", section 投机解码回滚): the drafts go into the buffer after    */
+/* the committed entries and each draft's output is read from the state     */
+/* through it (causal mask); commit is the caller moving the count.  The    */
+/* outputs are computed by running the recurrence in double from the        */
+/* checkpoint through the entries, which the unrolled form only reorders.   */
+/* Readings: the flush fires when c + 2T >= L (the article's rule, one      */
+/* window early) and happens before the drafts are appended; the drafts     */
+/* read the checkpoint as stored after it; every step, the drafts' own      */
+/* included, uses its processed dt' as stored in fp32 (what a later fold    */
+/* will see); a pad slot is a zero state with no history.                   */
+/* ------------------------------------------------------------------------ */
+int orc_replay_verify_run(const orc_verify_problem *pr, char *err, int errlen)
+{
+    const int64_t H = pr->heads, P = pr->dim, N = pr->dstate, G = pr->groups, Lb = pr->len, T = pr->ntok;
+    if (H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G != 0 || Lb < 1 || T < 1 || T > Lb) {
+        set_err(err, errlen, "bad shape: len=%lld drafts=%lld", Lb, T);
+        return ORC_INVALID;
+    }
+    const int64_t heads_per_group = H / G;
+    int64_t *owner = malloc(sizeof(int64_t) * (size_t)pr->slots);
+    double *S = malloc(sizeof(double) * (size_t)N);
+    if (!owner || !S) {
+        free(owner); free(S);
+        return ORC_INVALID;
+    }
+    for (int64_t s = 0; s < pr->slots; ++s)
+        owner[s] = -1;
+    int rc = ORC_OK;
+    for (int64_t b = 0; b < pr->batch && rc == ORC_OK; ++b) {
+        const int64_t slot = pr->slot_of ? pr->slot_of[b] : b;
+        if (slot == pr->pad_slot_id)
+            continue;
+        if (slot < 0 || slot >= pr->slots) {
+            set_err(err, errlen, "slot %lld of sequence %lld out of range", slot, b);
+            rc = ORC_INVALID;
+        } else if (owner[slot] != -1) {
+            set_err(err, errlen, "slot %lld is used by two sequences (second: %lld)", slot, b);
+            rc = ORC_ALIASING;
+        } else if (pr->count_in[b] < 0 || pr->count_in[b] >= Lb) {
+            set_err(err, errlen, "committed count %lld of sequence %lld not in [0, L)", pr->count_in[b], b);
+            rc = ORC_INVALID;
+        } else {
+            owner[slot] = b;
+        }
+    }
+    if (rc != ORC_OK) {
+        free(owner); free(S);
+        return rc;
+    }
+    const size_t es = pr->io_dtype == ORC_F32 ? 4 : 2;
+    for (int64_t b = 0; b < pr->batch; ++b) {
+        const int64_t slot = pr->slot_of ? pr->slot_of[b] : b;
+        const int pad = slot == pr->pad_slot_id;
+        const int64_t c_in = pad ? 0 : pr->count_in[b];
+        const int fold = !pad && c_in + 2 * T >= Lb;
+        const int64_t c = fold ? 0 : c_in;
+        pr->count_out[b] = c;
+        /* First every head's fold (the drafts' B, shared by a group, will
+         * overwrite the entries the other heads of the group fold). */
+        for (int64_t h = 0; fold && h < H; ++h) {
+            const int64_t g = h / heads_per_group;
+            const double A = (double)pr->A[h];
+            for (int64_t p = 0; p < P; ++p) {
+                const int64_t row = (slot * H + h) * P + p;
+                for (int64_t n = 0; n < N; ++n)
+                    S[n] = load_elem(pr->ckpt_in, row * N + n, pr->state_dtype);
+                for (int64_t j = 0; j < c_in; ++j) {
+                    const int64_t e = ((slot * Lb + j) * H + h) * P + p;
+                    const double dj = (double)pr->dtbuf[e];
+                    const double xj = load_elem(pr->xbuf, e, pr->io_dtype);
+                    const double aj = exp(A * dj);
+                    const int64_t be = ((slot * Lb + j) * G + g) * N;
+                    for (int64_t n = 0; n < N; ++n)
+                        S[n] = S[n] * aj + dj * xj * load_elem(pr->Bbuf, be + n, pr->io_dtype);
+                }
+                for (int64_t n = 0; n < N; ++n)
+                    store_elem(pr->ckpt_out, row * N + n, pr->state_dtype, S[n]);
+            }
+        }
+        /* Then the drafts: from the checkpoint as stored and the committed
+         * entries (none after a fold), each read out after its own step and
+         * appended as entry c + k. */
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t g = h / heads_per_group;
+            const double A = (double)pr->A[h];
+            const double Dh = pr->D ? (double)pr->D[h] : 0.0;
+            const double bias = pr->dt_bias ? (double)pr->dt_bias[h] : 0.0;
+            for (int64_t p = 0; p < P; ++p) {
+                const int64_t row = (slot * H + h) * P + p;
+                for (int64_t n = 0; n < N; ++n)
+                    S[n] = pad ? 0.0 : load_elem(fold ? pr->ckpt_out : pr->ckpt_in, row * N + n, pr->state_dtype);
+                for (int64_t j = 0; j < c; ++j) {
+                    const int64_t e = ((slot * Lb + j) * H + h) * P + p;
+                    const double dj = (double)pr->dtbuf[e];
+                    const double xj = load_elem(pr->xbuf, e, pr->io_dtype);
+                    const double aj = exp(A * dj);
+                    const int64_t be = ((slot * Lb + j) * G + g) * N;
+                    for (int64_t n = 0; n < N; ++n)
+                        S[n] = S[n] * aj + dj * xj * load_elem(pr->Bbuf, be + n, pr->io_dtype);
+                }
+                for (int64_t k = 0; k < T; ++k) {
+                    const int64_t r = b * T + k;
+                    const int64_t xi = (r * H + h) * P + p;
+                    const int64_t dti = pr->dt_per_head ? (r * H + h) : xi;
+                    double d = load_elem(pr->dt, dti, pr->dt_dtype) + bias;
+                    if (pr->dt_softplus)
+                        d = orc_softplus(d);
+                    d = (double)(float)d;  /* the step as stored */
+                    const double xv = load_elem(pr->x, xi, pr->io_dtype);
+                    const int64_t bc = (r * G + g) * N;
+                    const double a = exp(A * d);
+                    double y = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        S[n] = S[n] * a + d * xv * load_elem(pr->B, bc + n, pr->io_dtype);
+                        y += S[n] * load_elem(pr->C, bc + n, pr->io_dtype);
+                    }
+                    y += Dh * xv;
+                    if (pr->z != NULL)
+                        y *= orc_silu(load_elem(pr->z, xi, pr->io_dtype));
+                    if (pr->y_exact != NULL)
+                        pr->y_exact[xi] = y;
+                    store_elem(pr->y, xi, pr->io_dtype, y);
+                    if (!pad) {  /* draft k becomes entry c + k */
+                        const int64_t e = ((slot * Lb + c + k) * H + h) * P + p;
+                        memcpy((char *)pr->xbuf + (size_t)e * es, (const char *)pr->x + (size_t)xi * es, es);
+                        pr->dtbuf[e] = (float)d;
+                        if (h % heads_per_group == 0 && p == 0) {
+                            const int64_t be = ((slot * Lb + c + k) * G + g) * N;
+                            memcpy((char *)pr->Bbuf + (size_t)be * es, (const char *)pr->B + (size_t)bc * es,
+                                   es * (size_t)N);
+                        }
+                    }
+                }
             }
         }
     }

@@ -131,6 +131,48 @@ double orc_e4m3_decode(uint8_t code);
 
 int orc_replay_run(const orc_replay_problem *problem, char *err, int errlen);
 
+/* Speculative decoding on the checkpoint + buffer form (article "ReplaySSM:
+ * Cache SSM Inputs, Not State", section 投机解码回滚).  Each sequence brings
+ * T draft tokens: x, z [batch, T, heads, dim]; dt [batch, T, heads, dim] (or
+ * [batch, T, heads] with dt_per_head); B, C [batch, T, groups, dstate]; y
+ * [batch, T, heads, dim].  With c = count_in[b] committed entries:
+ *   - if c + 2T >= L the c entries are first folded into the checkpoint
+ *     (written back once, in state_dtype) and c becomes 0 -- the flush one
+ *     window early, so that the next step always has T free entries;
+ *   - the drafts are appended as entries c .. c+T-1 (x and B keep their bits,
+ *     the processed step is stored in fp32);
+ *   - draft k's output is read from the state after entries 0 .. c+k, i.e.
+ *     the checkpoint as stored, the committed entries and drafts 0 .. k in
+ *     order (causal mask), with every step's dt' as stored in fp32;
+ *   - count_out[b] = c: nothing is committed; the caller advances the count
+ *     by the accepted prefix, and later entries are simply overwritten.
+ * A pad slot has no history and no checkpoint: zero state, the drafts only,
+ * nothing written, count 0.  The other fields mean what they mean for
+ * orc_replay_run (no read copy). */
+typedef struct {
+    int64_t slots, heads, dim, dstate, groups;
+    int32_t state_dtype, io_dtype, dt_dtype;
+    int32_t dt_per_head;
+    const void *ckpt_in;            /* [slots, heads, dim, dstate] checkpoints, read only        */
+    void *ckpt_out;                 /* same shape; caller fills it with ckpt_in first            */
+    const void *x, *dt, *B, *C, *z; /* the drafts, see above                                     */
+    const float *A, *D, *dt_bias;
+    void *y;                        /* [batch, T, heads, dim] io dtype                            */
+    double *y_exact;                /* [batch, T, heads, dim] or NULL                             */
+    int32_t dt_softplus;
+    int64_t pad_slot_id;
+    int64_t batch, ntok;            /* sequences, drafts per sequence (T >= 1, T <= L)            */
+    const int64_t *slot_of;         /* [batch] slot of each sequence; NULL: slot b                */
+    int64_t len;                    /* buffer length L                                            */
+    void *xbuf;                     /* [slots, L, heads, dim] io dtype, in/out                    */
+    float *dtbuf;                   /* [slots, L, heads, dim] fp32 processed steps, in/out         */
+    void *Bbuf;                     /* [slots, L, groups, dstate] io dtype, in/out                */
+    const int64_t *count_in;        /* [batch] committed entries (0 <= c < L)                     */
+    int64_t *count_out;             /* [batch] committed entries after the call                   */
+} orc_verify_problem;
+
+int orc_replay_verify_run(const orc_verify_problem *problem, char *err, int errlen);
+
 double orc_softplus(double v);
 double orc_silu(double z);
 double orc_decode(uint32_t bits, int dtype);

@@ -978,6 +978,153 @@ def pin_ssd_dt_limit(lib):
     _close(r.states[-1].numpy(), want, rtol=1e-12, atol=1e-15, what="dt_limit closed form")
 
 
+def _verify_scenario(seed, L, T, counts, heads=4, dim=3, dstate=8, groups=2, io=torch.bfloat16,
+                     state_dtype=torch.float64, with_z=True, pad_last=False):
+    """The replay scenario with T draft tokens per sequence instead of one."""
+    sc = _replay_scenario(seed, L, counts, heads, dim, dstate, groups, io, state_dtype, with_z, pad_last)
+    g = torch.Generator().manual_seed(seed + 1000)
+    nseq = len(counts)
+    sc["x"] = torch.randn((nseq, T, heads, dim), generator=g).to(io)
+    sc["dt"] = torch.rand((nseq, T, heads, dim), generator=g) * 0.3 - 1.0   # softplus(dt - 0.5) ~ 0.2 .. 0.3
+    sc["B"] = torch.randn((nseq, T, groups, dstate), generator=g).to(io)
+    sc["C"] = torch.randn((nseq, T, groups, dstate), generator=g).to(io)
+    sc["z"] = torch.randn((nseq, T, heads, dim), generator=g).to(io) if with_z else None
+    sc["bias"] = torch.full((heads,), 0.5)
+    return sc
+
+
+def _run_verify(sc, lib):
+    return oracle.replay_verify(sc["ckpt"], sc["x"], sc["dt"], sc["A"], sc["B"], sc["C"], sc["xbuf"], sc["dtbuf"],
+                                sc["Bbuf"], sc["count"], D=sc["D"], z=sc["z"], dt_bias=sc["bias"], dt_softplus=True,
+                                slot_of=sc["slot_of"], lib=lib)
+
+
+def _draft_steps(sc, b):
+    """The drafts' processed steps as the buffer stores them: fp32 of
+    softplus(dt + bias)."""
+    d = np.logaddexp(0.0, f64(sc["dt"][b]) + f64(sc["bias"])[None, :, None])
+    return torch.from_numpy(d).to(torch.float32)
+
+
+def _plain_verify_history(sc, b, ndrafts, lib, extra=None):
+    """Sequence b token by token by the plain update from its checkpoint: its
+    committed entries, then drafts 0 .. ndrafts-1, then `extra` = (x, dt', B,
+    C, z) of one more token; processed steps as dt, softplus off."""
+    s = int(sc["slot_of"][b])
+    c = int(sc["count"][b])
+    d = _draft_steps(sc, b)
+    xs = [sc["xbuf"][s, :c], sc["x"][b, :ndrafts]]
+    dts = [sc["dtbuf"][s, :c], d[:ndrafts]]
+    Bs = [sc["Bbuf"][s, :c], sc["B"][b, :ndrafts]]
+    Cs = [sc["C"][b, :1].expand(c, -1, -1), sc["C"][b, :ndrafts]]
+    zs = None if sc["z"] is None else [sc["z"][b, :1].expand(c, -1, -1), sc["z"][b, :ndrafts]]
+    if extra is not None:
+        xs.append(extra[0]); dts.append(extra[1]); Bs.append(extra[2]); Cs.append(extra[3])
+        if zs is not None:
+            zs.append(extra[4])
+    n = c + ndrafts + (1 if extra is not None else 0)
+    tab = torch.full((1, n), s, dtype=torch.int64)
+    return oracle.ssu(sc["ckpt"], torch.cat(xs), torch.cat(dts), sc["A"], torch.cat(Bs), torch.cat(Cs), D=sc["D"],
+                      z=None if zs is None else torch.cat(zs), read=oracle.Table.of(tab),
+                      cu_seqlens=torch.tensor([0, n]), lib=lib)
+
+
+def pin_verify_lossless(lib):
+    """Speculative decoding on checkpoint + buffer is lossless: draft k's y
+    equals the plain recurrence over the committed entries and drafts
+    0 .. k; the flush fires exactly when c + 2T >= L, leaving in the
+    checkpoint the state after the committed entries, and nothing is
+    committed (count = c, or 0 after the flush)."""
+    L, T = 9, 3
+    counts = [0, 1, 2, 3, 4, 8, 0]    # c + 2T >= 9 from c = 3 on
+    sc = _verify_scenario(61, L, T, counts)
+    r = _run_verify(sc, lib)
+    for b, c in enumerate(counts):
+        h = _plain_verify_history(sc, b, T, lib)
+        for k in range(T):
+            _close(r.y_exact[b, k].numpy(), h.y_exact[c + k].numpy(), rtol=1e-11, atol=1e-12,
+                   what=f"draft {k} y (c={c})")
+        s = int(sc["slot_of"][b])
+        fold = c + 2 * T >= L
+        if fold:
+            hc = _plain_verify_history(sc, b, 0, lib) if c > 0 else None
+            want = f64(sc["ckpt"][s]) if hc is None else f64(hc.state[s])
+            _close(f64(r.ckpt[s]), want, rtol=1e-11, atol=1e-13, what=f"flushed checkpoint (c={c})")
+            if int(r.count[b]) != 0:
+                raise AssertionError("a flush leaves no committed entry")
+        else:
+            if not torch.equal(r.ckpt[s], sc["ckpt"][s]):
+                raise AssertionError("a step without flush must not write the checkpoint")
+            if int(r.count[b]) != c:
+                raise AssertionError("verification commits nothing")
+
+
+def pin_verify_entries(lib):
+    """The drafts are appended as entries c .. c+T-1 (0 .. T-1 after a flush):
+    x and B with their bits, the processed step in fp32; the committed
+    entries below c are untouched."""
+    L, T = 8, 2
+    counts = [1, 3, 5]                 # the last flushes (5 + 4 >= 8)
+    sc = _verify_scenario(62, L, T, counts)
+    r = _run_verify(sc, lib)
+    for b, c in enumerate(counts):
+        s = int(sc["slot_of"][b])
+        at = 0 if c + 2 * T >= L else c
+        if not torch.equal(r.xbuf[s, at:at + T], sc["x"][b]) or not torch.equal(r.Bbuf[s, at:at + T], sc["B"][b]):
+            raise AssertionError(f"appended drafts (c={c})")
+        if not torch.equal(r.dtbuf[s, at:at + T], _draft_steps(sc, b)):
+            raise AssertionError("appended processed steps")
+        if at and not (torch.equal(r.xbuf[s, :c], sc["xbuf"][s, :c]) and torch.equal(r.Bbuf[s, :c], sc["Bbuf"][s, :c])):
+            raise AssertionError("committed entries changed")
+
+
+def pin_verify_rollback(lib):
+    """Rollback is moving the count: after verifying T drafts and accepting
+    the first a, the next plain replay step (count = c + a) gives the y of
+    the plain recurrence over the committed entries, drafts 0 .. a-1 and the
+    new token -- the rejected drafts leave no trace."""
+    L, T = 12, 3
+    counts = [0, 2, 4]
+    sc = _verify_scenario(63, L, T, counts)
+    r = _run_verify(sc, lib)
+    g = torch.Generator().manual_seed(64)
+    heads, dim = sc["x"].shape[2], sc["x"].shape[3]
+    groups, dstate = sc["B"].shape[2], sc["B"].shape[3]
+    for a in range(T + 1):
+        nx = torch.randn((len(counts), heads, dim), generator=g).to(sc["x"].dtype)
+        nd = torch.rand((len(counts), heads, dim), generator=g) * 0.3
+        nB = torch.randn((len(counts), groups, dstate), generator=g).to(sc["x"].dtype)
+        nC = torch.randn((len(counts), groups, dstate), generator=g).to(sc["x"].dtype)
+        nz = torch.randn((len(counts), heads, dim), generator=g).to(sc["x"].dtype)
+        step = oracle.replay(r.ckpt, nx, nd, sc["A"], nB, nC, r.xbuf, r.dtbuf, r.Bbuf, r.count + a, D=sc["D"], z=nz,
+                             slot_of=sc["slot_of"], lib=lib)
+        for b in range(len(counts)):
+            h = _plain_verify_history(sc, b, a, lib,
+                                      extra=(nx[b:b + 1], nd[b:b + 1], nB[b:b + 1], nC[b:b + 1], nz[b:b + 1]))
+            _close(step.y_exact[b].numpy(), h.y_exact[counts[b] + a].numpy(), rtol=1e-11, atol=1e-12,
+                   what=f"step after accepting {a} of {T} drafts (c={counts[b]})")
+
+
+def pin_verify_pad(lib):
+    """A pad slot: the drafts run from a zero state with no history (the
+    first draft's y is the zero-state closed form), nothing is written and
+    the count is 0."""
+    sc = _verify_scenario(65, 6, 2, [1, 2], with_z=False, pad_last=True)
+    r = _run_verify(sc, lib)
+    b = 1
+    gi = np.arange(sc["x"].shape[2]) // (sc["x"].shape[2] // sc["B"].shape[2])
+    d = _draft_steps(sc, b)[0].double().numpy()
+    xn = f64(sc["x"][b, 0])
+    bc = np.einsum("hn,hn->h", f64(sc["B"][b, 0])[gi], f64(sc["C"][b, 0])[gi])
+    _close(r.y_exact[b, 0].numpy(), d * bc[:, None] * xn + f64(sc["D"])[:, None] * xn, what="pad draft y")
+    if not torch.equal(r.ckpt, sc["ckpt"]) or int(r.count[b]) != 0:
+        raise AssertionError("a pad sequence writes nothing and keeps no entry")
+    s0 = int(sc["slot_of"][0])
+    untouched = [s for s in range(sc["ckpt"].shape[0]) if s != s0]
+    if not torch.equal(r.xbuf[untouched], sc["xbuf"][untouched]):
+        raise AssertionError("a pad sequence must not append")
+
+
 ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero, pin_zero_state,
             pin_A_zero, pin_decay_only, pin_unrolled, pin_basis_vectors, pin_group_map,
             pin_page_examples, pin_pad_never_written, pin_disable_and_untouched, pin_table_forms,
@@ -985,4 +1132,5 @@ ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero,
             pin_replay_lossless, pin_replay_buffer_entries, pin_replay_buffer_len_one,
             pin_replay_pad_and_aliasing, pin_empty_sequences, pin_bounded_decay, pin_e4m3_codes,
             pin_shadow_refresh, pin_replay_read_copy, pin_ssd_equals_token_loop, pin_ssd_chunked_form,
-            pin_ssd_seq_idx_authority, pin_ssd_dt_limit]
+            pin_ssd_seq_idx_authority, pin_ssd_dt_limit, pin_verify_lossless, pin_verify_entries,
+            pin_verify_rollback, pin_verify_pad]

@@ -59,6 +59,18 @@ MUTATIONS = [
     ("ssd_seq_idx_ignored", "if (c == 0 || pr->seq_idx[c] != pr->seq_idx[c - 1]) {", "if (c == 0) {"),
     ("ssd_dt_limit_dropped", "d = fmin(fmax(d, pr->dt_lo), pr->dt_hi);", "d = d;"),
     ("ssd_initial_ignored", "S[n] = pr->initial_states\n", "S[n] = 0 && pr->initial_states\n"),
+    # speculative decoding on checkpoint + buffer
+    ("verify_late_flush", "const int fold = !pad && c_in + 2 * T >= Lb;", "const int fold = !pad && c_in + T >= Lb;"),
+    ("verify_commits_drafts", "        pr->count_out[b] = c;\n", "        pr->count_out[b] = c + T;\n"),
+    ("verify_append_at_start", "const int64_t e = ((slot * Lb + c + k) * H + h) * P + p;",
+     "const int64_t e = ((slot * Lb + k) * H + h) * P + p;"),
+    ("verify_y_before_step",
+     "S[n] = S[n] * a + d * xv * load_elem(pr->B, bc + n, pr->io_dtype);\n"
+     "                        y += S[n] * load_elem(pr->C, bc + n, pr->io_dtype);",
+     "y += S[n] * load_elem(pr->C, bc + n, pr->io_dtype);\n"
+     "                        S[n] = S[n] * a + d * xv * load_elem(pr->B, bc + n, pr->io_dtype);"),
+    ("verify_drafts_from_old_checkpoint", "load_elem(fold ? pr->ckpt_out : pr->ckpt_in, row * N + n",
+     "load_elem(pr->ckpt_in, row * N + n"),
     ("ssd_decay_after_input",
      "S[n] = S[n] * a + d * xv * load_elem(pr->B, (t * G + g) * N + n, pr->io_dtype);",
      "S[n] = (S[n] + d * xv * load_elem(pr->B, (t * G + g) * N + n, pr->io_dtype)) * a;"),
