@@ -91,7 +91,7 @@ typedef struct ssu_slot_table {
 #define SSU_DEV_BAD_SEQLEN 0x4  /* cu_seqlens decreasing, negative or past `rows`   */
 #define SSU_DEV_TIMEOUT    0x8  /* an asynchronous state copy did not complete in
                                    about a second; the unit was skipped           */
-#define SSU_DEV_BAD_COUNT  0x10 /* ssu_replay_update: a buffered count outside [0, L) */
+#define SSU_DEV_BAD_COUNT  0x10 /* replay / verify: a buffered count outside [0, L) */
 #define SSU_DEV_BAD_COPY   0x20 /* ssu_batch_copy: a copy longer than max_bytes      */
 
 /* Arguments of the MATE signature that this library does not implement.  Set
@@ -249,6 +249,34 @@ typedef struct ssu_replay_buffers {
  * launches nothing.
  */
 ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot_table *slots,
+                             const ssu_replay_buffers *rb, void *stream);
+
+/*
+ * Speculative decoding on the checkpoint + buffer form (article "ReplaySSM:
+ * Cache SSM Inputs, Not State", section 投机解码回滚).  Each of `batch`
+ * sequences brings `ntok` = T draft tokens: the row operands of `args` (x, dt,
+ * z, B, C, y) hold row b * T + k for draft k of sequence b.  With c =
+ * count_in[b] committed entries in the sequence's buffer:
+ *   c + 2T >= L  the committed entries are first folded into the checkpoint
+ *                (written once) and c becomes 0 -- the flush one window early,
+ *                so that the next step finds T free entries;
+ *   then         the drafts are appended as entries c .. c+T-1 (x and B keep
+ *                their bits, dt' = softplus?(dt + dt_bias) in fp32) and draft
+ *                k's y is the output after the checkpoint (as stored), the
+ *                committed entries and drafts 0 .. k in order (causal mask),
+ *                every step with its dt' as stored;
+ *   count_out[b] = c: nothing is committed.  Accepting the first a drafts is
+ *                setting the count to count_out[b] + a (later entries are
+ *                overwritten by later appends); no state is restored.
+ * A pad slot reads as a zero state with no history: y from the drafts alone,
+ * nothing written, count_out[b] = 0.  A count outside [0, L) sets
+ * SSU_DEV_BAD_COUNT and skips the sequence; bad table entries and slots set
+ * their bits as for ssu_replay_update.  1 <= T <= L; no read copy
+ * (rb->shadow_format must be SSU_SHADOW_NONE); disable_state_update must be
+ * 0; the dstate and dtype rules of ssu_update_onetoken apply.  Two kernel
+ * launches on `stream`; batch == 0 launches nothing.
+ */
+ssu_status ssu_replay_verify(const ssu_args *args, int64_t batch, int64_t ntok, const ssu_slot_table *slots,
                              const ssu_replay_buffers *rb, void *stream);
 
 /*

@@ -29,7 +29,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_shadow_refresh",
+__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_replay_verify", "ssu_shadow_refresh",
            "ssu_ssd_prefill", "ssu_ssd_prefill_static", "ssd_combined_fwd_varlen",
            "ssu_batch_copy", "copy_table",
            "slot_copies", "ssu_prewarm",
@@ -139,6 +139,9 @@ def lib():
         L.ssu_replay_update.argtypes = [p_args, ctypes.c_int64, p_tab, ctypes.POINTER(ReplayBuffers),
                                         ctypes.c_void_p]
         L.ssu_replay_update.restype = ctypes.c_int
+        L.ssu_replay_verify.argtypes = [p_args, ctypes.c_int64, ctypes.c_int64, p_tab, ctypes.POINTER(ReplayBuffers),
+                                        ctypes.c_void_p]
+        L.ssu_replay_verify.restype = ctypes.c_int
         L.ssu_batch_copy.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
                                      ctypes.c_void_p]
         L.ssu_batch_copy.restype = ctypes.c_int
@@ -371,6 +374,55 @@ def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
                        count_out.data_ptr(), fmt, 0, _ptr(shadow),
                        _ptr(shadow_scale) if fmt == SHADOW_E4M3 else None)
     rc = lib().ssu_replay_update(ctypes.byref(a), batch, None if rt is None else ctypes.byref(rt),
+                                 ctypes.byref(rb), _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    return out, count_out
+
+
+def ssu_replay_verify(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, count_out=None, D=None, z=None,
+                      dt_bias=None, dt_softplus=False, state_batch_indices=None, pad_slot_id=-1, out=None,
+                      status=None, stream=None):
+    """Speculative decoding on the checkpoint + buffer form (article "ReplaySSM",
+    section 投机解码回滚): x ``[batch, T, heads, dim]``, dt the same (or
+    ``[batch, T, heads]``), B, C ``[batch, T, groups, dstate]``, z like x; the
+    checkpoints and buffers as for :func:`ssu_replay_update`.  The drafts are
+    appended after the ``count_in`` committed entries and verified; returns
+    ``(y [batch, T, heads, dim], count_out)`` with count_out the committed
+    entries (the flush, when it fires, leaves 0).  Accepting the first ``a``
+    drafts of sequence b is ``count[b] = count_out[b] + a``."""
+    _need(x.dim() == 4 and B.dim() == 4, "x must be [batch, T, heads, dim], B [batch, T, groups, dstate]")
+    batch, T = x.shape[0], x.shape[1]
+    if dt.dim() == 3:
+        dt = dt.unsqueeze(-1).expand(*dt.shape, x.shape[-1])
+    if out is None:
+        out = torch.empty_like(x)
+    if count_out is None:
+        count_out = torch.empty_like(count_in)
+    slots, heads, dim, dstate = state.shape
+    for name, t in (("x", x), ("out", out)) + ((("z", z),) if z is not None else ()):
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+    _need(B.is_contiguous() and C.is_contiguous(), "B and C must be contiguous")
+    _need(x_buf.dim() == 4 and x_buf.shape[0] == slots and tuple(x_buf.shape[2:]) == (heads, dim),
+          "x_buf must be [slots, L, heads, dim]")
+    L = x_buf.shape[1]
+    _need(x_buf.dtype == x.dtype and x_buf.is_contiguous(), "x_buf must be contiguous in x's dtype")
+    _need(tuple(dt_buf.shape) == tuple(x_buf.shape) and dt_buf.dtype == torch.float32 and dt_buf.is_contiguous(),
+          "dt_buf must be a contiguous fp32 tensor shaped like x_buf")
+    _need(B_buf.dim() == 4 and tuple(B_buf.shape) == (slots, L, B.shape[2], dstate) and B_buf.dtype == x.dtype
+          and B_buf.is_contiguous(), "B_buf must be [slots, L, groups, dstate], contiguous, in x's dtype")
+    for t in (count_in, count_out):
+        _need(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and t.numel() >= batch,
+              "counts must be contiguous int32 CUDA tensors with one entry per sequence")
+    _need(all(t.is_cuda for t in (x_buf, dt_buf, B_buf)), "buffers must be CUDA tensors")
+    rows = batch * T
+    flat = lambda t: None if t is None else t.reshape(rows, *t.shape[2:])
+    a = _args(state, flat(x), flat(dt), A, flat(B), flat(C), D, flat(z), dt_bias, dt_softplus, pad_slot_id,
+              flat(out), False, status, 0)
+    rt = _table(state_batch_indices, SLOTS_STRIDED)
+    rb = ReplayBuffers(L, x_buf.data_ptr(), dt_buf.data_ptr(), B_buf.data_ptr(), count_in.data_ptr(),
+                       count_out.data_ptr(), SHADOW_NONE, 0, None, None)
+    rc = lib().ssu_replay_verify(ctypes.byref(a), batch, T, None if rt is None else ctypes.byref(rt),
                                  ctypes.byref(rb), _stream(stream))
     if rc != OK:
         _raise(rc)

@@ -9,6 +9,7 @@
 
 #include "ssu_internal.h"
 #include "ssu_ssd_params.h"
+#include "ssu_verify.h"
 
 namespace {
 
@@ -251,6 +252,41 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
         kp.shadow_scale = rb->shadow_scale;
     }
     return launched(ssu::launch_replay(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
+}
+
+ssu_status ssu_replay_verify(const ssu_args *args, int64_t batch, int64_t ntok, const ssu_slot_table *slots,
+                             const ssu_replay_buffers *rb, void *stream) {
+    ssu::KParams kp;
+    int lanes = 0;
+    if (batch < 0) return fail(SSU_ERR_INVALID, "batch is negative");
+    if (ntok < 1) return fail(SSU_ERR_INVALID, "ntok must be at least 1");
+    ssu_status st = prepare(args, batch * ntok, slots, nullptr, &kp, &lanes);
+    if (st != SSU_OK) return st;
+    if (args->disable_state_update) return fail(SSU_ERR_INVALID, "disable_state_update is not defined for verification");
+    if (rb == nullptr) return fail(SSU_ERR_INVALID, "replay buffers are NULL");
+    if (rb->len < 1 || rb->len > ssu::kMaxReplayLen)
+        return fail(SSU_ERR_UNSUPPORTED, "buffer length %lld is not supported (1..%d)", (long long)rb->len,
+                    ssu::kMaxReplayLen);
+    if (ntok > rb->len) return fail(SSU_ERR_INVALID, "ntok (%lld) exceeds the buffer length (%lld)", (long long)ntok,
+                                    (long long)rb->len);
+    if (rb->reserved0 != 0) return fail(SSU_ERR_INVALID, "replay buffers: reserved0 must be 0");
+    if (rb->shadow_format != SSU_SHADOW_NONE)
+        return fail(SSU_ERR_UNSUPPORTED, "verification does not read a low-precision copy");
+    if (batch == 0) return ok();
+    if (!rb->x || !rb->dt || !rb->B || !rb->count_in || !rb->count_out)
+        return fail(SSU_ERR_INVALID, "replay buffers and counts must not be NULL");
+    if (rb->count_out == rb->count_in) return fail(SSU_ERR_INVALID, "count_out must not alias count_in");
+    if (args->heads > 65535 || batch > kMaxGrid) return fail(SSU_ERR_INVALID, "too many heads or sequences");
+    kp.nseq = batch;
+    kp.rows = batch * ntok;
+    kp.rlen = static_cast<int32_t>(rb->len);
+    kp.xbuf = rb->x;
+    kp.dtbuf = rb->dt;
+    kp.Bbuf = rb->B;
+    kp.cnt_in = rb->count_in;
+    kp.cnt_out = rb->count_out;
+    return launched(ssu::launch_verify(args->state_dtype, kp, batch, static_cast<int>(ntok),
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes, int32_t *d_status,

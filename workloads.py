@@ -74,7 +74,7 @@ class Workload:
 
     @property
     def nseq(self) -> int:
-        if self.kind in ("onetoken", "replay"):
+        if self.kind in ("onetoken", "replay", "verify"):
             return self.rows
         if self.cu_seqlens is not None:
             return self.cu_seqlens.numel() - 1
@@ -307,6 +307,28 @@ def replay_problem(seed: int, *, slots: int = 16, heads: int = 4, dim: int = 8, 
     w = Workload(f"replay_{seed}", "replay", state, x, dt, A, B, C, D=D, z=z, dt_bias=dt_bias,
                  dt_softplus=dt_softplus, read=read, pad_slot_id=pad_slot_id, xbuf=xbuf, dtbuf=dtbuf, Bbuf=Bbuf,
                  count=count, meta={"buffer_len": buffer_len})
+    return w.to(device)
+
+
+def verify_problem(seed: int, *, ntok: int = 2, buffer_len: int = 8, **kw) -> Workload:
+    """A small seeded problem for speculative decoding on the checkpoint +
+    buffer form: replay_problem's pool, buffers and counts (U{0..L-1}) with
+    ``ntok`` draft tokens per sequence -- x, z, dt ``[nseq, T, heads, dim]``,
+    B, C ``[nseq, T, groups, dstate]`` -- drawn as the one-token inputs."""
+    device = kw.pop("device", "cpu")
+    w = replay_problem(seed, buffer_len=buffer_len, **kw)
+    nseq, heads, dim = w.x.shape
+    groups, dstate = w.B.shape[1], w.B.shape[2]
+    g = _gen(seed + 7, "cpu")
+    io = w.x.dtype
+    x = _normal((nseq, ntok, heads, dim), g, "cpu", dtype=io)
+    z = _normal((nseq, ntok, heads, dim), g, "cpu", dtype=io) if w.z is not None else None
+    dt = (_normal((nseq, ntok, heads, dim), g, "cpu") if w.dt_softplus
+          else _uniform((nseq, ntok, heads, dim), g, "cpu", 0.0, 0.2))
+    B = _normal((nseq, ntok, groups, dstate), g, "cpu", dtype=io)
+    C = _normal((nseq, ntok, groups, dstate), g, "cpu", dtype=io)
+    w = replace(w, name=f"verify_{seed}", kind="verify", x=x, z=z, dt=dt, B=B, C=C,
+                meta=dict(w.meta, ntok=ntok))
     return w.to(device)
 
 
