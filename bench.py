@@ -56,6 +56,10 @@ DESCRIPTIONS = {
                                 "fold read the copy, folds rewrite it",
     "copy_slots_b256_fp32": "256 whole-slot state copies of 4 MiB (heads 128, dim 64, dstate 128, fp32) between "
                             "random disjoint slot sets of a 512-slot pool; steps alternate the direction",
+    "verify_b256_t4_fp32": "speculative decoding on the checkpoint + buffer form (ReplaySSM), batch 256, 4 drafts "
+                           "per sequence, heads 128, dim 64, dstate 128, groups 8, fp32 checkpoints (512 slots, 13 "
+                           "pad entries), buffer length 16, sequence b holding (b + step) % 9 committed entries (the "
+                           "flush c + 2T >= L fires for 1/9 of the sequences each step)",
     "ssd_prefill_16k_bf16": "packed variable-length SSD prefill, 8 sequences of U{1024..3072} tokens (14269 in "
                             "all), heads 128, dim 64, dstate 128, groups 8, chunk 256, bf16 x/z/B/C/y, fp32 dt "
                             "with bias and softplus, D, fp32 initial and final states",
@@ -63,11 +67,14 @@ DESCRIPTIONS = {
 COPY_METRIC = "whole-slot state copies/s and achieved HBM GB/s (read + write)"
 COPY_UNIT = "copies/s"
 SSD_METRIC = "SSD prefill tokens/s and achieved HBM GB/s (inputs and outputs once)"
+VERIFY_METRIC = "verified draft tokens/s and achieved HBM GB/s"
+VERIFY_UNIT = "draft-tokens/s"
 SSD_UNIT = "tokens/s"
 KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"],
+                  "verify": ["ssu_verify.cu", "ssu_verify.h", "ssu_device.cuh", "ssu_internal.h"],
                   "ssd": ["ssu_ssd.cu", "ssu_ssd_params.h", "ssu_device.cuh", "ssu_internal.h"]}
 
 
@@ -512,6 +519,145 @@ def copy_oracle_rate(w_cpu, budget_s: float):
     return done / spent, f"{done} copies of {nbytes} bytes in {samples} samples"
 
 
+def verify_bytes(w, count) -> dict:
+    """Bytes one verification call must move: per non-pad sequence the
+    checkpoint once, its c committed entries, the drafts' inputs, outputs and
+    appended entries, and on a flush the checkpoint written once; pad
+    sequences only their drafts' inputs and outputs."""
+    batch, T, H, P = w.x.shape
+    G, N = w.B.shape[2], w.B.shape[3]
+    io = w.x.element_size()
+    sb = H * P * N * w.state.element_size()
+    entry = H * P * (io + 4) + G * N * io               # x, dt' and B of one buffered step
+    draft_in = H * P * (io * (2 if w.z is not None else 1) + w.dt.element_size()) + 2 * G * N * io
+    draft_out = H * P * io
+    L = w.xbuf.shape[1]
+    total = 0
+    for b in range(batch):
+        total += T * (draft_in + draft_out) + 4 + 4 + 4  # drafts, y, table entry and counts
+        if int(w.read[b]) == w.pad_slot_id:
+            continue
+        c = int(count[b])
+        total += sb + c * entry + T * entry
+        if c + 2 * T >= L:
+            total += sb
+    return {"total": total, "state_bytes_per_unit": sb}
+
+
+def run_verify(args, rank, world, device):
+    """The verification workload: one step = one ssu_replay_verify call over
+    the batch (its fold and verify launches); the committed counts cycle
+    through (b + step) % 9, arrays prepared before the timed region."""
+    from selective_state_update_gb300 import build as ssu_build
+    import selective_state_update_gb300 as ssu
+    ssu_build.build()
+    ssu.lib()
+    w = make_workload(args, device, seed_offset=97 * rank)
+    batch, T = w.x.shape[0], w.x.shape[1]
+    period = w.xbuf.shape[1] - 2 * T + 1
+    counts = [((torch.arange(batch, device=device) + k) % period).to(torch.int32) for k in range(period)]
+    count_out = torch.empty(batch, dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    out = torch.empty_like(w.x)
+
+    def call(i):
+        return ssu.ssu_replay_verify(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, counts[i % period],
+                                     count_out=count_out, D=w.D, z=w.z, dt_bias=w.dt_bias, dt_softplus=w.dt_softplus,
+                                     state_batch_indices=w.read, pad_slot_id=w.pad_slot_id, out=out, status=status)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    whole0, whole1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(device) as clocks:
+        whole0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            call(i)
+            ev[i][1].record(stream)
+        whole1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(whole0.elapsed_time(whole1), device)
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if int(status.item()) != 0:
+        raise SystemExit(f"ssu_replay_verify reported status {int(status.item())}")
+    acct = [verify_bytes(w, counts[k].cpu()) for k in range(period)]
+    algo = statistics.mean(a["total"] for a in acct)
+    # End to end: the drafts' inputs and the counts from pinned host memory,
+    # the call, y back to pinned host memory.
+    dev_in = [t for t in (w.x, w.dt, w.z, w.B, w.C) if t is not None]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_counts = [c.cpu().pin_memory() for c in counts]
+    host_y = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + batch * 4
+    d2h = host_y.numel() * host_y.element_size()
+    e2e_steps = max(3, min(args.steps, 400))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        for hsrc, d in zip(host_in, dev_in):
+            d.copy_(hsrc, non_blocking=True)
+        counts[i % period].copy_(host_counts[i % period], non_blocking=True)
+        call(i)
+        host_y.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, device)
+    peak, peak_src = hbm_peak()
+    achieved = algo / (call_ms * 1e-3) / 1e9
+    units = batch * T
+    return {
+        "metric": VERIFY_METRIC, "value": aggregate_rate(units, world, args.steps, total_ms), "unit": VERIFY_UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+                               + (f" (batch {args.batch})" if args.batch else ""),
+                   "sequences_per_gpu": batch, "drafts_per_sequence": T,
+                   "parallelism": f"{world} independent replicas (one pool and batch per GPU)",
+                   "l2": "no flush: %.2f GB of checkpoints read per step" % (algo / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("verify", args.workload),
+                     "algorithmic_bytes_per_launch": algo,
+                     "kernel": "verify call (ssu_verify_fold_kernel + ssu_verify_kernel)", "launch_ms": call_ms},
+        "e2e": {"value": aggregate_rate(units, world, e2e_steps, e2e_s * 1e3), "unit": VERIFY_UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
+def verify_oracle_rate(w_cpu, budget_s: float):
+    """The oracle's verification on samples of the workload: a few sequences
+    at a time (with their committed entries), all heads."""
+    import oracle
+    oracle.build()
+    batch, T = w_cpu.x.shape[0], w_cpu.x.shape[1]
+    done, spent, idx, per = 0, 0.0, 0, 2
+    while spent < budget_s:
+        seqs = [(idx + i) % batch for i in range(per)]
+        idx += per
+        sel = torch.tensor(seqs)
+        slots = w_cpu.read[sel].long()
+        keep = slots != w_cpu.pad_slot_id
+        used = slots[keep]
+        order = torch.cat([used, torch.tensor([s for s in range(w_cpu.state.shape[0]) if s not in set(used.tolist())][:1])])
+        remap = {int(s): i for i, s in enumerate(order.tolist())}
+        slot_of = torch.tensor([remap.get(int(s), -1) if k else -1 for s, k in zip(slots, keep)])
+        t0 = time.perf_counter()
+        oracle.replay_verify(w_cpu.state[order], w_cpu.x[sel], w_cpu.dt[sel], w_cpu.A, w_cpu.B[sel], w_cpu.C[sel],
+                             w_cpu.xbuf[order], w_cpu.dtbuf[order], w_cpu.Bbuf[order], w_cpu.count[sel], D=w_cpu.D,
+                             z=None if w_cpu.z is None else w_cpu.z[sel], dt_bias=w_cpu.dt_bias,
+                             dt_softplus=w_cpu.dt_softplus, slot_of=slot_of, pad_slot_id=-1)
+        spent += time.perf_counter() - t0
+        done += per * T
+    return done / spent, f"{done} draft tokens in samples of {per} sequences"
+
+
 def ssd_accounting(w) -> dict:
     """Bytes the prefill must move at least (every input read once, y and the
     returned states written once) and the tensor-core work of the chunked
@@ -737,7 +883,7 @@ def _oracle_call(sub):
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
          "varlen_fp16": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008,
-         "replay_f16copy_b256_fp32": 1009, "ssd_prefill_16k_bf16": 1010}
+         "replay_f16copy_b256_fp32": 1009, "ssd_prefill_16k_bf16": 1010, "verify_b256_t4_fp32": 1011}
 
 
 def make_workload(args, device, seed_offset=0):
@@ -745,7 +891,8 @@ def make_workload(args, device, seed_offset=0):
     kw = {}
     if args.batch is not None:
         if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
-                                 "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16"):
+                                 "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16",
+                                 "verify_b256_t4_fp32"):
             raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32, replay_b256_fp32, "
                              "copy_slots_b256_fp32 and ssd_prefill_16k_bf16 workloads only")
         kw["batch"] = args.batch
@@ -789,6 +936,17 @@ def run_reference(args):
     w_cpu = _cpu_workload(args)
     import oracle
     oracle.build()
+    if getattr(w_cpu, "kind", "") == "verify":
+        budget = min(150.0, 5.0 + 1.0 * (args.steps + args.warmup))
+        value, sample = verify_oracle_rate(w_cpu, budget)
+        return {
+            "impl": "reference", "metric": VERIFY_METRIC, "value": value, "unit": VERIFY_UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w_cpu.x.shape[0] * w_cpu.x.shape[1] / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "cpu_baseline": {"value": value, "unit": VERIFY_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": VERIFY_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
     if getattr(w_cpu, "kind", "") == "ssd":
         budget = min(150.0, 5.0 + 1.0 * (args.steps + args.warmup))
         value, sample = ssd_oracle_rate(w_cpu, budget)
@@ -871,9 +1029,14 @@ def main():
     cpu = None
     is_copy = args.workload.startswith("copy_")
     is_ssd = args.workload.startswith("ssd_")
+    is_verify = args.workload.startswith("verify_")
     if rank == 0 and not args.no_cpu_baseline:
         w_cpu = _cpu_workload(args)
-        if is_ssd:
+        if is_verify:
+            rate, desc = verify_oracle_rate(w_cpu, args.cpu_baseline_seconds)
+            cpu = {"value": rate, "unit": VERIFY_UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+        elif is_ssd:
             rate, desc = ssd_oracle_rate(w_cpu, args.cpu_baseline_seconds)
             cpu = {"value": rate, "unit": SSD_UNIT, "cores": 1, "kind": "oracle",
                    "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
@@ -894,7 +1057,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     device = torch.device("cuda", local_rank if world > 1 else torch.cuda.current_device())
     torch.cuda.set_device(device)
-    run = run_ssd if is_ssd else (run_copy if is_copy else run_ours)
+    run = run_verify if is_verify else (run_ssd if is_ssd else (run_copy if is_copy else run_ours))
     res = run(args, rank, world, device)
     res["cpu_baseline"] = cpu
     if rank == 0:

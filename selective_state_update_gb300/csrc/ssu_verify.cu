@@ -24,7 +24,8 @@
 // state carried through the window in registers reads the same bytes (the
 // checkpoint once, each entry once) and gives the drafts' outputs in order,
 // which at a few drafts per sequence needs no tensor cores.  Four threads
-// share a state row (dstate / 4 columns each).
+// share a state row (dstate / 4 columns each, in interleaved groups of four);
+// the entries' and drafts' operands are staged in shared memory once per CTA.
 #include <cstdint>
 
 #include "ssu_device.cuh"
@@ -58,44 +59,139 @@ __device__ __forceinline__ bool verify_sequence(const KParams &p, int64_t b, int
     return true;
 }
 
-// One buffered entry j applied to this thread's NPT columns of row `row`.
+// Shared-memory staging of one CTA: the buffered entries' B (fp32, per
+// entry) and their x, dt' for the CTA's 64 rows; the drafts' B, C and x, dt,
+// z for the rows.  Everything is loaded once, cooperatively and coalesced,
+// before the state walks through it.
+struct VerifyStage {
+    float *eB;   // [L][N]
+    float *ex;   // [L][64]
+    float *ed;   // [L][64]
+    float *dB;   // [T][N]
+    float *dC;   // [T][N]
+    float *dx;   // [T][64]
+    float *dd;   // [T][64] processed steps
+    float *dz;   // [T][64]
+};
+
+__host__ __device__ inline size_t verify_smem_bytes(int L, int T, int N) {
+    return sizeof(float) * (static_cast<size_t>(L) * N + 2 * L * kVerifyRows + 2 * static_cast<size_t>(T) * N +
+                            3 * T * kVerifyRows);
+}
+
+__device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, int N) {
+    VerifyStage st;
+    st.eB = smem;
+    st.ex = st.eB + L * N;
+    st.ed = st.ex + L * kVerifyRows;
+    st.dB = st.ed + L * kVerifyRows;
+    st.dC = st.dB + T * N;
+    st.dx = st.dC + T * N;
+    st.dd = st.dx + T * kVerifyRows;
+    st.dz = st.dd + T * kVerifyRows;
+    return st;
+}
+
+// Entries 0 .. c-1 of (slot, head h, group g) for rows row0 .. row0+63.
+__device__ __forceinline__ void stage_entries(const KParams &p, const VerifyStage &st, int64_t slot, int c, int h,
+                                              int g, int row0) {
+    for (int i = threadIdx.x; i < c * p.N; i += kVerifyThreads) {
+        const int j = i / p.N, n = i % p.N;
+        st.eB[j * p.N + n] = load_small(p.Bbuf, ((slot * p.rlen + j) * p.G + g) * static_cast<int64_t>(p.N) + n,
+                                        p.io_dtype);
+    }
+    for (int i = threadIdx.x; i < c * kVerifyRows; i += kVerifyThreads) {
+        const int j = i / kVerifyRows, r = i % kVerifyRows, row = row0 + r;
+        if (row >= p.P) continue;
+        const int64_t e = ((slot * p.rlen + j) * p.H + h) * static_cast<int64_t>(p.P) + row;
+        st.ed[j * kVerifyRows + r] = p.dtbuf[e];
+        st.ex[j * kVerifyRows + r] = load_small(p.xbuf, e, p.io_dtype);
+    }
+}
+
+// Columns of a row: thread q of the row's four owns the groups of four
+// columns 16 i + 4 q .. + 3 (i < NPT / 4), so that the four threads read
+// neighbouring 16-byte pieces.
+__device__ __forceinline__ int col_of(int i4, int q) { return 16 * i4 + 4 * q; }
+
+// The committed entries applied to this thread's columns of its row.
 template <int NPT>
-__device__ __forceinline__ void apply_entry(const KParams &p, int64_t slot, int j, int h, int g, int row, int q,
-                                            float Ah, float *s) {
-    const int64_t e = ((slot * p.rlen + j) * p.H + h) * static_cast<int64_t>(p.P) + row;
-    const float dj = p.dtbuf[e];
-    const float dA = decay(Ah, dj);
-    const float dx = dj * load_small(p.xbuf, e, p.io_dtype);
-    const int64_t be = ((slot * p.rlen + j) * p.G + g) * static_cast<int64_t>(p.N) + q * NPT;
+__device__ __forceinline__ void apply_entries(const KParams &p, const VerifyStage &st, int c, int r, int q, float Ah,
+                                              float *s) {
+    for (int j = 0; j < c; ++j) {
+        const float dj = st.ed[j * kVerifyRows + r];
+        const float dA = decay_inline(Ah, dj);
+        const float dx = dj * st.ex[j * kVerifyRows + r];
+        const float *Bj = st.eB + j * p.N;
 #pragma unroll
-    for (int i = 0; i < NPT; ++i) s[i] = fmaf(s[i], dA, dx * load_small(p.Bbuf, be + i, p.io_dtype));
+        for (int i4 = 0; i4 < NPT / 4; ++i4) {
+            const float4 bv = *reinterpret_cast<const float4 *>(Bj + col_of(i4, q));
+            s[4 * i4] = fmaf(s[4 * i4], dA, dx * bv.x);
+            s[4 * i4 + 1] = fmaf(s[4 * i4 + 1], dA, dx * bv.y);
+            s[4 * i4 + 2] = fmaf(s[4 * i4 + 2], dA, dx * bv.z);
+            s[4 * i4 + 3] = fmaf(s[4 * i4 + 3], dA, dx * bv.w);
+        }
+    }
+}
+
+// This thread's columns of a state row (`row` points at the row's start).
+template <typename TS, int NPT>
+__device__ __forceinline__ void load_state_part(const TS *row, int q, float *s) {
+#pragma unroll
+    for (int i4 = 0; i4 < NPT / 4; ++i4) {
+        const TS *src = row + col_of(i4, q);
+        if constexpr (sizeof(TS) == 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src);
+            s[4 * i4] = v.x, s[4 * i4 + 1] = v.y, s[4 * i4 + 2] = v.z, s[4 * i4 + 3] = v.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[4 * i4 + e] = to_float(src[e]);
+        }
+    }
 }
 
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads) ssu_verify_fold_kernel(const KParams p, int T) {
+__device__ __forceinline__ void store_state_part(TS *row, int q, const float *s) {
+#pragma unroll
+    for (int i4 = 0; i4 < NPT / 4; ++i4) {
+        TS *dst = row + col_of(i4, q);
+        if constexpr (sizeof(TS) == 4) {
+            *reinterpret_cast<float4 *>(dst) = make_float4(s[4 * i4], s[4 * i4 + 1], s[4 * i4 + 2], s[4 * i4 + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) store_ts(dst + e, s[4 * i4 + e]);
+        }
+    }
+}
+
+template <typename TS, int NPT>
+__global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(const KParams p, int T) {
+    extern __shared__ __align__(16) float vsmem[];
     const int64_t b = blockIdx.x;
-    const int h = blockIdx.y, g = h / p.heads_per_group;
-    const int row = blockIdx.z * kVerifyRows + threadIdx.x / 4, q = threadIdx.x & 3;
+    const int h = blockIdx.y, g = h / p.heads_per_group, row0 = blockIdx.z * kVerifyRows;
+    const int r = threadIdx.x / 4, row = row0 + r, q = threadIdx.x & 3;
     int64_t slot;
     int c;
     bool pad;
     if (!verify_sequence(p, b, &slot, &c, &pad)) return;  // flagged (again) by the verify launch
-    if (pad || c + 2 * T < p.rlen || row >= p.P) return;   // no flush here
-    TS *srow = static_cast<TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N + q * NPT;
+    if (pad || c + 2 * T < p.rlen) return;                 // no flush here
+    const VerifyStage st = verify_stage(vsmem, p.rlen, T, p.N);
+    stage_entries(p, st, slot, c, h, g, row0);
+    __syncthreads();
+    if (row >= p.P) return;
+    TS *srow = static_cast<TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N;
     float s[NPT];
-#pragma unroll
-    for (int i = 0; i < NPT; ++i) s[i] = to_float(srow[i]);
-    const float Ah = p.A[h];
-    for (int j = 0; j < c; ++j) apply_entry<NPT>(p, slot, j, h, g, row, q, Ah, s);
-#pragma unroll
-    for (int i = 0; i < NPT; ++i) store_ts(srow + i, s[i]);
+    load_state_part<TS, NPT>(srow, q, s);
+    apply_entries<NPT>(p, st, c, r, q, p.A[h], s);
+    store_state_part<TS, NPT>(srow, q, s);
 }
 
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads) ssu_verify_kernel(const KParams p, int T) {
+__global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KParams p, int T) {
+    extern __shared__ __align__(16) float vsmem[];
     const int64_t b = blockIdx.x;
-    const int h = blockIdx.y, g = h / p.heads_per_group;
-    const int row = blockIdx.z * kVerifyRows + threadIdx.x / 4, q = threadIdx.x & 3;
+    const int h = blockIdx.y, g = h / p.heads_per_group, row0 = blockIdx.z * kVerifyRows;
+    const int r = threadIdx.x / 4, row = row0 + r, q = threadIdx.x & 3;
     const bool active = row < p.P;  // the four threads of a row agree
     int64_t slot;
     int c;
@@ -104,41 +200,64 @@ __global__ void __launch_bounds__(kVerifyThreads) ssu_verify_kernel(const KParam
     const bool fold = !pad && c + 2 * T >= p.rlen;
     if (fold) c = 0;
     if (h == 0 && blockIdx.z == 0 && threadIdx.x == 0) p.cnt_out[b] = c;
-    // the checkpoint as stored (after the fold launch), then the committed entries
+    const VerifyStage st = verify_stage(vsmem, p.rlen, T, p.N);
+    // the state row part in flight while the entries and drafts are staged
     float s[NPT];
-    const TS *srow =
-        static_cast<const TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N + q * NPT;
+    const TS *srow = static_cast<const TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N;
+    if (pad || !active) {
 #pragma unroll
-    for (int i = 0; i < NPT; ++i) s[i] = (pad || !active) ? 0.f : to_float(srow[i]);
-    const float Ah = p.A[h];
+        for (int i = 0; i < NPT; ++i) s[i] = 0.f;
+    } else {
+        load_state_part<TS, NPT>(srow, q, s);
+    }
+    stage_entries(p, st, slot, c, h, g, row0);
     const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+    for (int i = threadIdx.x; i < T * p.N; i += kVerifyThreads) {
+        const int k = i / p.N, n = i % p.N;
+        const int64_t rr = b * T + k;
+        st.dB[k * p.N + n] = load_small(p.B, rr * p.Bs[0] + g * p.Bs[1] + n * p.Bs[2], p.io_dtype);
+        st.dC[k * p.N + n] = load_small(p.C, rr * p.Cs[0] + g * p.Cs[1] + n * p.Cs[2], p.io_dtype);
+    }
+    for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
+        const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
+        if (rrow >= p.P) continue;
+        const int64_t rr = b * T + k;
+        st.dd[k * kVerifyRows + rw] =
+            processed_step(load_small(p.dt, rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2], p.dt_dtype), bias,
+                           p.softplus);
+        st.dx[k * kVerifyRows + rw] = load_small(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2], p.io_dtype);
+        st.dz[k * kVerifyRows + rw] =
+            p.z ? load_small(p.z, rr * p.zs[0] + h * p.zs[1] + rrow * p.zs[2], p.io_dtype) : 0.f;
+    }
+    __syncthreads();
+    const float Ah = p.A[h];
     const float Dh = p.D ? p.D[h] : 0.f;
-    if (active)
-        for (int j = 0; j < c; ++j) apply_entry<NPT>(p, slot, j, h, g, row, q, Ah, s);
+    if (active) apply_entries<NPT>(p, st, c, r, q, Ah, s);
     // the drafts in order, each read out after its own step and appended
     for (int k = 0; k < T; ++k) {
-        const int64_t r = b * T + k;
-        float part = 0.f, d = 0.f, xv = 0.f;
+        const int64_t rr = b * T + k;
+        const float d = st.dd[k * kVerifyRows + r], xv = st.dx[k * kVerifyRows + r];
+        float part = 0.f;
         if (active) {
-            d = processed_step(load_small(p.dt, r * p.dts[0] + h * p.dts[1] + row * p.dts[2], p.dt_dtype), bias,
-                               p.softplus);
-            xv = load_small(p.x, r * p.xs[0] + h * p.xs[1] + row * p.xs[2], p.io_dtype);
-            const float dA = decay(Ah, d), dx = d * xv;
-            const int64_t bo = r * p.Bs[0] + g * p.Bs[1], co = r * p.Cs[0] + g * p.Cs[1];
+            const float dA = decay_inline(Ah, d), dx = d * xv;
+            const float *Bk = st.dB + k * p.N, *Ck = st.dC + k * p.N;
 #pragma unroll
-            for (int i = 0; i < NPT; ++i) {
-                const int n = q * NPT + i;
-                s[i] = fmaf(s[i], dA, dx * load_small(p.B, bo + n * p.Bs[2], p.io_dtype));
-                part = fmaf(s[i], load_small(p.C, co + n * p.Cs[2], p.io_dtype), part);
+            for (int i4 = 0; i4 < NPT / 4; ++i4) {
+                const float4 bv = *reinterpret_cast<const float4 *>(Bk + col_of(i4, q));
+                const float4 cv = *reinterpret_cast<const float4 *>(Ck + col_of(i4, q));
+                const float bb[4] = {bv.x, bv.y, bv.z, bv.w}, cc[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s[4 * i4 + e] = fmaf(s[4 * i4 + e], dA, dx * bb[e]);
+                    part = fmaf(s[4 * i4 + e], cc[e], part);
+                }
             }
         }
         const float sum = row_sum<4>(part);
         if (!active) continue;
-        if (q == 0) {
-            const float z = p.z ? load_small(p.z, r * p.zs[0] + h * p.zs[1] + row * p.zs[2], p.io_dtype) : 0.f;
-            store_small(p.y, r * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
-                        output(sum, Dh, xv, silu_gate(z, p.z != nullptr)));
-        }
+        if (q == 0)
+            store_small(p.y, rr * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
+                        output(sum, Dh, xv, silu_gate(st.dz[k * kVerifyRows + r], p.z != nullptr)));
         if (pad) continue;
         const int64_t e = ((slot * p.rlen + c + k) * p.H + h) * static_cast<int64_t>(p.P) + row;
         if (q == 0) {  // x keeps its bits, the processed step is stored in fp32
@@ -146,19 +265,20 @@ __global__ void __launch_bounds__(kVerifyThreads) ssu_verify_kernel(const KParam
                 static_cast<float *>(p.xbuf)[e] = xv;
             else
                 static_cast<unsigned short *>(p.xbuf)[e] =
-                    static_cast<const unsigned short *>(p.x)[r * p.xs[0] + h * p.xs[1] + row * p.xs[2]];
+                    static_cast<const unsigned short *>(p.x)[rr * p.xs[0] + h * p.xs[1] + row * p.xs[2]];
             p.dtbuf[e] = d;
         }
         if (h % p.heads_per_group == 0 && row == 0) {  // B once per group: the first head's first row
-            const int64_t be = ((slot * p.rlen + c + k) * p.G + g) * static_cast<int64_t>(p.N) + q * NPT;
-            const int64_t bo = r * p.Bs[0] + g * p.Bs[1];
-#pragma unroll
+            const int64_t be = ((slot * p.rlen + c + k) * p.G + g) * static_cast<int64_t>(p.N);
+            const int64_t bo = rr * p.Bs[0] + g * p.Bs[1];
+#pragma unroll 1
             for (int i = 0; i < NPT; ++i) {
-                const int64_t src = bo + (q * NPT + i) * p.Bs[2];
+                const int n = col_of(i / 4, q) + i % 4;
+                const int64_t src = bo + n * p.Bs[2];
                 if (p.io_dtype == kF32)
-                    static_cast<float *>(p.Bbuf)[be + i] = static_cast<const float *>(p.B)[src];
+                    static_cast<float *>(p.Bbuf)[be + n] = static_cast<const float *>(p.B)[src];
                 else
-                    static_cast<unsigned short *>(p.Bbuf)[be + i] = static_cast<const unsigned short *>(p.B)[src];
+                    static_cast<unsigned short *>(p.Bbuf)[be + n] = static_cast<const unsigned short *>(p.B)[src];
             }
         }
     }
@@ -168,10 +288,19 @@ template <typename TS, int NPT>
 static cudaError_t launch_verify_t(const KParams &p, int64_t batch, int T, cudaStream_t stream) {
     const dim3 grid(static_cast<unsigned>(batch), static_cast<unsigned>(p.H),
                     static_cast<unsigned>((p.P + kVerifyRows - 1) / kVerifyRows));
-    ssu_verify_fold_kernel<TS, NPT><<<grid, kVerifyThreads, 0, stream>>>(p, T);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    ssu_verify_kernel<TS, NPT><<<grid, kVerifyThreads, 0, stream>>>(p, T);
+    const size_t smem = verify_smem_bytes(p.rlen, T, p.N);
+    cudaError_t e;
+    if (smem > 48 * 1024) {
+        if ((e = cudaFuncSetAttribute(ssu_verify_fold_kernel<TS, NPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem))) != cudaSuccess)
+            return e;
+        if ((e = cudaFuncSetAttribute(ssu_verify_kernel<TS, NPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem))) != cudaSuccess)
+            return e;
+    }
+    ssu_verify_fold_kernel<TS, NPT><<<grid, kVerifyThreads, smem, stream>>>(p, T);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ssu_verify_kernel<TS, NPT><<<grid, kVerifyThreads, smem, stream>>>(p, T);
     return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
-"""bench.py's byte and flop accounting for the SSD prefill, against counts
-worked out by hand for a one-chunk problem (CPU only)."""
+"""bench.py's byte and flop accounting (SSD prefill, speculative verification), against counts
+worked out by hand for small problems (CPU only)."""
 import bench
+import torch
 import workloads
 
 
@@ -31,3 +32,19 @@ def test_ssd_accounting_ragged_tiles():
     causal = (16 + 32) * 16
     assert a["flops"] == 2 * 17 * 8 * 16 * 2 + 2 * causal * 16 + 2 * causal * 8
     assert a["outputs"] == 17 * 8 * 2 + 8 * 16 * 4
+
+
+def test_verify_bytes_by_hand():
+    # 3 sequences, T = 2, L = 6, heads 2, dim 4, dstate 8, groups 1, bf16 io, fp32 pool;
+    # counts 0 (no flush), 2 (2 + 4 >= 6: flush), pad
+    w = workloads.verify_problem(5, ntok=2, buffer_len=6, nseq=3, slots=8, heads=2, dim=4, dstate=8, groups=1)
+    w.read = torch.tensor([1, 2, -1], dtype=torch.int32)
+    count = torch.tensor([0, 2, 0], dtype=torch.int32)
+    a = bench.verify_bytes(w, count)
+    sb = 2 * 4 * 8 * 4                     # one fp32 checkpoint
+    entry = 2 * 4 * (2 + 4) + 1 * 8 * 2    # x (bf16) + dt' (fp32) of every head row, B of the group
+    draft_in = 2 * 4 * (2 * 2 + 4) + 2 * 8 * 2   # x, z (bf16), dt (fp32); B, C (bf16)
+    draft_out = 2 * 4 * 2
+    per_seq = 2 * (draft_in + draft_out) + 12
+    want = 3 * per_seq + (sb + 0 + 2 * entry) + (sb + 2 * entry + 2 * entry + sb)
+    assert a["total"] == want

@@ -274,6 +274,28 @@ def replay_f16copy_b256_fp32(device="cpu", seed=1009, batch=256, buffer_len=16) 
     return w
 
 
+def verify_b256_t4_fp32(device="cpu", seed=1011, batch=256, buffer_len=16, ntok=4) -> Workload:
+    """Speculative decoding on the checkpoint + buffer form at batch 256: the
+    b256_fp32 shapes and distributions (fp32 checkpoints, 512 slots, 13 pad
+    entries), a buffer of 16 entries, 4 drafts per sequence; sequence b holds
+    b % 9 committed entries, so the flush (c + 2T >= L, i.e. c = 8) fires for
+    1/9 of the sequences."""
+    heads, dim, dstate, groups, pad = 128, 64, 128, 8, 0
+    slots = 2 * batch
+    g = _gen(seed, device)
+    inp = _decode_inputs(g, device, batch * ntok, heads, dim, dstate, groups, torch.bfloat16)
+    for k in ("x", "z", "dt", "B", "C"):
+        inp[k] = inp[k].view(batch, ntok, *inp[k].shape[1:])
+    state = _pool(g, device, slots, heads, dim, dstate, torch.float32)
+    xbuf, dtbuf, Bbuf = _replay_buffers(g, device, slots, buffer_len, heads, dim, dstate, groups, torch.bfloat16)
+    gh = _gen(seed + 7, "cpu")
+    read, _ = _distinct_tables_with_pad(gh, batch, slots, pad, max(1, round(0.05 * batch)), device)
+    count = (torch.arange(batch, dtype=torch.int32) % (buffer_len - 2 * ntok + 1)).to(device)
+    return Workload("verify_b256_t4_fp32", "verify", state, dt_softplus=True, read=read, pad_slot_id=pad,
+                    xbuf=xbuf, dtbuf=dtbuf, Bbuf=Bbuf, count=count, meta={"buffer_len": buffer_len, "ntok": ntok},
+                    **inp)
+
+
 def replay_problem(seed: int, *, slots: int = 16, heads: int = 4, dim: int = 8, dstate: int = 16,
                    groups: int = 2, nseq: int = 4, buffer_len: int = 4, state_dtype=torch.float32,
                    io_dtype=torch.bfloat16, with_D: bool = True, with_z: bool = True, with_bias: bool = True,
@@ -558,5 +580,6 @@ NAMED = {
     "replay_e4m3_b256_fp32": replay_e4m3_b256_fp32,
     "replay_f16copy_b256_fp32": replay_f16copy_b256_fp32,
     "copy_slots_b256_fp32": copy_slots_b256_fp32,
+    "verify_b256_t4_fp32": verify_b256_t4_fp32,
     "ssd_prefill_16k_bf16": ssd_prefill_16k_bf16,
 }
