@@ -276,7 +276,8 @@ ssu_status ssu_replay_verify(const ssu_args *args, int64_t batch, int64_t ntok, 
     if (!rb->x || !rb->dt || !rb->B || !rb->count_in || !rb->count_out)
         return fail(SSU_ERR_INVALID, "replay buffers and counts must not be NULL");
     if (rb->count_out == rb->count_in) return fail(SSU_ERR_INVALID, "count_out must not alias count_in");
-    if (args->heads > 65535 || batch > kMaxGrid) return fail(SSU_ERR_INVALID, "too many heads or sequences");
+    if (args->heads > 65535 || batch > kMaxGrid || (args->dim + 63) / 64 > 65535)
+        return fail(SSU_ERR_INVALID, "too many heads, sequences or dim rows for one launch");
     kp.nseq = batch;
     kp.rows = batch * ntok;
     kp.rlen = static_cast<int32_t>(rb->len);

@@ -215,3 +215,62 @@ def test_ssd_workspace_size_and_empty_call(libssu):
     # no chunks: nothing to do, nothing launched, no pointer looked at
     a = _ssd_args(nchunks=0, x=None, B=None, workspace=None)
     assert libssu.ssu_ssd_prefill(ctypes.byref(a), None) == ssu.OK
+
+
+def _replay_buffers(**kw):
+    rb = ssu.ReplayBuffers(len=8, x=4096, dt=8192, B=12288, count_in=16384, count_out=16400)
+    for k, v in kw.items():
+        setattr(rb, k, v)
+    return rb
+
+
+@pytest.mark.parametrize("rb_kw,args_kw,code,needle", [
+    (dict(len=0), {}, ssu.ERR_UNSUPPORTED, "buffer length"),
+    (dict(len=33), {}, ssu.ERR_UNSUPPORTED, "buffer length"),
+    (dict(count_out=16384), {}, ssu.ERR_INVALID, "alias"),
+    (dict(x=None), {}, ssu.ERR_INVALID, "NULL"),
+    (dict(count_in=None), {}, ssu.ERR_INVALID, "NULL"),
+    (dict(reserved0=1), {}, ssu.ERR_INVALID, "reserved0"),
+    (dict(shadow_format=7, shadow=20480), {}, ssu.ERR_INVALID, "SSU_SHADOW"),
+    (dict(shadow_format=1, shadow=None), {}, ssu.ERR_INVALID, "read copy"),
+    ({}, dict(disable_state_update=1), ssu.ERR_INVALID, "disable_state_update"),
+])
+def test_replay_host_checks_reject_before_launch(libssu, rb_kw, args_kw, code, needle):
+    a, rb = _args(**args_kw), _replay_buffers(**rb_kw)
+    assert libssu.ssu_replay_update(ctypes.byref(a), 2, None, ctypes.byref(rb), None) == code
+    assert needle in libssu.ssu_last_error().decode()
+
+
+def test_replay_empty_call_and_missing_buffers(libssu):
+    a = _args()
+    assert libssu.ssu_replay_update(ctypes.byref(a), 2, None, None, None) == ssu.ERR_INVALID
+    assert libssu.ssu_replay_update(ctypes.byref(a), -1, None, ctypes.byref(_replay_buffers()), None) == ssu.ERR_INVALID
+    # nothing to do: no buffer pointer is looked at
+    rb = _replay_buffers(x=None, dt=None, B=None, count_in=None, count_out=None)
+    assert libssu.ssu_replay_update(ctypes.byref(a), 0, None, ctypes.byref(rb), None) == ssu.OK
+
+
+@pytest.mark.parametrize("ntok,rb_kw,args_kw,code,needle", [
+    (0, {}, {}, ssu.ERR_INVALID, "ntok"),
+    (9, {}, {}, ssu.ERR_INVALID, "exceeds the buffer length"),
+    (2, dict(len=33), {}, ssu.ERR_UNSUPPORTED, "buffer length"),
+    (2, dict(shadow_format=1, shadow=20480), {}, ssu.ERR_UNSUPPORTED, "low-precision copy"),
+    (2, dict(count_out=16384), {}, ssu.ERR_INVALID, "alias"),
+    (2, dict(B=None), {}, ssu.ERR_INVALID, "NULL"),
+    (2, dict(reserved0=3), {}, ssu.ERR_INVALID, "reserved0"),
+    (2, {}, dict(disable_state_update=1), ssu.ERR_INVALID, "disable_state_update"),
+    (2, {}, dict(groups=3), ssu.ERR_INVALID, "divisible"),
+])
+def test_verify_host_checks_reject_before_launch(libssu, ntok, rb_kw, args_kw, code, needle):
+    """ssu_replay_verify: T drafts must fit the buffer, no read copy, the
+    replay buffers' rules; all decided before any launch."""
+    a, rb = _args(**args_kw), _replay_buffers(**rb_kw)
+    assert libssu.ssu_replay_verify(ctypes.byref(a), 2, ntok, None, ctypes.byref(rb), None) == code
+    assert needle in libssu.ssu_last_error().decode()
+
+
+def test_verify_empty_call_launches_nothing(libssu):
+    a = _args()
+    rb = _replay_buffers(x=None, dt=None, B=None, count_in=None, count_out=None)
+    assert libssu.ssu_replay_verify(ctypes.byref(a), 0, 4, None, ctypes.byref(rb), None) == ssu.OK
+    assert libssu.ssu_replay_verify(ctypes.byref(a), -1, 4, None, ctypes.byref(rb), None) == ssu.ERR_INVALID
