@@ -41,6 +41,19 @@ __device__ __forceinline__ float load_small(const void *base, int64_t i, int dty
                          : bits_to_float(static_cast<const unsigned short *>(base)[i], dtype);
 }
 
+// Element i of an io-dtype array as its stored bits (16-bit types zero-extended).
+__device__ __forceinline__ uint32_t load_bits(const void *base, int64_t i, int dtype) {
+    return dtype == kF32 ? __float_as_uint(static_cast<const float *>(base)[i])
+                         : static_cast<const unsigned short *>(base)[i];
+}
+
+__device__ __forceinline__ void store_bits(void *base, int64_t i, int dtype, uint32_t v) {
+    if (dtype == kF32)
+        static_cast<uint32_t *>(base)[i] = v;
+    else
+        static_cast<unsigned short *>(base)[i] = static_cast<unsigned short>(v);
+}
+
 __device__ __forceinline__ void store_ts(float *o, float v) { *o = v; }
 __device__ __forceinline__ void store_ts(__half *o, float v) { *o = __float2half_rn(v); }
 __device__ __forceinline__ void store_ts(__nv_bfloat16 *o, float v) { *o = __float2bfloat16_rn(v); }
@@ -72,11 +85,13 @@ struct VerifyStage {
     float *dx;   // [T][64]
     float *dd;   // [T][64] processed steps
     float *dz;   // [T][64]
+    uint32_t *rB;  // [T][N] the drafts' B as stored bits, for the append
+    uint32_t *rx;  // [T][64] the drafts' x as stored bits
 };
 
 __host__ __device__ inline size_t verify_smem_bytes(int L, int T, int N) {
-    return sizeof(float) * (static_cast<size_t>(L) * N + 2 * L * kVerifyRows + 2 * static_cast<size_t>(T) * N +
-                            3 * T * kVerifyRows);
+    return sizeof(float) * (static_cast<size_t>(L) * N + 2 * L * kVerifyRows + 3 * static_cast<size_t>(T) * N +
+                            4 * T * kVerifyRows);
 }
 
 __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, int N) {
@@ -89,6 +104,8 @@ __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, i
     st.dx = st.dC + T * N;
     st.dd = st.dx + T * kVerifyRows;
     st.dz = st.dd + T * kVerifyRows;
+    st.rB = reinterpret_cast<uint32_t *>(st.dz + T * kVerifyRows);
+    st.rx = st.rB + T * N;
     return st;
 }
 
@@ -215,8 +232,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KPa
     for (int i = threadIdx.x; i < T * p.N; i += kVerifyThreads) {
         const int k = i / p.N, n = i % p.N;
         const int64_t rr = b * T + k;
-        st.dB[k * p.N + n] = load_small(p.B, rr * p.Bs[0] + g * p.Bs[1] + n * p.Bs[2], p.io_dtype);
+        const uint32_t bb = load_bits(p.B, rr * p.Bs[0] + g * p.Bs[1] + n * p.Bs[2], p.io_dtype);
         st.dC[k * p.N + n] = load_small(p.C, rr * p.Cs[0] + g * p.Cs[1] + n * p.Cs[2], p.io_dtype);
+        st.dB[k * p.N + n] = bits_to_float(bb, p.io_dtype);
+        st.rB[k * p.N + n] = bb;
     }
     for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
         const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
@@ -225,15 +244,37 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KPa
         st.dd[k * kVerifyRows + rw] =
             processed_step(load_small(p.dt, rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2], p.dt_dtype), bias,
                            p.softplus);
-        st.dx[k * kVerifyRows + rw] = load_small(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2], p.io_dtype);
+        const uint32_t xb = load_bits(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2], p.io_dtype);
+        st.dx[k * kVerifyRows + rw] = bits_to_float(xb, p.io_dtype);
+        st.rx[k * kVerifyRows + rw] = xb;
         st.dz[k * kVerifyRows + rw] =
             p.z ? load_small(p.z, rr * p.zs[0] + h * p.zs[1] + rrow * p.zs[2], p.io_dtype) : 0.f;
     }
     __syncthreads();
+    // The drafts become entries c .. c+T-1, written by the whole CTA from the
+    // stage before the state walk, so that the stores drain while it runs:
+    // x and B keep their bits, the processed step is stored in fp32; B once
+    // per group, by the group's first head.  No CTA reads these entries.
+    if (!pad) {
+        for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
+            const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
+            if (rrow >= p.P) continue;
+            const int64_t e = ((slot * p.rlen + c + k) * p.H + h) * static_cast<int64_t>(p.P) + rrow;
+            store_bits(p.xbuf, e, p.io_dtype, st.rx[i]);
+            p.dtbuf[e] = st.dd[i];
+        }
+        if (h % p.heads_per_group == 0 && blockIdx.z == 0) {
+            for (int i = threadIdx.x; i < T * p.N; i += kVerifyThreads) {
+                const int k = i / p.N, n = i % p.N;
+                store_bits(p.Bbuf, ((slot * p.rlen + c + k) * p.G + g) * static_cast<int64_t>(p.N) + n, p.io_dtype,
+                           st.rB[i]);
+            }
+        }
+    }
     const float Ah = p.A[h];
     const float Dh = p.D ? p.D[h] : 0.f;
     if (active) apply_entries<NPT>(p, st, c, r, q, Ah, s);
-    // the drafts in order, each read out after its own step and appended
+    // the drafts in order, each read out after its own step
     for (int k = 0; k < T; ++k) {
         const int64_t rr = b * T + k;
         const float d = st.dd[k * kVerifyRows + r], xv = st.dx[k * kVerifyRows + r];
@@ -258,29 +299,6 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KPa
         if (q == 0)
             store_small(p.y, rr * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
                         output(sum, Dh, xv, silu_gate(st.dz[k * kVerifyRows + r], p.z != nullptr)));
-        if (pad) continue;
-        const int64_t e = ((slot * p.rlen + c + k) * p.H + h) * static_cast<int64_t>(p.P) + row;
-        if (q == 0) {  // x keeps its bits, the processed step is stored in fp32
-            if (p.io_dtype == kF32)
-                static_cast<float *>(p.xbuf)[e] = xv;
-            else
-                static_cast<unsigned short *>(p.xbuf)[e] =
-                    static_cast<const unsigned short *>(p.x)[rr * p.xs[0] + h * p.xs[1] + row * p.xs[2]];
-            p.dtbuf[e] = d;
-        }
-        if (h % p.heads_per_group == 0 && row == 0) {  // B once per group: the first head's first row
-            const int64_t be = ((slot * p.rlen + c + k) * p.G + g) * static_cast<int64_t>(p.N);
-            const int64_t bo = rr * p.Bs[0] + g * p.Bs[1];
-#pragma unroll 1
-            for (int i = 0; i < NPT; ++i) {
-                const int n = col_of(i / 4, q) + i % 4;
-                const int64_t src = bo + n * p.Bs[2];
-                if (p.io_dtype == kF32)
-                    static_cast<float *>(p.Bbuf)[be + n] = static_cast<const float *>(p.B)[src];
-                else
-                    static_cast<unsigned short *>(p.Bbuf)[be + n] = static_cast<const unsigned short *>(p.B)[src];
-            }
-        }
     }
 }
 
