@@ -10,11 +10,14 @@ Entry points (same names as the C ABI):
   ssu_update_onetoken  one decode token per sequence
   ssu_replay_update    one decode token per sequence, state kept as a
                        checkpoint plus a buffer of recent inputs
+  ssu_replay_verify    speculative decoding on that form: T drafts per
+                       sequence appended and verified, nothing committed
   ssu_update_packed    packed variable-length / MTP rows (cu_seqlens) or the
                        dense [batch, steps, heads, dim] form
   ssu_shadow_refresh   the low-precision read copy of checkpoints
   ssu_ssd_prefill      packed variable-length SSD prefill (and
                        ssd_combined_fwd_varlen, the MATE-shaped call)
+  ssu_ssd_prefill_static  the same on the library's own device scratch
   ssu_batch_copy       batched state copies with memmove semantics
   ssu_prewarm          load a configuration's kernel before graph capture
 and ``selective_state_update``, the MATE/FlashInfer-shaped call (MATE
@@ -432,13 +435,22 @@ def ssu_replay_verify(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
 _SSD_WORKSPACE = {}
 
 
-def _ssd_workspace(device, nbytes: int) -> torch.Tensor:
-    """A per-device workspace that only grows (the "cached workspace" of the
-    MATE page): a steady-state call allocates nothing."""
-    key = str(device)
+def _ssd_workspace(device, nbytes: int, stream) -> torch.Tensor:
+    """A workspace per (device, stream) that only grows (the "cached
+    workspace" of the MATE page): a steady-state call allocates nothing, and
+    calls on different streams never share one.  It is allocated on the
+    stream the call runs on, so the caching allocator hands a replaced one
+    out again only after that stream's work on it."""
+    handle = _stream(stream)
+    key = (str(device), handle)
     ws = _SSD_WORKSPACE.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        if stream is None:  # the call runs on the current stream
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        else:
+            s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(handle, device=device)
+            with torch.cuda.stream(s):
+                ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _SSD_WORKSPACE[key] = ws
     return ws
 
@@ -472,7 +484,7 @@ def ssu_ssd_prefill(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, 
     rc = lib().ssu_ssd_workspace_size(nchunks, heads, groups, dim, dstate, chunk_size, ctypes.byref(nbytes))
     if rc != OK:
         _raise(rc)
-    ws = _ssd_workspace(x.device, nbytes.value)
+    ws = _ssd_workspace(x.device, nbytes.value, stream)
     hi = float(dt_limit[1])
     a = SsdArgs(tokens=tokens, heads=heads, dim=dim, dstate=dstate, groups=groups, nseq=nseq, nchunks=nchunks,
                 chunk_size=chunk_size, io_dtype=_DTYPE.get(x.dtype, -1), dt_dtype=_DTYPE[dt.dtype],
