@@ -893,8 +893,7 @@ def make_workload(args, device, seed_offset=0):
         if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
                                  "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16",
                                  "verify_b256_t4_fp32"):
-            raise SystemExit("--batch applies to the b256_fp32, mtp_64x7_fp32, replay_b256_fp32, "
-                             "copy_slots_b256_fp32 and ssd_prefill_16k_bf16 workloads only")
+            raise SystemExit(f"--batch does not apply to the {args.workload} workload")
         kw["batch"] = args.batch
     w = gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
     if getattr(w, "shadow", None) is not None and str(device) != "cpu":
