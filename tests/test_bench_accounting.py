@@ -48,3 +48,55 @@ def test_verify_bytes_by_hand():
     per_seq = 2 * (draft_in + draft_out) + 12
     want = 3 * per_seq + (sb + 0 + 2 * entry) + (sb + 2 * entry + 2 * entry + sb)
     assert a["total"] == want
+
+
+def _tiny(kind, rows, heads=2, dim=4, dstate=16, groups=1, slots=12, **kw):
+    """A hand-sized workload: fp32 pool, bf16 x/B/C, fp32 dt, A, no optional operands."""
+    return workloads.Workload(
+        name="tiny", kind=kind, state=torch.zeros(slots, heads, dim, dstate),
+        x=torch.zeros(rows, heads, dim, dtype=torch.bfloat16), dt=torch.zeros(rows, heads, dim),
+        A=torch.zeros(heads), B=torch.zeros(rows, groups, dstate, dtype=torch.bfloat16),
+        C=torch.zeros(rows, groups, dstate, dtype=torch.bfloat16), **kw)
+
+
+def test_onetoken_bytes_by_hand():
+    # 3 sequences: read [5, pad, 7], dst [pad, 2, 3]; a (slot, all heads) state is 2*4*16*4 B
+    w = _tiny("onetoken", 3, read=torch.tensor([5, -1, 7], dtype=torch.int32),
+              dst=torch.tensor([-1, 2, 3], dtype=torch.int32))
+    a = bench.algorithmic_bytes(w)
+    sb = 2 * 4 * 16 * 4
+    x = 3 * 2 * 4 * 2                                  # bf16 x, and y the same
+    small = x + 3 * 2 * 4 * 4 + 2 * (3 * 16 * 2) + 2 * 4 + 2 * 3 * 4 + x   # x, dt, B, C, A, tables, y
+    assert (a["seeds"], a["writes"]) == (2, 2)
+    assert a["state_read"] == 2 * sb and a["state_write"] == 2 * sb
+    assert a["small"] == small and a["total"] == 4 * sb + small
+
+
+def test_packed_bytes_by_hand():
+    # two sequences of 3 tokens (dense 2-D tables): seeds at max(acc-1, 0) = 1 and 0,
+    # one pad seed (sequence 1's entry 0), one pad destination
+    read = torch.tensor([[4, 9, 6], [-1, 8, 10]], dtype=torch.int32)
+    dst = torch.tensor([[1, 2, 3], [5, -1, 11]], dtype=torch.int32)
+    w = _tiny("packed", 6, read=read, dst=dst, dense_steps=3, num_accepted=torch.tensor([2, 1], dtype=torch.int32))
+    a = bench.algorithmic_bytes(w)
+    assert (a["seeds"], a["writes"]) == (1, 5)        # seq 0 seeds at slot 9; seq 1's seed entry is pad
+    w.disable_state_update = True
+    assert bench.algorithmic_bytes(w)["writes"] == 0
+
+
+def test_replay_bytes_by_hand():
+    # L = 4; counts [0, 3 (folds: 3 + 1 == L), 2, pad]; one (slot, entry) entry is
+    # x (bf16) + dt' (fp32) per head row and B per group
+    L, heads, dim, dstate, groups = 4, 2, 4, 16, 1
+    slots = 8
+    w = _tiny("replay", 4, heads=heads, dim=dim, dstate=dstate, groups=groups, slots=slots,
+              read=torch.tensor([1, 2, 3, -1], dtype=torch.int32),
+              xbuf=torch.zeros(slots, L, heads, dim, dtype=torch.bfloat16),
+              dtbuf=torch.zeros(slots, L, heads, dim), Bbuf=torch.zeros(slots, L, groups, dstate, dtype=torch.bfloat16),
+              count=torch.tensor([0, 3, 2, 0], dtype=torch.int32))
+    a = bench.algorithmic_bytes(w)
+    sb = heads * dim * dstate * 4
+    entry = heads * dim * (2 + 4) + groups * dstate * 2
+    assert a["folds"] == 1
+    assert a["state_read"] == 3 * sb + (0 + 3 + 2) * entry      # every live checkpoint, its entries
+    assert a["state_write"] == sb + 2 * entry                  # the fold's checkpoint, one entry each other
