@@ -100,3 +100,12 @@ def test_replay_bytes_by_hand():
     assert a["folds"] == 1
     assert a["state_read"] == 3 * sb + (0 + 3 + 2) * entry      # every live checkpoint, its entries
     assert a["state_write"] == sb + 2 * entry                  # the fold's checkpoint, one entry each other
+
+
+def test_threaded_oracle_rate_runs_the_oracle_on_several_threads():
+    """The CPU baseline on all host cores: the unchanged oracle on several
+    threads at once over one-sequence samples, a positive rate."""
+    w = workloads.b256_fp32(device="cpu", seed=1002, batch=6)
+    rate, desc = bench.oracle_rate_threaded(w, 0.5, 2)
+    assert rate > 0 and "on 2 threads" in desc
+    assert bench.host_threads() >= 1
