@@ -1088,11 +1088,15 @@ def main():
                    "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
             threads = host_threads()
             if threads > 1:
-                # all host cores, the single-core figure kept beside it
-                trate, tdesc = oracle_rate_threaded(w_cpu, args.cpu_baseline_seconds, threads)
-                cpu = {"value": trate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                       "sample": f"{tdesc} of {args.workload} (plain C, double precision)",
-                       "single_core": {"value": rate, "sample": cpu["sample"]}}
+                # all host cores, the single-core figure kept beside it; should the
+                # threaded run fail, the single-core figure stands and says why
+                try:
+                    trate, tdesc = oracle_rate_threaded(w_cpu, args.cpu_baseline_seconds, threads)
+                    cpu = {"value": trate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                           "sample": f"{tdesc} of {args.workload} (plain C, double precision)",
+                           "single_core": {"value": rate, "sample": cpu["sample"]}}
+                except Exception as e:  # noqa: BLE001 -- a baseline, not the measurement
+                    cpu["sample"] += f"; the {threads}-thread run failed: {type(e).__name__}: {e}"
         del w_cpu
 
     if not torch.cuda.is_available():
