@@ -15,17 +15,22 @@
 //            It runs on its own launch because the drafts' B, which a group
 //            of heads shares, takes the place of entries that the group's
 //            other heads fold.
-//   verify   one CTA per (sequence, head, 64 dim rows): the state is carried
-//            in registers from the checkpoint (as stored) through the
-//            committed entries and then the drafts, each draft's y read
-//            after its own step; the drafts are appended as entries
-//            c .. c+T-1 and count_out = c (nothing committed).
-// The page evaluates the drafts as two masked GEMMs over the window; the
-// state carried through the window in registers reads the same bytes (the
-// checkpoint once, each entry once) and gives the drafts' outputs in order,
-// which at a few drafts per sequence needs no tensor cores.  Four threads
-// share a state row (dstate / 4 columns each, in interleaved groups of four);
-// the entries' and drafts' operands are staged in shared memory once per CTA.
+//   verify   one CTA per (sequence, head, 64 dim rows): every draft is read
+//            out against the checkpoint (as stored) and the window, without
+//            forming a state; the drafts are appended as entries c .. c+T-1
+//            and count_out = c (nothing committed).
+// Readout of draft k, with M = c + k the last step it sees (steps m < c are
+// the committed entries, m >= c the drafts), a_m = exp(A dt'_m) and
+// g_{i:M} = a_i ... a_M (g_{M+1:M} = 1):
+//     y_k = g_{0:M} (S_ckpt . C_k) + sum_{m <= M} g_{m+1:M} dt'_m x_m (B_m . C_k) + D x_k
+// (the unrolled recurrence of section 核心做法; the causal mask is m <= M).
+// The page forms the two sums as masked GEMMs over the window; at a few
+// drafts per sequence they are T dot products per state row (S_ckpt . C_k)
+// and (c + T) x T dot products per CTA (B_m . C_k), then a walk over the
+// window per (row, draft) -- no tensor cores, and no state kept in registers
+// once the dots are taken.  Four threads share a state row (dstate / 4
+// columns each, in interleaved groups of four); the entries' and drafts'
+// operands are staged in shared memory once per CTA.
 #include <cstdint>
 
 #include "ssu_device.cuh"
@@ -61,10 +66,11 @@ __device__ __forceinline__ void store_ts(__nv_bfloat16 *o, float v) { *o = __flo
 // The sequence's slot, its committed count, and whether it is a pad slot;
 // false (flagged) for a bad table entry, slot or count.
 __device__ __forceinline__ bool verify_sequence(const KParams &p, int64_t b, int64_t *slot, int *c, bool *pad) {
+    const int cb = p.cnt_in[b];  // in flight beside the table lookup (count_in holds one entry per sequence)
     if (!table_slot(p, p.rd, b, 0, b, b, slot)) return false;
     if (!slot_ok(p, *slot)) return false;
     *pad = *slot == p.pad;
-    *c = *pad ? 0 : p.cnt_in[b];
+    *c = *pad ? 0 : cb;
     if (*c < 0 || *c >= p.rlen) {
         flag(p.status, kDevBadCount);
         return false;
@@ -87,11 +93,13 @@ struct VerifyStage {
     float *dz;   // [T][64]
     uint32_t *rB;  // [T][N] the drafts' B as stored bits, for the append
     uint32_t *rx;  // [T][64] the drafts' x as stored bits
+    float *bc;   // [c + T][T] B_m . C_k (entry m < c, else draft m - c)
+    float *us;   // [T][64] S_ckpt row . C_k
 };
 
 __host__ __device__ inline size_t verify_smem_bytes(int L, int T, int N) {
     return sizeof(float) * (static_cast<size_t>(L) * N + 2 * L * kVerifyRows + 3 * static_cast<size_t>(T) * N +
-                            4 * T * kVerifyRows);
+                            5 * T * kVerifyRows + static_cast<size_t>(L + T) * T);
 }
 
 __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, int N) {
@@ -106,6 +114,8 @@ __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, i
     st.dz = st.dd + T * kVerifyRows;
     st.rB = reinterpret_cast<uint32_t *>(st.dz + T * kVerifyRows);
     st.rx = st.rB + T * N;
+    st.us = reinterpret_cast<float *>(st.rx + T * kVerifyRows);
+    st.bc = st.us + T * kVerifyRows;
     return st;
 }
 
@@ -203,8 +213,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
     store_state_part<TS, NPT>(srow, q, s);
 }
 
+// Three CTAs per SM while a thread's share of a state row (NPT values) fits
+// in the register budget that leaves (up to dstate 128), two above.
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KParams p, int T) {
+__global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verify_kernel(const KParams p, int T) {
     extern __shared__ __align__(16) float vsmem[];
     const int64_t b = blockIdx.x;
     const int h = blockIdx.y, g = h / p.heads_per_group, row0 = blockIdx.z * kVerifyRows;
@@ -271,34 +283,52 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KPa
             }
         }
     }
+    // B_m . C_k for every step m <= c + k that draft k sees, one warp per dot
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = warp; i < (c + T) * T; i += kVerifyThreads / 32) {
+        const int m = i / T, k = i % T;
+        if (m > c + k) continue;  // masked: the same for the whole warp
+        const float *Bm = m < c ? st.eB + m * p.N : st.dB + (m - c) * p.N;
+        const float *Ck = st.dC + k * p.N;
+        float v = 0.f;
+        for (int n = lane; n < p.N; n += 32) v = fmaf(Bm[n], Ck[n], v);
+        v = row_sum<32>(v);
+        if (lane == 0) st.bc[i] = v;
+    }
+    // S_ckpt . C_k of this row, over the row's four threads
+    for (int k = 0; k < T; ++k) {
+        const float *Ck = st.dC + k * p.N;
+        float part = 0.f;
+#pragma unroll
+        for (int i4 = 0; i4 < NPT / 4; ++i4) {
+            const float4 cv = *reinterpret_cast<const float4 *>(Ck + col_of(i4, q));
+            part = fmaf(s[4 * i4], cv.x, part);
+            part = fmaf(s[4 * i4 + 1], cv.y, part);
+            part = fmaf(s[4 * i4 + 2], cv.z, part);
+            part = fmaf(s[4 * i4 + 3], cv.w, part);
+        }
+        part = row_sum<4>(part);
+        if (q == 0) st.us[k * kVerifyRows + r] = part;
+    }
+    __syncthreads();
+    if (!active) return;
+    // draft k (thread q of the row takes k = q, q + 4, ...): the walk from
+    // step c + k down to step 0 gathers the decayed window sum and g_{0:M}
     const float Ah = p.A[h];
     const float Dh = p.D ? p.D[h] : 0.f;
-    if (active) apply_entries<NPT>(p, st, c, r, q, Ah, s);
-    // the drafts in order, each read out after its own step
-    for (int k = 0; k < T; ++k) {
-        const int64_t rr = b * T + k;
-        const float d = st.dd[k * kVerifyRows + r], xv = st.dx[k * kVerifyRows + r];
-        float part = 0.f;
-        if (active) {
-            const float dA = decay_inline(Ah, d), dx = d * xv;
-            const float *Bk = st.dB + k * p.N, *Ck = st.dC + k * p.N;
-#pragma unroll
-            for (int i4 = 0; i4 < NPT / 4; ++i4) {
-                const float4 bv = *reinterpret_cast<const float4 *>(Bk + col_of(i4, q));
-                const float4 cv = *reinterpret_cast<const float4 *>(Ck + col_of(i4, q));
-                const float bb[4] = {bv.x, bv.y, bv.z, bv.w}, cc[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s[4 * i4 + e] = fmaf(s[4 * i4 + e], dA, dx * bb[e]);
-                    part = fmaf(s[4 * i4 + e], cc[e], part);
-                }
-            }
+    for (int k = q; k < T; k += 4) {
+        float acc = 0.f, gam = 1.f;
+        for (int m = c + k; m >= 0; --m) {
+            const bool entry = m < c;
+            const float d = entry ? st.ed[m * kVerifyRows + r] : st.dd[(m - c) * kVerifyRows + r];
+            const float xv = entry ? st.ex[m * kVerifyRows + r] : st.dx[(m - c) * kVerifyRows + r];
+            acc = fmaf(gam, (d * xv) * st.bc[m * T + k], acc);
+            gam *= decay_inline(Ah, d);
         }
-        const float sum = row_sum<4>(part);
-        if (!active) continue;
-        if (q == 0)
-            store_small(p.y, rr * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
-                        output(sum, Dh, xv, silu_gate(st.dz[k * kVerifyRows + r], p.z != nullptr)));
+        const float sum = fmaf(gam, st.us[k * kVerifyRows + r], acc);
+        const int64_t rr = b * T + k;
+        store_small(p.y, rr * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
+                    output(sum, Dh, st.dx[k * kVerifyRows + r], silu_gate(st.dz[k * kVerifyRows + r], p.z != nullptr)));
     }
 }
 
