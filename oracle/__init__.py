@@ -166,7 +166,7 @@ def load_library(path: str):
     lib.orc_shadow_refresh.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     lib.orc_shadow_refresh.restype = ctypes.c_int
-    lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.orc_e4m3_encode.argtypes = [ctypes.c_double]
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
     lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.orc_e4m3_decode.restype = ctypes.c_double

@@ -199,12 +199,12 @@ double orc_e4m3_decode(uint8_t code)
 
 /* Round to nearest even onto the E4M3 grid, values past the largest finite
  * one clamped to +-448 ("saturate to finite").  NaN maps to the NaN code. */
-uint8_t orc_e4m3_encode(float v)
+uint8_t orc_e4m3_encode(double v)
 {
     if (isnan(v))
         return 0x7f;
     uint8_t sign = signbit(v) ? 0x80 : 0;
-    double r = fabs(round_to_format((double)v, 3, -6, 8));
+    double r = fabs(round_to_format(v, 3, -6, 8));
     if (isinf(r) || r > 448.0)
         r = 448.0;
     if (r == 0.0)
@@ -218,7 +218,13 @@ uint8_t orc_e4m3_encode(float v)
     return sign | (uint8_t)(biased << 3) | frac;
 }
 
-/* One state row into its read copy (format per orc_shadow_refresh). */
+/* One state row into its read copy (format per orc_shadow_refresh).  The
+ * E4M3 form maps the row's largest magnitude amax onto the largest finite
+ * E4M3 value, 448: each value v is stored as the code of v * 448 / amax
+ * (the quotient in double, then rounded to nearest even onto the E4M3
+ * grid), and the row keeps the scale amax / 448 in fp32 (the type it is
+ * stored in), so that code * scale gives v back.  An all-zero row keeps
+ * zero codes and the scale 1. */
 static void shadow_row(const double *v, int64_t n, int32_t format, void *codes, float *scale)
 {
     if (format == ORC_SHADOW_F16) {
@@ -226,20 +232,13 @@ static void shadow_row(const double *v, int64_t n, int32_t format, void *codes, 
             ((uint16_t *)codes)[i] = double_to_half_bits(v[i]);
         return;
     }
-    /* the row values are fp32 numbers, so these are exact fp32 operations */
-    float amax = 0.0f;
+    double amax = 0.0;
     for (int64_t i = 0; i < n; ++i)
-        if ((float)fabs(v[i]) > amax)
-            amax = (float)fabs(v[i]);
-    volatile float s = amax > 0.0f ? amax / 448.0f : 1.0f;  /* fp32 division */
-    volatile float f = amax > 0.0f ? 448.0f / amax : 1.0f;  /* fp32 division */
-    if (!(f <= FLT_MAX))
-        f = FLT_MAX;
-    *scale = s;
-    for (int64_t i = 0; i < n; ++i) {
-        volatile float q = (float)v[i] * f;                  /* fp32 product */
-        ((uint8_t *)codes)[i] = orc_e4m3_encode(q);
-    }
+        if (fabs(v[i]) > amax)
+            amax = fabs(v[i]);
+    *scale = amax > 0.0 ? (float)round_to_format(amax / 448.0, 23, -126, 127) : 1.0f;
+    for (int64_t i = 0; i < n; ++i)
+        ((uint8_t *)codes)[i] = orc_e4m3_encode(amax > 0.0 ? v[i] * 448.0 / amax : v[i]);
 }
 
 static double shadow_value(const void *codes, const float *scale, int64_t row, int64_t n, int64_t i, int32_t format)

@@ -114,19 +114,18 @@ int orc_ssd_run(const orc_ssd_problem *problem, char *err, int errlen);
  * a fold rewrites it from the new checkpoint.
  *   ORC_SHADOW_F16   binary16, round to nearest even.
  *   ORC_SHADOW_E4M3  OCP FP8 E4M3 (bias 7, 3 fraction bits, no infinities,
- *                    largest 448) with one fp32 scale per state row:
- *                    scale = amax / 448 and factor = 448 / amax (both 1 for
- *                    an all-zero row, the factor clamped to FLT_MAX), computed
- *                    in fp32; code = E4M3(v * factor) with the product in
- *                    fp32, rounded to nearest even and clamped to +-448;
- *                    value = E4M3 value * scale. */
+ *                    largest 448) with one fp32 scale per state row: amax =
+ *                    the row's largest magnitude, code = E4M3(v * 448 / amax)
+ *                    with the quotient in double, rounded to nearest even;
+ *                    scale = amax / 448 stored in fp32 (1, and zero codes,
+ *                    for an all-zero row); value = E4M3 value * scale. */
 enum { ORC_SHADOW_NONE = 0, ORC_SHADOW_F16 = 1, ORC_SHADOW_E4M3 = 2 };
 
 /* The read copy of `rows` state rows of `dstate` elements (`state` in
  * state_dtype); `scale` may be NULL for ORC_SHADOW_F16. */
 int orc_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate, int32_t format,
                        void *shadow, float *scale);
-uint8_t orc_e4m3_encode(float v);
+uint8_t orc_e4m3_encode(double v);
 double orc_e4m3_decode(uint8_t code);
 
 int orc_replay_run(const orc_replay_problem *problem, char *err, int errlen);

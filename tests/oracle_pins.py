@@ -751,24 +751,55 @@ def pin_e4m3_codes(lib):
             raise AssertionError(f"E4M3 of {v}")
 
 
+def _e4m3_nearest(q: torch.Tensor) -> torch.Tensor:
+    """E4M3 codes of float64 values `q` (|q| <= 448) found by brute force: the
+    non-negative finite grid is enumerated by torch's float8_e4m3fn decoding
+    of codes 0..126, the nearest grid value to |q| is taken, an exact tie goes
+    to the even code, and the sign bit is that of q."""
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    a = q.abs().reshape(-1, 1)
+    d = (a - grid.view(1, -1)).abs()
+    best = d.min(dim=1, keepdim=True).values
+    cand = d == best
+    odd = (torch.arange(127) % 2 == 1).view(1, -1)
+    pick_even = cand & ~odd
+    idx = torch.where(pick_even.any(dim=1), pick_even.to(torch.int64).argmax(dim=1),
+                      cand.to(torch.int64).argmax(dim=1))
+    sign = torch.signbit(q.reshape(-1)).to(torch.int64) * 0x80
+    return (idx | sign).to(torch.uint8).view(q.shape)
+
+
 def pin_shadow_refresh(lib):
     """The read copy of a pool: fp16 codes are torch's round-to-nearest-even
-    cast; E4M3 codes and row scales equal a restatement with torch's
-    float8_e4m3fn cast (scale = amax / 448 and factor 448 / amax in fp32,
-    codes of v * factor); an all-zero row gets scale 1 and zero codes."""
+    cast.  E4M3: the row's largest magnitude amax maps to 448; every code is
+    the nearest E4M3 grid value to v * 448 / amax (exact ties to the even
+    code), found by brute force over the grid; the row scale is amax / 448
+    rounded to fp32; an all-zero row gets scale 1 and zero codes; rows of
+    exact midpoints between grid values round to the even neighbour."""
     g = torch.Generator().manual_seed(62)
     st = torch.randn((3, 2, 4, 32), generator=g) * torch.rand((3, 2, 4, 1), generator=g) * 5
     st[1, 0, 2] = 0.0
+    # a row whose amax is 448, so that v * 448 / amax = v exactly: midpoints
+    # between neighbouring grid values (normal and subnormal), each a tie
+    ties = torch.tensor([448.0, 1.0625, 1.1875, -1.0625, 2.0 ** -10, 3 * 2.0 ** -10, 5 * 2.0 ** -10, 17.0,
+                         19.0, 208.0, 432.0, -0.0, 0.0, 2.0 ** -7 + 2.0 ** -11, 0.5, -0.5625])
+    st[2, 1, 3] = torch.cat([ties, torch.zeros(32 - ties.numel())])
     h, none = oracle.shadow_refresh(st, oracle.SHADOW_F16, lib=lib)
     if none is not None or not torch.equal(h, st.half()):
         raise AssertionError("fp16 read copy")
     codes, scale = oracle.shadow_refresh(st, oracle.SHADOW_E4M3, lib=lib)
-    amax = st.abs().amax(dim=-1)
-    want_scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
-    factor = torch.where(amax > 0, 448.0 / amax, torch.ones_like(amax))
-    want_codes = (st * factor[..., None]).to(torch.float8_e4m3fn).view(torch.uint8)
-    if not (torch.equal(scale, want_scale) and torch.equal(codes, want_codes)):
-        raise AssertionError("E4M3 read copy")
+    sd = st.to(torch.float64)
+    amax = sd.abs().amax(dim=-1)
+    want_scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+    q = torch.where(amax[..., None] > 0, sd * 448.0 / torch.where(amax > 0, amax, 1.0)[..., None], sd)
+    want_codes = _e4m3_nearest(q)
+    if not torch.equal(scale, want_scale):
+        raise AssertionError("E4M3 row scales")
+    if not torch.equal(codes, want_codes):
+        raise AssertionError(f"E4M3 read copy: {int((codes != want_codes).sum())} codes differ")
+    tie_codes = codes[2, 1, 3, :ties.numel()].tolist()
+    if tie_codes[1] != 0x38 or tie_codes[2] != 0x3a or tie_codes[4] != 0 or tie_codes[5] != 2:
+        raise AssertionError(f"E4M3 ties: {tie_codes[:6]}")
     if float(scale[1, 0, 2]) != 1.0 or int(codes[1, 0, 2].abs().sum()) != 0:
         raise AssertionError("zero row")
     bf = st.to(torch.bfloat16)  # a 16-bit pool: the copy is of the stored values

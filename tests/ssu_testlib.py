@@ -82,3 +82,32 @@ def assert_y_close(got: torch.Tensor, ref_exact: torch.Tensor, what: str = "y"):
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} out of tolerance; first at "
                              f"{tuple(i)}: got {g[tuple(i)]!r} ref {r[tuple(i)]!r}")
+
+
+def assert_e4m3_codes_close(got: torch.Tensor, want: torch.Tensor, values: torch.Tensor, what: str = "E4M3 codes"):
+    """E4M3 read-copy codes (uint8, rows along the last axis) against the
+    oracle's, which round v * 448 / amax, formed in double, to the nearest
+    grid value.  The kernels form that quotient in fp32 (the factor 448 / amax
+    and the product each rounded, together within 2^-22 relative of the exact
+    quotient), so where the exact quotient lies within 2^-20 of the midpoint
+    between two neighbouring grid values a code may sit one step away on the
+    other side; everywhere else the codes must be equal."""
+    got, want = got.cpu().view(torch.uint8), want.cpu().view(torch.uint8)
+    assert got.shape == want.shape == values.shape
+    diff = got != want
+    if not diff.any():
+        return
+    vd = values.detach().cpu().to(torch.float64)
+    amax = vd.abs().amax(dim=-1, keepdim=True)
+    q = (vd * 448.0 / torch.where(amax > 0, amax, torch.ones_like(amax)))[diff]
+    g, w = got[diff].to(torch.int64), want[diff].to(torch.int64)
+    gm, wm = g & 0x7F, w & 0x7F
+    grid = torch.arange(0, 128, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    mid = (grid[gm] + grid[wm]) / 2
+    near = (q.abs() - mid).abs() <= 2.0 ** -20 * q.abs()
+    ok = ((gm - wm).abs() == 1) & ((g & 0x80) == (w & 0x80)) & near
+    if not ok.all():
+        i = int(torch.nonzero(~ok)[0])
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {int(diff.sum())} differing codes are not one step "
+                             f"apart at a tie; first: got {int(g[i]):#x} want {int(w[i]):#x} for v*448/amax = "
+                             f"{float(q[i])!r}")

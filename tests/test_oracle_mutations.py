@@ -48,8 +48,12 @@ MUTATIONS = [
      "const int64_t dti = pr->dt_per_head ? (r * H) : xi;"),
     # the low-precision read copy of the checkpoint
     ("read_copy_ignored", "sq += (pr->shadow_format != ORC_SHADOW_NONE", "sq += (0"),
-    ("e4m3_scale_240", "amax > 0.0f ? amax / 448.0f : 1.0f", "amax > 0.0f ? amax / 240.0f : 1.0f"),
-    ("e4m3_factor_240", "amax > 0.0f ? 448.0f / amax : 1.0f", "amax > 0.0f ? 240.0f / amax : 1.0f"),
+    ("e4m3_scale_240", "round_to_format(amax / 448.0, 23", "round_to_format(amax / 240.0, 23"),
+    ("e4m3_factor_240", "v[i] * 448.0 / amax", "v[i] * 240.0 / amax"),
+    ("e4m3_signed_amax", "if (fabs(v[i]) > amax)\n            amax = fabs(v[i]);",
+     "if (v[i] > amax)\n            amax = v[i];"),
+    ("e4m3_two_fraction_bits", "double r = fabs(round_to_format(v, 3, -6, 8));",
+     "double r = fabs(round_to_format(v, 2, -6, 8));"),
     ("fold_skips_read_copy",
      "if (pr->shadow_format != ORC_SHADOW_NONE) {\n                            /* the read copy",
      "if (0) {\n                            /* the read copy"),
