@@ -3,6 +3,8 @@ Python binding), cut sampled sub-problems out of full-size workloads for the
 oracle, and compare results."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import replace
 
 import numpy as np
@@ -170,3 +172,41 @@ def assert_untouched(before: torch.Tensor, after: torch.Tensor, written):
     if written:
         mask[torch.tensor(sorted(written), device=before.device)] = False
     assert torch.equal(before[mask], after[mask]), "a slot that is not written changed"
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def complete_check(w_cpu: workloads.Workload, y_gpu: torch.Tensor, state_gpu: torch.Tensor, per_chunk: int = 16):
+    """Compare EVERY sequence of a full-size run with the oracle, element by
+    element: the sequences are cut into independent sub-problems of
+    `per_chunk` sequences (each with its own compact pool; the workloads give
+    every sequence its own slots), the oracle runs them on all host threads
+    (its C entry point runs without the GIL), and each sub-problem's y rows
+    and written slots are held to the output and state tolerances.  Returns
+    the number of sequences compared."""
+    y_all = y_gpu.cpu()
+    pool = state_gpu.cpu()
+    nseq = w_cpu.nseq
+    chunks = [list(range(i, min(i + per_chunk, nseq))) for i in range(0, nseq, per_chunk)]
+
+    def one(seqs):
+        sub, rows, slot_map = subproblem(w_cpu, seqs)
+        ref = run_oracle(sub)
+        if rows:
+            assert_y_close(y_all[rows], ref.y_exact, what=f"y (sequences {seqs[0]}..{seqs[-1]})")
+        inv = {v: k for k, v in slot_map.items()}
+        written = [i for i in range(sub.state.shape[0]) if ref.touched[i] & 2]
+        if written:
+            assert_state_close(pool[[inv[i] for i in written]], ref.state[written],
+                               what=f"state (sequences {seqs[0]}..{seqs[-1]})")
+        return len(seqs)
+
+    with ThreadPoolExecutor(max(1, min(host_threads(), len(chunks)))) as ex:
+        done = sum(ex.map(one, chunks))
+    assert done == nseq
+    return done

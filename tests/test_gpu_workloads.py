@@ -1,13 +1,13 @@
 """The five decode workloads at full size, in the launch configuration the
-benchmark times: the oracle checks sampled sequences one by one (every pad
-case included), and properties that hold at any size are checked on the whole
-pool (untouched slots bit-identical, pad slot never written, no device
-status bits)."""
+benchmark times: every sequence is compared with the oracle element by element
+(y and every written slot), and properties that hold at any size are checked
+on the whole pool (untouched slots bit-identical, pad slot never written, no
+device status bits)."""
 import pytest
 import torch
 
 import workloads
-from gpu_harness import (DEV, assert_untouched, full_check, run_gpu, sampled_check, written_slots)
+from gpu_harness import (DEV, assert_untouched, complete_check, full_check, run_gpu, written_slots)
 from ssu_testlib import assert_y_close, run_oracle
 
 pytestmark = pytest.mark.gpu
@@ -25,32 +25,6 @@ def _run_full(w_cpu):
     return w, y
 
 
-def _sample(w_cpu, n_random, seed):
-    """Sequences to check: every sequence with a pad entry, empties, plus a
-    seeded random selection."""
-    g = torch.Generator().manual_seed(seed)
-    nseq = w_cpu.nseq
-    picks = set(torch.randperm(nseq, generator=g)[:n_random].tolist())
-    pad = w_cpu.pad_slot_id
-    for t in (w_cpu.read, w_cpu.dst):
-        if t is None:
-            continue
-        if w_cpu.kind == "onetoken":
-            picks |= set(torch.nonzero(t.reshape(-1) == pad).view(-1).tolist())
-        elif t.dim() == 2:
-            picks |= set(torch.nonzero((t == pad).any(dim=1)).view(-1).tolist())
-    lens = w_cpu.meta.get("lengths")
-    if lens:
-        picks |= {b for b, L in enumerate(lens) if L == 0}
-        if w_cpu.slot_mode == workloads.SLOTS_PER_ROW and w_cpu.read is not None:
-            cu = [0]
-            for L in lens:
-                cu.append(cu[-1] + L)
-            flat = w_cpu.read.reshape(-1)
-            picks |= {b for b in range(nseq) if any(int(flat[r]) == pad for r in range(cu[b], cu[b + 1]))}
-    return sorted(picks)
-
-
 def test_tiny_onetoken(libssu):
     full_check(workloads.tiny_onetoken())
 
@@ -60,25 +34,25 @@ def test_b256_fp32(libssu, in_place):
     w_cpu = workloads.b256_fp32(in_place=in_place)
     w, y = _run_full(w_cpu)
     assert torch.equal(w.state[0].cpu(), w_cpu.state[0]), "pad slot 0 was written"
-    sampled_check(w_cpu, _sample(w_cpu, 16, 1), y, w.state)
+    assert complete_check(w_cpu, y, w.state) == 256
 
 
 def test_b1024_bf16(libssu):
     w_cpu = workloads.b1024_bf16()
     w, y = _run_full(w_cpu)
-    sampled_check(w_cpu, _sample(w_cpu, 24, 2), y, w.state)
+    assert complete_check(w_cpu, y, w.state) == 1024
 
 
 def test_mtp_64x7_fp32(libssu):
     w_cpu = workloads.mtp_64x7_fp32()
     w, y = _run_full(w_cpu)
-    sampled_check(w_cpu, _sample(w_cpu, 10, 3), y, w.state)
+    assert complete_check(w_cpu, y, w.state) == 64
 
 
 def test_varlen_fp16(libssu):
     w_cpu = workloads.varlen_fp16()
     w, y = _run_full(w_cpu)
-    sampled_check(w_cpu, _sample(w_cpu, 16, 4), y, w.state)
+    assert complete_check(w_cpu, y, w.state) == 128
 
 
 @pytest.mark.parametrize("slot_mode", [workloads.SLOTS_PER_ROW, workloads.SLOTS_STRIDED])
