@@ -2,14 +2,25 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one call of the update over one batch of the workload (default:
-batch-256 one-token decode, fp32 state pool; every step of the update runs in
-one kernel launch).  Inputs are resident in HBM when the timed region starts;
-the touched state (about 2 GB per step) is far larger than L2, so no flush is
-needed between steps.  Prints ONE JSON line.
+One step = one call of the update over one batch of the workload (every step
+of the update runs in one kernel launch).  Without --workload the five decode
+configurations are timed one after another in the same run: the batch-256
+one-token decode with an fp32 pool is the headline line, and every
+configuration (the tiny one-token case, batch 256 fp32, batch 1024 bf16, MTP
+packed 64 x 7 fp32, variable-length packed fp16 and its disable_state_update
+run) gets its own entry under "configs".  Inputs are resident in HBM when a
+timed region starts; the state moved per step is far larger than L2 (except
+for the tiny case, which is launch-bound), so no flush is needed between
+steps.  Prints ONE JSON line.
 
 --impl reference times the CPU oracle (the plain double-precision definition)
 on the host cores, on bounded samples of the same workload.
+
+--record-traffic CSV reads an ncu CSV (dram__bytes_read.sum and
+dram__bytes_write.sum per launch) of a --workload run and records the DRAM
+bytes per call of that workload's kernels, with the hash of their sources, in
+profiles/traffic.json; the bench line reports it as roofline.traffic while the
+sources are unchanged.
 """
 from __future__ import annotations
 
@@ -46,6 +57,8 @@ DESCRIPTIONS = {
                      "num_accepted U{1..7}",
     "varlen_fp16": "variable-length packed decode, 128 sequences of length U{0..8}, heads 64, dim 64, "
                    "dstate 128, groups 1, fp16 pool of 2048 slots, flat per-row read table, 3% pad",
+    "varlen_fp16_disable": "varlen_fp16 with disable_state_update=True on identical inputs (seeds read, "
+                           "nothing written)",
     "tiny_onetoken": "one-token decode, batch 2, heads 8, dim 8, dstate 128, groups 2, fp16 zero state",
     "replay_b256_fp32": "one-token decode on the checkpoint + buffer form (ReplaySSM), batch 256, heads 128, "
                         "dim 64, dstate 128, groups 8, fp32 checkpoints (512 slots), buffer length 16, "
@@ -183,18 +196,81 @@ def kernel_hash(kind: str) -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_NAMES = {"onetoken": ["ssu_onetoken_kernel"], "packed": ["ssu_packed_kernel"], "replay": ["ssu_replay_kernel"],
+                "copy": ["ssu_copy_kernel"], "verify": ["ssu_verify_fold_kernel", "ssu_verify_kernel"],
+                "ssd": ["ssd_chunk_state_kernel", "ssd_state_pass_kernel", "ssd_chunk_cb_kernel",
+                        "ssd_chunk_scan_kernel"]}
+
+
 def profiled_traffic(kind: str, workload: str):
-    """DRAM bytes per launch recorded from an ncu capture in profiles/, if that
-    capture was taken of the kernel source as it is now."""
-    path = os.path.join(ROOT, "profiles", f"ssu_{kind}_{workload}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per call recorded in profiles/traffic.json from an ncu
+    capture (--record-traffic), if that capture was taken of the kernel
+    sources as they are now; None otherwise."""
+    try:
+        with open(TRAFFIC_JSON) as f:
+            rec = json.load(f).get(f"{kind}/{workload}")
+    except (OSError, ValueError):
         return None
-    text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    hm = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m or not hm or hm.group(1) != kernel_hash(kind):
+    if not rec or rec.get("kernel_source_sha256_16") != kernel_hash(kind):
         return None
-    return int(m.group(1))
+    return int(rec["bytes_per_call"])
+
+
+_NCU_SCALE = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "kibyte": 1024, "mibyte": 1024 ** 2,
+              "gibyte": 1024 ** 3}
+
+
+def traffic_from_ncu_csv(path: str, kind: str) -> dict:
+    """Per kernel of `kind`: the launches in an ncu --csv log and the median
+    DRAM bytes (read + write) per launch; the call's bytes are the sum over
+    the kind's kernels (each launches once per call)."""
+    import csv
+    per = {}
+    with open(path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        name = row.get("Kernel Name", "")
+        base = next((k for k in KERNEL_NAMES[kind] if re.search(rf"\b{k}\b", name)), None)
+        metric = row.get("Metric Name", "")
+        if base is None or metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        v = float(row["Metric Value"].replace(",", "")) * _NCU_SCALE[row.get("Metric Unit", "byte").lower()]
+        per.setdefault(base, {}).setdefault(row["ID"], 0.0)
+        per[base][row["ID"]] += v
+    if not per:
+        raise SystemExit(f"no launch of {KERNEL_NAMES[kind]} with DRAM byte counters in {path}")
+    out = {k: {"launches": len(v), "median_bytes": statistics.median(v.values())} for k, v in per.items()}
+    return {"kernels": out, "bytes_per_call": int(sum(k["median_bytes"] for k in out.values()))}
+
+
+def record_traffic(csv_path: str, workload: str, command: str) -> dict:
+    kind = workload_kind(workload)
+    rec = traffic_from_ncu_csv(csv_path, kind)
+    rec.update({"kernel_source_sha256_16": kernel_hash(kind), "command": command,
+                "recorded": time.strftime("%Y-%m-%d")})
+    try:
+        with open(TRAFFIC_JSON) as f:
+            allrec = json.load(f)
+    except (OSError, ValueError):
+        allrec = {}
+    allrec[f"{kind}/{workload}"] = rec
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(allrec, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return rec
+
+
+def workload_kind(workload: str) -> str:
+    if workload.startswith("copy_"):
+        return "copy"
+    if workload.startswith("ssd_"):
+        return "ssd"
+    if workload.startswith("verify_"):
+        return "verify"
+    if workload.startswith("replay_"):
+        return "replay"
+    return "onetoken" if workload in ("tiny_onetoken", "b256_fp32", "b1024_bf16") else "packed"
 
 
 def hbm_peak():
@@ -323,12 +399,18 @@ def _per_step_inputs(w):
             if t is not None]
 
 
-def run_ours(args, rank, world, device):
-    from selective_state_update_gb300 import build as ssu_build
+DECODE_SUITE = ["b256_fp32", "tiny_onetoken", "b1024_bf16", "mtp_64x7_fp32", "varlen_fp16", "varlen_fp16_disable"]
+
+
+def time_decode(workload, args, rank, world, device) -> dict:
+    """Time one decode workload: `args.warmup` untimed calls, then
+    `args.steps` timed calls bracketed by a barrier and a synchronize, with
+    CUDA events on the launching stream around each call and around the whole
+    region, clocks sampled meanwhile; then the end-to-end rate through the
+    public call with the step's inputs copied from pinned host memory and y
+    copied back inside the timed region."""
     import selective_state_update_gb300 as ssu
-    ssu_build.build()
-    ssu.lib()
-    w = make_workload(args, device, seed_offset=97 * rank)
+    w = make_workload(workload, args.batch, device, seed_offset=97 * rank)
     torch.cuda.synchronize()
     acct = algorithmic_bytes(w)
     tokens = w.rows
@@ -390,30 +472,23 @@ def run_ours(args, rank, world, device):
     peak, peak_src = hbm_peak()
     achieved = acct["total"] / (launch_ms * 1e-3) / 1e9
     kind = w.kind
-    result = {
-        "metric": METRIC,
+    moved = acct["state_read"] + acct["state_write"]
+    rec = {
         "value": aggregate_rate(tokens, world, args.steps, total_ms),
         "unit": UNIT,
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"
+        "config": {"workload": f"{workload}: {DESCRIPTIONS[workload]}"
                                + (f" (batch {args.batch})" if args.batch else ""),
                    "sequences_per_gpu": w.nseq, "rows_per_gpu": tokens,
                    "state_dtype": str(w.state.dtype).replace("torch.", ""),
                    "io_dtype": str(w.x.dtype).replace("torch.", ""),
                    "parallelism": f"{world} independent replicas (one pool and batch per GPU)",
-                   "l2": "no flush: inputs larger than L2 (%.2f GB of state moved per step)"
-                         % ((acct["state_read"] + acct["state_write"]) / 1e9)},
+                   "l2": ("no flush: inputs larger than L2 (%.2f GB of state moved per step)" % (moved / 1e9))
+                         if moved > 200e6 else
+                         "no flush: launch-bound case (%.1f KB of state per step, L2-resident)" % (moved / 1e3)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth",
-                     "traffic": profiled_traffic(kind, args.workload),
+                     "traffic": profiled_traffic(kind, workload),
                      "algorithmic_bytes_per_launch": acct["total"],
                      "kernel": f"ssu_{kind}_kernel", "launch_ms": launch_ms},
         "e2e": {"value": aggregate_rate(tokens, world, e2e_steps, e2e_s * 1e3), "unit": UNIT,
@@ -421,6 +496,48 @@ def run_ours(args, rank, world, device):
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
+    del w, out, host_in, dev_in, host_y
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_ours(args, rank, world, device):
+    from selective_state_update_gb300 import build as ssu_build
+    import selective_state_update_gb300 as ssu
+    ssu_build.build()
+    ssu.lib()
+    suite = [args.workload] if args.workload else DECODE_SUITE
+    recs = {name: time_decode(name, args, rank, world, device) for name in suite}
+    head = recs[suite[0]]
+    result = {
+        "metric": METRIC,
+        "value": head["value"],
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": head["config"],
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+    }
+    if len(suite) > 1:
+        result["configs"] = {
+            name: {"workload": r["config"]["workload"], "value": r["value"], "unit": r["unit"],
+                   "ms_per_step": r["ms_per_step"], "launch_ms": r["roofline"]["launch_ms"],
+                   "algorithmic_bytes_per_launch": r["roofline"]["algorithmic_bytes_per_launch"],
+                   "achieved_gbs": r["roofline"]["achieved"], "roofline_frac": r["roofline"]["frac"],
+                   "traffic": r["roofline"]["traffic"], "kernel": r["roofline"]["kernel"],
+                   "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"], "l2": r["config"]["l2"]}
+            for name, r in recs.items()}
+        result["gpu_launches_all_configs"] = sum(r["gpu_launches"] for r in recs.values())
     return result
 
 
@@ -431,7 +548,7 @@ def run_copy(args, rank, world, device):
     import selective_state_update_gb300 as ssu
     ssu_build.build()
     ssu.lib()
-    w = make_workload(args, device, seed_offset=97 * rank)
+    w = make_workload(args.workload, args.batch, device, seed_offset=97 * rank)
     slot_bytes = w.state[0].numel() * w.state.element_size()
     tables = [ssu.slot_copies(w.state, w.src, w.dst), ssu.slot_copies(w.state, w.dst, w.src)]
     status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -552,7 +669,7 @@ def run_verify(args, rank, world, device):
     import selective_state_update_gb300 as ssu
     ssu_build.build()
     ssu.lib()
-    w = make_workload(args, device, seed_offset=97 * rank)
+    w = make_workload(args.workload, args.batch, device, seed_offset=97 * rank)
     batch, T = w.x.shape[0], w.x.shape[1]
     period = w.xbuf.shape[1] - 2 * T + 1
     counts = [((torch.arange(batch, device=device) + k) % period).to(torch.int32) for k in range(period)]
@@ -695,7 +812,7 @@ def run_ssd(args, rank, world, device):
     import selective_state_update_gb300 as ssu
     ssu_build.build()
     ssu.lib()
-    w = make_workload(args, device, seed_offset=97 * rank)
+    w = make_workload(args.workload, args.batch, device, seed_offset=97 * rank)
     acct = ssd_accounting(w)
     status = torch.zeros(1, dtype=torch.int32, device=device)
     out = torch.empty_like(w.x)
@@ -882,20 +999,20 @@ def _oracle_call(sub):
 
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
-         "varlen_fp16": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008,
+         "varlen_fp16": 1005, "varlen_fp16_disable": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008,
          "replay_f16copy_b256_fp32": 1009, "ssd_prefill_16k_bf16": 1010, "verify_b256_t4_fp32": 1011}
 
 
-def make_workload(args, device, seed_offset=0):
-    gen = workloads.NAMED[args.workload]
+def make_workload(workload, batch, device, seed_offset=0):
+    gen = workloads.NAMED[workload]
     kw = {}
-    if args.batch is not None:
-        if args.workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
-                                 "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16",
-                                 "verify_b256_t4_fp32"):
-            raise SystemExit(f"--batch does not apply to the {args.workload} workload")
-        kw["batch"] = args.batch
-    w = gen(device=device, seed=SEEDS[args.workload] + seed_offset, **kw)
+    if batch is not None:
+        if workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
+                            "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16",
+                            "verify_b256_t4_fp32"):
+            raise SystemExit(f"--batch does not apply to the {workload} workload")
+        kw["batch"] = batch
+    w = gen(device=device, seed=SEEDS[workload] + seed_offset, **kw)
     if getattr(w, "shadow", None) is not None and str(device) != "cpu":
         # the read copy of the checkpoints, built by the library
         import selective_state_update_gb300 as ssu
@@ -904,7 +1021,7 @@ def make_workload(args, device, seed_offset=0):
 
 
 def _cpu_workload(args):
-    return make_workload(args, "cpu")
+    return make_workload(args.workload or DECODE_SUITE[0], args.batch, "cpu")
 
 
 def oracle_rate(w_cpu, budget_s: float):
@@ -971,6 +1088,7 @@ def oracle_rate_threaded(w_cpu, budget_s: float, threads: int):
 
 
 def run_reference(args):
+    wl = args.workload or DECODE_SUITE[0]
     w_cpu = _cpu_workload(args)
     import oracle
     oracle.build()
@@ -981,7 +1099,7 @@ def run_reference(args):
             "impl": "reference", "metric": VERIFY_METRIC, "value": value, "unit": VERIFY_UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w_cpu.x.shape[0] * w_cpu.x.shape[1] / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "config": {"workload": f"{wl}: {DESCRIPTIONS[wl]}"},
             "cpu_baseline": {"value": value, "unit": VERIFY_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": VERIFY_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
@@ -992,7 +1110,7 @@ def run_reference(args):
             "impl": "reference", "metric": SSD_METRIC, "value": value, "unit": SSD_UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * ssd_accounting(w_cpu)["tokens"] / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "config": {"workload": f"{wl}: {DESCRIPTIONS[wl]}"},
             "cpu_baseline": {"value": value, "unit": SSD_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": SSD_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
@@ -1003,7 +1121,7 @@ def run_reference(args):
             "impl": "reference", "metric": COPY_METRIC, "value": value, "unit": COPY_UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+            "config": {"workload": f"{wl}: {DESCRIPTIONS[wl]}"},
             "cpu_baseline": {"value": value, "unit": COPY_UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": COPY_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }
@@ -1033,7 +1151,7 @@ def run_reference(args):
         "steps": done_steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(done_steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+        "config": {"workload": f"{wl}: {DESCRIPTIONS[wl]}"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -1045,12 +1163,22 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(workloads.NAMED), default="b256_fp32")
+    ap.add_argument("--workload", choices=sorted(workloads.NAMED), default=None,
+                    help="time one workload (default: the five decode configurations, batch 256 fp32 as headline)")
     ap.add_argument("--batch", type=int, default=None,
                     help="b256_fp32 / mtp_64x7_fp32 with another number of sequences (profiling captures)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="record the DRAM bytes per call of --workload's kernels from an ncu CSV into "
+                         "profiles/traffic.json (no GPU needed)")
+    ap.add_argument("--record-command", default="", help="the command the ncu CSV was captured with")
     args = ap.parse_args()
+    if args.record_traffic:
+        if not args.workload:
+            ap.error("--record-traffic needs --workload")
+        print(json.dumps(record_traffic(args.record_traffic, args.workload, args.record_command)))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
@@ -1065,27 +1193,28 @@ def main():
 
     # The oracle baseline runs before the first GPU call (no fork after CUDA init).
     cpu = None
-    is_copy = args.workload.startswith("copy_")
-    is_ssd = args.workload.startswith("ssd_")
-    is_verify = args.workload.startswith("verify_")
+    wl = args.workload or DECODE_SUITE[0]
+    is_copy = wl.startswith("copy_")
+    is_ssd = wl.startswith("ssd_")
+    is_verify = wl.startswith("verify_")
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         w_cpu = _cpu_workload(args)
         if is_verify:
             rate, desc = verify_oracle_rate(w_cpu, args.cpu_baseline_seconds)
             cpu = {"value": rate, "unit": VERIFY_UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+                   "sample": f"{desc} of {wl} (single-threaded plain C, double precision)"}
         elif is_ssd:
             rate, desc = ssd_oracle_rate(w_cpu, args.cpu_baseline_seconds)
             cpu = {"value": rate, "unit": SSD_UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+                   "sample": f"{desc} of {wl} (single-threaded plain C, double precision)"}
         elif is_copy:
             rate, desc = copy_oracle_rate(w_cpu, args.cpu_baseline_seconds)
             cpu = {"value": rate, "unit": COPY_UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{desc} of {args.workload} (numpy, one thread)"}
+                   "sample": f"{desc} of {wl} (numpy, one thread)"}
         else:
             rate, desc = oracle_rate(w_cpu, args.cpu_baseline_seconds)
             cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{desc} of {args.workload} (single-threaded plain C, double precision)"}
+                   "sample": f"{desc} of {wl} (single-threaded plain C, double precision)"}
             threads = host_threads()
             if threads > 1:
                 # all host cores, the single-core figure kept beside it; should the
@@ -1093,7 +1222,7 @@ def main():
                 try:
                     trate, tdesc = oracle_rate_threaded(w_cpu, args.cpu_baseline_seconds, threads)
                     cpu = {"value": trate, "unit": UNIT, "cores": threads, "kind": "oracle",
-                           "sample": f"{tdesc} of {args.workload} (plain C, double precision)",
+                           "sample": f"{tdesc} of {wl} (plain C, double precision)",
                            "single_core": {"value": rate, "sample": cpu["sample"]}}
                 except Exception as e:  # noqa: BLE001 -- a baseline, not the measurement
                     cpu["sample"] += f"; the {threads}-thread run failed: {type(e).__name__}: {e}"

@@ -576,6 +576,7 @@ NAMED = {
     "b1024_bf16": b1024_bf16,
     "mtp_64x7_fp32": mtp_64x7_fp32,
     "varlen_fp16": varlen_fp16,
+    "varlen_fp16_disable": lambda device="cpu", seed=1005: varlen_fp16(device, seed, disable_state_update=True),
     "replay_b256_fp32": replay_b256_fp32,
     "replay_e4m3_b256_fp32": replay_e4m3_b256_fp32,
     "replay_f16copy_b256_fp32": replay_f16copy_b256_fp32,
