@@ -84,7 +84,7 @@ VERIFY_METRIC = "verified draft tokens/s and achieved HBM GB/s"
 VERIFY_UNIT = "draft-tokens/s"
 SSD_UNIT = "tokens/s"
 KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_internal.h"],
-                  "packed": ["ssu_packed.cu", "ssu_device.cuh", "ssu_internal.h"],
+                  "packed": ["ssu_packed.cu", "ssu_packed_long.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "verify": ["ssu_verify.cu", "ssu_verify.h", "ssu_device.cuh", "ssu_internal.h"],
@@ -197,7 +197,7 @@ def kernel_hash(kind: str) -> str:
 
 
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_NAMES = {"onetoken": ["ssu_onetoken_kernel"], "packed": ["ssu_packed_kernel"], "replay": ["ssu_replay_kernel"],
+KERNEL_NAMES = {"onetoken": ["ssu_onetoken_kernel"], "packed": ["ssu_packed_kernel", "ssu_packed_long_kernel"], "replay": ["ssu_replay_kernel"],
                 "copy": ["ssu_copy_kernel"], "verify": ["ssu_verify_fold_kernel", "ssu_verify_kernel"],
                 "ssd": ["ssd_chunk_state_kernel", "ssd_state_pass_kernel", "ssd_chunk_cb_kernel",
                         "ssd_chunk_scan_kernel"]}
@@ -259,6 +259,15 @@ def record_traffic(csv_path: str, workload: str, command: str) -> dict:
         json.dump(allrec, f, indent=1, sort_keys=True)
         f.write("\n")
     return rec
+
+
+LONG_ROWS_PER_SEQ = 6  # the library's packed kernel for long sequences takes rows >= 6 * nseq
+
+
+def kernel_name(w) -> str:
+    if w.kind == "packed" and w.rows >= LONG_ROWS_PER_SEQ * w.nseq:
+        return "ssu_packed_long_kernel"
+    return f"ssu_{w.kind}_kernel"
 
 
 def workload_kind(workload: str) -> str:
@@ -490,7 +499,7 @@ def time_decode(workload, args, rank, world, device) -> dict:
                      "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth",
                      "traffic": profiled_traffic(kind, workload),
                      "algorithmic_bytes_per_launch": acct["total"],
-                     "kernel": f"ssu_{kind}_kernel", "launch_ms": launch_ms},
+                     "kernel": kernel_name(w), "launch_ms": launch_ms},
         "e2e": {"value": aggregate_rate(tokens, world, e2e_steps, e2e_s * 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,

@@ -91,3 +91,32 @@ def test_groups_one_per_head(libssu):
     w = workloads.random_problem(900, kind="packed", slots=64, heads=8, groups=8, dim=16, dstate=64,
                                  nseq=3, max_len=3)
     full_check(w)
+
+
+# Sequences of six tokens or more on average take the long-sequence kernel
+# (one CTA per unit); the sweeps above take the persistent short-sequence one.
+@pytest.mark.parametrize("state_dtype", [F32, F16, BF16])
+@pytest.mark.parametrize("dstate", [16, 128, 256])
+@pytest.mark.parametrize("dim", [8, 100])
+def test_packed_long_shapes(libssu, state_dtype, dstate, dim):
+    w = workloads.random_problem(1000 + dstate + dim, kind="packed", slots=128, heads=4, groups=2, dim=dim,
+                                 dstate=dstate, nseq=4, min_len=6, max_len=9, state_dtype=state_dtype,
+                                 io_dtype=BF16, tables="distinct", pad_frac=0.15)
+    assert w.rows >= 6 * w.nseq
+    full_check(w)
+
+
+@pytest.mark.parametrize("with_D,with_z,with_bias,softplus", FLAGS[::3])
+@pytest.mark.parametrize("mode", [workloads.SLOTS_STRIDED, workloads.SLOTS_PER_ROW])
+def test_packed_long_flags_and_modes(libssu, mode, with_D, with_z, with_bias, softplus):
+    seed = 1100 + sum(v << i for i, v in enumerate((with_D, with_z, with_bias, softplus)))
+    w = workloads.random_problem(seed, kind="packed", slots=160, heads=4, groups=2, dim=16, dstate=64, nseq=5,
+                                 min_len=6, max_len=10, with_D=with_D, with_z=with_z, with_bias=with_bias,
+                                 dt_softplus=softplus, tables="distinct", slot_mode=mode, pad_frac=0.1)
+    full_check(w)
+
+
+def test_dense_form_long(libssu):
+    w = workloads.random_problem(1200, kind="packed", slots=96, heads=4, groups=2, dim=16, dstate=128,
+                                 nseq=4, max_len=7, dense=True)
+    full_check(w)

@@ -30,6 +30,29 @@ def test_packed_lengths_one_equals_onetoken_bitwise(libssu, state_dtype):
     assert torch.equal(ya, yb) and torch.equal(a.state, b.state)
 
 
+@pytest.mark.parametrize("state_dtype", [F32, F16])
+def test_long_and_short_sequence_kernels_agree_bitwise(libssu, state_dtype):
+    """The same sequences through the long-sequence kernel (six or more
+    tokens a sequence on average) and, with empty sequences appended to the
+    call, through the persistent short-sequence kernel: the same per-row
+    functions give the same bits."""
+    w = workloads.random_problem(31, kind="packed", slots=128, heads=8, groups=2, dim=64, dstate=128, nseq=6,
+                                 min_len=6, max_len=9, tables="distinct", pad_frac=0.1, state_dtype=state_dtype)
+    a = _gpu(w)
+    ya = run_gpu(a)
+    extra = 6
+    cu = torch.cat([w.cu_seqlens, w.cu_seqlens[-1:].repeat(extra)])
+    width = w.read.shape[1]
+    pad = torch.full((extra, width), w.pad_slot_id, dtype=w.read.dtype)
+    b = _gpu(replace(w, cu_seqlens=cu, read=torch.cat([w.read, pad]), dst=torch.cat([w.dst, pad]),
+                     num_accepted=torch.cat([w.num_accepted, torch.ones(extra, dtype=w.num_accepted.dtype)]),
+                     meta={"lengths": w.meta["lengths"] + [0] * extra}))
+    assert w.rows >= 6 * w.nseq and w.rows < 6 * (w.nseq + extra)
+    yb = run_gpu(b)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yb) and torch.equal(a.state, b.state)
+
+
 def test_dense_equals_uniform_cu_bitwise(libssu):
     w = workloads.random_problem(12, kind="packed", slots=64, heads=4, groups=2, dim=64, dstate=128,
                                  nseq=5, max_len=3, dense=True)
@@ -128,6 +151,37 @@ def test_device_status_bad_entry_and_seqlens(libssu):
     run_gpu(g, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & ssu.DEV_BAD_SEQLEN
+
+
+def test_per_row_seed_past_the_sequence_is_flagged(libssu):
+    """With a per-row table, num_accepted past a sequence's length would seed
+    from another sequence's entry: the kernel flags BAD_ENTRY and skips that
+    sequence (no y, no state written); every other sequence is unchanged."""
+    w = workloads.random_problem(21, kind="packed", slots=256, heads=4, groups=2, dim=64, dstate=128, nseq=9,
+                                 max_len=4, allow_empty=False, slot_mode=workloads.SLOTS_PER_ROW, tables="read",
+                                 pad_frac=0.0)
+    lens = w.meta["lengths"]
+    b = 4
+    acc = w.num_accepted.clone()
+    acc[b] = lens[b] + 1
+    g = _gpu(replace(w, num_accepted=acc))
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y = run_gpu(g, status=status, y_fill=7.0)
+    ok = _gpu(w)
+    y_ok = run_gpu(ok)
+    torch.cuda.synchronize()
+    assert int(status.item()) == ssu.DEV_BAD_ENTRY
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    rows_b = list(range(cu[b], cu[b + 1]))
+    others = [r for r in range(cu[-1]) if r not in rows_b]
+    assert torch.all(y[rows_b].float() == 7.0), "the skipped sequence's y was written"
+    assert torch.equal(y[others], y_ok[others])
+    own = [int(w.read[r]) for r in rows_b]
+    assert torch.equal(g.state[own].cpu(), w.state[own]), "the skipped sequence wrote its slots"
+    rest = [s for s in range(w.state.shape[0]) if s not in own]
+    assert torch.equal(g.state[rest], ok.state[rest])
 
 
 def test_int64_tables_and_meta(libssu):

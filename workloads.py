@@ -402,7 +402,8 @@ def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads:
                    tables: str = "distinct", pad_slot_id: int = -1, pad_frac: float = 0.2,
                    slot_mode: int = SLOTS_STRIDED, with_accepted: bool = True,
                    allow_empty: bool = True, disable_state_update: bool = False,
-                   state_std: float = 0.5, dense: bool = False, device="cpu") -> Workload:
+                   state_std: float = 0.5, dense: bool = False, min_len: int = 0,
+                   device="cpu") -> Workload:
     """A small seeded problem for parity sweeps.
 
     ``tables``: "none" (sequence b uses slot b), "read" (read table only),
@@ -410,7 +411,8 @@ def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads:
     "inplace" (destination table equal to the read table).
     For ``kind="packed"`` the read/destination tables are 2-D ``[nseq, max_len]``
     in STRIDED mode, or flat ``[rows]`` in PER_ROW mode; ``dense`` makes every
-    sequence ``max_len`` long and drops cu_seqlens (the dense 4-D form).
+    sequence ``max_len`` long and drops cu_seqlens (the dense 4-D form);
+    ``min_len`` raises the shortest length of the others.
     """
     gh = _gen(seed, "cpu")
     if kind == "onetoken":
@@ -418,7 +420,7 @@ def random_problem(seed: int, *, kind: str = "onetoken", slots: int = 16, heads:
     elif dense:
         lens = torch.full((nseq,), max_len, dtype=torch.int64)
     else:
-        lens = torch.randint(0 if allow_empty else 1, max_len + 1, (nseq,), generator=gh)
+        lens = torch.randint(max(min_len, 0 if allow_empty else 1), max_len + 1, (nseq,), generator=gh)
     rows = int(lens.sum())
     cu = torch.zeros(nseq + 1, dtype=torch.int64)
     cu[1:] = torch.cumsum(lens, 0)
