@@ -20,7 +20,8 @@
  * computed in fp32 and rounded to nearest even into the io dtype.
  *
  * Conventions for every entry point:
- *  - Pointers named "device" are CUDA device pointers on the current device;
+ *  - Pointers named "device" are CUDA device pointers on the current device
+ *    (a state pool on another device is rejected with SSU_ERR_INVALID);
  *    the caller owns every buffer.  The library allocates no device memory,
  *    copies nothing between host and device, and never synchronizes: one
  *    call is one kernel launch on `stream` (a cudaStream_t; NULL = the
@@ -87,7 +88,8 @@ typedef struct ssu_slot_table {
 
 /* Bits ORed into *d_status by the kernels. */
 #define SSU_DEV_BAD_SLOT   0x1  /* slot not in [0, slots) and not pad_slot_id       */
-#define SSU_DEV_BAD_ENTRY  0x2  /* table entry index outside [0, extent)            */
+#define SSU_DEV_BAD_ENTRY  0x2  /* table entry index outside [0, extent), or a
+                                   per-row seed step past its sequence's rows      */
 #define SSU_DEV_BAD_SEQLEN 0x4  /* cu_seqlens decreasing, negative or past `rows`   */
 #define SSU_DEV_TIMEOUT    0x8  /* an asynchronous state copy did not complete in
                                    about a second; the unit was skipped           */
@@ -161,7 +163,11 @@ ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch,
  *                i.e. x as [nseq, steps, heads, dim] flattened.
  *   num_accepted device [nseq] of meta_type or NULL.  The read slot of
  *                sequence b is at step max(num_accepted[b] - 1, 0) (step 0
- *                without the array).
+ *                without the array).  With a SSU_SLOTS_PER_ROW read table
+ *                that step must be one of the sequence's own rows (below
+ *                its length): a later one would name another sequence's
+ *                entry, so the sequence sets SSU_DEV_BAD_ENTRY and is
+ *                skipped.
  *   read, dst    slot tables addressed per their mode (see ssu_slot_mode).
  *                No read table: sequence b reads and writes slot b (every
  *                token overwrites it; the last token's state remains).  No
@@ -212,11 +218,13 @@ typedef struct ssu_replay_buffers {
 } ssu_replay_buffers;
 
 /* Formats of the read copy.  E4M3 is OCP FP8 E4M3 (bias 7, 3 fraction bits,
- * no infinities, largest 448) with one fp32 scale per state row: over the
- * row's stored values, scale = amax / 448 and factor = 448 / amax (both 1
- * for an all-zero row, the factor clamped to the largest finite float), in
- * fp32; code = E4M3(v * factor), the product in fp32, rounded to nearest even
- * and clamped to +-448; the value read is E4M3(code) * scale.  F16 is
+ * no infinities, largest 448) with one fp32 scale per state row: the row's
+ * largest magnitude amax maps to 448, code = E4M3(v * 448 / amax) rounded to
+ * nearest even and clamped to +-448, and scale = amax / 448 in fp32 (1, with
+ * zero codes, for an all-zero row); the value read is E4M3(code) * scale.
+ * The kernels form the quotient in fp32 as v * (448 / amax), so a code can
+ * sit one step from the exactly rounded one where v * 448 / amax lies within
+ * about 2^-22 (relative) of a midpoint between two E4M3 values.  F16 is
  * binary16, round to nearest even. */
 #define SSU_SHADOW_NONE 0
 #define SSU_SHADOW_F16  1
@@ -357,7 +365,9 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *args, void *stream);
  * device on the first call made with that device current -- make that first
  * call before capturing a graph.  The scratch needs no initialisation.  Calls
  * that overlap in time (other streams, other threads) share the scratch and
- * corrupt each other's results: serialise them.
+ * corrupt each other's results: serialise them.  The 64 MiB are reserved on
+ * every device that loads the library, for the life of the process, whether
+ * or not this entry point is ever called.
  */
 #define SSU_SSD_STATIC_SCRATCH_BYTES (64ull << 20)
 ssu_status ssu_ssd_prefill_static(const ssu_ssd_args *args, void *stream);
@@ -418,6 +428,22 @@ ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t ro
 ssu_status ssu_prewarm(int32_t state_dtype, int32_t io_dtype, int32_t dt_dtype,
                        int64_t heads, int64_t dim, int64_t dstate, int64_t groups,
                        int32_t packed);
+
+/*
+ * Self-test of the kernels' exit path, for tests only: ssu_update_onetoken
+ * with every bounded wait limited to `wait_cycles` SM clock cycles (1000 up
+ * to the default of about a second) and the stage of unit `withhold_unit`
+ * (units are numbered (b * heads + h) * dim_tiles + dim_tile, dim tiles of
+ * 64 rows) never filled.  The consumers' wait for that unit runs out with no
+ * copy pending; the CTA that owns the unit stops issuing copies, waits for
+ * the copies it already issued, sets SSU_DEV_TIMEOUT in *d_status and
+ * returns.  The results of that CTA's remaining units are left unwritten;
+ * every other CTA completes normally.  No device fault is involved and the
+ * context stays usable.
+ */
+ssu_status ssu_selftest_timeout(const ssu_args *args, int64_t batch, const ssu_slot_table *read,
+                                const ssu_slot_table *dst, int64_t withhold_unit, int64_t wait_cycles,
+                                void *stream);
 
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *ssu_last_error(void);

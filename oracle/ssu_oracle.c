@@ -28,7 +28,7 @@
  *     dA = exp(A[h] dt'), state = state*dA + dt'*x*B, y = state.C + D*x,
  *     optional y *= silu(z).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - head -> group map: contiguous blocks, g = h / (heads / groups).  PARITY
  *     UNPINNED by the pages (they only require divisibility).
  *   - no table at all: sequence b uses slot b for reading and writing.
@@ -374,6 +374,14 @@ int orc_ssu_run(const orc_problem *pr, char *err, int errlen)
         if (pr->num_accepted != NULL) {
             t_seed = pr->num_accepted[b] - 1;
             if (t_seed < 0) t_seed = 0;
+        }
+        /* A per-row table holds one entry per packed row ("SSU at a glance",
+         * Slot semantics): the seed step must be one of the sequence's own
+         * rows, or the entry would belong to another sequence. */
+        if (rtab != NULL && rtab->entries != NULL && rtab->mode == ORC_SLOTS_PER_ROW && t_seed >= len) {
+            set_err(err, errlen, "seed step past the rows of sequence %lld (step %lld)", b, t_seed);
+            rc = ORC_INVALID;
+            break;
         }
         if (resolve(rtab, b, t_seed, start[b], &seed[b]) != 0) {
             set_err(err, errlen, "read-table entry out of range (sequence %lld, step %lld)", b, t_seed);

@@ -27,12 +27,13 @@ update entry points from the call shape.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 from typing import Optional
 
 import torch
 
-__all__ = ["ssu_update_onetoken", "ssu_update_packed", "ssu_replay_update", "ssu_replay_verify", "ssu_shadow_refresh",
+__all__ = ["ssu_update_onetoken", "ssu_selftest_timeout", "ssu_update_packed", "ssu_replay_update", "ssu_replay_verify", "ssu_shadow_refresh",
            "ssu_ssd_prefill", "ssu_ssd_prefill_static", "ssd_combined_fwd_varlen",
            "ssu_batch_copy", "copy_table",
            "slot_copies", "ssu_prewarm",
@@ -135,6 +136,9 @@ def lib():
         p_args, p_tab = ctypes.POINTER(Args), ctypes.POINTER(SlotTable)
         L.ssu_update_onetoken.argtypes = [p_args, ctypes.c_int64, p_tab, p_tab, ctypes.c_void_p]
         L.ssu_update_onetoken.restype = ctypes.c_int
+        L.ssu_selftest_timeout.argtypes = [p_args, ctypes.c_int64, p_tab, p_tab, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p]
+        L.ssu_selftest_timeout.restype = ctypes.c_int
         L.ssu_update_packed.argtypes = [p_args, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32, p_tab, p_tab,
                                         ctypes.c_void_p]
@@ -253,6 +257,21 @@ def _stream(stream) -> int:
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
+def _on_device_of_first(fn):
+    """Run a wrapper with the device of its first tensor argument current, so
+    that the launch, the default stream and the library's per-device set-up
+    all belong to the device the operands live on."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        t = args[0] if args else next(iter(kwargs.values()), None)
+        if isinstance(t, torch.Tensor) and t.is_cuda and t.device.index != torch.cuda.current_device():
+            with torch.cuda.device(t.device):
+                return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return wrapper
+
+
+@_on_device_of_first
 def ssu_update_onetoken(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                         state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
                         out=None, disable_state_update=False, status=None, stream=None,
@@ -274,6 +293,29 @@ def ssu_update_onetoken(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_
     return out
 
 
+@_on_device_of_first
+def ssu_selftest_timeout(state, x, dt, A, B, C, withhold_unit: int, wait_cycles: int, D=None, z=None,
+                         dt_bias=None, dt_softplus=False, state_batch_indices=None, dst_state_batch_indices=None,
+                         pad_slot_id=-1, out=None, status=None, stream=None) -> torch.Tensor:
+    """Test of the kernels' exit path (``ssu_selftest_timeout`` in
+    ``include/ssu.h``): the one-token update with unit ``withhold_unit``
+    never staged and every wait limited to ``wait_cycles`` SM cycles; the
+    device status gets DEV_TIMEOUT.  Returns y (partly unwritten)."""
+    dt = _dt3(dt, x)
+    if out is None:
+        out = torch.empty_like(x)
+    a = _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, status, 0)
+    rt = _table(state_batch_indices, SLOTS_STRIDED)
+    wt = _table(dst_state_batch_indices, SLOTS_STRIDED)
+    rc = lib().ssu_selftest_timeout(ctypes.byref(a), x.shape[0], None if rt is None else ctypes.byref(rt),
+                                    None if wt is None else ctypes.byref(wt), int(withhold_unit), int(wait_cycles),
+                                    _stream(stream))
+    if rc != OK:
+        _raise(rc)
+    return out
+
+
+@_on_device_of_first
 def ssu_update_packed(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                       state_batch_indices=None, dst_state_batch_indices=None, pad_slot_id=-1,
                       out=None, disable_state_update=False, cu_seqlens=None, num_accepted_tokens=None,
@@ -332,6 +374,7 @@ def ssu_update_packed(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_so
     return out_flat
 
 
+@_on_device_of_first
 def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, count_out=None, D=None, z=None,
                       dt_bias=None, dt_softplus=False, state_batch_indices=None, pad_slot_id=-1, out=None,
                       status=None, stream=None, shadow=None, shadow_scale=None):
@@ -383,6 +426,7 @@ def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
     return out, count_out
 
 
+@_on_device_of_first
 def ssu_replay_verify(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, count_out=None, D=None, z=None,
                       dt_bias=None, dt_softplus=False, state_batch_indices=None, pad_slot_id=-1, out=None,
                       status=None, stream=None):
@@ -455,6 +499,7 @@ def _ssd_workspace(device, nbytes: int, stream) -> torch.Tensor:
     return ws
 
 
+@_on_device_of_first
 def ssu_ssd_prefill(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, last_chunk_indices=None,
                     out=None, D=None, z=None, dt_bias=None, dt_softplus=False, dt_limit=(0.0, float("inf")),
                     initial_states=None, return_intermediate_states=False, state_dtype=None, nseq=None,
@@ -505,6 +550,7 @@ def ssu_ssd_prefill(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, 
 SSD_STATIC_SCRATCH_BYTES = 64 << 20  # SSU_SSD_STATIC_SCRATCH_BYTES
 
 
+@_on_device_of_first
 def ssu_ssd_prefill_static(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, seq_idx, last_chunk_indices=None,
                            out=None, D=None, z=None, dt_bias=None, dt_softplus=False, dt_limit=(0.0, float("inf")),
                            initial_states=None, return_intermediate_states=False, state_dtype=None, nseq=None,
@@ -548,6 +594,7 @@ def ssu_ssd_prefill_static(x, dt, A, B, C, chunk_size: int, cu_chunk_seqlens, se
     return out, states
 
 
+@_on_device_of_first
 def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seqlens, last_chunk_indices, seq_idx,
                             out=None, D=None, z=None, dt_bias=None, dt_softplus=False, dt_limit=(0.0, float("inf")),
                             initial_states=None, return_intermediate_states=False, state_dtype=None,
@@ -565,6 +612,7 @@ def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seq
     return states
 
 
+@_on_device_of_first
 def ssu_shadow_refresh(state: torch.Tensor, shadow: torch.Tensor, shadow_scale: Optional[torch.Tensor] = None,
                        stream=None) -> None:
     """The low-precision read copy of a contiguous state tensor ``[..., dstate]``
@@ -585,6 +633,7 @@ def ssu_shadow_refresh(state: torch.Tensor, shadow: torch.Tensor, shadow_scale: 
         _raise(rc)
 
 
+@_on_device_of_first
 def ssu_batch_copy(copies: torch.Tensor, max_bytes: int, status: Optional[torch.Tensor] = None,
                    stream=None) -> None:
     """Batched copies with memmove semantics (see ``include/ssu.h``).
@@ -634,6 +683,7 @@ def ssu_prewarm(*, state_dtype: torch.dtype, io_dtype: torch.dtype, heads: int, 
         _raise(rc)
 
 
+@_on_device_of_first
 def selective_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=False,
                            state_batch_indices=None, pad_slot_id=-1, state_scale=None, out=None,
                            disable_state_update=False, intermediate_states_buffer=None,

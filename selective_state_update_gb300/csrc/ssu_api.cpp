@@ -107,6 +107,7 @@ ssu_status prepare(const ssu_args *a, int64_t rows, const ssu_slot_table *read, 
         return fail(SSU_ERR_INVALID, "x, dt, B, C and y must not be NULL");
     if (reinterpret_cast<uintptr_t>(a->state) % 16 != 0)
         return fail(SSU_ERR_INVALID, "state must be 16-byte aligned");
+
     if (rows > 0 && (a->y == a->x || a->y == a->z || a->y == a->dt || a->y == a->B || a->y == a->C ||
                      a->y == a->state))
         return fail(SSU_ERR_INVALID, "y must not alias an input");
@@ -148,6 +149,44 @@ ssu_status prepare(const ssu_args *a, int64_t rows, const ssu_slot_table *read, 
         kp->ys[i] = a->y_stride[i];
     }
     kp->status = a->d_status;
+    kp->wait_cycles = ssu::kDefaultWaitCycles;
+    kp->withhold_unit = -1;
+    return SSU_OK;
+}
+
+bool aligned16(const void *q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; }
+
+// Which small operands the packed kernel can stage with bulk copies: every
+// row it copies (B, C: dstate values of one row and group; x, z, dt: up to 64
+// dim rows of one row and head) starts on a 16-byte boundary and is a
+// multiple of 16 bytes long.
+int32_t packed_bulk_ops(const ssu_args *a) {
+    const int64_t io = a->io_dtype == SSU_F32 ? 4 : 2, dts = a->dt_dtype == SSU_F32 ? 4 : 2;
+    auto rows_ok = [](const void *base, const int64_t *st, int64_t sz, int64_t count) {
+        return base != nullptr && aligned16(base) && st[2] == 1 && (st[0] * sz) % 16 == 0 && (st[1] * sz) % 16 == 0 &&
+               (count * sz) % 16 == 0;
+    };
+    int32_t ops = 0;
+    if (rows_ok(a->B, a->B_stride, io, a->dstate) && rows_ok(a->C, a->C_stride, io, a->dstate)) ops |= ssu::kBulkBC;
+    if (rows_ok(a->x, a->x_stride, io, a->dim) && (a->z == nullptr || rows_ok(a->z, a->z_stride, io, a->dim)))
+        ops |= ssu::kBulkXZ;
+    if (rows_ok(a->dt, a->dt_stride, dts, a->dim)) ops |= ssu::kBulkDT;
+    return ops;
+}
+
+// The kernels launch on the current device: a state pool that lives on
+// another device would be addressed from the wrong one.  Checked right before
+// a launch, after every host check.
+ssu_status check_device(const void *state) {
+    int dev = -1;
+    cudaPointerAttributes pa;
+    if (cudaGetDevice(&dev) != cudaSuccess) return fail(SSU_ERR_CUDA, "no current CUDA device");
+    if (cudaPointerGetAttributes(&pa, state) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SSU_ERR_INVALID, "the state pointer is not one the CUDA runtime knows");
+    }
+    if (pa.type == cudaMemoryTypeDevice && pa.device != dev)
+        return fail(SSU_ERR_INVALID, "the state is on device %d but device %d is current", pa.device, dev);
     return SSU_OK;
 }
 
@@ -173,8 +212,30 @@ ssu_status ssu_update_onetoken(const ssu_args *args, int64_t batch, const ssu_sl
     if (batch * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "batch * heads * dim tiles exceeds 2^31-1");
     kp.nseq = batch;
     kp.rows = batch;
+    if ((st = check_device(args->state)) != SSU_OK) return st;
     return launched(ssu::launch_onetoken(args->state_dtype, lanes, kp, batch,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+ssu_status ssu_selftest_timeout(const ssu_args *args, int64_t batch, const ssu_slot_table *read,
+                                const ssu_slot_table *dst, int64_t withhold_unit, int64_t wait_cycles,
+                                void *stream) {
+    ssu::KParams kp;
+    int lanes = 0;
+    if (batch <= 0) return fail(SSU_ERR_INVALID, "batch must be positive");
+    ssu_status st = prepare(args, batch, read, dst, &kp, &lanes);
+    if (st != SSU_OK) return st;
+    if (batch * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "batch * heads * dim tiles exceeds 2^31-1");
+    if (withhold_unit < 0 || withhold_unit >= batch * kp.H * kp.ptiles)
+        return fail(SSU_ERR_INVALID, "withhold_unit must name a unit of the call");
+    if (wait_cycles < 1000 || wait_cycles > ssu::kDefaultWaitCycles)
+        return fail(SSU_ERR_INVALID, "wait_cycles must be in [1000, %lld]", (long long)ssu::kDefaultWaitCycles);
+    kp.nseq = batch;
+    kp.rows = batch;
+    kp.withhold_unit = withhold_unit;
+    kp.wait_cycles = wait_cycles;
+    if ((st = check_device(args->state)) != SSU_OK) return st;
+    return launched(ssu::launch_onetoken(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
 }
 
 ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows, const void *cu_seqlens,
@@ -195,12 +256,16 @@ ssu_status ssu_update_packed(const ssu_args *args, int64_t nseq, int64_t rows, c
     }
     if (nseq == 0 || rows == 0) return ok();  // nothing to read or write
     if (nseq * kp.H * kp.ptiles > kMaxGrid) return fail(SSU_ERR_INVALID, "nseq * heads * dim tiles exceeds 2^31-1");
+    if ((rows + nseq) > (int64_t(1) << 40) / (static_cast<int64_t>(kp.H) * kp.ptiles))
+        return fail(SSU_ERR_INVALID, "(rows + nseq) * heads * dim tiles exceeds 2^40");
     kp.nseq = nseq;
     kp.rows = rows;
+    kp.bulk_ops = packed_bulk_ops(args);
     kp.steps = cu_seqlens == nullptr ? steps : 0;
     kp.cu = cu_seqlens;
     kp.acc = num_accepted;
     kp.meta_is_i64 = meta_type == SSU_I64;
+    if ((st = check_device(args->state)) != SSU_OK) return st;
     return launched(ssu::launch_packed(args->state_dtype, lanes, kp, static_cast<cudaStream_t>(stream)));
 }
 
@@ -251,6 +316,7 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
         kp.shadow = rb->shadow;
         kp.shadow_scale = rb->shadow_scale;
     }
+    if ((st = check_device(args->state)) != SSU_OK) return st;
     return launched(ssu::launch_replay(args->state_dtype, lanes, kp, batch, static_cast<cudaStream_t>(stream)));
 }
 
@@ -286,6 +352,7 @@ ssu_status ssu_replay_verify(const ssu_args *args, int64_t batch, int64_t ntok, 
     kp.Bbuf = rb->B;
     kp.cnt_in = rb->count_in;
     kp.cnt_out = rb->count_out;
+    if ((st = check_device(args->state)) != SSU_OK) return st;
     return launched(ssu::launch_verify(args->state_dtype, kp, batch, static_cast<int>(ntok),
                                        static_cast<cudaStream_t>(stream)));
 }

@@ -251,16 +251,57 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for phase `parity` of `bar`; gives up after about a second of
-// SM clock cycles (a copy that never lands) and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of `bar`; gives up after `limit` SM clock cycles
+// (about a second at the default: a copy that never lands), or after 2^26
+// polls, and returns false.
+constexpr long long kWaitCycles = kDefaultWaitCycles;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 0; i < (1u << 26); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > 2000000000LL) break;
+        if (clock64() - t0 > limit) break;
     }
     return false;
+}
+
+// Exit of the ring kernels (one-token, packed, checkpoint + buffer).  Every
+// wait is bounded.  When one gives up, its role sets `abort` and leaves; the
+// producers stop filling stages once they see it.  All roles then meet at
+// the CTA's last barrier, and one consumer thread waits (bounded) for every
+// stage whose fill was issued but not consumed, so that no bulk copy still
+// targets the CTA's shared memory when it retires.  `filled[s]` is the round
+// of the last fill issued on stage s, plus one (0: none); fills of a stage
+// come in order and a refill needs the previous round consumed, so at most
+// one fill per stage is outstanding.
+constexpr int kMaxRingStages = 8;
+struct RingExit {
+    int abort;
+    int filled[kMaxRingStages];
+};
+
+__device__ __forceinline__ void ring_init(RingExit *r) {
+    r->abort = 0;
+    for (int s = 0; s < kMaxRingStages; ++s) r->filled[s] = 0;
+}
+__device__ __forceinline__ bool ring_aborted(const RingExit *r) {
+    return *reinterpret_cast<const volatile int *>(&r->abort) != 0;
+}
+__device__ __forceinline__ void ring_abort(RingExit *r) { *reinterpret_cast<volatile int *>(&r->abort) = 1; }
+// By the producer lane that issued the fill, after issuing its copies.
+__device__ __forceinline__ void ring_note_fill(RingExit *r, int s, int round) {
+    *reinterpret_cast<volatile int *>(&r->filled[s]) = round + 1;
+}
+// After the last barrier, by the consumer thread that counted `consumed`
+// stages (the ring index of the first stage it did not consume).
+__device__ __forceinline__ void ring_drain(const RingExit *r, uint64_t *full, int stages, long long consumed,
+                                          long long limit, int32_t *status) {
+    for (int s = 0; s < stages; ++s) {
+        const int f = *reinterpret_cast<const volatile int *>(&r->filled[s]);
+        if (f == 0) continue;
+        const long long k = static_cast<long long>(f - 1) * stages + s;
+        if (k >= consumed && !mbar_wait_bounded(&full[s], (f - 1) & 1, limit)) flag(status, kDevTimeout);
+    }
 }
 
 // Streaming (evict-first) 16-byte accesses: each state byte is used once.
@@ -355,16 +396,18 @@ __device__ __forceinline__ float step_size(float dt, float bias, int softplus) {
 }
 
 // One token applied to this thread's 16 elements of one state row:
-// S = S * dA + (dt' x) * B, and the partial sum of S * C over those elements.
+// S = S * dA + (dt' x) * B, and the partial sum of S * C over those elements
+// (four interleaved partial sums, so that the dependent chain is four FMAs
+// long instead of sixteen; every kernel uses this order).
 __device__ __forceinline__ float update_elems(float *s, const float *b, const float *c, float dA,
                                               float dtx) {
-    float acc = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < kElemsPerThread; ++i) {
         s[i] = fmaf(s[i], dA, dtx * b[i]);
-        acc = fmaf(s[i], c[i], acc);
+        acc[i % 4] = fmaf(s[i], c[i], acc[i % 4]);
     }
-    return acc;
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // y = (sum + D x) * gate, gate = silu(z) (or 1 without z).

@@ -9,10 +9,7 @@
 namespace ssu {
 
 // Each thread holds kRowsPerThread rows x kElemsPerThread dstate elements.
-#ifndef SSU_ROWS_PER_THREAD
-#define SSU_ROWS_PER_THREAD 4
-#endif
-constexpr int kRowsPerThread = SSU_ROWS_PER_THREAD;
+constexpr int kRowsPerThread = 4;
 // Rows of one (head, dim-tile) work unit: kTileRows dim rows of one head of
 // one sequence.
 constexpr int kTileRows = 16 * kRowsPerThread;
@@ -20,16 +17,9 @@ constexpr int kElemsPerThread = 16;
 // Row slots per CTA: kTileRows / kRowsPerThread.  A CTA has
 // kRowSlots * L threads, L = dstate / kElemsPerThread lanes per row.
 constexpr int kRowSlots = kTileRows / kRowsPerThread;
-// How many of a thread's rows the compute loops keep in flight at once
-// (more rows: more loads in flight, more registers, fewer resident CTAs).
-#ifndef SSU_ONETOKEN_UNROLL
-#define SSU_ONETOKEN_UNROLL 2
-#endif
-#ifndef SSU_PACKED_UNROLL
-#define SSU_PACKED_UNROLL 2
-#endif
-constexpr int kOnetokenUnroll = SSU_ONETOKEN_UNROLL;
-constexpr int kPackedUnroll = SSU_PACKED_UNROLL;
+// How many of a thread's rows the one-token compute loop keeps in flight at
+// once (more rows: more loads in flight, more registers, fewer resident CTAs).
+constexpr int kOnetokenUnroll = 2;
 
 struct SlotTab {
     const void *entries;  // nullptr: no table
@@ -71,7 +61,19 @@ struct KParams {
     int32_t shadow_fmt;
     void *shadow;
     float *shadow_scale;
+    // bounded waits: SM clock cycles before a wait gives up
+    int64_t wait_cycles;
+    // self-test of the exit path (ssu_selftest_timeout): the one-token
+    // producer skips the copy and the arrival of this unit (-1: none)
+    int64_t withhold_unit;
+    // packed kernel: which small operands arrive by bulk copies (kBulk* bits)
+    int32_t bulk_ops;
 };
+
+enum : int32_t { kBulkBC = 1, kBulkXZ = 2, kBulkDT = 4 };
+
+// SM clock cycles a bounded wait allows by default (about a second).
+constexpr int64_t kDefaultWaitCycles = 2000000000LL;
 
 enum : int32_t { kShadowNone = 0, kShadowF16 = 1, kShadowE4M3 = 2 };
 
@@ -79,6 +81,11 @@ enum : int32_t { kShadowNone = 0, kShadowF16 = 1, kShadowE4M3 = 2 };
 cudaError_t launch_onetoken(int state_dtype, int lanes, const KParams &p, int64_t batch,
                             cudaStream_t stream);
 cudaError_t launch_packed(int state_dtype, int lanes, const KParams &p, cudaStream_t stream);
+// The packed kernel for long sequences (one CTA per unit), which
+// launch_packed picks when rows >= kLongRowsPerSeq * nseq.
+constexpr int64_t kLongRowsPerSeq = 6;
+cudaError_t launch_packed_long(int state_dtype, int lanes, const KParams &p, cudaStream_t stream);
+cudaError_t prewarm_packed_long(int state_dtype, int lanes);
 // Load the kernel's module and read its attributes (no launch).
 cudaError_t prewarm_onetoken(int state_dtype, int lanes);
 cudaError_t prewarm_packed(int state_dtype, int lanes);

@@ -40,23 +40,8 @@ namespace ssu {
 constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Size of the pieces a state tile is moved in by the TMA engine.
-#ifndef SSU_LOAD_CHUNK
-#define SSU_LOAD_CHUNK 32768
-#endif
-#ifndef SSU_STORE_CHUNK
-#define SSU_STORE_CHUNK 32768
-#endif
-constexpr int kLoadChunk = SSU_LOAD_CHUNK;
-#ifndef SSU_ONETOKEN_CTAS
-#define SSU_ONETOKEN_CTAS 0
-#endif
-#ifndef SSU_PRODUCER_WARPS
-#define SSU_PRODUCER_WARPS 2
-#endif
-#ifndef SSU_DIRECT_STORE
-#define SSU_DIRECT_STORE 0
-#endif
-constexpr int kStoreChunk = SSU_STORE_CHUNK;
+constexpr int kLoadChunk = 32768;
+constexpr int kStoreChunk = 32768;
 
 template <typename TS, int L>
 struct OnetokenPipe {
@@ -64,24 +49,23 @@ struct OnetokenPipe {
     static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
     static constexpr int kStageBytes = align_up(kTileBytes + 2 * kN * 4 + kTileRows * 16 + 32, 128);
     // Dynamic shared memory an SM can give its CTAs (228 KB less the 1 KB
-    // each CTA reserves).  Small (16-bit) stages: three CTAs of four stages,
-    // so three consumer groups share the SM; fp32 stages: two CTAs of three.
+    // each CTA reserves, less a margin).  Small (16-bit) stages: three CTAs
+    // of four stages, so three consumer groups share the SM; fp32 stages: two
+    // CTAs of three.  The launcher reads how many CTAs the device really
+    // holds.
     static constexpr int kSmemPerSm = 222 * 1024;
-    static constexpr int kCtasPerSm = (SSU_ONETOKEN_CTAS > 0 &&
-                                       (kSmemPerSm / (SSU_ONETOKEN_CTAS > 0 ? SSU_ONETOKEN_CTAS : 1) - 1024) /
-                                               kStageBytes >= 2)
-                                          ? SSU_ONETOKEN_CTAS
-                                      : (kSmemPerSm / 3 - 1024) / kStageBytes >= 4 ? 3
+    static constexpr int kCtasPerSm = (kSmemPerSm / 3 - 1024) / kStageBytes >= 4   ? 3
                                       : (kSmemPerSm / 2 - 1024) / kStageBytes >= 3 ? 2
                                                                                    : 1;
     static constexpr int kRingBytes = kSmemPerSm / kCtasPerSm - 1024;
     static constexpr int kStages = (kRingBytes / kStageBytes) < 6 ? (kRingBytes / kStageBytes) : 6;
     static constexpr int kBarOffset = kStages * kStageBytes;
-    static constexpr int kBytes = kBarOffset + kStages * 16;
+    static constexpr int kExitOffset = kBarOffset + kStages * 16;
+    static constexpr int kBytes = kExitOffset + static_cast<int>(sizeof(RingExit));
     static constexpr int kConsumerWarps = (Tile<TS, L>::kThreads + 31) / 32;
-    static constexpr int kProducerWarps = SSU_PRODUCER_WARPS;
+    static constexpr int kProducerWarps = 2;
     static constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
-    static_assert(kStages >= 2, "state tile too large for a pipelined ring");
+    static_assert(kStages >= 2 && kStages <= kMaxRingStages, "state tile too large for a pipelined ring");
     // A producer waits for stage s to be free by the parity of the "empty"
     // phase it needs.  When it starts unit k it has finished its previous unit
     // k - kProducerWarps, whose wait guaranteed that every unit up to
@@ -116,20 +100,29 @@ struct StageView {
     }
 };
 
-// Stage one unit: header, B, C, row scalars, then the tile copy (or a plain
-// arrival when there is nothing to copy).  Returns false on a timed-out wait.
+// Stage one unit (global index u): header, B, C, row inputs, then the tile
+// copy (or a plain arrival when there is nothing to copy).  Returns false
+// when the CTA stops: a wait gave up or another role did.
 template <typename TS, int L>
-__device__ __forceinline__ bool produce_unit(const KParams &p, const UnitOperands<TS, L> &op, int k,
-                                             unsigned char *smem, uint64_t *full, uint64_t *empty, int lane) {
+__device__ __forceinline__ bool produce_unit(const KParams &p, const UnitOperands<TS, L> &op, int k, int64_t u,
+                                             unsigned char *smem, uint64_t *full, uint64_t *empty, RingExit *rx,
+                                             int lane) {
     using PS = OnetokenPipe<TS, L>;
     constexpr int N = PS::kN;
     constexpr int S = PS::kStages;
     const int s = k % S;
     const int round = k / S;
-    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1)) {
-        if (lane == 0) flag(p.status, kDevTimeout);
+    if (ring_aborted(rx)) return false;
+    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1, p.wait_cycles)) {
+        if (lane == 0) {
+            flag(p.status, kDevTimeout);
+            ring_abort(rx);
+        }
         return false;
     }
+    // Self-test of the exit path: this unit's stage is never filled, so the
+    // consumers' wait for it runs out with no copy pending.
+    if (u == p.withhold_unit) return true;
     const StageView<TS, L> st(smem, s);
     int32_t flags = 0;
     if (lane == 0) {
@@ -175,8 +168,10 @@ __device__ __forceinline__ bool produce_unit(const KParams &p, const UnitOperand
             const uint32_t n = bytes - off < static_cast<uint32_t>(kLoadChunk) ? bytes - off : kLoadChunk;
             bulk_load(dst + off, src + off, n, &full[s]);
         }
+        if (lane == 0) ring_note_fill(rx, s, round);
         if (lane != 0) mbar_arrive(&full[s]);
     } else {
+        if (lane == 0) ring_note_fill(rx, s, round);
         mbar_arrive(&full[s]);
     }
     return true;
@@ -186,7 +181,7 @@ __device__ __forceinline__ bool produce_unit(const KParams &p, const UnitOperand
 // w + 2P, ... (P = kProducerWarps), i.e. global units blockIdx.x + k * gridDim.x.
 template <typename TS, int L>
 __device__ __forceinline__ void onetoken_producer(const KParams &p, int64_t units, unsigned char *smem,
-                                                  uint64_t *full, uint64_t *empty, int w) {
+                                                  uint64_t *full, uint64_t *empty, RingExit *rx, int w) {
     constexpr int P = OnetokenPipe<TS, L>::kProducerWarps;
     const int lane = threadIdx.x & 31;
     const int64_t step = static_cast<int64_t>(P) * gridDim.x;
@@ -199,17 +194,18 @@ __device__ __forceinline__ void onetoken_producer(const KParams &p, int64_t unit
     for (int k = w; u < units; k += 2 * P, u += 2 * step) {
         walk.advance(p);
         if (u + step < units) b.load(p, walk.coords(p), lane);
-        if (!produce_unit<TS, L>(p, a, k, smem, full, empty, lane)) return;
+        if (!produce_unit<TS, L>(p, a, k, u, smem, full, empty, rx, lane)) return;
         if (u + step >= units) break;
         walk.advance(p);
         if (u + 2 * step < units) a.load(p, walk.coords(p), lane);
-        if (!produce_unit<TS, L>(p, b, k + P, smem, full, empty, lane)) return;
+        if (!produce_unit<TS, L>(p, b, k + P, u + step, smem, full, empty, rx, lane)) return;
     }
 }
 
+// Returns the ring index of the first unit not consumed.
 template <typename TS, int L>
-__device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t units, unsigned char *smem,
-                                                  uint64_t *full, uint64_t *empty) {
+__device__ __forceinline__ int onetoken_consumer(const KParams &p, int64_t units, unsigned char *smem,
+                                                 uint64_t *full, uint64_t *empty, RingExit *rx) {
     using T = Tile<TS, L>;
     using PS = OnetokenPipe<TS, L>;
     constexpr int N = PS::kN;
@@ -224,13 +220,14 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
     UnitWalker walk(p, blockIdx.x, gridDim.x);
     for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++k, walk.advance(p)) {
         const int s = k % S;
-        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1);
+        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1, p.wait_cycles);
         if (barrier_or(1, kConsumers, !ok)) {  // a wait gave up: every consumer stops here
             if (tid == 0) {
                 flag(p.status, kDevTimeout);
+                ring_abort(rx);
                 bulk_wait_all();
             }
-            return;
+            return k;
         }
         const StageView<TS, L> st(smem, s);
         const int32_t flags = st.hd->flags;
@@ -245,10 +242,6 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
             named_barrier(1, kConsumers);
             if (active) {
                 const float Dh = st.hd->Dh;
-#if SSU_DIRECT_STORE
-                TS *dst = static_cast<TS *>(p.state) +
-                          ((st.hd->ws * p.H + c.h) * static_cast<int64_t>(p.P) + c.row0) * N;
-#endif
                 float bv[kElemsPerThread], cv[kElemsPerThread];
                 T::gather(st.B, lane, bv);
                 T::gather(st.C, lane, cv);
@@ -269,22 +262,13 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
                         if (lane == 0)
                             store_small(p.y, c.b * p.ys[0] + c.h * p.ys[1] + (c.row0 + rr) * p.ys[2], p.io_dtype,
                                         output(sum, Dh, q.z, q.w));
-#if SSU_DIRECT_STORE
-                        if (flags & kUnitWrite) T::store_row(dst + rr * N, lane, sv);
-#else
                         // The new state goes back into the stage; the TMA
                         // engine writes the whole tile to its destination.
                         T::store_row_smem(st.tile + rr * N, lane, sv);
-#endif
                     }
                 }
             }
         }
-#if SSU_DIRECT_STORE
-        __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(&empty[s]);
-        continue;
-#endif
         fence_proxy_async_smem();
         named_barrier(1, kConsumers);
         if (tid == 0) {
@@ -308,6 +292,7 @@ __device__ __forceinline__ void onetoken_consumer(const KParams &p, int64_t unit
         prev_s = s;
     }
     if (tid == 0) bulk_wait_all();
+    return k;
 }
 
 // Register budget of the kernel (the min-CTAs launch bound): for 16-bit pools
@@ -328,18 +313,23 @@ __global__ void __launch_bounds__(OnetokenPipe<TS, L>::kThreads, (onetoken_min_c
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + PS::kBarOffset);
     uint64_t *empty = full + PS::kStages;
+    RingExit *rx = reinterpret_cast<RingExit *>(smem + PS::kExitOffset);
     if (threadIdx.x == 0) {
         for (int s = 0; s < PS::kStages; ++s) {
             mbar_init(&full[s], 32);
-            mbar_init(&empty[s], SSU_DIRECT_STORE ? PS::kConsumerWarps : 1);
+            mbar_init(&empty[s], 1);
         }
+        ring_init(rx);
     }
     __syncthreads();
     const int warp = threadIdx.x / 32;
+    int consumed = 0;
     if (warp >= PS::kConsumerWarps)
-        onetoken_producer<TS, L>(p, units, smem, full, empty, warp - PS::kConsumerWarps);
+        onetoken_producer<TS, L>(p, units, smem, full, empty, rx, warp - PS::kConsumerWarps);
     else
-        onetoken_consumer<TS, L>(p, units, smem, full, empty);
+        consumed = onetoken_consumer<TS, L>(p, units, smem, full, empty, rx);
+    __syncthreads();
+    if (threadIdx.x == 0) ring_drain(rx, full, PS::kStages, consumed, p.wait_cycles, p.status);
 }
 
 // Number of SMs of the current device (cached per device).
@@ -357,30 +347,39 @@ static int sm_count() {
 }
 
 // The ring needs more than the 48 KiB default of dynamic shared memory: opt
-// in once per device.
+// in once per device, then read how many CTAs of the kernel an SM of this
+// device holds (cached per device).
 template <typename TS, int L>
-static cudaError_t smem_opt_in() {
-    static std::atomic<unsigned long long> done{0};
+static cudaError_t resident_ctas(int *ctas) {
+    static std::atomic<int> cache[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (done.load(std::memory_order_relaxed) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(ssu_onetoken_kernel<TS, L>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             OnetokenPipe<TS, L>::kBytes);
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_relaxed);
-    return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        using PS = OnetokenPipe<TS, L>;
+        e = cudaFuncSetAttribute(ssu_onetoken_kernel<TS, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, PS::kBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ssu_onetoken_kernel<TS, L>, PS::kThreads, PS::kBytes);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    *ctas = n;
+    return cudaSuccess;
 }
 
 template <typename TS, int L>
 static cudaError_t launch_t(const KParams &p, int64_t batch, cudaStream_t stream) {
     using PS = OnetokenPipe<TS, L>;
-    cudaError_t e = smem_opt_in<TS, L>();
+    int per_sm = 0;
+    cudaError_t e = resident_ctas<TS, L>(&per_sm);
     if (e != cudaSuccess) return e;
     const int64_t units = batch * p.H * p.ptiles;
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    const int64_t slots_on_gpu = static_cast<int64_t>(sms) * PS::kCtasPerSm;
+    const int64_t slots_on_gpu = static_cast<int64_t>(sms) * per_sm;
     const int64_t grid = units < slots_on_gpu ? units : slots_on_gpu;
     ssu_onetoken_kernel<TS, L><<<static_cast<unsigned>(grid), PS::kThreads, PS::kBytes, stream>>>(p, units);
     return cudaGetLastError();
@@ -414,7 +413,8 @@ static cudaError_t attrs_t() {
     cudaError_t e = cudaFuncGetAttributes(&a, ssu_onetoken_kernel<TS, L>);
     if (e != cudaSuccess) return e;
     if (sm_count() <= 0) return cudaErrorInvalidDevice;
-    return smem_opt_in<TS, L>();
+    int per_sm = 0;
+    return resident_ctas<TS, L>(&per_sm);
 }
 
 template <typename TS>

@@ -47,17 +47,11 @@
 
 namespace ssu {
 
-#ifndef SSU_REPLAY_CTAS
-#define SSU_REPLAY_CTAS 0
-#endif
-#ifndef SSU_REPLAY_MAX_STAGES
-#define SSU_REPLAY_MAX_STAGES 6
-#endif
+// Most stages of a ring.
+constexpr int kReplayMaxStages = 6;
+static_assert(kReplayMaxStages <= kMaxRingStages, "ring exit record too small");
 // Size of the pieces the checkpoint tile is requested in (lanes in turn).
-#ifndef SSU_REPLAY_TILE_CHUNK
-#define SSU_REPLAY_TILE_CHUNK 32768
-#endif
-constexpr uint32_t kReplayTileChunk = SSU_REPLAY_TILE_CHUNK;
+constexpr uint32_t kReplayTileChunk = 32768;
 
 template <typename TS, int L>
 struct ReplayPipe {
@@ -74,13 +68,12 @@ struct ReplayPipe {
     // largest copy tile (one byte per element), inside the checkpoint tile.
     static constexpr int kShadowScaleOffset = kTileRows * kN;
     static_assert(kShadowScaleOffset + kTileRows * 4 <= kTileBytes, "read-copy scales do not fit the tile");
-    // Dynamic shared memory an SM can give its CTAs (228 KB less 1 KB per CTA).
-    static constexpr int kSmemPerSm = 222 * 1024;
     // Register budget: two CTAs per SM where a tile and a few KB of entries
-    // fit twice in half of the SM's shared memory and two CTAs still leave
-    // 128 registers a thread.
+    // fit twice in half of an SM's shared memory (228 KB on this part, less a
+    // margin) and two CTAs still leave 128 registers a thread.  The ring
+    // itself is sized at launch from the device's shared memory per SM.
     static constexpr int kMinCtas =
-        (kSmemPerSm / 2 - 1024) / (kTileBytes + 4096) >= 2 && 65536 / (2 * kThreads) >= 128 ? 2 : 1;
+        (222 * 1024 / 2 - 1024) / (kTileBytes + 4096) >= 2 && 65536 / (2 * kThreads) >= 128 ? 2 : 1;
 };
 
 // Per-stage header written by the producer.
@@ -108,7 +101,7 @@ constexpr int kDtStride = kTileRows + 4;
 // C dots; per-entry decays and input terms of a fold) and the mbarriers.
 struct ReplayLayout {
     int xe, de, be, bc, cs, rowq, hd, stage;
-    int stages, producers, dots, rowa, rowb, bars, bytes, ctas;
+    int stages, producers, dots, rowa, rowb, bars, exit, bytes, ctas;
 
     __host__ __device__ static int up(int v) { return (v + 127) / 128 * 128; }
 
@@ -130,25 +123,26 @@ struct ReplayLayout {
         rowa = up(dots + len * 4);                             // f32 [len - 1][kTileRows]
         rowb = up(rowa + (len - 1) * kTileRows * 4);           // f32 [len - 1][kTileRows]
         bars = up(rowb + (len - 1) * kTileRows * 4);           // u64 full[stages], empty[stages]
-        bytes = bars + 2 * 8 * stages;
+        exit = bars + 2 * 8 * stages;                          // RingExit
+        bytes = exit + static_cast<int>(sizeof(RingExit));
     }
     static int scratch(int len) {
-        return up(len * 4) + 2 * up((len - 1) * kTileRows * 4) + 2 * 8 * SSU_REPLAY_MAX_STAGES;
+        return up(len * 4) + 2 * up((len - 1) * kTileRows * 4) + 2 * 8 * kReplayMaxStages +
+               static_cast<int>(sizeof(RingExit));
     }
     // Two CTAs per SM when registers allow two (max_ctas) and each still gets
     // a ring of two stages, else one CTA with as many stages as fit (at most
-    // SSU_REPLAY_MAX_STAGES; a single stage -- fp32 checkpoints of dstate 256
-    // with long fp32 buffers -- runs without overlap).  Returns false when
-    // not even one stage fits.
+    // kReplayMaxStages; a single stage -- fp32 checkpoints of dstate 256 with
+    // long fp32 buffers -- runs without overlap).  `smem_per_sm` is what the
+    // CTAs of an SM may take in all.  Returns false when not even one stage
+    // fits.
     bool choose(int tile_bytes, int n, int len, int io, int smem_per_sm, int max_ctas, int max_producers) {
         place(tile_bytes, n, len, io);
         const int sc = scratch(len);
         auto fit = [&](int k) { return (smem_per_sm / k - 1024 - sc) / stage; };
-        ctas = SSU_REPLAY_CTAS > 0 && SSU_REPLAY_CTAS <= max_ctas && fit(SSU_REPLAY_CTAS) >= 2
-                   ? SSU_REPLAY_CTAS
-                   : (max_ctas >= 2 && fit(2) >= 2 ? 2 : 1);
+        ctas = max_ctas >= 2 && fit(2) >= 2 ? 2 : 1;
         stages = fit(ctas);
-        if (stages > SSU_REPLAY_MAX_STAGES) stages = SSU_REPLAY_MAX_STAGES;
+        if (stages > kReplayMaxStages) stages = kReplayMaxStages;
         if (stages < 1) return false;
         producers = stages < max_producers ? stages : max_producers;
         finish(len);
@@ -433,7 +427,7 @@ struct ReplayOperands : UnitOperands<TS, L> {
 template <typename TS, int L, int IO, int SH>
 __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLayout &lay,
                                                const ReplayOperands<TS, L> &op, int k, unsigned char *smem,
-                                               uint64_t *full, uint64_t *empty, int lane) {
+                                               uint64_t *full, uint64_t *empty, RingExit *rx, int lane) {
     constexpr int N = ReplayPipe<TS, L>::kN;
     constexpr int io = IO == kF32 ? 4 : 2;
     constexpr int kPerB = UnitOperands<TS, L>::kPerB;
@@ -500,8 +494,12 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
     }
 
     // Then the stage: header, B, C, row scalars, the copies.
-    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1)) {
-        if (lane == 0) flag(p.status, kDevTimeout);
+    if (ring_aborted(rx)) return false;
+    if (round > 0 && !mbar_wait_bounded(&empty[s], (round - 1) & 1, p.wait_cycles)) {
+        if (lane == 0) {
+            flag(p.status, kDevTimeout);
+            ring_abort(rx);
+        }
         return false;
     }
     unsigned char *base = smem + s * lay.stage;
@@ -597,6 +595,7 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
                       static_cast<uint32_t>(N) * io, &full[s]);
         }
     }
+    if (lane == 0) ring_note_fill(rx, s, round);
     if (lane != 0) mbar_arrive(&full[s]);
     return true;
 }
@@ -605,7 +604,8 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
 // (P = lay.producers), i.e. global units blockIdx.x + k * gridDim.x.
 template <typename TS, int L, int IO, int SH>
 __device__ __forceinline__ void replay_producer(const KParams &p, const ReplayLayout &lay, int64_t units,
-                                                unsigned char *smem, uint64_t *full, uint64_t *empty, int w) {
+                                                unsigned char *smem, uint64_t *full, uint64_t *empty, RingExit *rx,
+                                                int w) {
     const int P = lay.producers;
     if (w >= P) return;
     const int lane = threadIdx.x & 31;
@@ -617,17 +617,18 @@ __device__ __forceinline__ void replay_producer(const KParams &p, const ReplayLa
     for (int k = w; u < units; k += 2 * P, u += 2 * step) {
         walk.advance(p);
         if (u + step < units) b.load(p, walk.coords(p), lane);
-        if (!produce_replay<TS, L, IO, SH>(p, lay, a, k, smem, full, empty, lane)) return;
+        if (!produce_replay<TS, L, IO, SH>(p, lay, a, k, smem, full, empty, rx, lane)) return;
         if (u + step >= units) break;
         walk.advance(p);
         if (u + 2 * step < units) a.load(p, walk.coords(p), lane);
-        if (!produce_replay<TS, L, IO, SH>(p, lay, b, k + P, smem, full, empty, lane)) return;
+        if (!produce_replay<TS, L, IO, SH>(p, lay, b, k + P, smem, full, empty, rx, lane)) return;
     }
 }
 
+// Returns the ring index of the first unit not consumed.
 template <typename TS, int L, int IO, int SH>
-__device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLayout &lay, int64_t units,
-                                                unsigned char *smem, uint64_t *full, uint64_t *empty) {
+__device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLayout &lay, int64_t units,
+                                               unsigned char *smem, uint64_t *full, uint64_t *empty, RingExit *rx) {
     using T = Tile<TS, L>;
     using PS = ReplayPipe<TS, L>;
     constexpr int N = PS::kN;
@@ -646,13 +647,14 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
     UnitWalker walk(p, blockIdx.x, gridDim.x);
     for (int64_t u = blockIdx.x; u < units; u += gridDim.x, ++k, walk.advance(p)) {
         const int s = k % S;
-        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1);
+        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1, p.wait_cycles);
         if (barrier_or(1, kConsumers, !ok)) {  // a wait gave up: every consumer stops here
             if (tid == 0) {
                 flag(p.status, kDevTimeout);
+                ring_abort(rx);
                 bulk_wait_all();
             }
-            return;
+            return k;
         }
         unsigned char *base = smem + s * lay.stage;
         const ReplayHeader *hd = reinterpret_cast<const ReplayHeader *>(base + lay.hd);
@@ -847,6 +849,7 @@ __device__ __forceinline__ void replay_consumer(const KParams &p, const ReplayLa
         }
     }
     if (tid == 0) bulk_wait_all();
+    return k;
 }
 
 template <typename TS, int L, int IO, int SH>
@@ -856,18 +859,47 @@ __global__ void __launch_bounds__(ReplayPipe<TS, L>::kThreads, ReplayPipe<TS, L>
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + lay.stages;
+    RingExit *rx = reinterpret_cast<RingExit *>(smem + lay.exit);
     if (threadIdx.x == 0) {
         for (int s = 0; s < lay.stages; ++s) {
             mbar_init(&full[s], 32);
             mbar_init(&empty[s], 1);
         }
+        ring_init(rx);
     }
     __syncthreads();
     const int warp = threadIdx.x / 32;
+    int consumed = 0;
     if (warp >= PS::kConsumerWarps)
-        replay_producer<TS, L, IO, SH>(p, lay, units, smem, full, empty, warp - PS::kConsumerWarps);
+        replay_producer<TS, L, IO, SH>(p, lay, units, smem, full, empty, rx, warp - PS::kConsumerWarps);
     else
-        replay_consumer<TS, L, IO, SH>(p, lay, units, smem, full, empty);
+        consumed = replay_consumer<TS, L, IO, SH>(p, lay, units, smem, full, empty, rx);
+    __syncthreads();
+    if (threadIdx.x == 0) ring_drain(rx, full, lay.stages, consumed, p.wait_cycles, p.status);
+}
+
+// Dynamic shared memory the CTAs of one SM may take in all: the device's
+// shared memory per SM less a 6 KB margin (222 KB of 228 KB on this part),
+// and what one CTA may opt in to (cached per device).
+static cudaError_t replay_smem_budget(int *per_sm, int *per_cta) {
+    static std::atomic<int> cache_sm[64], cache_cta[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int sm = cache_sm[dev].load(std::memory_order_relaxed), cta = cache_cta[dev].load(std::memory_order_relaxed);
+    if (sm == 0 || cta == 0) {
+        if ((e = cudaDeviceGetAttribute(&sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&cta, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return e;
+        sm -= 6 * 1024;
+        cache_sm[dev].store(sm, std::memory_order_relaxed);
+        cache_cta[dev].store(cta, std::memory_order_relaxed);
+    }
+    *per_sm = sm;
+    *per_cta = cta;
+    return cudaSuccess;
 }
 
 // Number of SMs of the current device (cached per device).
@@ -895,8 +927,10 @@ static cudaError_t prepare_replay_kernel(int *reg_ctas) {
     if (dev < 0 || dev >= 64) dev = 0;
     int n = cache[dev].load(std::memory_order_relaxed);
     if (n == 0) {
+        int per_sm = 0, per_cta = 0;
+        if ((e = replay_smem_budget(&per_sm, &per_cta)) != cudaSuccess) return e;
         e = cudaFuncSetAttribute(ssu_replay_kernel<TS, L, IO, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 ReplayPipe<TS, L>::kSmemPerSm - 1024);
+                                 per_sm - 1024 < per_cta ? per_sm - 1024 : per_cta);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes a;
         e = cudaFuncGetAttributes(&a, ssu_replay_kernel<TS, L, IO, SH>);
@@ -916,9 +950,11 @@ static cudaError_t launch_replay_t(const KParams &p, int64_t batch, cudaStream_t
     int reg_ctas = 0;
     cudaError_t e = prepare_replay_kernel<TS, L, IO, SH>(&reg_ctas);
     if (e != cudaSuccess) return e;
+    int per_sm = 0, per_cta = 0;
+    if ((e = replay_smem_budget(&per_sm, &per_cta)) != cudaSuccess) return e;
     ReplayLayout lay;
-    if (!lay.choose(PS::kTileBytes, PS::kN, p.rlen, IO == kF32 ? 4 : 2, PS::kSmemPerSm, reg_ctas,
-                    PS::kProducerWarps))
+    if (!lay.choose(PS::kTileBytes, PS::kN, p.rlen, IO == kF32 ? 4 : 2, per_sm, reg_ctas, PS::kProducerWarps) ||
+        lay.bytes > per_cta)
         return cudaErrorInvalidConfiguration;
     const int64_t units = batch * p.H * p.ptiles;
     const int sms = replay_sm_count();

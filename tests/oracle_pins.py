@@ -518,6 +518,17 @@ def pin_seed_position_per_row(lib):
             raise AssertionError(f"per-row seed of the sequence starting at row {row}")
     if _touched(res, oracle.TOUCH_WRITTEN) != sorted(tab.tolist()):
         raise AssertionError("per-row: every row publishes to its own entry")
+    # num_accepted past a sequence's length would seed from the next
+    # sequence's entry (sequence 0: entry 2 belongs to sequence 2): refused
+    for acc in ([3, 1, 1, 1], [2, 1, 4, 1], [2, 1, 1, 2]):
+        try:
+            oracle.ssu(state, x, dt, torch.zeros(1), B, C, read=oracle.Table.of(tab, oracle.SLOTS_PER_ROW),
+                       cu_seqlens=cu, num_accepted=torch.tensor(acc), lib=lib)
+        except oracle.OracleError as e:
+            if e.code != oracle.INVALID:
+                raise
+        else:
+            raise AssertionError(f"per-row seed past the sequence accepted (num_accepted {acc})")
 
 
 def pin_per_head_dt(lib):

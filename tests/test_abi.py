@@ -274,3 +274,14 @@ def test_verify_empty_call_launches_nothing(libssu):
     rb = _replay_buffers(x=None, dt=None, B=None, count_in=None, count_out=None)
     assert libssu.ssu_replay_verify(ctypes.byref(a), 0, 4, None, ctypes.byref(rb), None) == ssu.OK
     assert libssu.ssu_replay_verify(ctypes.byref(a), -1, 4, None, ctypes.byref(rb), None) == ssu.ERR_INVALID
+
+
+def test_selftest_timeout_host_checks(libssu):
+    a = _args()
+    assert libssu.ssu_selftest_timeout(ctypes.byref(a), 2, None, None, 8, 10 ** 6, None) == ssu.ERR_INVALID
+    assert "withhold_unit" in libssu.ssu_last_error().decode()
+    assert libssu.ssu_selftest_timeout(ctypes.byref(a), 2, None, None, -1, 10 ** 6, None) == ssu.ERR_INVALID
+    assert libssu.ssu_selftest_timeout(ctypes.byref(a), 2, None, None, 1, 10, None) == ssu.ERR_INVALID
+    assert "wait_cycles" in libssu.ssu_last_error().decode()
+    assert libssu.ssu_selftest_timeout(ctypes.byref(a), 2, None, None, 1, 10 ** 10, None) == ssu.ERR_INVALID
+    assert libssu.ssu_selftest_timeout(ctypes.byref(a), 0, None, None, 0, 10 ** 6, None) == ssu.ERR_INVALID

@@ -31,6 +31,8 @@ MUTATIONS = [
      "if (!pr->disable_state_update && wslot[r] >= 0)"),
     ("disable_ignored", "if (!pr->disable_state_update && wslot[r]", "if (wslot[r]"),
     ("per_row_as_strided", "return row_start + step;", "return b + step;"),
+    ("per_row_seed_past_sequence", "rtab->mode == ORC_SLOTS_PER_ROW && t_seed >= len)",
+     "rtab->mode == ORC_SLOTS_PER_ROW && t_seed >= len + 8)"),
     ("publish_seed_entry", "if (resolve(wtab, b, t, start[b], &w) != 0)",
      "if (resolve(wtab, b, 0, start[b], &w) != 0)"),
     ("bf16_truncates", "double r = round_to_format(v, 7, -126, 127);", "double r = trunc(v * 128.0) / 128.0;"),
