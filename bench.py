@@ -88,7 +88,7 @@ KERNEL_SOURCES = {"onetoken": ["ssu_onetoken.cu", "ssu_device.cuh", "ssu_interna
                   "replay": ["ssu_replay.cuh", "ssu_replay_bf16.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "copy": ["ssu_copy.cu", "ssu_device.cuh", "ssu_internal.h"],
                   "verify": ["ssu_verify.cu", "ssu_verify.h", "ssu_device.cuh", "ssu_internal.h"],
-                  "ssd": ["ssu_ssd.cu", "ssu_ssd_params.h", "ssu_device.cuh", "ssu_internal.h"]}
+                  "ssd": ["ssu_ssd.cu", "ssu_ssd_tc.cu", "ssu_ssd_params.h", "ssu_device.cuh", "ssu_internal.h"]}
 
 
 # --------------------------------------------------------------------------
@@ -199,8 +199,7 @@ def kernel_hash(kind: str) -> str:
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_NAMES = {"onetoken": ["ssu_onetoken_kernel"], "packed": ["ssu_packed_kernel", "ssu_packed_long_kernel"], "replay": ["ssu_replay_kernel"],
                 "copy": ["ssu_copy_kernel"], "verify": ["ssu_verify_fold_kernel", "ssu_verify_kernel"],
-                "ssd": ["ssd_chunk_state_kernel", "ssd_state_pass_kernel", "ssd_chunk_cb_kernel",
-                        "ssd_chunk_scan_kernel"]}
+                "ssd": ["ssd_chunk_state_kernel", "ssd_state_pass_kernel", "ssd_scan_tc_kernel"]}
 
 
 def profiled_traffic(kind: str, workload: str):
@@ -799,24 +798,21 @@ def ssd_accounting(w) -> dict:
     outputs = T * H * P * io + nseq * sb
     nchunks = w.seq_idx.numel()
     ch = nchunks * H
-    # chunk states, then per 64-token block of the scan: C . S_in^T and the
-    # causal C . B^T and M . X products (full 16 x 16 tiles up to the diagonal)
+    # chunk states, then the scan's C . S_in^T and the causal C . B^T and
+    # W . X products, counted on 16 x 16 tiles up to the diagonal
     lens = (w.cu_chunk_seqlens[1:] - w.cu_chunk_seqlens[:-1]).tolist()
     causal = sum(sum((t // 16 + 1) * 16 for t in range(0, L, 16)) * 16 for L in lens)  # (t, s) pairs, 16-row tiles
     flops = H * (2 * T * P * N + 2 * T * N * P + 2 * causal * N + 2 * causal * P)
     # the chunk states cross the workspace four times (written, read and
-    # replaced by the entering states, read by the scan); the C . B^T tiles
-    # are written once per (chunk, group) and read by each head of the group
-    Q = w.chunk_size
-    tiles = (Q // 16) * (Q // 16 + 1) // 2
-    cb = nchunks * G * tiles * 256 * 4  # the causal part of C . B^T
+    # replaced by the entering states, read by the scan); C . B^T stays in
+    # the scan's tensor memory
     return {"inputs": inputs, "outputs": outputs, "total": inputs + outputs, "flops": flops,
-            "workspace": 4 * ch * P * N * 4 + cb * (1 + H // G), "tokens": T}
+            "workspace": 4 * ch * P * N * 4, "tokens": T}
 
 
 def run_ssd(args, rank, world, device):
     """The SSD prefill workload: one step = one ssu_ssd_prefill call over the
-    packed batch (four kernel launches)."""
+    packed batch (three kernel launches)."""
     from selective_state_update_gb300 import build as ssu_build
     import selective_state_update_gb300 as ssu
     ssu_build.build()
@@ -895,11 +891,11 @@ def run_ssd(args, rank, world, device):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("ssd", args.workload),
                      "algorithmic_bytes_per_launch": acct["total"],
-                     "kernel": "ssd prefill call (ssd_chunk_state + ssd_state_pass + ssd_chunk_cb + ssd_chunk_scan)",
+                     "kernel": "ssd prefill call (ssd_chunk_state + ssd_state_pass + ssd_scan_tc)",
                      "launch_ms": call_ms},
         "e2e": {"value": aggregate_rate(acct["tokens"], world, e2e_steps, e2e_s * 1e3), "unit": SSD_UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
     }
 

@@ -308,8 +308,12 @@ ssu_status ssu_replay_verify(const ssu_args *args, int64_t batch, int64_t ntok, 
  * in state_dtype.  Implemented: x, z, B, C and y bf16, contiguous; dt fp32 /
  * fp16 / bf16 [tokens, heads]; dim 64; dstate 64 or 128; chunk_size 64, 128
  * or 256 (others return SSU_ERR_UNSUPPORTED).  The contractions run on the
- * tensor cores with bf16 operands and fp32 accumulation; the chunk states
- * use a two-part bf16 split of the decay-weighted x.  `workspace` is
+ * tensor cores with fp32 accumulation: C . B^T with bf16 operands; the chunk
+ * states with a two-part bf16 split of the decay-weighted x; the entering
+ * state's term with a two-part bf16 split of the state; the causal weights
+ * (C . B^T) exp(cs_t - cs_s) dt'_s times x with fp16 operands (x is exact in
+ * fp16 where bf16 values lie in fp16's normal range, about 6.1e-5 to 65504
+ * in magnitude).  `workspace` is
  * caller-owned device memory of at least ssu_ssd_workspace_size() bytes,
  * 256-byte aligned; its contents need no initialisation.  Malformed chunks
  * (negative, decreasing, longer than chunk_size or past `tokens`) set
@@ -344,12 +348,14 @@ typedef struct ssu_ssd_args {
 } ssu_ssd_args;
 
 /* Workspace ssu_ssd_prefill needs for these sizes (bytes, into *bytes):
- * the chunk states (fp32), per-chunk prefix sums, dt' and decays, and the
- * causal 16 x 16 tiles of C . B^T of every (chunk, group) in fp32. */
+ * the chunk states (fp32; later the entering states as bf16 high and low
+ * parts in their place), per-chunk prefix sums, dt' and decays, and the
+ * largest |x| and dt' of every (chunk, head).  `groups`
+ * is checked (positive) but takes no part in the size. */
 ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t groups, int64_t dim, int64_t dstate,
                                   int64_t chunk_size, uint64_t *bytes);
 
-/* One packed SSD prefill call: four kernel launches on `stream` (at most
+/* One packed SSD prefill call: three kernel launches on `stream` (at most
  * 65535 chunks and 65535 heads per call). */
 ssu_status ssu_ssd_prefill(const ssu_ssd_args *args, void *stream);
 
@@ -359,7 +365,7 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *args, void *stream);
  * wrapper caches a workspace it allocates).  args->workspace must be NULL and
  * args->workspace_bytes 0.  The workspace the call needs
  * (ssu_ssd_workspace_size) must fit SSU_SSD_STATIC_SCRATCH_BYTES (64 MiB: for
- * heads 128, groups 8, dim 64, dstate 128 and chunk 256, up to 12 chunks);
+ * heads 128, dim 64, dstate 128 and chunk 256, up to 15 chunks);
  * a larger call returns SSU_ERR_INVALID before anything runs.  Nothing is
  * allocated: the scratch is a device array of the library, looked up once per
  * device on the first call made with that device current -- make that first

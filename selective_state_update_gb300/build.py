@@ -25,7 +25,7 @@ LIB = os.path.join(OUT_DIR, "libssu.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-Wall", "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["ssu_api.cpp", "ssu_onetoken.cu", "ssu_packed.cu", "ssu_packed_long.cu", "ssu_replay_f32.cu", "ssu_replay_f16.cu",
-           "ssu_replay_bf16.cu", "ssu_copy.cu", "ssu_shadow.cu", "ssu_ssd.cu", "ssu_verify.cu"]
+           "ssu_replay_bf16.cu", "ssu_copy.cu", "ssu_shadow.cu", "ssu_ssd.cu", "ssu_ssd_tc.cu", "ssu_verify.cu"]
 HEADERS = ["ssu_internal.h", "ssu_device.cuh", "ssu_replay.cuh", "ssu_ssd_params.h", "ssu_verify.h"]
 
 

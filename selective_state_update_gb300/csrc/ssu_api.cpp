@@ -369,23 +369,22 @@ ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes,
 }
 
 // Workspace carve-up of the SSD prefill: chunk states, prefix sums, dt',
-// chunk decays, C . B^T tiles, their diagonal; each part 256-byte aligned.
+// chunk decays, the largest |x| and dt' per (chunk, head); each part
+// 256-byte aligned.
 struct SsdWorkspace {
-    uint64_t state, acs, dtp, dec, cb, cbd, total;
+    uint64_t state, acs, dtp, dec, scl, total;
 };
-static SsdWorkspace ssd_workspace(uint64_t nchunks, uint64_t heads, uint64_t groups, uint64_t dim, uint64_t dstate,
+static SsdWorkspace ssd_workspace(uint64_t nchunks, uint64_t heads, uint64_t dim, uint64_t dstate,
                                   uint64_t chunk_size) {
     auto up = [](uint64_t v) { return (v + 255) / 256 * 256; };
-    const uint64_t ch = nchunks * heads, cg = nchunks * groups;
-    const uint64_t tiles = (chunk_size / 16) * (chunk_size / 16 + 1) / 2;
+    const uint64_t ch = nchunks * heads;
     SsdWorkspace w{};
     w.state = 0;
     w.acs = w.state + up(ch * dim * dstate * 4);
     w.dtp = w.acs + up(ch * chunk_size * 4);
     w.dec = w.dtp + up(ch * chunk_size * 4);
-    w.cb = w.dec + up(ch * 4);
-    w.cbd = w.cb + up(cg * tiles * 256 * 4);
-    w.total = w.cbd + up(cg * chunk_size * 4);
+    w.scl = w.dec + up(ch * 4);
+    w.total = w.scl + up(ch * 16);
     return w;
 }
 
@@ -394,7 +393,7 @@ ssu_status ssu_ssd_workspace_size(int64_t nchunks, int64_t heads, int64_t groups
     if (!bytes) return fail(SSU_ERR_INVALID, "bytes is NULL");
     if (nchunks < 0 || heads <= 0 || groups <= 0 || dim <= 0 || dstate <= 0 || chunk_size <= 0)
         return fail(SSU_ERR_INVALID, "sizes must be positive (nchunks >= 0)");
-    *bytes = ssd_workspace(nchunks, heads, groups, dim, dstate, chunk_size).total;
+    *bytes = ssd_workspace(nchunks, heads, dim, dstate, chunk_size).total;
     return ok();
 }
 
@@ -421,7 +420,7 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *a, void *stream) {
     const void *aligned[] = {a->x, a->B, a->C, a->y, a->states, a->workspace, a->z, a->initial_states};
     for (const void *q : aligned)
         if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return fail(SSU_ERR_INVALID, "tensors must be 16-byte aligned");
-    const SsdWorkspace wl = ssd_workspace(a->nchunks, a->heads, a->groups, a->dim, a->dstate, a->chunk_size);
+    const SsdWorkspace wl = ssd_workspace(a->nchunks, a->heads, a->dim, a->dstate, a->chunk_size);
     const uint64_t need = wl.total;
     if (a->workspace_bytes < need)
         return fail(SSU_ERR_INVALID, "workspace of %lld bytes is smaller than the %lld needed",
@@ -456,8 +455,7 @@ ssu_status ssu_ssd_prefill(const ssu_ssd_args *a, void *stream) {
         p.ws_acs = reinterpret_cast<float *>(w + wl.acs);
         p.ws_dtp = reinterpret_cast<float *>(w + wl.dtp);
         p.ws_dec = reinterpret_cast<float *>(w + wl.dec);
-        p.ws_cb = reinterpret_cast<float *>(w + wl.cb);
-        p.ws_cbd = reinterpret_cast<float *>(w + wl.cbd);
+        p.ws_scl = reinterpret_cast<float *>(w + wl.scl);
     }
     return launched(ssu::launch_ssd(p, static_cast<cudaStream_t>(stream)));
 }

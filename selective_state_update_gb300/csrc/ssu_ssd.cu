@@ -15,29 +15,21 @@
 // silu(z).  A chunk opens a sequence when seq_idx changes (the page: seq_idx
 // is the authority); its S_in is then the initial state (or zero).
 //
-// Four kernels over a caller-owned workspace; every contraction runs on the
-// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation), with
-// operands staged in shared memory in the inputs' own row layout by 16-byte
-// cp.async and read as fragments with ldmatrix:
-//   chunk_state  one CTA per (head, chunk): dt', the prefix and suffix sums
-//                of a, and Sc = (w x)^T B with w_t = exp(sum_{s>t} a) dt'_t;
-//                w x is split into a bf16 high and low part so that Sc keeps
-//                ~2^-17 relative precision (the returned states need it);
+// Three kernels over a caller-owned workspace:
+//   chunk_state  one CTA per (head, chunk), on the tensor cores (mma.sync
+//                m16n8k16, bf16 operands, fp32 accumulation; operands staged
+//                in shared memory in the inputs' own row layout by 16-byte
+//                cp.async and read as fragments with ldmatrix): dt', the
+//                prefix and suffix sums of a, and Sc = (w x)^T B with
+//                w_t = exp(sum_{s>t} a) dt'_t; w x is split into a bf16 high
+//                and low part so that Sc keeps ~2^-17 relative precision (the
+//                returned states need it);
 //   state_pass   one CTA per (run of a sequence's chunks, head): replaces
 //                each Sc in the workspace by the chunk's entering state (as
-//                bf16 high and low parts) and writes the returned states;
-//   chunk_cb     one CTA per (group, chunk): the causal 16 x 16 tiles of
-//                C . B^T in fp32, stored in mma fragment order so that the
-//                heads of the group read them back with coalesced loads, and
-//                the diagonal C_t . B_t on its own;
-//   chunk_scan   one CTA per (head, chunk): y from the entering state
-//                (C . S_in^T scaled by exp(cs_t)) and from the strictly causal
-//                weights (C . B^T) exp(cs_t - cs_s) dt'_s times x, the state
-//                and the weights as bf16 high + low parts (one-part bf16
-//                operands measured errors of up to 2.4 % of a token's row);
-//                the diagonal weight (C_t . B_t) dt'_t and D are applied in
-//                fp32, since the two can cancel for every dim row of a token
-//                (both multiply x_t).
+//                bf16 high and low parts, in the operand order of the scan's
+//                MMA) and writes the returned states;
+//   scan         one CTA per (group, chunk), on the 5th-generation tensor
+//                cores with C . B^T kept in tensor memory (ssu_ssd_tc.cu).
 #include <cstdint>
 #include <mutex>
 
@@ -60,15 +52,9 @@ __device__ __forceinline__ void mma_bf16(float *d, const uint32_t *a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Four 8 x 8 b16 matrices from shared memory; lanes 8i..8i+7 give the row
-// addresses of matrix i.  Lane l receives (row l/4, columns 2(l%4), 2(l%4)+1)
-// of each matrix, or with .trans (rows 2(l%4), 2(l%4)+1, column l/4).
-__device__ __forceinline__ void ldsm_x4(uint32_t *r, const void *smem_row) {
-    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem_row));
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
+// Four 8 x 8 b16 matrices from shared memory, transposed; lanes 8i..8i+7
+// give the row addresses of matrix i.  Lane l receives rows 2(l%4),
+// 2(l%4)+1 of column l/4 of each matrix.
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t *r, const void *smem_row) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(smem_row));
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -100,14 +86,6 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t *hi, uin
     *lo = pack_bf16(x0 - h0, x1 - h1);
 }
 
-// 2^x by the special-function unit (PTX ex2.approx.ftz: relative error
-// below 2^-22, results below 2^-126 flushed to zero); x <= 0 here.
-__device__ __forceinline__ float ex2_fast(float x) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
@@ -122,11 +100,6 @@ template <int N>
 __host__ __device__ constexpr int canon(int p, int n) {
     return (p >> 3) * (N * 8) + (n >> 3) * 64 + (p & 7) * 8 + (n & 7);
 }
-
-// The causal 16 x 16 tiles (row tile m, column tile j <= m) of a chunk of Q
-// tokens, numbered row tile by row tile.
-__host__ __device__ constexpr int cb_tiles(int Q) { return (Q / 16) * (Q / 16 + 1) / 2; }
-__device__ __forceinline__ int cb_tile(int m, int j) { return m * (m + 1) / 2 + j; }
 
 // Index of (chunk c, head h) in the per-(chunk, head) workspace arrays:
 // head-major, so that the chunks of one sequence and head are neighbours.
@@ -189,6 +162,7 @@ struct ChunkStateSmem {
     float rs[Q];                 // inclusive cumulative sums of a, reversed
     float w[Q];                  // dt', then exp(sum of the later a) dt'
     float tmp[8];
+    float mx[2][8];              // per warp: largest |x| and largest dt'
 };
 
 constexpr int kStateThreads = 256;
@@ -220,8 +194,10 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
     float *ws_acs = p.ws_acs + ws_unit(p, c, h) * Q;
     float *ws_dtp = p.ws_dtp + ws_unit(p, c, h) * Q;
     const float Ah = p.A[h];
+    float dmax = 0.f;  // largest dt' of this thread's token
     if (tid < Q) {
         const float d = tid < L ? ssd_step(p, t0 + tid, h) : 0.f;
+        dmax = d;
         ws_dtp[tid] = d;
         sm.w[tid] = d;
         sm.cs[tid] = tid < L ? Ah * d : 0.f;
@@ -283,6 +259,28 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
         const int n = n0 + 8 * j + 2 * q;
         *reinterpret_cast<float2 *>(out + canon<N>(p0 + gq, n)) = make_float2(acc[j][0], acc[j][1]);
         *reinterpret_cast<float2 *>(out + canon<N>(p0 + gq + 8, n)) = make_float2(acc[j][2], acc[j][3]);
+    }
+    // the largest |x| and dt' of the chunk and head, from which the scan
+    // picks the power-of-two scales of its fp16 operands (rows from L on are
+    // zero); bf16 magnitudes compare as unsigned integers
+    uint32_t xm = 0;
+    for (int i = tid; i < Q * (P / 8); i += kStateThreads) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&sm.xs[i / (P / 8)][(i % (P / 8)) * 8]);
+        xm = __vmaxu2(xm, __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                   __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
+    }
+    float xmax = fmaxf(__uint_as_float(xm << 16), __uint_as_float(xm & 0xffff0000u));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        xmax = fmaxf(xmax, __shfl_xor_sync(0xffffffffu, xmax, off));
+        dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, off));
+    }
+    if (lane == 0) sm.mx[0][warp] = xmax, sm.mx[1][warp] = dmax;
+    __syncthreads();
+    if (tid == 0) {
+        float a = 0.f, b = 0.f;
+        for (int i = 0; i < kStateThreads / 32; ++i) a = fmaxf(a, sm.mx[0][i]), b = fmaxf(b, sm.mx[1][i]);
+        *reinterpret_cast<float4 *>(p.ws_scl + ws_unit(p, c, h) * 4) = make_float4(a, b, 0.f, 0.f);
     }
 }
 
@@ -412,254 +410,6 @@ __global__ void __launch_bounds__(kPassThreads) ssd_state_pass_kernel(const SsdP
 }
 
 // ---------------------------------------------------------------------------
-// Stage 4: C . B^T per (group, chunk), causal 16 x 16 tiles in fragment order.
-// ---------------------------------------------------------------------------
-template <int Q, int N>
-struct ChunkCbSmem {
-    __nv_bfloat16 cm[Q][N + 8];  // C rows, cm[t][n]
-    __nv_bfloat16 bm[Q][N + 8];  // B rows, bm[s][n]
-};
-
-constexpr int kCbThreads = 256;
-
-template <int Q, int N>
-__global__ void __launch_bounds__(kCbThreads) ssd_chunk_cb_kernel(const SsdParams p) {
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<ChunkCbSmem<Q, N> *>(smem_raw);
-    const int g = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
-    const int64_t t0 = meta_at(p.cu_chunk, c, p.meta_i64), t1 = meta_at(p.cu_chunk, c + 1, p.meta_i64);
-    if (t0 < 0 || t1 < t0 || t1 - t0 > Q || t1 > p.tokens) return;  // flagged by chunk_state
-    const int L = static_cast<int>(t1 - t0);
-    const int64_t gs = static_cast<int64_t>(p.G) * N, g0 = static_cast<int64_t>(g) * N;
-    stage_rows<kCbThreads>(&sm.cm[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.C), t0, gs, g0, Q, L, N);
-    stage_rows<kCbThreads>(&sm.bm[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.B), t0, gs, g0, Q, L, N);
-    cp_async_wait_all();
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
-    const int mt_end = (L + 15) / 16;  // row tiles holding tokens
-    float *cb = p.ws_cb + (static_cast<int64_t>(c) * p.G + g) * cb_tiles(Q) * 256;
-    float *cbd = p.ws_cbd + (static_cast<int64_t>(c) * p.G + g) * Q;
-    for (int tile = warp; tile < mt_end * (mt_end + 1) / 2; tile += kCbThreads / 32) {
-        int m = 0;
-        while ((m + 1) * (m + 2) / 2 <= tile) ++m;
-        const int j = tile - m * (m + 1) / 2;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int k0 = 0; k0 < N; k0 += 16) {
-            uint32_t a[4], b[4];
-            // C: matrices (t 0-7 | 8-15) x (n 0-7 | 8-15) of cm
-            ldsm_x4(a, &sm.cm[16 * m + (lane & 7) + (mi & 1) * 8][k0 + (mi >> 1) * 8]);
-            // B[k = n][col = s] = bm[s][n]: matrices (n 0-7 | 8-15) x (s 0-7 | 8-15)
-            ldsm_x4(b, &sm.bm[16 * j + (lane & 7) + (mi >> 1) * 8][k0 + (mi & 1) * 8]);
-            mma_bf16(acc[0], a, b[0], b[1]);
-            mma_bf16(acc[1], a, b[2], b[3]);
-        }
-        float4 *o = reinterpret_cast<float4 *>(cb + static_cast<int64_t>(tile) * 256 + lane * 8);
-        o[0] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-        o[1] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-        if (j == m) {  // the diagonal: (row gq, col 2q + e) of columns 0-7, (row gq + 8, col 8 + 2q + e) of 8-15
-            if (gq == 2 * q) cbd[16 * m + gq] = acc[0][0], cbd[16 * m + gq + 8] = acc[1][2];
-            if (gq == 2 * q + 1) cbd[16 * m + gq] = acc[0][1], cbd[16 * m + gq + 8] = acc[1][3];
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Stage 5: the chunk scan, one CTA per (head, chunk); warp w takes the row
-// tiles w and Q/16 - 1 - w (16 tokens each) so that the causal work is
-// balanced.  Per row tile:
-//   Y1 = C . S_in^T, scaled by exp(cs_t)   (S_in as bf16 high + low parts,
-//                                           split once by the state pass)
-//   Y2 = sum over column tiles j of W_j . x_j, W[t][s] = (C . B^T)
-//        exp(cs_t - cs_s) dt'_s for s < t, as bf16 high + low parts; for a
-//        tile that lies wholly before the rows the decay factors through the
-//        tile's last token r, exp(cs_t - cs_r) exp(cs_r - cs_s), both at most
-//        1 (cs only decreases), the second with dt'_s kept per column (E)
-//   y = Y1 + Y2 + ((C_t . B_t) dt'_t + D) x_t   (the diagonal in fp32: it can
-//        cancel D for every dim row of a token), gated by silu(z).
-// ---------------------------------------------------------------------------
-template <int Q, int P, int N>
-struct ChunkScanSmem {
-    __nv_bfloat16 xs[Q][P + 8];  // x rows, xs[s][p]
-    __nv_bfloat16 zy[Q][P + 8];  // z rows, replaced row by row by y before its store
-    __nv_bfloat16 ss[P][N + 8];  // entering state, bf16 high part, ss[p][n]
-    __nv_bfloat16 sl[P][N + 8];  // and the bf16 low part of what is left
-    float cs[Q];                 // inclusive cumulative sums of a, times log2(e)
-    float dtp[Q];                // dt'
-    float cbd[Q];                // C_t . B_t
-    float E[Q];                  // exp(cs_r - cs_s) dt'_s, r the last token of s's 16-token tile
-};
-
-template <int Q, int P, int N>
-__global__ void __launch_bounds__(Q, 2) ssd_chunk_scan_kernel(const SsdParams p) {
-    static_assert(P == 64 && Q % 64 == 0, "tiling");
-    constexpr int kThreads = Q;  // Q / 32 warps
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<ChunkScanSmem<Q, P, N> *>(smem_raw);
-    const int h = blockIdx.x, c = blockIdx.y, tid = threadIdx.x;
-    const int g = h / p.hpg;
-    const int64_t t0 = meta_at(p.cu_chunk, c, p.meta_i64), t1 = meta_at(p.cu_chunk, c + 1, p.meta_i64);
-    if (t0 < 0 || t1 < t0 || t1 - t0 > Q || t1 > p.tokens) return;  // flagged by chunk_state
-    const int L = static_cast<int>(t1 - t0);
-    if (L == 0) return;
-    const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, q = lane & 3, mi = lane >> 3;
-    const __nv_bfloat16 *Cg = static_cast<const __nv_bfloat16 *>(p.C);
-    // C fragments (A of C . S_in^T) of row tile m, straight from global memory
-    uint32_t cf[N / 16][4];
-    auto load_cf = [&](int m) {
-        const int ta = 16 * m + gq, tc = ta + 8;
-        const unsigned int *ra = reinterpret_cast<const unsigned int *>(Cg + ((t0 + ta) * p.G + g) * N);
-        const unsigned int *rc = reinterpret_cast<const unsigned int *>(Cg + ((t0 + tc) * p.G + g) * N);
-#pragma unroll
-        for (int ks = 0; ks < N / 16; ++ks) {
-            const int n2 = 8 * ks + q;  // (16 ks + 2 q) / 2
-            cf[ks][0] = ta < L ? __ldg(ra + n2) : 0u;
-            cf[ks][1] = tc < L ? __ldg(rc + n2) : 0u;
-            cf[ks][2] = ta < L ? __ldg(ra + n2 + 4) : 0u;
-            cf[ks][3] = tc < L ? __ldg(rc + n2 + 4) : 0u;
-        }
-    };
-    load_cf(warp);  // the first row tile's, in flight during the staging below
-    stage_rows<kThreads>(&sm.xs[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.x), t0,
-                         static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
-    if (p.z)
-        stage_rows<kThreads>(&sm.zy[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.z), t0,
-                             static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
-    const int64_t ch = ws_unit(p, c, h);
-    {  // the entering state's parts, from the canonical order into padded rows
-        const unsigned char *slot = reinterpret_cast<const unsigned char *>(p.ws_state + ch * P * N);
-        for (int i = tid; i < 2 * P * N / 8; i += kThreads) {
-            const int part = i / (P * N / 8), b = (i % (P * N / 8)) * 16;
-            const int pp = (b / (N * 16)) * 8 + (b % 128) / 16, n8 = ((b / 128) % (N / 8)) * 8;
-            cp_async16(part ? &sm.sl[pp][n8] : &sm.ss[pp][n8], slot + part * (P * N * 2) + b, true);
-        }
-    }
-    constexpr float kLog2e = 1.4426950408889634f;
-    for (int t = tid; t < Q; t += kThreads) {
-        sm.cs[t] = p.ws_acs[ch * Q + t] * kLog2e;
-        sm.dtp[t] = p.ws_dtp[ch * Q + t];
-        sm.cbd[t] = p.ws_cbd[(static_cast<int64_t>(c) * p.G + g) * Q + t];
-    }
-    __syncthreads();
-    for (int t = tid; t < Q; t += kThreads) sm.E[t] = t < L ? ex2_fast(sm.cs[t | 15] - sm.cs[t]) * sm.dtp[t] : 0.f;
-    cp_async_wait_all();
-    __syncthreads();
-
-    const float *cbg = p.ws_cb + (static_cast<int64_t>(c) * p.G + g) * cb_tiles(Q) * 256;
-    const float Dh = p.D ? p.D[h] : 0.f;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-        const int m = half ? Q / 16 - 1 - warp : warp;
-        if (16 * m >= L) continue;
-        const int ta = 16 * m + gq, tc = ta + 8;  // the two rows this lane holds
-        float acc[P / 8][4];
-#pragma unroll
-        for (int j = 0; j < P / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-        // y from the entering state, C . S_in^T (the high parts for every p-tile,
-        // then the low parts: no accumulator is used twice in a row)
-        if (half) load_cf(m);
-#pragma unroll
-        for (int ks = 0; ks < N / 16; ++ks) {
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                for (int j = 0; j < P / 8; j += 2) {
-                    // S_in^T: B[k = n][col = p] = ss[p][n]: matrices (n 0-7 | 8-15) x (p-tile j | j+1)
-                    uint32_t b[4];
-                    ldsm_x4(b, part ? &sm.sl[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]
-                                    : &sm.ss[8 * j + (lane & 7) + (mi >> 1) * 8][16 * ks + (mi & 1) * 8]);
-                    mma_bf16(acc[j], cf[ks], b[0], b[1]);
-                    mma_bf16(acc[j + 1], cf[ks], b[2], b[3]);
-                }
-            }
-        }
-        const float csa = sm.cs[ta], csc = sm.cs[tc];
-        const float ea = exp2f(csa), ec = exp2f(csc);
-#pragma unroll
-        for (int j = 0; j < P / 8; ++j) acc[j][0] *= ea, acc[j][1] *= ea, acc[j][2] *= ec, acc[j][3] *= ec;
-        // strictly causal part, 16 tokens s at a time; the next tile's C . B^T
-        // is loaded while this one is used
-        const float4 *row_tiles = reinterpret_cast<const float4 *>(cbg + static_cast<int64_t>(cb_tile(m, 0)) * 256) +
-                                  lane * 2;
-        float4 v0 = __ldg(row_tiles), v1 = __ldg(row_tiles + 1), w0 = v0, w1 = v1;
-        if (m > 0) w0 = __ldg(row_tiles + 64), w1 = __ldg(row_tiles + 65);
-        for (int js = 0; js <= m; ++js) {
-            const float cb[2][4] = {{v0.x, v0.y, v0.z, v0.w}, {v1.x, v1.y, v1.z, v1.w}};
-            v0 = w0, v1 = w1;  // two tiles ahead in flight
-            if (js + 2 <= m) w0 = __ldg(row_tiles + (js + 2) * 64), w1 = __ldg(row_tiles + (js + 2) * 64 + 1);
-            uint32_t mf[4], ml[4];
-            if (js < m) {  // the tile lies wholly before the rows: decays through its last token
-                const float r = sm.cs[16 * js + 15];
-                const float Ra = ex2_fast(csa - r), Rc = ex2_fast(csc - r);
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const float2 e = *reinterpret_cast<const float2 *>(&sm.E[16 * js + 8 * jj + 2 * q]);
-                    split_bf16(cb[jj][0] * Ra * e.x, cb[jj][1] * Ra * e.y, &mf[2 * jj], &ml[2 * jj]);
-                    split_bf16(cb[jj][2] * Rc * e.x, cb[jj][3] * Rc * e.y, &mf[2 * jj + 1], &ml[2 * jj + 1]);
-                }
-            } else {  // the diagonal tile: W[t][s] for s < t, one exponential each
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int s0 = 16 * js + 8 * jj + 2 * q, s1 = s0 + 1;
-                    const float d0 = sm.dtp[s0], d1 = sm.dtp[s1], e0 = sm.cs[s0], e1 = sm.cs[s1];
-                    const float m00 = s0 < ta ? cb[jj][0] * ex2_fast(csa - e0) * d0 : 0.f;
-                    const float m01 = s1 < ta ? cb[jj][1] * ex2_fast(csa - e1) * d1 : 0.f;
-                    const float m10 = s0 < tc ? cb[jj][2] * ex2_fast(csc - e0) * d0 : 0.f;
-                    const float m11 = s1 < tc ? cb[jj][3] * ex2_fast(csc - e1) * d1 : 0.f;
-                    split_bf16(m00, m01, &mf[2 * jj], &ml[2 * jj]);
-                    split_bf16(m10, m11, &mf[2 * jj + 1], &ml[2 * jj + 1]);
-                }
-            }
-            // (A operand order: {rows g, k 2q}, {rows g+8, k 2q}, {rows g, k 2q+8}, {rows g+8, k 2q+8})
-            uint32_t bx[P / 16][4];
-#pragma unroll
-            for (int j = 0; j < P / 8; j += 2) {
-                // X: B[k = s][col = p] = xs[s][p]: matrices (s 0-7 | 8-15) x (p-tile j | j+1), transposed
-                ldsm_x4_trans(bx[j / 2], &sm.xs[16 * js + (lane & 7) + (mi & 1) * 8][8 * j + (mi >> 1) * 8]);
-                mma_bf16(acc[j], mf, bx[j / 2][0], bx[j / 2][1]);
-                mma_bf16(acc[j + 1], mf, bx[j / 2][2], bx[j / 2][3]);
-            }
-#pragma unroll
-            for (int j = 0; j < P / 8; j += 2) {
-                mma_bf16(acc[j], ml, bx[j / 2][0], bx[j / 2][1]);
-                mma_bf16(acc[j + 1], ml, bx[j / 2][2], bx[j / 2][3]);
-            }
-        }
-        // epilogue: + ((C_t . B_t) dt'_t + D) x_t in fp32, gate, store
-        const float wa = fmaf(sm.cbd[ta], sm.dtp[ta], Dh), wc = fmaf(sm.cbd[tc], sm.dtp[tc], Dh);
-#pragma unroll
-        for (int j = 0; j < P / 8; ++j) {
-            const int pp = 8 * j + 2 * q;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int t = r ? tc : ta;
-                if (t >= L) continue;
-                const uint32_t xb = *reinterpret_cast<const uint32_t *>(&sm.xs[t][pp]);
-                const float wd = r ? wc : wa;
-                float v0 = fmaf(wd, bf16_lo(xb), acc[j][2 * r]);
-                float v1 = fmaf(wd, bf16_hi(xb), acc[j][2 * r + 1]);
-                uint32_t *zy = reinterpret_cast<uint32_t *>(&sm.zy[t][pp]);
-                if (p.z) {
-                    const uint32_t zb = *zy;
-                    const float z0 = bf16_lo(zb), z1 = bf16_hi(zb);
-                    v0 *= __fdividef(z0, 1.f + __expf(-z0));
-                    v1 *= __fdividef(z1, 1.f + __expf(-z1));
-                }
-                *zy = pack_bf16(v0, v1);  // this lane's z element becomes its y element
-            }
-        }
-        // the warp's 16 rows of y, 16 bytes per lane and store
-        __syncwarp();
-        for (int i = lane; i < 16 * (P / 8); i += 32) {
-            const int t = 16 * m + i / (P / 8), k = (i % (P / 8)) * 8;
-            if (t < L)
-                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y) + ((t0 + t) * p.H + h) * static_cast<int64_t>(P) + k) =
-                    *reinterpret_cast<const uint4 *>(&sm.zy[t][k]);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Launch.
 // ---------------------------------------------------------------------------
 template <typename K>
@@ -669,12 +419,9 @@ static cudaError_t allow_smem(K kernel, size_t bytes) {
 
 template <int Q, int P, int N>
 static cudaError_t launch_qpn(const SsdParams &p, cudaStream_t stream) {
-    const size_t s1 = sizeof(ChunkStateSmem<Q, P, N>), s4 = sizeof(ChunkCbSmem<Q, N>),
-                 s5 = sizeof(ChunkScanSmem<Q, P, N>);
+    const size_t s1 = sizeof(ChunkStateSmem<Q, P, N>);
     cudaError_t e;
     if ((e = allow_smem(ssd_chunk_state_kernel<Q, P, N>, s1)) != cudaSuccess) return e;
-    if ((e = allow_smem(ssd_chunk_cb_kernel<Q, N>, s4)) != cudaSuccess) return e;
-    if ((e = allow_smem(ssd_chunk_scan_kernel<Q, P, N>, s5)) != cudaSuccess) return e;
     const dim3 g1(static_cast<unsigned>(p.H), static_cast<unsigned>(p.nchunks));
     ssd_chunk_state_kernel<Q, P, N><<<g1, kStateThreads, s1, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -686,11 +433,7 @@ static cudaError_t launch_qpn(const SsdParams &p, cudaStream_t stream) {
     default: return cudaErrorInvalidValue;
     }
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const dim3 g4(static_cast<unsigned>(p.G), static_cast<unsigned>(p.nchunks));
-    ssd_chunk_cb_kernel<Q, N><<<g4, kCbThreads, s4, stream>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ssd_chunk_scan_kernel<Q, P, N><<<g1, Q, s5, stream>>>(p);
-    return cudaGetLastError();
+    return launch_ssd_scan_tc(p, stream);
 }
 
 cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream) {

@@ -23,11 +23,12 @@ struct SsdParams {
     float *ws_state;                 // [H, nchunks, P*N]: chunk states (fp32), then entering states (bf16 hi | lo)
     float *ws_acs, *ws_dtp;          // [H, nchunks, Q]
     float *ws_dec;                   // [H, nchunks]
-    float *ws_cb;                    // [nchunks, G, causal 16 x 16 tiles of Q, 256] C . B^T (fragment order)
-    float *ws_cbd;                   // [nchunks, G, Q] C_t . B_t
+    float *ws_scl;                   // [H, nchunks, 4]: largest |x| and dt' of the chunk, 2 unused
     int32_t *status;
 };
 cudaError_t launch_ssd(const SsdParams &p, cudaStream_t stream);
+// The chunk scan on the 5th-generation tensor cores (ssu_ssd_tc.cu).
+cudaError_t launch_ssd_scan_tc(const SsdParams &p, cudaStream_t stream);
 
 // The library-owned workspace of ssu_ssd_prefill_static on the current
 // device: kSsdStaticScratchBytes at *ptr (looked up once per device).

@@ -207,9 +207,9 @@ def test_ssd_workspace_size_and_empty_call(libssu):
     n = ctypes.c_uint64(0)
     assert libssu.ssu_ssd_workspace_size(3, 4, 2, 64, 128, 64, ctypes.byref(n)) == ssu.OK
     up = lambda v: (v + 255) // 256 * 256
-    tiles = 4 * 5 // 2  # causal 16 x 16 tiles of a 64-token chunk
-    assert n.value == (up(12 * 64 * 128 * 4) + 2 * up(12 * 64 * 4) + up(12 * 4) + up(6 * tiles * 256 * 4)
-                       + up(6 * 64 * 4))
+    # 3 chunks x 4 heads: the chunk states (fp32), prefix sums and dt' per token, one decay,
+    # the largest |x| and dt' (16 bytes)
+    assert n.value == up(12 * 64 * 128 * 4) + 2 * up(12 * 64 * 4) + up(12 * 4) + up(12 * 16)
     assert libssu.ssu_ssd_workspace_size(3, 0, 2, 64, 128, 64, ctypes.byref(n)) == ssu.ERR_INVALID
     assert libssu.ssu_ssd_workspace_size(3, 4, 0, 64, 128, 64, ctypes.byref(n)) == ssu.ERR_INVALID
     # no chunks: nothing to do, nothing launched, no pointer looked at

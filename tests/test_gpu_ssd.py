@@ -2,15 +2,15 @@
 prefill; ssd_combined_fwd_varlen) on the GPU, through libssu's C ABI, against
 the oracle's token recurrence.
 
-Tolerances.  y: the chunk scan multiplies bf16-rounded operands (the
-entering state and the decayed C . B^T products; C, B and x are bf16
-already), each rounded to 2^-9 relative, and y itself is stored in bf16.
-The rounding errors of one output element add up over the terms of its sum,
-which are shared by the 64 dim rows of the same token (the same C . B^T
-weights and entering-state rows), so the error is a small multiple of 2^-9
-times the size of that token's terms; y is held to |d| <= 1e-2 |ref| +
-1e-2 max_p |ref[t, h, :]| + 1e-3 (max over the token's dim rows, which
-cancellation in one element does not make small).
+Tolerances.  y: the chunk scan multiplies the decayed C . B^T weights as
+fp16 (rounded to 2^-12 relative; x, staged as fp16 beside them, is exact),
+the entering state as a bf16 high and low part (2^-17), and y itself is
+stored in bf16 (2^-9).  The rounding errors of one output element add up
+over the terms of its sum, which are shared by the 64 dim rows of the same
+token (the same weights and entering-state rows), so the error is a small
+multiple of 2^-9 times the size of that token's terms; y is held to
+|d| <= 1e-2 |ref| + 1e-2 max_p |ref[t, h, :]| + 1e-3 (max over the token's
+dim rows, which cancellation in one element does not make small).
 States: the chunk states come from a two-part bf16 split of the
 decay-weighted x (residual 2^-17 relative per term), fp32 accumulation of up
 to chunk_size terms and decays exp() of fp32 sums of up to chunk_size terms;
@@ -195,3 +195,24 @@ def test_ssd_combined_fwd_varlen_signature(libssu):
     with pytest.raises(NotImplementedError):
         ssu.ssd_combined_fwd_varlen(g.x, g.dt, g.A, g.B, g.C, 128, g.cu_seqlens, g.cu_chunk_seqlens,
                                     g.last_chunk_indices, g.seq_idx, checkpoint_states=g.initial_states)
+
+
+@pytest.mark.parametrize("scale_x,scale_bc,dt_shift", [(1e5, 1.0, 0.0), (1e-7, 1.0, 0.0), (1.0, 40.0, 3.0),
+                                                      (3e4, 20.0, 0.0)])
+def test_ssd_operands_outside_fp16_range(libssu, scale_x, scale_bc, dt_shift):
+    """x beyond fp16's largest value (65504) or deep in its subnormal range,
+    and weights (C . B^T) dt' beyond 65504: the scan stages its fp16
+    operands with power-of-two scales picked per chunk and head, so y and the
+    states match the oracle relative to their own size."""
+    w = workloads.ssd_problem(290, [200, 77], heads=4, dim=64, dstate=128, groups=2, chunk_size=128)
+    w.x = (w.x.float() * scale_x).to(w.x.dtype)
+    w.B = (w.B.float() * scale_bc).to(w.B.dtype)
+    w.C = (w.C.float() * scale_bc).to(w.C.dtype)
+    w.dt = w.dt + dt_shift
+    ref = run_oracle_ssd(w)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    y, states = run_gpu_ssd(w, status=status)
+    assert int(status.item()) == 0
+    k = 1.0 / float(ref.y_exact.abs().max())
+    assert_ssd_y_close(y.double().cpu() * k, ref.y_exact * k, what=f"y / {1 / k:.3g}")
+    assert_ssd_states_close(states, ref.states[w.last_chunk_indices.long()])
