@@ -8,8 +8,10 @@
 //     y_t = exp(cs_t) C_t . S_in + sum_{s<t} (C_t . B_s) exp(cs_t - cs_s) dt'_s x_s
 //           + ((C_t . B_t) dt'_t + D) x_t,   gated by silu(z_t).
 //
-// One CTA per (group, chunk) walks the group's heads.  C . B^T is the same
-// for every head of the group, so it is computed once, by tcgen05.mma into
+// A persistent grid (one CTA per SM) splits the (chunk, group, head) units
+// into equal contiguous ranges; a CTA walks its range one (chunk, group)
+// segment at a time.  C . B^T is the same for every head of the group, so
+// it is computed once per segment, by tcgen05.mma into
 // tensor memory (the row tiles of 128 tokens side by side, causal: tile m
 // holds columns s < 128 (m + 1)).  Per head and row tile:
 //   Y1 = C . S_in^T         tcgen05.mma, S_in as bf16 high and low parts
@@ -186,7 +188,8 @@ struct TcLayout {
     static constexpr int kAux0 = kW + kWBytes;
     static constexpr int kAux1 = kAux0 + kAuxBytes;
     static constexpr int kCbd = kAux1 + kAuxBytes;  // the diagonal C_t . B_t of the rows, by tile parity
-    static constexpr int kBars = kCbd + 2 * 128 * 4; // 16 mbarriers
+    static constexpr int kWmax = kCbd + 2 * 128 * 4; // per segment parity and warp: the largest |C . B^T|
+    static constexpr int kBars = kWmax + 2 * 8 * 4;  // 16 mbarriers
     static constexpr int kTaddr = kBars + 16 * 8;
     static constexpr int kBytes = kTaddr + 16;
     // tensor-memory columns: C . B^T of tile 0 at 0, of tile 1 at 128; Y1, Y2
@@ -238,8 +241,11 @@ __device__ __forceinline__ void load_head(const SsdParams &p, unsigned char *sme
     }
     // x rows as fp16 (the weights' type) times 2^kx, which puts the head's
     // largest |x| in [2^13, 2^14): exact for every value down to 2^-11 of
-    // that largest one, eight values per 16-byte piece; both loader warps
-    // (`ld` = 0..63) take every 64th piece, 16 loads in flight per lane
+    // that largest one.  One 16-byte piece = 8 dim rows j of token s.  Loader
+    // warp wl takes the token octets wl, wl + 2, ...; in one store phase
+    // (8 lanes k) lane k writes piece j = k of token 8 o + (k + q + 4 u) % 8,
+    // so the 8 pieces land in 8 different bank groups (pieces of one token
+    // are 16 Q bytes apart, a multiple of 128); 16 loads in flight per lane.
     const float4 scl = __ldg(reinterpret_cast<const float4 *>(p.ws_scl + ch * 4));
     const int kx = fp16_scale_exp(scl.x);
     const float sx = pow2i(kx);
@@ -247,33 +253,69 @@ __device__ __forceinline__ void load_head(const SsdParams &p, unsigned char *sme
         aux[4 * Q] = pow2i(-kx);
         aux[4 * Q + 1] = scl.y;
     }
-    const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(p.x);
-    constexpr int kPieces = Q * (kTcP / 8);
-    for (int base = ld; base < kPieces; base += 64 * 16) {
+    const __nv_bfloat16 *xg = static_cast<const __nv_bfloat16 *>(p.x) + static_cast<int64_t>(h) * kTcP;
+    constexpr int kOct = Q / 8;
+    const int wl = ld >> 5, q = (ld >> 3) & 3, k = ld & 7;
+    for (int o0 = wl; o0 < kOct; o0 += 16) {
         uint4 v[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = base + 64 * u, s = i >> 3, j = i & 7;
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (i < kPieces && s < L)
-                v[u] = __ldg(reinterpret_cast<const uint4 *>(xg + ((t0 + s) * p.H + h) * kTcP + 8 * j));
+        for (int u2 = 0; u2 < 16; ++u2) {
+            const int o = o0 + 2 * (u2 >> 1), s = 8 * o + ((k + q + 4 * (u2 & 1)) & 7);
+            v[u2] = make_uint4(0u, 0u, 0u, 0u);
+            if (o < kOct && s < L)
+                v[u2] = __ldg(reinterpret_cast<const uint4 *>(xg + (t0 + s) * p.H * kTcP + 8 * k));
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = base + 64 * u, s = i >> 3, j = i & 7;
-            if (i >= kPieces) continue;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t o[4];
+        for (int u2 = 0; u2 < 16; ++u2) {
+            const int o = o0 + 2 * (u2 >> 1), s = 8 * o + ((k + q + 4 * (u2 & 1)) & 7);
+            if (o >= kOct) continue;
+            const uint32_t w[4] = {v[u2].x, v[u2].y, v[u2].z, v[u2].w};
+            uint32_t out[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const __half2 hv =
                     __floats2half2_rn(__uint_as_float(w[e] << 16) * sx, __uint_as_float(w[e] & 0xffff0000u) * sx);
-                o[e] = *reinterpret_cast<const uint32_t *>(&hv);
+                out[e] = *reinterpret_cast<const uint32_t *>(&hv);
             }
-            *reinterpret_cast<uint4 *>(xs + j * (16 * Q) + 16 * s) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(xs + k * (16 * Q) + 16 * s) = make_uint4(out[0], out[1], out[2], out[3]);
         }
     }
 }
+
+// The CTA's share of the units u = (chunk c, group g, head i of the group),
+// numbered u = (c G + g) hpg + i: a contiguous range, equal in count for
+// every CTA.  A segment is the part of the range within one (chunk, group):
+// it shares C . B^T.  Every role walks the same segments in the same order.
+struct TcSegment {
+    int64_t c, t0;
+    int g, ia, nh, L;
+};
+struct TcWalk {
+    int64_t u, ue;
+    __device__ TcWalk(const SsdParams &p) {
+        const int64_t units = p.nchunks * p.G * p.hpg;
+        u = units * blockIdx.x / gridDim.x;
+        ue = units * (blockIdx.x + 1) / gridDim.x;
+    }
+    // The next segment holding work (chunks that are malformed -- flagged
+    // by chunk_state -- or empty are passed over); false at the end.
+    __device__ bool next(const SsdParams &p, int Q, TcSegment &sg) {
+        while (u < ue) {
+            const int64_t cg = u / p.hpg;
+            sg.ia = static_cast<int>(u - cg * p.hpg);
+            sg.nh = static_cast<int>(min(static_cast<int64_t>(p.hpg - sg.ia), ue - u));
+            u += sg.nh;
+            sg.c = cg / p.G;
+            sg.g = static_cast<int>(cg - sg.c * p.G);
+            const int64_t t0 = load_index(p.cu_chunk, sg.c, p.meta_i64), t1 = load_index(p.cu_chunk, sg.c + 1, p.meta_i64);
+            if (t0 < 0 || t1 <= t0 || t1 - t0 > Q || t1 > p.tokens) continue;
+            sg.t0 = t0;
+            sg.L = static_cast<int>(t1 - t0);
+            return true;
+        }
+        return false;
+    }
+};
 
 template <int Q, int N>
 __global__ void __launch_bounds__(kTcThreads, 1) ssd_scan_tc_kernel(const SsdParams p) {
@@ -281,13 +323,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) ssd_scan_tc_kernel(const SsdPar
     extern __shared__ __align__(1024) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TL::kBars);
     uint32_t *taddr_slot = reinterpret_cast<uint32_t *>(smem + TL::kTaddr);
-    const int g = blockIdx.x, c = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t t0 = load_index(p.cu_chunk, c, p.meta_i64), t1 = load_index(p.cu_chunk, c + 1, p.meta_i64);
-    if (t0 < 0 || t1 < t0 || t1 - t0 > Q || t1 > p.tokens) return;  // flagged by chunk_state (uniform)
-    const int L = static_cast<int>(t1 - t0);
-    if (L == 0) return;
-    const int ntiles = L > 128 ? 2 : 1;
-    const int hpg = p.hpg, h0 = g * hpg;
+    float *wmax = reinterpret_cast<float *>(smem + TL::kWmax);  // [2][8]: per segment parity, per warp
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long lim = kWaitCycles;
     constexpr float kLog2e = 1.4426950408889634f;
 
@@ -312,102 +349,122 @@ __global__ void __launch_bounds__(kTcThreads, 1) ssd_scan_tc_kernel(const SsdPar
     tc_fence_after();
     const uint32_t tmem = *taddr_slot;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(taddr_slot + 1);
-    unsigned int *cbmax = taddr_slot + 2;  // largest |C_t . B_s| of the chunk (float bits)
-    if (tid == 0) *abort_flag = 0, *cbmax = 0u;
+    if (tid == 0) *abort_flag = 0;
     __syncthreads();
+
+    // Per head buffer b: its uses so far (the k-th use completes phase k of
+    // Full[b] and XFree[b]); the head of a segment's j-th unit uses buffer
+    // j % 2, so a segment's first head (loaded with C and B) uses buffer 0.
+    int uses0 = 0, uses1 = 0;
+    int seg = 0;  // segments begun (phase of CB)
+    TcWalk walk(p);
+    TcSegment sg;
 
     if (warp >= 9) {
         // ---------------- loads (two warps) ----------------
         const int ld = tid - 9 * 32;  // 0..63
         const __nv_bfloat16 *Cg = static_cast<const __nv_bfloat16 *>(p.C);
         const __nv_bfloat16 *Bg = static_cast<const __nv_bfloat16 *>(p.B);
-        for (int i = ld; i < Q * (N / 8); i += 64) {
-            const int t = i / (N / 8), k = i % (N / 8);
-            const bool ok = t < L;
-            const int64_t src = ((t0 + t) * p.G + g) * N + 8 * k;
-            const int dst = (t >> 3) * (16 * N) + k * 128 + (t & 7) * 16;
-            cp16(smem + TL::kC + dst, ok ? Cg + src : Cg, ok);
-            cp16(smem + TL::kB + dst, ok ? Bg + src : Bg, ok);
-        }
-        cp_wait_all();
-        fence_proxy_async_smem();
-        load_head<Q, N>(p, smem, 0, h0, c, t0, L, &bars[kBarFull0], ld);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[kBarFull0]);
-        int last = 0;  // the last head loaded
-        for (int i = 1; i < hpg; ++i) {
-            const int buf = i & 1;
-            bool ok;
-            if (i == 1)
-                ok = !TL::kAlias || mbar_wait_bounded(&bars[kBarCB], 0, lim);
-            else
-                ok = mbar_wait_bounded(&bars[buf ? kBarXFree1 : kBarXFree0], ((i - 2) >> 1) & 1, lim);
-            if (!ok || *abort_flag) {
-                if (ld == 0) {
-                    flag(p.status, kDevTimeout);
-                    *abort_flag = 1;
-                }
-                break;
+        bool ok = true;
+        while (ok && walk.next(p, Q, sg)) {
+            // both head buffers and C, B free: the previous segment is done
+            // (its last MMAs have read C and B, its weights are formed)
+            if (uses0 > 0) ok = mbar_wait_bounded(&bars[kBarXFree0], (uses0 - 1) & 1, lim);
+            if (ok && uses1 > 0) ok = mbar_wait_bounded(&bars[kBarXFree1], (uses1 - 1) & 1, lim);
+            if (ok && *abort_flag) ok = false;
+            if (!ok) break;
+            for (int i = ld; i < Q * (N / 8); i += 64) {
+                const int t = i / (N / 8), k = i % (N / 8);
+                const bool in = t < sg.L;
+                const int64_t src = ((sg.t0 + t) * p.G + sg.g) * N + 8 * k;
+                const int dst = (t >> 3) * (16 * N) + k * 128 + (t & 7) * 16;
+                cp16(smem + TL::kC + dst, in ? Cg + src : Cg, in);
+                cp16(smem + TL::kB + dst, in ? Bg + src : Bg, in);
             }
-            load_head<Q, N>(p, smem, buf, h0 + i, c, t0, L, &bars[buf ? kBarFull1 : kBarFull0], ld);
+            cp_wait_all();
             fence_proxy_async_smem();
-            mbar_arrive(&bars[buf ? kBarFull1 : kBarFull0]);
-            last = i;
+            for (int j = 0; j < sg.nh; ++j) {
+                const int buf = j & 1;
+                if (j == 1 && TL::kAlias)
+                    ok = mbar_wait_bounded(&bars[kBarCB], seg & 1, lim);  // B's place holds buffer 1
+                else if (j >= 2)
+                    ok = mbar_wait_bounded(&bars[buf ? kBarXFree1 : kBarXFree0], ((buf ? uses1 : uses0) - 1) & 1, lim);
+                if (ok && *abort_flag) ok = false;
+                if (!ok) break;
+                load_head<Q, N>(p, smem, buf, sg.g * p.hpg + sg.ia + j, sg.c, sg.t0, sg.L,
+                                &bars[buf ? kBarFull1 : kBarFull0], ld);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[buf ? kBarFull1 : kBarFull0]);
+                (buf ? uses1 : uses0) += 1;
+            }
+            ++seg;
         }
-        // the bulk copies of the last head loaded have landed before the CTA
+        if (!ok && ld == 0) {
+            flag(p.status, kDevTimeout);
+            *abort_flag = 1;
+        }
+        // the bulk copies of the last heads loaded have landed before the CTA
         // retires (already so unless a wait gave up)
-        if (ld == 0) mbar_wait_bounded(&bars[(last & 1) ? kBarFull1 : kBarFull0], (last >> 1) & 1, lim);
+        if (ld == 0) {
+            if (uses0 > 0) mbar_wait_bounded(&bars[kBarFull0], (uses0 - 1) & 1, lim);
+            if (uses1 > 0) mbar_wait_bounded(&bars[kBarFull1], (uses1 - 1) & 1, lim);
+        }
     } else if (warp == 8) {
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             const uint32_t sC = smem_addr(smem + TL::kC), sB = smem_addr(smem + TL::kB);
             const uint32_t sW = smem_addr(smem + TL::kW);
             constexpr uint32_t kSboNK = 16 * N;  // M/N-direction core-matrix stride of C, B, S_in
-            bool ok = mbar_wait_bounded(&bars[kBarFull0], 0, lim);
-            tc_fence_after();
-            if (ok) {
-                // C . B^T: tile 0 (columns s < 128), tile 1 (all Q columns)
-                for (int kk = 0; kk < N / 16; ++kk)
-                    mma(tmem, smem_desc(sC + 256 * kk, 128, kSboNK), smem_desc(sB + 256 * kk, 128, kSboNK),
-                        idesc_f16(128, TL::kNcols0, 0, 0), kk > 0);
-                if (ntiles > 1)
-                    for (int kk = 0; kk < N / 16; ++kk)
-                        mma(tmem + TL::kCB1, smem_desc(sC + 128 / 8 * kSboNK + 256 * kk, 128, kSboNK),
-                            smem_desc(sB + 256 * kk, 128, kSboNK), idesc_f16(128, 256, 0, 0), kk > 0);
-                mma_commit(&bars[kBarCB]);
-            }
+            bool ok = true;
             int blk = 0, tile = 0;  // running counts of weight blocks and (head, tile) results
-            for (int i = 0; ok && i < hpg; ++i) {
-                const int buf = i & 1;
-                if (i > 0 && !(ok = mbar_wait_bounded(&bars[buf ? kBarFull1 : kBarFull0], (i >> 1) & 1, lim))) break;
-                tc_fence_after();
-                const uint32_t sX = smem_addr(smem + (buf ? TL::kBuf1 : TL::kBuf0));
-                const uint32_t sS = sX + TL::kXBytes;
-                for (int m = 0; ok && m < ntiles; ++m, ++tile) {
-                    if (tile > 0 && !(ok = mbar_wait_bounded(&bars[kBarYFree], (tile - 1) & 1, lim))) break;
+            while (ok && walk.next(p, Q, sg)) {
+                const int ntiles = sg.L > 128 ? 2 : 1;
+                for (int j = 0; ok && j < sg.nh; ++j) {
+                    const int buf = j & 1;
+                    if (!(ok = mbar_wait_bounded(&bars[buf ? kBarFull1 : kBarFull0], (buf ? uses1 : uses0) & 1, lim))) break;
                     tc_fence_after();
-                    // Y1 = C_m . S_in^T, high part then low part
-                    const uint32_t cm = sC + m * (128 / 8) * kSboNK;
-                    for (int part = 0; part < 2; ++part)
+                    if (j == 0) {
+                        // C . B^T: tile 0 (columns s < 128), tile 1 (all Q columns)
                         for (int kk = 0; kk < N / 16; ++kk)
-                            mma(tmem + TL::kY1, smem_desc(cm + 256 * kk, 128, kSboNK),
-                                smem_desc(sS + part * (kTcP * N * 2) + 256 * kk, 128, kSboNK),
-                                idesc_f16(128, kTcP, 0, 0), part > 0 || kk > 0);
-                    // Y2 = sum over blocks W_b . X_b
-                    const int nblk = (m == 0 ? TL::kNcols0 : Q) / kTcBlock;
-                    for (int b = 0; b < nblk; ++b, ++blk) {
-                        const int wb = blk % kWBufs;
-                        if (!(ok = mbar_wait_bounded(&bars[kBarWFull0 + wb], (blk / kWBufs) & 1, lim))) break;
-                        tc_fence_after();
-                        for (int k2 = 0; k2 < kTcBlock / 16; ++k2)
-                            mma(tmem + TL::kY2, smem_desc(sW + wb * TL::kWBuf + 256 * k2, 128, (kTcBlock / 8) * 128),
-                                smem_desc(sX + 16 * (kTcBlock * b + 16 * k2), 128, 16 * Q),
-                                idesc_f16(128, kTcP, 0, 1, 0), b > 0 || k2 > 0);
-                        mma_commit(&bars[kBarWFree0 + wb]);
+                            mma(tmem, smem_desc(sC + 256 * kk, 128, kSboNK), smem_desc(sB + 256 * kk, 128, kSboNK),
+                                idesc_f16(128, TL::kNcols0, 0, 0), kk > 0);
+                        if (ntiles > 1)
+                            for (int kk = 0; kk < N / 16; ++kk)
+                                mma(tmem + TL::kCB1, smem_desc(sC + 128 / 8 * kSboNK + 256 * kk, 128, kSboNK),
+                                    smem_desc(sB + 256 * kk, 128, kSboNK), idesc_f16(128, 256, 0, 0), kk > 0);
+                        mma_commit(&bars[kBarCB]);
                     }
-                    if (ok) mma_commit(&bars[kBarYFull]);
+                    const uint32_t sX = smem_addr(smem + (buf ? TL::kBuf1 : TL::kBuf0));
+                    const uint32_t sS = sX + TL::kXBytes;
+                    for (int m = 0; ok && m < ntiles; ++m, ++tile) {
+                        if (tile > 0 && !(ok = mbar_wait_bounded(&bars[kBarYFree], (tile - 1) & 1, lim))) break;
+                        tc_fence_after();
+                        // Y1 = C_m . S_in^T, high part then low part
+                        const uint32_t cm = sC + m * (128 / 8) * kSboNK;
+                        for (int part = 0; part < 2; ++part)
+                            for (int kk = 0; kk < N / 16; ++kk)
+                                mma(tmem + TL::kY1, smem_desc(cm + 256 * kk, 128, kSboNK),
+                                    smem_desc(sS + part * (kTcP * N * 2) + 256 * kk, 128, kSboNK),
+                                    idesc_f16(128, kTcP, 0, 0), part > 0 || kk > 0);
+                        // Y2 = sum over blocks W_b . X_b
+                        const int nblk = (m == 0 ? TL::kNcols0 : Q) / kTcBlock;
+                        for (int b = 0; b < nblk; ++b, ++blk) {
+                            const int wb = blk % kWBufs;
+                            if (!(ok = mbar_wait_bounded(&bars[kBarWFull0 + wb], (blk / kWBufs) & 1, lim))) break;
+                            tc_fence_after();
+                            for (int k2 = 0; k2 < kTcBlock / 16; ++k2)
+                                mma(tmem + TL::kY2,
+                                    smem_desc(sW + wb * TL::kWBuf + 256 * k2, 128, (kTcBlock / 8) * 128),
+                                    smem_desc(sX + 16 * (kTcBlock * b + 16 * k2), 128, 16 * Q),
+                                    idesc_f16(128, kTcP, 0, 1, 0), b > 0 || k2 > 0);
+                            mma_commit(&bars[kBarWFree0 + wb]);
+                        }
+                        if (ok) mma_commit(&bars[kBarYFull]);
+                    }
+                    if (ok) mma_commit(&bars[buf ? kBarXFree1 : kBarXFree0]);
+                    (buf ? uses1 : uses0) += 1;
                 }
-                if (ok) mma_commit(&bars[buf ? kBarXFree1 : kBarXFree0]);
+                ++seg;
             }
             if (!ok) {
                 flag(p.status, kDevTimeout);
@@ -428,148 +485,166 @@ __global__ void __launch_bounds__(kTcThreads, 1) ssd_scan_tc_kernel(const SsdPar
         float *cbd_s = reinterpret_cast<float *>(smem + TL::kCbd);
         const __nv_bfloat16 *zg = static_cast<const __nv_bfloat16 *>(p.z);
         __nv_bfloat16 *yg = static_cast<__nv_bfloat16 *>(p.y);
-        bool ok = mbar_wait_bounded(&bars[kBarCB], 0, lim);
-        tc_fence_after();
-        if (ok) {
-            // the largest |C_t . B_s| over the chunk's rows: with dt' it
-            // bounds every weight (the decays are at most 1), and so picks
-            // the power-of-two scale of each head's fp16 weights
-            float mcb = 0.f;
-            for (int m = 0; m < ntiles; ++m) {
-                const int ncol = m == 0 ? TL::kNcols0 : Q;
-                for (int s0 = half * (ncol / 2); s0 < (half + 1) * (ncol / 2); s0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem + lane_base + (m == 0 ? 0u : static_cast<uint32_t>(TL::kCB1)) + s0, r);
-                    tmem_wait_ld();
-                    if (128 * m + t < L) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) mcb = fmaxf(mcb, fabsf(__uint_as_float(r[j])));
-                    }
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mcb = fmaxf(mcb, __shfl_xor_sync(0xffffffffu, mcb, off));
-            if (lane == 0) atomicMax(cbmax, __float_as_uint(mcb));
-        }
+        bool ok = true;
         int blk = 0, tile = 0, ephase = 0;
-        for (int i = 0; ok && i < hpg; ++i) {
-            const int buf = i & 1, h = h0 + i;
-            if (!(ok = mbar_wait_bounded(&bars[buf ? kBarFull1 : kBarFull0], (i >> 1) & 1, lim))) break;
-            float *aux = reinterpret_cast<float *>(smem + (buf ? TL::kAux1 : TL::kAux0));
-            const float *cs = aux, *dtp = aux + Q;
-            float *E = aux + 2 * Q, *cs2 = aux + 3 * Q;
-            // per column: cs log2(e), and E_s = 2^(cs2_r - cs2_s) dt'_s with r the last column of s's block
-            for (int s = tid; s < Q; s += kEpi) {
-                const float c2 = cs[s] * kLog2e;
-                cs2[s] = c2;
-                E[s] = ex2(cs[s | (kTcBlock - 1)] * kLog2e - c2) * dtp[s];
-            }
-            if (!(ok = epi_sync(&bars[kBarEpi], ephase, lim))) break;
-            const unsigned char *xs = smem + (buf ? TL::kBuf1 : TL::kBuf0);
-            const float Dh = p.D ? p.D[h] : 0.f;
-            // the weights are formed times 2^kw, x was staged times 2^kx
-            const int kw = fp16_scale_exp(__uint_as_float(*cbmax) * aux[4 * Q + 1]);
-            const float sw = pow2i(kw), xinv = aux[4 * Q], yinv = xinv * pow2i(-kw);
-            for (int m = 0; ok && m < ntiles; ++m, ++tile) {
-                const int tg = 128 * m + t;  // token row within the chunk
-                const float cst = cs2[tg < Q ? tg : Q - 1];
-                // the gate's z row of this thread's outputs, in flight while the weights are formed
-                const int64_t row = ((t0 + tg) * p.H + h) * static_cast<int64_t>(kTcP);
-                uint4 zpre[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
-                                 make_uint4(0u, 0u, 0u, 0u)};
-                if (zg && tg < L) {
+        float seg_cbmax = 0.f;
+        while (ok && walk.next(p, Q, sg)) {
+            const int ntiles = sg.L > 128 ? 2 : 1;
+            const int L = sg.L;
+            const int64_t t0 = sg.t0;
+            for (int j = 0; ok && j < sg.nh; ++j) {
+                const int buf = j & 1, h = sg.g * p.hpg + sg.ia + j;
+                if (j == 0) {
+                    if (!(ok = mbar_wait_bounded(&bars[kBarCB], seg & 1, lim))) break;
+                    tc_fence_after();
+                    // the largest |C_t . B_s| over the chunk's rows: with dt'
+                    // it bounds every weight (the decays are at most 1), and
+                    // so picks the power-of-two scale of each head's weights
+                    float mcb = 0.f;
+                    for (int m = 0; m < ntiles; ++m) {
+                        const int ncol = m == 0 ? TL::kNcols0 : Q;
+                        for (int s0 = half * (ncol / 2); s0 < (half + 1) * (ncol / 2); s0 += 16) {
+                            uint32_t r[16];
+                            tmem_ld16(tmem + lane_base + (m == 0 ? 0u : static_cast<uint32_t>(TL::kCB1)) + s0, r);
+                            tmem_wait_ld();
+                            if (128 * m + t < L) {
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        zpre[jj] = __ldg(reinterpret_cast<const uint4 *>(zg + row + 8 * (4 * half + jj)));
-                }
-                const uint32_t cbcol = m == 0 ? 0u : static_cast<uint32_t>(TL::kCB1);
-                const int nblk = (m == 0 ? TL::kNcols0 : Q) / kTcBlock;
-                for (int b = 0; b < nblk; ++b, ++blk) {
-                    const int wb = blk % kWBufs;
-                    if (blk >= kWBufs &&
-                        !(ok = mbar_wait_bounded(&bars[kBarWFree0 + wb], ((blk - kWBufs) / kWBufs) & 1, lim)))
-                        break;
-                    const int s0 = kTcBlock * b + 16 * half;  // this thread's 16 columns
-                    uint32_t r[16];
-                    tmem_ld16(tmem + lane_base + cbcol + s0, r);
-                    tmem_wait_ld();
-                    float wv[16];
-                    if (kTcBlock * b + kTcBlock <= tg) {
-                        // the block lies wholly before row t
-                        const float R = ex2(cst - cs2[kTcBlock * b + kTcBlock - 1]) * sw;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) wv[j] = __uint_as_float(r[j]) * R * E[s0 + j];
-                    } else if (kTcBlock * b > tg) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) wv[j] = 0.f;
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int s = s0 + j;
-                            const float cb = __uint_as_float(r[j]);
-                            if (s == tg) cbd_s[(tile & 1) * 128 + t] = cb;
-                            wv[j] = s < tg ? cb * ex2(cst - cs2[s]) * (dtp[s] * sw) : 0.f;
-                        }
-                    }
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const __half2 h2 = __floats2half2_rn(wv[2 * j], wv[2 * j + 1]);
-                        hv[j] = *reinterpret_cast<const uint32_t *>(&h2);
-                    }
-                    const int off = wb * TL::kWBuf + (t >> 3) * ((kTcBlock / 8) * 128) + 2 * half * 128 + (t & 7) * 16;
-                    *reinterpret_cast<uint4 *>(wsm + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                    *reinterpret_cast<uint4 *>(wsm + off + 128) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bars[kBarWFull0 + wb]);
-                }
-                if (!ok) break;
-                // the tile's results; the thread holding row t's diagonal has stored it
-                if (!(ok = mbar_wait_bounded(&bars[kBarYFull], tile & 1, lim))) break;
-                tc_fence_after();
-                if (!(ok = epi_sync(&bars[kBarEpi], ephase, lim))) break;
-                uint32_t y1[32], y2[32];
-                tmem_ld16(tmem + lane_base + TL::kY1 + 32 * half, y1);
-                tmem_ld16(tmem + lane_base + TL::kY1 + 32 * half + 16, y1 + 16);
-                tmem_ld16(tmem + lane_base + TL::kY2 + 32 * half, y2);
-                tmem_ld16(tmem + lane_base + TL::kY2 + 32 * half + 16, y2 + 16);
-                tmem_wait_ld();
-                const float cbd = cbd_s[(tile & 1) * 128 + t];
-                tc_fence_before();
-                mbar_arrive(&bars[kBarYFree]);
-                if (tg < L) {
-                    const float e1 = ex2(cst);
-                    const float wd = fmaf(cbd, dtp[tg], Dh) * xinv;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = 4 * half + jj;  // p-octet
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(xs + j * (16 * Q) + 16 * tg);
-                        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};  // fp16 pairs
-                        const uint32_t zw[4] = {zpre[jj].x, zpre[jj].y, zpre[jj].z, zpre[jj].w};
-                        uint32_t out[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float v[2];
-#pragma unroll
-                            for (int k = 0; k < 2; ++k) {
-                                const int pp = 8 * jj + 2 * e + k;
-                                const float xv1 = __half2float(__ushort_as_half(
-                                    static_cast<unsigned short>(k ? (xw[e] >> 16) : (xw[e] & 0xffffu))));
-                                v[k] = fmaf(wd, xv1, fmaf(e1, __uint_as_float(y1[pp]), __uint_as_float(y2[pp]) * yinv));
-                                if (zg) {
-                                    const float zz = __uint_as_float(k ? (zw[e] & 0xffff0000u) : (zw[e] << 16));
-                                    v[k] *= __fdividef(zz, 1.f + __expf(-zz));
-                                }
+                                for (int jj = 0; jj < 16; ++jj) mcb = fmaxf(mcb, fabsf(__uint_as_float(r[jj])));
                             }
-                            out[e] = pack_bf16x2(v[0], v[1]);
                         }
-                        *reinterpret_cast<uint4 *>(yg + row + 8 * j) = make_uint4(out[0], out[1], out[2], out[3]);
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mcb = fmaxf(mcb, __shfl_xor_sync(0xffffffffu, mcb, off));
+                    if (lane == 0) wmax[(seg & 1) * 8 + warp] = mcb;
+                }
+                if (!(ok = mbar_wait_bounded(&bars[buf ? kBarFull1 : kBarFull0], (buf ? uses1 : uses0) & 1, lim))) break;
+                float *aux = reinterpret_cast<float *>(smem + (buf ? TL::kAux1 : TL::kAux0));
+                const float *cs = aux, *dtp = aux + Q;
+                float *E = aux + 2 * Q, *cs2 = aux + 3 * Q;
+                // per column: cs log2(e), and E_s = 2^(cs2_r - cs2_s) dt'_s with r the last column of s's block
+                for (int s = tid; s < Q; s += kEpi) {
+                    const float c2 = cs[s] * kLog2e;
+                    cs2[s] = c2;
+                    E[s] = ex2(cs[s | (kTcBlock - 1)] * kLog2e - c2) * dtp[s];
+                }
+                if (!(ok = epi_sync(&bars[kBarEpi], ephase, lim))) break;
+                if (j == 0) {
+                    seg_cbmax = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) seg_cbmax = fmaxf(seg_cbmax, wmax[(seg & 1) * 8 + w]);
+                }
+                const unsigned char *xs = smem + (buf ? TL::kBuf1 : TL::kBuf0);
+                const float Dh = p.D ? p.D[h] : 0.f;
+                // the weights are formed times 2^kw, x was staged times 2^kx
+                const int kw = fp16_scale_exp(seg_cbmax * aux[4 * Q + 1]);
+                const float sw = pow2i(kw), xinv = aux[4 * Q], yinv = xinv * pow2i(-kw);
+                for (int m = 0; ok && m < ntiles; ++m, ++tile) {
+                    const int tg = 128 * m + t;  // token row within the chunk
+                    const float cst = cs2[tg < Q ? tg : Q - 1];
+                    // the gate's z row of this thread's outputs, in flight while the weights are formed
+                    const int64_t row = ((t0 + tg) * p.H + h) * static_cast<int64_t>(kTcP);
+                    uint4 zpre[4] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u),
+                                     make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+                    if (zg && tg < L) {
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            zpre[jj] = __ldg(reinterpret_cast<const uint4 *>(zg + row + 8 * (4 * half + jj)));
+                    }
+                    const uint32_t cbcol = m == 0 ? 0u : static_cast<uint32_t>(TL::kCB1);
+                    const int nblk = (m == 0 ? TL::kNcols0 : Q) / kTcBlock;
+                    for (int b = 0; b < nblk; ++b, ++blk) {
+                        const int wb = blk % kWBufs;
+                        if (blk >= kWBufs &&
+                            !(ok = mbar_wait_bounded(&bars[kBarWFree0 + wb], ((blk - kWBufs) / kWBufs) & 1, lim)))
+                            break;
+                        const int s0 = kTcBlock * b + 16 * half;  // this thread's 16 columns
+                        uint32_t r[16];
+                        tmem_ld16(tmem + lane_base + cbcol + s0, r);
+                        tmem_wait_ld();
+                        float wv[16];
+                        if (kTcBlock * b + kTcBlock <= tg) {
+                            // the block lies wholly before row t
+                            const float R = ex2(cst - cs2[kTcBlock * b + kTcBlock - 1]) * sw;
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) wv[jj] = __uint_as_float(r[jj]) * R * E[s0 + jj];
+                        } else if (kTcBlock * b > tg) {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) wv[jj] = 0.f;
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int s = s0 + jj;
+                                const float cb = __uint_as_float(r[jj]);
+                                if (s == tg) cbd_s[(tile & 1) * 128 + t] = cb;
+                                wv[jj] = s < tg ? cb * ex2(cst - cs2[s]) * (dtp[s] * sw) : 0.f;
+                            }
+                        }
+                        uint32_t hv[8];
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const __half2 h2 = __floats2half2_rn(wv[2 * jj], wv[2 * jj + 1]);
+                            hv[jj] = *reinterpret_cast<const uint32_t *>(&h2);
+                        }
+                        const int off =
+                            wb * TL::kWBuf + (t >> 3) * ((kTcBlock / 8) * 128) + 2 * half * 128 + (t & 7) * 16;
+                        *reinterpret_cast<uint4 *>(wsm + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                        *reinterpret_cast<uint4 *>(wsm + off + 128) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                        fence_proxy_async_smem();
+                        mbar_arrive(&bars[kBarWFull0 + wb]);
+                    }
+                    if (!ok) break;
+                    // the tile's results; the thread holding row t's diagonal has stored it
+                    if (!(ok = mbar_wait_bounded(&bars[kBarYFull], tile & 1, lim))) break;
+                    tc_fence_after();
+                    if (!(ok = epi_sync(&bars[kBarEpi], ephase, lim))) break;
+                    uint32_t y1[32], y2[32];
+                    tmem_ld16(tmem + lane_base + TL::kY1 + 32 * half, y1);
+                    tmem_ld16(tmem + lane_base + TL::kY1 + 32 * half + 16, y1 + 16);
+                    tmem_ld16(tmem + lane_base + TL::kY2 + 32 * half, y2);
+                    tmem_ld16(tmem + lane_base + TL::kY2 + 32 * half + 16, y2 + 16);
+                    tmem_wait_ld();
+                    const float cbd = cbd_s[(tile & 1) * 128 + t];
+                    tc_fence_before();
+                    mbar_arrive(&bars[kBarYFree]);
+                    if (tg < L) {
+                        const float e1 = ex2(cst);
+                        const float wd = fmaf(cbd, dtp[tg], Dh) * xinv;
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int jo = 4 * half + jj;  // p-octet
+                            const uint4 xv = *reinterpret_cast<const uint4 *>(xs + jo * (16 * Q) + 16 * tg);
+                            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};  // fp16 pairs
+                            const uint32_t zw[4] = {zpre[jj].x, zpre[jj].y, zpre[jj].z, zpre[jj].w};
+                            uint32_t out[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float v[2];
+#pragma unroll
+                                for (int k = 0; k < 2; ++k) {
+                                    const int pp = 8 * jj + 2 * e + k;
+                                    const float xv1 = __half2float(__ushort_as_half(
+                                        static_cast<unsigned short>(k ? (xw[e] >> 16) : (xw[e] & 0xffffu))));
+                                    v[k] = fmaf(wd, xv1,
+                                                fmaf(e1, __uint_as_float(y1[pp]), __uint_as_float(y2[pp]) * yinv));
+                                    if (zg) {
+                                        const float zz = __uint_as_float(k ? (zw[e] & 0xffff0000u) : (zw[e] << 16));
+                                        v[k] *= __fdividef(zz, 1.f + __expf(-zz));
+                                    }
+                                }
+                                out[e] = pack_bf16x2(v[0], v[1]);
+                            }
+                            *reinterpret_cast<uint4 *>(yg + row + 8 * jo) = make_uint4(out[0], out[1], out[2], out[3]);
+                        }
                     }
                 }
+                // this head's buffer (x rows, state, sums) may be refilled and,
+                // after a segment's last head, C . B^T replaced
+                if (!ok) break;
+                tc_fence_before();
+                mbar_arrive(&bars[buf ? kBarXFree1 : kBarXFree0]);
+                (buf ? uses1 : uses0) += 1;
             }
-            // this head's buffer (x rows, state, sums) may be refilled
-            if (!ok) break;
-            mbar_arrive(&bars[buf ? kBarXFree1 : kBarXFree0]);
+            ++seg;
         }
         if (!ok) {
             if (tid == 0) flag(p.status, kDevTimeout);
@@ -582,14 +657,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) ssd_scan_tc_kernel(const SsdPar
     if (warp == 8) tmem_dealloc512(tmem);
 }
 
+// Number of SMs of the current device (cached per device).
+static int tc_sm_count() {
+    static int cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = __atomic_load_n(&cache[dev], __ATOMIC_RELAXED);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        __atomic_store_n(&cache[dev], n, __ATOMIC_RELAXED);
+    }
+    return n;
+}
+
+// A persistent grid: one CTA per SM (the layout takes most of an SM's shared
+// memory), or one per unit when there are fewer units.
 template <int Q, int N>
 cudaError_t launch_scan_tc_qn(const SsdParams &p, cudaStream_t stream) {
     using TL = TcLayout<Q, N>;
     cudaError_t e = cudaFuncSetAttribute(ssd_scan_tc_kernel<Q, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TL::kBytes);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(p.G), static_cast<unsigned>(p.nchunks));
-    ssd_scan_tc_kernel<Q, N><<<grid, kTcThreads, TL::kBytes, stream>>>(p);
+    const int sms = tc_sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int64_t units = p.nchunks * p.G * p.hpg;
+    if (units == 0) return cudaSuccess;
+    const int64_t grid = units < sms ? units : sms;
+    ssd_scan_tc_kernel<Q, N><<<static_cast<unsigned>(grid), kTcThreads, TL::kBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -216,3 +216,15 @@ def test_ssd_operands_outside_fp16_range(libssu, scale_x, scale_bc, dt_shift):
     k = 1.0 / float(ref.y_exact.abs().max())
     assert_ssd_y_close(y.double().cpu() * k, ref.y_exact * k, what=f"y / {1 / k:.3g}")
     assert_ssd_states_close(states, ref.states[w.last_chunk_indices.long()])
+
+
+@pytest.mark.parametrize("chunk_size,dstate,lengths", [(64, 128, [130, 64, 255, 1, 77]), (256, 128, [300, 513, 77]),
+                                                       (128, 64, [129, 400, 3, 250])])
+def test_ssd_scan_ranges_cross_chunks_and_groups(libssu, chunk_size, dstate, lengths):
+    """More (chunk, group, head) units than SMs: each CTA of the scan takes a
+    contiguous range that starts and ends inside a group's heads and crosses
+    into the next group or chunk, whose C . B^T it computes afresh."""
+    w = workloads.ssd_problem(300 + chunk_size, lengths, heads=32, dim=64, dstate=dstate, groups=2,
+                              chunk_size=chunk_size)
+    assert int(w.seq_idx.numel()) * 32 > torch.cuda.get_device_properties(0).multi_processor_count
+    check(w)
