@@ -32,6 +32,7 @@
 // columns each, in interleaved groups of four); the entries' and drafts'
 // operands are staged in shared memory once per CTA.
 #include <cstdint>
+#include <type_traits>
 
 #include "ssu_device.cuh"
 #include "ssu_verify.h"
@@ -41,22 +42,44 @@ namespace ssu {
 constexpr int kVerifyRows = 64;             // dim rows per CTA
 constexpr int kVerifyThreads = 4 * kVerifyRows;
 
-__device__ __forceinline__ float load_small(const void *base, int64_t i, int dtype) {
-    return dtype == kF32 ? static_cast<const float *>(base)[i]
-                         : bits_to_float(static_cast<const unsigned short *>(base)[i], dtype);
+// Element i of an array of dtype IO: its stored bits (16-bit types
+// zero-extended), its value, and a store of stored bits.  IO is a template
+// argument: the staging code is compiled once per operand dtype and chosen
+// once per CTA.
+template <int IO>
+__device__ __forceinline__ uint32_t io_bits(const void *base, int64_t i) {
+    if constexpr (IO == kF32)
+        return __float_as_uint(static_cast<const float *>(base)[i]);
+    else
+        return static_cast<const unsigned short *>(base)[i];
 }
-
-// Element i of an io-dtype array as its stored bits (16-bit types zero-extended).
-__device__ __forceinline__ uint32_t load_bits(const void *base, int64_t i, int dtype) {
-    return dtype == kF32 ? __float_as_uint(static_cast<const float *>(base)[i])
-                         : static_cast<const unsigned short *>(base)[i];
+template <int IO>
+__device__ __forceinline__ float io_value(uint32_t bits) {
+    if constexpr (IO == kF32)
+        return __uint_as_float(bits);
+    else if constexpr (IO == kBF16)
+        return __uint_as_float(bits << 16);
+    else
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
 }
-
-__device__ __forceinline__ void store_bits(void *base, int64_t i, int dtype, uint32_t v) {
-    if (dtype == kF32)
+template <int IO>
+__device__ __forceinline__ float io_load(const void *base, int64_t i) { return io_value<IO>(io_bits<IO>(base, i)); }
+template <int IO>
+__device__ __forceinline__ void io_store_bits(void *base, int64_t i, uint32_t v) {
+    if constexpr (IO == kF32)
         static_cast<uint32_t *>(base)[i] = v;
     else
         static_cast<unsigned short *>(base)[i] = static_cast<unsigned short>(v);
+}
+// A run-time dtype of the operands as a template argument.
+template <typename F>
+__device__ __forceinline__ void with_io(int dtype, F &&f) {
+    if (dtype == kF32)
+        f(std::integral_constant<int, kF32>{});
+    else if (dtype == kBF16)
+        f(std::integral_constant<int, kBF16>{});
+    else
+        f(std::integral_constant<int, kF16>{});
 }
 
 __device__ __forceinline__ void store_ts(float *o, float v) { *o = v; }
@@ -95,11 +118,14 @@ struct VerifyStage {
     uint32_t *rx;  // [T][64] the drafts' x as stored bits
     float *bc;   // [c + T][T] B_m . C_k (entry m < c, else draft m - c)
     float *us;   // [T][64] S_ckpt row . C_k
+    float *ga;   // [c + T][64] decay exp(A dt'_m) of each step and row
+    float *te;   // [c + T][64] input term dt'_m x_m of each step and row
 };
 
 __host__ __device__ inline size_t verify_smem_bytes(int L, int T, int N) {
     return sizeof(float) * (static_cast<size_t>(L) * N + 2 * L * kVerifyRows + 3 * static_cast<size_t>(T) * N +
-                            5 * T * kVerifyRows + static_cast<size_t>(L + T) * T);
+                            5 * T * kVerifyRows + static_cast<size_t>(L + T) * T +
+                            2 * static_cast<size_t>(L + T) * kVerifyRows);
 }
 
 __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, int N) {
@@ -116,23 +142,27 @@ __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, i
     st.rx = st.rB + T * N;
     st.us = reinterpret_cast<float *>(st.rx + T * kVerifyRows);
     st.bc = st.us + T * kVerifyRows;
+    st.ga = st.bc + (L + T) * T;
+    st.te = st.ga + (L + T) * kVerifyRows;
     return st;
 }
 
 // Entries 0 .. c-1 of (slot, head h, group g) for rows row0 .. row0+63.
+template <int IO, int N>
 __device__ __forceinline__ void stage_entries(const KParams &p, const VerifyStage &st, int64_t slot, int c, int h,
                                               int g, int row0) {
-    for (int i = threadIdx.x; i < c * p.N; i += kVerifyThreads) {
-        const int j = i / p.N, n = i % p.N;
-        st.eB[j * p.N + n] = load_small(p.Bbuf, ((slot * p.rlen + j) * p.G + g) * static_cast<int64_t>(p.N) + n,
-                                        p.io_dtype);
+    const int64_t eb0 = (slot * p.rlen * p.G + g) * static_cast<int64_t>(N);  // entry 0's B
+    for (int i = threadIdx.x; i < c * N; i += kVerifyThreads) {
+        const int j = i / N, n = i % N;
+        st.eB[i] = io_load<IO>(p.Bbuf, eb0 + static_cast<int64_t>(j) * p.G * N + n);
     }
+    const int64_t e0 = (slot * p.rlen * p.H + h) * static_cast<int64_t>(p.P) + row0;  // entry 0's row row0
     for (int i = threadIdx.x; i < c * kVerifyRows; i += kVerifyThreads) {
-        const int j = i / kVerifyRows, r = i % kVerifyRows, row = row0 + r;
-        if (row >= p.P) continue;
-        const int64_t e = ((slot * p.rlen + j) * p.H + h) * static_cast<int64_t>(p.P) + row;
-        st.ed[j * kVerifyRows + r] = p.dtbuf[e];
-        st.ex[j * kVerifyRows + r] = load_small(p.xbuf, e, p.io_dtype);
+        const int j = i / kVerifyRows, r = i % kVerifyRows;
+        if (row0 + r >= p.P) continue;
+        const int64_t e = e0 + static_cast<int64_t>(j) * p.H * p.P + r;
+        st.ed[i] = p.dtbuf[e];
+        st.ex[i] = io_load<IO>(p.xbuf, e);
     }
 }
 
@@ -203,7 +233,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
     if (!verify_sequence(p, b, &slot, &c, &pad)) return;  // flagged (again) by the verify launch
     if (pad || c + 2 * T < p.rlen) return;                 // no flush here
     const VerifyStage st = verify_stage(vsmem, p.rlen, T, p.N);
-    stage_entries(p, st, slot, c, h, g, row0);
+    with_io(p.io_dtype, [&](auto io) { stage_entries<decltype(io)::value, 4 * NPT>(p, st, slot, c, h, g, row0); });
     __syncthreads();
     if (row >= p.P) return;
     TS *srow = static_cast<TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N;
@@ -239,65 +269,83 @@ __global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verif
     } else {
         load_state_part<TS, NPT>(srow, q, s);
     }
-    stage_entries(p, st, slot, c, h, g, row0);
     const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
-    for (int i = threadIdx.x; i < T * p.N; i += kVerifyThreads) {
-        const int k = i / p.N, n = i % p.N;
-        const int64_t rr = b * T + k;
-        const uint32_t bb = load_bits(p.B, rr * p.Bs[0] + g * p.Bs[1] + n * p.Bs[2], p.io_dtype);
-        st.dC[k * p.N + n] = load_small(p.C, rr * p.Cs[0] + g * p.Cs[1] + n * p.Cs[2], p.io_dtype);
-        st.dB[k * p.N + n] = bits_to_float(bb, p.io_dtype);
-        st.rB[k * p.N + n] = bb;
-    }
-    for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
-        const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
-        if (rrow >= p.P) continue;
-        const int64_t rr = b * T + k;
-        st.dd[k * kVerifyRows + rw] =
-            processed_step(load_small(p.dt, rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2], p.dt_dtype), bias,
-                           p.softplus);
-        const uint32_t xb = load_bits(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2], p.io_dtype);
-        st.dx[k * kVerifyRows + rw] = bits_to_float(xb, p.io_dtype);
-        st.rx[k * kVerifyRows + rw] = xb;
-        st.dz[k * kVerifyRows + rw] =
-            p.z ? load_small(p.z, rr * p.zs[0] + h * p.zs[1] + rrow * p.zs[2], p.io_dtype) : 0.f;
-    }
-    __syncthreads();
-    // The drafts become entries c .. c+T-1, written by the whole CTA from the
-    // stage before the state walk, so that the stores drain while it runs:
-    // x and B keep their bits, the processed step is stored in fp32; B once
-    // per group, by the group's first head.  No CTA reads these entries.
-    if (!pad) {
+    with_io(p.io_dtype, [&](auto io) {
+        constexpr int IO = decltype(io)::value;
+        constexpr int N = 4 * NPT;
+        stage_entries<IO, N>(p, st, slot, c, h, g, row0);
+        for (int i = threadIdx.x; i < T * N; i += kVerifyThreads) {
+            const int k = i / N, n = i % N;
+            const int64_t rr = b * T + k;
+            const uint32_t bb = io_bits<IO>(p.B, rr * p.Bs[0] + g * p.Bs[1] + n * p.Bs[2]);
+            st.dC[i] = io_load<IO>(p.C, rr * p.Cs[0] + g * p.Cs[1] + n * p.Cs[2]);
+            st.dB[i] = io_value<IO>(bb);
+            st.rB[i] = bb;
+        }
         for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
             const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
             if (rrow >= p.P) continue;
-            const int64_t e = ((slot * p.rlen + c + k) * p.H + h) * static_cast<int64_t>(p.P) + rrow;
-            store_bits(p.xbuf, e, p.io_dtype, st.rx[i]);
-            p.dtbuf[e] = st.dd[i];
+            const int64_t rr = b * T + k;
+            const float dtv = p.dt_dtype == kF32 ? static_cast<const float *>(p.dt)[rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2]]
+                                                 : bits_to_float(static_cast<const unsigned short *>(p.dt)[rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2]], p.dt_dtype);
+            st.dd[i] = processed_step(dtv, bias, p.softplus);
+            const uint32_t xb = io_bits<IO>(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2]);
+            st.dx[i] = io_value<IO>(xb);
+            st.rx[i] = xb;
+            st.dz[i] = p.z ? io_load<IO>(p.z, rr * p.zs[0] + h * p.zs[1] + rrow * p.zs[2]) : 0.f;
         }
-        if (h % p.heads_per_group == 0 && blockIdx.z == 0) {
-            for (int i = threadIdx.x; i < T * p.N; i += kVerifyThreads) {
-                const int k = i / p.N, n = i % p.N;
-                store_bits(p.Bbuf, ((slot * p.rlen + c + k) * p.G + g) * static_cast<int64_t>(p.N) + n, p.io_dtype,
-                           st.rB[i]);
+        __syncthreads();
+        // The drafts become entries c .. c+T-1, written by the whole CTA from
+        // the stage before the state walk, so that the stores drain while it
+        // runs: x and B keep their bits, the processed step is stored in fp32;
+        // B once per group, by the group's first head.  No CTA reads these
+        // entries.
+        if (!pad) {
+            const int64_t e0 = ((slot * p.rlen + c) * p.H + h) * static_cast<int64_t>(p.P) + row0;
+            for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
+                const int k = i / kVerifyRows, rw = i % kVerifyRows;
+                if (row0 + rw >= p.P) continue;
+                const int64_t e = e0 + static_cast<int64_t>(k) * p.H * p.P + rw;
+                io_store_bits<IO>(p.xbuf, e, st.rx[i]);
+                p.dtbuf[e] = st.dd[i];
+            }
+            if (h % p.heads_per_group == 0 && blockIdx.z == 0) {
+                const int64_t eb = ((slot * p.rlen + c) * p.G + g) * static_cast<int64_t>(N);
+                for (int i = threadIdx.x; i < T * N; i += kVerifyThreads) {
+                    const int k = i / N, n = i % N;
+                    io_store_bits<IO>(p.Bbuf, eb + static_cast<int64_t>(k) * p.G * N + n, st.rB[i]);
+                }
             }
         }
+    });
+    // Each step's decay and input term per row, once (the walks of the
+    // drafts share them): steps m < c are the entries, m >= c the drafts.
+    const float Ah = p.A[h];
+    for (int i = threadIdx.x; i < (c + T) * kVerifyRows; i += kVerifyThreads) {
+        const int m = i / kVerifyRows;
+        const bool entry = m < c;
+        const float d = entry ? st.ed[i] : st.dd[i - c * kVerifyRows];
+        const float xv = entry ? st.ex[i] : st.dx[i - c * kVerifyRows];
+        st.ga[i] = decay_inline(Ah, d);
+        st.te[i] = d * xv;
     }
     // B_m . C_k for every step m <= c + k that draft k sees, one warp per dot
+    constexpr int N = 4 * NPT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = warp; i < (c + T) * T; i += kVerifyThreads / 32) {
         const int m = i / T, k = i % T;
         if (m > c + k) continue;  // masked: the same for the whole warp
-        const float *Bm = m < c ? st.eB + m * p.N : st.dB + (m - c) * p.N;
-        const float *Ck = st.dC + k * p.N;
+        const float *Bm = m < c ? st.eB + m * N : st.dB + (m - c) * N;
+        const float *Ck = st.dC + k * N;
         float v = 0.f;
-        for (int n = lane; n < p.N; n += 32) v = fmaf(Bm[n], Ck[n], v);
+#pragma unroll
+        for (int n = lane; n < N; n += 32) v = fmaf(Bm[n], Ck[n], v);
         v = row_sum<32>(v);
         if (lane == 0) st.bc[i] = v;
     }
     // S_ckpt . C_k of this row, over the row's four threads
     for (int k = 0; k < T; ++k) {
-        const float *Ck = st.dC + k * p.N;
+        const float *Ck = st.dC + k * N;
         float part = 0.f;
 #pragma unroll
         for (int i4 = 0; i4 < NPT / 4; ++i4) {
@@ -314,16 +362,12 @@ __global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verif
     if (!active) return;
     // draft k (thread q of the row takes k = q, q + 4, ...): the walk from
     // step c + k down to step 0 gathers the decayed window sum and g_{0:M}
-    const float Ah = p.A[h];
     const float Dh = p.D ? p.D[h] : 0.f;
     for (int k = q; k < T; k += 4) {
         float acc = 0.f, gam = 1.f;
         for (int m = c + k; m >= 0; --m) {
-            const bool entry = m < c;
-            const float d = entry ? st.ed[m * kVerifyRows + r] : st.dd[(m - c) * kVerifyRows + r];
-            const float xv = entry ? st.ex[m * kVerifyRows + r] : st.dx[(m - c) * kVerifyRows + r];
-            acc = fmaf(gam, (d * xv) * st.bc[m * T + k], acc);
-            gam *= decay_inline(Ah, d);
+            acc = fmaf(gam, st.te[m * kVerifyRows + r] * st.bc[m * T + k], acc);
+            gam *= st.ga[m * kVerifyRows + r];
         }
         const float sum = fmaf(gam, st.us[k * kVerifyRows + r], acc);
         const int64_t rr = b * T + k;
