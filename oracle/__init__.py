@@ -139,7 +139,14 @@ class _SsdProblem(ctypes.Structure):
 
 
 # Formats of the low-precision read copy (ssu_oracle.h, ORC_SHADOW_*).
-SHADOW_NONE, SHADOW_F16, SHADOW_E4M3 = 0, 1, 2
+SHADOW_NONE, SHADOW_F16, SHADOW_E4M3, SHADOW_NVFP4 = 0, 1, 2, 3
+
+
+def nvfp4_scale_words(dstate: int) -> int:
+    """Floats of one row's NVFP4 scale record (ssu_oracle.h): the fp32 row
+    scale, then the dstate / 16 E4M3 block-scale codes as bytes, padded to a
+    multiple of 16 bytes."""
+    return (4 + dstate // 16 + 15) // 16 * 4
 
 _lib = None
 
@@ -170,6 +177,12 @@ def load_library(path: str):
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
     lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.orc_e4m3_decode.restype = ctypes.c_double
+    lib.orc_e2m1_encode.argtypes = [ctypes.c_double]
+    lib.orc_e2m1_encode.restype = ctypes.c_uint8
+    lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_decode.restype = ctypes.c_double
+    lib.orc_nvfp4_scale_words.argtypes = [ctypes.c_int64]
+    lib.orc_nvfp4_scale_words.restype = ctypes.c_int64
     return lib
 
 
@@ -332,7 +345,9 @@ def replay(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tenso
     dtbuf ``[slots, L, heads, dim]`` fp32; Bbuf ``[slots, L, groups, dstate]`` (x's dtype);
     count ``[batch]`` entries buffered per sequence.  With a read copy
     (``shadow_format`` SHADOW_F16: ``shadow`` fp16 codes as int16/float16,
-    SHADOW_E4M3: uint8 codes and ``shadow_scale [slots, heads, dim]`` fp32),
+    SHADOW_E4M3: uint8 codes and ``shadow_scale [slots, heads, dim]`` fp32,
+    SHADOW_NVFP4: uint8 ``[slots, heads, dim, dstate / 2]`` code pairs and
+    ``shadow_scale [slots, heads, dim, nvfp4_scale_words(dstate)]`` fp32 records),
     steps that do not fold read it instead of the checkpoint and a fold
     rewrites it.  Inputs are not modified."""
     lib = lib or _load()
@@ -426,7 +441,9 @@ def replay_verify(ckpt: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torc
 def shadow_refresh(state: torch.Tensor, shadow_format: int, lib=None):
     """The read copy of a state pool ``[..., dstate]``: (codes, row scales)
     -- fp16 codes as float16 and no scales for SHADOW_F16, uint8 E4M3 codes
-    and fp32 scales of shape ``state.shape[:-1]`` for SHADOW_E4M3."""
+    and fp32 scales of shape ``state.shape[:-1]`` for SHADOW_E4M3, uint8 code
+    pairs ``[..., dstate / 2]`` and fp32 scale records ``[...,
+    nvfp4_scale_words(dstate)]`` for SHADOW_NVFP4."""
     lib = lib or _load()
     st = _cpu(state).contiguous()
     dstate = st.shape[-1]
@@ -435,6 +452,9 @@ def shadow_refresh(state: torch.Tensor, shadow_format: int, lib=None):
         codes, scale = torch.empty(st.shape, dtype=torch.float16), None
     elif shadow_format == SHADOW_E4M3:
         codes, scale = torch.empty(st.shape, dtype=torch.uint8), torch.empty(st.shape[:-1], dtype=torch.float32)
+    elif shadow_format == SHADOW_NVFP4:
+        codes = torch.empty((*st.shape[:-1], dstate // 2), dtype=torch.uint8)
+        scale = torch.zeros((*st.shape[:-1], nvfp4_scale_words(dstate)), dtype=torch.float32)
     else:
         raise ValueError("unknown read-copy format")
     rc = lib.orc_shadow_refresh(st.data_ptr(), _DTYPE_CODE[st.dtype], rows, dstate, shadow_format, codes.data_ptr(),

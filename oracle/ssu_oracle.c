@@ -218,6 +218,36 @@ uint8_t orc_e4m3_encode(double v)
     return sign | (uint8_t)(biased << 3) | frac;
 }
 
+/* FP4 E2M1: 1 sign, 2 exponent bits (bias 1), 1 fraction bit; exponent
+ * field 0 holds the subnormal 0.5; no infinities and no NaN, so the
+ * magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4 and 6 (codes 0-7, bit 3 the sign). */
+double orc_e2m1_decode(uint8_t code)
+{
+    const int e = (code >> 1) & 3, f = code & 1;
+    const double v = e == 0 ? 0.5 * f : ldexp(1.0 + 0.5 * f, e - 1);
+    return (code & 8) ? -v : v;
+}
+
+/* Round to nearest even onto the E2M1 grid, magnitudes past 6 clamped to 6
+ * ("saturate to finite"); NaN, which the format cannot hold, maps to +6. */
+uint8_t orc_e2m1_encode(double v)
+{
+    if (isnan(v))
+        return 7;
+    const uint8_t sign = signbit(v) ? 8 : 0;
+    double r = fabs(round_to_format(v, 1, 0, 2));
+    if (isinf(r) || r > 6.0)
+        r = 6.0;
+    for (uint8_t code = 0; code < 8; ++code)
+        if (orc_e2m1_decode(code) == r)
+            return sign | code;
+    return sign; /* not reached: every rounded magnitude is on the grid */
+}
+
+/* Floats of one row's NVFP4 scale record: the fp32 row scale, then the
+ * dstate / 16 E4M3 block scale codes, padded to a multiple of 16 bytes. */
+int64_t orc_nvfp4_scale_words(int64_t dstate) { return (4 + dstate / 16 + 15) / 16 * 4; }
+
 /* One state row into its read copy (format per orc_shadow_refresh).  The
  * E4M3 form maps the row's largest magnitude amax onto the largest finite
  * E4M3 value, 448: each value v is stored as the code of v * 448 / amax
@@ -230,6 +260,40 @@ static void shadow_row(const double *v, int64_t n, int32_t format, void *codes, 
     if (format == ORC_SHADOW_F16) {
         for (int64_t i = 0; i < n; ++i)
             ((uint16_t *)codes)[i] = double_to_half_bits(v[i]);
+        return;
+    }
+    if (format == ORC_SHADOW_NVFP4) {
+        /* Two scale levels, as NVFP4 defines them: the row's largest magnitude
+         * amax maps onto 6 * 448, the product of the largest E2M1 and E4M3
+         * values, through the fp32 row scale s = amax / (6 * 448); each block
+         * of 16 elements keeps the E4M3 code of (its largest magnitude) /
+         * (6 s), which maps the block's largest onto 6; an element is the E2M1
+         * code of v / (block scale * s), quotients in double, both roundings
+         * to nearest even.  An all-zero row keeps s = 1 and zero codes; a block
+         * whose scale rounds to zero keeps zero codes. */
+        double amax = 0.0;
+        for (int64_t i = 0; i < n; ++i)
+            if (fabs(v[i]) > amax)
+                amax = fabs(v[i]);
+        const float s = amax > 0.0 ? (float)round_to_format(amax / (6.0 * 448.0), 23, -126, 127) : 1.0f;
+        scale[0] = s;
+        uint8_t *bcodes = (uint8_t *)(scale + 1);
+        uint8_t *out = (uint8_t *)codes;
+        for (int64_t k = 0; k < n / 16; ++k) {
+            double bmax = 0.0;
+            for (int64_t i = 16 * k; i < 16 * k + 16; ++i)
+                if (fabs(v[i]) > bmax)
+                    bmax = fabs(v[i]);
+            bcodes[k] = orc_e4m3_encode(bmax / (6.0 * (double)s));
+            const double bs = orc_e4m3_decode(bcodes[k]);
+            for (int64_t i = 16 * k; i < 16 * k + 16; ++i) {
+                const uint8_t c = bs > 0.0 ? orc_e2m1_encode(v[i] / (bs * (double)s)) : 0;
+                if (i % 2 == 0)
+                    out[i / 2] = c;
+                else
+                    out[i / 2] |= (uint8_t)(c << 4);
+            }
+        }
         return;
     }
     double amax = 0.0;
@@ -245,24 +309,42 @@ static double shadow_value(const void *codes, const float *scale, int64_t row, i
 {
     if (format == ORC_SHADOW_F16)
         return half_bits_to_double(((const uint16_t *)codes)[row * n + i]);
+    if (format == ORC_SHADOW_NVFP4) {
+        const float *rec = scale + row * orc_nvfp4_scale_words(n);
+        const uint8_t byte = ((const uint8_t *)codes)[(row * n + i) / 2];
+        const uint8_t c = i % 2 == 0 ? (byte & 15) : (byte >> 4);
+        return orc_e2m1_decode(c) * orc_e4m3_decode(((const uint8_t *)(rec + 1))[i / 16]) * (double)rec[0];
+    }
     return orc_e4m3_decode(((const uint8_t *)codes)[row * n + i]) * (double)scale[row];
+}
+
+/* Byte offset of row `row`'s codes and float offset of its scales. */
+static size_t shadow_code_offset(int64_t row, int64_t n, int32_t format)
+{
+    return format == ORC_SHADOW_F16 ? (size_t)(row * n) * 2 : format == ORC_SHADOW_NVFP4 ? (size_t)(row * n) / 2 : (size_t)(row * n);
+}
+static int64_t shadow_scale_offset(int64_t row, int64_t n, int32_t format)
+{
+    return format == ORC_SHADOW_NVFP4 ? row * orc_nvfp4_scale_words(n) : row;
 }
 
 int orc_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate, int32_t format,
                        void *shadow, float *scale)
 {
-    if (format != ORC_SHADOW_F16 && format != ORC_SHADOW_E4M3)
+    if (format != ORC_SHADOW_F16 && format != ORC_SHADOW_E4M3 && format != ORC_SHADOW_NVFP4)
         return ORC_INVALID;
-    if (format == ORC_SHADOW_E4M3 && scale == NULL)
+    if (format != ORC_SHADOW_F16 && scale == NULL)
+        return ORC_INVALID;
+    if (format == ORC_SHADOW_NVFP4 && dstate % 16 != 0)
         return ORC_INVALID;
     double *v = malloc(sizeof(double) * (size_t)dstate);
     if (!v)
         return ORC_INVALID;
-    const size_t cb = format == ORC_SHADOW_F16 ? 2 : 1;
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t i = 0; i < dstate; ++i)
             v[i] = load_elem(state, r * dstate + i, state_dtype);
-        shadow_row(v, dstate, format, (char *)shadow + (size_t)(r * dstate) * cb, scale ? scale + r : NULL);
+        shadow_row(v, dstate, format, (char *)shadow + shadow_code_offset(r, dstate, format),
+                   scale ? scale + shadow_scale_offset(r, dstate, format) : NULL);
     }
     free(v);
     return ORC_OK;
@@ -521,8 +603,10 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
         return ORC_INVALID;
     }
     if (pr->shadow_format != ORC_SHADOW_NONE &&
-        ((pr->shadow_format != ORC_SHADOW_F16 && pr->shadow_format != ORC_SHADOW_E4M3) || pr->shadow == NULL ||
-         (pr->shadow_format == ORC_SHADOW_E4M3 && pr->shadow_scale == NULL))) {
+        ((pr->shadow_format != ORC_SHADOW_F16 && pr->shadow_format != ORC_SHADOW_E4M3 &&
+          pr->shadow_format != ORC_SHADOW_NVFP4) ||
+         pr->shadow == NULL || (pr->shadow_format != ORC_SHADOW_F16 && pr->shadow_scale == NULL) ||
+         (pr->shadow_format == ORC_SHADOW_NVFP4 && pr->dstate % 16 != 0))) {
         set_err(err, errlen, "bad read copy (format %lld, or its arrays missing)", pr->shadow_format, 0);
         return ORC_INVALID;
     }
@@ -606,8 +690,9 @@ int orc_replay_run(const orc_replay_problem *pr, char *err, int errlen)
                             for (int64_t n = 0; n < N; ++n)
                                 S[n] = load_elem(pr->ckpt_out, row * N + n, pr->state_dtype);
                             shadow_row(S, N, pr->shadow_format,
-                                       (char *)pr->shadow + (size_t)(row * N) * (pr->shadow_format == ORC_SHADOW_F16 ? 2 : 1),
-                                       pr->shadow_scale ? pr->shadow_scale + row : NULL);
+                                       (char *)pr->shadow + shadow_code_offset(row, N, pr->shadow_format),
+                                       pr->shadow_scale ? pr->shadow_scale + shadow_scale_offset(row, N, pr->shadow_format)
+                                                        : NULL);
                         }
                     }
                 } else {

@@ -75,7 +75,8 @@ typedef struct {
     int64_t *count_out;             /* [batch] entries buffered after the call                    */
     int32_t shadow_format;          /* ORC_SHADOW_*: the low-precision read copy, or none         */
     void *shadow;                   /* [slots, heads, dim, dstate] codes, in/out (NULL: none)     */
-    float *shadow_scale;            /* [slots, heads, dim] row scales (E4M3), in/out              */
+    float *shadow_scale;            /* [slots, heads, dim] row scales (E4M3) or scale records
+                                       (NVFP4), in/out                                             */
 } orc_replay_problem;
 
 /* Packed variable-length SSD prefill (MATE documentation, page "Mamba / SSU",
@@ -118,8 +119,17 @@ int orc_ssd_run(const orc_ssd_problem *problem, char *err, int errlen);
  *                    the row's largest magnitude, code = E4M3(v * 448 / amax)
  *                    with the quotient in double, rounded to nearest even;
  *                    scale = amax / 448 stored in fp32 (1, and zero codes,
- *                    for an all-zero row); value = E4M3 value * scale. */
-enum { ORC_SHADOW_NONE = 0, ORC_SHADOW_F16 = 1, ORC_SHADOW_E4M3 = 2 };
+ *                    for an all-zero row); value = E4M3 value * scale.
+ *   ORC_SHADOW_NVFP4 FP4 E2M1 codes (two a byte, the even element in the low
+ *                    nibble) with two scale levels: per row the fp32 scale
+ *                    s = amax / (6 * 448); per block of 16 elements the E4M3
+ *                    code of (block amax) / (6 s); code = E2M1(v / (block
+ *                    scale * s)), quotients in double, roundings to nearest
+ *                    even, saturating.  `scale` holds one record per row of
+ *                    orc_nvfp4_scale_words(dstate) floats: s, then the block
+ *                    scale codes as bytes.  value = E2M1 * block scale * s.
+ *                    dstate a multiple of 16. */
+enum { ORC_SHADOW_NONE = 0, ORC_SHADOW_F16 = 1, ORC_SHADOW_E4M3 = 2, ORC_SHADOW_NVFP4 = 3 };
 
 /* The read copy of `rows` state rows of `dstate` elements (`state` in
  * state_dtype); `scale` may be NULL for ORC_SHADOW_F16. */
@@ -127,6 +137,9 @@ int orc_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int
                        void *shadow, float *scale);
 uint8_t orc_e4m3_encode(double v);
 double orc_e4m3_decode(uint8_t code);
+uint8_t orc_e2m1_encode(double v);
+double orc_e2m1_decode(uint8_t code);
+int64_t orc_nvfp4_scale_words(int64_t dstate);
 
 int orc_replay_run(const orc_replay_problem *problem, char *err, int errlen);
 

@@ -820,6 +820,191 @@ def pin_shadow_refresh(lib):
         raise AssertionError("bf16 pool read copy")
 
 
+# E2M1 magnitudes by code (OCP Microscaling formats, FP4 E2M1: bias 1, one
+# fraction bit, exponent field 0 the subnormal 0.5), written out from the
+# format's definition.
+_E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _e2m1_nearest(q: torch.Tensor) -> torch.Tensor:
+    """E2M1 codes of float64 values `q` by brute force: the nearest of the
+    eight magnitudes to |q| (|q| past 6 takes 6), an exact tie to the even
+    code, the sign in bit 3."""
+    grid = torch.tensor(_E2M1_GRID, dtype=torch.float64)
+    a = q.abs().reshape(-1, 1).clamp(max=6.0)
+    d = (a - grid.view(1, -1)).abs()
+    cand = d == d.min(dim=1, keepdim=True).values
+    even = cand & (torch.arange(8) % 2 == 0).view(1, -1)
+    idx = torch.where(even.any(dim=1), even.to(torch.int64).argmax(dim=1), cand.to(torch.int64).argmax(dim=1))
+    sign = torch.signbit(q.reshape(-1)).to(torch.int64) * 8
+    return (idx | sign).to(torch.uint8).view(q.shape)
+
+
+def pin_e2m1_codes(lib):
+    """FP4 E2M1 as the NVFP4 read copy stores it: the sixteen codes decode to
+    the format's magnitudes with the sign in bit 3; random values, every
+    midpoint between neighbours (a tie: to the even code) and values past 6
+    (saturated) encode as the brute-force nearest grid value."""
+    for code in range(16):
+        want = _E2M1_GRID[code & 7] * (-1.0 if code & 8 else 1.0)
+        got = lib.orc_e2m1_decode(code)
+        if got != want or (code == 8 and not np.signbit(got)):
+            raise AssertionError(f"E2M1 code {code} decodes to {got}, not {want}")
+    g = torch.Generator().manual_seed(64)
+    mids = [(a + b) / 2 for a, b in zip(_E2M1_GRID, _E2M1_GRID[1:])]
+    vals = torch.cat([(torch.rand(3000, generator=g) - 0.5) * 16, torch.tensor(mids, dtype=torch.float32),
+                      -torch.tensor(mids, dtype=torch.float32), torch.tensor([6.5, 7.0, 1e9, -9.0, 0.0, -0.0])])
+    vals = vals.to(torch.float64)
+    want = _e2m1_nearest(vals)
+    got = torch.tensor([lib.orc_e2m1_encode(float(v)) for v in vals], dtype=torch.uint8)
+    if not torch.equal(got, want):
+        i = int(torch.nonzero(got != want)[0])
+        raise AssertionError(f"E2M1 of {float(vals[i])}: {int(got[i])}, nearest {int(want[i])}")
+    if [lib.orc_e2m1_encode(m) for m in mids] != [0, 2, 2, 4, 4, 6, 6]:
+        raise AssertionError("E2M1 ties")
+
+
+def _nvfp4_expected(st: torch.Tensor):
+    """The NVFP4 read copy of `st` built by brute force: s = amax / (6 * 448)
+    rounded to fp32 (1 for an all-zero row); per block of 16 the E4M3 code
+    nearest (block amax) / (6 s); per element the E2M1 code nearest
+    v / (block scale * s) (zero where the block scale is zero)."""
+    sd = st.to(torch.float64).reshape(-1, st.shape[-1])
+    rows, n = sd.shape
+    amax = sd.abs().amax(dim=1)
+    s = torch.where(amax > 0, amax / (6.0 * 448.0), torch.ones_like(amax)).to(torch.float32).to(torch.float64)
+    bmax = sd.abs().view(rows, n // 16, 16).amax(dim=2)
+    bcode = _e4m3_nearest(bmax / (6.0 * s[:, None]))
+    bsv = bcode.view(torch.float8_e4m3fn).to(torch.float64)
+    den = (bsv * s[:, None]).repeat_interleave(16, dim=1)
+    q = torch.where(den > 0, sd / torch.where(den > 0, den, 1.0), torch.zeros_like(sd))
+    codes = _e2m1_nearest(q)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).view(*st.shape[:-1], n // 2)
+    return packed, s.to(torch.float32).view(st.shape[:-1]), bcode.view(*st.shape[:-1], n // 16)
+
+
+def _nvfp4_dequant(codes: torch.Tensor, rec: torch.Tensor) -> torch.Tensor:
+    n = codes.shape[-1] * 2
+    grid = torch.tensor([_E2M1_GRID[c & 7] * (-1.0 if c & 8 else 1.0) for c in range(16)], dtype=torch.float64)
+    v = torch.stack([grid[(codes & 15).long()], grid[(codes >> 4).long()]], dim=-1).reshape(*codes.shape[:-1], n)
+    bsv = rec.view(torch.uint8)[..., 4:4 + n // 16].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    return v * bsv.repeat_interleave(16, dim=-1) * rec[..., :1].to(torch.float64)
+
+
+def _nvfp4_error_bound(st: torch.Tensor, rec: torch.Tensor) -> torch.Tensor:
+    """Per element, the most the NVFP4 copy may be off: half the largest E2M1
+    step (1) times block scale times s, or, where the block scale rounded
+    below (block amax) / (6 s) so that its largest values saturate at 6,
+    6 s times that shortfall."""
+    n = st.shape[-1]
+    sd = st.to(torch.float64)
+    s = rec[..., :1].to(torch.float64)
+    bs = rec.view(torch.uint8)[..., 4:4 + n // 16].contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+    bmax = sd.abs().view(*st.shape[:-1], n // 16, 16).amax(dim=-1)
+    per_block = s * torch.maximum(bs, 6.0 * (bmax / (6.0 * s) - bs).clamp(min=0.0))
+    return per_block.repeat_interleave(16, dim=-1)
+
+
+def pin_nvfp4_refresh(lib):
+    """The NVFP4 read copy of a pool, against a brute-force construction: the
+    row scale is amax / (6 * 448) in fp32, each block of 16 keeps the nearest
+    E4M3 code of its amax / (6 s), each element the nearest E2M1 code of
+    v / (block scale * s), two codes a byte (the even element low); an
+    all-zero row keeps scale 1 and zero codes; a row already on the grid
+    (codes times block scales times a power-of-two s) round-trips exactly;
+    every element lies within its block's largest half-step (block scale * s)
+    of its value, or within the shortfall of a block scale that rounded down;
+    a bf16 pool is copied as its stored values."""
+    g = torch.Generator().manual_seed(65)
+    st = torch.randn((3, 2, 4, 64), generator=g) * torch.rand((3, 2, 4, 1), generator=g) * 5
+    st[1, 0, 2] = 0.0
+    st[2, 1, 1, 16:32] = 1e-9 * torch.randn(16, generator=g)  # a block far below the row's largest
+    codes, rec = oracle.shadow_refresh(st, oracle.SHADOW_NVFP4, lib=lib)
+    if codes.shape != (3, 2, 4, 32) or rec.shape != (3, 2, 4, oracle.nvfp4_scale_words(64)):
+        raise AssertionError(f"NVFP4 shapes {tuple(codes.shape)} {tuple(rec.shape)}")
+    wc, ws, wb = _nvfp4_expected(st)
+    if not torch.equal(rec[..., 0], ws):
+        raise AssertionError("NVFP4 row scales")
+    if not torch.equal(rec.view(torch.uint8)[..., 4:8], wb):
+        raise AssertionError("NVFP4 block scales")
+    if not torch.equal(codes, wc):
+        raise AssertionError(f"NVFP4 codes: {int((codes != wc).sum())} bytes differ")
+    if float(rec[1, 0, 2, 0]) != 1.0 or int(codes[1, 0, 2].sum()) != 0:
+        raise AssertionError("NVFP4 zero row")
+    dq = _nvfp4_dequant(codes, rec)
+    if not torch.all((dq - st.to(torch.float64)).abs() <= _nvfp4_error_bound(st, rec) * (1 + 1e-12)):
+        raise AssertionError("NVFP4 element error above its block's bound")
+    # a row on the grid: E2M1 magnitudes times E4M3 block scales times s = 2^-7,
+    # each block holding one 6 so that its amax / (6 s) is its scale
+    grid_row = torch.tensor([_E2M1_GRID[(3 * i) % 8] * (-1.0 if i % 5 == 0 else 1.0) for i in range(64)])
+    grid_row[0::16] = 6.0
+    bscale = torch.tensor([448.0, 1.0, 0.25, 20.0]).repeat_interleave(16)
+    exact = (grid_row * bscale * 2.0 ** -7).view(1, 64)
+    c1, r1 = oracle.shadow_refresh(exact, oracle.SHADOW_NVFP4, lib=lib)
+    if not torch.equal(_nvfp4_dequant(c1, r1), exact.to(torch.float64)):
+        raise AssertionError("a row on the NVFP4 grid must round-trip")
+    bf = st.to(torch.bfloat16)
+    c16, s16 = oracle.shadow_refresh(bf, oracle.SHADOW_NVFP4, lib=lib)
+    c32, s32 = oracle.shadow_refresh(bf.float(), oracle.SHADOW_NVFP4, lib=lib)
+    if not (torch.equal(c16, c32) and torch.equal(s16, s32)):
+        raise AssertionError("bf16 pool NVFP4 read copy")
+
+
+def pin_replay_nvfp4_read_copy(lib):
+    """Steps that do not fold read the NVFP4 copy: a checkpoint on the copy's
+    grid gives exactly the checkpoint's y; a general one moves y by no more
+    than the copy's rounding (per element the bound of pin_nvfp4_refresh) and
+    does move it; a fold rewrites the copy from the new checkpoint, other
+    steps leave it."""
+    L = 4
+    counts = [0, 1, 2, 3, 3, 2]
+    sc = _replay_scenario(46, L, counts, dstate=32, state_dtype=torch.float32)
+    ck = sc["ckpt"]
+    codes, rec = oracle.shadow_refresh(ck, oracle.SHADOW_NVFP4, lib=lib)
+    # a checkpoint on the NVFP4 grid: each block's first element +6, the row
+    # scale a power of two (the block holding the row's largest keeps the
+    # scale 448), so that the values are exact in fp32 and their copy is the
+    # same codes and scales
+    cg = codes.clone()
+    cg[..., 0::8] = (cg[..., 0::8] & 0xF0) | 7
+    rg = rec.clone()
+    rg[..., 0] = torch.exp2(torch.round(torch.log2(rec[..., 0])))
+    grid = _nvfp4_dequant(cg, rg).to(torch.float32)
+    c2, r2 = oracle.shadow_refresh(grid, oracle.SHADOW_NVFP4, lib=lib)
+    if not (torch.equal(c2, cg) and torch.equal(r2.view(torch.int32), rg.view(torch.int32))):
+        raise AssertionError("the NVFP4 copy of values on its grid must be those codes and scales")
+    sg = dict(sc, ckpt=grid)
+    plain = _run_replay(sg, lib)
+    r = _run_replay(sg, lib, shadow=cg, shadow_scale=rg, shadow_format=oracle.SHADOW_NVFP4)
+    if not torch.equal(r.y_exact, plain.y_exact):
+        raise AssertionError("an exact NVFP4 read copy must give the checkpoint's y")
+    plain = _run_replay(sc, lib)
+    r = _run_replay(sc, lib, shadow=codes, shadow_scale=rec, shadow_format=oracle.SHADOW_NVFP4)
+    half = _nvfp4_error_bound(ck, rec)
+    moved = False
+    for b, c in enumerate(counts):
+        s = int(sc["slot_of"][b])
+        if c + 1 == L:
+            cs, ss = oracle.shadow_refresh(r.ckpt[s], oracle.SHADOW_NVFP4, lib=lib)
+            if not (torch.equal(r.shadow[s], cs) and torch.equal(r.shadow_scale[s], ss)):
+                raise AssertionError("a fold must rewrite the NVFP4 copy from the new checkpoint")
+            continue
+        if not (torch.equal(r.shadow[s], codes[s]) and torch.equal(r.shadow_scale[s], rec[s])):
+            raise AssertionError("a step that does not fold must not write the NVFP4 copy")
+        Cb = sc["C"][b].double()
+        hpg = ck.shape[1] // Cb.shape[0]
+        dy = (plain.y_exact[b] - r.y_exact[b]).abs()
+        for h in range(ck.shape[1]):
+            err = half[s, h] @ Cb[h // hpg].abs()
+            zz = sc["z"][b, h].double()
+            gate = (zz / (1 + torch.exp(-zz))).abs()
+            if not torch.all(dy[h] <= gate * err * (1 + 1e-9) + 1e-12):
+                raise AssertionError("NVFP4 read-copy error above its bound")
+        moved |= float(dy.max()) > 0
+    if not moved:
+        raise AssertionError("the readout did not use the NVFP4 copy")
+
+
 def _e4m3_dequant(codes, scale):
     return codes.view(torch.float8_e4m3fn).to(torch.float64) * scale.to(torch.float64)[..., None]
 
@@ -1173,6 +1358,7 @@ ALL_PINS = [pin_conversions, pin_scalar_functions, pin_hand_worked, pin_dt_zero,
             pin_seed_position, pin_seed_position_per_row, pin_per_head_dt, pin_aliasing_refused,
             pin_replay_lossless, pin_replay_buffer_entries, pin_replay_buffer_len_one,
             pin_replay_pad_and_aliasing, pin_empty_sequences, pin_bounded_decay, pin_e4m3_codes,
-            pin_shadow_refresh, pin_replay_read_copy, pin_ssd_equals_token_loop, pin_ssd_chunked_form,
+            pin_shadow_refresh, pin_replay_read_copy, pin_e2m1_codes, pin_nvfp4_refresh,
+            pin_replay_nvfp4_read_copy, pin_ssd_equals_token_loop, pin_ssd_chunked_form,
             pin_ssd_seq_idx_authority, pin_ssd_dt_limit, pin_verify_lossless, pin_verify_entries,
             pin_verify_rollback, pin_verify_pad]

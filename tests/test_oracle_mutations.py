@@ -61,6 +61,20 @@ MUTATIONS = [
      "if (0) {\n                            /* the read copy"),
     ("e4m3_no_saturation", "if (isinf(r) || r > 448.0)\n        r = 448.0;", ""),
     ("e4m3_exponent_bias", "ldexp((double)(f + 8), e - 10)", "ldexp((double)(f + 8), e - 11)"),
+    # the NVFP4 read copy
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * f, e - 1)", "ldexp(1.0 + 0.5 * f, e - 2)"),
+    ("e2m1_no_saturation", "if (isinf(r) || r > 6.0)\n        r = 6.0;", ""),
+    ("e2m1_ties_away", "double r = fabs(round_to_format(v, 1, 0, 2));",
+     "double r = fabs(round_to_format(v * (1.0 + 1e-12), 1, 0, 2));"),
+    ("nvfp4_row_scale_448", "round_to_format(amax / (6.0 * 448.0), 23", "round_to_format(amax / 448.0, 23"),
+    ("nvfp4_block_scale_undivided", "orc_e4m3_encode(bmax / (6.0 * (double)s))", "orc_e4m3_encode(bmax / (double)s)"),
+    ("nvfp4_blocks_of_32", "for (int64_t k = 0; k < n / 16; ++k) {", "for (int64_t k = 0; k < n / 32; ++k) {"),
+    ("nvfp4_nibble_order", "                if (i % 2 == 0)\n                    out[i / 2] = c;",
+     "                if (i % 2 == 1)\n                    out[i / 2] = c;"),
+    ("nvfp4_signed_block_max", "if (fabs(v[i]) > bmax)\n                    bmax = fabs(v[i]);",
+     "if (v[i] > bmax)\n                    bmax = v[i];"),
+    ("nvfp4_read_ignores_block_scale", "return orc_e2m1_decode(c) * orc_e4m3_decode(((const uint8_t *)(rec + 1))[i / 16]) * (double)rec[0];",
+     "return orc_e2m1_decode(c) * 448.0 * (double)rec[0];"),
     # SSD prefill
     ("ssd_seq_idx_ignored", "if (c == 0 || pr->seq_idx[c] != pr->seq_idx[c - 1]) {", "if (c == 0) {"),
     ("ssd_dt_limit_dropped", "d = fmin(fmax(d, pr->dt_lo), pr->dt_hi);", "d = d;"),
