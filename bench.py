@@ -65,6 +65,9 @@ DESCRIPTIONS = {
                         "sequence b starting with b % 16 buffered entries (1/16 of the sequences fold per step)",
     "replay_e4m3_b256_fp32": "replay_b256_fp32 with an E4M3 read copy of the checkpoints (one fp32 scale per "
                              "state row): steps that do not fold read the copy, folds rewrite it",
+    "replay_nvfp4_b256_fp32": "replay_b256_fp32 with an NVFP4 read copy of the checkpoints (E2M1 codes, an E4M3 "
+                              "scale per 16 elements, an fp32 scale per state row): steps that do not fold read "
+                              "the copy, folds rewrite it",
     "replay_f16copy_b256_fp32": "replay_b256_fp32 with an fp16 read copy of the checkpoints: steps that do not "
                                 "fold read the copy, folds rewrite it",
     "copy_slots_b256_fp32": "256 whole-slot state copies of 4 MiB (heads 128, dim 64, dstate 128, fp32) between "
@@ -126,8 +129,8 @@ def replay_bytes(w) -> dict:
     sb = H * P * N * w.state.element_size()
     # a read copy: what a step that does not fold reads instead of the
     # checkpoint, and what a fold writes besides it
-    cb = sb if w.shadow is None else (H * P * N * w.shadow.element_size()
-                                      + (0 if w.shadow_scale is None else H * P * 4))
+    cb = sb if w.shadow is None else (w.shadow[0].numel() * w.shadow.element_size()
+                                      + (0 if w.shadow_scale is None else w.shadow_scale[0].numel() * 4))
     io = w.x.element_size()
     entry = H * P * (io + 4) + G * N * io
     L = w.xbuf.shape[1]
@@ -977,13 +980,20 @@ def _sample_problem(w, seqs):
                       Bbuf=w.Bbuf[order], count=w.count[seqs], meta=dict(w.meta))
         if w.shadow is not None:
             import oracle
-            fmt = oracle.SHADOW_F16 if w.shadow.dtype == torch.float16 else oracle.SHADOW_E4M3
-            sub.shadow, sub.shadow_scale = oracle.shadow_refresh(sub.state, fmt)
+            sub.shadow, sub.shadow_scale = oracle.shadow_refresh(sub.state, _oracle_shadow_format(w))
         return sub
     return replace(w, state=w.state[order], x=sel(w.x), dt=sel(w.dt), B=sel(w.B), C=sel(w.C), z=sel(w.z),
                    read=remap(rd), dst=remap(wr), pad_slot_id=new_pad,
                    cu_seqlens=sub_cu if w.kind == "packed" else None,
                    num_accepted=None if w.num_accepted is None else w.num_accepted[seqs], dense_steps=0)
+
+
+def _oracle_shadow_format(w):
+    import oracle
+    if w.shadow is None:
+        return oracle.SHADOW_NONE
+    return {"f16": oracle.SHADOW_F16, "e4m3": oracle.SHADOW_E4M3,
+            "nvfp4": oracle.SHADOW_NVFP4}[w.meta["shadow_format"]]
 
 
 def _oracle_call(sub):
@@ -992,9 +1002,7 @@ def _oracle_call(sub):
         return oracle.replay(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, sub.xbuf, sub.dtbuf, sub.Bbuf, sub.count,
                              D=sub.D, z=sub.z, dt_bias=sub.dt_bias, dt_softplus=sub.dt_softplus,
                              slot_of=sub.read, pad_slot_id=sub.pad_slot_id, shadow=sub.shadow,
-                             shadow_scale=sub.shadow_scale,
-                             shadow_format=oracle.SHADOW_NONE if sub.shadow is None else
-                             (oracle.SHADOW_F16 if sub.shadow.dtype == torch.float16 else oracle.SHADOW_E4M3))
+                             shadow_scale=sub.shadow_scale, shadow_format=_oracle_shadow_format(sub))
     mode = oracle.SLOTS_PER_ROW if sub.slot_mode == workloads.SLOTS_PER_ROW else oracle.SLOTS_STRIDED
     return oracle.ssu(sub.state, sub.x, sub.dt, sub.A, sub.B, sub.C, D=sub.D, z=sub.z, dt_bias=sub.dt_bias,
                       dt_softplus=sub.dt_softplus, read=oracle.Table.of(sub.read, mode),
@@ -1004,7 +1012,7 @@ def _oracle_call(sub):
 
 
 SEEDS = {"tiny_onetoken": 1001, "b256_fp32": 1002, "b1024_bf16": 1003, "mtp_64x7_fp32": 1004,
-         "varlen_fp16": 1005, "varlen_fp16_disable": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008,
+         "varlen_fp16": 1005, "varlen_fp16_disable": 1005, "replay_b256_fp32": 1006, "copy_slots_b256_fp32": 1007, "replay_e4m3_b256_fp32": 1008, "replay_nvfp4_b256_fp32": 1012,
          "replay_f16copy_b256_fp32": 1009, "ssd_prefill_16k_bf16": 1010, "verify_b256_t4_fp32": 1011}
 
 
@@ -1013,6 +1021,7 @@ def make_workload(workload, batch, device, seed_offset=0):
     kw = {}
     if batch is not None:
         if workload not in ("b256_fp32", "mtp_64x7_fp32", "replay_b256_fp32", "replay_e4m3_b256_fp32",
+                            "replay_nvfp4_b256_fp32",
                             "replay_f16copy_b256_fp32", "copy_slots_b256_fp32", "ssd_prefill_16k_bf16",
                             "verify_b256_t4_fp32"):
             raise SystemExit(f"--batch does not apply to the {workload} workload")

@@ -209,12 +209,15 @@ typedef struct ssu_replay_buffers {
      * "ReplaySSM", section 低精度读写分离): steps that do not fold read it
      * instead of the checkpoint, a fold rewrites it from the new checkpoint
      * (as ssu_shadow_refresh would).  It never feeds the recurrence. */
-    int32_t shadow_format;     /* SSU_SHADOW_NONE, _F16 or _E4M3                          */
+    int32_t shadow_format;     /* SSU_SHADOW_NONE, _F16, _E4M3 or _NVFP4                  */
     int32_t reserved0;         /* must be 0                                               */
     void *shadow;              /* device [slots, heads, dim, dstate]: fp16 values or E4M3
-                                  codes (one byte), 16-byte aligned                       */
-    float *shadow_scale;       /* device [slots, heads, dim] fp32 row scales (E4M3 only),
-                                  16-byte aligned                                         */
+                                  codes (one byte); NVFP4: [slots, heads, dim, dstate / 2]
+                                  bytes of two E2M1 codes; 16-byte aligned                */
+    float *shadow_scale;       /* device, 16-byte aligned: E4M3 [slots, heads, dim] fp32
+                                  row scales; NVFP4 [slots, heads, dim,
+                                  SSU_NVFP4_SCALE_WORDS(dstate)] scale records; unused
+                                  for F16                                                 */
 } ssu_replay_buffers;
 
 /* Formats of the read copy.  E4M3 is OCP FP8 E4M3 (bias 7, 3 fraction bits,
@@ -229,6 +232,21 @@ typedef struct ssu_replay_buffers {
 #define SSU_SHADOW_NONE 0
 #define SSU_SHADOW_F16  1
 #define SSU_SHADOW_E4M3 2
+/* NVFP4 (the article's headline format for the copy): FP4 E2M1 codes (sign,
+ * 2 exponent bits with bias 1, 1 fraction bit: magnitudes 0, 0.5, 1, 1.5,
+ * 2, 3, 4, 6), two a byte with the even element in the low nibble, scaled on
+ * two levels: per block of 16 elements an E4M3 code of (block amax) / (6 s),
+ * and per state row an fp32 s = amax / (6 * 448) (1, with zero codes, for an
+ * all-zero row); element code = E2M1(v / (block scale * s)), the quotients in
+ * fp32, roundings to nearest even, saturating.  The value read is
+ * E2M1(code) * E4M3(block code) * s.  Each row's record in shadow_scale holds
+ * s, then the dstate / 16 block codes as bytes, padded to a multiple of 16
+ * bytes (SSU_NVFP4_SCALE_WORDS floats).  A code or block code can sit one step
+ * from the exactly rounded one where its quotient lies within about 2^-21
+ * (relative) of a midpoint.  Replay steps take it at dstate 64, 128 and 256;
+ * ssu_shadow_refresh at any multiple of 32. */
+#define SSU_SHADOW_NVFP4 3
+#define SSU_NVFP4_SCALE_WORDS(dstate) ((4 + (dstate) / 16 + 15) / 16 * 4)
 
 /*
  * One decode token per sequence on the checkpoint + buffer form of the state
@@ -414,9 +432,12 @@ ssu_status ssu_batch_copy(const ssu_copy *copies, int64_t n, uint64_t max_bytes,
 /*
  * The read copy (see ssu_replay_buffers) of `rows` consecutive state rows of
  * `dstate` elements: state rows r in [0, rows) of `state` (state_dtype) into
- * `shadow` rows (format SSU_SHADOW_F16 or SSU_SHADOW_E4M3) and, for E4M3,
- * `scale[r]`.  Use it to build the copy of checkpoints written by other
- * means (a prefill, a copy).  rows == 0 launches nothing.
+ * `shadow` rows (format SSU_SHADOW_F16, SSU_SHADOW_E4M3 or SSU_SHADOW_NVFP4)
+ * and, for E4M3, `scale[r]`, for NVFP4 the record of SSU_NVFP4_SCALE_WORDS
+ * floats at scale + r * SSU_NVFP4_SCALE_WORDS(dstate) (dstate a multiple of
+ * 32; the record's padding is left as it is).  Use it to build the copy of
+ * checkpoints written by other means (a prefill, a copy).  rows == 0 launches
+ * nothing.
  */
 ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate,
                               int32_t format, void *shadow, float *scale, void *stream);

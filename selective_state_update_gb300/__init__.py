@@ -104,17 +104,44 @@ class SsdArgs(ctypes.Structure):
 
 
 # formats of the read copy (SSU_SHADOW_*)
-SHADOW_NONE, SHADOW_F16, SHADOW_E4M3 = 0, 1, 2
+SHADOW_NONE, SHADOW_F16, SHADOW_E4M3, SHADOW_NVFP4 = 0, 1, 2, 3
 
 
-def _shadow_format(shadow: Optional[torch.Tensor]) -> int:
+def nvfp4_scale_words(dstate: int) -> int:
+    """Floats of one row's NVFP4 scale record (SSU_NVFP4_SCALE_WORDS): the
+    fp32 row scale, then the dstate / 16 E4M3 block codes as bytes, padded to
+    a multiple of 16 bytes."""
+    return (4 + dstate // 16 + 15) // 16 * 4
+
+
+def _shadow_format(shadow: Optional[torch.Tensor], state: torch.Tensor) -> int:
+    """The read copy's format from its tensor: float16 values (F16); one uint8
+    / float8_e4m3fn code per state element (E4M3); uint8 bytes of two E2M1
+    codes, or float4_e2m1fn_x2, with half the state's last dimension (NVFP4)."""
     if shadow is None:
         return SHADOW_NONE
     if shadow.dtype == torch.float16:
         return SHADOW_F16
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    half = tuple(shadow.shape) == (*state.shape[:-1], state.shape[-1] // 2)
+    if (shadow.dtype == torch.uint8 and half) or (fp4 is not None and shadow.dtype == fp4):
+        return SHADOW_NVFP4
     if shadow.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
         return SHADOW_E4M3
-    raise ValueError("a read copy is float16 (fp16 values) or uint8 / float8_e4m3fn (E4M3 codes)")
+    raise ValueError("a read copy is float16 (fp16 values), uint8 / float8_e4m3fn (E4M3 codes) or uint8 / "
+                     "float4_e2m1fn_x2 with half the last dimension (NVFP4 code pairs)")
+
+
+def _check_copy_scales(fmt: int, shadow_scale: Optional[torch.Tensor], state: torch.Tensor) -> None:
+    if fmt == SHADOW_E4M3:
+        _need(shadow_scale is not None and shadow_scale.dtype == torch.float32 and shadow_scale.is_cuda
+              and shadow_scale.is_contiguous() and tuple(shadow_scale.shape) == tuple(state.shape[:-1]),
+              "an E4M3 read copy needs contiguous fp32 row scales shaped like the state without dstate")
+    elif fmt == SHADOW_NVFP4:
+        want = (*state.shape[:-1], nvfp4_scale_words(state.shape[-1]))
+        _need(shadow_scale is not None and shadow_scale.dtype == torch.float32 and shadow_scale.is_cuda
+              and shadow_scale.is_contiguous() and tuple(shadow_scale.shape) == want,
+              f"an NVFP4 read copy needs contiguous fp32 scale records of shape {want}")
 
 
 _lib = None
@@ -408,17 +435,15 @@ def ssu_replay_update(state, x, dt, A, B, C, x_buf, dt_buf, B_buf, count_in, cou
     _need(all(t.is_cuda for t in (x_buf, dt_buf, B_buf)), "buffers must be CUDA tensors")
     a = _args(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, pad_slot_id, out, False, status, 0)
     rt = _table(state_batch_indices, SLOTS_STRIDED)
-    fmt = _shadow_format(shadow)
+    fmt = _shadow_format(shadow, state)
     if fmt != SHADOW_NONE:
-        _need(shadow.is_cuda and shadow.is_contiguous() and tuple(shadow.shape) == tuple(state.shape),
+        shape = (*state.shape[:-1], state.shape[-1] // 2) if fmt == SHADOW_NVFP4 else tuple(state.shape)
+        _need(shadow.is_cuda and shadow.is_contiguous() and tuple(shadow.shape) == shape,
               "the read copy must be a contiguous CUDA tensor shaped like the checkpoints")
-        if fmt == SHADOW_E4M3:
-            _need(shadow_scale is not None and shadow_scale.dtype == torch.float32 and shadow_scale.is_cuda
-                  and shadow_scale.is_contiguous() and tuple(shadow_scale.shape) == tuple(state.shape[:-1]),
-                  "an E4M3 read copy needs contiguous fp32 row scales [slots, heads, dim]")
+        _check_copy_scales(fmt, shadow_scale, state)
     rb = ReplayBuffers(L, x_buf.data_ptr(), dt_buf.data_ptr(), B_buf.data_ptr(), count_in.data_ptr(),
                        count_out.data_ptr(), fmt, 0, _ptr(shadow),
-                       _ptr(shadow_scale) if fmt == SHADOW_E4M3 else None)
+                       _ptr(shadow_scale) if fmt in (SHADOW_E4M3, SHADOW_NVFP4) else None)
     rc = lib().ssu_replay_update(ctypes.byref(a), batch, None if rt is None else ctypes.byref(rt),
                                  ctypes.byref(rb), _stream(stream))
     if rc != OK:
@@ -616,18 +641,19 @@ def ssd_combined_fwd_varlen(x, dt, A, B, C, chunk_size, cu_seqlens, cu_chunk_seq
 def ssu_shadow_refresh(state: torch.Tensor, shadow: torch.Tensor, shadow_scale: Optional[torch.Tensor] = None,
                        stream=None) -> None:
     """The low-precision read copy of a contiguous state tensor ``[..., dstate]``
-    into ``shadow`` (float16, or uint8 / float8_e4m3fn E4M3 codes with fp32
-    ``shadow_scale`` of shape ``state.shape[:-1]``)."""
-    fmt = _shadow_format(shadow)
+    into ``shadow``: float16 values; uint8 / float8_e4m3fn E4M3 codes with fp32
+    ``shadow_scale`` of shape ``state.shape[:-1]``; or NVFP4 -- uint8 code
+    pairs of shape ``[..., dstate / 2]`` with fp32 scale records of shape
+    ``[..., nvfp4_scale_words(dstate)]``."""
+    fmt = _shadow_format(shadow, state)
     _need(fmt != SHADOW_NONE, "shadow must be given")
+    shape = (*state.shape[:-1], state.shape[-1] // 2) if fmt == SHADOW_NVFP4 else tuple(state.shape)
     _need(state.is_cuda and state.is_contiguous() and shadow.is_cuda and shadow.is_contiguous()
-          and shadow.shape == state.shape, "state and shadow must be contiguous CUDA tensors of one shape")
-    if fmt == SHADOW_E4M3:
-        _need(shadow_scale is not None and shadow_scale.dtype == torch.float32 and shadow_scale.is_contiguous()
-              and tuple(shadow_scale.shape) == tuple(state.shape[:-1]), "E4M3 needs fp32 row scales")
+          and tuple(shadow.shape) == shape, "state and shadow must be contiguous CUDA tensors of matching shapes")
+    _check_copy_scales(fmt, shadow_scale, state)
     dstate = state.shape[-1]
     rc = lib().ssu_shadow_refresh(state.data_ptr(), _DTYPE[state.dtype], state.numel() // dstate, dstate, fmt,
-                                  shadow.data_ptr(), _ptr(shadow_scale) if fmt == SHADOW_E4M3 else None,
+                                  shadow.data_ptr(), _ptr(shadow_scale) if fmt != SHADOW_F16 else None,
                                   _stream(stream))
     if rc != OK:
         _raise(rc)

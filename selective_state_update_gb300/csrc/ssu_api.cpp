@@ -303,7 +303,8 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
     if (rb->reserved0 != 0) return fail(SSU_ERR_INVALID, "replay buffers: reserved0 must be 0");
     kp.shadow_fmt = rb->shadow_format;
     if (rb->shadow_format != SSU_SHADOW_NONE) {
-        if (rb->shadow_format != SSU_SHADOW_F16 && rb->shadow_format != SSU_SHADOW_E4M3)
+        if (rb->shadow_format != SSU_SHADOW_F16 && rb->shadow_format != SSU_SHADOW_E4M3 &&
+            rb->shadow_format != SSU_SHADOW_NVFP4)
             return fail(SSU_ERR_INVALID, "shadow_format %d is not an SSU_SHADOW_* value", rb->shadow_format);
         if (rb->shadow == nullptr || reinterpret_cast<uintptr_t>(rb->shadow) % 16 != 0)
             return fail(SSU_ERR_INVALID, "the read copy must be a 16-byte aligned device pointer");
@@ -312,6 +313,12 @@ ssu_status ssu_replay_update(const ssu_args *args, int64_t batch, const ssu_slot
                 return fail(SSU_ERR_INVALID, "E4M3 row scales must be a 16-byte aligned device pointer");
             if (args->dim % 4 != 0)
                 return fail(SSU_ERR_UNSUPPORTED, "an E4M3 read copy needs dim to be a multiple of 4");
+        }
+        if (rb->shadow_format == SSU_SHADOW_NVFP4) {
+            if (rb->shadow_scale == nullptr || reinterpret_cast<uintptr_t>(rb->shadow_scale) % 16 != 0)
+                return fail(SSU_ERR_INVALID, "NVFP4 scale records must be a 16-byte aligned device pointer");
+            if (args->dstate != 64 && args->dstate != 128 && args->dstate != 256)
+                return fail(SSU_ERR_UNSUPPORTED, "an NVFP4 read copy needs dstate 64, 128 or 256");
         }
         kp.shadow = rb->shadow;
         kp.shadow_scale = rb->shadow_scale;
@@ -484,12 +491,14 @@ ssu_status ssu_ssd_prefill_static(const ssu_ssd_args *args, void *stream) {
 ssu_status ssu_shadow_refresh(const void *state, int32_t state_dtype, int64_t rows, int64_t dstate,
                               int32_t format, void *shadow, float *scale, void *stream) {
     if (!valid_dtype(state_dtype)) return fail(SSU_ERR_INVALID, "state_dtype %d is not an ssu_dtype", state_dtype);
-    if (format != SSU_SHADOW_F16 && format != SSU_SHADOW_E4M3)
-        return fail(SSU_ERR_INVALID, "format %d is not SSU_SHADOW_F16 or SSU_SHADOW_E4M3", format);
+    if (format != SSU_SHADOW_F16 && format != SSU_SHADOW_E4M3 && format != SSU_SHADOW_NVFP4)
+        return fail(SSU_ERR_INVALID, "format %d is not SSU_SHADOW_F16, SSU_SHADOW_E4M3 or SSU_SHADOW_NVFP4", format);
     if (rows < 0 || dstate <= 0 || dstate > 4096) return fail(SSU_ERR_INVALID, "rows must be >= 0, dstate in [1, 4096]");
+    if (format == SSU_SHADOW_NVFP4 && dstate % 32 != 0)
+        return fail(SSU_ERR_UNSUPPORTED, "an NVFP4 read copy needs dstate to be a multiple of 32");
     if (rows == 0) return ok();
-    if (!state || !shadow || (format == SSU_SHADOW_E4M3 && !scale))
-        return fail(SSU_ERR_INVALID, "state, shadow (and scale for E4M3) must not be NULL");
+    if (!state || !shadow || (format != SSU_SHADOW_F16 && !scale))
+        return fail(SSU_ERR_INVALID, "state, shadow (and scale for E4M3 and NVFP4) must not be NULL");
     return launched(ssu::launch_shadow_refresh(state, state_dtype, rows, static_cast<int>(dstate), format, shadow,
                                                scale, static_cast<cudaStream_t>(stream)));
 }

@@ -15,6 +15,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -53,6 +54,30 @@ __device__ __forceinline__ float shadow_factor_of(float amax) {
 }
 __device__ __forceinline__ unsigned char e4m3_code(float v) {
     return static_cast<unsigned char>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float e4m3_value(unsigned int code) {
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code & 0xffu), __NV_E4M3)));
+}
+
+// NVFP4 form of the read copy: FP4 E2M1 codes, two a byte (the even element
+// in the low nibble); per block of 16 elements an E4M3 scale code; per row an
+// fp32 scale s = amax / (6 * 448), the row's record holding s and then the
+// block codes, padded to a multiple of 16 bytes.  The block code is
+// E4M3((block amax) / (6 s)) and an element's code E2M1(v / (block scale *
+// s)), the quotients in fp32, both roundings to nearest even and saturating.
+__host__ __device__ constexpr int nvfp4_scale_words(int n) { return (4 + n / 16 + 15) / 16 * 4; }
+__device__ __forceinline__ float nvfp4_row_scale(float amax) { return amax > 0.f ? __fdiv_rn(amax, 2688.f) : 1.f; }
+__device__ __forceinline__ unsigned int nvfp4_block_code(float bmax, float s) {
+    return e4m3_code(__fdiv_rn(bmax, __fmul_rn(6.f, s)));
+}
+// The byte of two E2M1 codes of a and b (a in the low nibble).
+__device__ __forceinline__ unsigned int e2m1x2_code(float a, float b) {
+    return __nv_cvt_float2_to_fp4x2(make_float2(a, b), __NV_E2M1, cudaRoundNearest);
+}
+// The two values of a byte of E2M1 codes (the low nibble first).
+__device__ __forceinline__ float2 e2m1x2_values(unsigned int byte) {
+    __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte & 0xffu), __NV_E2M1);
+    return __half22float2(__half2(h));
 }
 // Two values from two codes (the low byte first), one conversion.
 __device__ __forceinline__ float2 e4m3x2_values(unsigned int codes) {

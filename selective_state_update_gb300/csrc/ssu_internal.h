@@ -75,7 +75,7 @@ enum : int32_t { kBulkBC = 1, kBulkXZ = 2, kBulkDT = 4 };
 // SM clock cycles a bounded wait allows by default (about a second).
 constexpr int64_t kDefaultWaitCycles = 2000000000LL;
 
-enum : int32_t { kShadowNone = 0, kShadowF16 = 1, kShadowE4M3 = 2 };
+enum : int32_t { kShadowNone = 0, kShadowF16 = 1, kShadowE4M3 = 2, kShadowNVFP4 = 3 };
 
 // Launchers (one translation unit per kernel).  `lanes` = dstate / 16.
 cudaError_t launch_onetoken(int state_dtype, int lanes, const KParams &p, int64_t batch,

@@ -68,6 +68,10 @@ struct ReplayPipe {
     // largest copy tile (one byte per element), inside the checkpoint tile.
     static constexpr int kShadowScaleOffset = kTileRows * kN;
     static_assert(kShadowScaleOffset + kTileRows * 4 <= kTileBytes, "read-copy scales do not fit the tile");
+    // Where the NVFP4 scale records sit: after the largest tile of code pairs.
+    static constexpr int kNvfp4RecOffset = kTileRows * kN / 2;
+    static_assert(kNvfp4RecOffset + kTileRows * nvfp4_scale_words(kN) * 4 <= kTileBytes,
+                  "NVFP4 scale records do not fit the tile");
     // Register budget: two CTAs per SM where a tile and a few KB of entries
     // fit twice in half of an SM's shared memory (228 KB on this part, less a
     // margin) and two CTAs still leave 128 registers a thread.  The ring
@@ -312,8 +316,9 @@ __device__ __forceinline__ void entry_terms(int c, int rows, float Ah, const flo
 }
 
 // This thread's 16 values of row rr of a read copy staged in shared memory
-// (E4M3 codes times nothing -- the caller applies the row scale -- or fp16),
-// in the element layout of Tile::gather.
+// (E4M3 codes times nothing, or E2M1 codes times their block scale -- the
+// caller applies the row scale -- or fp16), in the element layout of
+// Tile::gather.
 template <typename TS, int L>
 __device__ __forceinline__ void load_copy_row(const unsigned char *tile, int rr, int lane, int fmt, float *v) {
     using T = Tile<TS, L>;
@@ -322,7 +327,21 @@ __device__ __forceinline__ void load_copy_row(const unsigned char *tile, int rr,
 #pragma unroll
     for (int k = 0; k < T::kChunks; ++k) {
         const int e0 = (lane + L * k) * V;
-        if (fmt == kShadowE4M3) {
+        if (fmt == kShadowNVFP4) {
+            const unsigned char *rec = tile + kTileRows * N / 2 + rr * nvfp4_scale_words(N) * 4;
+            const float bs = e4m3_value(rec[4 + e0 / 16]);
+            uint32_t w;
+            if constexpr (V == 8)
+                w = *reinterpret_cast<const uint32_t *>(tile + rr * (N / 2) + e0 / 2);
+            else
+                w = *reinterpret_cast<const unsigned short *>(tile + rr * (N / 2) + e0 / 2);
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                const float2 f = e2m1x2_values(w >> (8 * i));
+                v[k * V + 2 * i] = f.x * bs;
+                v[k * V + 2 * i + 1] = f.y * bs;
+            }
+        } else if (fmt == kShadowE4M3) {
             uint32_t w[V / 4];
             if constexpr (V == 8) {
                 const uint2 u = *reinterpret_cast<const uint2 *>(tile + rr * N + e0);
@@ -357,8 +376,9 @@ __device__ __forceinline__ void load_copy_row(const unsigned char *tile, int rr,
 
 // Writes the read copy of one folded state row (this thread's 16 values `sv`
 // as the pool stores them) to global memory: E4M3 codes and the row scale,
-// or fp16.  Every lane of the row takes part (the row maximum is a shuffle);
-// only `live` rows are written.
+// NVFP4 codes and the row's scale record, or fp16.  Every lane of the row
+// takes part (the row and block maxima are shuffles); only `live` rows are
+// written.
 template <typename TS, int L, int SH>
 __device__ __forceinline__ void write_copy_row(const KParams &p, int64_t row, int lane, bool live, const float *sv) {
     using T = Tile<TS, L>;
@@ -395,6 +415,47 @@ __device__ __forceinline__ void write_copy_row(const KParams &p, int64_t row, in
                 *reinterpret_cast<uint32_t *>(dst) = w[0];
         }
         if (lane == 0) p.shadow_scale[row] = sc;
+    } else if constexpr (SH == kShadowNVFP4) {
+        // a block of 16 elements is G neighbouring lanes' chunks (same k)
+        constexpr int G = 16 / V;
+        static_assert(L % G == 0, "an NVFP4 block must lie within one row's lanes");
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < kElemsPerThread; ++i) amax = fmaxf(amax, fabsf(st[i]));
+#pragma unroll
+        for (int off = L / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float sr = nvfp4_row_scale(amax);
+        uint32_t w[T::kChunks], bc[T::kChunks];
+#pragma unroll
+        for (int k = 0; k < T::kChunks; ++k) {
+            float bmax = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) bmax = fmaxf(bmax, fabsf(st[k * V + i]));
+#pragma unroll
+            for (int off = G / 2; off > 0; off >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, off));
+            bc[k] = nvfp4_block_code(bmax, sr);
+            const float den = __fmul_rn(e4m3_value(bc[k]), sr);
+            w[k] = 0;
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+                const float q0 = den > 0.f ? __fdiv_rn(st[k * V + 2 * i], den) : 0.f;
+                const float q1 = den > 0.f ? __fdiv_rn(st[k * V + 2 * i + 1], den) : 0.f;
+                w[k] |= e2m1x2_code(q0, q1) << (8 * i);
+            }
+        }
+        if (!live) return;
+        unsigned char *out = static_cast<unsigned char *>(p.shadow) + row * (N / 2);
+        unsigned char *rec = reinterpret_cast<unsigned char *>(p.shadow_scale + row * nvfp4_scale_words(N));
+#pragma unroll
+        for (int k = 0; k < T::kChunks; ++k) {
+            const int e0 = (lane + L * k) * V;
+            if constexpr (V == 8)
+                *reinterpret_cast<uint32_t *>(out + e0 / 2) = w[k];
+            else
+                *reinterpret_cast<unsigned short *>(out + e0 / 2) = static_cast<unsigned short>(w[k]);
+            if (lane % G == 0) rec[4 + e0 / 16] = static_cast<unsigned char>(bc[k]);
+        }
+        if (lane == 0) *reinterpret_cast<float *>(rec) = sr;
     } else if (SH == kShadowF16 && live) {
         unsigned char *out = static_cast<unsigned char *>(p.shadow) + row * N * 2;
 #pragma unroll
@@ -566,18 +627,27 @@ __device__ __forceinline__ bool produce_replay(const KParams &p, const ReplayLay
     // (codes, then E4M3 row scales at kShadowScaleOffset), else the tile.
     const bool read_copy = SH != kShadowNone && !(flags & kRFold);
     const int64_t row_first = (rs * p.H + cu.h) * static_cast<int64_t>(p.P) + cu.row0;
-    const uint32_t tile_bytes =
-        static_cast<uint32_t>(rows) * N * (read_copy ? (SH == kShadowF16 ? 2 : 1) : sizeof(TS));
-    const uint32_t scale_bytes = read_copy && SH == kShadowE4M3 ? static_cast<uint32_t>(rows) * 4 : 0;
+    // bytes of one row of the tile as requested: the read copy's codes or the checkpoint
+    const uint32_t row_bytes = !read_copy ? N * sizeof(TS)
+                               : SH == kShadowF16 ? N * 2 : SH == kShadowNVFP4 ? N / 2 : N;
+    const uint32_t tile_bytes = static_cast<uint32_t>(rows) * row_bytes;
+    const uint32_t scale_bytes = !read_copy ? 0
+                                 : SH == kShadowE4M3 ? static_cast<uint32_t>(rows) * 4
+                                 : SH == kShadowNVFP4 ? static_cast<uint32_t>(rows) * nvfp4_scale_words(N) * 4 : 0;
     uint32_t bytes = tile_bytes + scale_bytes;
     if (bulk_entries) bytes += static_cast<uint32_t>(c) * (rows * (io + 4) + N * io);
     if (lane == 0) mbar_arrive_expect(&full[s], bytes);
     __syncwarp();
-    if (scale_bytes != 0 && lane == 31)
-        bulk_load(base + ReplayPipe<TS, L>::kShadowScaleOffset, p.shadow_scale + row_first, scale_bytes, &full[s]);
+    if (scale_bytes != 0 && lane == 31) {
+        if constexpr (SH == kShadowNVFP4)
+            bulk_load(base + ReplayPipe<TS, L>::kNvfp4RecOffset, p.shadow_scale + row_first * nvfp4_scale_words(N),
+                      scale_bytes, &full[s]);
+        else
+            bulk_load(base + ReplayPipe<TS, L>::kShadowScaleOffset, p.shadow_scale + row_first, scale_bytes, &full[s]);
+    }
     {
         const unsigned char *src =
-            read_copy ? static_cast<const unsigned char *>(p.shadow) + row_first * N * (SH == kShadowF16 ? 2 : 1)
+            read_copy ? static_cast<const unsigned char *>(p.shadow) + row_first * row_bytes
                       : reinterpret_cast<const unsigned char *>(static_cast<const TS *>(p.state) + row_first * N);
         for (uint32_t off = static_cast<uint32_t>(lane) * kReplayTileChunk; off < tile_bytes;
              off += 32u * kReplayTileChunk)
@@ -706,7 +776,12 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                         float acc = 0.f;
 #pragma unroll
                         for (int i = 0; i < kElemsPerThread; ++i) acc = fmaf(sv[i], cv[i], acc);
-                        rsum[j] = row_sum<L>(acc) * (SH == kShadowE4M3 ? rscale[rq] : 1.f);
+                        float rs = 1.f;
+                        if constexpr (SH == kShadowE4M3) rs = rscale[rq];
+                        if constexpr (SH == kShadowNVFP4)
+                            rs = *reinterpret_cast<const float *>(copy + PS::kNvfp4RecOffset +
+                                                                   rq * nvfp4_scale_words(N) * 4);
+                        rsum[j] = row_sum<L>(acc) * rs;
                     }
                 }
                 entry_dots<N, kConsumers, IO>(c, be, sB, sC, dots, tid);
@@ -965,6 +1040,16 @@ static cudaError_t launch_replay_t(const KParams &p, int64_t batch, cudaStream_t
     return cudaGetLastError();
 }
 
+// The NVFP4 read copy needs a 16-element block to lie within one row's
+// lanes (dstate 64 and up; the host rejects the rest).
+template <typename TS, int LN, int IO>
+static cudaError_t launch_replay_nvfp4(const KParams &p, int64_t batch, cudaStream_t stream) {
+    if constexpr (LN % (16 / Tile<TS, LN>::kVec) == 0 && Tile<TS, LN>::kN >= 64)
+        return launch_replay_t<TS, LN, IO, kShadowNVFP4>(p, batch, stream);
+    else
+        return cudaErrorInvalidValue;
+}
+
 template <typename TS, int IO>
 static cudaError_t launch_replay_lanes(int lanes, const KParams &p, int64_t batch, cudaStream_t stream) {
     // one kernel per read-copy format: each carries only its own paths
@@ -972,7 +1057,8 @@ static cudaError_t launch_replay_lanes(int lanes, const KParams &p, int64_t batc
 #define SSU_REPLAY_CASE(LN)                                                                          \
     case LN * 4 + kShadowNone: return launch_replay_t<TS, LN, IO, kShadowNone>(p, batch, stream);   \
     case LN * 4 + kShadowF16: return launch_replay_t<TS, LN, IO, kShadowF16>(p, batch, stream);     \
-    case LN * 4 + kShadowE4M3: return launch_replay_t<TS, LN, IO, kShadowE4M3>(p, batch, stream);
+    case LN * 4 + kShadowE4M3: return launch_replay_t<TS, LN, IO, kShadowE4M3>(p, batch, stream);   \
+    case LN * 4 + kShadowNVFP4: return launch_replay_nvfp4<TS, LN, IO>(p, batch, stream);
         SSU_REPLAY_CASE(1)
         SSU_REPLAY_CASE(2)
         SSU_REPLAY_CASE(4)

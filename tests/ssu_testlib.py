@@ -111,3 +111,66 @@ def assert_e4m3_codes_close(got: torch.Tensor, want: torch.Tensor, values: torch
         raise AssertionError(f"{what}: {int((~ok).sum())} of {int(diff.sum())} differing codes are not one step "
                              f"apart at a tie; first: got {int(g[i]):#x} want {int(w[i]):#x} for v*448/amax = "
                              f"{float(q[i])!r}")
+
+
+_E2M1 = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _near_tie(q: torch.Tensor, a: torch.Tensor, b: torch.Tensor) -> torch.Tensor:
+    """|q| within 2^-20 (relative) of the midpoint between grid values a, b."""
+    mid = (a + b) / 2
+    return (q.abs() - mid).abs() <= 2.0 ** -20 * q.abs()
+
+
+def assert_nvfp4_close(got_codes: torch.Tensor, got_rec: torch.Tensor, values: torch.Tensor, what: str = "NVFP4"):
+    """An NVFP4 read copy (code pairs [..., n/2], scale records) against the
+    exact definition applied to `values` (rows along the last axis): the row
+    scale amax / (6 * 448) in fp32 bit for bit; each block's E4M3 code the
+    nearest to (block amax) / (6 s), or one step away where that quotient lies
+    within 2^-20 of a midpoint (the kernels form it in fp32); each element's
+    E2M1 code the nearest to v / (block scale * s) with the block scale the
+    copy holds, or one step away at such a near-tie."""
+    n = values.shape[-1]
+    vd = values.detach().cpu().to(torch.float64).reshape(-1, n)
+    rows = vd.shape[0]
+    codes = got_codes.detach().cpu().view(torch.uint8).reshape(rows, n // 2)
+    rec = got_rec.detach().cpu().reshape(rows, -1)
+    amax = vd.abs().amax(dim=1)
+    want_s = torch.where(amax > 0, amax / 2688.0, torch.ones_like(amax)).to(torch.float32)
+    s = rec[:, 0]
+    if not torch.equal(s, want_s):
+        i = int(torch.nonzero(s != want_s)[0])
+        raise AssertionError(f"{what}: row scale {float(s[i])!r}, want {float(want_s[i])!r}")
+    sd = s.to(torch.float64)
+    bcode = rec.view(torch.uint8)[:, 4:4 + n // 16].contiguous()
+    bmax = vd.abs().view(rows, n // 16, 16).amax(dim=2)
+    qb = bmax / (6.0 * sd[:, None])
+    e4 = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    want_b = (qb.reshape(-1, 1) - e4.view(1, -1)).abs().argmin(dim=1).view(rows, n // 16)
+    gb = bcode.to(torch.int64) & 0x7F
+    if (gb > 126).any():
+        raise AssertionError(f"{what}: a block code is E4M3 NaN")
+    bad = (gb != want_b) & ~(((gb - want_b).abs() == 1) & _near_tie(qb, e4[gb], e4[want_b]))
+    exact_tie = ((qb.reshape(-1, 1) - e4.view(1, -1)).abs() == (qb.reshape(-1, 1) - e4[want_b].reshape(-1, 1)).abs())
+    bad &= ~(exact_tie.sum(dim=1).view(rows, n // 16) > 1)  # an exact tie: either neighbour, checked below
+    if bad.any() or (bcode & 0x80).any():
+        i = torch.nonzero(bad)[0].tolist() if bad.any() else [0, 0]
+        raise AssertionError(f"{what}: block code {int(gb[i[0], i[1]])} at {i}, nearest {int(want_b[i[0], i[1]])}")
+    bs = e4[gb].repeat_interleave(16, dim=1)
+    den = bs * sd[:, None]
+    q = torch.where(den > 0, vd / torch.where(den > 0, den, 1.0), torch.zeros_like(vd))
+    grid = torch.tensor(_E2M1, dtype=torch.float64)
+    c = torch.stack([codes & 15, codes >> 4], dim=-1).reshape(rows, n).to(torch.int64)
+    mag = c & 7
+    dist = (q.abs().clamp(max=6.0).unsqueeze(-1) - grid.view(1, 1, -1)).abs()
+    best = dist.min(dim=-1).values
+    ok_mag = (dist.gather(-1, mag.unsqueeze(-1)).squeeze(-1) == best)
+    near = torch.zeros_like(ok_mag)
+    for k in range(7):
+        near |= ((mag == k) | (mag == k + 1)) & _near_tie(q, grid[k], grid[k + 1])
+    sign_ok = (q == 0) | (((c >> 3) & 1).to(torch.bool) == torch.signbit(q)) | (mag == 0)
+    bad = ~((ok_mag | near) & sign_ok)
+    if bad.any():
+        r, e = torch.nonzero(bad)[0].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())} element codes off; first row {r} element {e}: code "
+                             f"{int(c[r, e])} for v / (block scale * s) = {float(q[r, e])!r}")

@@ -146,7 +146,9 @@ def test_batch_copy_host_checks(libssu):
 
 
 def test_shadow_refresh_host_checks(libssu):
-    assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 3, 32, 48, None) == ssu.ERR_INVALID     # format
+    assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 9, 32, 48, None) == ssu.ERR_INVALID     # format
+    assert libssu.ssu_shadow_refresh(16, 0, 4, 48, 3, 32, 48, None) == ssu.ERR_UNSUPPORTED  # NVFP4, dstate 48
+    assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 3, 32, None, None) == ssu.ERR_INVALID   # NVFP4 without scales
     assert libssu.ssu_shadow_refresh(16, 9, 4, 128, 2, 32, 48, None) == ssu.ERR_INVALID     # state dtype
     assert libssu.ssu_shadow_refresh(16, 0, 0, 128, 2, None, None, None) == ssu.OK          # nothing to do
     assert libssu.ssu_shadow_refresh(16, 0, 4, 128, 2, 32, None, None) == ssu.ERR_INVALID   # E4M3 without scales
@@ -233,6 +235,7 @@ def _replay_buffers(**kw):
     (dict(reserved0=1), {}, ssu.ERR_INVALID, "reserved0"),
     (dict(shadow_format=7, shadow=20480), {}, ssu.ERR_INVALID, "SSU_SHADOW"),
     (dict(shadow_format=1, shadow=None), {}, ssu.ERR_INVALID, "read copy"),
+    (dict(shadow_format=3, shadow=20480), {}, ssu.ERR_INVALID, "NVFP4 scale records"),
     ({}, dict(disable_state_update=1), ssu.ERR_INVALID, "disable_state_update"),
 ])
 def test_replay_host_checks_reject_before_launch(libssu, rb_kw, args_kw, code, needle):

@@ -13,8 +13,8 @@ import oracle
 import selective_state_update_gb300 as ssu
 import workloads
 from gpu_harness import DEV, run_gpu
-from ssu_testlib import (STATE_F32_ATOL, STATE_F32_RTOL, assert_e4m3_codes_close, assert_state_close, assert_y_close,
-                         f64)
+from ssu_testlib import (STATE_F32_ATOL, STATE_F32_RTOL, assert_e4m3_codes_close, assert_nvfp4_close,
+                         assert_state_close, assert_y_close, f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -210,25 +210,35 @@ def test_replay_b256_sampled(libssu):
 # ---------------------------------------------------------------------------
 # The low-precision read copy (article "ReplaySSM", section 低精度读写分离).
 # ---------------------------------------------------------------------------
-_FMT = {"f16": (oracle.SHADOW_F16, torch.float16), "e4m3": (oracle.SHADOW_E4M3, torch.uint8)}
+_FMT = {"f16": (oracle.SHADOW_F16, torch.float16), "e4m3": (oracle.SHADOW_E4M3, torch.uint8),
+        "nvfp4": (oracle.SHADOW_NVFP4, torch.uint8)}
 
 
-@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("fmt", ["f16", "e4m3", "nvfp4"])
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_shadow_refresh_is_the_oracles(libssu, fmt, state_dtype):
     """The GPU's read copy of a pool equals the oracle's: fp16 bit for bit;
     E4M3 row scales bit for bit and codes equal except one step at a tie of
-    the fp32 quotient (assert_e4m3_codes_close)."""
+    the fp32 quotient (assert_e4m3_codes_close); NVFP4 row scales bit for
+    bit, block and element codes the nearest except one step at such a tie
+    (assert_nvfp4_close)."""
     code, dtype = _FMT[fmt]
     g = torch.Generator().manual_seed(70)
     st = (torch.randn((5, 3, 20, 128), generator=g) * torch.rand((5, 3, 20, 1), generator=g) * 3).to(state_dtype)
     st[2, 1, 7] = 0
+    st[3, 0, 4, 32:48] *= 1e-6  # a block far below its row's largest
     want, want_scale = oracle.shadow_refresh(st, code)
-    sh = torch.empty(st.shape, dtype=dtype, device=DEV)
-    sc = torch.empty(st.shape[:-1], dtype=torch.float32, device=DEV) if fmt == "e4m3" else None
+    if fmt == "nvfp4":
+        sh = torch.zeros((*st.shape[:-1], 64), dtype=torch.uint8, device=DEV)
+        sc = torch.zeros((*st.shape[:-1], ssu.nvfp4_scale_words(128)), dtype=torch.float32, device=DEV)
+    else:
+        sh = torch.empty(st.shape, dtype=dtype, device=DEV)
+        sc = torch.empty(st.shape[:-1], dtype=torch.float32, device=DEV) if fmt == "e4m3" else None
     ssu.ssu_shadow_refresh(st.to(DEV), sh, sc)
     torch.cuda.synchronize()
-    if fmt == "e4m3":
+    if fmt == "nvfp4":
+        assert_nvfp4_close(sh, sc, st)
+    elif fmt == "e4m3":
         assert torch.equal(sc.cpu(), want_scale)
         assert_e4m3_codes_close(sh, want, st)
     else:
@@ -267,17 +277,20 @@ def _check_read_copy(w, fmt):
     assert torch.equal(sh_got[keep], sh0[keep]), "a read copy changed without a fold"
     if folded:
         want, want_scale = oracle.shadow_refresh(got[folded], code)
-        if fmt == "e4m3":
+        if fmt == "nvfp4":
+            assert_nvfp4_close(sh_got[folded], sc.cpu()[folded], got[folded], "a fold's NVFP4 read copy")
+        elif fmt == "e4m3":
             assert_e4m3_codes_close(sh_got[folded], want, got[folded], "a fold's read copy")
         else:
             assert torch.equal(sh_got[folded], want), "a fold's read copy differs from the copy of its checkpoint"
-        if sc is not None:
+        if fmt == "e4m3":
             assert torch.equal(sc.cpu()[folded], want_scale)
-            assert torch.equal(sc.cpu()[keep], sc0[keep])
+    if sc is not None:
+        assert torch.equal(sc.cpu()[keep], sc0[keep])
     assert torch.equal(g.xbuf.cpu(), ref.xbuf) and torch.equal(g.Bbuf.cpu(), ref.Bbuf)
 
 
-@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("fmt", ["f16", "e4m3", "nvfp4"])
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("buffer_len", [1, 3, 16])
 def test_replay_read_copy_against_oracle(libssu, fmt, state_dtype, buffer_len):
@@ -286,17 +299,19 @@ def test_replay_read_copy_against_oracle(libssu, fmt, state_dtype, buffer_len):
     _check_read_copy(w, fmt)
 
 
-@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("fmt", ["f16", "e4m3", "nvfp4"])
 @pytest.mark.parametrize("dstate,dim", [(16, 8), (128, 100), (256, 64)])
 def test_replay_read_copy_shapes(libssu, fmt, dstate, dim):
     if fmt == "e4m3" and dim % 4:
         pytest.skip("E4M3 row scales need dim % 4 == 0")
+    if fmt == "nvfp4" and dstate < 64:
+        pytest.skip("an NVFP4 read copy needs dstate 64, 128 or 256")
     w = workloads.replay_problem(90 + dstate + dim, slots=24, heads=6, groups=3, dim=dim, dstate=dstate, nseq=5,
                                  buffer_len=5)
     _check_read_copy(w, fmt)
 
 
-@pytest.mark.parametrize("fmt", ["f16", "e4m3"])
+@pytest.mark.parametrize("fmt", ["f16", "e4m3", "nvfp4"])
 def test_replay_read_copy_many_units(libssu, fmt):
     w = workloads.replay_problem(95, slots=96, heads=24, groups=4, dim=128, dstate=64, nseq=80, buffer_len=7,
                                  pad_frac=0.1)
@@ -307,6 +322,15 @@ def test_read_copy_e4m3_needs_dim_multiple_of_4(libssu):
     w = workloads.replay_problem(96, slots=8, heads=2, groups=1, dim=6, dstate=32, nseq=2, buffer_len=2).to(DEV)
     sh = torch.zeros(w.state.shape, dtype=torch.uint8, device=DEV)
     sc = torch.ones(w.state.shape[:-1], dtype=torch.float32, device=DEV)
+    with pytest.raises(NotImplementedError):
+        ssu.ssu_replay_update(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count, D=w.D,
+                              z=w.z, state_batch_indices=w.read, shadow=sh, shadow_scale=sc)
+
+
+def test_read_copy_nvfp4_needs_dstate_64_to_256(libssu):
+    w = workloads.replay_problem(97, slots=8, heads=2, groups=1, dim=8, dstate=32, nseq=2, buffer_len=2).to(DEV)
+    sh = torch.zeros((*w.state.shape[:-1], 16), dtype=torch.uint8, device=DEV)
+    sc = torch.zeros((*w.state.shape[:-1], ssu.nvfp4_scale_words(32)), dtype=torch.float32, device=DEV)
     with pytest.raises(NotImplementedError):
         ssu.ssu_replay_update(w.state, w.x, w.dt, w.A, w.B, w.C, w.xbuf, w.dtbuf, w.Bbuf, w.count, D=w.D,
                               z=w.z, state_batch_indices=w.read, shadow=sh, shadow_scale=sc)

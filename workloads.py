@@ -64,8 +64,9 @@ class Workload:
     dtbuf: Optional[torch.Tensor] = None       # [slots, L, heads, dim] fp32 processed steps
     Bbuf: Optional[torch.Tensor] = None        # [slots, L, groups, dstate] io dtype
     count: Optional[torch.Tensor] = None       # [batch] int32 buffered entries per sequence
-    shadow: Optional[torch.Tensor] = None      # read copy of the checkpoints (fp16 or uint8 E4M3 codes)
-    shadow_scale: Optional[torch.Tensor] = None  # [slots, heads, dim] fp32 E4M3 row scales
+    shadow: Optional[torch.Tensor] = None      # read copy of the checkpoints (fp16, uint8 E4M3 codes, or
+                                               # uint8 NVFP4 code pairs [..., dstate / 2])
+    shadow_scale: Optional[torch.Tensor] = None  # fp32 E4M3 row scales [slots, heads, dim] or NVFP4 scale records
     meta: dict = field(default_factory=dict)
 
     @property
@@ -261,6 +262,21 @@ def replay_e4m3_b256_fp32(device="cpu", seed=1008, batch=256, buffer_len=16) -> 
     w.shadow = torch.zeros(w.state.shape, dtype=torch.uint8, device=device)
     w.shadow_scale = torch.ones(w.state.shape[:-1], dtype=torch.float32, device=device)
     w.meta["shadow_format"] = "e4m3"
+    return w
+
+
+def replay_nvfp4_b256_fp32(device="cpu", seed=1012, batch=256, buffer_len=16) -> Workload:
+    """replay_b256_fp32 with an NVFP4 read copy of the checkpoints (E2M1 code
+    pairs [slots, heads, dim, dstate / 2] and per-row scale records of
+    (4 + dstate / 16 + 15) // 16 * 4 floats, allocated here, filled by the
+    caller with the copy of the checkpoints)."""
+    w = replay_b256_fp32(device=device, seed=seed, batch=batch, buffer_len=buffer_len)
+    w.name = "replay_nvfp4_b256_fp32"
+    n = w.state.shape[-1]
+    w.shadow = torch.zeros((*w.state.shape[:-1], n // 2), dtype=torch.uint8, device=device)
+    w.shadow_scale = torch.zeros((*w.state.shape[:-1], (4 + n // 16 + 15) // 16 * 4), dtype=torch.float32,
+                                 device=device)
+    w.meta["shadow_format"] = "nvfp4"
     return w
 
 
@@ -581,6 +597,7 @@ NAMED = {
     "varlen_fp16_disable": lambda device="cpu", seed=1005: varlen_fp16(device, seed, disable_state_update=True),
     "replay_b256_fp32": replay_b256_fp32,
     "replay_e4m3_b256_fp32": replay_e4m3_b256_fp32,
+    "replay_nvfp4_b256_fp32": replay_nvfp4_b256_fp32,
     "replay_f16copy_b256_fp32": replay_f16copy_b256_fp32,
     "copy_slots_b256_fp32": copy_slots_b256_fp32,
     "verify_b256_t4_fp32": verify_b256_t4_fp32,
