@@ -53,11 +53,19 @@ static_assert(kReplayMaxStages <= kMaxRingStages, "ring exit record too small");
 // Size of the pieces the checkpoint tile is requested in (lanes in turn).
 constexpr uint32_t kReplayTileChunk = 32768;
 
-template <typename TS, int L>
+template <typename TS, int L, int SH = kShadowNone>
 struct ReplayPipe {
+    // State rows per consumer thread: four, as in the plain kernels, or two
+    // when the consumers decode an NVFP4 copy, so that its decode and the
+    // unit's short dependent phases run on twice the warps (measured: NVFP4
+    // 0.358 ms against 0.416 ms with four; fp32 0.331 against 0.294, where the
+    // 96-register budget of two costs more than the warps gain).  Four at
+    // dstate 256 in any case.
+    static constexpr int kRows = SH == kShadowNVFP4 && L < 16 ? 2 : 4;
+    static constexpr int kSlots = kTileRows / kRows;
     static constexpr int kN = Tile<TS, L>::kN;
     static constexpr int kTileBytes = kTileRows * kN * static_cast<int>(sizeof(TS));
-    static constexpr int kConsumerWarps = (Tile<TS, L>::kThreads + 31) / 32;
+    static constexpr int kConsumerWarps = (kSlots * L + 31) / 32;
     static constexpr int kConsumers = 32 * kConsumerWarps;
     // Producer warps take units in turn; a producer waits for its stage by
     // the parity of the "empty" phase, which is unambiguous only with no more
@@ -77,7 +85,7 @@ struct ReplayPipe {
     // margin) and two CTAs still leave 128 registers a thread.  The ring
     // itself is sized at launch from the device's shared memory per SM.
     static constexpr int kMinCtas =
-        (222 * 1024 / 2 - 1024) / (kTileBytes + 4096) >= 2 && 65536 / (2 * kThreads) >= 128 ? 2 : 1;
+        (222 * 1024 / 2 - 1024) / (kTileBytes + 4096) >= 2 && 65536 / (2 * kThreads) >= 96 ? 2 : 1;
 };
 
 // Per-stage header written by the producer.
@@ -700,13 +708,14 @@ template <typename TS, int L, int IO, int SH>
 __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLayout &lay, int64_t units,
                                                unsigned char *smem, uint64_t *full, uint64_t *empty, RingExit *rx) {
     using T = Tile<TS, L>;
-    using PS = ReplayPipe<TS, L>;
+    using PS = ReplayPipe<TS, L, SH>;
     constexpr int N = PS::kN;
     constexpr int kConsumers = PS::kConsumers;
     constexpr int io = IO == kF32 ? 4 : 2;
     const int S = lay.stages;
     const int tid = threadIdx.x;
-    const bool active = tid < T::kThreads;
+    constexpr int kReplayRows = PS::kRows, kReplaySlots = PS::kSlots;
+    const bool active = tid < kReplaySlots * L;
     const int lane = tid % L;
     const int slot_row = tid / L;
     float *dots = reinterpret_cast<float *>(smem + lay.dots);
@@ -749,12 +758,12 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
             if (!fold) {
                 // S_ckpt . C of this thread's rows (every lane of a row ends
                 // with the sum) beside the B_j . C dots.
-                float rsum[kRowsPerThread];
+                float rsum[kReplayRows];
                 if constexpr (SH == kShadowNone) {
                     if (active) {
 #pragma unroll
-                        for (int j = 0; j < kRowsPerThread; ++j) {
-                            const int rr = slot_row + j * kRowSlots;  // row within the tile
+                        for (int j = 0; j < kReplayRows; ++j) {
+                            const int rr = slot_row + j * kReplaySlots;  // row within the tile
                             float sv[kElemsPerThread];
                             T::load_row_smem(tile + (rr < rows ? rr : 0) * N, lane, sv);
                             float acc = 0.f;
@@ -768,8 +777,8 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                     const unsigned char *copy = reinterpret_cast<const unsigned char *>(tile);
                     const float *rscale = reinterpret_cast<const float *>(copy + PS::kShadowScaleOffset);
 #pragma unroll
-                    for (int j = 0; j < kRowsPerThread; ++j) {
-                        const int rr = slot_row + j * kRowSlots;
+                    for (int j = 0; j < kReplayRows; ++j) {
+                        const int rr = slot_row + j * kReplaySlots;
                         const int rq = rr < rows ? rr : 0;
                         float sv[kElemsPerThread];
                         load_copy_row<TS, L>(copy, rq, lane, SH, sv);
@@ -798,12 +807,12 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                     const int per = (c + L) / L;  // ceil((c + 1) / L)
                     const int hi = c - lane * per;
                     const int lo = hi - per + 1 > 0 ? hi - per + 1 : 0;
-                    float w[kRowsPerThread], hs[kRowsPerThread];
-                    float4 q[kRowsPerThread];
-                    int rq[kRowsPerThread];
+                    float w[kReplayRows], hs[kReplayRows];
+                    float4 q[kReplayRows];
+                    int rq[kReplayRows];
 #pragma unroll
-                    for (int j = 0; j < kRowsPerThread; ++j) {
-                        const int rr = slot_row + j * kRowSlots;
+                    for (int j = 0; j < kReplayRows; ++j) {
+                        const int rr = slot_row + j * kReplaySlots;
                         rq[j] = rr < rows ? rr : 0;
                         q[j] = rowq[rq[j]];
                         w[j] = 1.f;
@@ -813,7 +822,7 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                     if (e == c) {
                         const float dc = dots[c];
 #pragma unroll
-                        for (int j = 0; j < kRowsPerThread; ++j) {
+                        for (int j = 0; j < kReplayRows; ++j) {
                             hs[j] = fmaf(q[j].y, dc, 0.f);
                             w[j] = q[j].x;
                         }
@@ -822,7 +831,7 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                     for (; e >= lo; --e) {
                         const float de_ = dots[e];
 #pragma unroll
-                        for (int j = 0; j < kRowsPerThread; ++j) {
+                        for (int j = 0; j < kReplayRows; ++j) {
                             const float d = de[e * kDtStride + rq[j]];
                             const float t = d * io_at<IO>(xe, e * x_stride<IO>() + rq[j]);
                             hs[j] = fmaf(w[j] * t, de_, hs[j]);
@@ -832,7 +841,7 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
 #pragma unroll
                     for (int off = 1; off < L; off <<= 1) {
 #pragma unroll
-                        for (int j = 0; j < kRowsPerThread; ++j) {
+                        for (int j = 0; j < kReplayRows; ++j) {
                             const float w2 = __shfl_down_sync(0xffffffffu, w[j], off);
                             const float h2 = __shfl_down_sync(0xffffffffu, hs[j], off);
                             if ((lane & (2 * off - 1)) == 0) {
@@ -843,8 +852,8 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                     }
                     if (lane == 0) {
 #pragma unroll
-                        for (int j = 0; j < kRowsPerThread; ++j) {
-                            const int rr = slot_row + j * kRowSlots;
+                        for (int j = 0; j < kReplayRows; ++j) {
+                            const int rr = slot_row + j * kReplaySlots;
                             if (rr < rows)
                                 store_small(p.y, cu.b * p.ys[0] + cu.h * p.ys[1] + (cu.row0 + rr) * p.ys[2], IO,
                                             output(fmaf(w[j], rsum[j], hs[j]), Dh, q[j].z, q[j].w));
@@ -858,8 +867,8 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
                 }
                 if (active) {
                     float bv[kElemsPerThread];
-                    for (int j = 0; j < kRowsPerThread; ++j) {
-                        const int rr = slot_row + j * kRowSlots;
+                    for (int j = 0; j < kReplayRows; ++j) {
+                        const int rr = slot_row + j * kReplaySlots;
                         const bool live = rr < rows;
                         const int rq = live ? rr : 0;
                         float sv[kElemsPerThread];
@@ -928,9 +937,9 @@ __device__ __forceinline__ int replay_consumer(const KParams &p, const ReplayLay
 }
 
 template <typename TS, int L, int IO, int SH>
-__global__ void __launch_bounds__(ReplayPipe<TS, L>::kThreads, ReplayPipe<TS, L>::kMinCtas)
+__global__ void __launch_bounds__(ReplayPipe<TS, L, SH>::kThreads, ReplayPipe<TS, L, SH>::kMinCtas)
     ssu_replay_kernel(const KParams p, const ReplayLayout lay, int64_t units) {
-    using PS = ReplayPipe<TS, L>;
+    using PS = ReplayPipe<TS, L, SH>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     uint64_t *empty = full + lay.stages;
@@ -1011,7 +1020,7 @@ static cudaError_t prepare_replay_kernel(int *reg_ctas) {
         e = cudaFuncGetAttributes(&a, ssu_replay_kernel<TS, L, IO, SH>);
         if (e != cudaSuccess) return e;
         const int regs = (a.numRegs + 7) / 8 * 8;  // allocated per thread in units of 8
-        n = regs > 0 ? 65536 / (regs * ReplayPipe<TS, L>::kThreads) : 1;
+        n = regs > 0 ? 65536 / (regs * ReplayPipe<TS, L, SH>::kThreads) : 1;
         if (n < 1) n = 1;
         cache[dev].store(n, std::memory_order_relaxed);
     }
@@ -1021,7 +1030,7 @@ static cudaError_t prepare_replay_kernel(int *reg_ctas) {
 
 template <typename TS, int L, int IO, int SH>
 static cudaError_t launch_replay_t(const KParams &p, int64_t batch, cudaStream_t stream) {
-    using PS = ReplayPipe<TS, L>;
+    using PS = ReplayPipe<TS, L, SH>;
     int reg_ctas = 0;
     cudaError_t e = prepare_replay_kernel<TS, L, IO, SH>(&reg_ctas);
     if (e != cudaSuccess) return e;
