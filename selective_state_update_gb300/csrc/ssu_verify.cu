@@ -147,15 +147,20 @@ __device__ __forceinline__ VerifyStage verify_stage(float *smem, int L, int T, i
     return st;
 }
 
-// Entries 0 .. c-1 of (slot, head h, group g) for rows row0 .. row0+63.
+// Entries 0 .. c-1 of (slot, group g): their B.
 template <int IO, int N>
-__device__ __forceinline__ void stage_entries(const KParams &p, const VerifyStage &st, int64_t slot, int c, int h,
-                                              int g, int row0) {
+__device__ __forceinline__ void stage_entry_B(const KParams &p, const VerifyStage &st, int64_t slot, int c, int g) {
     const int64_t eb0 = (slot * p.rlen * p.G + g) * static_cast<int64_t>(N);  // entry 0's B
     for (int i = threadIdx.x; i < c * N; i += kVerifyThreads) {
         const int j = i / N, n = i % N;
         st.eB[i] = io_load<IO>(p.Bbuf, eb0 + static_cast<int64_t>(j) * p.G * N + n);
     }
+}
+
+// Entries 0 .. c-1 of (slot, head h): their x and dt' rows row0 .. row0+63.
+template <int IO>
+__device__ __forceinline__ void stage_entry_rows(const KParams &p, const VerifyStage &st, int64_t slot, int c, int h,
+                                                 int row0) {
     const int64_t e0 = (slot * p.rlen * p.H + h) * static_cast<int64_t>(p.P) + row0;  // entry 0's row row0
     for (int i = threadIdx.x; i < c * kVerifyRows; i += kVerifyThreads) {
         const int j = i / kVerifyRows, r = i % kVerifyRows;
@@ -233,7 +238,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
     if (!verify_sequence(p, b, &slot, &c, &pad)) return;  // flagged (again) by the verify launch
     if (pad || c + 2 * T < p.rlen) return;                 // no flush here
     const VerifyStage st = verify_stage(vsmem, p.rlen, T, p.N);
-    with_io(p.io_dtype, [&](auto io) { stage_entries<decltype(io)::value, 4 * NPT>(p, st, slot, c, h, g, row0); });
+    with_io(p.io_dtype, [&](auto io) {
+        stage_entry_B<decltype(io)::value, 4 * NPT>(p, st, slot, c, g);
+        stage_entry_rows<decltype(io)::value>(p, st, slot, c, h, row0);
+    });
     __syncthreads();
     if (row >= p.P) return;
     TS *srow = static_cast<TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N;
@@ -243,13 +251,20 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
     store_state_part<TS, NPT>(srow, q, s);
 }
 
-// Three CTAs per SM while a thread's share of a state row (NPT values) fits
-// in the register budget that leaves (up to dstate 128), two above.
+// One CTA per (sequence, group, 64 dim rows) walks the group's heads: the
+// group's entries' B, the drafts' B and C and the (c + T) T dots B_m . C_k are
+// staged and formed once; per head, the entries' and drafts' rows, the
+// appends, the step terms, S_ckpt . C_k and the walks.  The next head's state
+// row part is loaded into registers while a head is computed (dstate up to
+// 128; above, it is loaded when the head starts).
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verify_kernel(const KParams p, int T) {
+__global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KParams p, int T) {
     extern __shared__ __align__(16) float vsmem[];
+    constexpr int N = 4 * NPT;
+    constexpr bool kPrefetch = NPT <= 32;
     const int64_t b = blockIdx.x;
-    const int h = blockIdx.y, g = h / p.heads_per_group, row0 = blockIdx.z * kVerifyRows;
+    const int g = blockIdx.y, row0 = blockIdx.z * kVerifyRows;
+    const int hpg = p.heads_per_group, h0 = g * hpg;
     const int r = threadIdx.x / 4, row = row0 + r, q = threadIdx.x & 3;
     const bool active = row < p.P;  // the four threads of a row agree
     int64_t slot;
@@ -258,22 +273,23 @@ __global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verif
     if (!verify_sequence(p, b, &slot, &c, &pad)) return;
     const bool fold = !pad && c + 2 * T >= p.rlen;
     if (fold) c = 0;
-    if (h == 0 && blockIdx.z == 0 && threadIdx.x == 0) p.cnt_out[b] = c;
-    const VerifyStage st = verify_stage(vsmem, p.rlen, T, p.N);
-    // the state row part in flight while the entries and drafts are staged
+    if (g == 0 && blockIdx.z == 0 && threadIdx.x == 0) p.cnt_out[b] = c;
+    const VerifyStage st = verify_stage(vsmem, p.rlen, T, N);
+    const bool live = !pad && active;
+    auto state_row = [&](int h) {
+        return static_cast<const TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * N;
+    };
+    // the first head's state row part in flight while the group's operands are staged
     float s[NPT];
-    const TS *srow = static_cast<const TS *>(p.state) + ((slot * p.H + h) * static_cast<int64_t>(p.P) + row) * p.N;
-    if (pad || !active) {
+    if (live) {
+        load_state_part<TS, NPT>(state_row(h0), q, s);
+    } else {
 #pragma unroll
         for (int i = 0; i < NPT; ++i) s[i] = 0.f;
-    } else {
-        load_state_part<TS, NPT>(srow, q, s);
     }
-    const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
     with_io(p.io_dtype, [&](auto io) {
         constexpr int IO = decltype(io)::value;
-        constexpr int N = 4 * NPT;
-        stage_entries<IO, N>(p, st, slot, c, h, g, row0);
+        stage_entry_B<IO, N>(p, st, slot, c, g);
         for (int i = threadIdx.x; i < T * N; i += kVerifyThreads) {
             const int k = i / N, n = i % N;
             const int64_t rr = b * T + k;
@@ -282,55 +298,18 @@ __global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verif
             st.dB[i] = io_value<IO>(bb);
             st.rB[i] = bb;
         }
-        for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
-            const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
-            if (rrow >= p.P) continue;
-            const int64_t rr = b * T + k;
-            const float dtv = p.dt_dtype == kF32 ? static_cast<const float *>(p.dt)[rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2]]
-                                                 : bits_to_float(static_cast<const unsigned short *>(p.dt)[rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2]], p.dt_dtype);
-            st.dd[i] = processed_step(dtv, bias, p.softplus);
-            const uint32_t xb = io_bits<IO>(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2]);
-            st.dx[i] = io_value<IO>(xb);
-            st.rx[i] = xb;
-            st.dz[i] = p.z ? io_load<IO>(p.z, rr * p.zs[0] + h * p.zs[1] + rrow * p.zs[2]) : 0.f;
-        }
         __syncthreads();
-        // The drafts become entries c .. c+T-1, written by the whole CTA from
-        // the stage before the state walk, so that the stores drain while it
-        // runs: x and B keep their bits, the processed step is stored in fp32;
-        // B once per group, by the group's first head.  No CTA reads these
-        // entries.
-        if (!pad) {
-            const int64_t e0 = ((slot * p.rlen + c) * p.H + h) * static_cast<int64_t>(p.P) + row0;
-            for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
-                const int k = i / kVerifyRows, rw = i % kVerifyRows;
-                if (row0 + rw >= p.P) continue;
-                const int64_t e = e0 + static_cast<int64_t>(k) * p.H * p.P + rw;
-                io_store_bits<IO>(p.xbuf, e, st.rx[i]);
-                p.dtbuf[e] = st.dd[i];
-            }
-            if (h % p.heads_per_group == 0 && blockIdx.z == 0) {
-                const int64_t eb = ((slot * p.rlen + c) * p.G + g) * static_cast<int64_t>(N);
-                for (int i = threadIdx.x; i < T * N; i += kVerifyThreads) {
-                    const int k = i / N, n = i % N;
-                    io_store_bits<IO>(p.Bbuf, eb + static_cast<int64_t>(k) * p.G * N + n, st.rB[i]);
-                }
+        // the drafts' B become entries c .. c+T-1 of the group (once: the
+        // group's first 64-row block)
+        if (!pad && blockIdx.z == 0) {
+            const int64_t eb = ((slot * p.rlen + c) * p.G + g) * static_cast<int64_t>(N);
+            for (int i = threadIdx.x; i < T * N; i += kVerifyThreads) {
+                const int k = i / N, n = i % N;
+                io_store_bits<IO>(p.Bbuf, eb + static_cast<int64_t>(k) * p.G * N + n, st.rB[i]);
             }
         }
     });
-    // Each step's decay and input term per row, once (the walks of the
-    // drafts share them): steps m < c are the entries, m >= c the drafts.
-    const float Ah = p.A[h];
-    for (int i = threadIdx.x; i < (c + T) * kVerifyRows; i += kVerifyThreads) {
-        const int m = i / kVerifyRows;
-        const bool entry = m < c;
-        const float d = entry ? st.ed[i] : st.dd[i - c * kVerifyRows];
-        const float xv = entry ? st.ex[i] : st.dx[i - c * kVerifyRows];
-        st.ga[i] = decay_inline(Ah, d);
-        st.te[i] = d * xv;
-    }
     // B_m . C_k for every step m <= c + k that draft k sees, one warp per dot
-    constexpr int N = 4 * NPT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = warp; i < (c + T) * T; i += kVerifyThreads / 32) {
         const int m = i / T, k = i % T;
@@ -343,36 +322,98 @@ __global__ void __launch_bounds__(kVerifyThreads, (NPT >= 64 ? 2 : 3)) ssu_verif
         v = row_sum<32>(v);
         if (lane == 0) st.bc[i] = v;
     }
-    // S_ckpt . C_k of this row, over the row's four threads
-    for (int k = 0; k < T; ++k) {
-        const float *Ck = st.dC + k * N;
-        float part = 0.f;
+    for (int j = 0; j < hpg; ++j) {
+        const int h = h0 + j;
+        float sn[kPrefetch ? NPT : 1];
+        if constexpr (kPrefetch) {
+            if (live && j + 1 < hpg) load_state_part<TS, NPT>(state_row(h + 1), q, sn);
+        }
+        // this head's rows of the entries and the drafts
+        const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
+        with_io(p.io_dtype, [&](auto io) {
+            constexpr int IO = decltype(io)::value;
+            stage_entry_rows<IO>(p, st, slot, c, h, row0);
+            for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
+                const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
+                if (rrow >= p.P) continue;
+                const int64_t rr = b * T + k;
+                const int64_t di = rr * p.dts[0] + h * p.dts[1] + rrow * p.dts[2];
+                const float dtv = p.dt_dtype == kF32 ? static_cast<const float *>(p.dt)[di]
+                                                     : bits_to_float(static_cast<const unsigned short *>(p.dt)[di], p.dt_dtype);
+                st.dd[i] = processed_step(dtv, bias, p.softplus);
+                const uint32_t xb = io_bits<IO>(p.x, rr * p.xs[0] + h * p.xs[1] + rrow * p.xs[2]);
+                st.dx[i] = io_value<IO>(xb);
+                st.rx[i] = xb;
+                st.dz[i] = p.z ? io_load<IO>(p.z, rr * p.zs[0] + h * p.zs[1] + rrow * p.zs[2]) : 0.f;
+            }
+            __syncthreads();
+            // the drafts' x and dt' become entries c .. c+T-1 of this head
+            if (!pad) {
+                const int64_t e0 = ((slot * p.rlen + c) * p.H + h) * static_cast<int64_t>(p.P) + row0;
+                for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
+                    const int k = i / kVerifyRows, rw = i % kVerifyRows;
+                    if (row0 + rw >= p.P) continue;
+                    const int64_t e = e0 + static_cast<int64_t>(k) * p.H * p.P + rw;
+                    io_store_bits<IO>(p.xbuf, e, st.rx[i]);
+                    p.dtbuf[e] = st.dd[i];
+                }
+            }
+        });
+        // each step's decay and input term per row, shared by the drafts' walks
+        const float Ah = p.A[h];
+        for (int i = threadIdx.x; i < (c + T) * kVerifyRows; i += kVerifyThreads) {
+            const int m = i / kVerifyRows;
+            const bool entry = m < c;
+            const float d = entry ? st.ed[i] : st.dd[i - c * kVerifyRows];
+            const float xv = entry ? st.ex[i] : st.dx[i - c * kVerifyRows];
+            st.ga[i] = decay_inline(Ah, d);
+            st.te[i] = d * xv;
+        }
+        // S_ckpt . C_k of this row, over the row's four threads
+        for (int k = 0; k < T; ++k) {
+            const float *Ck = st.dC + k * N;
+            float part = 0.f;
 #pragma unroll
-        for (int i4 = 0; i4 < NPT / 4; ++i4) {
-            const float4 cv = *reinterpret_cast<const float4 *>(Ck + col_of(i4, q));
-            part = fmaf(s[4 * i4], cv.x, part);
-            part = fmaf(s[4 * i4 + 1], cv.y, part);
-            part = fmaf(s[4 * i4 + 2], cv.z, part);
-            part = fmaf(s[4 * i4 + 3], cv.w, part);
+            for (int i4 = 0; i4 < NPT / 4; ++i4) {
+                const float4 cv = *reinterpret_cast<const float4 *>(Ck + col_of(i4, q));
+                part = fmaf(s[4 * i4], cv.x, part);
+                part = fmaf(s[4 * i4 + 1], cv.y, part);
+                part = fmaf(s[4 * i4 + 2], cv.z, part);
+                part = fmaf(s[4 * i4 + 3], cv.w, part);
+            }
+            part = row_sum<4>(part);
+            if (q == 0) st.us[k * kVerifyRows + r] = part;
         }
-        part = row_sum<4>(part);
-        if (q == 0) st.us[k * kVerifyRows + r] = part;
-    }
-    __syncthreads();
-    if (!active) return;
-    // draft k (thread q of the row takes k = q, q + 4, ...): the walk from
-    // step c + k down to step 0 gathers the decayed window sum and g_{0:M}
-    const float Dh = p.D ? p.D[h] : 0.f;
-    for (int k = q; k < T; k += 4) {
-        float acc = 0.f, gam = 1.f;
-        for (int m = c + k; m >= 0; --m) {
-            acc = fmaf(gam, st.te[m * kVerifyRows + r] * st.bc[m * T + k], acc);
-            gam *= st.ga[m * kVerifyRows + r];
+        __syncthreads();
+        // draft k (thread q of the row takes k = q, q + 4, ...): the walk
+        // from step c + k down to step 0 gathers the decayed window sum and
+        // g_{0:M}
+        if (active) {
+            const float Dh = p.D ? p.D[h] : 0.f;
+            for (int k = q; k < T; k += 4) {
+                float acc = 0.f, gam = 1.f;
+                for (int m = c + k; m >= 0; --m) {
+                    acc = fmaf(gam, st.te[m * kVerifyRows + r] * st.bc[m * T + k], acc);
+                    gam *= st.ga[m * kVerifyRows + r];
+                }
+                const float sum = fmaf(gam, st.us[k * kVerifyRows + r], acc);
+                const int64_t rr = b * T + k;
+                store_small(p.y, rr * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
+                            output(sum, Dh, st.dx[k * kVerifyRows + r],
+                                   silu_gate(st.dz[k * kVerifyRows + r], p.z != nullptr)));
+            }
         }
-        const float sum = fmaf(gam, st.us[k * kVerifyRows + r], acc);
-        const int64_t rr = b * T + k;
-        store_small(p.y, rr * p.ys[0] + h * p.ys[1] + row * p.ys[2], p.io_dtype,
-                    output(sum, Dh, st.dx[k * kVerifyRows + r], silu_gate(st.dz[k * kVerifyRows + r], p.z != nullptr)));
+        __syncthreads();  // the head's stage is read out before the next head's is written
+        if (j + 1 < hpg) {
+            if constexpr (kPrefetch) {
+                if (live) {
+#pragma unroll
+                    for (int i = 0; i < NPT; ++i) s[i] = sn[i];
+                }
+            } else if (live) {
+                load_state_part<TS, NPT>(state_row(h + 1), q, s);
+            }
+        }
     }
 }
 
@@ -392,7 +433,9 @@ static cudaError_t launch_verify_t(const KParams &p, int64_t batch, int T, cudaS
     }
     ssu_verify_fold_kernel<TS, NPT><<<grid, kVerifyThreads, smem, stream>>>(p, T);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ssu_verify_kernel<TS, NPT><<<grid, kVerifyThreads, smem, stream>>>(p, T);
+    const dim3 ggrid(static_cast<unsigned>(batch), static_cast<unsigned>(p.G),
+                     static_cast<unsigned>((p.P + kVerifyRows - 1) / kVerifyRows));
+    ssu_verify_kernel<TS, NPT><<<ggrid, kVerifyThreads, smem, stream>>>(p, T);
     return cudaGetLastError();
 }
 
