@@ -254,14 +254,14 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
 // One CTA per (sequence, group, 64 dim rows) walks the group's heads: the
 // group's entries' B, the drafts' B and C and the (c + T) T dots B_m . C_k are
 // staged and formed once; per head, the entries' and drafts' rows, the
-// appends, the step terms, S_ckpt . C_k and the walks.  The next head's state
-// row part is loaded into registers while a head is computed (dstate up to
-// 128; above, it is loaded when the head starts).
+// appends, the step terms, S_ckpt . C_k and the walks, the head's state row
+// part loaded while its rows are staged.  Three CTAs per SM (measured: 0.626
+// ms per call against 0.680 ms with the next head's state prefetched into
+// registers at two CTAs per SM).
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KParams p, int T) {
+__global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KParams p, int T) {
     extern __shared__ __align__(16) float vsmem[];
     constexpr int N = 4 * NPT;
-    constexpr bool kPrefetch = NPT <= 32;
     const int64_t b = blockIdx.x;
     const int g = blockIdx.y, row0 = blockIdx.z * kVerifyRows;
     const int hpg = p.heads_per_group, h0 = g * hpg;
@@ -324,10 +324,6 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KPa
     }
     for (int j = 0; j < hpg; ++j) {
         const int h = h0 + j;
-        float sn[kPrefetch ? NPT : 1];
-        if constexpr (kPrefetch) {
-            if (live && j + 1 < hpg) load_state_part<TS, NPT>(state_row(h + 1), q, sn);
-        }
         // this head's rows of the entries and the drafts
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
         with_io(p.io_dtype, [&](auto io) {
@@ -404,16 +400,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_kernel(const KPa
             }
         }
         __syncthreads();  // the head's stage is read out before the next head's is written
-        if (j + 1 < hpg) {
-            if constexpr (kPrefetch) {
-                if (live) {
-#pragma unroll
-                    for (int i = 0; i < NPT; ++i) s[i] = sn[i];
-                }
-            } else if (live) {
-                load_state_part<TS, NPT>(state_row(h + 1), q, s);
-            }
-        }
+        if (live && j + 1 < hpg) load_state_part<TS, NPT>(state_row(h + 1), q, s);
     }
 }
 
