@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
 // ms per call against 0.680 ms with the next head's state prefetched into
 // registers at two CTAs per SM).
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KParams p, int T) {
+__global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KParams p, int T, int fold_here) {
     extern __shared__ __align__(16) float vsmem[];
     constexpr int N = 4 * NPT;
     const int64_t b = blockIdx.x;
@@ -272,6 +272,10 @@ __global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KPa
     bool pad;
     if (!verify_sequence(p, b, &slot, &c, &pad)) return;
     const bool fold = !pad && c + 2 * T >= p.rlen;
+    // With fold_here (dim within one 64-row block, so this CTA owns every row
+    // of the group's heads) a flush folds the c committed entries here, head
+    // by head, before the readout; otherwise the fold launch has done it.
+    const int cf = fold && fold_here ? c : 0;  // committed entries folded here
     if (fold) c = 0;
     if (g == 0 && blockIdx.z == 0 && threadIdx.x == 0) p.cnt_out[b] = c;
     const VerifyStage st = verify_stage(vsmem, p.rlen, T, N);
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KPa
     }
     with_io(p.io_dtype, [&](auto io) {
         constexpr int IO = decltype(io)::value;
-        stage_entry_B<IO, N>(p, st, slot, c, g);
+        stage_entry_B<IO, N>(p, st, slot, c + cf, g);  // (one of c and cf is 0)
         for (int i = threadIdx.x; i < T * N; i += kVerifyThreads) {
             const int k = i / N, n = i % N;
             const int64_t rr = b * T + k;
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KPa
         const float bias = p.dt_bias ? p.dt_bias[h] : 0.f;
         with_io(p.io_dtype, [&](auto io) {
             constexpr int IO = decltype(io)::value;
-            stage_entry_rows<IO>(p, st, slot, c, h, row0);
+            stage_entry_rows<IO>(p, st, slot, c + cf, h, row0);
             for (int i = threadIdx.x; i < T * kVerifyRows; i += kVerifyThreads) {
                 const int k = i / kVerifyRows, rw = i % kVerifyRows, rrow = row0 + rw;
                 if (rrow >= p.P) continue;
@@ -355,8 +359,20 @@ __global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KPa
                 }
             }
         });
-        // each step's decay and input term per row, shared by the drafts' walks
         const float Ah = p.A[h];
+        if (cf > 0 && live) {
+            // the flush: the committed entries into this head's checkpoint rows
+            // (the fold launch's arithmetic), written back as stored; the
+            // drafts then read the new checkpoint
+            apply_entries<NPT>(p, st, cf, r, q, Ah, s);
+            TS *srow = const_cast<TS *>(state_row(h));
+            store_state_part<TS, NPT>(srow, q, s);
+            if constexpr (sizeof(TS) != 4) {
+#pragma unroll
+                for (int i = 0; i < NPT; ++i) s[i] = to_float(static_cast<TS>(s[i]));
+            }
+        }
+        // each step's decay and input term per row, shared by the drafts' walks
         for (int i = threadIdx.x; i < (c + T) * kVerifyRows; i += kVerifyThreads) {
             const int m = i / kVerifyRows;
             const bool entry = m < c;
@@ -418,11 +434,18 @@ static cudaError_t launch_verify_t(const KParams &p, int64_t batch, int T, cudaS
                                       static_cast<int>(smem))) != cudaSuccess)
             return e;
     }
-    ssu_verify_fold_kernel<TS, NPT><<<grid, kVerifyThreads, smem, stream>>>(p, T);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // One 64-row block: the verify CTAs fold the flushing sequences themselves.
+    // More: a separate fold launch first, because the drafts' B, which a
+    // group's first block appends, takes the place of entries that the
+    // group's other blocks still fold.
+    const int fold_here = p.P <= kVerifyRows ? 1 : 0;
+    if (!fold_here) {
+        ssu_verify_fold_kernel<TS, NPT><<<grid, kVerifyThreads, smem, stream>>>(p, T);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     const dim3 ggrid(static_cast<unsigned>(batch), static_cast<unsigned>(p.G),
                      static_cast<unsigned>((p.P + kVerifyRows - 1) / kVerifyRows));
-    ssu_verify_kernel<TS, NPT><<<ggrid, kVerifyThreads, smem, stream>>>(p, T);
+    ssu_verify_kernel<TS, NPT><<<ggrid, kVerifyThreads, smem, stream>>>(p, T, fold_here);
     return cudaGetLastError();
 }
 
