@@ -255,11 +255,12 @@ __global__ void __launch_bounds__(kVerifyThreads, 2) ssu_verify_fold_kernel(cons
 // group's entries' B, the drafts' B and C and the (c + T) T dots B_m . C_k are
 // staged and formed once; per head, the entries' and drafts' rows, the
 // appends, the step terms, S_ckpt . C_k and the walks, the head's state row
-// part loaded while its rows are staged.  Three CTAs per SM (measured: 0.626
-// ms per call against 0.680 ms with the next head's state prefetched into
-// registers at two CTAs per SM).
+// part loaded while its rows are staged.  Four CTAs per SM (measured: 0.517
+// ms per call against 0.558 ms at three and 0.680 ms at two with the next
+// head's state prefetched into registers): the warps, not the registers,
+// hide each head's chain.
 template <typename TS, int NPT>
-__global__ void __launch_bounds__(kVerifyThreads, 3) ssu_verify_kernel(const KParams p, int T, int fold_here) {
+__global__ void __launch_bounds__(kVerifyThreads, 4) ssu_verify_kernel(const KParams p, int T, int fold_here) {
     extern __shared__ __align__(16) float vsmem[];
     constexpr int N = 4 * NPT;
     const int64_t b = blockIdx.x;
