@@ -154,10 +154,16 @@ __device__ __forceinline__ void stage_rows(__nv_bfloat16 *dst, int ld, const __n
 // ---------------------------------------------------------------------------
 // Stages 1-2: per (head, chunk) the cumulative sums and the chunk's own state.
 // ---------------------------------------------------------------------------
+// The chunk is staged in parts of QH tokens (128 at most), so that three
+// CTAs share an SM.
+template <int Q>
+__host__ __device__ constexpr int chunk_part() { return Q < 128 ? Q : 128; }
+
 template <int Q, int P, int N>
 struct ChunkStateSmem {
-    __nv_bfloat16 xs[Q][P + 8];  // x of the chunk, xs[t][p]
-    __nv_bfloat16 bs[Q][N + 8];  // B of the chunk's group, bs[t][n]
+    static constexpr int QH = chunk_part<Q>();
+    __nv_bfloat16 xs[QH][P + 8];  // x of one part of the chunk, xs[t][p]
+    __nv_bfloat16 bs[QH][N + 8];  // B of the chunk's group for the part, bs[t][n]
     float cs[Q];                 // inclusive cumulative sums of a
     float rs[Q];                 // inclusive cumulative sums of a, reversed
     float w[Q];                  // dt', then exp(sum of the later a) dt'
@@ -168,7 +174,7 @@ struct ChunkStateSmem {
 constexpr int kStateThreads = 256;
 
 template <int Q, int P, int N>
-__global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kStateThreads, 3) ssd_chunk_state_kernel(const SsdParams p) {
     static_assert(P == 64 && N % 64 == 0 && Q <= kStateThreads, "tiling");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<ChunkStateSmem<Q, P, N> *>(smem_raw);
@@ -186,11 +192,17 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
         return;
     }
     const int L = static_cast<int>(t1 - t0);
-    // the chunk's x and B rows, in flight while the decays are formed
-    stage_rows<kStateThreads>(&sm.xs[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.x), t0,
-                              static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, Q, L, P);
-    stage_rows<kStateThreads>(&sm.bs[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.B), t0,
-                              static_cast<int64_t>(p.G) * N, static_cast<int64_t>(g) * N, Q, L, N);
+    constexpr int QH = chunk_part<Q>();
+    // x and B rows of part pt (tokens pt QH ...), zero from L on
+    auto stage_part = [&](int pt) {
+        const int Lp = L - pt * QH;
+        stage_rows<kStateThreads>(&sm.xs[0][0], P + 8, static_cast<const __nv_bfloat16 *>(p.x), t0 + pt * QH,
+                                  static_cast<int64_t>(p.H) * P, static_cast<int64_t>(h) * P, QH, Lp, P);
+        stage_rows<kStateThreads>(&sm.bs[0][0], N + 8, static_cast<const __nv_bfloat16 *>(p.B), t0 + pt * QH,
+                                  static_cast<int64_t>(p.G) * N, static_cast<int64_t>(g) * N, QH, Lp, N);
+    };
+    // the first part's x and B rows, in flight while the decays are formed
+    stage_part(0);
     float *ws_acs = p.ws_acs + ws_unit(p, c, h) * Q;
     float *ws_dtp = p.ws_dtp + ws_unit(p, c, h) * Q;
     const float Ah = p.A[h];
@@ -227,30 +239,49 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
     float acc[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    for (int k0 = 0; k0 < L; k0 += 16) {
-        // A = (w x)^T: matrices (p 0-7 | 8-15) x (t 0-7 | 8-15) of xs, transposed
-        uint32_t ax[4], ahi[4], alo[4];
-        ldsm_x4_trans(ax, &sm.xs[k0 + (lane & 7) + (mi >> 1) * 8][p0 + (mi & 1) * 8]);
-        const float w0 = sm.w[k0 + 2 * q], w1 = sm.w[k0 + 2 * q + 1];
-        const float w8 = sm.w[k0 + 2 * q + 8], w9 = sm.w[k0 + 2 * q + 9];
-        split_bf16(bf16_lo(ax[0]) * w0, bf16_hi(ax[0]) * w1, &ahi[0], &alo[0]);
-        split_bf16(bf16_lo(ax[1]) * w0, bf16_hi(ax[1]) * w1, &ahi[1], &alo[1]);
-        split_bf16(bf16_lo(ax[2]) * w8, bf16_hi(ax[2]) * w9, &ahi[2], &alo[2]);
-        split_bf16(bf16_lo(ax[3]) * w8, bf16_hi(ax[3]) * w9, &ahi[3], &alo[3]);
-        // the high part for every n-tile, then the low part: no accumulator is
-        // used twice in a row
-        uint32_t bb[NT / 2][4];
-#pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-            // B[t][n]: matrices (t 0-7 | 8-15) x (n-tile j | j+1), transposed
-            ldsm_x4_trans(bb[j / 2], &sm.bs[k0 + (lane & 7) + (mi & 1) * 8][n0 + 8 * j + (mi >> 1) * 8]);
-            mma_bf16(acc[j], ahi, bb[j / 2][0], bb[j / 2][1]);
-            mma_bf16(acc[j + 1], ahi, bb[j / 2][2], bb[j / 2][3]);
+    uint32_t xm = 0;  // the largest |x| bits, over the parts
+    for (int pt = 0; pt < Q / QH; ++pt) {
+        if (pt > 0) {
+            if (pt * QH >= L) break;  // the rest of the chunk is empty
+            __syncthreads();          // every warp is done with the previous part
+            stage_part(pt);
+            cp_async_wait_all();
+            __syncthreads();
         }
+        const int kend = min(L, (pt + 1) * QH);
+        for (int k0 = pt * QH; k0 < kend; k0 += 16) {
+            const int kr = k0 - pt * QH;  // row of the part in shared memory
+            // A = (w x)^T: matrices (p 0-7 | 8-15) x (t 0-7 | 8-15) of xs, transposed
+            uint32_t ax[4], ahi[4], alo[4];
+            ldsm_x4_trans(ax, &sm.xs[kr + (lane & 7) + (mi >> 1) * 8][p0 + (mi & 1) * 8]);
+            const float w0 = sm.w[k0 + 2 * q], w1 = sm.w[k0 + 2 * q + 1];
+            const float w8 = sm.w[k0 + 2 * q + 8], w9 = sm.w[k0 + 2 * q + 9];
+            split_bf16(bf16_lo(ax[0]) * w0, bf16_hi(ax[0]) * w1, &ahi[0], &alo[0]);
+            split_bf16(bf16_lo(ax[1]) * w0, bf16_hi(ax[1]) * w1, &ahi[1], &alo[1]);
+            split_bf16(bf16_lo(ax[2]) * w8, bf16_hi(ax[2]) * w9, &ahi[2], &alo[2]);
+            split_bf16(bf16_lo(ax[3]) * w8, bf16_hi(ax[3]) * w9, &ahi[3], &alo[3]);
+            // the high part for every n-tile, then the low part: no accumulator is
+            // used twice in a row
+            uint32_t bb[NT / 2][4];
 #pragma unroll
-        for (int j = 0; j < NT; j += 2) {
-            mma_bf16(acc[j], alo, bb[j / 2][0], bb[j / 2][1]);
-            mma_bf16(acc[j + 1], alo, bb[j / 2][2], bb[j / 2][3]);
+            for (int j = 0; j < NT; j += 2) {
+                // B[t][n]: matrices (t 0-7 | 8-15) x (n-tile j | j+1), transposed
+                ldsm_x4_trans(bb[j / 2], &sm.bs[kr + (lane & 7) + (mi & 1) * 8][n0 + 8 * j + (mi >> 1) * 8]);
+                mma_bf16(acc[j], ahi, bb[j / 2][0], bb[j / 2][1]);
+                mma_bf16(acc[j + 1], ahi, bb[j / 2][2], bb[j / 2][3]);
+            }
+#pragma unroll
+            for (int j = 0; j < NT; j += 2) {
+                mma_bf16(acc[j], alo, bb[j / 2][0], bb[j / 2][1]);
+                mma_bf16(acc[j + 1], alo, bb[j / 2][2], bb[j / 2][3]);
+            }
+        }
+        // the part's largest |x| (rows from L on are zero); bf16 magnitudes
+        // compare as unsigned integers
+        for (int i = tid; i < QH * (P / 8); i += kStateThreads) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(&sm.xs[i / (P / 8)][(i % (P / 8)) * 8]);
+            xm = __vmaxu2(xm, __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
+                                       __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
         }
     }
     float *out = p.ws_state + ws_unit(p, c, h) * P * N;
@@ -261,14 +292,7 @@ __global__ void __launch_bounds__(kStateThreads, 2) ssd_chunk_state_kernel(const
         *reinterpret_cast<float2 *>(out + canon<N>(p0 + gq + 8, n)) = make_float2(acc[j][2], acc[j][3]);
     }
     // the largest |x| and dt' of the chunk and head, from which the scan
-    // picks the power-of-two scales of its fp16 operands (rows from L on are
-    // zero); bf16 magnitudes compare as unsigned integers
-    uint32_t xm = 0;
-    for (int i = tid; i < Q * (P / 8); i += kStateThreads) {
-        const uint4 v = *reinterpret_cast<const uint4 *>(&sm.xs[i / (P / 8)][(i % (P / 8)) * 8]);
-        xm = __vmaxu2(xm, __vmaxu2(__vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu),
-                                   __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu)));
-    }
+    // picks the power-of-two scales of its fp16 operands
     float xmax = fmaxf(__uint_as_float(xm << 16), __uint_as_float(xm & 0xffff0000u));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
