@@ -434,26 +434,50 @@ __device__ void packed_producer(const KParams &p, unsigned char *smem, uint64_t 
     post_stop<TS, L>(p, k, smem, full, empty, rx, lane);
 }
 
+// Eight 16-bit values (one 16-byte piece, lower address first) widened to
+// fp32, bit for bit as bits_to_float does one value.
+__device__ __forceinline__ void widen8(uint4 u, bool bf, float4 *dst) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (bf) {
+            f[2 * k] = __uint_as_float(w[k] << 16);
+            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        } else {
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&w[k]));
+            f[2 * k] = v.x;
+            f[2 * k + 1] = v.y;
+        }
+    }
+    dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+    dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
 // Everything a chunk's tokens share before the token loop, spread over the
-// consumer threads: 16-bit B and C converted to fp32 once, and the row
-// scalars {dA, dt' x, x, gate} of every (token, row) into `rowq`
-// ([kTokChunk][kTileRows]), from the same non-inlined function as the other
-// kernels, hence the same bits.
+// consumer threads: 16-bit B and C converted to fp32 once, a 16-byte piece
+// per thread, and the row scalars {dA, dt' x, x, gate} of every (token, row)
+// into `rowq` ([kTokChunk][kTileRows]), from the same non-inlined function as
+// the other kernels, hence the same bits.  The index splits divide by
+// compile-time powers of two.
+template <int N>
 __device__ __forceinline__ void chunk_prep(const KParams &p, unsigned char *ops, const OpLayout &ol, int ntok,
                                            int rows_here, float Ah, float bias, float4 *rowq, int tid,
                                            int nthreads) {
     if (ol.io == 2) {
-        for (int i = tid; i < ntok * p.N; i += nthreads) {
-            const int t = i / p.N, n = i - t * p.N;
+        constexpr int kPieces = N / 8;
+        const bool bf = p.io_dtype == kBF16;
+        for (int i = tid; i < ntok * kPieces; i += nthreads) {
+            const int t = i / kPieces, c = i - t * kPieces;
             unsigned char *o = ops + t * ol.stride;
-            reinterpret_cast<float *>(o + ol.offBf)[n] =
-                bits_to_float(reinterpret_cast<const unsigned short *>(o)[n], p.io_dtype);
-            reinterpret_cast<float *>(o + ol.offCf)[n] =
-                bits_to_float(reinterpret_cast<const unsigned short *>(o + ol.offC)[n], p.io_dtype);
+            widen8(reinterpret_cast<const uint4 *>(o)[c], bf, reinterpret_cast<float4 *>(o + ol.offBf) + 2 * c);
+            widen8(reinterpret_cast<const uint4 *>(o + ol.offC)[c], bf,
+                   reinterpret_cast<float4 *>(o + ol.offCf) + 2 * c);
         }
     }
-    for (int i = tid; i < ntok * rows_here; i += nthreads) {
-        const int t = i / rows_here, rr = i - t * rows_here;
+    for (int i = tid; i < ntok * kTileRows; i += nthreads) {
+        const int t = i / kTileRows, rr = i - t * kTileRows;
+        if (rr >= rows_here) continue;
         const unsigned char *o = ops + t * ol.stride;
         const float xv = ol.io == 4 ? reinterpret_cast<const float *>(o + ol.offX)[rr]
                                     : bits_to_float(reinterpret_cast<const unsigned short *>(o + ol.offX)[rr],
@@ -488,16 +512,24 @@ __device__ int packed_consumer(const KParams &p, unsigned char *smem, uint64_t *
     int k = 0;
     for (;; ++k) {
         const int s = k % S;
-        if (!mbar_wait_bounded(&full[s], (k / S) & 1, p.wait_cycles)) {
-            if ((tid & 31) == 0) {
+        const bool ok = mbar_wait_bounded(&full[s], (k / S) & 1, p.wait_cycles);
+        unsigned char *stg = stage_base<TS, L>(smem, s);
+        const PackedHeader *hd = reinterpret_cast<const PackedHeader *>(stg + PS::kHeaderOffset);
+        const int flags = ok ? hd->flags : kChunkStop;  // the header is read only from a full stage
+        float4 *rowq = reinterpret_cast<float4 *>(stg + PS::kRowqOffset);
+        if (!(flags & kChunkStop))
+            chunk_prep<N>(p, stg + PS::kSeedBytes, ol, hd->ntok, hd->rows_here, hd->Ah, hd->bias, rowq, tid,
+                          PS::kConsumers);
+        // The chunk's one barrier: its row scalars are ready, and every
+        // consumer learns whether any wait gave up, so that all stop together
+        // rather than leave the others at a barrier.
+        if (barrier_or(1, PS::kConsumers, !ok)) {
+            if (tid == 0) {
                 flag(p.status, kDevTimeout);
                 ring_abort(rx);
             }
             break;
         }
-        unsigned char *stg = stage_base<TS, L>(smem, s);
-        const PackedHeader *hd = reinterpret_cast<const PackedHeader *>(stg + PS::kHeaderOffset);
-        const int flags = hd->flags;
         if (flags & kChunkStop) {
             ++k;
             break;
@@ -506,9 +538,6 @@ __device__ int packed_consumer(const KParams &p, unsigned char *smem, uint64_t *
         const int rows_mine = active ? rows_here : 0;
         const float Dh = hd->Dh;
         const int64_t r0 = hd->r0;
-        float4 *rowq = reinterpret_cast<float4 *>(stg + PS::kRowqOffset);
-        chunk_prep(p, stg + PS::kSeedBytes, ol, ntok, rows_here, hd->Ah, hd->bias, rowq, tid, PS::kConsumers);
-        named_barrier(1, PS::kConsumers);
         if (flags & kChunkFirst) {
             const TS *seed = reinterpret_cast<const TS *>(stg);
 #pragma unroll
