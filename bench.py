@@ -205,10 +205,13 @@ KERNEL_NAMES = {"onetoken": ["ssu_onetoken_kernel"], "packed": ["ssu_packed_kern
                 "ssd": ["ssd_chunk_state_kernel", "ssd_state_pass_kernel", "ssd_scan_tc_kernel"]}
 
 
-def profiled_traffic(kind: str, workload: str):
+def profiled_traffic(kind: str, workload: str, batch=None):
     """DRAM bytes per call recorded in profiles/traffic.json from an ncu
     capture (--record-traffic), if that capture was taken of the kernel
-    sources as they are now; None otherwise."""
+    sources as they are now; None otherwise, and None for a run at another
+    batch (--batch): the records are of the workloads at their own sizes."""
+    if batch is not None:
+        return None
     try:
         with open(TRAFFIC_JSON) as f:
             rec = json.load(f).get(f"{kind}/{workload}")
@@ -499,7 +502,7 @@ def time_decode(workload, args, rank, world, device) -> dict:
                          "no flush: launch-bound case (%.1f KB of state per step, L2-resident)" % (moved / 1e3)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} copy bandwidth",
-                     "traffic": profiled_traffic(kind, workload),
+                     "traffic": profiled_traffic(kind, workload, args.batch),
                      "algorithmic_bytes_per_launch": acct["total"],
                      "kernel": kernel_name(w), "launch_ms": launch_ms},
         "e2e": {"value": aggregate_rate(tokens, world, e2e_steps, e2e_s * 1e3), "unit": UNIT,
@@ -615,7 +618,7 @@ def run_copy(args, rank, world, device):
                    "parallelism": f"{world} independent replicas (one pool per GPU)",
                    "l2": "no flush: %.2f GB moved per step" % (algo / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("copy", args.workload),
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("copy", args.workload, args.batch),
                      "algorithmic_bytes_per_launch": algo, "kernel": "ssu_copy_kernel", "launch_ms": launch_ms},
         "e2e": {"value": aggregate_rate(n, world, e2e_steps, e2e_s * 1e3), "unit": COPY_UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
@@ -749,7 +752,7 @@ def run_verify(args, rank, world, device):
                    "parallelism": f"{world} independent replicas (one pool and batch per GPU)",
                    "l2": "no flush: %.2f GB of checkpoints read per step" % (algo / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("verify", args.workload),
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("verify", args.workload, args.batch),
                      "algorithmic_bytes_per_launch": algo,
                      "kernel": "verify call (ssu_verify_fold_kernel + ssu_verify_kernel)", "launch_ms": call_ms},
         "e2e": {"value": aggregate_rate(units, world, e2e_steps, e2e_s * 1e3), "unit": VERIFY_UNIT,
@@ -892,7 +895,7 @@ def run_ssd(args, rank, world, device):
                    "tensor_flops_per_call": acct["flops"],
                    "workspace_bytes_moved_per_call": acct["workspace"]},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("ssd", args.workload),
+                     "peak_source": f"{peak_src} copy bandwidth", "traffic": profiled_traffic("ssd", args.workload, args.batch),
                      "algorithmic_bytes_per_launch": acct["total"],
                      "kernel": "ssd prefill call (ssd_chunk_state + ssd_state_pass + ssd_scan_tc)",
                      "launch_ms": call_ms},

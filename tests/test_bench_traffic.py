@@ -36,6 +36,8 @@ def test_record_and_lookup(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "TRAFFIC_JSON", str(out))
     bench.record_traffic(str(p), "verify_b256_t4_fp32", "ncu ...")
     assert bench.profiled_traffic("verify", "verify_b256_t4_fp32") == int(12.5e6 + 1.35e9)
+    # a run at another batch is not the recorded workload
+    assert bench.profiled_traffic("verify", "verify_b256_t4_fp32", batch=32) is None
     rec = json.loads(out.read_text())
     rec["verify/verify_b256_t4_fp32"]["kernel_source_sha256_16"] = "0" * 16
     out.write_text(json.dumps(rec))
