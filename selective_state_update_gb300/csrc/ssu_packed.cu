@@ -434,9 +434,40 @@ __device__ void packed_producer(const KParams &p, unsigned char *smem, uint64_t 
     post_stop<TS, L>(p, k, smem, full, empty, rx, lane);
 }
 
+// Where a group of four fp32 values of a widened dstate vector sits, in
+// float4 units: element e of the vector belongs to lane (e / kVec) % L as
+// values 4 q .. 4 q + 3 of its chunk k = e / (kVec L) (q = (e % kVec) / 4), and
+// lane l's group (k, q) is stored at (k kVec / 4 + q) L + l.  The lanes of a
+// row then read consecutive 16-byte pieces (with kVec = 8 the natural order
+// would put them 32 bytes apart: two-way bank conflicts).
+template <int kVec, int L>
+__device__ __forceinline__ int widened_group(int e) {
+    const int cc = e / kVec, q = (e % kVec) / 4;
+    return ((cc / L) * (kVec / 4) + q) * L + cc % L;
+}
+
+// This thread's 16 values of a widened dstate vector, in the element layout
+// of Tile::gather.
+template <typename TS, int L>
+__device__ __forceinline__ void gather_widened(const float *v4, int lane, float *v) {
+    constexpr int kVec = Tile<TS, L>::kVec;
+#pragma unroll
+    for (int k = 0; k < Tile<TS, L>::kChunks; ++k) {
+#pragma unroll
+        for (int q = 0; q < kVec / 4; ++q) {
+            const float4 f = reinterpret_cast<const float4 *>(v4)[(k * (kVec / 4) + q) * L + lane];
+            v[k * kVec + 4 * q + 0] = f.x;
+            v[k * kVec + 4 * q + 1] = f.y;
+            v[k * kVec + 4 * q + 2] = f.z;
+            v[k * kVec + 4 * q + 3] = f.w;
+        }
+    }
+}
+
 // Eight 16-bit values (one 16-byte piece, lower address first) widened to
-// fp32, bit for bit as bits_to_float does one value.
-__device__ __forceinline__ void widen8(uint4 u, bool bf, float4 *dst) {
+// fp32, bit for bit as bits_to_float does one value: values 0-3 to lo,
+// 4-7 to hi.
+__device__ __forceinline__ void widen8(uint4 u, bool bf, float4 *lo, float4 *hi) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     float f[8];
 #pragma unroll
@@ -450,17 +481,17 @@ __device__ __forceinline__ void widen8(uint4 u, bool bf, float4 *dst) {
             f[2 * k + 1] = v.y;
         }
     }
-    dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-    dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+    *lo = make_float4(f[0], f[1], f[2], f[3]);
+    *hi = make_float4(f[4], f[5], f[6], f[7]);
 }
 
 // Everything a chunk's tokens share before the token loop, spread over the
 // consumer threads: 16-bit B and C converted to fp32 once, a 16-byte piece
-// per thread, and the row scalars {dA, dt' x, x, gate} of every (token, row)
+// per thread, in the order of widened_group, and the row scalars {dA, dt' x, x, gate} of every (token, row)
 // into `rowq` ([kTokChunk][kTileRows]), from the same non-inlined function as
 // the other kernels, hence the same bits.  The index splits divide by
 // compile-time powers of two.
-template <int N>
+template <typename TS, int L, int N>
 __device__ __forceinline__ void chunk_prep(const KParams &p, unsigned char *ops, const OpLayout &ol, int ntok,
                                            int rows_here, float Ah, float bias, float4 *rowq, int tid,
                                            int nthreads) {
@@ -470,9 +501,11 @@ __device__ __forceinline__ void chunk_prep(const KParams &p, unsigned char *ops,
         for (int i = tid; i < ntok * kPieces; i += nthreads) {
             const int t = i / kPieces, c = i - t * kPieces;
             unsigned char *o = ops + t * ol.stride;
-            widen8(reinterpret_cast<const uint4 *>(o)[c], bf, reinterpret_cast<float4 *>(o + ol.offBf) + 2 * c);
-            widen8(reinterpret_cast<const uint4 *>(o + ol.offC)[c], bf,
-                   reinterpret_cast<float4 *>(o + ol.offCf) + 2 * c);
+            constexpr int kVec = Tile<TS, L>::kVec;
+            const int g0 = widened_group<kVec, L>(8 * c), g1 = widened_group<kVec, L>(8 * c + 4);
+            float4 *b4 = reinterpret_cast<float4 *>(o + ol.offBf), *c4 = reinterpret_cast<float4 *>(o + ol.offCf);
+            widen8(reinterpret_cast<const uint4 *>(o)[c], bf, b4 + g0, b4 + g1);
+            widen8(reinterpret_cast<const uint4 *>(o + ol.offC)[c], bf, c4 + g0, c4 + g1);
         }
     }
     for (int i = tid; i < ntok * kTileRows; i += nthreads) {
@@ -518,7 +551,7 @@ __device__ int packed_consumer(const KParams &p, unsigned char *smem, uint64_t *
         const int flags = ok ? hd->flags : kChunkStop;  // the header is read only from a full stage
         float4 *rowq = reinterpret_cast<float4 *>(stg + PS::kRowqOffset);
         if (!(flags & kChunkStop))
-            chunk_prep<N>(p, stg + PS::kSeedBytes, ol, hd->ntok, hd->rows_here, hd->Ah, hd->bias, rowq, tid,
+            chunk_prep<TS, L, N>(p, stg + PS::kSeedBytes, ol, hd->ntok, hd->rows_here, hd->Ah, hd->bias, rowq, tid,
                           PS::kConsumers);
         // The chunk's one barrier: its row scalars are ready, and every
         // consumer learns whether any wait gave up, so that all stop together
@@ -565,8 +598,13 @@ __device__ int packed_consumer(const KParams &p, unsigned char *smem, uint64_t *
         for (int t = 0; t < ntok; ++t) {
             const unsigned char *o = stg + PS::kSeedBytes + t * ol.stride;
             float bv[kElemsPerThread], cv[kElemsPerThread];
-            T::gather(reinterpret_cast<const float *>(o + ol.offBf), lane, bv);
-            T::gather(reinterpret_cast<const float *>(o + ol.offCf), lane, cv);
+            if (ol.io == 4) {  // as staged
+                T::gather(reinterpret_cast<const float *>(o + ol.offBf), lane, bv);
+                T::gather(reinterpret_cast<const float *>(o + ol.offCf), lane, cv);
+            } else {  // as widened
+                gather_widened<TS, L>(reinterpret_cast<const float *>(o + ol.offBf), lane, bv);
+                gather_widened<TS, L>(reinterpret_cast<const float *>(o + ol.offCf), lane, cv);
+            }
             const int64_t ws = hd->ws[t];
             TS *dst = ws >= 0 ? static_cast<TS *>(p.state) + ws * slot_elems + head_rows : nullptr;
 #pragma unroll
